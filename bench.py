@@ -1,0 +1,503 @@
+"""Benchmark of the OSCAR mixed-precision INT2 KV-cache decode step on GB300.
+
+A step is one decode token for every layer of the workload: for each layer,
+append the new K/V (demoting the oldest recent token into the INT2 history)
+and run decode attention over the BF16 sink | INT2 history | BF16 recent pool.
+The metric is KV tokens/s = sum over layers of the sequence lengths attended,
+divided by the step time, plus achieved HBM GB/s of the dominant kernel (the
+INT2 history kernel) against the measured peak.
+
+Workloads (synthetic, seeded; Qwen3-shaped random data, no model weights):
+  qwen3_8b_36l  (default) 36 layers x (32 q / 8 kv heads, d=128), batch 1,
+                102,400-token context (64 sink + 102,080 history + 256 recent)
+  qwen3_4b_b32  36 layers, batch 32 x 102,400 tokens sharing a 92,160-token prefix
+  qwen3_8b_l1   1 layer, batch 1, 32,768 tokens
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV tokens/s and achieved HBM GB/s vs GB300 peak, 100K ctx"
+UNIT = "KV tokens/s"
+HIST_BYTES = 80          # per history token per kv head: 32 B K codes + 32 B V codes + 16 B fp16 scale/zero
+BF16_BYTES = 512         # per BF16 token per kv head: K and V, 128 x 2 B each
+
+WORKLOADS = {
+    "qwen3_8b_36l": dict(layers=36, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
+    "qwen3_4b_b32": dict(layers=36, hq=32, hkv=8, batch=32, ctx=102400, shared=92160),
+    "qwen3_8b_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=32768, shared=0),
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.proc, self.lines = gpu, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# workload construction
+
+
+def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_capacity: int = 64, algo: int = 1):
+    import torch
+    import bit_kv_cache_decode_gb300 as osc
+    import synth
+
+    w = WORKLOADS[name]
+    L, B, H, hq, nl, shared = w["ctx"], w["batch"], w["hkv"], w["hq"], w["layers"], w["shared"]
+    Lmax = L + steps_capacity
+    n_hist_max = (Lmax - 320 + 63) // 64
+    # page tables: shared prefix pages first (sink page + history pages covering the prefix), then private pages
+    shp = (shared - 64) // 64 if shared else 0
+    priv = n_hist_max - shp
+    n_int2 = shp + B * priv
+    n_bf16 = (1 + 4 * B) if shared else 5 * B
+    hist_pt = np.zeros((B, n_hist_max), np.int32)
+    bf16_pt = np.zeros((B, 5), np.int32)
+    for r in range(B):
+        hist_pt[r, :shp] = np.arange(shp)
+        hist_pt[r, shp:] = shp + r * priv + np.arange(priv)
+        if shared:
+            bf16_pt[r, 0] = 0
+            bf16_pt[r, 1:] = 1 + 4 * r + np.arange(4)
+        else:
+            bf16_pt[r] = 5 * r + np.arange(5)
+    cfg = osc.CacheConfig(num_layers=nl, num_kv_heads=H, num_q_heads=hq, num_int2_pages=n_int2,
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=512, v_mode=osc.V_ABSORBED)
+    cache = osc.OscarCache(cfg, device=device)
+    cache.set_decode_algo(algo)
+    # offline calibration on the host (library routine), one per (layer, kv head)
+    sm = synth.sm_scale()
+
+    def cal(lh):
+        layer, h = lh
+        qc, kc, vc = synth.calibration(seed, layer, h)
+        return osc.calibrate(qc, kc, vc, sm)
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 8) as ex:
+        cals = list(ex.map(cal, [(l, h) for l in range(nl) for h in range(H)]))
+    gen = torch.Generator(device=device)
+    bf16_pages = None
+    if with_bf16:
+        npg = (Lmax + 63) // 64
+        bf16_pages = torch.empty((nl, B * npg if not shared else (shared // 64 + B * (npg - shared // 64)), H, 2, 64,
+                                  128), dtype=torch.bfloat16, device=device)
+        bpt = np.zeros((B, npg), np.int32)
+        sp = shared // 64
+        for r in range(B):
+            bpt[r, :sp] = np.arange(sp)
+            bpt[r, sp:] = sp + r * (npg - sp) + np.arange(npg - sp)
+    hp_d = torch.from_numpy(hist_pt).to(device)
+    bp_d = torch.from_numpy(bf16_pt).to(device)
+    for layer in range(nl):
+        cs = cals[layer * H:(layer + 1) * H]
+        cache.set_rotation(layer, np.stack([c["U_K"] for c in cs]), np.stack([c["U_V"] for c in cs]),
+                           np.stack([c["tau_K"] for c in cs]), np.stack([c["tau_V"] for c in cs]))
+        outl = np.stack([synth.head_stats(seed, layer, h).outliers for h in range(H)])
+        gen.manual_seed(seed * 1000003 + layer)
+        if shared:
+            kp, vp = synth.torch_kv_tokens(shared, H, outl, gen, device)
+        for r in range(B):
+            n_priv = L - shared
+            k, v = synth.torch_kv_tokens(n_priv, H, outl, gen, device)
+            if shared:
+                k, v = torch.cat([kp, k]), torch.cat([vp, v])
+            cu = torch.tensor([0, L], dtype=torch.int32, device=device)
+            cache.quantize_prefill(layer, k, v, cu, hp_d[r:r + 1], bp_d[r:r + 1], total_tokens=L)
+            if with_bf16:
+                pages = torch.from_numpy(bpt[r, :(L + 63) // 64]).to(device).long()
+                kk = torch.zeros(((L + 63) // 64) * 64, H, 128, dtype=torch.bfloat16, device=device)
+                vv = torch.zeros_like(kk)
+                kk[:L], vv[:L] = k, v
+                bf16_pages[layer, pages, :, 0] = kk.view(-1, 64, H, 128).transpose(1, 2)
+                bf16_pages[layer, pages, :, 1] = vv.view(-1, 64, H, 128).transpose(1, 2)
+            del k, v
+        torch.cuda.synchronize()
+    if cache.get_status() != 0:
+        raise RuntimeError("device status error while building the workload")
+    return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, B=B, H=H, hq=hq, layers=nl,
+                bf16_pages=bf16_pages, bf16_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
+                hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared)
+
+
+def step_inputs(wl, steps: int, device, seed: int):
+    """New-token K/V and queries for `steps` steps x layers, drawn on the device."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 7)
+    nl, B, H, hq = wl["layers"], wl["B"], wl["H"], wl["hq"]
+    kv = torch.randn(steps, nl, 2, B, H, 128, generator=g, device=device).to(torch.bfloat16)
+    q = torch.randn(steps, nl, B, hq, 128, generator=g, device=device).to(torch.bfloat16)
+    return kv, q
+
+
+def history_bytes(L: int, B: int, H: int) -> int:
+    return B * max(0, L - 320) * H * HIST_BYTES
+
+
+def step_algorithmic_bytes(L: int, B: int, H: int, hq: int, layers: int) -> int:
+    per_layer = history_bytes(L, B, H) + B * min(L, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
+    return per_layer * layers
+
+
+# ---------------------------------------------------------------------------------------------
+
+
+def run_ours(args, rank: int, world: int, device):
+    import torch
+    import bit_kv_cache_decode_gb300 as osc
+    import synth
+
+    seed = 1234 + rank
+    wl = build_workload(args.workload, seed, device, with_bf16=not args.no_bf16,
+                        steps_capacity=3 * (args.steps + args.warmup) + 8, algo=args.algo)
+    cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
+    stream = torch.cuda.current_stream()
+    sm = synth.sm_scale()
+    total_steps = args.warmup + args.steps
+    kv_new, q_all = step_inputs(wl, total_steps, device, seed)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
+    seq = torch.full((B,), wl["L"], dtype=torch.int32, device=device)
+    seq1 = seq + 1
+    launches_per_layer = 5   # append, query rotation, INT2 history, BF16 segment, merge
+
+    def one_step(i):
+        for layer in range(nl):
+            cache.append_kv(layer, kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
+            cache.decode_attention(layer, q_all[i, layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out)
+        seq.add_(1)
+        seq1.add_(1)
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+    L_start = wl["L"] + args.warmup
+    barrier(world)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cache.profile_begin(nl * args.steps)
+    with ClockSampler(device.index if device.index is not None else 0) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.warmup, total_steps):
+            one_step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    int2_ms, int2_n = cache.profile_read()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world, device)
+    if cache.get_status() != 0:
+        raise RuntimeError("device status error during the timed steps")
+    # units: KV tokens attended per step (+1 for the appended token, all layers)
+    kv_tokens = sum(B * (L_start + 1 + s) * nl for s in range(args.steps))
+    value = kv_tokens * world / (ms / 1e3)
+    ms_step = ms / args.steps
+    step_bytes = sum(step_algorithmic_bytes(L_start + 1 + s, B, H, hq, nl) for s in range(args.steps)) / args.steps
+    peak, peak_src = peaks()
+    # dominant kernel: INT2 history kernel, algorithmic bytes per launch at the mean context of the timed steps
+    L_mid = L_start + 1 + (args.steps - 1) / 2
+    hb = history_bytes(int(L_mid), B, H)
+    int2_avg_ms = int2_ms / max(int2_n, 1)
+    achieved = hb / (int2_avg_ms / 1e3) / 1e9
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items()},
+                   "head_dim": 128, "sink": 64, "recent": 256, "group": 64, "page": 64, "v_mode": "absorbed",
+                   "storage": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
+                   "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
+                   "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma"},
+        "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+                "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak},
+        "roofline": {"bound": "hbm", "kernel": "INT2 history decode", "achieved": achieved, "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": hb, "avg_launch_us": int2_avg_ms * 1e3,
+                     "launches": int2_n},
+        "gpu_launches": launches_per_layer * nl * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_bf16:
+        res["bf16_baseline"] = run_bf16(wl, args, q_all, device)
+        res["bf16_baseline"]["speedup_of_int2_step"] = res["bf16_baseline"]["ms_per_step"] / ms_step
+    res["e2e"] = run_e2e(wl, args, device)
+    if rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(wl, seed, device, budget_s=args.cpu_budget)
+    return res
+
+
+def run_bf16(wl, args, q_all, device):
+    """The all-BF16 paged decode kernel on the same K/V, all layers, timed like the INT2 step."""
+    import torch
+    import bit_kv_cache_decode_gb300 as osc
+    import synth
+    nl, B, H, hq, L = wl["layers"], wl["B"], wl["H"], wl["hq"], wl["L"]
+    ws = torch.zeros(osc.bf16_decode_workspace_bytes(B, hq, 512), dtype=torch.uint8, device=device)
+    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
+    seq = torch.full((B,), L, dtype=torch.int32, device=device)
+    pages, pt = wl["bf16_pages"], wl["bf16_pt"]
+    sm = synth.sm_scale()
+
+    def step(i):
+        for layer in range(nl):
+            osc.bf16_decode(pages[layer], q_all[i, layer], seq, pt, sm, H, ws, 512, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    by = B * L * H * BF16_BYTES * nl
+    return {"kernel": "BF16 paged decode (same build)", "ms_per_step": ms, "kv_tokens_per_s": B * L * nl / (ms / 1e3),
+            "gbs": by / (ms / 1e3) / 1e9, "algorithmic_bytes_per_step": by}
+
+
+def run_e2e(wl, args, device):
+    """Same step through the public API with host buffers: pinned host -> device copy of the step's new K/V
+    and queries, the step, and a device -> host read of every layer's output."""
+    import torch
+    import synth
+    cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
+    sm = synth.sm_scale()
+    n_in = nl * (2 * B * H + B * hq) * 128
+    host_in = torch.randn(n_in, dtype=torch.float32).to(torch.bfloat16).pin_memory()
+    host_out = torch.empty(nl * B * hq * 128, dtype=torch.bfloat16).pin_memory()
+    dev_in = torch.empty_like(host_in, device=device)
+    dev_out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
+    # sequence lengths continue from where the timed run left the cache
+    seq = torch.full((B,), wl["L"] + args.warmup + args.steps, dtype=torch.int32, device=device)
+    seq1 = seq + 1
+    kvn = dev_in[:nl * 2 * B * H * 128].view(nl, 2, B, H, 128)
+    qn = dev_in[nl * 2 * B * H * 128:].view(nl, B, hq, 128)
+
+    def step():
+        dev_in.copy_(host_in, non_blocking=True)
+        for layer in range(nl):
+            cache.append_kv(layer, kvn[layer, 0], kvn[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
+            cache.decode_attention(layer, qn[layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=dev_out[layer])
+        host_out.copy_(dev_out.view(-1), non_blocking=True)
+        seq.add_(1)
+        seq1.add_(1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Ls = int(seq[0].item())
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    kv_tokens = sum(B * (Ls + 1 + s) * nl for s in range(args.steps)) / args.steps
+    return {"value": kv_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": host_in.numel() * 2, "d2h_bytes_per_step": host_out.numel() * 2}
+
+
+def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
+    """The CPU oracle's decode of one layer of the workload (unpack, dequantise, fp64 exact softmax),
+    from the pool bytes of layer 0, on the host cores; KV heads are added until the time budget is used."""
+    from oracle import attention as A
+    from oracle import pool as P
+    cache, H, hq, L = wl["cache"], wl["H"], wl["hq"], wl["L"]
+    import torch
+    torch.cuda.synchronize()
+    cfg = wl["cfg"]
+    pm = P.PoolModel(P.PoolGeometry(hkv=H), cfg.num_int2_pages, cfg.num_bf16_pages)
+    pm.int2[:] = cache.int2_pages(0).cpu().numpy()
+    pm.bf16[:] = cache.bf16_pages(0).cpu().numpy().view(np.uint16).reshape(pm.bf16.shape)
+    prm = [P.HeadParams(c["U_K"], c["U_V"], c["tau_K"], c["tau_V"]) for c in wl["cals"][:H]]
+    q = np.random.default_rng(seed).standard_normal((hq, 128)).astype(np.float32)
+    Lnow = int(L)
+    t0 = time.perf_counter()
+    heads = 0
+    while heads < H:
+        A.decode_request(q, Lnow, pm, wl["hist_np"][0], wl["bf16_np"][0], prm, True, 1 / math.sqrt(128),
+                         kv_heads=[heads])
+        heads += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    units = Lnow * heads / H            # KV tokens of one layer-step, scaled by the share of heads done
+    return {"value": units / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"layer 0, {heads} of {H} kv heads ({heads * hq // H} q heads), context {Lnow}, "
+                      f"{dt:.1f} s; numpy fp64 unpack + dequantise + exact softmax"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: one step = the oracle's decode of one layer of the workload for a
+    bounded sample of kv heads (host cores)."""
+    if rank != 0:
+        return None
+    from oracle import attention as A
+    from oracle import pool as P
+    from oracle import rotation
+    import synth
+    w = WORKLOADS[args.workload]
+    L, H, hq = w["ctx"], w["hkv"], w["hq"]
+    seed = 1234
+    # build layer 0 of the workload with the oracle itself (one kv head per step sample)
+    geo = P.PoolGeometry(hkv=1)
+    nh = (L - 320 + 63) // 64
+    pm = P.PoolModel(geo, nh, 5)
+    qc, kc, vc = synth.calibration(seed, 0, 0)
+    cal = rotation.calibrate(qc, kc, vc, synth.sm_scale())
+    prm = [P.HeadParams(cal["U_K"].astype(np.float32), cal["U_V"].astype(np.float32),
+                        cal["tau_K"].astype(np.float32), cal["tau_V"].astype(np.float32))]
+    k, v = synth.kv_tokens(seed, 0, 0, L)
+    P.prefill(pm, k[:, None], v[:, None], np.arange(nh), np.arange(5), prm, True)
+    q = synth.queries(seed, 0, 0, hq // H)
+    for _ in range(args.warmup):
+        A.decode_request(q, L, pm, np.arange(nh), np.arange(5), prm, True, synth.sm_scale())
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        A.decode_request(q, L, pm, np.arange(nh), np.arange(5), prm, True, synth.sm_scale())
+    dt = (time.perf_counter() - t0) / args.steps
+    value = L / H / dt        # one kv head of one layer per step: L/H of the layer's KV tokens
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.workload, **w},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"layer 0, 1 of {H} kv heads, context {L}, per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------------------------
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_36l")
+    ap.add_argument("--algo", type=int, default=None, help="INT2 decode kernel: 0 simt, 1 mma (default: library's)")
+    ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import __graft_entry__
+    __graft_entry__.build()
+    if args.algo is None:
+        args.algo = 1
+    res = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,377 @@
+// C ABI of the OSCAR INT2 KV-cache library: layout carving, argument checks,
+// launches, status and tracing. The functions and data layouts are described
+// in include/oscar.h.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kernels.cuh"
+
+using namespace oscar;
+
+struct oscar_cache {
+  oscar_layout lay;
+  uint8_t* pool;
+  uint8_t* ws;
+  size_t layer_bytes, int2_bytes, bf16_bytes, params_bytes;
+  size_t pool_bytes, ws_bytes;
+  DecodeWorkspace dws;
+  int* status;
+  int sms;
+  int algo;
+  // tracing
+  bool prof_on;
+  int prof_cap, prof_n;
+  std::vector<cudaEvent_t> prof_ev;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_pow2_le8(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+
+int check_layout(const oscar_layout* L) {
+  if (!L) return OSCAR_ERR_INVALID_ARG;
+  if (L->num_layers < 1 || L->num_kv_heads < 1 || L->num_q_heads < 1 || L->num_int2_pages < 0 ||
+      L->num_bf16_pages < 0 || L->max_batch < 1 || L->max_splits < 1 || L->sink < 0 || L->recent < 1)
+    return OSCAR_ERR_INVALID_ARG;
+  if (L->num_q_heads % L->num_kv_heads != 0) return OSCAR_ERR_INVALID_ARG;
+  if (L->page_size < 1 || L->sink % L->page_size != 0 || L->recent % L->page_size != 0) return OSCAR_ERR_INVALID_ARG;
+  if (L->group < 1 || L->head_dim % L->group != 0) return OSCAR_ERR_INVALID_ARG;
+  if (L->v_mode != OSCAR_V_ABSORBED && L->v_mode != OSCAR_V_EXPLICIT) return OSCAR_ERR_INVALID_ARG;
+  if (L->head_dim != kD || L->group != kG || L->page_size != kP) return OSCAR_ERR_UNSUPPORTED;
+  if (!is_pow2_le8(L->num_q_heads / L->num_kv_heads)) return OSCAR_ERR_UNSUPPORTED;
+  if (L->max_splits > 4096) return OSCAR_ERR_UNSUPPORTED;
+  return OSCAR_OK;
+}
+
+void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, size_t* layerb, size_t* poolb,
+           size_t* wsb) {
+  *int2b = align_up((size_t)L->num_int2_pages * L->num_kv_heads * kBlockBytes);
+  *bf16b = align_up((size_t)L->num_bf16_pages * L->num_kv_heads * kBf16BlockBytes);
+  *prmb = align_up((size_t)L->num_kv_heads * kParamFloats * sizeof(float));
+  *layerb = *int2b + *bf16b + *prmb;
+  *poolb = *layerb * L->num_layers;
+  const size_t B = L->max_batch, hq = L->num_q_heads, hkv = L->num_kv_heads;
+  *wsb = kAlign                                                    // status word
+         + align_up(B * hq * kD * sizeof(float))                   // qrot
+         + align_up(B * hkv * kFragWords * sizeof(uint32_t))       // qfrag
+         + align_up(B * hq * kNG * sizeof(float))                  // qsum
+         + align_up(B * hq * (L->max_splits + 1) * kPartFloats * sizeof(float));  // partials
+}
+
+LayerView view(const oscar_cache* c, int layer) {
+  LayerView v;
+  uint8_t* base = c->pool + (size_t)layer * c->layer_bytes;
+  v.int2 = base;
+  v.bf16 = base + c->int2_bytes;
+  v.params = reinterpret_cast<const float*>(base + c->int2_bytes + c->bf16_bytes);
+  v.n_int2 = c->lay.num_int2_pages;
+  v.n_bf16 = c->lay.num_bf16_pages;
+  v.hkv = c->lay.num_kv_heads;
+  v.hq = c->lay.num_q_heads;
+  v.sink = c->lay.sink;
+  v.recent = c->lay.recent;
+  v.v_explicit = c->lay.v_mode == OSCAR_V_EXPLICIT;
+  v.status = c->status;
+  return v;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int g_configured = 0;
+
+int configure_once() {
+  if (g_configured) return OSCAR_OK;
+  int rc = configure_write_path_kernels();
+  if (rc == OSCAR_OK) rc = configure_decode_kernels();
+  if (rc == OSCAR_OK) g_configured = 1;
+  return rc;
+}
+
+// Split policy: enough (request, kv head, split) CTAs to fill the GPU a few times
+// over, never more splits than pages, and no empty trailing split.
+void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int* nsplit, int* pps) {
+  if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
+  long want = ((long)sms * ctas_per_sm + (long)B * hkv - 1) / ((long)B * hkv);
+  int n = (int)std::min<long>(std::max<long>(want, 1), max_splits);
+  n = std::min(n, max_pages);
+  int p = (max_pages + n - 1) / n;
+  *pps = p;
+  *nsplit = (max_pages + p - 1) / p;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* oscar_error_string(int code) {
+  switch (code) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case OSCAR_ERR_CUDA: return "CUDA runtime error";
+    case OSCAR_ERR_DEVICE_STATUS: return "device status word has error bits";
+    case OSCAR_ERR_TIMEOUT: return "bounded device wait expired";
+    case OSCAR_ERR_NOT_ORTHOGONAL: return "rotation is not orthogonal (max|U^T U - I| > 1e-3)";
+    default: return "unknown status";
+  }
+}
+
+int oscar_cache_bytes(const oscar_layout* layout, size_t* pool_bytes, size_t* workspace_bytes) {
+  int rc = check_layout(layout);
+  if (rc != OSCAR_OK) return rc;
+  size_t a, b, c, d, pb, wb;
+  sizes(layout, &a, &b, &c, &d, &pb, &wb);
+  if (pool_bytes) *pool_bytes = pb;
+  if (workspace_bytes) *workspace_bytes = wb;
+  return OSCAR_OK;
+}
+
+int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, oscar_cache** out) {
+  if (!out) return OSCAR_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_layout(layout);
+  if (rc != OSCAR_OK) return rc;
+  if (!pool || !workspace) return OSCAR_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(pool) | reinterpret_cast<uintptr_t>(workspace)) % kAlign != 0)
+    return OSCAR_ERR_INVALID_ARG;
+  rc = configure_once();
+  if (rc != OSCAR_OK) return rc;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  oscar_cache* c = new (std::nothrow) oscar_cache();
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  c->lay = *layout;
+  c->pool = static_cast<uint8_t*>(pool);
+  c->ws = static_cast<uint8_t*>(workspace);
+  sizes(layout, &c->int2_bytes, &c->bf16_bytes, &c->params_bytes, &c->layer_bytes, &c->pool_bytes, &c->ws_bytes);
+  const size_t B = layout->max_batch, hq = layout->num_q_heads, hkv = layout->num_kv_heads;
+  uint8_t* p = c->ws;
+  c->status = reinterpret_cast<int*>(p);
+  p += kAlign;
+  c->dws.qrot = reinterpret_cast<float*>(p);
+  p += align_up(B * hq * kD * sizeof(float));
+  c->dws.qfrag = reinterpret_cast<uint32_t*>(p);
+  p += align_up(B * hkv * kFragWords * sizeof(uint32_t));
+  c->dws.qsum = reinterpret_cast<float*>(p);
+  p += align_up(B * hq * kNG * sizeof(float));
+  c->dws.partials = reinterpret_cast<float*>(p);
+  c->dws.max_splits = layout->max_splits;
+  c->sms = sms;
+  c->algo = OSCAR_DECODE_SIMT;
+  c->prof_on = false;
+  c->prof_cap = c->prof_n = 0;
+  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) { delete c; return OSCAR_ERR_CUDA; }
+  *out = c;
+  return OSCAR_OK;
+}
+
+int oscar_cache_destroy(oscar_cache* c) {
+  if (!c) return OSCAR_OK;
+  for (cudaEvent_t e : c->prof_ev) cudaEventDestroy(e);
+  delete c;
+  return OSCAR_OK;
+}
+
+int oscar_layer_offsets(const oscar_cache* c, int layer, size_t* int2_off, size_t* bf16_off, size_t* params_off) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers) return OSCAR_ERR_INVALID_ARG;
+  const size_t base = (size_t)layer * c->layer_bytes;
+  if (int2_off) *int2_off = base;
+  if (bf16_off) *bf16_off = base + c->int2_bytes;
+  if (params_off) *params_off = base + c->int2_bytes + c->bf16_bytes;
+  return OSCAR_OK;
+}
+
+int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float* U_V, const float* tau_K,
+                       const float* tau_V, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || !U_K || !tau_K || !tau_V) return OSCAR_ERR_INVALID_ARG;
+  const bool expl = c->lay.v_mode == OSCAR_V_EXPLICIT;
+  if (expl && !U_V) return OSCAR_ERR_INVALID_ARG;
+  const int hkv = c->lay.num_kv_heads;
+  for (int h = 0; h < hkv; ++h) {
+    for (int which = 0; which < 2; ++which) {
+      const float* U = which == 0 ? U_K : U_V;
+      if (!U) continue;
+      U += (size_t)h * kD * kD;
+      for (int i = 0; i < kD; ++i)
+        for (int j = i; j < kD; ++j) {
+          double s = 0.0;
+          for (int r = 0; r < kD; ++r) s += (double)U[r * kD + i] * (double)U[r * kD + j];
+          const double e = std::fabs(s - (i == j ? 1.0 : 0.0));
+          if (!(e <= 1e-3)) return OSCAR_ERR_NOT_ORTHOGONAL;
+        }
+    }
+  }
+  std::vector<float> host((size_t)hkv * kParamFloats, 0.f);
+  for (int h = 0; h < hkv; ++h) {
+    float* dst = host.data() + (size_t)h * kParamFloats;
+    std::memcpy(dst + kUKOff, U_K + (size_t)h * kD * kD, kD * kD * sizeof(float));
+    if (U_V) std::memcpy(dst + kUVOff, U_V + (size_t)h * kD * kD, kD * kD * sizeof(float));
+    std::memcpy(dst + kTauKOff, tau_K + (size_t)h * kD, kD * sizeof(float));
+    std::memcpy(dst + kTauVOff, tau_V + (size_t)h * kD, kD * sizeof(float));
+  }
+  LayerView v = view(c, layer);
+  cudaError_t e = cudaMemcpyAsync(const_cast<float*>(v.params), host.data(), host.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+  // the source is pageable: the call returns once `host` has been staged, so it may be freed
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+int oscar_quantize_prefill(oscar_cache* c, int layer, int B, const void* k, const void* v, const int32_t* cu_seqlens,
+                           int total_tokens, const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt,
+                           void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || total_tokens < 0 || max_hist_pages < 0)
+    return OSCAR_ERR_INVALID_ARG;
+  if (B == 0 || total_tokens == 0) return OSCAR_OK;
+  if (!k || !v || !cu_seqlens || !bf16_pt || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
+  return launch_prefill(view(c, layer), B, k, v, cu_seqlens, total_tokens, hist_pt, max_hist_pages, bf16_pt,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int oscar_append_kv(oscar_cache* c, int layer, int B, const void* k, const void* v, const int32_t* seq_lens_before,
+                    const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || max_hist_pages < 0) return OSCAR_ERR_INVALID_ARG;
+  if (B == 0) return OSCAR_OK;
+  if (!k || !v || !seq_lens_before || !bf16_pt || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
+  return launch_append(view(c, layer), B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int oscar_set_decode_algo(oscar_cache* c, int algo) {
+  if (!c || (algo != OSCAR_DECODE_SIMT && algo != OSCAR_DECODE_MMA)) return OSCAR_ERR_INVALID_ARG;
+  c->algo = algo;
+  return OSCAR_OK;
+}
+
+int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens,
+                           const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, float sm_scale,
+                           void* out, int out_dtype, float* lse, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || B > c->lay.max_batch || max_hist_pages < 0)
+    return OSCAR_ERR_INVALID_ARG;
+  if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
+  if (B == 0) return OSCAR_OK;
+  if (!q || !seq_lens || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return OSCAR_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DecodeArgs a;
+  a.B = B;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.hist_pt = hist_pt;
+  a.max_hist_pages = max_hist_pages;
+  a.bf16_pt = bf16_pt;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.algo = c->algo;
+  choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, 4, &a.nsplit,
+                &a.pages_per_split);
+  a.ev0 = a.ev1 = nullptr;
+  if (c->prof_on && c->prof_n < c->prof_cap) {
+    a.ev0 = c->prof_ev[2 * c->prof_n];
+    a.ev1 = c->prof_ev[2 * c->prof_n + 1];
+    c->prof_n++;
+  }
+  return launch_decode(view(c, layer), c->dws, a, st);
+}
+
+int oscar_get_status(oscar_cache* c, int* code) {
+  if (!c || !code) return OSCAR_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return OSCAR_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, c->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return OSCAR_ERR_CUDA;
+  *code = v;
+  return v == 0 ? OSCAR_OK : OSCAR_ERR_DEVICE_STATUS;
+}
+
+int oscar_pack_rotated(oscar_cache* c, int layer, int kind, const float* xrot, const int32_t* page_ids,
+                       const int32_t* rows, int N, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || N < 0 || (kind != OSCAR_KIND_K && kind != OSCAR_KIND_V))
+    return OSCAR_ERR_INVALID_ARG;
+  if (N == 0) return OSCAR_OK;
+  if (!xrot || !page_ids || !rows) return OSCAR_ERR_INVALID_ARG;
+  return launch_pack_rotated(view(c, layer), kind, xrot, page_ids, rows, N, static_cast<cudaStream_t>(stream));
+}
+
+int oscar_rotate(oscar_cache* c, int layer, int kind, const void* x, float* y, int N, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || N < 0 || (kind != OSCAR_KIND_K && kind != OSCAR_KIND_V))
+    return OSCAR_ERR_INVALID_ARG;
+  if (N == 0) return OSCAR_OK;
+  if (!x || !y) return OSCAR_ERR_INVALID_ARG;
+  return launch_rotate(view(c, layer), kind, x, y, N, static_cast<cudaStream_t>(stream));
+}
+
+int oscar_bf16_decode_workspace_bytes(int max_batch, int num_q_heads, int max_splits, size_t* bytes) {
+  if (max_batch < 1 || num_q_heads < 1 || max_splits < 1 || !bytes) return OSCAR_ERR_INVALID_ARG;
+  *bytes = kAlign + align_up((size_t)max_batch * num_q_heads * max_splits * kPartFloats * sizeof(float));
+  return OSCAR_OK;
+}
+
+int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_pages, int num_pages, const void* q,
+                      const int32_t* seq_lens, const int32_t* page_table, int max_pages, float sm_scale, void* out,
+                      int out_dtype, float* lse, void* workspace, size_t workspace_bytes, int max_splits,
+                      void* stream) {
+  if (B < 0 || num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads || num_pages < 0 || max_pages < 1 ||
+      max_splits < 1)
+    return OSCAR_ERR_INVALID_ARG;
+  if (!is_pow2_le8(num_q_heads / num_kv_heads)) return OSCAR_ERR_UNSUPPORTED;
+  if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
+  if (B == 0) return OSCAR_OK;
+  if (!kv_pages || !q || !seq_lens || !page_table || !out || !workspace) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return OSCAR_ERR_INVALID_ARG;
+  size_t need = 0;
+  oscar_bf16_decode_workspace_bytes(B, num_q_heads, max_splits, &need);
+  if (workspace_bytes < need) return OSCAR_ERR_INVALID_ARG;
+  int rc = configure_once();
+  if (rc != OSCAR_OK) return rc;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  int nsplit, pps;
+  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, &nsplit, &pps);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
+                            sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
+                            pps, reinterpret_cast<int*>(w), static_cast<cudaStream_t>(stream));
+}
+
+int oscar_profile_begin(oscar_cache* c, int capacity) {
+  if (!c || capacity < 1) return OSCAR_ERR_INVALID_ARG;
+  while ((int)c->prof_ev.size() < 2 * capacity) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return OSCAR_ERR_CUDA;
+    c->prof_ev.push_back(e);
+  }
+  c->prof_cap = capacity;
+  c->prof_n = 0;
+  c->prof_on = true;
+  return OSCAR_OK;
+}
+
+int oscar_profile_read(oscar_cache* c, double* total_ms, int* launches) {
+  if (!c || !total_ms || !launches) return OSCAR_ERR_INVALID_ARG;
+  c->prof_on = false;
+  double tot = 0.0;
+  for (int i = 0; i < c->prof_n; ++i) {
+    if (cudaEventSynchronize(c->prof_ev[2 * i + 1]) != cudaSuccess) return OSCAR_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, c->prof_ev[2 * i], c->prof_ev[2 * i + 1]) != cudaSuccess) return OSCAR_ERR_CUDA;
+    tot += ms;
+  }
+  *total_ms = tot;
+  *launches = c->prof_n;
+  return OSCAR_OK;
+}
+
+}  // extern "C"

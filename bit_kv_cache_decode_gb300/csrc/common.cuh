@@ -1,0 +1,69 @@
+// Shared device definitions of the OSCAR INT2 KV-cache library (sm_103a).
+//
+// Geometry of the mixed-precision token pool (news article "超越 TurboQuant…
+// Together AI 最新论文 OSCAR…", section "OSCAR 的设计思路": BF16 sink | INT2
+// history | BF16 recent, 4 two-bit codes per byte; MarkTechPost article
+// "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局": 64-channel
+// groups, per-token asymmetric INT2).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/oscar.h"
+
+namespace oscar {
+
+constexpr int kD = 128;                       // head_dim
+constexpr int kG = 64;                        // channels per quantisation group
+constexpr int kNG = kD / kG;                  // groups per token row
+constexpr int kP = 64;                        // tokens per page
+constexpr int kCodeBytes = kP * kD / 4;       // 2048: K (or V) codes of a page block
+constexpr int kMetaBytes = kP * kNG * 4;      // 512: fp16 (scale, zero) per group per row
+constexpr int kKCodesOff = 0;
+constexpr int kVCodesOff = kCodeBytes;
+constexpr int kKMetaOff = 2 * kCodeBytes;
+constexpr int kVMetaOff = 2 * kCodeBytes + kMetaBytes;
+constexpr int kBlockBytes = 2 * kCodeBytes + 2 * kMetaBytes;   // 5120
+constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D] then V [P][D]
+// rotation parameters per kv head: U_K [D][D], U_V [D][D], tau_K [D], tau_V [D] (float32)
+constexpr int kParamFloats = 2 * kD * kD + 2 * kD;
+constexpr int kUKOff = 0, kUVOff = kD * kD, kTauKOff = 2 * kD * kD, kTauVOff = 2 * kD * kD + kD;
+// one split partial: m (log2 units), l, then acc[D]; padded to 132 floats (528 B, 16 B aligned)
+constexpr int kPartFloats = kD + 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Device view of one layer of a cache.
+struct LayerView {
+  uint8_t* int2;          // [n_int2][hkv][kBlockBytes]
+  uint8_t* bf16;          // [n_bf16][hkv][kBf16BlockBytes]
+  const float* params;    // [hkv][kParamFloats]
+  int n_int2, n_bf16, hkv, hq, sink, recent, v_explicit;
+  int* status;            // device status word
+};
+
+__device__ __forceinline__ void flag(int* status, int bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ const uint8_t* int2_block(const LayerView& lv, int page, int head) {
+  return lv.int2 + ((size_t)page * lv.hkv + head) * kBlockBytes;
+}
+__device__ __forceinline__ uint8_t* int2_block_w(const LayerView& lv, int page, int head) {
+  return lv.int2 + ((size_t)page * lv.hkv + head) * kBlockBytes;
+}
+__device__ __forceinline__ __nv_bfloat16* bf16_row(const LayerView& lv, int page, int head, int kind, int row) {
+  return reinterpret_cast<__nv_bfloat16*>(lv.bf16 + ((size_t)page * lv.hkv + head) * kBf16BlockBytes) +
+         (size_t)kind * kP * kD + (size_t)row * kD;
+}
+
+// Byte offset, inside a page block, of packed byte b (0..31) of row t in the V codes region:
+// rows (2p, 2p+1) share 64 bytes; channel octet o = b/2 is a 32-bit word whose low half is row 2p.
+__device__ __forceinline__ int v_byte_off(int t, int b) {
+  return kVCodesOff + (t >> 1) * 64 + (b >> 1) * 4 + (t & 1) * 2 + (b & 1);
+}
+
+// 7-bit bit reversal (d = 128).
+__device__ __forceinline__ int bitrev7(int i) { return (int)(__brev((unsigned)i) >> 25); }
+
+}  // namespace oscar

@@ -1,0 +1,61 @@
+// Host-side launch interface of the OSCAR kernels (sm_103a).
+#pragma once
+
+#include "common.cuh"
+
+namespace oscar {
+
+constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
+constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
+constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4;           // U + row + 4 partial rows
+constexpr int kQprepSmem = (kD * kD + 8 * kD) * 4;                 // U_K + up to 8 query rows
+constexpr int kMergeSmem = (kD * (kD + 1) + 4 * kD) * 4;           // padded U_V + work rows
+
+// Decode workspace carved from the caller's workspace buffer.
+struct DecodeWorkspace {
+  float* qrot;        // [max_batch][hq][kD] rotated queries (float32, rotated channel order)
+  uint32_t* qfrag;    // [max_batch][hkv][kFragWords] fp16 MMA B fragments of the rotated queries
+  float* qsum;        // [max_batch][hq][kNG] per-group sums of the rotated query (float32)
+  float* partials;    // [max_batch][hq][max_splits + 1][kPartFloats]
+  int max_splits;
+};
+
+// B fragments of one kv head's query group for the tensor-core decode:
+// 8 k-blocks x 2 n-tiles x 32 lanes x 2 registers.
+constexpr int kFragWords = 8 * 2 * 32 * 2;
+
+int launch_pack_rotated(const LayerView& lv, int kind, const float* xrot, const int* page_ids, const int* rows,
+                        int N, cudaStream_t st);
+int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N, cudaStream_t st);
+int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, const int* cu_seqlens, int total,
+                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
+int launch_append(const LayerView& lv, int B, const void* k, const void* v, const int* seq_lens_before,
+                  const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
+int configure_write_path_kernels();
+
+struct DecodeArgs {
+  int B;
+  const void* q;
+  const int* seq_lens;
+  const int* hist_pt;
+  int max_hist_pages;
+  const int* bf16_pt;
+  float sm_scale;
+  void* out;
+  int out_dtype;
+  float* lse;
+  int nsplit;            // history splits launched per (request, kv head)
+  int pages_per_split;
+  int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
+  cudaEvent_t ev0, ev1;  // optional events around the history kernel (may be null)
+};
+
+int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
+int configure_decode_kernels();
+
+int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,
+                       const int* seq_lens, const int* page_table, int max_pages, float sm_scale, void* out,
+                       int out_dtype, float* lse, float* partials, int max_splits, int nsplit, int pages_per_split,
+                       int* status, cudaStream_t st);
+
+}  // namespace oscar

@@ -1,0 +1,296 @@
+// Write path of the OSCAR mixed-precision token pool (sm_103a): rotate, clip,
+// quantise, pack and place tokens (MarkTechPost article "Together AI 开源 OSCAR…",
+// section "服务系统：混合精度缓存布局", write path; news article "超越 TurboQuant…
+// OSCAR…", section "OSCAR 的设计思路": new tokens enter the recent window and the
+// oldest recent token is demoted into the INT2 history).
+#include "kernels.cuh"
+#include "rotate.cuh"
+
+namespace oscar {
+
+namespace {
+
+__device__ __forceinline__ bool valid_page(int p, int n) { return p >= 0 && p < n; }
+
+// Copy one bf16 row (128 values) from global to the float array xs (shared), one warp.
+__device__ __forceinline__ void load_row_f32(const __nv_bfloat16* src, float* xs) {
+  const int lane = threadIdx.x & 31;
+  const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(src);
+  float2 a = __bfloat1622float2(s2[lane]);
+  float2 b = __bfloat1622float2(s2[lane + 32]);
+  xs[2 * lane] = a.x; xs[2 * lane + 1] = a.y;
+  xs[64 + 2 * lane] = b.x; xs[64 + 2 * lane + 1] = b.y;
+}
+
+// Copy one bf16 row (256 bytes) src -> dst, one warp (8 bytes per lane).
+__device__ __forceinline__ void copy_row_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst) {
+  const int lane = threadIdx.x & 31;
+  reinterpret_cast<uint2*>(dst)[lane] = reinterpret_cast<const uint2*>(src)[lane];
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Pre-rotated float32 rows -> quantised INT2 history rows (debug / bit-exact check).
+// One warp per (token, kv head).
+__global__ void k_pack_rotated(LayerView lv, int kind, const float* __restrict__ xrot,
+                               const int* __restrict__ page_ids, const int* __restrict__ rows, int N) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= N * lv.hkv) return;
+  const int n = warp / lv.hkv, h = warp % lv.hkv;
+  const int page = page_ids[n], row = rows[n];
+  if (!valid_page(page, lv.n_int2) || row < 0 || row >= kP) {
+    if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE);
+    return;
+  }
+  const float* x = xrot + ((size_t)n * lv.hkv + h) * kD;
+  float y[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) y[r] = x[rot_channel(lane, r)];
+  const float* tau = lv.params + (size_t)h * kParamFloats + (kind == OSCAR_KIND_K ? kTauKOff : kTauVOff);
+  quantize_pack_row(y, tau, int2_block_w(lv, page, h), row, kind);
+}
+
+// ---------------------------------------------------------------------------
+// y = x R for N rows of every kv head (debug). One warp per (token, head).
+__global__ void k_rotate(LayerView lv, int kind, const __nv_bfloat16* __restrict__ x, float* __restrict__ y, int N) {
+  __shared__ float xs[4][kD];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = blockIdx.x * (blockDim.x >> 5) + wib;
+  if (warp >= N * lv.hkv) return;
+  const int n = warp / lv.hkv, h = warp % lv.hkv;
+  load_row_f32(x + ((size_t)n * lv.hkv + h) * kD, xs[wib]);
+  __syncwarp();
+  const float* U = lv.params + (size_t)h * kParamFloats + (kind == OSCAR_KIND_K ? kUKOff : kUVOff);
+  float v[1][4];
+  warp_rotate<1>(U, xs[wib], v);
+  float* out = y + ((size_t)n * lv.hkv + h) * kD;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) out[rot_channel(lane, r)] = v[0][r];
+}
+
+// ---------------------------------------------------------------------------
+// Bulk prefill. grid = (ceil(total / kPrefillTok), hkv, 2 kinds); block = 128 threads.
+// Each CTA stages U of (head, kind) in shared memory and handles kPrefillTok
+// consecutive tokens, 8 rows per warp pass. History rows are rotated (V only
+// in explicit mode), clipped, quantised and packed; sink and recent rows are
+// copied as bf16.
+__global__ void __launch_bounds__(128) k_prefill(LayerView lv, const __nv_bfloat16* __restrict__ k,
+                                                 const __nv_bfloat16* __restrict__ v,
+                                                 const int* __restrict__ cu_seqlens, int B, int total,
+                                                 const int* __restrict__ hist_pt, int max_hist_pages,
+                                                 const int* __restrict__ bf16_pt) {
+  extern __shared__ __align__(16) float smem[];
+  float* Us = smem;                       // [128][128]
+  float* xs_all = smem + kD * kD;         // [4 warps][8 rows][128]
+  const int h = blockIdx.y, kind = blockIdx.z;
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool rotate = (kind == OSCAR_KIND_K) || lv.v_explicit;
+  const float* prm = lv.params + (size_t)h * kParamFloats;
+  if (rotate) {
+    const float4* src = reinterpret_cast<const float4*>(prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff));
+    float4* dst = reinterpret_cast<float4*>(Us);
+    for (int i = threadIdx.x; i < kD * kD / 4; i += blockDim.x) dst[i] = src[i];
+  }
+  __syncthreads();
+  const float* tau = prm + (kind == OSCAR_KIND_K ? kTauKOff : kTauVOff);
+  const __nv_bfloat16* src_all = (kind == OSCAR_KIND_K) ? k : v;
+  float* xs = xs_all + wib * 8 * kD;
+  const int bf16_per_req = (lv.sink + lv.recent) / kP;
+  const int tok0 = blockIdx.x * kPrefillTok;
+  const int tok1 = min(tok0 + kPrefillTok, total);
+  for (int base = tok0 + wib * 8; base < tok1; base += 4 * 8) {
+    // classify up to 8 rows; stage the history rows for rotation
+    int where[8];      // -1: nothing, 0: history, 1: bf16
+    int page[8], row[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      where[t] = -1; page[t] = 0; row[t] = 0;
+      const int g = base + t;
+      if (g >= tok1) continue;
+      int lo = 0, hi = B;                         // request r: cu[r] <= g < cu[r+1]
+      while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (cu_seqlens[mid] <= g) lo = mid; else hi = mid; }
+      const int r = lo, pos = g - cu_seqlens[r], L = cu_seqlens[r + 1] - cu_seqlens[r];
+      if (pos < lv.sink) {
+        page[t] = bf16_pt[r * bf16_per_req + pos / kP]; row[t] = pos % kP; where[t] = 1;
+      } else if (pos >= max(lv.sink, L - lv.recent)) {
+        const int slot = (pos - lv.sink) % lv.recent;
+        page[t] = bf16_pt[r * bf16_per_req + lv.sink / kP + slot / kP]; row[t] = slot % kP; where[t] = 1;
+      } else {
+        const int hh = pos - lv.sink;
+        if (hh / kP >= max_hist_pages) { if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN); continue; }
+        page[t] = hist_pt[r * max_hist_pages + hh / kP]; row[t] = hh % kP; where[t] = 0;
+      }
+      const int cap = where[t] == 0 ? lv.n_int2 : lv.n_bf16;
+      if (!valid_page(page[t], cap)) { if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE); where[t] = -1; }
+    }
+    bool any_hist = false;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const __nv_bfloat16* src = src_all + ((size_t)(base + t) * lv.hkv + h) * kD;
+      if (where[t] == 1) {
+        copy_row_bf16(src, bf16_row(lv, page[t], h, kind, row[t]));
+      } else if (where[t] == 0) {
+        load_row_f32(src, xs + t * kD);
+        any_hist = true;
+      }
+    }
+    if (!any_hist) continue;
+    __syncwarp();
+    float y[8][4];
+    if (rotate) {
+      warp_rotate<8>(Us, xs, y);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) y[t][r] = xs[t * kD + rot_channel(lane, r)];
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (where[t] == 0) quantize_pack_row(y[t], tau, int2_block_w(lv, page[t], h), row[t], kind);
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Append one token per request with demotion. grid = (B, hkv, 2 kinds); block = 128.
+// The CTA stages U in shared memory (when a demotion needs it), rotates the
+// demoted row with 4 warps each summing 32 rows of U, then warp 0 finishes
+// the Hadamard/bit-reversal, quantises and packs. Only after that is the ring
+// slot overwritten with the new token.
+__global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat16* __restrict__ k,
+                                                const __nv_bfloat16* __restrict__ v,
+                                                const int* __restrict__ seq_lens_before,
+                                                const int* __restrict__ hist_pt, int max_hist_pages,
+                                                const int* __restrict__ bf16_pt) {
+  extern __shared__ __align__(16) float smem[];
+  float* Us = smem;                 // [128][128]
+  float* xs = smem + kD * kD;       // [128]
+  float* part = xs + kD;            // [4][128]
+  const int b = blockIdx.x, h = blockIdx.y, kind = blockIdx.z;
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bf16_per_req = (lv.sink + lv.recent) / kP;
+  const int L_old = seq_lens_before[b];
+  if (L_old < 0) { if (threadIdx.x == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN); return; }
+  const float* prm = lv.params + (size_t)h * kParamFloats;
+  const bool rotate = (kind == OSCAR_KIND_K) || lv.v_explicit;
+  // --- demotion of the oldest recent token ---
+  if (L_old >= lv.sink + lv.recent) {
+    const int old = L_old - lv.recent;
+    const int slot = (old - lv.sink) % lv.recent;
+    const int spage = bf16_pt[b * bf16_per_req + lv.sink / kP + slot / kP];
+    const int hh = old - lv.sink;
+    const bool ok_h = hh / kP < max_hist_pages;
+    const int hpage = ok_h ? hist_pt[b * max_hist_pages + hh / kP] : -1;
+    if (!ok_h || !valid_page(spage, lv.n_bf16) || !valid_page(hpage, lv.n_int2)) {
+      if (threadIdx.x == 0) flag(lv.status, ok_h ? OSCAR_STATUS_BAD_PAGE : OSCAR_STATUS_BAD_SEQLEN);
+    } else {
+      const __nv_bfloat16* src = bf16_row(lv, spage, h, kind, slot % kP);
+      if (threadIdx.x < 64) {
+        float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(src)[threadIdx.x]);
+        xs[2 * threadIdx.x] = f.x; xs[2 * threadIdx.x + 1] = f.y;
+      }
+      if (rotate) {
+        const float4* us = reinterpret_cast<const float4*>(prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff));
+        float4* ud = reinterpret_cast<float4*>(Us);
+#pragma unroll 8
+        for (int i = threadIdx.x; i < kD * kD / 4; i += 128) ud[i] = us[i];
+      }
+      __syncthreads();
+      float y[4];
+      if (rotate) {
+        // warp w sums rows [32w, 32w+32) of U
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int i = wib * 32; i < wib * 32 + 32; ++i) {
+          const float xi = xs[i];
+          const float* row = Us + i * kD + lane;
+          acc[0] = fmaf(xi, row[0], acc[0]); acc[1] = fmaf(xi, row[32], acc[1]);
+          acc[2] = fmaf(xi, row[64], acc[2]); acc[3] = fmaf(xi, row[96], acc[3]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) part[wib * kD + lane + 32 * r] = acc[r];
+        __syncthreads();
+        if (wib == 0) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int j = lane + 32 * r;
+            y[r] = ((part[j] + part[kD + j]) + part[2 * kD + j]) + part[3 * kD + j];
+          }
+          fwht128(y);
+        }
+      } else if (wib == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) y[r] = xs[rot_channel(lane, r)];
+      }
+      if (wib == 0) {
+        const float* tau = prm + (kind == OSCAR_KIND_K ? kTauKOff : kTauVOff);
+        quantize_pack_row(y, tau, int2_block_w(lv, hpage, h), hh % kP, kind);
+      }
+      __syncthreads();   // the slot is read above before it is overwritten below
+    }
+  }
+  // --- write the new token ---
+  if (wib != 0) return;
+  const int pos = L_old;
+  int page, row;
+  if (pos < lv.sink) {
+    page = bf16_pt[b * bf16_per_req + pos / kP]; row = pos % kP;
+  } else {
+    const int slot = (pos - lv.sink) % lv.recent;
+    page = bf16_pt[b * bf16_per_req + lv.sink / kP + slot / kP]; row = slot % kP;
+  }
+  if (!valid_page(page, lv.n_bf16)) { if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE); return; }
+  const __nv_bfloat16* src = (kind == OSCAR_KIND_K ? k : v) + ((size_t)b * lv.hkv + h) * kD;
+  copy_row_bf16(src, bf16_row(lv, page, h, kind, row));
+}
+
+// ---------------------------------------------------------------------------
+// host launchers
+
+int launch_pack_rotated(const LayerView& lv, int kind, const float* xrot, const int* page_ids, const int* rows,
+                        int N, cudaStream_t st) {
+  if (N == 0) return OSCAR_OK;
+  const int warps = N * lv.hkv, wpb = 4;
+  k_pack_rotated<<<(warps + wpb - 1) / wpb, wpb * 32, 0, st>>>(lv, kind, xrot, page_ids, rows, N);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N, cudaStream_t st) {
+  if (N == 0) return OSCAR_OK;
+  const int warps = N * lv.hkv, wpb = 4;
+  k_rotate<<<(warps + wpb - 1) / wpb, wpb * 32, 0, st>>>(lv, kind, static_cast<const __nv_bfloat16*>(x), y, N);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, const int* cu_seqlens, int total,
+                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st) {
+  if (total == 0 || B == 0) return OSCAR_OK;
+  dim3 grid((total + kPrefillTok - 1) / kPrefillTok, lv.hkv, 2);
+  k_prefill<<<grid, 128, kPrefillSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
+                                             static_cast<const __nv_bfloat16*>(v), cu_seqlens, B, total, hist_pt,
+                                             max_hist_pages, bf16_pt);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+int launch_append(const LayerView& lv, int B, const void* k, const void* v, const int* seq_lens_before,
+                  const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st) {
+  if (B == 0) return OSCAR_OK;
+  dim3 grid(B, lv.hkv, 2);
+  k_append<<<grid, 128, kAppendSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
+                                           static_cast<const __nv_bfloat16*>(v), seq_lens_before, hist_pt,
+                                           max_hist_pages, bf16_pt);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}
+
+int configure_write_path_kernels() {
+  if (cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_append, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  return OSCAR_OK;
+}
+
+}  // namespace oscar

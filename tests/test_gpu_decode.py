@@ -1,0 +1,178 @@
+"""GPU parity of decode attention against the oracle's fp64 attention over the
+same dequantised cache (the pool bytes the GPU wrote, decoded by the oracle).
+
+Tolerance: per (request, q-head) row, max_i |o_i - ref_i| / max_i |ref_i| <= 2e-3
+on fp32 output. With bf16 output each element must also lie within one bf16
+ulp of the reference plus the same 2e-3 slack (bf16 rounding alone reaches
+2^-8 relative)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import bit_kv_cache_decode_gb300 as osc
+    from gpu_cases import (DEV, bf16_ulp, head_params, pool_from_device, queries, row_rel_err, to_dev_bf16, tokens,
+                           upload_params)
+import synth
+from oracle import attention as A
+from oracle import pool as P
+
+TOL = 2e-3
+ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma")]
+
+
+def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64):
+    """Prefill B requests on the GPU. With shared_prefix > 0 all requests share their first
+    `shared_prefix` tokens (sink page and the history pages covering them)."""
+    B = len(lens)
+    nh = [max(0, (L - 320 + 63) // 64) for L in lens]
+    mhp = max(1, max(nh))
+    shp = (shared_prefix - 64) // 64 if shared_prefix else 0           # shared history pages
+    n_int2 = shp + sum(n - shp for n in nh) + 1
+    n_bf16 = 1 + 4 * B if shared_prefix else 5 * B
+    rng = np.random.default_rng(seed)
+    perm_i, perm_b = rng.permutation(n_int2).astype(np.int32), rng.permutation(n_bf16).astype(np.int32)
+    hist_pt = np.full((B, mhp), -1, np.int32)
+    bf16_pt = np.zeros((B, 5), np.int32)
+    oi, ob = shp, (1 if shared_prefix else 0)
+    for r in range(B):
+        hist_pt[r, :shp] = perm_i[:shp]
+        hist_pt[r, shp:nh[r]] = perm_i[oi:oi + nh[r] - shp]
+        oi += nh[r] - shp
+        if shared_prefix:
+            bf16_pt[r, 0] = perm_b[0]
+            bf16_pt[r, 1:] = perm_b[ob:ob + 4]
+            ob += 4
+        else:
+            bf16_pt[r] = perm_b[ob:ob + 5]
+            ob += 5
+    cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=n_int2,
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=max_splits, v_mode=v_mode)
+    cache = osc.OscarCache(cfg, device=DEV)
+    cache.set_decode_algo(algo)
+    prm = head_params(seed, 0, hkv)
+    upload_params(cache, 0, prm)
+    ks, vs = [], []
+    for r, L in enumerate(lens):
+        k, v = tokens(seed, 0, hkv, L, extra=r + 1)
+        if shared_prefix:
+            k0, v0 = tokens(seed, 0, hkv, shared_prefix, extra=0)
+            k[:shared_prefix], v[:shared_prefix] = k0, v0
+        ks.append(k)
+        vs.append(v)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cache.quantize_prefill(0, to_dev_bf16(np.concatenate(ks)), to_dev_bf16(np.concatenate(vs)), cu, hist_pt, bf16_pt)
+    assert cache.get_status() == 0
+    return cache, prm, hist_pt, bf16_pt
+
+
+def _check(cache, prm, hist_pt, bf16_pt, lens, gq, v_mode, seed, out_dtype=1, kv_heads=None):
+    hkv = cache.cfg.num_kv_heads
+    B = len(lens)
+    q = queries(seed, 0, hkv, gq, batch=B)
+    out = cache.decode_attention(0, to_dev_bf16(q), np.array(lens, np.int32), hist_pt, bf16_pt, synth.sm_scale(),
+                                 out_dtype=out_dtype,
+                                 lse=(lse_t := torch.zeros(B, hkv * gq, device=DEV, dtype=torch.float32)))
+    assert cache.get_status() == 0
+    got = out.double().cpu().numpy()
+    lse = lse_t.double().cpu().numpy()
+    pm = pool_from_device(cache, 0)
+    worst = 0.0
+    for r, L in enumerate(lens):
+        ref, ref_lse = A.decode_request(q[r], L, pm, hist_pt[r], bf16_pt[r], prm, v_mode == osc.V_ABSORBED,
+                                        synth.sm_scale(), kv_heads=kv_heads)
+        rows = ~np.isnan(ref[:, 0])
+        err = row_rel_err(got[r][rows], ref[rows])
+        worst = max(worst, float(err.max()))
+        assert np.abs(lse[r][rows] - ref_lse[rows]).max() < 2e-3 * max(1.0, np.abs(ref_lse[rows]).max())
+        if out_dtype == osc.OUT_FP32:
+            assert err.max() <= TOL, (r, L, err.max())
+        else:
+            slack = TOL * np.abs(ref[rows]).max(axis=-1, keepdims=True)
+            assert np.all(np.abs(got[r][rows] - ref[rows]) <= bf16_ulp(ref[rows]) + slack), (r, L)
+    return worst
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_tiny_config_decode(algo, v_mode, out_dtype):
+    # one request, one kv head shared by 4 query heads, 64 sink + 704 history + 256 recent
+    lens, gq = [1024], 4
+    cache, prm, hp, bp = _build(lens, 1, gq, v_mode, seed=11, algo=algo)
+    _check(cache, prm, hp, bp, lens, gq, v_mode, seed=11, out_dtype=out_dtype)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_edge_lengths(algo):
+    lens = [1, 2, 63, 64, 65, 319, 320, 321, 383, 384, 385, 448, 1000]
+    cache, prm, hp, bp = _build(lens, 2, 4, 0, seed=12, algo=algo)
+    _check(cache, prm, hp, bp, lens, 4, 0, seed=12)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("gq", [1, 2, 8])
+def test_gqa_widths(algo, gq):
+    lens = [900, 1500]
+    cache, prm, hp, bp = _build(lens, 2, gq, 1, seed=13, algo=algo)
+    _check(cache, prm, hp, bp, lens, gq, 1, seed=13)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_shared_prefix_batch(algo):
+    lens = [64 + 64 * 20 + 300, 64 + 64 * 20 + 700, 64 + 64 * 20 + 256]
+    cache, prm, hp, bp = _build(lens, 2, 4, 0, seed=14, shared_prefix=64 + 64 * 20, algo=algo)
+    assert (hp[0, :20] == hp[1, :20]).all() and (bp[:, 0] == bp[0, 0]).all()
+    _check(cache, prm, hp, bp, lens, 4, 0, seed=14)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_many_splits_ragged_tail(algo):
+    # long enough for many splits and a partial last page
+    lens = [64 + 64 * 150 + 37 + 256]
+    cache, prm, hp, bp = _build(lens, 1, 4, 0, seed=15, algo=algo, max_splits=200)
+    _check(cache, prm, hp, bp, lens, 4, 0, seed=15)
+
+
+def test_bad_page_in_decode_reported():
+    lens = [2000]
+    cache, prm, hp, bp = _build(lens, 1, 4, 0, seed=16)
+    hp_bad = hp.copy()
+    hp_bad[0, 3] = -7
+    q = queries(16, 0, 1, 4)
+    cache.decode_attention(0, to_dev_bf16(q), np.array(lens, np.int32), hp_bad, bp, synth.sm_scale())
+    assert cache.get_status() & osc.STATUS_BAD_PAGE
+    # a sequence longer than its page table
+    cache.decode_attention(0, to_dev_bf16(q), np.array([64 * 100], np.int32), hp, bp, synth.sm_scale())
+    assert cache.get_status() & osc.STATUS_BAD_SEQLEN
+
+
+def test_bf16_comparison_kernel():
+    rng = np.random.default_rng(17)
+    hkv, gq, B = 2, 4, 3
+    lens = [1, 700, 3000]
+    mp = (max(lens) + 63) // 64
+    npages = sum((L + 63) // 64 for L in lens)
+    perm = rng.permutation(npages).astype(np.int32)
+    pt = np.zeros((B, mp), np.int32)
+    pages = np.zeros((npages, hkv, 2, 64, 128), np.uint16)
+    o = 0
+    for r, L in enumerate(lens):
+        n = (L + 63) // 64
+        pt[r, :n] = perm[o:o + n]
+        o += n
+        k, v = tokens(17, 0, hkv, L, extra=r)
+        for pos in range(L):
+            pages[pt[r, pos // 64], :, 0, pos % 64] = synth.bf16_bits(k[pos])
+            pages[pt[r, pos // 64], :, 1, pos % 64] = synth.bf16_bits(v[pos])
+    q = queries(17, 0, hkv, gq, batch=B)
+    ws = torch.zeros(osc.bf16_decode_workspace_bytes(B, hkv * gq, 32), dtype=torch.uint8, device=DEV)
+    kv = torch.from_numpy(pages.view(np.int16)).to(DEV).view(torch.bfloat16)
+    out = osc.bf16_decode(kv, to_dev_bf16(q), np.array(lens, np.int32), pt, synth.sm_scale(), hkv, ws, 32,
+                          out_dtype=osc.OUT_FP32)
+    got = out.double().cpu().numpy()
+    for r, L in enumerate(lens):
+        ref, _ = A.bf16_decode_request(q[r], L, pages, pt[r], synth.sm_scale())
+        assert row_rel_err(got[r], ref).max() <= TOL

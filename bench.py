@@ -188,7 +188,7 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
     if cache.get_status() != 0:
         raise RuntimeError("device status error while building the workload")
     return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, B=B, H=H, hq=hq, layers=nl,
-                bf16_pages=bf16_pages, bf16_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
+                bf16_pages=bf16_pages, base_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
                 hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared)
 
 
@@ -306,7 +306,7 @@ def run_bf16(wl, args, q_all, device):
     ws = torch.zeros(osc.bf16_decode_workspace_bytes(B, hq, 512), dtype=torch.uint8, device=device)
     out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
     seq = torch.full((B,), L, dtype=torch.int32, device=device)
-    pages, pt = wl["bf16_pages"], wl["bf16_pt"]
+    pages, pt = wl["bf16_pages"], wl["base_pt"]
     sm = synth.sm_scale()
 
     def step(i):

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "liboscar.so")
 
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_STATUS, ERR_TIMEOUT, ERR_NOT_ORTHOGONAL = -1, -2, -3, -4, -5, -6
+ERR_TOO_LARGE = -7
 STATUS_BAD_PAGE, STATUS_BAD_SEQLEN, STATUS_TIMEOUT = 1, 2, 4
 V_ABSORBED, V_EXPLICIT = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
@@ -33,6 +34,7 @@ EXPORTS = (
     "oscar_quantize_prefill", "oscar_append_kv", "oscar_decode_attention", "oscar_set_decode_algo",
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
+    "oscar_decode_attention_noalloc",
 )
 
 
@@ -73,6 +75,8 @@ def _load() -> ctypes.CDLL:
         "oscar_calibrate": [vp, vp, vp, c_int, c_float, c_float, c_float, vp, vp, vp, vp, vp, vp],
         "oscar_profile_begin": [vp, c_int],
         "oscar_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)],
+        "oscar_decode_attention_noalloc": [ctypes.POINTER(Layout), vp, c_int, c_int, vp, i32p, i32p, c_int, i32p,
+                                           c_float, vp, c_int, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -303,4 +307,26 @@ def calibrate(Q, K, V, sm_scale: float, c_K: float = 0.96, c_V: float = 0.92):
     _check(_lib.oscar_calibrate(_ptr(q), _ptr(k), _ptr(v), q.shape[0], float(sm_scale), float(c_K), float(c_V),
                                 _ptr(out["U_K"]), _ptr(out["U_V"]), _ptr(out["tau_K"]), _ptr(out["tau_V"]),
                                 _ptr(out["eig_K"]), _ptr(out["eig_V"])), "oscar_calibrate")
+    return out
+
+
+def decode_attention_noalloc(cfg: CacheConfig, pool, layer: int, q, seq_lens, hist_pt, bf16_pt, sm_scale: float,
+                             out=None, out_dtype: int = OUT_BF16, lse=None, status=None, stream=None):
+    """Decode attention through the allocation-free entry point, for callers that cannot allocate device
+    memory (for instance inside CUDA graph capture): same result as OscarCache.decode_attention, with the
+    cache given by its config and pool tensor, scratch in the library's fixed device array, and the call's
+    status bits written to ``status`` (an int32 device tensor of one element) when given. Calls that may
+    overlap on the GPU share that scratch and must not be issued concurrently."""
+    import torch
+    dev = pool.device
+    sl = _dev_i32(seq_lens, dev)
+    hp = _dev_i32(hist_pt, dev)
+    bp = _dev_i32(bf16_pt, dev)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16, device=dev)
+    lay = cfg.layout()
+    _check(_lib.oscar_decode_attention_noalloc(ctypes.byref(lay), _ptr(pool), layer, sl.numel(), _ptr(q), _ptr(sl),
+                                               _ptr(hp), hp.shape[1] if hp.dim() == 2 else 0, _ptr(bp),
+                                               float(sm_scale), _ptr(out), out_dtype, _ptr(lse), _ptr(status),
+                                               _stream(stream)), "oscar_decode_attention_noalloc")
     return out

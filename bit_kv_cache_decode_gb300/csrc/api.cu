@@ -118,6 +118,7 @@ const char* oscar_error_string(int code) {
     case OSCAR_ERR_DEVICE_STATUS: return "device status word has error bits";
     case OSCAR_ERR_TIMEOUT: return "bounded device wait expired";
     case OSCAR_ERR_NOT_ORTHOGONAL: return "rotation is not orthogonal (max|U^T U - I| > 1e-3)";
+    case OSCAR_ERR_TOO_LARGE: return "call needs more than the fixed device scratch of the allocation-free decode";
     default: return "unknown status";
   }
 }
@@ -375,3 +376,37 @@ int oscar_profile_read(oscar_cache* c, double* total_ms, int* launches) {
 }
 
 }  // extern "C"
+
+namespace oscar {
+
+// Device view of layer `layer` of a pool laid out for `L`, with its status
+// word at `status`; for entry points that work without a cache handle.
+int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, LayerView* out) {
+  int rc = check_layout(L);
+  if (rc != OSCAR_OK) return rc;
+  if (!pool || !out || layer < 0 || layer >= L->num_layers) return OSCAR_ERR_INVALID_ARG;
+  size_t int2b, bf16b, prmb, layerb, poolb, wsb;
+  sizes(L, &int2b, &bf16b, &prmb, &layerb, &poolb, &wsb);
+  uint8_t* base = static_cast<uint8_t*>(pool) + (size_t)layer * layerb;
+  out->int2 = base;
+  out->bf16 = base + int2b;
+  out->params = reinterpret_cast<const float*>(base + int2b + bf16b);
+  out->n_int2 = L->num_int2_pages;
+  out->n_bf16 = L->num_bf16_pages;
+  out->hkv = L->num_kv_heads;
+  out->hq = L->num_q_heads;
+  out->sink = L->sink;
+  out->recent = L->recent;
+  out->v_explicit = L->v_mode == OSCAR_V_EXPLICIT;
+  out->status = status;
+  return OSCAR_OK;
+}
+
+// The history split choice of oscar_decode_attention, for at most max_splits splits.
+void decode_split_policy(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps) {
+  choose_splits(B, hkv, max_pages, max_splits, sms, 4, nsplit, pps);
+}
+
+int configure_kernels() { return configure_once(); }
+
+}  // namespace oscar

@@ -1,0 +1,114 @@
+// Decode attention that allocates no device memory (sm_103a).
+//
+// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
+// being captured (allocation is not a capturable stream operation), serving
+// engines whose allocator already owns all device memory and forbids side
+// allocations, and hosts that may not allocate on a latency-critical path.
+// oscar_decode_attention needs a caller-allocated workspace for its scratch
+// (rotated queries, query fragments and sums, split partials, status word);
+// this entry point runs the same kernels with that scratch taken from a fixed
+// static device array instead.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(4) << 20;   // 4 MiB per device
+constexpr int kMaxDevices = 64;
+
+// The scratch itself. Every GPU that loads the library holds it until the
+// process exits. In host code this name is only a stand-in for the symbol;
+// kernels get the device address resolved below.
+static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
+
+std::mutex g_mu;
+uint8_t* g_addr[kMaxDevices];
+int g_sms[kMaxDevices];
+
+// Once per device, with that device current: resolve the array's device address.
+int scratch_for_current_device(uint8_t** addr, int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return OSCAR_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return OSCAR_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+    g_sms[dev] = n;
+    g_addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *addr = g_addr[dev];
+  *sms = g_sms[dev];
+  return OSCAR_OK;
+}
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B,
+                                              const void* q, const int32_t* seq_lens, const int32_t* hist_pt,
+                                              int max_hist_pages, const int32_t* bf16_pt, float sm_scale, void* out,
+                                              int out_dtype, float* lse, int* status, void* stream) {
+  using namespace oscar;
+  if (!layout || !pool || B < 0 || max_hist_pages < 0) return OSCAR_ERR_INVALID_ARG;
+  if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
+  if (B == 0) return OSCAR_OK;
+  if (!q || !seq_lens || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || sm_scale == INFINITY) return OSCAR_ERR_INVALID_ARG;
+  LayerView lv;
+  int rc = pool_layer_view(layout, pool, layer, nullptr, &lv);
+  if (rc != OSCAR_OK) return rc;
+  // scratch carving: status word | rotated queries | query fragments | query group sums | partials
+  const size_t hq = layout->num_q_heads, hkv = layout->num_kv_heads;
+  const size_t fixed = 256 + up256((size_t)B * hq * kD * sizeof(float)) +
+                       up256((size_t)B * hkv * kFragWords * sizeof(uint32_t)) +
+                       up256((size_t)B * hq * kNG * sizeof(float));
+  const size_t per_slot = (size_t)B * hq * kPartFloats * sizeof(float);
+  if (fixed + 2 * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
+  rc = configure_kernels();
+  if (rc != OSCAR_OK) return rc;
+  uint8_t* scratch = nullptr;
+  int sms = 0;
+  rc = scratch_for_current_device(&scratch, &sms);
+  if (rc != OSCAR_OK) return rc;
+  const int max_slots = (int)std::min<size_t>((kScratchBytes - fixed) / per_slot, 4097);
+  DecodeWorkspace ws;
+  uint8_t* p = scratch;
+  int* dstatus = reinterpret_cast<int*>(p);
+  p += 256;
+  ws.qrot = reinterpret_cast<float*>(p);
+  p += up256((size_t)B * hq * kD * sizeof(float));
+  ws.qfrag = reinterpret_cast<uint32_t*>(p);
+  p += up256((size_t)B * hkv * kFragWords * sizeof(uint32_t));
+  ws.qsum = reinterpret_cast<float*>(p);
+  p += up256((size_t)B * hq * kNG * sizeof(float));
+  ws.partials = reinterpret_cast<float*>(p);
+  lv.status = dstatus;
+  DecodeArgs a;
+  a.B = B;
+  a.q = q;
+  a.seq_lens = seq_lens;
+  a.hist_pt = hist_pt;
+  a.max_hist_pages = max_hist_pages;
+  a.bf16_pt = bf16_pt;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.algo = OSCAR_DECODE_SIMT;
+  a.ev0 = a.ev1 = nullptr;
+  decode_split_policy(B, (int)hkv, max_hist_pages, max_slots - 1, sms, &a.nsplit, &a.pages_per_split);
+  ws.max_splits = a.nsplit;            // the BF16 partial sits right after the history splits
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps the previous call's contents: the status word must start at zero
+  if (cudaMemsetAsync(dstatus, 0, sizeof(int), st) != cudaSuccess) return OSCAR_ERR_CUDA;
+  rc = launch_decode(lv, ws, a, st);
+  if (rc != OSCAR_OK) return rc;
+  if (status && cudaMemcpyAsync(status, dstatus, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  return OSCAR_OK;
+}

@@ -59,3 +59,10 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
                        int* status, cudaStream_t st);
 
 }  // namespace oscar
+
+namespace oscar {
+// api.cu helpers for entry points that work without a cache handle
+int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, LayerView* out);
+void decode_split_policy(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps);
+int configure_kernels();
+}  // namespace oscar

@@ -257,6 +257,43 @@ int oscar_profile_begin(oscar_cache* cache, int capacity);
  * launches and their count. */
 int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
 
+/* ---- allocation-free decode ---------------------------------------------- */
+
+#define OSCAR_ERR_TOO_LARGE (-7)  /* the call needs more than the fixed device scratch */
+
+/* Decode attention that allocates nothing. The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc, such as code
+ * that runs while a CUDA graph is being captured (allocation is not a
+ * capturable operation), serving engines whose allocator already owns all
+ * device memory and forbids side allocations, and hosts that may not allocate
+ * on a latency-critical path.
+ *
+ * It computes exactly what oscar_decode_attention computes, with the same
+ * arguments, except:
+ *  - the cache is given by its layout and pool instead of a handle: `pool` is
+ *    the device buffer a cache with this `layout` was created on (rotation and
+ *    tokens already written through the other entry points);
+ *  - no workspace is used: the scratch (status word, rotated queries, split
+ *    partials) lives in a 4 MiB static device array inside the library, which
+ *    every GPU that loads the library holds until the process exits;
+ *  - this call's device status bits are copied to `status` (device int32,
+ *    may be NULL) at the end of the call.
+ * The call performs no cudaMalloc, cudaFree or other allocating call.
+ * Set-up: the first call on a device resolves the array's address for that
+ * device (cudaGetSymbolAddress) and configures the kernels; make that first
+ * call before any stream capture. Every call shares the array and it keeps the
+ * last call's contents (the status word is cleared at the start of each
+ * call): calls that may overlap on the GPU (different streams, or threads
+ * without ordering) race and give wrong results; calls ordered on one stream
+ * are safe. The history is split into fewer pieces when needed to fit; a call
+ * whose B * Hq * 1576 + B * Hkv * 4096 bytes (plus 1 KB) exceed 4 MiB, i.e. too
+ * many query rows even with one split, returns OSCAR_ERR_TOO_LARGE before any
+ * device work. */
+int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B, const void* q,
+                                   const int32_t* seq_lens, const int32_t* hist_pt, int max_hist_pages,
+                                   const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse,
+                                   int* status, void* stream);
+
 /* Human-readable name of a status code. */
 const char* oscar_error_string(int code);
 

@@ -60,7 +60,7 @@ void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, si
   *wsb = kAlign                                                    // status word
          + align_up(B * hq * kD * sizeof(float))                   // qrot
          + align_up(B * hkv * kFragWords * sizeof(uint32_t))       // qfrag
-         + align_up(B * hq * kNG * sizeof(float))                  // qsum
+         + align_up(B * hq * kQConst * sizeof(float))              // qconst
          + align_up(B * hq * (L->max_splits + 1) * kPartFloats * sizeof(float));  // partials
 }
 
@@ -93,16 +93,32 @@ int configure_once() {
   return rc;
 }
 
-// Split policy: enough (request, kv head, split) CTAs to fill the GPU a few times
-// over, never more splits than pages, and no empty trailing split.
-void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int* nsplit, int* pps) {
+// Split policy over the page-table width: choose the number of history splits
+// per (request, kv head) that minimises waves x (pages per CTA + a fixed
+// per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs; pages per
+// split are rounded up to `align` and there is no empty trailing split.
+void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int align, int* nsplit,
+                   int* pps) {
   if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
-  long want = ((long)sms * ctas_per_sm + (long)B * hkv - 1) / ((long)B * hkv);
-  int n = (int)std::min<long>(std::max<long>(want, 1), max_splits);
-  n = std::min(n, max_pages);
-  int p = (max_pages + n - 1) / n;
-  *pps = p;
-  *nsplit = (max_pages + p - 1) / p;
+  const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
+  const int nmax = std::min(max_splits, max_pages);
+  long best_cost = -1;
+  int best_p = max_pages;
+  for (int n = 1; n <= nmax; ++n) {
+    int p = (max_pages + n - 1) / n;
+    p = (p + align - 1) / align * align;
+    const int used = (max_pages + p - 1) / p;
+    const long waves = (units * used + slots - 1) / slots;
+    const long cost = waves * (p + 2L * align);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_p = p; }
+  }
+  *pps = best_p;
+  *nsplit = (max_pages + best_p - 1) / best_p;
+}
+
+void algo_policy(int algo, int gq, int* ctas_per_sm, int* align) {
+  if (algo == OSCAR_DECODE_MMA) { *ctas_per_sm = gq <= 4 ? 3 : 2; *align = 4; }
+  else { *ctas_per_sm = 4; *align = 1; }
 }
 
 }  // namespace
@@ -160,12 +176,12 @@ int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, 
   p += align_up(B * hq * kD * sizeof(float));
   c->dws.qfrag = reinterpret_cast<uint32_t*>(p);
   p += align_up(B * hkv * kFragWords * sizeof(uint32_t));
-  c->dws.qsum = reinterpret_cast<float*>(p);
-  p += align_up(B * hq * kNG * sizeof(float));
+  c->dws.qconst = reinterpret_cast<float*>(p);
+  p += align_up(B * hq * kQConst * sizeof(float));
   c->dws.partials = reinterpret_cast<float*>(p);
   c->dws.max_splits = layout->max_splits;
   c->sms = sms;
-  c->algo = OSCAR_DECODE_SIMT;
+  c->algo = kDefaultDecodeAlgo;
   c->prof_on = false;
   c->prof_cap = c->prof_n = 0;
   if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) { delete c; return OSCAR_ERR_CUDA; }
@@ -274,8 +290,12 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.out_dtype = out_dtype;
   a.lse = lse;
   a.algo = c->algo;
-  choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, 4, &a.nsplit,
-                &a.pages_per_split);
+  {
+    int cps, align;
+    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, &cps, &align);
+    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, &a.nsplit,
+                  &a.pages_per_split);
+  }
   a.ev0 = a.ev1 = nullptr;
   if (c->prof_on && c->prof_n < c->prof_cap) {
     a.ev0 = c->prof_ev[2 * c->prof_n];
@@ -340,7 +360,7 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   int nsplit, pps;
-  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, &nsplit, &pps);
+  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, &nsplit, &pps);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
@@ -403,8 +423,11 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 }
 
 // The history split choice of oscar_decode_attention, for at most max_splits splits.
-void decode_split_policy(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps) {
-  choose_splits(B, hkv, max_pages, max_splits, sms, 4, nsplit, pps);
+void decode_split_policy(int B, int hkv, int gq, int max_pages, int max_splits, int sms, int algo, int* nsplit,
+                         int* pps) {
+  int cps, align;
+  algo_policy(algo, gq, &cps, &align);
+  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, nsplit, pps);
 }
 
 int configure_kernels() { return configure_once(); }

@@ -66,7 +66,7 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   const size_t hq = layout->num_q_heads, hkv = layout->num_kv_heads;
   const size_t fixed = 256 + up256((size_t)B * hq * kD * sizeof(float)) +
                        up256((size_t)B * hkv * kFragWords * sizeof(uint32_t)) +
-                       up256((size_t)B * hq * kNG * sizeof(float));
+                       up256((size_t)B * hq * kQConst * sizeof(float));
   const size_t per_slot = (size_t)B * hq * kPartFloats * sizeof(float);
   if (fixed + 2 * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
   rc = configure_kernels();
@@ -84,8 +84,8 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   p += up256((size_t)B * hq * kD * sizeof(float));
   ws.qfrag = reinterpret_cast<uint32_t*>(p);
   p += up256((size_t)B * hkv * kFragWords * sizeof(uint32_t));
-  ws.qsum = reinterpret_cast<float*>(p);
-  p += up256((size_t)B * hq * kNG * sizeof(float));
+  ws.qconst = reinterpret_cast<float*>(p);
+  p += up256((size_t)B * hq * kQConst * sizeof(float));
   ws.partials = reinterpret_cast<float*>(p);
   lv.status = dstatus;
   DecodeArgs a;
@@ -99,9 +99,10 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.algo = OSCAR_DECODE_SIMT;
+  a.algo = kDefaultDecodeAlgo;
   a.ev0 = a.ev1 = nullptr;
-  decode_split_policy(B, (int)hkv, max_hist_pages, max_slots - 1, sms, &a.nsplit, &a.pages_per_split);
+  decode_split_policy(B, (int)hkv, (int)(hq / hkv), max_hist_pages, max_slots - 1, sms, a.algo, &a.nsplit,
+                      &a.pages_per_split);
   ws.max_splits = a.nsplit;            // the BF16 partial sits right after the history splits
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word must start at zero

@@ -67,21 +67,35 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query prologue: q~ = q R_K for every query head, in rotated channel order,
-// plus per-group sums of q~. grid = (hkv, B), block = 128, U_K staged in
-// shared memory; warp w handles the group's query heads w, w+4.
-__global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws) {
+// Query prologue: q~ = q R_K for every query head, in rotated channel order
+// (ws.qrot), the per-head constants (ws.qconst) and the fp16 B fragments of
+// the tensor-core history kernel (ws.qfrag). grid = (hkv, B), block = 128,
+// U_K staged in shared memory; warp w rotates the group's query heads w, w+4.
+//
+// Fragment encoding (decode_mma.cu unpacks a code c of channel ch as the fp16
+// value 1024 + c * 4^(ch % 4)): fragment value of channel ch of head h is
+// fp16(q~[h][ch] * 2^sigma_h * 4^-(ch % 4)), sigma_h a power-of-two scale that
+// puts max|q~| near 2^12, and the group's constant part is
+// off_g = 1024 * sum_{ch in g} fragment value, so that
+//   sum_{ch in g} (1024 + c 4^(ch%4)) frag(ch) - off_g = 2^sigma sum_{ch in g} c q~[ch].
+// k-block kb (16 channels) at lane (g', t') holds the pairs of k rows
+// (2t', 2t'+1) -> channels (32t'+kb, 32t'+kb+8) and (2t'+8, 2t'+9) ->
+// channels (32t'+16+kb, 32t'+24+kb); column g' is (head 4nt + g'/2, group g'%2)
+// and is zero where the channel is not in that group.
+__global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws,
+                                               float scale_log2) {
   extern __shared__ __align__(16) float smem[];
   float* Us = smem;
-  float* xs = smem + kD * kD;  // [8][128]
-  const int h = blockIdx.x, b = blockIdx.y;
+  float* xs = smem + kD * kD;  // [8][128]: raw query rows, then rotated rows in rotated channel order
+  __shared__ int sig[8];
+  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int gq = lv.hq / lv.hkv;
-  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wib = tid >> 5, lane = tid & 31;
   const float4* us = reinterpret_cast<const float4*>(lv.params + (size_t)h * kParamFloats + kUKOff);
   float4* ud = reinterpret_cast<float4*>(Us);
 #pragma unroll 8
-  for (int i = threadIdx.x; i < kD * kD / 4; i += 128) ud[i] = us[i];
-  for (int i = threadIdx.x; i < gq * kD; i += 128) {
+  for (int i = tid; i < kD * kD / 4; i += 128) ud[i] = us[i];
+  for (int i = tid; i < gq * kD; i += 128) {
     const int qi = i / kD, c = i % kD;
     xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq + qi) * kD + c]);
   }
@@ -89,14 +103,62 @@ __global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16
   for (int qi = wib; qi < gq; qi += 4) {
     float y[1][4];
     warp_rotate<1>(Us, xs + qi * kD, y);
+    __syncwarp();                                   // row qi fully read before it is overwritten
     const int hq = h * gq + qi;
     float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
-    float s = 0.f;
+    float s = 0.f, mx = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) { dst[rot_channel(lane, r)] = y[0][r]; s += y[0][r]; }
+    for (int r = 0; r < 4; ++r) {
+      const int ch = rot_channel(lane, r);
+      dst[ch] = y[0][r];
+      xs[qi * kD + ch] = y[0][r];
+      s += y[0][r];
+      mx = fmaxf(mx, fabsf(y[0][r]));
+    }
 #pragma unroll
     for (int m = 2; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);   // lanes of equal parity = one group
-    if (lane < 2) ws.qsum[((size_t)b * lv.hq + hq) * kNG + lane] = s;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    if (lane < 2) ws.qconst[((size_t)b * lv.hq + hq) * kQConst + kQSum0 + lane] = s;
+    if (lane == 0) {
+      int e = 0;
+      if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx in [2^(e-1), 2^e)
+      sig[qi] = min(max(12 - e, -60), 60);
+    }
+  }
+  __syncthreads();
+  if (tid < gq) {
+    const int qi = tid, hq = h * gq + qi;
+    float* qc = ws.qconst + ((size_t)b * lv.hq + hq) * kQConst;
+    const float sc = ldexpf(1.f, sig[qi]);
+    float off[kNG] = {0.f, 0.f}, sum[kNG] = {0.f, 0.f};
+    for (int ch = 0; ch < kD; ++ch) {
+      const float v = xs[qi * kD + ch];
+      const float f = __half2float(__float2half_rn(v * sc * ldexpf(1.f, -2 * (ch & 3))));
+      off[ch / kG] += f;
+      sum[ch / kG] += v;
+    }
+    qc[kQF] = scale_log2 * ldexpf(1.f, -sig[qi]);
+    qc[kQZ0] = scale_log2 * sum[0];
+    qc[kQZ1] = scale_log2 * sum[1];
+    qc[kQOff0] = 1024.f * off[0];
+    qc[kQOff1] = 1024.f * off[1];
+    qc[kQSigma] = (float)sig[qi];
+  }
+  const int nt_count = (gq + 3) / 4;
+  uint32_t* frag = ws.qfrag + ((size_t)b * lv.hkv + h) * kFragWords;
+  for (int wi = tid; wi < 8 * 2 * 64; wi += 128) {
+    const int r = wi & 1, lp = (wi >> 1) & 31, nt = (wi >> 6) & 1, kb = wi >> 7;
+    const int gp = lp >> 2, tp = lp & 3;
+    const int head = 4 * nt + (gp >> 1), grp = gp & 1;
+    uint32_t word = 0;
+    if (nt < nt_count && head < gq && (tp >> 1) == grp) {
+      const float sc = ldexpf(1.f, sig[head] - 2 * (kb & 3));
+      const int ch0 = 32 * tp + 16 * r + kb;
+      const __half2 v = __floats2half2_rn(xs[head * kD + ch0] * sc, xs[head * kD + ch0 + 8] * sc);
+      word = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    frag[((kb * 2 + nt) * 32 + lp) * 2 + r] = word;
   }
 }
 
@@ -126,7 +188,7 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
   }
   const int p0 = s * pages_per_split, p1 = min(p0 + pages_per_split, npages);
   for (int i = tid; i < GQ * kD; i += 128) qs[i / kD][i % kD] = ws.qrot[((size_t)b * lv.hq + hq0) * kD + i];
-  if (tid < GQ * kNG) qg[tid / kNG][tid % kNG] = ws.qsum[((size_t)b * lv.hq + hq0) * kNG + tid];
+  if (tid < GQ * kNG) qg[tid / kNG][tid % kNG] = ws.qconst[((size_t)b * lv.hq + hq0 + tid / kNG) * kQConst + kQSum0 + tid % kNG];
   if (tid < GQ) { mrow[tid] = -INFINITY; lrow[tid] = 0.f; }
   float acc[GQ];
 #pragma unroll
@@ -445,7 +507,7 @@ int launch_int2_mma(const LayerView& lv, const DecodeWorkspace& ws, const Decode
 template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
-  k_qprep<<<dim3(lv.hkv, a.B), 128, kQprepSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(a.q), ws);
+  k_qprep<<<dim3(lv.hkv, a.B), 128, kQprepSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(a.q), ws, scale_log2);
   if (a.ev0) cudaEventRecord(a.ev0, st);
   if (a.algo == OSCAR_DECODE_MMA) {
     int rc = launch_int2_mma(lv, ws, a, scale_log2, st);
@@ -497,7 +559,10 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
   }
 }
 
+int configure_mma_kernels();   // decode_mma.cu
+
 int configure_decode_kernels() {
+  if (configure_mma_kernels() != OSCAR_OK) return OSCAR_ERR_CUDA;
   cudaError_t e = cudaFuncSetAttribute(k_qprep, cudaFuncAttributeMaxDynamicSharedMemorySize, kQprepSmem);
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
 #define OSCAR_MERGE_ATTR(G)                                                                              \

@@ -5,6 +5,7 @@
 
 namespace oscar {
 
+constexpr int kDefaultDecodeAlgo = OSCAR_DECODE_MMA;
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
 constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
 constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4;           // U + row + 4 partial rows
@@ -15,10 +16,18 @@ constexpr int kMergeSmem = (kD * (kD + 1) + 4 * kD) * 4;           // padded U_V
 struct DecodeWorkspace {
   float* qrot;        // [max_batch][hq][kD] rotated queries (float32, rotated channel order)
   uint32_t* qfrag;    // [max_batch][hkv][kFragWords] fp16 MMA B fragments of the rotated queries
-  float* qsum;        // [max_batch][hq][kNG] per-group sums of the rotated query (float32)
+  float* qconst;      // [max_batch][hq][kQConst] per-query-head constants, see kQ* below
   float* partials;    // [max_batch][hq][max_splits + 1][kPartFloats]
   int max_splits;
 };
+
+// Per-query-head constants written by the query prologue.
+constexpr int kQConst = 8;
+constexpr int kQSum0 = 0, kQSum1 = 1;    // sum of the rotated query over group 0 / 1
+constexpr int kQF = 2;                   // sm_scale * log2(e) * 2^-sigma (fragment scale undo)
+constexpr int kQZ0 = 3, kQZ1 = 4;        // sm_scale * log2(e) * group sums (zero-point terms)
+constexpr int kQOff0 = 5, kQOff1 = 6;    // 1024 * sum of the group's fp16 fragment values
+constexpr int kQSigma = 7;               // sigma, the power-of-two scale of the fragments
 
 // B fragments of one kv head's query group for the tensor-core decode:
 // 8 k-blocks x 2 n-tiles x 32 lanes x 2 registers.
@@ -63,6 +72,7 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
 namespace oscar {
 // api.cu helpers for entry points that work without a cache handle
 int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, LayerView* out);
-void decode_split_policy(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps);
+void decode_split_policy(int B, int hkv, int gq, int max_pages, int max_splits, int sms, int algo, int* nsplit,
+                         int* pps);
 int configure_kernels();
 }  // namespace oscar

@@ -286,7 +286,7 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
  * call): calls that may overlap on the GPU (different streams, or threads
  * without ordering) race and give wrong results; calls ordered on one stream
  * are safe. The history is split into fewer pieces when needed to fit; a call
- * whose B * Hq * 1576 + B * Hkv * 4096 bytes (plus 1 KB) exceed 4 MiB, i.e. too
+ * whose B * Hq * 1600 + B * Hkv * 4096 bytes (plus 1 KB) exceed 4 MiB, i.e. too
  * many query rows even with one split, returns OSCAR_ERR_TOO_LARGE before any
  * device work. */
 int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B, const void* q,

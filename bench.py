@@ -217,59 +217,81 @@ def step_algorithmic_bytes(L: int, B: int, H: int, hq: int, layers: int) -> int:
 
 def run_ours(args, rank: int, world: int, device):
     import torch
-    import bit_kv_cache_decode_gb300 as osc
     import synth
 
     seed = 1234 + rank
+    total_steps = args.warmup + args.steps
     wl = build_workload(args.workload, seed, device, with_bf16=not args.no_bf16,
-                        steps_capacity=3 * (args.steps + args.warmup) + 8, algo=args.algo)
+                        steps_capacity=3 * total_steps + 16, algo=args.algo)
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
     stream = torch.cuda.current_stream()
     sm = synth.sm_scale()
-    total_steps = args.warmup + args.steps
     kv_new, q_all = step_inputs(wl, total_steps, device, seed)
-    out = torch.empty(B, hq, 128, dtype=torch.bfloat16, device=device)
+    kv_cur = torch.empty_like(kv_new[0])          # the step's new K/V, [layers, 2, B, H, 128]
+    q_cur = torch.empty_like(q_all[0])            # the step's queries, [layers, B, Hq, 128]
+    out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
     seq = torch.full((B,), wl["L"], dtype=torch.int32, device=device)
     seq1 = seq + 1
-    launches_per_layer = 5   # append, query rotation, INT2 history, BF16 segment, merge
+    # append, query rotation, then either one fused decode launch (mma) or history + BF16 segment + merge (simt)
+    launches_per_layer = 3 if args.algo == 1 else 5
 
-    def one_step(i):
+    def layers():
         for layer in range(nl):
-            cache.append_kv(layer, kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
-            cache.decode_attention(layer, q_all[i, layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out)
+            cache.append_kv(layer, kv_cur[layer, 0], kv_cur[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
+            cache.decode_attention(layer, q_cur[layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out[layer])
         seq.add_(1)
         seq1.add_(1)
 
-    for i in range(args.warmup):
-        one_step(i)
+    # capture one step (all layers) into a CUDA graph
     torch.cuda.synchronize()
-    L_start = wl["L"] + args.warmup
+    kv_cur.copy_(kv_new[0])
+    q_cur.copy_(q_all[0])
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        layers()                                   # one eager step on the capture stream first
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            layers()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    if cache.get_status() != 0:
+        raise RuntimeError("device status error during capture")
+
+    def step(i):
+        kv_cur.copy_(kv_new[i], non_blocking=True)
+        q_cur.copy_(q_all[i], non_blocking=True)
+        graph.replay()
+
+    for i in range(1, args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    L_start = int(seq[0].item())
     barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    cache.profile_begin(nl * args.steps)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         torch.cuda.synchronize()
         ev0.record(stream)
         for i in range(args.warmup, total_steps):
-            one_step(i)
+            step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-    int2_ms, int2_n = cache.profile_read()
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world, device)
     if cache.get_status() != 0:
         raise RuntimeError("device status error during the timed steps")
-    # units: KV tokens attended per step (+1 for the appended token, all layers)
+    # units: KV tokens attended per step (the appended token included), all layers
     kv_tokens = sum(B * (L_start + 1 + s) * nl for s in range(args.steps))
     value = kv_tokens * world / (ms / 1e3)
     ms_step = ms / args.steps
     step_bytes = sum(step_algorithmic_bytes(L_start + 1 + s, B, H, hq, nl) for s in range(args.steps)) / args.steps
     peak, peak_src = peaks()
-    # dominant kernel: INT2 history kernel, algorithmic bytes per launch at the mean context of the timed steps
-    L_mid = L_start + 1 + (args.steps - 1) / 2
-    hb = history_bytes(int(L_mid), B, H)
-    int2_avg_ms = int2_ms / max(int2_n, 1)
-    achieved = hb / (int2_avg_ms / 1e3) / 1e9
+    # dominant kernel: the decode call (query prologue + fused decode, PDL-chained), timed per call with the
+    # library's CUDA events in a second timed region that issues the same steps without the graph
+    dec_ms, dec_n, L_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, seq1, out)
+    hb = history_bytes(L_prof, B, H) + B * min(L_prof, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
+    dec_avg_ms = dec_ms / max(dec_n, 1)
+    achieved = hb / (dec_avg_ms / 1e3) / 1e9
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -278,23 +300,45 @@ def run_ours(args, rank: int, world: int, device):
                    "head_dim": 128, "sink": 64, "recent": 256, "group": 64, "page": 64, "v_mode": "absorbed",
                    "storage": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
                    "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
-                   "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma"},
+                   "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
+                   "launch": "one CUDA graph per step (36 layers x (append + decode)), new tokens copied in"},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
                 "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak},
-        "roofline": {"bound": "hbm", "kernel": "INT2 history decode", "achieved": achieved, "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                     "algorithmic_bytes_per_launch": hb, "avg_launch_us": int2_avg_ms * 1e3,
-                     "launches": int2_n},
-        "gpu_launches": launches_per_layer * nl * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "decode call: query prologue + " +
+                     ("fused INT2/BF16/merge kernel" if args.algo == 1 else "history + BF16 + merge kernels"),
+                     "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_launch": hb,
+                     "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
+        "gpu_launches": (launches_per_layer * nl + 2) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_bf16:
         res["bf16_baseline"] = run_bf16(wl, args, q_all, device)
         res["bf16_baseline"]["speedup_of_int2_step"] = res["bf16_baseline"]["ms_per_step"] / ms_step
-    res["e2e"] = run_e2e(wl, args, device)
+    res["e2e"] = run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq)
+    res["e2e_eager"] = run_e2e_eager(wl, args, device, start_len=int(seq[0].item()))
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(wl, seed, device, budget_s=args.cpu_budget)
     return res
+
+
+def profile_decode_calls(wl, args, kv_new, q_all, seq, seq1, out):
+    """Eager steps with the library tracing every decode call: returns (summed ms, calls, mean context)."""
+    import torch
+    import synth
+    cache, nl = wl["cache"], wl["layers"]
+    sm = synth.sm_scale()
+    torch.cuda.synchronize()
+    L0 = int(seq1[0].item())
+    cache.profile_begin(nl * args.steps)
+    for i in range(args.steps):
+        for layer in range(nl):
+            cache.append_kv(layer, kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
+            cache.decode_attention(layer, q_all[i, layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out[layer])
+        seq.add_(1)
+        seq1.add_(1)
+    ms, n = cache.profile_read()
+    return ms, n, L0 + (args.steps - 1) // 2
 
 
 def run_bf16(wl, args, q_all, device):
@@ -328,9 +372,40 @@ def run_bf16(wl, args, q_all, device):
             "gbs": by / (ms / 1e3) / 1e9, "algorithmic_bytes_per_step": by}
 
 
-def run_e2e(wl, args, device):
-    """Same step through the public API with host buffers: pinned host -> device copy of the step's new K/V
-    and queries, the step, and a device -> host read of every layer's output."""
+def run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq):
+    """The step end to end from host buffers: each step copies its new K/V and queries from pinned host
+    memory into the captured step's input buffers, replays the step, and copies every layer's output back."""
+    import torch
+    nl, B, H, hq = wl["layers"], wl["B"], wl["H"], wl["hq"]
+    host_kv = torch.randn(kv_cur.shape, dtype=torch.float32).to(torch.bfloat16).pin_memory()
+    host_q = torch.randn(q_cur.shape, dtype=torch.float32).to(torch.bfloat16).pin_memory()
+    host_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+
+    def step():
+        kv_cur.copy_(host_kv, non_blocking=True)
+        q_cur.copy_(host_q, non_blocking=True)
+        graph.replay()
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    Ls = int(seq[0].item())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    kv_tokens = sum(B * (Ls + 1 + s) * nl for s in range(args.steps)) / args.steps
+    return {"value": kv_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": (host_kv.numel() + host_q.numel()) * 2, "d2h_bytes_per_step": host_out.numel() * 2,
+            "path": "pinned host -> device copy, graph replay of the C-ABI calls, device -> host copy"}
+
+
+def run_e2e_eager(wl, args, device, start_len: int):
+    """As run_e2e but issuing the C-ABI calls directly from Python every step (no graph)."""
     import torch
     import synth
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
@@ -340,8 +415,8 @@ def run_e2e(wl, args, device):
     host_out = torch.empty(nl * B * hq * 128, dtype=torch.bfloat16).pin_memory()
     dev_in = torch.empty_like(host_in, device=device)
     dev_out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
-    # sequence lengths continue from where the timed run left the cache
-    seq = torch.full((B,), wl["L"] + args.warmup + args.steps, dtype=torch.int32, device=device)
+    torch.cuda.synchronize()
+    seq = torch.full((B,), start_len, dtype=torch.int32, device=device)   # the cache's current length
     seq1 = seq + 1
     kvn = dev_in[:nl * 2 * B * H * 128].view(nl, 2, B, H, 128)
     qn = dev_in[nl * 2 * B * H * 128:].view(nl, B, hq, 128)
@@ -358,8 +433,8 @@ def run_e2e(wl, args, device):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     Ls = int(seq[0].item())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
         step()
@@ -368,7 +443,8 @@ def run_e2e(wl, args, device):
     ms = e0.elapsed_time(e1) / args.steps
     kv_tokens = sum(B * (Ls + 1 + s) * nl for s in range(args.steps)) / args.steps
     return {"value": kv_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": host_in.numel() * 2, "d2h_bytes_per_step": host_out.numel() * 2}
+            "h2d_bytes_per_step": host_in.numel() * 2, "d2h_bytes_per_step": host_out.numel() * 2,
+            "path": "pinned host -> device copy, direct C-ABI calls from Python, device -> host copy"}
 
 
 def cpu_baseline(wl, seed, device, budget_s: float = 20.0):

@@ -61,7 +61,8 @@ void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, si
          + align_up(B * hq * kD * sizeof(float))                   // qrot
          + align_up(B * hkv * kFragWords * sizeof(uint32_t))       // qfrag
          + align_up(B * hq * kQConst * sizeof(float))              // qconst
-         + align_up(B * hq * (L->max_splits + 1) * kPartFloats * sizeof(float));  // partials
+         + align_up(B * hq * (L->max_splits + (L->sink + L->recent) / kP) * kPartFloats * sizeof(float))  // partials
+         + align_up(B * hkv * sizeof(uint32_t));                   // completion counters
 }
 
 LayerView view(const oscar_cache* c, int layer) {
@@ -95,20 +96,21 @@ int configure_once() {
 
 // Split policy over the page-table width: choose the number of history splits
 // per (request, kv head) that minimises waves x (pages per CTA + a fixed
-// per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs; pages per
-// split are rounded up to `align` and there is no empty trailing split.
-void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int align, int* nsplit,
-                   int* pps) {
+// per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs and every
+// group launches `extra` more CTAs; pages per split are rounded up to `align`
+// and there is no empty trailing split.
+void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int align, int extra,
+                   int* nsplit, int* pps) {
   if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
   const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
-  const int nmax = std::min(max_splits, max_pages);
+  const int nmax = std::min(std::min(max_splits, max_pages), kMaxMmaSplits);
   long best_cost = -1;
   int best_p = max_pages;
   for (int n = 1; n <= nmax; ++n) {
     int p = (max_pages + n - 1) / n;
     p = (p + align - 1) / align * align;
     const int used = (max_pages + p - 1) / p;
-    const long waves = (units * used + slots - 1) / slots;
+    const long waves = (units * (used + extra) + slots - 1) / slots;
     const long cost = waves * (p + 2L * align);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_p = p; }
   }
@@ -116,9 +118,9 @@ void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int c
   *nsplit = (max_pages + best_p - 1) / best_p;
 }
 
-void algo_policy(int algo, int gq, int* ctas_per_sm, int* align) {
-  if (algo == OSCAR_DECODE_MMA) { *ctas_per_sm = gq <= 4 ? 3 : 2; *align = 4; }
-  else { *ctas_per_sm = 4; *align = 1; }
+void algo_policy(int algo, int gq, int nbf, int* ctas_per_sm, int* align, int* extra) {
+  if (algo == OSCAR_DECODE_MMA) { *ctas_per_sm = gq <= 4 ? 4 : 2; *align = 4; *extra = nbf; }
+  else { *ctas_per_sm = 4; *align = 1; *extra = 0; }
 }
 
 }  // namespace
@@ -180,11 +182,18 @@ int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, 
   p += align_up(B * hq * kQConst * sizeof(float));
   c->dws.partials = reinterpret_cast<float*>(p);
   c->dws.max_splits = layout->max_splits;
+  c->dws.nslots = layout->max_splits + (layout->sink + layout->recent) / kP;
+  p += align_up(B * hq * c->dws.nslots * kPartFloats * sizeof(float));
+  c->dws.counters = reinterpret_cast<uint32_t*>(p);
   c->sms = sms;
   c->algo = kDefaultDecodeAlgo;
   c->prof_on = false;
   c->prof_cap = c->prof_n = 0;
-  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) { delete c; return OSCAR_ERR_CUDA; }
+  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(c->dws.counters, 0, B * hkv * sizeof(uint32_t)) != cudaSuccess) {
+    delete c;
+    return OSCAR_ERR_CUDA;
+  }
   *out = c;
   return OSCAR_OK;
 }
@@ -229,7 +238,12 @@ int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float*
   for (int h = 0; h < hkv; ++h) {
     float* dst = host.data() + (size_t)h * kParamFloats;
     std::memcpy(dst + kUKOff, U_K + (size_t)h * kD * kD, kD * kD * sizeof(float));
-    if (U_V) std::memcpy(dst + kUVOff, U_V + (size_t)h * kD * kD, kD * kD * sizeof(float));
+    if (U_V) {
+      const float* u = U_V + (size_t)h * kD * kD;
+      std::memcpy(dst + kUVOff, u, kD * kD * sizeof(float));
+      for (int i = 0; i < kD; ++i)
+        for (int j = 0; j < kD; ++j) dst[kUVtOff + j * kD + i] = u[i * kD + j];
+    }
     std::memcpy(dst + kTauKOff, tau_K + (size_t)h * kD, kD * sizeof(float));
     std::memcpy(dst + kTauVOff, tau_V + (size_t)h * kD, kD * sizeof(float));
   }
@@ -290,10 +304,11 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.out_dtype = out_dtype;
   a.lse = lse;
   a.algo = c->algo;
+  a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
-    int cps, align;
-    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, &cps, &align);
-    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, &a.nsplit,
+    int cps, align, extra;
+    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra);
+    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, &a.nsplit,
                   &a.pages_per_split);
   }
   a.ev0 = a.ev1 = nullptr;
@@ -360,7 +375,7 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   int nsplit, pps;
-  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, &nsplit, &pps);
+  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, 0, &nsplit, &pps);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
@@ -423,11 +438,11 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 }
 
 // The history split choice of oscar_decode_attention, for at most max_splits splits.
-void decode_split_policy(int B, int hkv, int gq, int max_pages, int max_splits, int sms, int algo, int* nsplit,
-                         int* pps) {
-  int cps, align;
-  algo_policy(algo, gq, &cps, &align);
-  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, nsplit, pps);
+void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
+                         int* nsplit, int* pps) {
+  int cps, align, extra;
+  algo_policy(algo, gq, nbf, &cps, &align, &extra);
+  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, extra, nsplit, pps);
 }
 
 int configure_kernels() { return configure_once(); }

@@ -28,9 +28,11 @@ constexpr int kKMetaOff = 2 * kCodeBytes;
 constexpr int kVMetaOff = 2 * kCodeBytes + kMetaBytes;
 constexpr int kBlockBytes = 2 * kCodeBytes + 2 * kMetaBytes;   // 5120
 constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D] then V [P][D]
-// rotation parameters per kv head: U_K [D][D], U_V [D][D], tau_K [D], tau_V [D] (float32)
-constexpr int kParamFloats = 2 * kD * kD + 2 * kD;
-constexpr int kUKOff = 0, kUVOff = kD * kD, kTauKOff = 2 * kD * kD, kTauVOff = 2 * kD * kD + kD;
+// rotation parameters per kv head (float32): U_K [D][D], U_V [D][D], U_V transposed [D][D]
+// (for coalesced reads of R_V^T in the merge), tau_K [D], tau_V [D]
+constexpr int kParamFloats = 3 * kD * kD + 2 * kD;
+constexpr int kUKOff = 0, kUVOff = kD * kD, kUVtOff = 2 * kD * kD, kTauKOff = 3 * kD * kD,
+              kTauVOff = 3 * kD * kD + kD;
 // one split partial: m (log2 units), l, then acc[D]; padded to 132 floats (528 B, 16 B aligned)
 constexpr int kPartFloats = kD + 4;
 constexpr float kLog2e = 1.4426950408889634f;

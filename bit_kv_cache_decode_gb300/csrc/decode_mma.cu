@@ -8,7 +8,7 @@
 // Work: grid (split, kv head, request); 4 warps per CTA; warp w takes history
 // pages p0 + w, p0 + w + 4, ... of the CTA's split. Each (page, kv head) block
 // (5120 B: K codes | V codes | K meta | V meta) is copied into a per-warp
-// 3-stage shared-memory ring by one cp.async.bulk with an mbarrier; waits are
+// 2-stage shared-memory ring by one cp.async.bulk with an mbarrier; waits are
 // bounded and report OSCAR_STATUS_TIMEOUT instead of hanging.
 //
 // Per 16-token tile the two contractions run on mma.sync.m16n8k16 f16 -> f32:
@@ -22,49 +22,34 @@
 //    fp16 codes of one channel for two tokens), B = p * scale [16 tokens x 8
 //    columns], built from the logits' accumulator layout with two movmatrix
 //    transposes; the zero-point part sum_t p_t z_t is accumulated in fp32.
-// The kernel ends with a combine of the 4 warps' online-softmax partials and
-// writes one partial (m, l, acc[128]) per query head and split.
+// A history CTA ends with a combine of its 4 warps' online-softmax partials
+// and writes one partial (m, l, acc[128]) per query head and split.
+//
+// The same launch carries the BF16 sink + recent tokens as one extra CTA per
+// BF16 page (bulk-copied, CUDA-core dot products) and the log-sum-exp merge: every CTA
+// of a (request, kv head) group takes a ticket after writing its partials, and
+// the last one merges the group's partials (applying R_V^T to the history part
+// in explicit-V mode) and writes the attention output. The ticket counter is
+// reset by that CTA, so it is zero again between launches.
 #include "kernels.cuh"
+#include "rotate.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
-constexpr unsigned kWaitLimit = 1u << 24;
+constexpr int kStages = 2;
 constexpr uint32_t kMagic = 0x64006400u;       // fp16 1024.0 in both halves
 // stage ring, mbarriers, a timeout flag, and slack to align the ring to 128 bytes
 constexpr int kMmaSmem = kWarps * kStages * kBlockBytes + kWarps * kStages * 8 + 16 + 128;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Bounded wait for the phase with the given parity; false when the limit expires.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (unsigned i = 0; i < kWaitLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
+// 2^x with the SFU (inputs are logit differences <= 0 or -inf)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -87,6 +72,13 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// (x & mask) | magic as one three-input logic op (LUT 0xEA = (a & b) | c)
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
+  return d;
+}
+
 // exact fp16 codes: ((1024 + c*4^k) * 4^-k) - 1024*4^-k = c, for both halves
 __device__ __forceinline__ uint32_t exact_codes(uint32_t biased, int k) {
   const uint32_t scale = 0x3C003C00u - (uint32_t)(k * 0x08000800u);   // 4^-k = 2^-2k: exponent - 2k
@@ -96,14 +88,33 @@ __device__ __forceinline__ uint32_t exact_codes(uint32_t biased, int k) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+struct FusedArgs {
+  const int* seq_lens;
+  const int* hist_pt;
+  int max_hist_pages;
+  int pages_per_split;
+  int nsplit;                        // history CTAs per group; the next nbf CTAs take one BF16 page each
+  int nbf;
+  const int* bf16_pt;
+  const __nv_bfloat16* q;            // raw queries, for the BF16 tokens
+  float scale_log2;                  // sm_scale * log2(e)
+  void* out;
+  int out_dtype;
+  float* lse;
+};
+
+__device__ __forceinline__ float* part_row(const DecodeWorkspace& ws, int b, int hq_total, int hq, int slot) {
+  return ws.partials + (((size_t)b * hq_total + hq) * ws.nslots + slot) * kPartFloats;
+}
+
+// History split `split` of group (b, h): see the file comment.
 template <int NT>
-__global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
-    k_int2_mma(LayerView lv, DecodeWorkspace ws, const int* __restrict__ seq_lens, const int* __restrict__ hist_pt,
-               int max_hist_pages, int pages_per_split) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+__device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
+                                           uint8_t* smem, int split, int h, int b) {
+  const int* __restrict__ seq_lens = fa.seq_lens;
+  const int* __restrict__ hist_pt = fa.hist_pt;
+  const int max_hist_pages = fa.max_hist_pages, pages_per_split = fa.pages_per_split;
   int& any_timeout = *reinterpret_cast<int*>(smem + kWarps * kStages * kBlockBytes + kWarps * kStages * 8);
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gq = lv.hq / lv.hkv;
@@ -130,7 +141,6 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(bar_s + 8 * s);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
 
@@ -149,9 +159,15 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
     return true;
   };
   uint32_t issued = 0;                 // bit s: a load is outstanding in stage s
+  // Before the programmatic wait only pages the preceding append cannot touch are
+  // fetched: it writes one row of the last history page (the demoted token).
 #pragma unroll
   for (int i = 0; i < kStages; ++i)
-    if (i < my_pages && issue(i)) issued |= 1u << i;
+    if (i < my_pages && p0 + kWarps * i < npages - 1 && issue(i)) issued |= 1u << i;
+  pdl_wait();
+#pragma unroll
+  for (int i = 0; i < kStages; ++i)
+    if (i < my_pages && p0 + kWarps * i >= npages - 1 && issue(i)) issued |= 1u << i;
 
   // ---- per-lane constants -------------------------------------------------------
   uint32_t qf[8][NT][2];
@@ -220,16 +236,19 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
         const uint2 kw0 = *reinterpret_cast<const uint2*>(blk + kKCodesOff + r0 * 32 + 8 * t);
         const uint2 kw1 = *reinterpret_cast<const uint2*>(blk + kKCodesOff + r1 * 32 + 8 * t);
         const uint32_t x0h = kw0.x >> 8, x1h = kw0.y >> 8, y0h = kw1.x >> 8, y1h = kw1.y >> 8;
-        float c[NT][4];
+        float c[NT][4];                            // start from -offset: the MMAs add the biased sums
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) {
+          c[nt][0] = c[nt][2] = -cO0[nt];
+          c[nt][1] = c[nt][3] = -cO1[nt];
+        }
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
           const uint32_t m = 0x00030003u << (2 * (kb & 3));
-          const uint32_t a0 = ((kb < 4 ? kw0.x : x0h) & m) | kMagic;
-          const uint32_t a1 = ((kb < 4 ? kw1.x : y0h) & m) | kMagic;
-          const uint32_t a2 = ((kb < 4 ? kw0.y : x1h) & m) | kMagic;
-          const uint32_t a3 = ((kb < 4 ? kw1.y : y1h) & m) | kMagic;
+          const uint32_t a0 = and_or(kb < 4 ? kw0.x : x0h, m, kMagic);
+          const uint32_t a1 = and_or(kb < 4 ? kw1.x : y0h, m, kMagic);
+          const uint32_t a2 = and_or(kb < 4 ? kw0.y : x1h, m, kMagic);
+          const uint32_t a3 = and_or(kb < 4 ? kw1.y : y1h, m, kMagic);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(c[nt], a0, a1, a2, a3, qf[kb][nt][0], qf[kb][nt][1]);
         }
@@ -241,12 +260,15 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
         const float2 sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float l0 = fmaf(sz00.x, c[nt][0] - cO0[nt], sz01.x * (c[nt][1] - cO1[nt]));
-          float l1 = fmaf(sz10.x, c[nt][2] - cO0[nt], sz11.x * (c[nt][3] - cO1[nt]));
-          l0 = fmaf(cF[nt], l0, fmaf(sz00.y, cZ0[nt], sz01.y * cZ1[nt]));
-          l1 = fmaf(cF[nt], l1, fmaf(sz10.y, cZ0[nt], sz11.y * cZ1[nt]));
-          lg[mt][nt][0] = r0 < ntok ? l0 : -INFINITY;
-          lg[mt][nt][1] = r1 < ntok ? l1 : -INFINITY;
+          lg[mt][nt][0] = fmaf(cF[nt], fmaf(sz00.x, c[nt][0], sz01.x * c[nt][1]), fmaf(sz00.y, cZ0[nt], sz01.y * cZ1[nt]));
+          lg[mt][nt][1] = fmaf(cF[nt], fmaf(sz10.x, c[nt][2], sz11.x * c[nt][3]), fmaf(sz10.y, cZ0[nt], sz11.y * cZ1[nt]));
+        }
+        if (ntok < kP) {                           // ragged last page: rows past the end take no weight
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (r0 >= ntok) lg[mt][nt][0] = -INFINITY;
+            if (r1 >= ntok) lg[mt][nt][1] = -INFINITY;
+          }
         }
       }
 
@@ -289,13 +311,15 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
         float2 sv01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));
         float2 sv10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));
         float2 sv11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
-        if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);       // rows past the end: no stale metadata
-        if (r1 >= ntok) sv10 = sv11 = make_float2(0.f, 0.f);
+        if (ntok < kP) {                           // rows past the end: no stale metadata
+          if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);
+          if (r1 >= ntok) sv10 = sv11 = make_float2(0.f, 0.f);
+        }
         uint32_t bf[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float pa = exp2f(lg[kt][nt][0] - mrun[nt]);
-          const float pb = exp2f(lg[kt][nt][1] - mrun[nt]);
+          const float pa = fast_exp2(lg[kt][nt][0] - mrun[nt]);
+          const float pb = fast_exp2(lg[kt][nt][1] - mrun[nt]);
           lsum[nt] += pa + pb;
           zacc[nt][0] = fmaf(pa, sv00.y, fmaf(pb, sv10.y, zacc[nt][0]));
           zacc[nt][1] = fmaf(pa, sv01.y, fmaf(pb, sv11.y, zacc[nt][1]));
@@ -309,10 +333,10 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
         for (int mt = 0; mt < 8; ++mt) {
           const int k = mt & 3;
           const uint32_t m = 0x00030003u << (2 * k);
-          const uint32_t a0 = exact_codes(((mt < 4 ? wab.x : wah) & m) | kMagic, k);   // channel 16g + mt, tokens 2t, 2t+1
-          const uint32_t a1 = exact_codes(((mt < 4 ? wab.y : wbh) & m) | kMagic, k);   // channel 16g + 8 + mt
-          const uint32_t a2 = exact_codes(((mt < 4 ? wcd.x : wch) & m) | kMagic, k);   // tokens 2t + 8, 2t + 9
-          const uint32_t a3 = exact_codes(((mt < 4 ? wcd.y : wdh) & m) | kMagic, k);
+          const uint32_t a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
+          const uint32_t a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
+          const uint32_t a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
+          const uint32_t a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
         }
@@ -362,7 +386,6 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
     }
   }
   __syncthreads();
-  const int nslots = ws.max_splits + 1;
   for (int hh = 0; hh < gq; ++hh) {
     float M = -INFINITY;
 #pragma unroll
@@ -380,7 +403,7 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
     } else {
       M = -INFINITY;
     }
-    float* part = ws.partials + (((size_t)b * lv.hq + h * gq + hh) * nslots + split) * kPartFloats;
+    float* part = part_row(ws, b, lv.hq, h * gq + hh, split);
     if (tid == 0) {
       part[0] = M;
       part[1] = Ls;
@@ -389,21 +412,259 @@ __global__ void __launch_bounds__(128, NT == 1 ? 3 : 2)
   }
 }
 
+// BF16 page c of group (b, h): c = 0 is the sink page, c >= 1 the recent ring
+// pages. Attention is order-independent, so each page is attended as a unit:
+// the (page, kv head) block (K [64][128] then V [64][128], 32 KB) arrives in
+// one bulk copy; row r is live if r < n_sink (sink page) or if its ring slot
+// 64 (c - 1) + r < n_recent (ring pages). Dot products walk the 16-byte
+// columns of a K row in a token-rotated order to avoid bank conflicts.
+__device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
+                                          uint8_t* smem, int c, int h, int b) {
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem);                  // K [64][128], V [64][128]
+  float* qs = reinterpret_cast<float*>(smem + kBf16BlockBytes);                 // [8][128]
+  float* pb = qs + 8 * kD;                                                      // [8][64]
+  float* ms = pb + 8 * kP;                                                      // [8]
+  float* ls = ms + 8;                                                           // [8]
+  const uint32_t bar = smem_addr(ls + 8);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int gq = lv.hq / lv.hkv, hq0 = h * gq;
+  pdl_wait();                                      // the append writes into these pages
+  const int L = fa.seq_lens[b];
+  if (L < 1 && tid == 0 && c == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);
+  const int n_sink = max(0, min(L, lv.sink));
+  const int n_rec = L > lv.sink ? min(L - lv.sink, lv.recent) : 0;
+  const int sink_pages = lv.sink / kP;
+  int nrow;                                        // live rows are 0 .. nrow-1
+  if (c < sink_pages) nrow = max(0, min(kP, n_sink - c * kP));
+  else nrow = max(0, min(kP, n_rec - (c - sink_pages) * kP));
+  const int page = nrow > 0 ? fa.bf16_pt[(size_t)b * ((lv.sink + lv.recent) / kP) + c] : -1;
+  const bool ok = nrow > 0 && page >= 0 && page < lv.n_bf16;
+  if (nrow > 0 && !ok && tid == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE);
+  bool landed = true;
+  if (ok) {
+    if (tid == 0) {
+      mbar_init(bar);
+      bulk_load(smem_addr(kv), lv.bf16 + ((size_t)page * lv.hkv + h) * kBf16BlockBytes, kBf16BlockBytes, bar);
+    }
+    for (int i = tid; i < gq * kD; i += 128) qs[i] = __bfloat162float(fa.q[((size_t)b * lv.hq + hq0) * kD + i]);
+    __syncthreads();                               // barrier initialised before anyone waits on it
+    landed = __syncthreads_and(mbar_wait(bar, 0));
+    if (!landed && tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+  }
+  const int live = (ok && landed) ? nrow : 0;
+  for (int item = tid; item < gq * kP; item += 128) {
+    const int tk = item % kP, hh = item / kP;
+    float l = -INFINITY;
+    if (tk < live) {
+      const __nv_bfloat16* krow = kv + tk * kD;
+      float dot = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < kD / 8; ++j) {
+        const int i = (j + tk) & (kD / 8 - 1);
+        const uint4 k8 = *reinterpret_cast<const uint4*>(krow + 8 * i);
+        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&k8);
+        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * kD + 8 * i);
+        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * kD + 8 * i + 4);
+        float2 f;
+        f = __bfloat1622float2(k2[0]); dot = fmaf(f.x, qa.x, fmaf(f.y, qa.y, dot));
+        f = __bfloat1622float2(k2[1]); dot = fmaf(f.x, qa.z, fmaf(f.y, qa.w, dot));
+        f = __bfloat1622float2(k2[2]); dot = fmaf(f.x, qb.x, fmaf(f.y, qb.y, dot));
+        f = __bfloat1622float2(k2[3]); dot = fmaf(f.x, qb.z, fmaf(f.y, qb.w, dot));
+      }
+      l = dot * fa.scale_log2;
+    }
+    pb[hh * kP + tk] = l;
+  }
+  __syncthreads();
+  for (int hh = w; hh < gq; hh += 4) {
+    const float l0 = pb[hh * kP + lane], l1 = pb[hh * kP + lane + 32];
+    float m = fmaxf(l0, l1);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, x));
+    const float p0 = m == -INFINITY ? 0.f : exp2f(l0 - m), p1 = m == -INFINITY ? 0.f : exp2f(l1 - m);
+    float sum = p0 + p1;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, x);
+    pb[hh * kP + lane] = p0;
+    pb[hh * kP + lane + 32] = p1;
+    if (lane == 0) { ms[hh] = m; ls[hh] = sum; }
+  }
+  __syncthreads();
+  float acc[8];
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
+  const __nv_bfloat16* vcol = kv + kP * kD + tid;
+  for (int tk = 0; tk < live; ++tk) {
+    const float vv = __bfloat162float(vcol[tk * kD]);
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+      if (hh < gq) acc[hh] = fmaf(pb[hh * kP + tk], vv, acc[hh]);
+  }
+#pragma unroll
+  for (int hh = 0; hh < 8; ++hh) {
+    if (hh >= gq) break;
+    float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.nsplit + c);
+    if (tid == 0) { part[0] = ms[hh]; part[1] = ls[hh]; }
+    part[4 + tid] = acc[hh];
+  }
+}
+
+// Merge of group (b, h) by its last CTA: warp w handles query heads w, w+4;
+// lane q handles channels 4q..4q+3. Slots [0, nsplit) are history splits, slots
+// nsplit .. nsplit + nbf - 1 the BF16 pages. Partials are read with L1-bypassing loads (other
+// CTAs of this launch wrote them). Pass 1 gives every slot its weight, pass 2
+// streams the accumulators with many loads in flight.
+__device__ __forceinline__ void merge_group(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
+                                            uint8_t* smem, int h, int b) {
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int gq = lv.hq / lv.hkv;
+  const bool expl = lv.v_explicit != 0;
+  const int ns = fa.nsplit;
+  float* ybuf = reinterpret_cast<float*>(smem) + w * 2 * kD;          // [128] accumulator, then [128] after P_br H
+  float* wts = reinterpret_cast<float*>(smem) + 4 * 2 * kD + w * (ns + 1);   // slot weights of this warp's head
+  for (int hh = w; hh < gq; hh += 4) {
+    const int hq = h * gq + hh;
+    const float* row0 = part_row(ws, b, lv.hq, hq, 0);
+    float M1 = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M1 = fmaxf(M1, __ldcg(row0 + (size_t)s * kPartFloats));
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, x));
+    float L1 = 0.f;
+    for (int s = lane; s < ns; s += 32) {
+      const float m = __ldcg(row0 + (size_t)s * kPartFloats);
+      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M1);
+      wts[s] = wgt;
+      L1 = fmaf(__ldcg(row0 + (size_t)s * kPartFloats + 1), wgt, L1);
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) L1 += __shfl_xor_sync(0xffffffffu, L1, x);
+    __syncwarp();
+    float4 A1 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+    for (int s = 0; s < ns; ++s) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(row0 + (size_t)s * kPartFloats + 4) + lane);
+      const float wgt = wts[s];
+      A1.x = fmaf(a.x, wgt, A1.x); A1.y = fmaf(a.y, wgt, A1.y); A1.z = fmaf(a.z, wgt, A1.z); A1.w = fmaf(a.w, wgt, A1.w);
+    }
+    // BF16 pages: slots ns .. ns + nbf - 1
+    float M2 = -INFINITY;
+    for (int s = 0; s < fa.nbf; ++s) M2 = fmaxf(M2, __ldcg(row0 + (size_t)(ns + s) * kPartFloats));
+    float L2 = 0.f;
+    float4 A2 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < fa.nbf; ++s) {
+      const float* rb = row0 + (size_t)(ns + s) * kPartFloats;
+      const float m = __ldcg(rb);
+      if (m == -INFINITY) continue;
+      const float wgt = exp2f(m - M2);
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(rb + 4) + lane);
+      L2 = fmaf(__ldcg(rb + 1), wgt, L2);
+      A2.x = fmaf(a.x, wgt, A2.x); A2.y = fmaf(a.y, wgt, A2.y); A2.z = fmaf(a.z, wgt, A2.z); A2.w = fmaf(a.w, wgt, A2.w);
+    }
+    if (expl && M1 != -INFINITY) {
+      // history accumulator is in the rotated value basis: multiply by R_V^T = P_br H U_V^T
+      *reinterpret_cast<float4*>(ybuf + 4 * lane) = A1;
+      __syncwarp();
+      float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] = ybuf[bitrev7(lane + 32 * r)];
+      fwht128(v);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) ybuf[kD + lane + 32 * r] = v[r];
+      __syncwarp();
+      const float4* uvt = reinterpret_cast<const float4*>(lv.params + (size_t)h * kParamFloats + kUVtOff);
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int i = 0; i < kD; ++i) {
+        const float z = ybuf[kD + i];
+        const float4 u = uvt[i * (kD / 4) + lane];       // U_V^T[i][4 lane .. 4 lane + 3]
+        o.x = fmaf(z, u.x, o.x); o.y = fmaf(z, u.y, o.y); o.z = fmaf(z, u.z, o.z); o.w = fmaf(z, u.w, o.w);
+      }
+      A1 = o;
+      __syncwarp();
+    }
+    const float M = fmaxf(M1, M2);
+    const float w1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - M);
+    const float w2 = (M2 == -INFINITY) ? 0.f : exp2f(M2 - M);
+    const float Ls = L1 * w1 + L2 * w2;
+    const float inv = 1.f / Ls;
+    float4 o;
+    o.x = (A1.x * w1 + A2.x * w2) * inv;
+    o.y = (A1.y * w1 + A2.y * w2) * inv;
+    o.z = (A1.z * w1 + A2.z * w2) * inv;
+    o.w = (A1.w * w1 + A2.w * w2) * inv;
+    const size_t oi = ((size_t)b * lv.hq + hq) * kD + 4 * lane;
+    if (fa.out_dtype == OSCAR_OUT_FP32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(fa.out) + oi) = o;
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(fa.out) + oi) = pk;
+    }
+    if (fa.lse != nullptr && lane == 0) fa.lse[(size_t)b * lv.hq + hq] = (M + log2f(Ls)) * 0.6931471805599453f;
+    __syncwarp();
+  }
+}
+
+// grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
+template <int NT>
+__global__ void __launch_bounds__(128, NT == 1 ? 4 : 2) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  __shared__ int is_last;
+  const int h = blockIdx.y, b = blockIdx.z;
+  if (blockIdx.x < fa.nsplit) int2_split<NT>(lv, ws, fa, smem, blockIdx.x, h, b);
+  else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
+  // completion ticket: the partial writes above are made visible before the ticket is taken
+  __threadfence();
+  __syncthreads();
+  uint32_t* ctr = ws.counters + (size_t)b * lv.hkv + h;
+  if (threadIdx.x == 0) is_last = atomicAdd(ctr, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  merge_group(lv, ws, fa, smem, h, b);
+  if (threadIdx.x == 0) *ctr = 0u;
+}
+
 }  // namespace
 
-int launch_int2_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float, cudaStream_t st) {
-  const dim3 grid(a.nsplit, lv.hkv, a.B);
-  if (lv.hq / lv.hkv <= 4)
-    k_int2_mma<1><<<grid, 128, kMmaSmem, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages, a.pages_per_split);
-  else
-    k_int2_mma<2><<<grid, 128, kMmaSmem, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages, a.pages_per_split);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
+                      cudaStream_t st) {
+  FusedArgs fa;
+  fa.seq_lens = a.seq_lens;
+  fa.hist_pt = a.hist_pt;
+  fa.max_hist_pages = a.max_hist_pages;
+  fa.pages_per_split = a.pages_per_split;
+  fa.nsplit = a.nsplit;
+  fa.nbf = a.nbf;
+  fa.bf16_pt = a.bf16_pt;
+  fa.q = static_cast<const __nv_bfloat16*>(a.q);
+  fa.scale_log2 = scale_log2;
+  fa.out = a.out;
+  fa.out_dtype = a.out_dtype;
+  fa.lse = a.lse;
+  // programmatic dependent of the query prologue: starts early, prefetches, then waits
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(a.nsplit + a.nbf, lv.hkv, a.B);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kMmaSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = (lv.hq / lv.hkv <= 4) ? cudaLaunchKernelEx(&cfg, k_decode_mma<1>, lv, ws, fa)
+                                              : cudaLaunchKernelEx(&cfg, k_decode_mma<2>, lv, ws, fa);
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels() {
-  if (cudaFuncSetAttribute(k_int2_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_decode_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
-  if (cudaFuncSetAttribute(k_int2_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_decode_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
   return OSCAR_OK;
 }

@@ -68,14 +68,17 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
                        up256((size_t)B * hkv * kFragWords * sizeof(uint32_t)) +
                        up256((size_t)B * hq * kQConst * sizeof(float));
   const size_t per_slot = (size_t)B * hq * kPartFloats * sizeof(float);
-  if (fixed + 2 * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
+  const size_t counters = up256((size_t)B * hkv * sizeof(uint32_t));
+  const int nbf = (layout->sink + layout->recent) / kP;
+  // layout: fixed part | partials (rounded up to 256 B) | counters
+  if (fixed + 256 + counters + (size_t)(nbf + 1) * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
   rc = configure_kernels();
   if (rc != OSCAR_OK) return rc;
   uint8_t* scratch = nullptr;
   int sms = 0;
   rc = scratch_for_current_device(&scratch, &sms);
   if (rc != OSCAR_OK) return rc;
-  const int max_slots = (int)std::min<size_t>((kScratchBytes - fixed) / per_slot, 4097);
+  const int max_slots = (int)std::min<size_t>((kScratchBytes - fixed - 256 - counters) / per_slot, 4096 + nbf);
   DecodeWorkspace ws;
   uint8_t* p = scratch;
   int* dstatus = reinterpret_cast<int*>(p);
@@ -101,12 +104,16 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.lse = lse;
   a.algo = kDefaultDecodeAlgo;
   a.ev0 = a.ev1 = nullptr;
-  decode_split_policy(B, (int)hkv, (int)(hq / hkv), max_hist_pages, max_slots - 1, sms, a.algo, &a.nsplit,
+  a.nbf = nbf;
+  decode_split_policy(B, (int)hkv, (int)(hq / hkv), nbf, max_hist_pages, max_slots - nbf, sms, a.algo, &a.nsplit,
                       &a.pages_per_split);
-  ws.max_splits = a.nsplit;            // the BF16 partial sits right after the history splits
+  ws.max_splits = a.nsplit;            // the BF16 partials sit right after the history splits
+  ws.nslots = a.nsplit + nbf;
+  ws.counters = reinterpret_cast<uint32_t*>(p + up256((size_t)B * hq * ws.nslots * kPartFloats * sizeof(float)));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word must start at zero
   if (cudaMemsetAsync(dstatus, 0, sizeof(int), st) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaMemsetAsync(ws.counters, 0, (size_t)B * hkv * sizeof(uint32_t), st) != cudaSuccess) return OSCAR_ERR_CUDA;
   rc = launch_decode(lv, ws, a, st);
   if (rc != OSCAR_OK) return rc;
   if (status && cudaMemcpyAsync(status, dstatus, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

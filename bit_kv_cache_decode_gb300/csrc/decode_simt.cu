@@ -15,6 +15,7 @@
 // partials hold (m, l, acc) with l = sum 2^(logit - m), acc = sum 2^(logit - m) v.
 #include "kernels.cuh"
 #include "rotate.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 
@@ -69,8 +70,10 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 // ---------------------------------------------------------------------------
 // Query prologue: q~ = q R_K for every query head, in rotated channel order
 // (ws.qrot), the per-head constants (ws.qconst) and the fp16 B fragments of
-// the tensor-core history kernel (ws.qfrag). grid = (hkv, B), block = 128,
-// U_K staged in shared memory; warp w rotates the group's query heads w, w+4.
+// the tensor-core history kernel (ws.qfrag). grid = (hkv, B), block = 256,
+// U_K staged in shared memory by one bulk copy; warp w rotates query head w.
+// Launched as a programmatic dependent of the append kernel: it lets the decode
+// kernel start at once and waits for the append only before it exits.
 //
 // Fragment encoding (decode_mma.cu unpacks a code c of channel ch as the fp16
 // value 1024 + c * 4^(ch % 4)): fragment value of channel ch of head h is
@@ -82,25 +85,38 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 // (2t', 2t'+1) -> channels (32t'+kb, 32t'+kb+8) and (2t'+8, 2t'+9) ->
 // channels (32t'+16+kb, 32t'+24+kb); column g' is (head 4nt + g'/2, group g'%2)
 // and is zero where the channel is not in that group.
-__global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws,
+__global__ void __launch_bounds__(256) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws,
                                                float scale_log2) {
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(128) float smem[];
   float* Us = smem;
   float* xs = smem + kD * kD;  // [8][128]: raw query rows, then rotated rows in rotated channel order
+  const uint32_t bar = smem_addr(xs + 8 * kD);
   __shared__ int sig[8];
+  __shared__ int landed;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int gq = lv.hq / lv.hkv;
   const int wib = tid >> 5, lane = tid & 31;
-  const float4* us = reinterpret_cast<const float4*>(lv.params + (size_t)h * kParamFloats + kUKOff);
-  float4* ud = reinterpret_cast<float4*>(Us);
-#pragma unroll 8
-  for (int i = tid; i < kD * kD / 4; i += 128) ud[i] = us[i];
-  for (int i = tid; i < gq * kD; i += 128) {
+  pdl_launch_dependents();
+  if (tid == 0) {
+    mbar_init(bar);
+    bulk_load(smem_addr(Us), lv.params + (size_t)h * kParamFloats + kUKOff, kD * kD * 4, bar);
+  }
+  for (int i = tid; i < gq * kD; i += 256) {
     const int qi = i / kD, c = i % kD;
     xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq + qi) * kD + c]);
   }
   __syncthreads();
-  for (int qi = wib; qi < gq; qi += 4) {
+  const bool ok = mbar_wait(bar, 0);
+  if (tid == 0) landed = 1;
+  __syncthreads();
+  if (!ok) landed = 0;                           // benign race: any thread that timed out clears it
+  __syncthreads();
+  if (!landed) {
+    if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+    pdl_wait();
+    return;
+  }
+  for (int qi = wib; qi < gq; qi += 8) {
     float y[1][4];
     warp_rotate<1>(Us, xs + qi * kD, y);
     __syncwarp();                                   // row qi fully read before it is overwritten
@@ -147,7 +163,7 @@ __global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16
   }
   const int nt_count = (gq + 3) / 4;
   uint32_t* frag = ws.qfrag + ((size_t)b * lv.hkv + h) * kFragWords;
-  for (int wi = tid; wi < 8 * 2 * 64; wi += 128) {
+  for (int wi = tid; wi < 8 * 2 * 64; wi += 256) {
     const int r = wi & 1, lp = (wi >> 1) & 31, nt = (wi >> 6) & 1, kb = wi >> 7;
     const int gp = lp >> 2, tp = lp & 3;
     const int head = 4 * nt + (gp >> 1), grp = gp & 1;
@@ -160,6 +176,7 @@ __global__ void __launch_bounds__(128) k_qprep(LayerView lv, const __nv_bfloat16
     }
     frag[((kb * 2 + nt) * 32 + lp) * 2 + r] = word;
   }
+  pdl_wait();                                    // the decode kernel waits on this grid, and through it on the append
 }
 
 // ---------------------------------------------------------------------------
@@ -247,10 +264,9 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
     }
     __syncthreads();
   }
-  const int nslots = ws.max_splits + 1;
 #pragma unroll
   for (int hh = 0; hh < GQ; ++hh) {
-    float* part = part_ptr(ws.partials, b, lv.hq, hq0 + hh, nslots, s);
+    float* part = part_ptr(ws.partials, b, lv.hq, hq0 + hh, ws.nslots, s);
     if (tid == 0) { part[0] = mrow[hh]; part[1] = lrow[hh]; }
     part[4 + tid] = acc[hh];
   }
@@ -319,11 +335,11 @@ __device__ __forceinline__ void attend_bf16_list(const uint8_t* __restrict__ pag
 }
 
 // BF16 sink + recent segment of the mixed-precision pool. grid = (hkv, B), block = 128.
-// Writes its partial into slot max_splits.
+// Writes its partial into slot `slot` (right after the history splits).
 template <int GQ>
 __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace ws, const __nv_bfloat16* __restrict__ q,
                                                   const int* __restrict__ seq_lens, const int* __restrict__ bf16_pt,
-                                                  float scale_log2) {
+                                                  float scale_log2, int slot) {
   __shared__ __align__(16) __nv_bfloat16 ks[kP][kD + 8];
   __shared__ __align__(16) __nv_bfloat16 vs[kP][kD];
   __shared__ float qs[GQ][kD];
@@ -355,46 +371,40 @@ __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace 
   };
   attend_bf16_list<GQ>(lv.bf16, lv.hkv, h, n_sink + n_rec, scale_log2, locate, ks, vs, qs, pbuf, mrow, lrow, alpha,
                        valid, acc);
-  const int nslots = ws.max_splits + 1;
 #pragma unroll
   for (int hh = 0; hh < GQ; ++hh) {
-    float* part = part_ptr(ws.partials, b, lv.hq, hq0 + hh, nslots, ws.max_splits);
+    float* part = part_ptr(ws.partials, b, lv.hq, hq0 + hh, ws.nslots, slot);
     if (tid == 0) { part[0] = mrow[hh]; part[1] = lrow[hh]; }
     part[4 + tid] = acc[hh];
   }
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of the history splits and the BF16 partial.
-// grid = (hkv, B), block = 128 (thread = output channel). In explicit-V mode
-// the combined history accumulator, which lives in the rotated value basis,
-// is multiplied by R_V^T = P_br H U_V^T before it meets the BF16 partial.
+// Log-sum-exp merge of the history splits (slots [0, nsplit)) and the BF16
+// partial (slot nsplit). grid = (hkv, B), block = 128 (thread = output
+// channel). In explicit-V mode the combined history accumulator, which lives
+// in the rotated value basis, is multiplied by R_V^T = P_br H U_V^T before it
+// meets the BF16 partial.
 template <int GQ>
 __global__ void __launch_bounds__(128) k_merge(LayerView lv, DecodeWorkspace ws, int nsplit, void* out, int out_dtype,
                                                float* lse) {
   extern __shared__ __align__(16) float smem[];
-  float* Uv = smem;                         // [128][129] padded rows, explicit mode only
-  float* wv = smem + kD * (kD + 1);         // [128] history accumulator, rotated basis
+  float* wv = smem;                         // [128] history accumulator, rotated basis
   float* zv = wv + kD;                      // [128] after P_br and H
   const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x, lane = c & 31;
   const bool expl = lv.v_explicit != 0;
-  if (expl) {
-    const float* u = lv.params + (size_t)h * kParamFloats + kUVOff;
-    for (int i = c; i < kD * kD; i += 128) Uv[(i / kD) * (kD + 1) + (i % kD)] = u[i];
-  }
-  __syncthreads();
-  const int nslots = ws.max_splits + 1;
+  const float* uvt = lv.params + (size_t)h * kParamFloats + kUVtOff;
   for (int qi = 0; qi < GQ; ++qi) {
     const int hq = h * GQ + qi;
-    const float* pb = part_ptr(ws.partials, b, lv.hq, hq, nslots, 0);
+    const float* pb = part_ptr(ws.partials, b, lv.hq, hq, ws.nslots, 0);
     float M1 = -INFINITY;
     for (int s = 0; s < nsplit; ++s) M1 = fmaxf(M1, pb[s * kPartFloats]);
     float L1 = 0.f, A1 = 0.f;
     if (M1 != -INFINITY) {
+#pragma unroll 8
       for (int s = 0; s < nsplit; ++s) {
         const float m = pb[s * kPartFloats];
-        if (m == -INFINITY) continue;
-        const float w = exp2f(m - M1);
+        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M1);
         L1 = fmaf(pb[s * kPartFloats + 1], w, L1);
         A1 = fmaf(pb[s * kPartFloats + 4 + c], w, A1);
       }
@@ -411,14 +421,13 @@ __global__ void __launch_bounds__(128) k_merge(LayerView lv, DecodeWorkspace ws,
         }
         __syncthreads();
         float o = 0.f;
-        const float* urow = Uv + c * (kD + 1);
 #pragma unroll 8
-        for (int i = 0; i < kD; ++i) o = fmaf(zv[i], urow[i], o);
+        for (int i = 0; i < kD; ++i) o = fmaf(zv[i], uvt[i * kD + c], o);   // (z U_V^T)[c]
         A1 = o;
         __syncthreads();
       }
     }
-    const float* pbf = pb + (size_t)ws.max_splits * kPartFloats;
+    const float* pbf = pb + (size_t)nsplit * kPartFloats;
     const float m2 = pbf[0], l2 = pbf[1], A2 = pbf[4 + c];
     const float M = fmaxf(M1, m2);
     const float w1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - M);
@@ -501,25 +510,39 @@ __global__ void __launch_bounds__(128) k_merge_plain(const float* __restrict__ p
 // ---------------------------------------------------------------------------
 // host launchers
 
-int launch_int2_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
-                    cudaStream_t st);   // decode_mma.cu
+int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
+                      cudaStream_t st);   // decode_mma.cu
 
 template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
-  k_qprep<<<dim3(lv.hkv, a.B), 128, kQprepSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(a.q), ws, scale_log2);
-  if (a.ev0) cudaEventRecord(a.ev0, st);
-  if (a.algo == OSCAR_DECODE_MMA) {
-    int rc = launch_int2_mma(lv, ws, a, scale_log2, st);
-    if (rc != OSCAR_OK) return rc;
-  } else {
-    k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
-                                                                 a.pages_per_split, scale_log2);
+  if (a.ev0) cudaEventRecord(a.ev0, st);     // the traced span is the whole decode call
+  {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(lv.hkv, a.B);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = kQprepSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_qprep, lv, static_cast<const __nv_bfloat16*>(a.q), ws, scale_log2) != cudaSuccess)
+      return OSCAR_ERR_CUDA;
   }
-  if (a.ev1) cudaEventRecord(a.ev1, st);
+  if (a.algo == OSCAR_DECODE_MMA) {
+    // one fused launch: history splits, BF16 chunks and the merge by the group's last CTA
+    const int rc = launch_decode_mma(lv, ws, a, scale_log2, st);
+    if (a.ev1) cudaEventRecord(a.ev1, st);
+    return rc;
+  }
+  k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
+                                                               a.pages_per_split, scale_log2);
   k_bf16_seg<GQ><<<dim3(lv.hkv, a.B), 128, 0, st>>>(lv, ws, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens,
-                                                    a.bf16_pt, scale_log2);
+                                                    a.bf16_pt, scale_log2, a.nsplit);
   k_merge<GQ><<<dim3(lv.hkv, a.B), 128, kMergeSmem, st>>>(lv, ws, a.nsplit, a.out, a.out_dtype, a.lse);
+  if (a.ev1) cudaEventRecord(a.ev1, st);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 

@@ -6,19 +6,22 @@
 namespace oscar {
 
 constexpr int kDefaultDecodeAlgo = OSCAR_DECODE_MMA;
+constexpr int kMaxMmaSplits = 2048;        // bounds the fused merge's per-slot weight table in shared memory
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
 constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
-constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4;           // U + row + 4 partial rows
-constexpr int kQprepSmem = (kD * kD + 8 * kD) * 4;                 // U_K + up to 8 query rows
-constexpr int kMergeSmem = (kD * (kD + 1) + 4 * kD) * 4;           // padded U_V + work rows
+constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;      // U + row + 4 partial rows + mbarrier
+constexpr int kQprepSmem = (kD * kD + 8 * kD) * 4 + 16;            // U_K + up to 8 query rows + mbarrier
+constexpr int kMergeSmem = 4 * kD * 4;                             // work rows of the merge
 
 // Decode workspace carved from the caller's workspace buffer.
 struct DecodeWorkspace {
   float* qrot;        // [max_batch][hq][kD] rotated queries (float32, rotated channel order)
   uint32_t* qfrag;    // [max_batch][hkv][kFragWords] fp16 MMA B fragments of the rotated queries
   float* qconst;      // [max_batch][hq][kQConst] per-query-head constants, see kQ* below
-  float* partials;    // [max_batch][hq][max_splits + 1][kPartFloats]
-  int max_splits;
+  float* partials;    // [max_batch][hq][nslots][kPartFloats]: history splits, then BF16 chunks
+  uint32_t* counters; // [max_batch][hkv] completion tickets of the fused decode (zero between calls)
+  int max_splits;     // history splits available
+  int nslots;         // partial slots per (request, q head) = max_splits + BF16 chunks
 };
 
 // Per-query-head constants written by the query prologue.
@@ -54,6 +57,7 @@ struct DecodeArgs {
   int out_dtype;
   float* lse;
   int nsplit;            // history splits launched per (request, kv head)
+  int nbf;               // BF16 (sink + recent) chunks of 64 tokens per (request, kv head)
   int pages_per_split;
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   cudaEvent_t ev0, ev1;  // optional events around the history kernel (may be null)
@@ -72,7 +76,7 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
 namespace oscar {
 // api.cu helpers for entry points that work without a cache handle
 int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, LayerView* out);
-void decode_split_policy(int B, int hkv, int gq, int max_pages, int max_splits, int sms, int algo, int* nsplit,
-                         int* pps);
+void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
+                         int* nsplit, int* pps);
 int configure_kernels();
 }  // namespace oscar

@@ -5,6 +5,7 @@
 // oldest recent token is demoted into the INT2 history).
 #include "kernels.cuh"
 #include "rotate.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 
@@ -165,12 +166,15 @@ __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat1
                                                 const int* __restrict__ seq_lens_before,
                                                 const int* __restrict__ hist_pt, int max_hist_pages,
                                                 const int* __restrict__ bf16_pt) {
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(128) float smem[];
   float* Us = smem;                 // [128][128]
   float* xs = smem + kD * kD;       // [128]
   float* part = xs + kD;            // [4][128]
+  const uint32_t bar = smem_addr(part + 4 * kD);
+  __shared__ int landed;
   const int b = blockIdx.x, h = blockIdx.y, kind = blockIdx.z;
   const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();          // the query prologue may start; it waits for this grid before exiting
   const int bf16_per_req = (lv.sink + lv.recent) / kP;
   const int L_old = seq_lens_before[b];
   if (L_old < 0) { if (threadIdx.x == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN); return; }
@@ -188,17 +192,22 @@ __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat1
       if (threadIdx.x == 0) flag(lv.status, ok_h ? OSCAR_STATUS_BAD_PAGE : OSCAR_STATUS_BAD_SEQLEN);
     } else {
       const __nv_bfloat16* src = bf16_row(lv, spage, h, kind, slot % kP);
+      if (rotate && threadIdx.x == 0) {
+        mbar_init(bar);
+        bulk_load(smem_addr(Us), prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff), kD * kD * 4, bar);
+      }
       if (threadIdx.x < 64) {
         float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(src)[threadIdx.x]);
         xs[2 * threadIdx.x] = f.x; xs[2 * threadIdx.x + 1] = f.y;
       }
-      if (rotate) {
-        const float4* us = reinterpret_cast<const float4*>(prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff));
-        float4* ud = reinterpret_cast<float4*>(Us);
-#pragma unroll 8
-        for (int i = threadIdx.x; i < kD * kD / 4; i += 128) ud[i] = us[i];
-      }
+      if (threadIdx.x == 0) landed = 1;
       __syncthreads();
+      if (rotate && !mbar_wait(bar, 0)) landed = 0;
+      __syncthreads();
+      if (!landed) {                // U never arrived: report, leave the row untouched
+        if (threadIdx.x == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+        return;
+      }
       float y[4];
       if (rotate) {
         // warp w sums rows [32w, 32w+32) of U

@@ -248,13 +248,15 @@ int oscar_calibrate(const float* Q, const float* K, const float* V, int N, float
 
 /* ---- tracing ------------------------------------------------------------- */
 
-/* Start timing the INT2 history kernel: while enabled, every
- * oscar_decode_attention records a CUDA event pair around that kernel on its
- * stream (at most `capacity` launches are kept). */
+/* Start tracing decode calls: while enabled, every oscar_decode_attention
+ * records a CUDA event pair on its stream around all of its kernels (query
+ * prologue through merge); at most `capacity` calls are kept. Event records
+ * can be captured into a CUDA graph; the graph then re-records the same
+ * events on every replay. */
 int oscar_profile_begin(oscar_cache* cache, int capacity);
 
-/* Stop, synchronise and report the summed device time (ms) of the recorded
- * launches and their count. */
+/* Stop, synchronise and report the summed device time (ms) of the traced
+ * calls and their count. */
 int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
 
 /* ---- allocation-free decode ---------------------------------------------- */
@@ -285,9 +287,10 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
  * last call's contents (the status word is cleared at the start of each
  * call): calls that may overlap on the GPU (different streams, or threads
  * without ordering) race and give wrong results; calls ordered on one stream
- * are safe. The history is split into fewer pieces when needed to fit; a call
- * whose B * Hq * 1600 + B * Hkv * 4096 bytes (plus 1 KB) exceed 4 MiB, i.e. too
- * many query rows even with one split, returns OSCAR_ERR_TOO_LARGE before any
+ * are safe. The history is split into fewer pieces when needed to fit. A call
+ * whose per-query state does not fit even with one history split, i.e. when
+ * B * Hq * (544 + 528 * (1 + (sink + recent) / 64)) + B * Hkv * 4100 bytes plus
+ * about 1.5 KB of rounding exceed 4 MiB, returns OSCAR_ERR_TOO_LARGE before any
  * device work. */
 int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B, const void* q,
                                    const int32_t* seq_lens, const int32_t* hist_pt, int max_hist_pages,

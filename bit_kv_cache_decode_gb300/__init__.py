@@ -34,7 +34,7 @@ EXPORTS = (
     "oscar_quantize_prefill", "oscar_append_kv", "oscar_decode_attention", "oscar_set_decode_algo",
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
-    "oscar_decode_attention_noalloc",
+    "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
 )
 
 
@@ -75,6 +75,8 @@ def _load() -> ctypes.CDLL:
         "oscar_calibrate": [vp, vp, vp, c_int, c_float, c_float, c_float, vp, vp, vp, vp, vp, vp],
         "oscar_profile_begin": [vp, c_int],
         "oscar_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)],
+        "oscar_trace_ctas": [vp, vp, c_int],
+        "oscar_decode_step": [vp, c_int, c_int, vp, vp, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
         "oscar_decode_attention_noalloc": [ctypes.POINTER(Layout), vp, c_int, c_int, vp, i32p, i32p, c_int, i32p,
                                            c_float, vp, c_int, vp, vp, vp],
     }
@@ -240,6 +242,21 @@ class OscarCache:
                                            out_dtype, _ptr(lse), _stream(stream)), "oscar_decode_attention")
         return out
 
+    def decode_step(self, layer: int, q, k, v, seq_lens_before, hist_pt, bf16_pt, sm_scale: float, out=None,
+                    out_dtype: int = OUT_BF16, lse=None, stream=None):
+        """append_kv(k, v) then decode_attention(q) over seq_lens_before + 1 tokens, in one call."""
+        import torch
+        sl = _dev_i32(seq_lens_before, self.device)
+        hp = _dev_i32(hist_pt, self.device)
+        bp = _dev_i32(bf16_pt, self.device)
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
+                              device=self.device)
+        _check(_lib.oscar_decode_step(self._h, layer, sl.numel(), _ptr(q), _ptr(k), _ptr(v), _ptr(sl), _ptr(hp),
+                                      hp.shape[1] if hp.dim() == 2 else 0, _ptr(bp), float(sm_scale), _ptr(out),
+                                      out_dtype, _ptr(lse), _stream(stream)), "oscar_decode_step")
+        return out
+
     def set_decode_algo(self, algo: int):
         _check(_lib.oscar_set_decode_algo(self._h, algo), "oscar_set_decode_algo")
 
@@ -262,6 +279,12 @@ class OscarCache:
         _check(_lib.oscar_rotate(self._h, layer, kind, _ptr(x), _ptr(y), int(x.shape[0]), _stream(stream)),
                "oscar_rotate")
         return y
+
+    def trace_ctas(self, buf=None):
+        """Record per-CTA timelines of following tensor-core decode launches into ``buf`` (an int64 device
+        tensor of 8 * n elements, n records); None stops recording."""
+        n = 0 if buf is None else buf.numel() // 8
+        _check(_lib.oscar_trace_ctas(self._h, _ptr(buf), n), "oscar_trace_ctas")
 
     def profile_begin(self, capacity: int):
         _check(_lib.oscar_profile_begin(self._h, capacity), "oscar_profile_begin")

@@ -61,8 +61,8 @@ void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, si
          + align_up(B * hq * kD * sizeof(float))                   // qrot
          + align_up(B * hkv * kFragWords * sizeof(uint32_t))       // qfrag
          + align_up(B * hq * kQConst * sizeof(float))              // qconst
-         + align_up(B * hq * (L->max_splits + (L->sink + L->recent) / kP) * kPartFloats * sizeof(float))  // partials
-         + align_up(B * hkv * sizeof(uint32_t));                   // completion counters
+         + align_up(B * hq * partial_slots(L->max_splits, (L->sink + L->recent) / kP) * kPartFloats * sizeof(float))
+         + align_up(B * hkv * kCountersPerGroup * sizeof(uint32_t));   // completion tickets
 }
 
 LayerView view(const oscar_cache* c, int layer) {
@@ -182,7 +182,9 @@ int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, 
   p += align_up(B * hq * kQConst * sizeof(float));
   c->dws.partials = reinterpret_cast<float*>(p);
   c->dws.max_splits = layout->max_splits;
-  c->dws.nslots = layout->max_splits + (layout->sink + layout->recent) / kP;
+  c->dws.cta_trace = nullptr;
+  c->dws.trace_cap = 0;
+  c->dws.nslots = partial_slots(layout->max_splits, (layout->sink + layout->recent) / kP);
   p += align_up(B * hq * c->dws.nslots * kPartFloats * sizeof(float));
   c->dws.counters = reinterpret_cast<uint32_t*>(p);
   c->sms = sms;
@@ -190,7 +192,7 @@ int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, 
   c->prof_on = false;
   c->prof_cap = c->prof_n = 0;
   if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess ||
-      cudaMemset(c->dws.counters, 0, B * hkv * sizeof(uint32_t)) != cudaSuccess) {
+      cudaMemset(c->dws.counters, 0, B * hkv * kCountersPerGroup * sizeof(uint32_t)) != cudaSuccess) {
     delete c;
     return OSCAR_ERR_CUDA;
   }
@@ -304,6 +306,8 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.out_dtype = out_dtype;
   a.lse = lse;
   a.algo = c->algo;
+  a.len_add = 0;
+  a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
     int cps, align, extra;
@@ -318,6 +322,56 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
     c->prof_n++;
   }
   return launch_decode(view(c, layer), c->dws, a, st);
+}
+
+int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const void* k, const void* v,
+                      const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
+                      const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || B > c->lay.max_batch || max_hist_pages < 0)
+    return OSCAR_ERR_INVALID_ARG;
+  if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
+  if (B == 0) return OSCAR_OK;
+  if (!q || !k || !v || !seq_lens_before || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt))
+    return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return OSCAR_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  LayerView lv = view(c, layer);
+  DecodeArgs a;
+  a.B = B;
+  a.q = q;
+  a.seq_lens = seq_lens_before;
+  a.len_add = 1;                         // attend over the appended token too
+  a.hist_pt = hist_pt;
+  a.max_hist_pages = max_hist_pages;
+  a.bf16_pt = bf16_pt;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.algo = c->algo;
+  a.nbf = (c->lay.sink + c->lay.recent) / kP;
+  {
+    int cps, align, extra;
+    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra);
+    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, &a.nsplit,
+                  &a.pages_per_split);
+  }
+  a.ev0 = a.ev1 = nullptr;
+  if (c->prof_on && c->prof_n < c->prof_cap) {
+    a.ev0 = c->prof_ev[2 * c->prof_n];
+    a.ev1 = c->prof_ev[2 * c->prof_n + 1];
+    c->prof_n++;
+  }
+  // tensor-core path: the append kernel also runs the query prologue
+  a.skip_qprep = a.algo == OSCAR_DECODE_MMA;
+  if (a.ev0) cudaEventRecord(a.ev0, st);
+  int rc = a.skip_qprep ? launch_append_qprep(lv, c->dws, B, q, k, v, seq_lens_before, hist_pt, max_hist_pages,
+                                              bf16_pt, sm_scale, st)
+                        : launch_append(lv, B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt, st);
+  if (rc != OSCAR_OK) return rc;
+  a.ev0 = nullptr;                       // recorded above: the profiled span starts at the append
+  return launch_decode(lv, c->dws, a, st);
 }
 
 int oscar_get_status(oscar_cache* c, int* code) {
@@ -380,6 +434,14 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
                             pps, reinterpret_cast<int*>(w), static_cast<cudaStream_t>(stream));
+}
+
+int oscar_trace_ctas(oscar_cache* c, void* buf, int capacity) {
+  if (!c || capacity < 0 || (buf != nullptr && capacity == 0)) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(buf) % 8) return OSCAR_ERR_INVALID_ARG;
+  c->dws.cta_trace = static_cast<unsigned long long*>(buf);
+  c->dws.trace_cap = buf ? capacity : 0;
+  return OSCAR_OK;
 }
 
 int oscar_profile_begin(oscar_cache* c, int capacity) {

@@ -12,11 +12,13 @@
 // bounded and report OSCAR_STATUS_TIMEOUT instead of hanging.
 //
 // Per 16-token tile the two contractions run on mma.sync.m16n8k16 f16 -> f32:
-//  * logits: A = codes [16 tokens x 16 channels], B = query fragments
-//    [16 channels x 8 columns], column = (head, group) of a 4-head n-tile; the
-//    code c of channel ch is fed as the fp16 value 1024 + c*4^(ch%4) (one
-//    LOP3: mask | 0x6400), whose constant part and scale the query prologue
-//    folded into the fragments and the per-head offsets;
+//  * logits: A = codes [16 tokens x 16 channels of one group], B = query
+//    fragments [16 channels x 8 columns], column = (head, hi or lo fp16 part
+//    of the query) of a 4-head n-tile, one accumulator per channel group; the
+//    code c of channel ch is shifted into mantissa bits 6-7 or 8-9 and fed as
+//    the fp16 value 1024 + c*64 or 1024 + c*256 (one LOP3: mask | 0x6400),
+//    whose constant part and scale the query prologue folded into the
+//    fragments and the per-head offsets;
 //  * P.Vhat: A = codes [16 channels x 16 tokens] (the V page layout pairs two
 //    tokens in one 32-bit word, so mask | 0x6400 and one HFMA2 give the exact
 //    fp16 codes of one channel for two tokens), B = p * scale [16 tokens x 8
@@ -40,6 +42,7 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kBucket = kMergeBucket;          // history splits merged together at the first level
 constexpr int kStages = 2;
 constexpr uint32_t kMagic = 0x64006400u;       // fp16 1024.0 in both halves
 // stage ring, mbarriers, a timeout flag, and slack to align the ring to 128 bytes
@@ -90,6 +93,7 @@ __device__ __forceinline__ uint32_t exact_codes(uint32_t biased, int k) {
 
 struct FusedArgs {
   const int* seq_lens;
+  int len_add;                       // attend over seq_lens[b] + len_add tokens
   const int* hist_pt;
   int max_hist_pages;
   int pages_per_split;
@@ -110,7 +114,7 @@ __device__ __forceinline__ float* part_row(const DecodeWorkspace& ws, int b, int
 // History split `split` of group (b, h): see the file comment.
 template <int NT>
 __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
-                                           uint8_t* smem, int split, int h, int b) {
+                                           uint8_t* smem, int split, int h, int b, unsigned long long* trace) {
   const int* __restrict__ seq_lens = fa.seq_lens;
   const int* __restrict__ hist_pt = fa.hist_pt;
   const int max_hist_pages = fa.max_hist_pages, pages_per_split = fa.pages_per_split;
@@ -122,7 +126,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   __syncthreads();
 
   // ---- pages of this warp --------------------------------------------------------
-  const int L = seq_lens[b];
+  const int L = seq_lens[b] + fa.len_add;
   int Lh = max(0, L - lv.sink - lv.recent);
   int npages = (Lh + kP - 1) / kP;
   if (npages > max_hist_pages) {
@@ -182,18 +186,20 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         qf[kb][nt][1] = v.y;
       }
   }
-  float cF[NT], cZ0[NT], cZ1[NT], cO0[NT], cO1[NT];
+  float cF[NT], cZ0[NT], cZ1[NT], cO0h[NT], cO0l[NT], cO1h[NT], cO1l[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = 4 * nt + t;
-    cF[nt] = cZ0[nt] = cZ1[nt] = cO0[nt] = cO1[nt] = 0.f;
+    cF[nt] = cZ0[nt] = cZ1[nt] = cO0h[nt] = cO0l[nt] = cO1h[nt] = cO1l[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
       cF[nt] = qc[kQF];
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
-      cO0[nt] = qc[kQOff0];
-      cO1[nt] = qc[kQOff1];
+      cO0h[nt] = qc[kQOff0H];
+      cO0l[nt] = qc[kQOff0L];
+      cO1h[nt] = qc[kQOff1H];
+      cO1l[nt] = qc[kQOff1L];
     }
   }
 
@@ -219,6 +225,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     const int s = i % kStages;
     if (issued & (1u << s)) {
       const bool landed = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * s, (phase >> s) & 1u));
+      if (trace != nullptr && i == 0 && tid == 0) trace[3] = global_ns();      // first page of warp 0 landed
       if (!landed) {                   // warp-uniform decision: the shuffles and MMAs below need every lane
         timed_out = true;
         break;
@@ -233,24 +240,35 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
         const int r0 = 16 * mt + g, r1 = r0 + 8;
-        const uint2 kw0 = *reinterpret_cast<const uint2*>(blk + kKCodesOff + r0 * 32 + 8 * t);
-        const uint2 kw1 = *reinterpret_cast<const uint2*>(blk + kKCodesOff + r1 * 32 + 8 * t);
-        const uint32_t x0h = kw0.x >> 8, x1h = kw0.y >> 8, y0h = kw1.x >> 8, y1h = kw1.y >> 8;
-        float c[NT][4];                            // start from -offset: the MMAs add the biased sums
+        // words t (channels 16t .. 16t+15, group 0) and t + 4 (group 1) of rows r0, r1
+        const uint32_t kx[2] = {*reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r0 * 32 + 4 * t),
+                                *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r0 * 32 + 16 + 4 * t)};
+        const uint32_t ky[2] = {*reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r1 * 32 + 4 * t),
+                                *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r1 * 32 + 16 + 4 * t)};
+        float c[2][NT][4];                         // per group; start from -offset: the MMAs add the biased sums
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          c[nt][0] = c[nt][2] = -cO0[nt];
-          c[nt][1] = c[nt][3] = -cO1[nt];
+          c[0][nt][0] = c[0][nt][2] = -cO0h[nt];
+          c[0][nt][1] = c[0][nt][3] = -cO0l[nt];
+          c[1][nt][0] = c[1][nt][2] = -cO1h[nt];
+          c[1][nt][1] = c[1][nt][3] = -cO1l[nt];
         }
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t m = 0x00030003u << (2 * (kb & 3));
-          const uint32_t a0 = and_or(kb < 4 ? kw0.x : x0h, m, kMagic);
-          const uint32_t a1 = and_or(kb < 4 ? kw1.x : y0h, m, kMagic);
-          const uint32_t a2 = and_or(kb < 4 ? kw0.y : x1h, m, kMagic);
-          const uint32_t a3 = and_or(kb < 4 ? kw1.y : y1h, m, kMagic);
+        for (int G = 0; G < 2; ++G) {
+          // code i (bits 2i of each 16-bit half) is moved into bits 6-7 (i even) or 8-9 (i odd):
+          // shift left 6 for i = 0, 1; left 2 for i = 2, 3; right 2 for i = 4, 5; right 6 for i = 6, 7
+          const uint32_t wx[4] = {kx[G] << 6, kx[G] << 2, kx[G] >> 2, kx[G] >> 6};
+          const uint32_t wy[4] = {ky[G] << 6, ky[G] << 2, ky[G] >> 2, ky[G] >> 6};
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(c[nt], a0, a1, a2, a3, qf[kb][nt][0], qf[kb][nt][1]);
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t a0 = and_or(wx[j], 0x00C000C0u, kMagic);   // row r0, codes 2j (k rows 2t, 2t+1)
+            const uint32_t a1 = and_or(wy[j], 0x00C000C0u, kMagic);   // row r1
+            const uint32_t a2 = and_or(wx[j], 0x03000300u, kMagic);   // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
+            const uint32_t a3 = and_or(wy[j], 0x03000300u, kMagic);   // row r1
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+          }
         }
         const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r0 * 8);
         const uint2 mk1 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r1 * 8);
@@ -260,8 +278,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         const float2 sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          lg[mt][nt][0] = fmaf(cF[nt], fmaf(sz00.x, c[nt][0], sz01.x * c[nt][1]), fmaf(sz00.y, cZ0[nt], sz01.y * cZ1[nt]));
-          lg[mt][nt][1] = fmaf(cF[nt], fmaf(sz10.x, c[nt][2], sz11.x * c[nt][3]), fmaf(sz10.y, cZ0[nt], sz11.y * cZ1[nt]));
+          const float a00 = c[0][nt][0] + c[0][nt][1], a01 = c[1][nt][0] + c[1][nt][1];   // row r0: hi + lo per group
+          const float a10 = c[0][nt][2] + c[0][nt][3], a11 = c[1][nt][2] + c[1][nt][3];   // row r1
+          lg[mt][nt][0] = fmaf(cF[nt], fmaf(sz00.x, a00, sz01.x * a01), fmaf(sz00.y, cZ0[nt], sz01.y * cZ1[nt]));
+          lg[mt][nt][1] = fmaf(cF[nt], fmaf(sz10.x, a10, sz11.x * a11), fmaf(sz10.y, cZ0[nt], sz11.y * cZ1[nt]));
         }
         if (ntok < kP) {                           // ragged last page: rows past the end take no weight
 #pragma unroll
@@ -355,6 +375,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     any_timeout = 1;
   }
 
+  if (trace != nullptr && lane == 0) atomicMax(&trace[4], global_ns());      // last warp's main loop done
   // ---- reduce per-lane sums over the 8 lanes of a head, then combine the warps ---------
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -429,7 +450,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int gq = lv.hq / lv.hkv, hq0 = h * gq;
   pdl_wait();                                      // the append writes into these pages
-  const int L = fa.seq_lens[b];
+  const int L = fa.seq_lens[b] + fa.len_add;
   if (L < 1 && tid == 0 && c == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);
   const int n_sink = max(0, min(L, lv.sink));
   const int n_rec = L > lv.sink ? min(L - lv.sink, lv.recent) : 0;
@@ -509,59 +530,65 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
   }
 }
 
-// Merge of group (b, h) by its last CTA: warp w handles query heads w, w+4;
-// lane q handles channels 4q..4q+3. Slots [0, nsplit) are history splits, slots
-// nsplit .. nsplit + nbf - 1 the BF16 pages. Partials are read with L1-bypassing loads (other
-// CTAs of this launch wrote them). Pass 1 gives every slot its weight, pass 2
-// streams the accumulators with many loads in flight.
-__device__ __forceinline__ void merge_group(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
-                                            uint8_t* smem, int h, int b) {
+// Online-softmax combine of slots [s0, s1) of one query head's partials, by
+// one warp: lane q handles channels 4q..4q+3. Every lane reads the slot
+// maxima itself (broadcast loads), so no shuffles are needed. Partials are read
+// with L1-bypassing loads: other CTAs of this launch wrote them. Returns the
+// combined (M, L, A) with L, A relative to 2^M; no live slot gives M = -inf.
+__device__ __forceinline__ void combine_slots(const float* row0, int s0, int s1, int lane, float& M, float& L,
+                                              float4& A) {
+  M = -INFINITY;
+#pragma unroll 8
+  for (int s = s0; s < s1; ++s) M = fmaxf(M, __ldcg(row0 + (size_t)s * kPartFloats));
+  L = 0.f;
+  A = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M == -INFINITY) return;
+#pragma unroll 8
+  for (int s = s0; s < s1; ++s) {
+    const float* r = row0 + (size_t)s * kPartFloats;
+    const float m = __ldcg(r);
+    const float l = __ldcg(r + 1);
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
+    const float wgt = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+    L = fmaf(l, wgt, L);
+    A.x = fmaf(a.x, wgt, A.x); A.y = fmaf(a.y, wgt, A.y); A.z = fmaf(a.z, wgt, A.z); A.w = fmaf(a.w, wgt, A.w);
+  }
+}
+
+// First-level merge: slots [s0, s1) of every query head of group (b, h) into slot `dst`.
+__device__ __forceinline__ void merge_bucket(const LayerView& lv, const DecodeWorkspace& ws, int h, int b, int s0,
+                                             int s1, int dst) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lv.hq / lv.hkv;
+  for (int hh = w; hh < gq; hh += 4) {
+    const float* row0 = part_row(ws, b, lv.hq, h * gq + hh, 0);
+    float M, L;
+    float4 A;
+    combine_slots(row0, s0, s1, lane, M, L, A);
+    float* d = part_row(ws, b, lv.hq, h * gq + hh, dst);
+    if (lane == 0) { d[0] = M; d[1] = L; }
+    reinterpret_cast<float4*>(d + 4)[lane] = A;
+  }
+}
+
+// Final merge of group (b, h): history buckets [hb0, hb0 + nb) and the BF16
+// bucket `bfs`; warp w handles query heads w, w+4, lane q channels 4q..4q+3.
+// In explicit-V mode the history part, which lives in the rotated value basis,
+// is multiplied by R_V^T = P_br H U_V^T before it meets the BF16 part.
+__device__ __forceinline__ void merge_final(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
+                                            uint8_t* smem, int h, int b, int hb0, int nb, int bfs) {
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int gq = lv.hq / lv.hkv;
   const bool expl = lv.v_explicit != 0;
-  const int ns = fa.nsplit;
-  float* ybuf = reinterpret_cast<float*>(smem) + w * 2 * kD;          // [128] accumulator, then [128] after P_br H
-  float* wts = reinterpret_cast<float*>(smem) + 4 * 2 * kD + w * (ns + 1);   // slot weights of this warp's head
+  float* ybuf = reinterpret_cast<float*>(smem) + w * 2 * kD;       // [128] accumulator, then [128] after P_br H
   for (int hh = w; hh < gq; hh += 4) {
     const int hq = h * gq + hh;
     const float* row0 = part_row(ws, b, lv.hq, hq, 0);
-    float M1 = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M1 = fmaxf(M1, __ldcg(row0 + (size_t)s * kPartFloats));
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, x));
-    float L1 = 0.f;
-    for (int s = lane; s < ns; s += 32) {
-      const float m = __ldcg(row0 + (size_t)s * kPartFloats);
-      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M1);
-      wts[s] = wgt;
-      L1 = fmaf(__ldcg(row0 + (size_t)s * kPartFloats + 1), wgt, L1);
-    }
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) L1 += __shfl_xor_sync(0xffffffffu, L1, x);
-    __syncwarp();
-    float4 A1 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-    for (int s = 0; s < ns; ++s) {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(row0 + (size_t)s * kPartFloats + 4) + lane);
-      const float wgt = wts[s];
-      A1.x = fmaf(a.x, wgt, A1.x); A1.y = fmaf(a.y, wgt, A1.y); A1.z = fmaf(a.z, wgt, A1.z); A1.w = fmaf(a.w, wgt, A1.w);
-    }
-    // BF16 pages: slots ns .. ns + nbf - 1
-    float M2 = -INFINITY;
-    for (int s = 0; s < fa.nbf; ++s) M2 = fmaxf(M2, __ldcg(row0 + (size_t)(ns + s) * kPartFloats));
-    float L2 = 0.f;
-    float4 A2 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < fa.nbf; ++s) {
-      const float* rb = row0 + (size_t)(ns + s) * kPartFloats;
-      const float m = __ldcg(rb);
-      if (m == -INFINITY) continue;
-      const float wgt = exp2f(m - M2);
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(rb + 4) + lane);
-      L2 = fmaf(__ldcg(rb + 1), wgt, L2);
-      A2.x = fmaf(a.x, wgt, A2.x); A2.y = fmaf(a.y, wgt, A2.y); A2.z = fmaf(a.z, wgt, A2.z); A2.w = fmaf(a.w, wgt, A2.w);
-    }
+    float M1, L1, M2, L2;
+    float4 A1, A2;
+    combine_slots(row0, hb0, hb0 + nb, lane, M1, L1, A1);
+    combine_slots(row0, bfs, bfs + 1, lane, M2, L2, A2);
     if (expl && M1 != -INFINITY) {
-      // history accumulator is in the rotated value basis: multiply by R_V^T = P_br H U_V^T
       *reinterpret_cast<float4*>(ybuf + 4 * lane) = A1;
       __syncwarp();
       float v[4];
@@ -614,18 +641,52 @@ __global__ void __launch_bounds__(128, NT == 1 ? 4 : 2) k_decode_mma(LayerView l
   uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
   __shared__ int is_last;
   const int h = blockIdx.y, b = blockIdx.z;
-  if (blockIdx.x < fa.nsplit) int2_split<NT>(lv, ws, fa, smem, blockIdx.x, h, b);
+  // optional timeline record of this CTA (ns, %globaltimer):
+  // [0] linear CTA id, [1] SM id, [2] start, [3] first history page landed (warp 0),
+  // [4] last warp's main loop done, [5] partials written, [6] merge done (group's last CTA only), [7] 0
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  unsigned long long* trace =
+      (ws.cta_trace != nullptr && (int)cta < ws.trace_cap) ? ws.cta_trace + 8ull * cta : nullptr;
+  if (trace != nullptr) {
+    if (threadIdx.x == 0) {
+      trace[0] = cta;
+      trace[1] = sm_id();
+      trace[2] = global_ns();
+      trace[3] = trace[4] = trace[5] = trace[6] = trace[7] = 0;
+    }
+    __syncthreads();
+  }
+  if (blockIdx.x < fa.nsplit) int2_split<NT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
   else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
-  // completion ticket: the partial writes above are made visible before the ticket is taken
-  __threadfence();
+  if (trace != nullptr && threadIdx.x == 0) trace[5] = global_ns();
+  // Two-level completion tickets. Slots: history splits [0, nsplit), BF16 pages
+  // [nsplit, nsplit + nbf), bucket partials from nsplit + nbf on (history buckets,
+  // then the BF16 bucket). Counters per group: one per bucket, then the group's.
+  const int nb = (fa.nsplit + kBucket - 1) / kBucket;
+  const int hb0 = fa.nsplit + fa.nbf;
+  const bool hist = (int)blockIdx.x < fa.nsplit;
+  const int j = hist ? (int)blockIdx.x / kBucket : nb;
+  const int members = hist ? min(kBucket, fa.nsplit - j * kBucket) : fa.nbf;
+  uint32_t* ctr = ws.counters + ((size_t)b * lv.hkv + h) * kCountersPerGroup;
+  __threadfence();                                 // this CTA's partials are visible before its ticket
   __syncthreads();
-  uint32_t* ctr = ws.counters + (size_t)b * lv.hkv + h;
-  if (threadIdx.x == 0) is_last = atomicAdd(ctr, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) is_last = atomicAdd(&ctr[j], 1u) == (unsigned)members - 1;
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  merge_group(lv, ws, fa, smem, h, b);
-  if (threadIdx.x == 0) *ctr = 0u;
+  if (hist) merge_bucket(lv, ws, h, b, j * kBucket, j * kBucket + members, hb0 + j);
+  else merge_bucket(lv, ws, h, b, fa.nsplit, fa.nsplit + fa.nbf, hb0 + nb);
+  if (threadIdx.x == 0) ctr[j] = 0u;
+  if (trace != nullptr && threadIdx.x == 0) { trace[6] = global_ns(); trace[7] = 1; }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&ctr[nb + 1], 1u) == (unsigned)nb;   // nb history buckets + BF16
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  merge_final(lv, ws, fa, smem, h, b, hb0, nb, hb0 + nb);
+  if (threadIdx.x == 0) ctr[nb + 1] = 0u;
+  if (trace != nullptr && threadIdx.x == 0) { trace[6] = global_ns(); trace[7] = 2; }
 }
 
 }  // namespace
@@ -634,6 +695,7 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
                       cudaStream_t st) {
   FusedArgs fa;
   fa.seq_lens = a.seq_lens;
+  fa.len_add = a.len_add;
   fa.hist_pt = a.hist_pt;
   fa.max_hist_pages = a.max_hist_pages;
   fa.pages_per_split = a.pages_per_split;

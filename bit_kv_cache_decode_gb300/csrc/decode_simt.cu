@@ -16,6 +16,7 @@
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
+#include "qprep.cuh"
 
 namespace oscar {
 
@@ -68,23 +69,10 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query prologue: q~ = q R_K for every query head, in rotated channel order
-// (ws.qrot), the per-head constants (ws.qconst) and the fp16 B fragments of
-// the tensor-core history kernel (ws.qfrag). grid = (hkv, B), block = 256,
-// U_K staged in shared memory by one bulk copy; warp w rotates query head w.
-// Launched as a programmatic dependent of the append kernel: it lets the decode
-// kernel start at once and waits for the append only before it exits.
-//
-// Fragment encoding (decode_mma.cu unpacks a code c of channel ch as the fp16
-// value 1024 + c * 4^(ch % 4)): fragment value of channel ch of head h is
-// fp16(q~[h][ch] * 2^sigma_h * 4^-(ch % 4)), sigma_h a power-of-two scale that
-// puts max|q~| near 2^12, and the group's constant part is
-// off_g = 1024 * sum_{ch in g} fragment value, so that
-//   sum_{ch in g} (1024 + c 4^(ch%4)) frag(ch) - off_g = 2^sigma sum_{ch in g} c q~[ch].
-// k-block kb (16 channels) at lane (g', t') holds the pairs of k rows
-// (2t', 2t'+1) -> channels (32t'+kb, 32t'+kb+8) and (2t'+8, 2t'+9) ->
-// channels (32t'+16+kb, 32t'+24+kb); column g' is (head 4nt + g'/2, group g'%2)
-// and is zero where the channel is not in that group.
+// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256, U_K staged in
+// shared memory by one bulk copy; warp w rotates query head w. Launched as a
+// programmatic dependent of the append kernel: it lets the decode kernel start
+// at once and waits for the append only before it exits.
 __global__ void __launch_bounds__(256) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws,
                                                float scale_log2) {
   extern __shared__ __align__(128) float smem[];
@@ -95,87 +83,24 @@ __global__ void __launch_bounds__(256) k_qprep(LayerView lv, const __nv_bfloat16
   __shared__ int landed;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int gq = lv.hq / lv.hkv;
-  const int wib = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();
   if (tid == 0) {
     mbar_init(bar);
     bulk_load(smem_addr(Us), lv.params + (size_t)h * kParamFloats + kUKOff, kD * kD * 4, bar);
   }
-  for (int i = tid; i < gq * kD; i += 256) {
-    const int qi = i / kD, c = i % kD;
-    xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq + qi) * kD + c]);
-  }
-  __syncthreads();
-  const bool ok = mbar_wait(bar, 0);
+  for (int i = tid; i < gq * kD; i += 256) xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
   if (tid == 0) landed = 1;
   __syncthreads();
-  if (!ok) landed = 0;                           // benign race: any thread that timed out clears it
+  if (!mbar_wait(bar, 0)) landed = 0;            // any thread that timed out clears it
   __syncthreads();
   if (!landed) {
     if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
     pdl_wait();
     return;
   }
-  for (int qi = wib; qi < gq; qi += 8) {
-    float y[1][4];
-    warp_rotate<1>(Us, xs + qi * kD, y);
-    __syncwarp();                                   // row qi fully read before it is overwritten
-    const int hq = h * gq + qi;
-    float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
-    float s = 0.f, mx = 0.f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int ch = rot_channel(lane, r);
-      dst[ch] = y[0][r];
-      xs[qi * kD + ch] = y[0][r];
-      s += y[0][r];
-      mx = fmaxf(mx, fabsf(y[0][r]));
-    }
-#pragma unroll
-    for (int m = 2; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);   // lanes of equal parity = one group
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    if (lane < 2) ws.qconst[((size_t)b * lv.hq + hq) * kQConst + kQSum0 + lane] = s;
-    if (lane == 0) {
-      int e = 0;
-      if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx in [2^(e-1), 2^e)
-      sig[qi] = min(max(12 - e, -60), 60);
-    }
-  }
+  qprep_rotate(lv, ws, Us, xs, sig, b, h, 8);
   __syncthreads();
-  if (tid < gq) {
-    const int qi = tid, hq = h * gq + qi;
-    float* qc = ws.qconst + ((size_t)b * lv.hq + hq) * kQConst;
-    const float sc = ldexpf(1.f, sig[qi]);
-    float off[kNG] = {0.f, 0.f}, sum[kNG] = {0.f, 0.f};
-    for (int ch = 0; ch < kD; ++ch) {
-      const float v = xs[qi * kD + ch];
-      const float f = __half2float(__float2half_rn(v * sc * ldexpf(1.f, -2 * (ch & 3))));
-      off[ch / kG] += f;
-      sum[ch / kG] += v;
-    }
-    qc[kQF] = scale_log2 * ldexpf(1.f, -sig[qi]);
-    qc[kQZ0] = scale_log2 * sum[0];
-    qc[kQZ1] = scale_log2 * sum[1];
-    qc[kQOff0] = 1024.f * off[0];
-    qc[kQOff1] = 1024.f * off[1];
-    qc[kQSigma] = (float)sig[qi];
-  }
-  const int nt_count = (gq + 3) / 4;
-  uint32_t* frag = ws.qfrag + ((size_t)b * lv.hkv + h) * kFragWords;
-  for (int wi = tid; wi < 8 * 2 * 64; wi += 256) {
-    const int r = wi & 1, lp = (wi >> 1) & 31, nt = (wi >> 6) & 1, kb = wi >> 7;
-    const int gp = lp >> 2, tp = lp & 3;
-    const int head = 4 * nt + (gp >> 1), grp = gp & 1;
-    uint32_t word = 0;
-    if (nt < nt_count && head < gq && (tp >> 1) == grp) {
-      const float sc = ldexpf(1.f, sig[head] - 2 * (kb & 3));
-      const int ch0 = 32 * tp + 16 * r + kb;
-      const __half2 v = __floats2half2_rn(xs[head * kD + ch0] * sc, xs[head * kD + ch0 + 8] * sc);
-      word = *reinterpret_cast<const uint32_t*>(&v);
-    }
-    frag[((kb * 2 + nt) * 32 + lp) * 2 + r] = word;
-  }
+  qprep_finish(lv, ws, xs, sig, b, h, scale_log2, 8);
   pdl_wait();                                    // the decode kernel waits on this grid, and through it on the append
 }
 
@@ -187,7 +112,7 @@ __global__ void __launch_bounds__(256) k_qprep(LayerView lv, const __nv_bfloat16
 template <int GQ>
 __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace ws, const int* __restrict__ seq_lens,
                                                    const int* __restrict__ hist_pt, int max_hist_pages,
-                                                   int pages_per_split, float scale_log2) {
+                                                   int pages_per_split, float scale_log2, int len_add) {
   __shared__ __align__(16) uint8_t blk[kBlockBytes];
   __shared__ float qs[GQ][kD];
   __shared__ float qg[GQ][kNG];
@@ -195,7 +120,7 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
   __shared__ float mrow[GQ], lrow[GQ], alpha[GQ];
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int hq0 = h * GQ;
-  const int L = seq_lens[b];
+  const int L = seq_lens[b] + len_add;
   int Lh = max(0, L - lv.sink - lv.recent);
   int npages = (Lh + kP - 1) / kP;
   if (npages > max_hist_pages) {
@@ -339,7 +264,7 @@ __device__ __forceinline__ void attend_bf16_list(const uint8_t* __restrict__ pag
 template <int GQ>
 __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace ws, const __nv_bfloat16* __restrict__ q,
                                                   const int* __restrict__ seq_lens, const int* __restrict__ bf16_pt,
-                                                  float scale_log2, int slot) {
+                                                  float scale_log2, int slot, int len_add) {
   __shared__ __align__(16) __nv_bfloat16 ks[kP][kD + 8];
   __shared__ __align__(16) __nv_bfloat16 vs[kP][kD];
   __shared__ float qs[GQ][kD];
@@ -348,7 +273,7 @@ __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace 
   __shared__ int valid[kP];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int hq0 = h * GQ;
-  const int L = seq_lens[b];
+  const int L = seq_lens[b] + len_add;
   if (L < 1 && tid == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);
   const int n_sink = max(0, min(L, lv.sink));
   const int n_rec = L > lv.sink ? min(L - lv.sink, lv.recent) : 0;
@@ -517,7 +442,7 @@ template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
   if (a.ev0) cudaEventRecord(a.ev0, st);     // the traced span is the whole decode call
-  {
+  if (!a.skip_qprep) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -538,9 +463,9 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
     return rc;
   }
   k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
-                                                               a.pages_per_split, scale_log2);
+                                                               a.pages_per_split, scale_log2, a.len_add);
   k_bf16_seg<GQ><<<dim3(lv.hkv, a.B), 128, 0, st>>>(lv, ws, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens,
-                                                    a.bf16_pt, scale_log2, a.nsplit);
+                                                    a.bf16_pt, scale_log2, a.nsplit, a.len_add);
   k_merge<GQ><<<dim3(lv.hkv, a.B), 128, kMergeSmem, st>>>(lv, ws, a.nsplit, a.out, a.out_dtype, a.lse);
   if (a.ev1) cudaEventRecord(a.ev1, st);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;

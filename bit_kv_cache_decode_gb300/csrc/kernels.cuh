@@ -6,10 +6,14 @@
 namespace oscar {
 
 constexpr int kDefaultDecodeAlgo = OSCAR_DECODE_MMA;
-constexpr int kMaxMmaSplits = 2048;        // bounds the fused merge's per-slot weight table in shared memory
+constexpr int kMaxMmaSplits = 2048;        // history splits of the fused decode
+constexpr int kMergeBucket = 8;            // history splits per first-level merge bucket
+constexpr int kCountersPerGroup = kMaxMmaSplits / kMergeBucket + 2;   // bucket tickets + BF16 bucket + group
+// partial slots per (request, q head): history splits, BF16 pages, history buckets, BF16 bucket
+inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf + (max_splits + kMergeBucket - 1) / kMergeBucket + 1; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
 constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
-constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;      // U + row + 4 partial rows + mbarrier
+constexpr int kAppendSmem = (kD * kD + kD + 4 * kD + 8 * kD) * 4 + 16;   // U + row + 4 partials + 8 queries + mbarrier
 constexpr int kQprepSmem = (kD * kD + 8 * kD) * 4 + 16;            // U_K + up to 8 query rows + mbarrier
 constexpr int kMergeSmem = 4 * kD * 4;                             // work rows of the merge
 
@@ -20,17 +24,20 @@ struct DecodeWorkspace {
   float* qconst;      // [max_batch][hq][kQConst] per-query-head constants, see kQ* below
   float* partials;    // [max_batch][hq][nslots][kPartFloats]: history splits, then BF16 chunks
   uint32_t* counters; // [max_batch][hkv] completion tickets of the fused decode (zero between calls)
+  unsigned long long* cta_trace;  // optional per-CTA timeline of the fused decode (see oscar_trace_ctas)
+  int trace_cap;      // records available in cta_trace
   int max_splits;     // history splits available
   int nslots;         // partial slots per (request, q head) = max_splits + BF16 chunks
 };
 
 // Per-query-head constants written by the query prologue.
-constexpr int kQConst = 8;
+constexpr int kQConst = 12;
 constexpr int kQSum0 = 0, kQSum1 = 1;    // sum of the rotated query over group 0 / 1
 constexpr int kQF = 2;                   // sm_scale * log2(e) * 2^-sigma (fragment scale undo)
 constexpr int kQZ0 = 3, kQZ1 = 4;        // sm_scale * log2(e) * group sums (zero-point terms)
-constexpr int kQOff0 = 5, kQOff1 = 6;    // 1024 * sum of the group's fp16 fragment values
-constexpr int kQSigma = 7;               // sigma, the power-of-two scale of the fragments
+constexpr int kQOff0H = 5, kQOff0L = 6;  // 1024 * sum of group 0's fragment values, high and low parts
+constexpr int kQOff1H = 7, kQOff1L = 8;  // same for group 1
+constexpr int kQSigma = 9;               // sigma, the power-of-two scale of the fragments
 
 // B fragments of one kv head's query group for the tensor-core decode:
 // 8 k-blocks x 2 n-tiles x 32 lanes x 2 registers.
@@ -60,10 +67,15 @@ struct DecodeArgs {
   int nbf;               // BF16 (sink + recent) chunks of 64 tokens per (request, kv head)
   int pages_per_split;
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
+  int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
+  int skip_qprep;        // the query prologue already ran (fused into the append)
   cudaEvent_t ev0, ev1;  // optional events around the history kernel (may be null)
 };
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
+int launch_append_qprep(const LayerView& lv, const DecodeWorkspace& ws, int B, const void* q, const void* k,
+                        const void* v, const int* seq_lens_before, const int* hist_pt, int max_hist_pages,
+                        const int* bf16_pt, float sm_scale, cudaStream_t st);
 int configure_decode_kernels();
 
 int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,

@@ -1,0 +1,136 @@
+// Query prologue of the decode (sm_103a): q~ = q R_K for the query heads of
+// one (request, kv head) group, and everything the history kernels read
+// about it (MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何
+// 不同做法": R_K = U_Q H_Had P_br; the read path's inverse rotation of the
+// keys is applied once to the query instead, R_K being orthogonal).
+//
+// Outputs, per query head:
+//  * ws.qrot  : q~ in rotated channel order (float32), for the CUDA-core kernel;
+//  * ws.qconst: group sums of q~, F = sm_scale log2(e) 2^-sigma, the scaled group
+//               sums (zero-point terms), the fragment offsets and sigma;
+//  * ws.qfrag : fp16 B fragments of the tensor-core logits. The tensor-core
+//               kernel feeds code c of channel ch as 1024 + c W(ch), the code
+//               sitting in mantissa bits 6-7 (W = 64, ch even) or 8-9 (W = 256,
+//               ch odd). With x(ch) = q~[ch] 2^sigma / W(ch) split into two fp16
+//               parts hi = fp16(x), lo = fp16(x - hi), the fragments carry hi
+//               and lo in separate columns and off_{g,part} = 1024 * sum_{ch in g}
+//               part(ch); then summing both columns,
+//               sum_{ch in g} (1024 + c W(ch)) (hi + lo)(ch) - off_g = 2^sigma sum c q~
+//               to about 22 bits. Keeping the codes in the top mantissa bits keeps
+//               the constant 1024 within 16/c of the code term.
+//               k-block kb = 4 G + j (G the channel group) at lane (g', t') holds
+//               k rows (2t', 2t'+1) -> channels (c0, c0 + 8) and (2t'+8, 2t'+9) ->
+//               channels (c0 + 1, c0 + 9), c0 = 16 (t' + 4 G) + 2 j; column g' is
+//               (head 4 nt + g'/2, part g'%2). sigma puts max|q~| near 2^12.
+#pragma once
+
+#include "kernels.cuh"
+#include "rotate.cuh"
+
+namespace oscar {
+
+// fp16 rounding of a fragment value, subnormal results flushed to zero so that
+// nothing depends on how the tensor cores treat fp16 subnormal inputs.
+__device__ __forceinline__ float frag_round(float x) {
+  const float r = __half2float(__float2half_rn(x));
+  return fabsf(r) < 6.103515625e-05f ? 0.f : r;
+}
+
+// Rotate the raw query rows xs[qi][0..127] (float, shared) of group (b, h)
+// with U (shared, row-major [128][128]): warp w handles query heads w, w +
+// nwarps, .... Each row is replaced by its rotation in rotated channel order;
+// q~ and its group sums go to the workspace and sigma of head qi to sig[qi].
+__device__ __forceinline__ void qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const float* Us,
+                                             float* xs, int* sig, int b, int h, int nwarps) {
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lv.hq / lv.hkv;
+  for (int qi = wib; qi < gq; qi += nwarps) {
+    float y[1][4];
+    warp_rotate<1>(Us, xs + qi * kD, y);
+    __syncwarp();                                   // row qi fully read before it is overwritten
+    const int hq = h * gq + qi;
+    float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
+    float s = 0.f, mx = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int ch = rot_channel(lane, r);
+      dst[ch] = y[0][r];
+      xs[qi * kD + ch] = y[0][r];
+      s += y[0][r];
+      mx = fmaxf(mx, fabsf(y[0][r]));
+    }
+#pragma unroll
+    for (int m = 2; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);   // lanes of equal parity = one group
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    if (lane < 2) ws.qconst[((size_t)b * lv.hq + hq) * kQConst + kQSum0 + lane] = s;
+    if (lane == 0) {
+      int e = 0;
+      if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx in [2^(e-1), 2^e)
+      sig[qi] = min(max(12 - e, -60), 60);
+    }
+  }
+}
+
+// After qprep_rotate and a block barrier: per-head constants (warp w handles
+// heads w, w + nwarps, ...; lane l owns channels 4l .. 4l + 3) and the
+// fragments (all threads of the block).
+__device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWorkspace& ws, const float* xs,
+                                             const int* sig, int b, int h, float scale_log2, int nwarps) {
+  const int tid = threadIdx.x, wib = tid >> 5, lane = tid & 31;
+  const int gq = lv.hq / lv.hkv;
+  for (int qi = wib; qi < gq; qi += nwarps) {
+    const float sc = ldexpf(1.f, sig[qi]);
+    float offh = 0.f, offl = 0.f, sum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e, fragment scale 1 / W = 2^-(6 + 2 (e & 1))
+      const float v = xs[qi * kD + 4 * lane + e];
+      const float x = v * sc * ldexpf(1.f, -6 - 2 * (e & 1));
+      const float hi = frag_round(x);
+      offh += hi;
+      offl += frag_round(x - hi);
+      sum += v;
+    }
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {              // lanes 0..15 hold group 0, 16..31 group 1
+      offh += __shfl_xor_sync(0xffffffffu, offh, m);
+      offl += __shfl_xor_sync(0xffffffffu, offl, m);
+      sum += __shfl_xor_sync(0xffffffffu, sum, m);
+    }
+    float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + qi) * kQConst;
+    if (lane == 0 || lane == 16) {
+      const int g = lane >> 4;
+      qc[g ? kQZ1 : kQZ0] = scale_log2 * sum;
+      qc[g ? kQOff1H : kQOff0H] = 1024.f * offh;
+      qc[g ? kQOff1L : kQOff0L] = 1024.f * offl;
+    }
+    if (lane == 0) {
+      qc[kQF] = scale_log2 * ldexpf(1.f, -sig[qi]);
+      qc[kQSigma] = (float)sig[qi];
+    }
+  }
+  const int nt_count = (gq + 3) / 4;
+  uint32_t* frag = ws.qfrag + ((size_t)b * lv.hkv + h) * kFragWords;
+  for (int wi = tid; wi < 8 * 2 * 64; wi += nwarps * 32) {
+    const int r = wi & 1, lp = (wi >> 1) & 31, nt = (wi >> 6) & 1, kb = wi >> 7;
+    const int gp = lp >> 2, tp = lp & 3;
+    const int head = 4 * nt + (gp >> 1), part = gp & 1;
+    uint32_t word = 0;
+    if (nt < nt_count && head < gq) {
+      // r = 0: channels (c0, c0 + 8), even, W = 64; r = 1: (c0 + 1, c0 + 9), odd, W = 256
+      const float sc = ldexpf(1.f, sig[head] - 6 - 2 * r);
+      const int c0 = 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;
+      float x[2] = {xs[head * kD + c0] * sc, xs[head * kD + c0 + 8] * sc};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float hi = frag_round(x[e]);
+        x[e] = part ? frag_round(x[e] - hi) : hi;
+      }
+      const __half2 v = __floats2half2_rn(x[0], x[1]);
+      word = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    frag[((kb * 2 + nt) * 32 + lp) * 2 + r] = word;
+  }
+}
+
+}  // namespace oscar

@@ -43,6 +43,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned sm_id() {
+  unsigned s;
+  asm volatile("mov.u32 %0, %smid;" : "=r"(s));
+  return s;
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start its
 // prologue now / wait until the kernels this one depends on have completed and
 // their writes are visible. Both are no-ops for a normally launched kernel.

@@ -194,6 +194,17 @@ int oscar_decode_attention(oscar_cache* cache, int layer, int B, const void* q, 
                            const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt,
                            float sm_scale, void* out, int out_dtype, float* lse, void* stream);
 
+/* One decode step of a layer: oscar_append_kv(k, v at position
+ * seq_lens_before[r]) followed by oscar_decode_attention(q) over
+ * seq_lens_before[r] + 1 tokens, with the same arguments, layouts and
+ * results as those two calls. With the tensor-core decode the append kernel
+ * also rotates the queries (it already holds U_K for the demotion), so the
+ * step is two launches: append + query prologue, then the decode kernel,
+ * which starts early and prefetches history pages while the append runs. */
+int oscar_decode_step(oscar_cache* cache, int layer, int B, const void* q, const void* k, const void* v,
+                      const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
+                      const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream);
+
 /* Choose the INT2 decode kernel (OSCAR_DECODE_MMA by default). */
 int oscar_set_decode_algo(oscar_cache* cache, int algo);
 
@@ -289,13 +300,23 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
  * without ordering) race and give wrong results; calls ordered on one stream
  * are safe. The history is split into fewer pieces when needed to fit. A call
  * whose per-query state does not fit even with one history split, i.e. when
- * B * Hq * (544 + 528 * (1 + (sink + recent) / 64)) + B * Hkv * 4100 bytes plus
- * about 1.5 KB of rounding exceed 4 MiB, returns OSCAR_ERR_TOO_LARGE before any
- * device work. */
+ * B * Hq * (544 + 528 * (3 + (sink + recent) / 64)) + B * Hkv * 5128 bytes plus
+ * about 1.5 KB of rounding exceed 4 MiB (B * Hq above about 850 with the
+ * default windows), returns OSCAR_ERR_TOO_LARGE before any device work. */
 int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B, const void* q,
                                    const int32_t* seq_lens, const int32_t* hist_pt, int max_hist_pages,
                                    const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse,
                                    int* status, void* stream);
+
+/* Record a timeline of the CTAs of every following tensor-core decode launch
+ * (each launch overwrites it): for CTA i (linear block index) the eight
+ * uint64 values at buf[8 i] are its id, SM id, start time, time its first
+ * history page landed, time its last warp finished the main loop, time its
+ * partials were written, time it finished the merge (last CTA of a request /
+ * kv-head group only, else 0) and 0; times are %globaltimer nanoseconds.
+ * buf: device memory for `capacity` records (64 bytes each); NULL stops
+ * recording. CTAs beyond `capacity` are not recorded. */
+int oscar_trace_ctas(oscar_cache* cache, void* buf, int capacity);
 
 /* Human-readable name of a status code. */
 const char* oscar_error_string(int code);

@@ -12,6 +12,7 @@ Workloads (synthetic, seeded; Qwen3-shaped random data, no model weights):
                 102,400-token context (64 sink + 102,080 history + 256 recent)
   qwen3_4b_b32  36 layers, batch 32 x 102,400 tokens sharing a 92,160-token prefix
   qwen3_8b_l1   1 layer, batch 1, 32,768 tokens
+  qwen3_8b_100k_l1  1 layer of qwen3_8b_36l (the same decode launch), for profiler captures
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
@@ -43,6 +44,7 @@ WORKLOADS = {
     "qwen3_8b_36l": dict(layers=36, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
     "qwen3_4b_b32": dict(layers=36, hq=32, hkv=8, batch=32, ctx=102400, shared=92160),
     "qwen3_8b_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=32768, shared=0),
+    "qwen3_8b_100k_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
 }
 
 
@@ -232,15 +234,15 @@ def run_ours(args, rank: int, world: int, device):
     out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
     seq = torch.full((B,), wl["L"], dtype=torch.int32, device=device)
     seq1 = seq + 1
-    # append, query rotation, then either one fused decode launch (mma) or history + BF16 segment + merge (simt)
-    launches_per_layer = 3 if args.algo == 1 else 5
+    # per layer, oscar_decode_step: the append kernel (which also rotates the queries on the tensor-core path)
+    # then one fused decode launch (mma), or append + query rotation + history + BF16 segment + merge (simt)
+    launches_per_layer = 2 if args.algo == 1 else 5
 
     def layers():
         for layer in range(nl):
-            cache.append_kv(layer, kv_cur[layer, 0], kv_cur[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
-            cache.decode_attention(layer, q_cur[layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out[layer])
+            cache.decode_step(layer, q_cur[layer], kv_cur[layer, 0], kv_cur[layer, 1], seq, wl["hist_pt"],
+                              wl["bf16_pt"], sm, out=out[layer])
         seq.add_(1)
-        seq1.add_(1)
 
     # capture one step (all layers) into a CUDA graph
     torch.cuda.synchronize()
@@ -271,11 +273,13 @@ def run_ours(args, rank: int, world: int, device):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         torch.cuda.synchronize()
+        nvtx_id = torch.cuda.nvtx.range_start("timed_steps")     # profiler filter for the launch list
         ev0.record(stream)
         for i in range(args.warmup, total_steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_end(nvtx_id)
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world, device)
     if cache.get_status() != 0:
@@ -288,7 +292,7 @@ def run_ours(args, rank: int, world: int, device):
     peak, peak_src = peaks()
     # dominant kernel: the decode call (query prologue + fused decode, PDL-chained), timed per call with the
     # library's CUDA events in a second timed region that issues the same steps without the graph
-    dec_ms, dec_n, L_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, seq1, out)
+    dec_ms, dec_n, L_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
     hb = history_bytes(L_prof, B, H) + B * min(L_prof, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
     dec_avg_ms = dec_ms / max(dec_n, 1)
     achieved = hb / (dec_avg_ms / 1e3) / 1e9
@@ -301,13 +305,13 @@ def run_ours(args, rank: int, world: int, device):
                    "storage": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
                    "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
-                   "launch": "one CUDA graph per step (36 layers x (append + decode)), new tokens copied in"},
+                   "launch": "one CUDA graph per step (oscar_decode_step per layer), new tokens copied in"},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
                 "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak},
         "roofline": {"bound": "hbm", "kernel": "decode call: query prologue + " +
                      ("fused INT2/BF16/merge kernel" if args.algo == 1 else "history + BF16 + merge kernels"),
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_launch": hb,
+                     "frac": achieved / peak, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
                      "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
         "gpu_launches": (launches_per_layer * nl + 2) * args.steps,
         "clocks": clk.summary(),
@@ -322,23 +326,50 @@ def run_ours(args, rank: int, world: int, device):
     return res
 
 
-def profile_decode_calls(wl, args, kv_new, q_all, seq, seq1, out):
-    """Eager steps with the library tracing every decode call: returns (summed ms, calls, mean context)."""
+def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
+    """Eager steps with the library's CUDA events around every oscar_decode_step (append + query rotation
+    kernel, PDL-chained into the fused decode kernel): returns (summed ms, calls, mean context)."""
     import torch
     import synth
     cache, nl = wl["cache"], wl["layers"]
     sm = synth.sm_scale()
     torch.cuda.synchronize()
-    L0 = int(seq1[0].item())
+    L0 = int(seq[0].item()) + 1
     cache.profile_begin(nl * args.steps)
     for i in range(args.steps):
         for layer in range(nl):
-            cache.append_kv(layer, kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
-            cache.decode_attention(layer, q_all[i, layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=out[layer])
+            cache.decode_step(layer, q_all[i, layer], kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"],
+                              wl["bf16_pt"], sm, out=out[layer])
         seq.add_(1)
-        seq1.add_(1)
     ms, n = cache.profile_read()
     return ms, n, L0 + (args.steps - 1) // 2
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
+# 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
+# CUDA sources it was taken on: a changed kernel reports null until it is captured again.
+NCU_DECODE_TRAFFIC = {"sources_sha256": "c6d03a48fe3934c6cc04e76312498fb2a866b0e1cf72db0119adfc3c64d0ff8e",
+                      "bytes_per_launch": 66883328 + 517888}
+
+
+def sources_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_kv_cache_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".cpp", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "oscar.h"), "rb").read())
+    return h.hexdigest()
+
+
+def decode_traffic(args):
+    if args.algo != 1 or args.workload not in ("qwen3_8b_36l", "qwen3_8b_100k_l1"):
+        return None
+    if NCU_DECODE_TRAFFIC["sources_sha256"] != sources_digest():
+        return None
+    return NCU_DECODE_TRAFFIC["bytes_per_launch"]
 
 
 def run_bf16(wl, args, q_all, device):

@@ -35,6 +35,7 @@ EXPORTS = (
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
     "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
+    "oscar_trace_timeline",
 )
 
 
@@ -76,6 +77,7 @@ def _load() -> ctypes.CDLL:
         "oscar_profile_begin": [vp, c_int],
         "oscar_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)],
         "oscar_trace_ctas": [vp, vp, c_int],
+        "oscar_trace_timeline": [vp, vp, c_int],
         "oscar_decode_step": [vp, c_int, c_int, vp, vp, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
         "oscar_decode_attention_noalloc": [ctypes.POINTER(Layout), vp, c_int, c_int, vp, i32p, i32p, c_int, i32p,
                                            c_float, vp, c_int, vp, vp, vp],
@@ -285,6 +287,12 @@ class OscarCache:
         tensor of 8 * n elements, n records); None stops recording."""
         n = 0 if buf is None else buf.numel() // 8
         _check(_lib.oscar_trace_ctas(self._h, _ptr(buf), n), "oscar_trace_ctas")
+
+    def trace_timeline(self, buf=None):
+        """Record a timeline of every CTA of the following kernel launches into ``buf`` (an int64 device tensor
+        of 4 + 4 * n elements, n records, buf[0] zeroed by the caller); None stops recording."""
+        n = 0 if buf is None else (buf.numel() - 4) // 4
+        _check(_lib.oscar_trace_timeline(self._h, _ptr(buf), n), "oscar_trace_timeline")
 
     def profile_begin(self, capacity: int):
         _check(_lib.oscar_profile_begin(self._h, capacity), "oscar_profile_begin")

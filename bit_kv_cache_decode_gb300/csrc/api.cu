@@ -21,6 +21,8 @@ struct oscar_cache {
   int* status;
   int sms;
   int algo;
+  unsigned long long* timeline;   // kernel timeline buffer (oscar_trace_timeline) or null
+  int timeline_cap;
   // tracing
   bool prof_on;
   int prof_cap, prof_n;
@@ -61,8 +63,7 @@ void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, si
          + align_up(B * hq * kD * sizeof(float))                   // qrot
          + align_up(B * hkv * kFragWords * sizeof(uint32_t))       // qfrag
          + align_up(B * hq * kQConst * sizeof(float))              // qconst
-         + align_up(B * hq * partial_slots(L->max_splits, (L->sink + L->recent) / kP) * kPartFloats * sizeof(float))
-         + align_up(B * hkv * kCountersPerGroup * sizeof(uint32_t));   // completion tickets
+         + align_up(B * hq * partial_slots(L->max_splits, (L->sink + L->recent) / kP) * kPartFloats * sizeof(float));
 }
 
 LayerView view(const oscar_cache* c, int layer) {
@@ -79,6 +80,9 @@ LayerView view(const oscar_cache* c, int layer) {
   v.recent = c->lay.recent;
   v.v_explicit = c->lay.v_mode == OSCAR_V_EXPLICIT;
   v.status = c->status;
+  v.layer = layer;
+  v.timeline = c->timeline;
+  v.timeline_cap = c->timeline_cap;
   return v;
 }
 
@@ -186,13 +190,13 @@ int oscar_cache_create(const oscar_layout* layout, void* pool, void* workspace, 
   c->dws.trace_cap = 0;
   c->dws.nslots = partial_slots(layout->max_splits, (layout->sink + layout->recent) / kP);
   p += align_up(B * hq * c->dws.nslots * kPartFloats * sizeof(float));
-  c->dws.counters = reinterpret_cast<uint32_t*>(p);
   c->sms = sms;
   c->algo = kDefaultDecodeAlgo;
+  c->timeline = nullptr;
+  c->timeline_cap = 0;
   c->prof_on = false;
   c->prof_cap = c->prof_n = 0;
-  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess ||
-      cudaMemset(c->dws.counters, 0, B * hkv * kCountersPerGroup * sizeof(uint32_t)) != cudaSuccess) {
+  if (cudaMemset(c->status, 0, sizeof(int)) != cudaSuccess) {
     delete c;
     return OSCAR_ERR_CUDA;
   }
@@ -307,7 +311,6 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.lse = lse;
   a.algo = c->algo;
   a.len_add = 0;
-  a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
     int cps, align, extra;
@@ -363,12 +366,10 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
     a.ev1 = c->prof_ev[2 * c->prof_n + 1];
     c->prof_n++;
   }
-  // tensor-core path: the append kernel also runs the query prologue
-  a.skip_qprep = a.algo == OSCAR_DECODE_MMA;
+  // append, then the decode chain (query prologue, decode, merge), each a
+  // programmatic dependent of the kernel before it
   if (a.ev0) cudaEventRecord(a.ev0, st);
-  int rc = a.skip_qprep ? launch_append_qprep(lv, c->dws, B, q, k, v, seq_lens_before, hist_pt, max_hist_pages,
-                                              bf16_pt, sm_scale, st)
-                        : launch_append(lv, B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt, st);
+  const int rc = launch_append(lv, B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt, st);
   if (rc != OSCAR_OK) return rc;
   a.ev0 = nullptr;                       // recorded above: the profiled span starts at the append
   return launch_decode(lv, c->dws, a, st);
@@ -444,6 +445,14 @@ int oscar_trace_ctas(oscar_cache* c, void* buf, int capacity) {
   return OSCAR_OK;
 }
 
+int oscar_trace_timeline(oscar_cache* c, void* buf, int capacity) {
+  if (!c || capacity < 0 || (buf != nullptr && capacity == 0)) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(buf) % 8) return OSCAR_ERR_INVALID_ARG;
+  c->timeline = static_cast<unsigned long long*>(buf);
+  c->timeline_cap = buf ? capacity : 0;
+  return OSCAR_OK;
+}
+
 int oscar_profile_begin(oscar_cache* c, int capacity) {
   if (!c || capacity < 1) return OSCAR_ERR_INVALID_ARG;
   while ((int)c->prof_ev.size() < 2 * capacity) {
@@ -496,6 +505,9 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
   out->recent = L->recent;
   out->v_explicit = L->v_mode == OSCAR_V_EXPLICIT;
   out->status = status;
+  out->layer = layer;
+  out->timeline = nullptr;
+  out->timeline_cap = 0;
   return OSCAR_OK;
 }
 

@@ -44,6 +44,9 @@ struct LayerView {
   const float* params;    // [hkv][kParamFloats]
   int n_int2, n_bf16, hkv, hq, sink, recent, v_explicit;
   int* status;            // device status word
+  int layer;              // layer index (timeline records only)
+  unsigned long long* timeline;   // optional kernel timeline (see oscar_trace_timeline), or null
+  int timeline_cap;       // records available in timeline
 };
 
 __device__ __forceinline__ void flag(int* status, int bits) { atomicOr(status, bits); }

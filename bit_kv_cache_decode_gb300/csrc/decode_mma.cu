@@ -28,21 +28,19 @@
 // and writes one partial (m, l, acc[128]) per query head and split.
 //
 // The same launch carries the BF16 sink + recent tokens as one extra CTA per
-// BF16 page (bulk-copied, CUDA-core dot products) and the log-sum-exp merge: every CTA
-// of a (request, kv head) group takes a ticket after writing its partials, and
-// the last one merges the group's partials (applying R_V^T to the history part
-// in explicit-V mode) and writes the attention output. The ticket counter is
-// reset by that CTA, so it is zero again between launches.
+// BF16 page (bulk-copied, CUDA-core dot products). The log-sum-exp merge of
+// all slots runs as the next kernel (merge.cu), a programmatic dependent that
+// is scheduled while this grid runs and waits for its completion.
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
+#include "timeline.cuh"
 
 namespace oscar {
 
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kBucket = kMergeBucket;          // history splits merged together at the first level
 constexpr int kStages = 2;
 constexpr uint32_t kMagic = 0x64006400u;       // fp16 1024.0 in both halves
 // stage ring, mbarriers, a timeout flag, and slack to align the ring to 128 bytes
@@ -64,6 +62,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = a * b + c with a separate accumulator input c
+__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(x));
@@ -80,15 +88,6 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
   uint32_t d;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
   return d;
-}
-
-// exact fp16 codes: ((1024 + c*4^k) * 4^-k) - 1024*4^-k = c, for both halves
-__device__ __forceinline__ uint32_t exact_codes(uint32_t biased, int k) {
-  const uint32_t scale = 0x3C003C00u - (uint32_t)(k * 0x08000800u);   // 4^-k = 2^-2k: exponent - 2k
-  const uint32_t offs = 0xE400E400u - (uint32_t)(k * 0x08000800u);    // -1024 * 4^-k
-  __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&biased), *reinterpret_cast<const __half2*>(&scale),
-                      *reinterpret_cast<const __half2*>(&offs));
-  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 struct FusedArgs {
@@ -148,30 +147,34 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   }
   __syncwarp();
 
-  // issue the load of the warp's i-th page into stage i % kStages; returns whether it was issued
-  auto issue = [&](int i) -> bool {
-    const int page = p0 + kWarps * i;
-    const int pid = pt[page];
+  // issue the load of the warp's i-th page (id pid) into stage i % kStages; returns whether it was issued
+  auto issue = [&](int i, int pid) -> bool {
     if (pid < 0 || pid >= lv.n_int2) {
       if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE);
       return false;
     }
     if (lane == 0) {
       const int s = i % kStages;
-      bulk_load(stage_s + s * kBlockBytes, int2_block(lv, pid, h), kBlockBytes, bar_s + 8 * s);
+      bulk_load_hint(stage_s + s * kBlockBytes, int2_block(lv, pid, h), kBlockBytes, bar_s + 8 * s, l2_evict_first());
     }
     return true;
   };
   uint32_t issued = 0;                 // bit s: a load is outstanding in stage s
-  // Before the programmatic wait only pages the preceding append cannot touch are
-  // fetched: it writes one row of the last history page (the demoted token).
-#pragma unroll
-  for (int i = 0; i < kStages; ++i)
-    if (i < my_pages && p0 + kWarps * i < npages - 1 && issue(i)) issued |= 1u << i;
+  // Only the first page of each warp is requested up front: with every warp of
+  // the grid asking for one page the first burst lands early, and the later
+  // stages are requested once it has (below). Before the programmatic wait only
+  // pages the preceding append cannot touch are fetched: it writes one row of
+  // the last history page (the demoted token).
+  // Page ids are read from the page table a stage ahead of their use.
+  const int pid0 = my_pages > 0 ? pt[p0] : 0;
+  const int pid1 = my_pages > 1 ? pt[p0 + kWarps] : 0;
+  if (my_pages > 0 && p0 < npages - 1 && issue(0, pid0)) issued |= 1u;
   pdl_wait();
-#pragma unroll
-  for (int i = 0; i < kStages; ++i)
-    if (i < my_pages && p0 + kWarps * i >= npages - 1 && issue(i)) issued |= 1u << i;
+  if (my_pages > 0 && p0 >= npages - 1 && issue(0, pid0)) issued |= 1u;
+  static_assert(kStages == 2, "the prologue requests pages 0 and 1");
+  auto issue_rest = [&]() {            // page 1, once page 0 is in (or was never requested)
+    if (1 < my_pages && issue(1, pid1)) issued |= 2u;
+  };
 
   // ---- per-lane constants -------------------------------------------------------
   uint32_t qf[8][NT][2];
@@ -186,21 +189,28 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         qf[kb][nt][1] = v.y;
       }
   }
-  float cF[NT], cZ0[NT], cZ1[NT], cO0h[NT], cO0l[NT], cO1h[NT], cO1l[NT];
+  // cOff[G][nt]: the logits accumulators' start, minus the fragment offsets of
+  // group G in the accumulator layout (columns 2t, 2t+1 = high, low part)
+  float cF[NT], cZ0[NT], cZ1[NT], cOff[2][NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = 4 * nt + t;
-    cF[nt] = cZ0[nt] = cZ1[nt] = cO0h[nt] = cO0l[nt] = cO1h[nt] = cO1l[nt] = 0.f;
+    float o0h = 0.f, o0l = 0.f, o1h = 0.f, o1l = 0.f;
+    cF[nt] = cZ0[nt] = cZ1[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
       cF[nt] = qc[kQF];
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
-      cO0h[nt] = qc[kQOff0H];
-      cO0l[nt] = qc[kQOff0L];
-      cO1h[nt] = qc[kQOff1H];
-      cO1l[nt] = qc[kQOff1L];
+      o0h = qc[kQOff0H];
+      o0l = qc[kQOff0L];
+      o1h = qc[kQOff1H];
+      o1l = qc[kQOff1L];
     }
+    cOff[0][nt][0] = cOff[0][nt][2] = -o0h;
+    cOff[0][nt][1] = cOff[0][nt][3] = -o0l;
+    cOff[1][nt][0] = cOff[1][nt][2] = -o1h;
+    cOff[1][nt][1] = cOff[1][nt][3] = -o1l;
   }
 
   // ---- running state ----------------------------------------------------------------
@@ -211,18 +221,20 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
-  float mrun[NT], lsum[NT], zacc[NT][2];
+  float mrun[NT], lsum[NT], zacc[NT][2], bacc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     mrun[nt] = -INFINITY;
     lsum[nt] = 0.f;
     zacc[nt][0] = zacc[nt][1] = 0.f;
+    bacc[nt][0] = bacc[nt][1] = bacc[nt][2] = bacc[nt][3] = 0.f;
   }
   uint32_t phase = 0;
   bool timed_out = false;
 
   for (int i = 0; i < my_pages; ++i) {
     const int s = i % kStages;
+    const int pid_ahead = (i + kStages < my_pages) ? pt[p0 + kWarps * (i + kStages)] : 0;   // used after this page
     if (issued & (1u << s)) {
       const bool landed = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * s, (phase >> s) & 1u));
       if (trace != nullptr && i == 0 && tid == 0) trace[3] = global_ns();      // first page of warp 0 landed
@@ -232,6 +244,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       }
       phase ^= 1u << s;
       issued &= ~(1u << s);
+      if (i == 0) issue_rest();
       const uint8_t* blk = stage0 + s * kBlockBytes;
       const int ntok = min(kP, Lh - (p0 + kWarps * i) * kP);
 
@@ -245,14 +258,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
                                 *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r0 * 32 + 16 + 4 * t)};
         const uint32_t ky[2] = {*reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r1 * 32 + 4 * t),
                                 *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r1 * 32 + 16 + 4 * t)};
-        float c[2][NT][4];                         // per group; start from -offset: the MMAs add the biased sums
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          c[0][nt][0] = c[0][nt][2] = -cO0h[nt];
-          c[0][nt][1] = c[0][nt][3] = -cO0l[nt];
-          c[1][nt][0] = c[1][nt][2] = -cO1h[nt];
-          c[1][nt][1] = c[1][nt][3] = -cO1l[nt];
-        }
+        float c[2][NT][4];                         // per group; starts from -offset: the MMAs add the biased sums
 #pragma unroll
         for (int G = 0; G < 2; ++G) {
           // code i (bits 2i of each 16-bit half) is moved into bits 6-7 (i even) or 8-9 (i odd):
@@ -266,8 +272,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             const uint32_t a2 = and_or(wx[j], 0x03000300u, kMagic);   // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
             const uint32_t a3 = and_or(wy[j], 0x03000300u, kMagic);   // row r1
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+            for (int nt = 0; nt < NT; ++nt) {
+              if (j == 0) mma16816_c(c[G][nt], a0, a1, a2, a3, qf[4 * G][nt][0], qf[4 * G][nt][1], cOff[G][nt]);
+              else mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+            }
           }
         }
         const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r0 * 8);
@@ -314,6 +322,8 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           zacc[nt][0] *= al;
           zacc[nt][1] *= al;
 #pragma unroll
+          for (int e = 0; e < 4; ++e) bacc[nt][e] *= al;
+#pragma unroll
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= al;
@@ -348,23 +358,35 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         }
         const uint2 wab = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t) * 64 + 8 * g);
         const uint2 wcd = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t + 4) * 64 + 8 * g);
-        const uint32_t wah = wab.x >> 8, wbh = wab.y >> 8, wch = wcd.x >> 8, wdh = wcd.y >> 8;
+        // code mt of each 16-bit half (bits 2 mt) moved into bits 6-7 (mt even) or 8-9 (mt odd), fed as the
+        // fp16 value 1024 + c * W_mt (W = 64 or 256): shift left 6, left 2, right 2, right 6 for mt / 2 = 0..3
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int k = mt & 3;
-          const uint32_t m = 0x00030003u << (2 * k);
-          const uint32_t a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
-          const uint32_t a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
-          const uint32_t a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
-          const uint32_t a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
+        for (int i = 0; i < 4; ++i) {
+          const int sh = 6 - 4 * i;
+          const uint32_t xa = sh > 0 ? wab.x << sh : wab.x >> -sh, xb = sh > 0 ? wab.y << sh : wab.y >> -sh;
+          const uint32_t xc = sh > 0 ? wcd.x << sh : wcd.x >> -sh, xd = sh > 0 ? wcd.y << sh : wcd.y >> -sh;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
+          for (int odd = 0; odd < 2; ++odd) {
+            const int mt = 2 * i + odd;
+            const uint32_t m = odd ? 0x03000300u : 0x00C000C0u;
+            const uint32_t a0 = and_or(xa, m, kMagic);   // channel 16g + mt, tokens 2t, 2t+1
+            const uint32_t a1 = and_or(xb, m, kMagic);   // channel 16g + 8 + mt
+            const uint32_t a2 = and_or(xc, m, kMagic);   // tokens 2t + 8, 2t + 9
+            const uint32_t a3 = and_or(xd, m, kMagic);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
+          }
         }
+        // 1024 * (column sums of B), the constant part of every biased code, for the epilogue
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[nt], kMagic, kMagic, kMagic, kMagic, bf[nt][0], bf[nt][1]);
       }
+    } else if (i == 0) {
+      issue_rest();                    // page 0 was not requested (bad page id): the rest still is
     }
     __syncwarp();
     const int next = i + kStages;
-    if (next < my_pages && issue(next)) issued |= 1u << s;
+    if (next < my_pages && issue(next, pid_ahead)) issued |= 1u << s;
   }
 
   if (timed_out) {
@@ -399,11 +421,13 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       cl[w * 8 + head] = lsum[nt];
     }
     const float zs = grp ? zacc[nt][1] : zacc[nt][0];
+    const float bias0 = grp ? bacc[nt][1] : bacc[nt][0], bias1 = grp ? bacc[nt][3] : bacc[nt][2];
     float* dst = ca + (w * 8 + head) * kD;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      dst[16 * g + mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
-      dst[16 * g + 8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
+      const float inv_w = (mt & 1) ? 1.f / 256.f : 1.f / 64.f;      // codes were fed as 1024 + c * W
+      dst[16 * g + mt] = fmaf((grp ? acc[nt][mt][1] : acc[nt][mt][0]) - bias0, inv_w, zs);
+      dst[16 * g + 8 + mt] = fmaf((grp ? acc[nt][mt][3] : acc[nt][mt][2]) - bias1, inv_w, zs);
     }
   }
   __syncthreads();
@@ -530,120 +554,16 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
   }
 }
 
-// Online-softmax combine of slots [s0, s1) of one query head's partials, by
-// one warp: lane q handles channels 4q..4q+3. Every lane reads the slot
-// maxima itself (broadcast loads), so no shuffles are needed. Partials are read
-// with L1-bypassing loads: other CTAs of this launch wrote them. Returns the
-// combined (M, L, A) with L, A relative to 2^M; no live slot gives M = -inf.
-__device__ __forceinline__ void combine_slots(const float* row0, int s0, int s1, int lane, float& M, float& L,
-                                              float4& A) {
-  M = -INFINITY;
-#pragma unroll 8
-  for (int s = s0; s < s1; ++s) M = fmaxf(M, __ldcg(row0 + (size_t)s * kPartFloats));
-  L = 0.f;
-  A = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M == -INFINITY) return;
-#pragma unroll 8
-  for (int s = s0; s < s1; ++s) {
-    const float* r = row0 + (size_t)s * kPartFloats;
-    const float m = __ldcg(r);
-    const float l = __ldcg(r + 1);
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
-    const float wgt = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
-    L = fmaf(l, wgt, L);
-    A.x = fmaf(a.x, wgt, A.x); A.y = fmaf(a.y, wgt, A.y); A.z = fmaf(a.z, wgt, A.z); A.w = fmaf(a.w, wgt, A.w);
-  }
-}
-
-// First-level merge: slots [s0, s1) of every query head of group (b, h) into slot `dst`.
-__device__ __forceinline__ void merge_bucket(const LayerView& lv, const DecodeWorkspace& ws, int h, int b, int s0,
-                                             int s1, int dst) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lv.hq / lv.hkv;
-  for (int hh = w; hh < gq; hh += 4) {
-    const float* row0 = part_row(ws, b, lv.hq, h * gq + hh, 0);
-    float M, L;
-    float4 A;
-    combine_slots(row0, s0, s1, lane, M, L, A);
-    float* d = part_row(ws, b, lv.hq, h * gq + hh, dst);
-    if (lane == 0) { d[0] = M; d[1] = L; }
-    reinterpret_cast<float4*>(d + 4)[lane] = A;
-  }
-}
-
-// Final merge of group (b, h): history buckets [hb0, hb0 + nb) and the BF16
-// bucket `bfs`; warp w handles query heads w, w+4, lane q channels 4q..4q+3.
-// In explicit-V mode the history part, which lives in the rotated value basis,
-// is multiplied by R_V^T = P_br H U_V^T before it meets the BF16 part.
-__device__ __forceinline__ void merge_final(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
-                                            uint8_t* smem, int h, int b, int hb0, int nb, int bfs) {
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int gq = lv.hq / lv.hkv;
-  const bool expl = lv.v_explicit != 0;
-  float* ybuf = reinterpret_cast<float*>(smem) + w * 2 * kD;       // [128] accumulator, then [128] after P_br H
-  for (int hh = w; hh < gq; hh += 4) {
-    const int hq = h * gq + hh;
-    const float* row0 = part_row(ws, b, lv.hq, hq, 0);
-    float M1, L1, M2, L2;
-    float4 A1, A2;
-    combine_slots(row0, hb0, hb0 + nb, lane, M1, L1, A1);
-    combine_slots(row0, bfs, bfs + 1, lane, M2, L2, A2);
-    if (expl && M1 != -INFINITY) {
-      *reinterpret_cast<float4*>(ybuf + 4 * lane) = A1;
-      __syncwarp();
-      float v[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) v[r] = ybuf[bitrev7(lane + 32 * r)];
-      fwht128(v);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) ybuf[kD + lane + 32 * r] = v[r];
-      __syncwarp();
-      const float4* uvt = reinterpret_cast<const float4*>(lv.params + (size_t)h * kParamFloats + kUVtOff);
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int i = 0; i < kD; ++i) {
-        const float z = ybuf[kD + i];
-        const float4 u = uvt[i * (kD / 4) + lane];       // U_V^T[i][4 lane .. 4 lane + 3]
-        o.x = fmaf(z, u.x, o.x); o.y = fmaf(z, u.y, o.y); o.z = fmaf(z, u.z, o.z); o.w = fmaf(z, u.w, o.w);
-      }
-      A1 = o;
-      __syncwarp();
-    }
-    const float M = fmaxf(M1, M2);
-    const float w1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - M);
-    const float w2 = (M2 == -INFINITY) ? 0.f : exp2f(M2 - M);
-    const float Ls = L1 * w1 + L2 * w2;
-    const float inv = 1.f / Ls;
-    float4 o;
-    o.x = (A1.x * w1 + A2.x * w2) * inv;
-    o.y = (A1.y * w1 + A2.y * w2) * inv;
-    o.z = (A1.z * w1 + A2.z * w2) * inv;
-    o.w = (A1.w * w1 + A2.w * w2) * inv;
-    const size_t oi = ((size_t)b * lv.hq + hq) * kD + 4 * lane;
-    if (fa.out_dtype == OSCAR_OUT_FP32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(fa.out) + oi) = o;
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(o.x, o.y), hi = __floats2bfloat162_rn(o.z, o.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(fa.out) + oi) = pk;
-    }
-    if (fa.lse != nullptr && lane == 0) fa.lse[(size_t)b * lv.hq + hq] = (M + log2f(Ls)) * 0.6931471805599453f;
-    __syncwarp();
-  }
-}
-
 // grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
 template <int NT>
 __global__ void __launch_bounds__(128, NT == 1 ? 4 : 2) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
+  TimelineSpan timeline_span(lv, kTlDecodeMma);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
-  __shared__ int is_last;
   const int h = blockIdx.y, b = blockIdx.z;
   // optional timeline record of this CTA (ns, %globaltimer):
   // [0] linear CTA id, [1] SM id, [2] start, [3] first history page landed (warp 0),
-  // [4] last warp's main loop done, [5] partials written, [6] merge done (group's last CTA only), [7] 0
+  // [4] last warp's main loop done, [5] partials written, [6], [7] 0
   const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   unsigned long long* trace =
       (ws.cta_trace != nullptr && (int)cta < ws.trace_cap) ? ws.cta_trace + 8ull * cta : nullptr;
@@ -656,37 +576,10 @@ __global__ void __launch_bounds__(128, NT == 1 ? 4 : 2) k_decode_mma(LayerView l
     }
     __syncthreads();
   }
+  pdl_launch_dependents();                         // the merge kernel may be scheduled now; it waits for this grid
   if (blockIdx.x < fa.nsplit) int2_split<NT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
   else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
   if (trace != nullptr && threadIdx.x == 0) trace[5] = global_ns();
-  // Two-level completion tickets. Slots: history splits [0, nsplit), BF16 pages
-  // [nsplit, nsplit + nbf), bucket partials from nsplit + nbf on (history buckets,
-  // then the BF16 bucket). Counters per group: one per bucket, then the group's.
-  const int nb = (fa.nsplit + kBucket - 1) / kBucket;
-  const int hb0 = fa.nsplit + fa.nbf;
-  const bool hist = (int)blockIdx.x < fa.nsplit;
-  const int j = hist ? (int)blockIdx.x / kBucket : nb;
-  const int members = hist ? min(kBucket, fa.nsplit - j * kBucket) : fa.nbf;
-  uint32_t* ctr = ws.counters + ((size_t)b * lv.hkv + h) * kCountersPerGroup;
-  __threadfence();                                 // this CTA's partials are visible before its ticket
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(&ctr[j], 1u) == (unsigned)members - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  if (hist) merge_bucket(lv, ws, h, b, j * kBucket, j * kBucket + members, hb0 + j);
-  else merge_bucket(lv, ws, h, b, fa.nsplit, fa.nsplit + fa.nbf, hb0 + nb);
-  if (threadIdx.x == 0) ctr[j] = 0u;
-  if (trace != nullptr && threadIdx.x == 0) { trace[6] = global_ns(); trace[7] = 1; }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(&ctr[nb + 1], 1u) == (unsigned)nb;   // nb history buckets + BF16
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  merge_final(lv, ws, fa, smem, h, b, hb0, nb, hb0 + nb);
-  if (threadIdx.x == 0) ctr[nb + 1] = 0u;
-  if (trace != nullptr && threadIdx.x == 0) { trace[6] = global_ns(); trace[7] = 2; }
 }
 
 }  // namespace
@@ -720,7 +613,8 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.numAttrs = 1;
   const cudaError_t e = (lv.hq / lv.hkv <= 4) ? cudaLaunchKernelEx(&cfg, k_decode_mma<1>, lv, ws, fa)
                                               : cudaLaunchKernelEx(&cfg, k_decode_mma<2>, lv, ws, fa);
-  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  return launch_merge(lv, ws, a.B, a.nsplit, a.nbf, a.out, a.out_dtype, a.lse, st);
 }
 
 int configure_mma_kernels() {

@@ -68,18 +68,17 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
                        up256((size_t)B * hkv * kFragWords * sizeof(uint32_t)) +
                        up256((size_t)B * hq * kQConst * sizeof(float));
   const size_t per_slot = (size_t)B * hq * kPartFloats * sizeof(float);
-  const size_t counters = up256((size_t)B * hkv * kCountersPerGroup * sizeof(uint32_t));
   const int nbf = (layout->sink + layout->recent) / kP;
-  // layout: fixed part | partials (rounded up to 256 B) | counters
-  if (fixed + 256 + counters + (size_t)partial_slots(1, nbf) * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
+  // layout: fixed part | partials
+  if (fixed + (size_t)partial_slots(1, nbf) * per_slot > kScratchBytes) return OSCAR_ERR_TOO_LARGE;
   rc = configure_kernels();
   if (rc != OSCAR_OK) return rc;
   uint8_t* scratch = nullptr;
   int sms = 0;
   rc = scratch_for_current_device(&scratch, &sms);
   if (rc != OSCAR_OK) return rc;
-  const int max_slots = (int)((kScratchBytes - fixed - 256 - counters) / per_slot);
-  // largest split count whose slots (splits, BF16 pages, buckets) fit
+  const int max_slots = (int)((kScratchBytes - fixed) / per_slot);
+  // largest split count whose slots (splits, then BF16 pages) fit
   int max_splits = 1;
   while (max_splits < kMaxMmaSplits && partial_slots(max_splits + 1, nbf) <= max_slots) ++max_splits;
   DecodeWorkspace ws;
@@ -109,19 +108,15 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.lse = lse;
   a.algo = kDefaultDecodeAlgo;
   a.len_add = 0;
-  a.skip_qprep = 0;
   a.ev0 = a.ev1 = nullptr;
   a.nbf = nbf;
   decode_split_policy(B, (int)hkv, (int)(hq / hkv), nbf, max_hist_pages, max_splits, sms, a.algo, &a.nsplit,
                       &a.pages_per_split);
   ws.max_splits = a.nsplit;
   ws.nslots = partial_slots(a.nsplit, nbf);
-  ws.counters = reinterpret_cast<uint32_t*>(p + up256((size_t)B * hq * ws.nslots * kPartFloats * sizeof(float)));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the status word must start at zero
   if (cudaMemsetAsync(dstatus, 0, sizeof(int), st) != cudaSuccess) return OSCAR_ERR_CUDA;
-  if (cudaMemsetAsync(ws.counters, 0, (size_t)B * hkv * kCountersPerGroup * sizeof(uint32_t), st) != cudaSuccess)
-    return OSCAR_ERR_CUDA;
   rc = launch_decode(lv, ws, a, st);
   if (rc != OSCAR_OK) return rc;
   if (status && cudaMemcpyAsync(status, dstatus, sizeof(int), cudaMemcpyDeviceToDevice, st) != cudaSuccess)

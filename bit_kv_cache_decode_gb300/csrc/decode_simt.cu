@@ -1,6 +1,7 @@
 // Decode attention over the mixed-precision pool, CUDA-core path, and the
 // pieces every decode path shares: the query prologue, the BF16 segment
-// kernel, the log-sum-exp merge and the all-BF16 comparison kernel (sm_103a).
+// kernel and the all-BF16 comparison kernel (sm_103a). The log-sum-exp merge
+// is in merge.cu.
 //
 // News article "超越 TurboQuant…OSCAR…", section "OSCAR 的设计思路": the INT2
 // kernel unpacks, restores scale/zero and accumulates in floating point; the
@@ -16,6 +17,7 @@
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
+#include "timeline.cuh"
 #include "qprep.cuh"
 
 namespace oscar {
@@ -69,38 +71,44 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256, U_K staged in
-// shared memory by one bulk copy; warp w rotates query head w. Launched as a
+// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256: U_K arrives in
+// 8 bulk copies of 16 rows and warp w sums the rows of copy w for every query
+// head of the group as soon as that copy lands. Launched as a
 // programmatic dependent of the append kernel: it lets the decode kernel start
 // at once and waits for the append only before it exits.
-__global__ void __launch_bounds__(256) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q, DecodeWorkspace ws,
-                                               float scale_log2) {
+__global__ void __launch_bounds__(kQprepWarps * 32) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q,
+                                                            DecodeWorkspace ws, float scale_log2) {
+  TimelineSpan timeline_span(lv, kTlQprep);
   extern __shared__ __align__(128) float smem[];
-  float* Us = smem;
-  float* xs = smem + kD * kD;  // [8][128]: raw query rows, then rotated rows in rotated channel order
-  const uint32_t bar = smem_addr(xs + 8 * kD);
+  float* Us = smem;                              // [128][128]
+  float* xs = Us + kD * kD;                      // [8][128]: raw query rows, then rotated rows
+  float* part = xs + 8 * kD;                     // [kQprepWarps][8][128] partial rotations
+  const uint32_t bars = smem_addr(part + kQprepWarps * 8 * kD);
   __shared__ int sig[8];
-  __shared__ int landed;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int gq = lv.hq / lv.hkv;
   pdl_launch_dependents();
   if (tid == 0) {
-    mbar_init(bar);
-    bulk_load(smem_addr(Us), lv.params + (size_t)h * kParamFloats + kUKOff, kD * kD * 4, bar);
+    // U_K in kQprepWarps chunks of 16 rows, one mbarrier each
+    const float* u = lv.params + (size_t)h * kParamFloats + kUKOff;
+    const uint64_t keep = l2_evict_last();
+    for (int c = 0; c < kQprepWarps; ++c) {
+      mbar_init(bars + 8 * c);
+      bulk_load_hint(smem_addr(Us + c * 16 * kD), u + c * 16 * kD, 16 * kD * 4, bars + 8 * c, keep);
+    }
   }
-  for (int i = tid; i < gq * kD; i += 256) xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
-  if (tid == 0) landed = 1;
-  __syncthreads();
-  if (!mbar_wait(bar, 0)) landed = 0;            // any thread that timed out clears it
-  __syncthreads();
-  if (!landed) {
+  for (int i = tid; i < gq * kD; i += kQprepWarps * 32)
+    xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
+  __syncthreads();                               // barriers initialised, query rows staged
+  if (!qprep_rotate(lv, ws, Us, xs, part, sig, b, h, bars)) {
     if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+    mbar_wait(bars + 8 * (tid >> 5), 0);         // one more bounded wait for copies still in flight
     pdl_wait();
     return;
   }
-  qprep_rotate(lv, ws, Us, xs, sig, b, h, 8);
   __syncthreads();
-  qprep_finish(lv, ws, xs, sig, b, h, scale_log2, 8);
+  qprep_finish(lv, ws, xs, sig, b, h, scale_log2, kQprepWarps);
+  timeline_span.mark();
   pdl_wait();                                    // the decode kernel waits on this grid, and through it on the append
 }
 
@@ -113,6 +121,7 @@ template <int GQ>
 __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace ws, const int* __restrict__ seq_lens,
                                                    const int* __restrict__ hist_pt, int max_hist_pages,
                                                    int pages_per_split, float scale_log2, int len_add) {
+  TimelineSpan timeline_span(lv, kTlInt2Simt);
   __shared__ __align__(16) uint8_t blk[kBlockBytes];
   __shared__ float qs[GQ][kD];
   __shared__ float qg[GQ][kNG];
@@ -265,6 +274,7 @@ template <int GQ>
 __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace ws, const __nv_bfloat16* __restrict__ q,
                                                   const int* __restrict__ seq_lens, const int* __restrict__ bf16_pt,
                                                   float scale_log2, int slot, int len_add) {
+  TimelineSpan timeline_span(lv, kTlBf16Seg);
   __shared__ __align__(16) __nv_bfloat16 ks[kP][kD + 8];
   __shared__ __align__(16) __nv_bfloat16 vs[kP][kD];
   __shared__ float qs[GQ][kD];
@@ -310,62 +320,6 @@ __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace 
 // channel). In explicit-V mode the combined history accumulator, which lives
 // in the rotated value basis, is multiplied by R_V^T = P_br H U_V^T before it
 // meets the BF16 partial.
-template <int GQ>
-__global__ void __launch_bounds__(128) k_merge(LayerView lv, DecodeWorkspace ws, int nsplit, void* out, int out_dtype,
-                                               float* lse) {
-  extern __shared__ __align__(16) float smem[];
-  float* wv = smem;                         // [128] history accumulator, rotated basis
-  float* zv = wv + kD;                      // [128] after P_br and H
-  const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x, lane = c & 31;
-  const bool expl = lv.v_explicit != 0;
-  const float* uvt = lv.params + (size_t)h * kParamFloats + kUVtOff;
-  for (int qi = 0; qi < GQ; ++qi) {
-    const int hq = h * GQ + qi;
-    const float* pb = part_ptr(ws.partials, b, lv.hq, hq, ws.nslots, 0);
-    float M1 = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M1 = fmaxf(M1, pb[s * kPartFloats]);
-    float L1 = 0.f, A1 = 0.f;
-    if (M1 != -INFINITY) {
-#pragma unroll 8
-      for (int s = 0; s < nsplit; ++s) {
-        const float m = pb[s * kPartFloats];
-        const float w = (m == -INFINITY) ? 0.f : exp2f(m - M1);
-        L1 = fmaf(pb[s * kPartFloats + 1], w, L1);
-        A1 = fmaf(pb[s * kPartFloats + 4 + c], w, A1);
-      }
-      if (expl) {
-        wv[c] = A1;
-        __syncthreads();
-        if (c < 32) {
-          float v[4];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) v[r] = wv[rot_channel(lane, r)];   // (a P_br)[lane + 32 r]
-          fwht128(v);
-#pragma unroll
-          for (int r = 0; r < 4; ++r) zv[lane + 32 * r] = v[r];
-        }
-        __syncthreads();
-        float o = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < kD; ++i) o = fmaf(zv[i], uvt[i * kD + c], o);   // (z U_V^T)[c]
-        A1 = o;
-        __syncthreads();
-      }
-    }
-    const float* pbf = pb + (size_t)nsplit * kPartFloats;
-    const float m2 = pbf[0], l2 = pbf[1], A2 = pbf[4 + c];
-    const float M = fmaxf(M1, m2);
-    const float w1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - M);
-    const float w2 = (m2 == -INFINITY) ? 0.f : exp2f(m2 - M);
-    const float Ls = L1 * w1 + l2 * w2;
-    const float o = (A1 * w1 + A2 * w2) / Ls;
-    const size_t oi = ((size_t)b * lv.hq + hq) * kD + c;
-    if (out_dtype == OSCAR_OUT_FP32) static_cast<float*>(out)[oi] = o;
-    else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(o);
-    if (lse != nullptr && c == 0) lse[(size_t)b * lv.hq + hq] = (M + log2f(Ls)) * 0.6931471805599453f;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // All-BF16 paged decode (the comparison kernel): split over pages, then a plain merge.
 template <int GQ>
@@ -442,13 +396,13 @@ template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
   if (a.ev0) cudaEventRecord(a.ev0, st);     // the traced span is the whole decode call
-  if (!a.skip_qprep) {
+  {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(lv.hkv, a.B);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(kQprepWarps * 32);
     cfg.dynamicSmemBytes = kQprepSmem;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -457,7 +411,7 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
       return OSCAR_ERR_CUDA;
   }
   if (a.algo == OSCAR_DECODE_MMA) {
-    // one fused launch: history splits, BF16 chunks and the merge by the group's last CTA
+    // one fused launch (history splits and BF16 pages), then the merge kernel
     const int rc = launch_decode_mma(lv, ws, a, scale_log2, st);
     if (a.ev1) cudaEventRecord(a.ev1, st);
     return rc;
@@ -466,9 +420,10 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
                                                                a.pages_per_split, scale_log2, a.len_add);
   k_bf16_seg<GQ><<<dim3(lv.hkv, a.B), 128, 0, st>>>(lv, ws, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens,
                                                     a.bf16_pt, scale_log2, a.nsplit, a.len_add);
-  k_merge<GQ><<<dim3(lv.hkv, a.B), 128, kMergeSmem, st>>>(lv, ws, a.nsplit, a.out, a.out_dtype, a.lse);
+  if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_CUDA;
+  const int rc = launch_merge(lv, ws, a.B, a.nsplit, 1, a.out, a.out_dtype, a.lse, st);
   if (a.ev1) cudaEventRecord(a.ev1, st);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+  return rc;
 }
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
@@ -510,14 +465,9 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
 int configure_mma_kernels();   // decode_mma.cu
 
 int configure_decode_kernels() {
-  if (configure_mma_kernels() != OSCAR_OK) return OSCAR_ERR_CUDA;
+  if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
   cudaError_t e = cudaFuncSetAttribute(k_qprep, cudaFuncAttributeMaxDynamicSharedMemorySize, kQprepSmem);
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
-#define OSCAR_MERGE_ATTR(G)                                                                              \
-  if (cudaFuncSetAttribute(k_merge<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSmem) != cudaSuccess) \
-    return OSCAR_ERR_CUDA;
-  OSCAR_MERGE_ATTR(1) OSCAR_MERGE_ATTR(2) OSCAR_MERGE_ATTR(4) OSCAR_MERGE_ATTR(8)
-#undef OSCAR_MERGE_ATTR
   return OSCAR_OK;
 }
 

@@ -7,15 +7,12 @@ namespace oscar {
 
 constexpr int kDefaultDecodeAlgo = OSCAR_DECODE_MMA;
 constexpr int kMaxMmaSplits = 2048;        // history splits of the fused decode
-constexpr int kMergeBucket = 8;            // history splits per first-level merge bucket
-constexpr int kCountersPerGroup = kMaxMmaSplits / kMergeBucket + 2;   // bucket tickets + BF16 bucket + group
-// partial slots per (request, q head): history splits, BF16 pages, history buckets, BF16 bucket
-inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf + (max_splits + kMergeBucket - 1) / kMergeBucket + 1; }
+// partial slots per (request, q head): history splits, then one per BF16 page
+inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
 constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
-constexpr int kAppendSmem = (kD * kD + kD + 4 * kD + 8 * kD) * 4 + 16;   // U + row + 4 partials + 8 queries + mbarrier
-constexpr int kQprepSmem = (kD * kD + 8 * kD) * 4 + 16;            // U_K + up to 8 query rows + mbarrier
-constexpr int kMergeSmem = 4 * kD * 4;                             // work rows of the merge
+constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;     // U + row + 4 partials + mbarrier
+constexpr int kQprepSmem = (kD * kD + 8 * kD + 8 * 8 * kD) * 4 + 64;   // U_K, 8 query rows, 8 x 8 partial rows, 8 mbarriers
 
 // Decode workspace carved from the caller's workspace buffer.
 struct DecodeWorkspace {
@@ -23,7 +20,6 @@ struct DecodeWorkspace {
   uint32_t* qfrag;    // [max_batch][hkv][kFragWords] fp16 MMA B fragments of the rotated queries
   float* qconst;      // [max_batch][hq][kQConst] per-query-head constants, see kQ* below
   float* partials;    // [max_batch][hq][nslots][kPartFloats]: history splits, then BF16 chunks
-  uint32_t* counters; // [max_batch][hkv] completion tickets of the fused decode (zero between calls)
   unsigned long long* cta_trace;  // optional per-CTA timeline of the fused decode (see oscar_trace_ctas)
   int trace_cap;      // records available in cta_trace
   int max_splits;     // history splits available
@@ -68,14 +64,17 @@ struct DecodeArgs {
   int pages_per_split;
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
-  int skip_qprep;        // the query prologue already ran (fused into the append)
-  cudaEvent_t ev0, ev1;  // optional events around the history kernel (may be null)
+  cudaEvent_t ev0, ev1;  // optional events around the decode kernels (may be null)
 };
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
-int launch_append_qprep(const LayerView& lv, const DecodeWorkspace& ws, int B, const void* q, const void* k,
-                        const void* v, const int* seq_lens_before, const int* hist_pt, int max_hist_pages,
-                        const int* bf16_pt, float sm_scale, cudaStream_t st);
+// Merge of the partial slots of every (request, q head): history slots [0, nsplit),
+// BF16 slots [nsplit, nsplit + nbfs). Launched as a programmatic dependent of the
+// kernel that wrote the partials.
+int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nsplit, int nbfs, void* out,
+                 int out_dtype, float* lse, cudaStream_t st);
+constexpr int kMergeChunk = 96;            // partial slots staged in shared memory at a time by the merge
+int configure_merge_kernel();
 int configure_decode_kernels();
 
 int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,

@@ -26,6 +26,7 @@
 
 #include "kernels.cuh"
 #include "rotate.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 
@@ -37,27 +38,66 @@ __device__ __forceinline__ float frag_round(float x) {
 }
 
 // Rotate the raw query rows xs[qi][0..127] (float, shared) of group (b, h)
-// with U (shared, row-major [128][128]): warp w handles query heads w, w +
-// nwarps, .... Each row is replaced by its rotation in rotated channel order;
-// q~ and its group sums go to the workspace and sigma of head qi to sig[qi].
-__device__ __forceinline__ void qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const float* Us,
-                                             float* xs, int* sig, int b, int h, int nwarps) {
-  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// with U (shared, row-major [128][128]), split over kQprepWarps warps: warp w
+// sums rows [16 w, 16 w + 16) of U for every head into part[w][qi][128]; after
+// a block barrier warp qi adds the kQprepWarps partial rows, applies the
+// Hadamard and bit-reversal stages and replaces row qi by q~ in rotated channel
+// order. q~ and its group sums go to the workspace, sigma of head qi to sig[qi].
+// Rows of U are used as they land: chunk w of the copy is waited on through
+// bars + 8 w. Returns false (block-uniform) when a chunk never landed.
+constexpr int kQprepWarps = 8;
+__device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const float* Us,
+                                             float* xs, float* part, int* sig, int b, int h, uint32_t bars) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lv.hq / lv.hkv;
-  for (int qi = wib; qi < gq; qi += nwarps) {
-    float y[1][4];
-    warp_rotate<1>(Us, xs + qi * kD, y);
-    __syncwarp();                                   // row qi fully read before it is overwritten
+  const bool landed = __syncthreads_and(mbar_wait(bars + 8 * w, 0));
+  if (!landed) return false;
+  float acc[8][4];
+#pragma unroll
+  for (int qi = 0; qi < 8; ++qi)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[qi][r] = 0.f;
+#pragma unroll 4
+  for (int i = 16 * w; i < 16 * w + 16; ++i) {
+    const float* row = Us + i * kD + lane;
+    const float u0 = row[0], u1 = row[32], u2 = row[64], u3 = row[96];
+#pragma unroll
+    for (int qi = 0; qi < 8; ++qi) {
+      if (qi < gq) {
+        const float xi = xs[qi * kD + i];
+        acc[qi][0] = fmaf(xi, u0, acc[qi][0]);
+        acc[qi][1] = fmaf(xi, u1, acc[qi][1]);
+        acc[qi][2] = fmaf(xi, u2, acc[qi][2]);
+        acc[qi][3] = fmaf(xi, u3, acc[qi][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int qi = 0; qi < 8; ++qi)
+    if (qi < gq)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) part[(w * 8 + qi) * kD + lane + 32 * r] = acc[qi][r];
+  __syncthreads();                                  // all partial rows written, xs no longer read
+  for (int qi = w; qi < gq; qi += kQprepWarps) {
+    float y[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float v = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kQprepWarps; ++ww) v += part[(ww * 8 + qi) * kD + lane + 32 * r];
+      y[r] = v;
+    }
+    fwht128(y);
     const int hq = h * gq + qi;
     float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
     float s = 0.f, mx = 0.f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int ch = rot_channel(lane, r);
-      dst[ch] = y[0][r];
-      xs[qi * kD + ch] = y[0][r];
-      s += y[0][r];
-      mx = fmaxf(mx, fabsf(y[0][r]));
+      dst[ch] = y[r];
+      xs[qi * kD + ch] = y[r];
+      s += y[r];
+      mx = fmaxf(mx, fabsf(y[r]));
     }
 #pragma unroll
     for (int m = 2; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);   // lanes of equal parity = one group
@@ -70,6 +110,7 @@ __device__ __forceinline__ void qprep_rotate(const LayerView& lv, const DecodeWo
       sig[qi] = min(max(12 - e, -60), 60);
     }
   }
+  return true;
 }
 
 // After qprep_rotate and a block barrier: per-head constants (warp w handles

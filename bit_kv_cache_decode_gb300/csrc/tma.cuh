@@ -6,7 +6,8 @@
 
 namespace oscar {
 
-constexpr unsigned kWaitLimit = 1u << 22;      // bounded mbarrier waits (each may suspend up to 1 us)
+constexpr unsigned kWaitLimit = 1u << 26;              // bounded mbarrier waits: tries, and ...
+constexpr unsigned long long kWaitNs = 2000000000ull;  // ... nanoseconds
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -27,20 +28,30 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false when the limit expires.
-// Each try_wait may suspend the thread for up to 1 us (the hint) instead of
-// spinning, so waiting warps leave the issue slots to working ones.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (unsigned i = 0; i < kWaitLimit; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000u)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
+// L2 eviction policies for bulk copies: data read once per step (streamed cache
+// pages) leaves L2 first, and small data every step needs (rotation matrices)
+// stays, so a step's stream does not push the next layer's matrices out.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_load with an L2 cache policy from l2_evict_first / l2_evict_last
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                               uint64_t policy) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
 }
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -48,6 +59,31 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false when the limit expires.
+// try_wait may suspend the thread for a system-dependent time instead of
+// spinning, so waiting warps leave the issue slots to working ones; the limit
+// is kept on %globaltimer, so it holds whatever that suspend time is.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (unsigned i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
+
 
 __device__ __forceinline__ unsigned sm_id() {
   unsigned s;

@@ -6,7 +6,7 @@
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
-#include "qprep.cuh"
+#include "timeline.cuh"
 
 namespace oscar {
 
@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(128) k_prefill(LayerView lv, const __nv_bfloat
                                                  const int* __restrict__ cu_seqlens, int B, int total,
                                                  const int* __restrict__ hist_pt, int max_hist_pages,
                                                  const int* __restrict__ bf16_pt) {
+  TimelineSpan timeline_span(lv, kTlPrefill);
   extern __shared__ __align__(16) float smem[];
   float* Us = smem;                       // [128][128]
   float* xs_all = smem + kD * kD;         // [4 warps][8 rows][128]
@@ -162,24 +163,18 @@ __global__ void __launch_bounds__(128) k_prefill(LayerView lv, const __nv_bfloat
 // it), rotates the demoted row with 4 warps each summing 32 rows of U, then
 // warp 0 finishes the Hadamard/bit-reversal, quantises and packs. Only after
 // that is the ring slot overwritten with the new token.
-// With QPREP the K CTA of each (request, kv head) also runs the decode's query
-// prologue (qprep.cuh) with the U_K it already holds, so a decode step needs
-// no separate prologue launch.
-template <bool QPREP>
 __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat16* __restrict__ k,
                                                 const __nv_bfloat16* __restrict__ v,
                                                 const int* __restrict__ seq_lens_before,
                                                 const int* __restrict__ hist_pt, int max_hist_pages,
-                                                const int* __restrict__ bf16_pt, const __nv_bfloat16* __restrict__ q,
-                                                DecodeWorkspace ws, float scale_log2) {
+                                                const int* __restrict__ bf16_pt) {
+  TimelineSpan timeline_span(lv, kTlAppend);
   extern __shared__ __align__(128) float smem[];
   float* Us = smem;                 // [128][128]
   float* xs = smem + kD * kD;       // [128] demoted row
   float* part = xs + kD;            // [4][128]
-  float* xq = part + 4 * kD;        // [8][128] query rows (QPREP)
-  const uint32_t bar = smem_addr(xq + 8 * kD);
+  const uint32_t bar = smem_addr(part + 4 * kD);
   __shared__ int landed;
-  __shared__ int sig[8];
   const int b = blockIdx.x, h = blockIdx.y, kind = blockIdx.z;
   const int tid = threadIdx.x, wib = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();          // the next kernel may start its prologue; it waits for this grid
@@ -189,7 +184,6 @@ __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat1
   if (bad && tid == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);
   const float* prm = lv.params + (size_t)h * kParamFloats;
   const bool rotate = (kind == OSCAR_KIND_K) || lv.v_explicit;
-  const bool qprep = QPREP && kind == OSCAR_KIND_K;
   // --- demotion of the oldest recent token: where it comes from and goes to ---
   bool demote = !bad && L_old >= lv.sink + lv.recent;
   int slot = 0, spage = -1, hh = 0, hpage = -1;
@@ -205,19 +199,16 @@ __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat1
       demote = false;
     }
   }
-  const bool need_u = qprep || (demote && rotate);
+  const bool need_u = demote && rotate;
   if (need_u && tid == 0) {
     mbar_init(bar);
-    bulk_load(smem_addr(Us), prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff), kD * kD * 4, bar);
+    bulk_load_hint(smem_addr(Us), prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff), kD * kD * 4, bar, l2_evict_last());
   }
   if (demote && tid < 64) {
     const __nv_bfloat16* src = bf16_row(lv, spage, h, kind, slot % kP);
     float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(src)[tid]);
     xs[2 * tid] = f.x; xs[2 * tid + 1] = f.y;
   }
-  const int gq = lv.hq / lv.hkv;
-  if (qprep)
-    for (int i = tid; i < gq * kD; i += 128) xq[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
   if (tid == 0) landed = 1;
   __syncthreads();
   if (need_u && !mbar_wait(bar, 0)) landed = 0;
@@ -258,11 +249,6 @@ __global__ void __launch_bounds__(128) k_append(LayerView lv, const __nv_bfloat1
       quantize_pack_row(y, tau, int2_block_w(lv, hpage, h), hh % kP, kind);
     }
     __syncthreads();   // the slot is read above before it is overwritten below
-  }
-  if (qprep) {
-    qprep_rotate(lv, ws, Us, xq, sig, b, h, 4);
-    __syncthreads();
-    qprep_finish(lv, ws, xq, sig, b, h, scale_log2, 4);
   }
   // --- write the new token ---
   if (bad || wib != 0) return;
@@ -311,30 +297,16 @@ int launch_append(const LayerView& lv, int B, const void* k, const void* v, cons
                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st) {
   if (B == 0) return OSCAR_OK;
   dim3 grid(B, lv.hkv, 2);
-  DecodeWorkspace none{};
-  k_append<false><<<grid, 128, kAppendSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
-                                                  static_cast<const __nv_bfloat16*>(v), seq_lens_before, hist_pt,
-                                                  max_hist_pages, bf16_pt, nullptr, none, 0.f);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
-}
-
-int launch_append_qprep(const LayerView& lv, const DecodeWorkspace& ws, int B, const void* q, const void* k,
-                        const void* v, const int* seq_lens_before, const int* hist_pt, int max_hist_pages,
-                        const int* bf16_pt, float sm_scale, cudaStream_t st) {
-  if (B == 0) return OSCAR_OK;
-  dim3 grid(B, lv.hkv, 2);
-  k_append<true><<<grid, 128, kAppendSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
-                                                 static_cast<const __nv_bfloat16*>(v), seq_lens_before, hist_pt,
-                                                 max_hist_pages, bf16_pt, static_cast<const __nv_bfloat16*>(q), ws,
-                                                 sm_scale * kLog2e);
+  k_append<<<grid, 128, kAppendSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
+                                           static_cast<const __nv_bfloat16*>(v), seq_lens_before, hist_pt,
+                                           max_hist_pages, bf16_pt);
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_write_path_kernels() {
   if (cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
-  if (cudaFuncSetAttribute(k_append<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_append<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_append, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
   return OSCAR_OK;
 }

@@ -197,10 +197,11 @@ int oscar_decode_attention(oscar_cache* cache, int layer, int B, const void* q, 
 /* One decode step of a layer: oscar_append_kv(k, v at position
  * seq_lens_before[r]) followed by oscar_decode_attention(q) over
  * seq_lens_before[r] + 1 tokens, with the same arguments, layouts and
- * results as those two calls. With the tensor-core decode the append kernel
- * also rotates the queries (it already holds U_K for the demotion), so the
- * step is two launches: append + query prologue, then the decode kernel,
- * which starts early and prefetches history pages while the append runs. */
+ * results as those two calls, issued as one chain: the append, then the
+ * query prologue, the decode kernel and the merge, each launched as a
+ * programmatic dependent of the one before it. The prologue runs while
+ * the append does, and the decode kernel prefetches history pages that the
+ * append cannot touch before it waits. */
 int oscar_decode_step(oscar_cache* cache, int layer, int B, const void* q, const void* k, const void* v,
                       const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
                       const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream);
@@ -300,9 +301,10 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
  * without ordering) race and give wrong results; calls ordered on one stream
  * are safe. The history is split into fewer pieces when needed to fit. A call
  * whose per-query state does not fit even with one history split, i.e. when
- * B * Hq * (544 + 528 * (3 + (sink + recent) / 64)) + B * Hkv * 5128 bytes plus
- * about 1.5 KB of rounding exceed 4 MiB (B * Hq above about 850 with the
- * default windows), returns OSCAR_ERR_TOO_LARGE before any device work. */
+ * B * Hq * (560 + 528 * (1 + (sink + recent) / 64)) + B * Hkv * 4096 bytes plus
+ * about 1.3 KB of rounding exceed 4 MiB (B * Hq above about 880 with the
+ * default windows and Hq / Hkv = 4), returns OSCAR_ERR_TOO_LARGE before any
+ * device work. */
 int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int layer, int B, const void* q,
                                    const int32_t* seq_lens, const int32_t* hist_pt, int max_hist_pages,
                                    const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse,
@@ -317,6 +319,22 @@ int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int l
  * buf: device memory for `capacity` records (64 bytes each); NULL stops
  * recording. CTAs beyond `capacity` are not recorded. */
 int oscar_trace_ctas(oscar_cache* cache, void* buf, int capacity);
+
+/* Record a timeline of every CTA of the following launches of this cache's
+ * kernels (append, prefill, query prologue, decode, merge), accumulating
+ * across launches until the buffer is full. buf: device uint64
+ * [4 + 4 * capacity]; the caller zeroes buf[0], which counts the records
+ * claimed (it may exceed `capacity`; the excess is not written). Record i is
+ * buf[4 + 4 i .. 4 + 4 i + 3] = {kind | layer << 8 | SM << 24 | linear CTA
+ * index << 32, start, end, mark}, times in %globaltimer nanoseconds, taken by
+ * thread 0 on entry and when it leaves the kernel; mark is, for the merge, the
+ * time its wait for the decode kernel returned and, for the query prologue,
+ * the time its work was done (before it waits for the append), else 0. Kinds: 1 append, 2 query
+ * prologue, 3 tensor-core decode, 4 merge, 5 CUDA-core history decode,
+ * 6 BF16 segment, 7 prefill. Launches issued while a buffer is set keep
+ * writing to it, also from CUDA graphs captured meanwhile; NULL stops
+ * recording for later launches. */
+int oscar_trace_timeline(oscar_cache* cache, void* buf, int capacity);
 
 /* Human-readable name of a status code. */
 const char* oscar_error_string(int code);

@@ -290,8 +290,8 @@ def run_ours(args, rank: int, world: int, device):
     ms_step = ms / args.steps
     step_bytes = sum(step_algorithmic_bytes(L_start + 1 + s, B, H, hq, nl) for s in range(args.steps)) / args.steps
     peak, peak_src = peaks()
-    # dominant kernel: the decode call (query prologue + fused decode, PDL-chained), timed per call with the
-    # library's CUDA events in a second timed region that issues the same steps without the graph
+    # dominant kernel: the fused decode kernel, timed per launch with the library's CUDA events in a second
+    # timed region that issues the same steps without the graph
     dec_ms, dec_n, L_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
     hb = history_bytes(L_prof, B, H) + B * min(L_prof, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
     dec_avg_ms = dec_ms / max(dec_n, 1)
@@ -308,8 +308,9 @@ def run_ours(args, rank: int, world: int, device):
                    "launch": "one CUDA graph per step (oscar_decode_step per layer), new tokens copied in"},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
                 "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak},
-        "roofline": {"bound": "hbm", "kernel": "decode call: query prologue + " +
-                     ("fused INT2/BF16/merge kernel" if args.algo == 1 else "history + BF16 + merge kernels"),
+        "roofline": {"bound": "hbm", "kernel": ("k_decode_mma (fused INT2 history + BF16 pages)" if args.algo == 1
+                                                else "k_int2_simt (INT2 history)") +
+                     ", CUDA events around each launch in an eager copy of the timed steps",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
                      "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
@@ -327,8 +328,8 @@ def run_ours(args, rank: int, world: int, device):
 
 
 def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
-    """Eager steps with the library's CUDA events around every oscar_decode_step (append + query rotation
-    kernel, PDL-chained into the fused decode kernel): returns (summed ms, calls, mean context)."""
+    """Eager steps with the library's CUDA events around the history (fused decode) kernel of every
+    oscar_decode_step: returns (summed ms, launches, mean context)."""
     import torch
     import synth
     cache, nl = wl["cache"], wl["layers"]
@@ -348,8 +349,8 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "c6d03a48fe3934c6cc04e76312498fb2a866b0e1cf72db0119adfc3c64d0ff8e",
-                      "bytes_per_launch": 66883328 + 517888}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "e63d824d2155b3840c5f28b5baf92ab3953f911c25082555911e557fc5f21205",
+                      "bytes_per_launch": 66777088 + 500224}
 
 
 def sources_digest() -> str:

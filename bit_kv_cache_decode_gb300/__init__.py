@@ -35,7 +35,7 @@ EXPORTS = (
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
     "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
-    "oscar_trace_timeline",
+    "oscar_trace_timeline", "oscar_check_wait_timeout",
 )
 
 
@@ -78,6 +78,7 @@ def _load() -> ctypes.CDLL:
         "oscar_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)],
         "oscar_trace_ctas": [vp, vp, c_int],
         "oscar_trace_timeline": [vp, vp, c_int],
+        "oscar_check_wait_timeout": [vp, vp],
         "oscar_decode_step": [vp, c_int, c_int, vp, vp, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
         "oscar_decode_attention_noalloc": [ctypes.POINTER(Layout), vp, c_int, c_int, vp, i32p, i32p, c_int, i32p,
                                            c_float, vp, c_int, vp, vp, vp],
@@ -287,6 +288,11 @@ class OscarCache:
         tensor of 8 * n elements, n records); None stops recording."""
         n = 0 if buf is None else buf.numel() // 8
         _check(_lib.oscar_trace_ctas(self._h, _ptr(buf), n), "oscar_trace_ctas")
+
+    def check_wait_timeout(self, stream=None):
+        """Run the bounded-wait self-check: a device wait that nothing completes must give up (about 2 s)
+        and set the TIMEOUT bit of the status word."""
+        _check(_lib.oscar_check_wait_timeout(self._h, _stream(stream)), "oscar_check_wait_timeout")
 
     def trace_timeline(self, buf=None):
         """Record a timeline of every CTA of the following kernel launches into ``buf`` (an int64 device tensor

@@ -368,10 +368,8 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   }
   // append, then the decode chain (query prologue, decode, merge), each a
   // programmatic dependent of the kernel before it
-  if (a.ev0) cudaEventRecord(a.ev0, st);
   const int rc = launch_append(lv, B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt, st);
   if (rc != OSCAR_OK) return rc;
-  a.ev0 = nullptr;                       // recorded above: the profiled span starts at the append
   return launch_decode(lv, c->dws, a, st);
 }
 
@@ -443,6 +441,11 @@ int oscar_trace_ctas(oscar_cache* c, void* buf, int capacity) {
   c->dws.cta_trace = static_cast<unsigned long long*>(buf);
   c->dws.trace_cap = buf ? capacity : 0;
   return OSCAR_OK;
+}
+
+int oscar_check_wait_timeout(oscar_cache* c, void* stream) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  return launch_wait_probe(c->status, static_cast<cudaStream_t>(stream));
 }
 
 int oscar_trace_timeline(oscar_cache* c, void* buf, int capacity) {

@@ -613,8 +613,7 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.numAttrs = 1;
   const cudaError_t e = (lv.hq / lv.hkv <= 4) ? cudaLaunchKernelEx(&cfg, k_decode_mma<1>, lv, ws, fa)
                                               : cudaLaunchKernelEx(&cfg, k_decode_mma<2>, lv, ws, fa);
-  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
-  return launch_merge(lv, ws, a.B, a.nsplit, a.nbf, a.out, a.out_dtype, a.lse, st);
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels() {

@@ -395,7 +395,6 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
 template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
-  if (a.ev0) cudaEventRecord(a.ev0, st);     // the traced span is the whole decode call
   {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -411,19 +410,22 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
       return OSCAR_ERR_CUDA;
   }
   if (a.algo == OSCAR_DECODE_MMA) {
-    // one fused launch (history splits and BF16 pages), then the merge kernel
+    // one fused launch (history splits and BF16 pages), then the merge kernel; the profiled
+    // span is the fused launch alone (the events make it wait for the query prologue)
+    if (a.ev0) cudaEventRecord(a.ev0, st);
     const int rc = launch_decode_mma(lv, ws, a, scale_log2, st);
     if (a.ev1) cudaEventRecord(a.ev1, st);
-    return rc;
+    if (rc != OSCAR_OK) return rc;
+    return launch_merge(lv, ws, a.B, a.nsplit, a.nbf, a.out, a.out_dtype, a.lse, st);
   }
+  if (a.ev0) cudaEventRecord(a.ev0, st);     // profiled span: the history kernel
   k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
                                                                a.pages_per_split, scale_log2, a.len_add);
+  if (a.ev1) cudaEventRecord(a.ev1, st);
   k_bf16_seg<GQ><<<dim3(lv.hkv, a.B), 128, 0, st>>>(lv, ws, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens,
                                                     a.bf16_pt, scale_log2, a.nsplit, a.len_add);
   if (cudaGetLastError() != cudaSuccess) return OSCAR_ERR_CUDA;
-  const int rc = launch_merge(lv, ws, a.B, a.nsplit, 1, a.out, a.out_dtype, a.lse, st);
-  if (a.ev1) cudaEventRecord(a.ev1, st);
-  return rc;
+  return launch_merge(lv, ws, a.B, a.nsplit, 1, a.out, a.out_dtype, a.lse, st);
 }
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {

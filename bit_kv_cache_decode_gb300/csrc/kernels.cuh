@@ -64,7 +64,7 @@ struct DecodeArgs {
   int pages_per_split;
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
-  cudaEvent_t ev0, ev1;  // optional events around the decode kernels (may be null)
+  cudaEvent_t ev0, ev1;  // optional events around the history (fused decode) kernel, may be null
 };
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
@@ -76,6 +76,7 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
 constexpr int kMergeChunk = 96;            // partial slots staged in shared memory at a time by the merge
 int configure_merge_kernel();
 int configure_decode_kernels();
+int launch_wait_probe(int* status, cudaStream_t st);   // checks.cu
 
 int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,
                        const int* seq_lens, const int* page_table, int max_pages, float sm_scale, void* out,

@@ -260,11 +260,14 @@ int oscar_calibrate(const float* Q, const float* K, const float* V, int N, float
 
 /* ---- tracing ------------------------------------------------------------- */
 
-/* Start tracing decode calls: while enabled, every oscar_decode_attention
- * records a CUDA event pair on its stream around all of its kernels (query
- * prologue through merge); at most `capacity` calls are kept. Event records
- * can be captured into a CUDA graph; the graph then re-records the same
- * events on every replay. */
+/* Start tracing decode calls: while enabled, every oscar_decode_attention and
+ * oscar_decode_step records a CUDA event pair on its stream around its
+ * history kernel (the fused tensor-core decode kernel, or the CUDA-core
+ * history kernel), the dominant launch of the call; at most `capacity` calls
+ * are kept. The events separate that kernel from the programmatic overlap
+ * with its neighbours, so it is timed alone. Event records can be captured
+ * into a CUDA graph; the graph then re-records the same events on every
+ * replay. */
 int oscar_profile_begin(oscar_cache* cache, int capacity);
 
 /* Stop, synchronise and report the summed device time (ms) of the traced
@@ -335,6 +338,13 @@ int oscar_trace_ctas(oscar_cache* cache, void* buf, int capacity);
  * writing to it, also from CUDA graphs captured meanwhile; NULL stops
  * recording for later launches. */
 int oscar_trace_timeline(oscar_cache* cache, void* buf, int capacity);
+
+/* Failure-detection self-check: launches one warp that waits on a device
+ * barrier nothing completes. Like every wait in the library it gives up after
+ * 2 seconds of %globaltimer time and sets OSCAR_STATUS_TIMEOUT in the status
+ * word (read with oscar_get_status). Nothing faults and nothing stays pending;
+ * the cache remains usable. */
+int oscar_check_wait_timeout(oscar_cache* cache, void* stream);
 
 /* Human-readable name of a status code. */
 const char* oscar_error_string(int code);

@@ -13,6 +13,8 @@ Workloads (synthetic, seeded; Qwen3-shaped random data, no model weights):
   qwen3_4b_b32  36 layers, batch 32 x 102,400 tokens sharing a 92,160-token prefix
   qwen3_8b_l1   1 layer, batch 1, 32,768 tokens
   qwen3_8b_100k_l1  1 layer of qwen3_8b_36l (the same decode launch), for profiler captures
+  qwen3_32b_mixed   1 layer x (64 q / 8 kv heads), batch 8, lengths ~ U[98,304, 131,072]: one timed bulk
+                    prefill of all requests, then decode steps (append + demotion + decode)
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
@@ -45,6 +47,8 @@ WORKLOADS = {
     "qwen3_4b_b32": dict(layers=36, hq=32, hkv=8, batch=32, ctx=102400, shared=92160),
     "qwen3_8b_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=32768, shared=0),
     "qwen3_8b_100k_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
+    # ctx as (lo, hi): per-request lengths drawn uniformly, all requests prefilled by one bulk call
+    "qwen3_32b_mixed": dict(layers=1, hq=64, hkv=8, batch=8, ctx=(98304, 131072), shared=0),
 }
 
 
@@ -118,7 +122,10 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
     import synth
 
     w = WORKLOADS[name]
-    L, B, H, hq, nl, shared = w["ctx"], w["batch"], w["hkv"], w["hq"], w["layers"], w["shared"]
+    B, H, hq, nl, shared = w["batch"], w["hkv"], w["hq"], w["layers"], w["shared"]
+    mixed = isinstance(w["ctx"], tuple)
+    lens = (synth.seq_lens_uniform(seed, B, *w["ctx"]) if mixed else np.full(B, w["ctx"])).astype(np.int64)
+    L = int(lens.max())
     Lmax = L + steps_capacity
     n_hist_max = (Lmax - 320 + 63) // 64
     # page tables: shared prefix pages first (sink page + history pages covering the prefix), then private pages
@@ -163,12 +170,28 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
             bpt[r, sp:] = sp + r * (npg - sp) + np.arange(npg - sp)
     hp_d = torch.from_numpy(hist_pt).to(device)
     bp_d = torch.from_numpy(bf16_pt).to(device)
+    prefill = {"ms": 0.0, "tokens": 0}
     for layer in range(nl):
         cs = cals[layer * H:(layer + 1) * H]
         cache.set_rotation(layer, np.stack([c["U_K"] for c in cs]), np.stack([c["U_V"] for c in cs]),
                            np.stack([c["tau_K"] for c in cs]), np.stack([c["tau_V"] for c in cs]))
         outl = np.stack([synth.head_stats(seed, layer, h).outliers for h in range(H)])
         gen.manual_seed(seed * 1000003 + layer)
+        if mixed:
+            # all requests in one bulk prefill call, timed: its throughput is this workload's write-path figure
+            tot = int(lens.sum())
+            k, v = synth.torch_kv_tokens(tot, H, outl, gen, device)
+            cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            cache.quantize_prefill(layer, k, v, cu, hp_d, bp_d, total_tokens=tot)
+            e1.record()
+            torch.cuda.synchronize()
+            prefill["ms"] += e0.elapsed_time(e1)
+            prefill["tokens"] += tot
+            del k, v
+            continue
         if shared:
             kp, vp = synth.torch_kv_tokens(shared, H, outl, gen, device)
         for r in range(B):
@@ -189,7 +212,8 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
         torch.cuda.synchronize()
     if cache.get_status() != 0:
         raise RuntimeError("device status error while building the workload")
-    return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, B=B, H=H, hq=hq, layers=nl,
+    return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, lens=lens, prefill=prefill, B=B, H=H, hq=hq,
+                layers=nl,
                 bf16_pages=bf16_pages, base_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
                 hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared)
 
@@ -209,9 +233,18 @@ def history_bytes(L: int, B: int, H: int) -> int:
     return B * max(0, L - 320) * H * HIST_BYTES
 
 
-def step_algorithmic_bytes(L: int, B: int, H: int, hq: int, layers: int) -> int:
-    per_layer = history_bytes(L, B, H) + B * min(L, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
-    return per_layer * layers
+def layer_bytes(lens, H: int, hq: int) -> int:
+    """Algorithmic bytes of one layer's decode over requests of lengths `lens` (logical: a page that several
+    requests share counts once per request): INT2 history, BF16 sink + recent, q and o."""
+    return sum(history_bytes(int(L), 1, H) + min(int(L), 320) * H * BF16_BYTES + 2 * hq * 128 * 2 for L in lens)
+
+
+def shared_unique_bytes(lens, shared: int, H: int, hq: int) -> int:
+    """As layer_bytes with the shared prefix's history and sink pages counted once."""
+    if not shared:
+        return layer_bytes(lens, H, hq)
+    shared_hist = (shared - 64) * H * HIST_BYTES
+    return layer_bytes(lens, H, hq) - (len(lens) - 1) * (shared_hist + 64 * H * BF16_BYTES)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -221,9 +254,10 @@ def run_ours(args, rank: int, world: int, device):
     import torch
     import synth
 
-    seed = 1234 + rank
+    seed = replica_seed(rank)
     total_steps = args.warmup + args.steps
-    wl = build_workload(args.workload, seed, device, with_bf16=not args.no_bf16,
+    mixed = isinstance(WORKLOADS[args.workload]["ctx"], tuple)
+    wl = build_workload(args.workload, seed, device, with_bf16=not (args.no_bf16 or mixed),
                         steps_capacity=3 * total_steps + 16, algo=args.algo)
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
     stream = torch.cuda.current_stream()
@@ -232,8 +266,7 @@ def run_ours(args, rank: int, world: int, device):
     kv_cur = torch.empty_like(kv_new[0])          # the step's new K/V, [layers, 2, B, H, 128]
     q_cur = torch.empty_like(q_all[0])            # the step's queries, [layers, B, Hq, 128]
     out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
-    seq = torch.full((B,), wl["L"], dtype=torch.int32, device=device)
-    seq1 = seq + 1
+    seq = torch.from_numpy(wl["lens"].astype(np.int32)).to(device)
     # per layer, oscar_decode_step: the append kernel (which also rotates the queries on the tensor-core path)
     # then one fused decode launch (mma), or append + query rotation + history + BF16 segment + merge (simt)
     launches_per_layer = 2 if args.algo == 1 else 5
@@ -268,7 +301,7 @@ def run_ours(args, rank: int, world: int, device):
     for i in range(1, args.warmup):
         step(i)
     torch.cuda.synchronize()
-    L_start = int(seq[0].item())
+    lens_start = seq.cpu().numpy().astype(np.int64)
     barrier(world)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(device.index if device.index is not None else 0) as clk:
@@ -285,15 +318,17 @@ def run_ours(args, rank: int, world: int, device):
     if cache.get_status() != 0:
         raise RuntimeError("device status error during the timed steps")
     # units: KV tokens attended per step (the appended token included), all layers
-    kv_tokens = sum(B * (L_start + 1 + s) * nl for s in range(args.steps))
-    value = kv_tokens * world / (ms / 1e3)
+    kv_tokens = sum(int(lens_start.sum() + B * (1 + s)) * nl for s in range(args.steps))
+    value = whole_job_rate(kv_tokens, ms, world)
     ms_step = ms / args.steps
-    step_bytes = sum(step_algorithmic_bytes(L_start + 1 + s, B, H, hq, nl) for s in range(args.steps)) / args.steps
+    step_bytes = sum(layer_bytes(lens_start + 1 + s, H, hq) * nl for s in range(args.steps)) / args.steps
+    step_unique = sum(shared_unique_bytes(lens_start + 1 + s, wl["shared"], H, hq) * nl
+                      for s in range(args.steps)) / args.steps
     peak, peak_src = peaks()
     # dominant kernel: the fused decode kernel, timed per launch with the library's CUDA events in a second
     # timed region that issues the same steps without the graph
-    dec_ms, dec_n, L_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
-    hb = history_bytes(L_prof, B, H) + B * min(L_prof, 320) * H * BF16_BYTES + 2 * B * hq * 128 * 2
+    dec_ms, dec_n, lens_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
+    hb = layer_bytes(lens_prof, H, hq)
     dec_avg_ms = dec_ms / max(dec_n, 1)
     achieved = hb / (dec_avg_ms / 1e3) / 1e9
     res = {
@@ -307,7 +342,8 @@ def run_ours(args, rank: int, world: int, device):
                    "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
                    "launch": "one CUDA graph per step (oscar_decode_step per layer), new tokens copied in"},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
-                "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak},
+                "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak,
+                "step_unique_bytes": step_unique, "step_unique_gbs": step_unique / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "kernel": ("k_decode_mma (fused INT2 history + BF16 pages)" if args.algo == 1
                                                 else "k_int2_simt (INT2 history)") +
                      ", CUDA events around each launch in an eager copy of the timed steps",
@@ -317,11 +353,19 @@ def run_ours(args, rank: int, world: int, device):
         "gpu_launches": (launches_per_layer * nl + 2) * args.steps,
         "clocks": clk.summary(),
     }
-    if not args.no_bf16:
+    if wl["bf16_pages"] is not None:
         res["bf16_baseline"] = run_bf16(wl, args, q_all, device)
         res["bf16_baseline"]["speedup_of_int2_step"] = res["bf16_baseline"]["ms_per_step"] / ms_step
+    if wl["prefill"]["tokens"]:
+        pf, lens0 = wl["prefill"], wl["lens"]
+        moved = pf["tokens"] * H * BF16_BYTES + layer_bytes(lens0, H, 0) * nl     # bf16 K/V read + pool written
+        res["prefill"] = {"call": "oscar_quantize_prefill, all requests in one call per layer",
+                          "tokens": pf["tokens"], "ms": pf["ms"],
+                          "tokens_per_s": pf["tokens"] / (pf["ms"] / 1e3),
+                          "algorithmic_bytes": moved, "gbs": moved / (pf["ms"] / 1e3) / 1e9,
+                          "frac_of_peak": moved / (pf["ms"] / 1e3) / 1e9 / peak}
     res["e2e"] = run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq)
-    res["e2e_eager"] = run_e2e_eager(wl, args, device, start_len=int(seq[0].item()))
+    res["e2e_eager"] = run_e2e_eager(wl, args, device, start_lens=seq.cpu().numpy())
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(wl, seed, device, budget_s=args.cpu_budget)
     return res
@@ -335,7 +379,7 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
     cache, nl = wl["cache"], wl["layers"]
     sm = synth.sm_scale()
     torch.cuda.synchronize()
-    L0 = int(seq[0].item()) + 1
+    lens0 = seq.cpu().numpy().astype(np.int64) + 1
     cache.profile_begin(nl * args.steps)
     for i in range(args.steps):
         for layer in range(nl):
@@ -343,7 +387,7 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
                               wl["bf16_pt"], sm, out=out[layer])
         seq.add_(1)
     ms, n = cache.profile_read()
-    return ms, n, L0 + (args.steps - 1) // 2
+    return ms, n, lens0 + (args.steps - 1) // 2
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
@@ -422,7 +466,7 @@ def run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    Ls = int(seq[0].item())
+    Ls = int(seq.sum().item())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
@@ -430,14 +474,14 @@ def run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    kv_tokens = sum(B * (Ls + 1 + s) * nl for s in range(args.steps)) / args.steps
+    kv_tokens = sum((Ls + B * (1 + s)) * nl for s in range(args.steps)) / args.steps
     return {"value": kv_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": (host_kv.numel() + host_q.numel()) * 2, "d2h_bytes_per_step": host_out.numel() * 2,
             "path": "pinned host -> device copy, graph replay of the C-ABI calls, device -> host copy"}
 
 
-def run_e2e_eager(wl, args, device, start_len: int):
-    """As run_e2e but issuing the C-ABI calls directly from Python every step (no graph)."""
+def run_e2e_eager(wl, args, device, start_lens):
+    """As run_e2e but issuing oscar_decode_step directly from Python every step (no graph)."""
     import torch
     import synth
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
@@ -448,24 +492,22 @@ def run_e2e_eager(wl, args, device, start_len: int):
     dev_in = torch.empty_like(host_in, device=device)
     dev_out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
     torch.cuda.synchronize()
-    seq = torch.full((B,), start_len, dtype=torch.int32, device=device)   # the cache's current length
-    seq1 = seq + 1
+    seq = torch.as_tensor(start_lens, dtype=torch.int32).to(device)   # the cache's current lengths
     kvn = dev_in[:nl * 2 * B * H * 128].view(nl, 2, B, H, 128)
     qn = dev_in[nl * 2 * B * H * 128:].view(nl, B, hq, 128)
 
     def step():
         dev_in.copy_(host_in, non_blocking=True)
         for layer in range(nl):
-            cache.append_kv(layer, kvn[layer, 0], kvn[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"])
-            cache.decode_attention(layer, qn[layer], seq1, wl["hist_pt"], wl["bf16_pt"], sm, out=dev_out[layer])
+            cache.decode_step(layer, qn[layer], kvn[layer, 0], kvn[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"], sm,
+                              out=dev_out[layer])
         host_out.copy_(dev_out.view(-1), non_blocking=True)
         seq.add_(1)
-        seq1.add_(1)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    Ls = int(seq[0].item())
+    Ls = int(seq.sum().item())
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
@@ -473,7 +515,7 @@ def run_e2e_eager(wl, args, device, start_len: int):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    kv_tokens = sum(B * (Ls + 1 + s) * nl for s in range(args.steps)) / args.steps
+    kv_tokens = sum((Ls + B * (1 + s)) * nl for s in range(args.steps)) / args.steps
     return {"value": kv_tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": host_in.numel() * 2, "d2h_bytes_per_step": host_out.numel() * 2,
             "path": "pinned host -> device copy, direct C-ABI calls from Python, device -> host copy"}
@@ -484,7 +526,7 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
     from the pool bytes of layer 0, on the host cores; KV heads are added until the time budget is used."""
     from oracle import attention as A
     from oracle import pool as P
-    cache, H, hq, L = wl["cache"], wl["H"], wl["hq"], wl["L"]
+    cache, H, hq, L = wl["cache"], wl["H"], wl["hq"], int(wl["lens"][0])
     import torch
     torch.cuda.synchronize()
     cfg = wl["cfg"]
@@ -549,6 +591,17 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------------------------
+
+
+def replica_seed(rank: int) -> int:
+    """Each rank runs an independent replica of the workload (weak scaling) from its own seed."""
+    return 1234 + rank
+
+
+def whole_job_rate(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Units per second of the whole job: every rank processed units_per_rank within the slowest
+    rank's time ms_max."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 def barrier(world):

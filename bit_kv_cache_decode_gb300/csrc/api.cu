@@ -103,14 +103,17 @@ int configure_once() {
 // per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs and every
 // group launches `extra` more CTAs; pages per split are rounded up to `align`
 // and there is no empty trailing split.
+// Splits of the history per (request, kv head): the fewest waves of CTAs, each
+// split at most max_pps pages when the split budget allows (0: no limit).
 void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int align, int extra,
-                   int* nsplit, int* pps) {
+                   int max_pps, int* nsplit, int* pps) {
   if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
   const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
   const int nmax = std::min(std::min(max_splits, max_pages), kMaxMmaSplits);
+  const int nmin = max_pps > 0 ? std::min(nmax, (max_pages + max_pps - 1) / max_pps) : 1;
   long best_cost = -1;
   int best_p = max_pages;
-  for (int n = 1; n <= nmax; ++n) {
+  for (int n = nmin; n <= nmax; ++n) {
     int p = (max_pages + n - 1) / n;
     p = (p + align - 1) / align * align;
     const int used = (max_pages + p - 1) / p;
@@ -122,9 +125,12 @@ void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int c
   *nsplit = (max_pages + best_p - 1) / best_p;
 }
 
-void algo_policy(int algo, int gq, int nbf, int* ctas_per_sm, int* align, int* extra) {
-  if (algo == OSCAR_DECODE_MMA) { *ctas_per_sm = gq <= 4 ? 4 : 2; *align = 4; *extra = nbf; }
-  else { *ctas_per_sm = 4; *align = 1; *extra = 0; }
+void algo_policy(int algo, int gq, int nbf, int* ctas_per_sm, int* align, int* extra, int* max_pps) {
+  if (algo == OSCAR_DECODE_MMA) {
+    *ctas_per_sm = gq <= 4 ? 4 : 2; *align = 4; *extra = nbf; *max_pps = kMaxPagesPerMmaSplit;
+  } else {
+    *ctas_per_sm = 4; *align = 1; *extra = 0; *max_pps = 0;
+  }
 }
 
 }  // namespace
@@ -313,9 +319,9 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.len_add = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
-    int cps, align, extra;
-    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra);
-    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, &a.nsplit,
+    int cps, align, extra, mpps;
+    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra, &mpps);
+    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, mpps, &a.nsplit,
                   &a.pages_per_split);
   }
   a.ev0 = a.ev1 = nullptr;
@@ -355,9 +361,9 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   a.algo = c->algo;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
-    int cps, align, extra;
-    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra);
-    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, &a.nsplit,
+    int cps, align, extra, mpps;
+    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra, &mpps);
+    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, mpps, &a.nsplit,
                   &a.pages_per_split);
   }
   a.ev0 = a.ev1 = nullptr;
@@ -428,7 +434,7 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   int nsplit, pps;
-  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, 0, &nsplit, &pps);
+  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, 0, 0, &nsplit, &pps);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
@@ -517,9 +523,9 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 // The history split choice of oscar_decode_attention, for at most max_splits splits.
 void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
                          int* nsplit, int* pps) {
-  int cps, align, extra;
-  algo_policy(algo, gq, nbf, &cps, &align, &extra);
-  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, extra, nsplit, pps);
+  int cps, align, extra, mpps;
+  algo_policy(algo, gq, nbf, &cps, &align, &extra, &mpps);
+  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, extra, mpps, nsplit, pps);
 }
 
 int configure_kernels() { return configure_once(); }

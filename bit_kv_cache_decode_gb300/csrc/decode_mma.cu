@@ -90,6 +90,15 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
   return d;
 }
 
+// exact fp16 codes: ((1024 + c*4^k) * 4^-k) - 1024*4^-k = c, for both halves
+__device__ __forceinline__ uint32_t exact_codes(uint32_t biased, int k) {
+  const uint32_t scale = 0x3C003C00u - (uint32_t)(k * 0x08000800u);   // 4^-k = 2^-2k: exponent - 2k
+  const uint32_t offs = 0xE400E400u - (uint32_t)(k * 0x08000800u);    // -1024 * 4^-k
+  __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&biased), *reinterpret_cast<const __half2*>(&scale),
+                      *reinterpret_cast<const __half2*>(&offs));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 struct FusedArgs {
   const int* seq_lens;
   int len_add;                       // attend over seq_lens[b] + len_add tokens
@@ -221,13 +230,12 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][mt][e] = 0.f;
-  float mrun[NT], lsum[NT], zacc[NT][2], bacc[NT][4];
+  float mrun[NT], lsum[NT], zacc[NT][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     mrun[nt] = -INFINITY;
     lsum[nt] = 0.f;
     zacc[nt][0] = zacc[nt][1] = 0.f;
-    bacc[nt][0] = bacc[nt][1] = bacc[nt][2] = bacc[nt][3] = 0.f;
   }
   uint32_t phase = 0;
   bool timed_out = false;
@@ -322,8 +330,6 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           zacc[nt][0] *= al;
           zacc[nt][1] *= al;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) bacc[nt][e] *= al;
-#pragma unroll
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= al;
@@ -358,28 +364,20 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         }
         const uint2 wab = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t) * 64 + 8 * g);
         const uint2 wcd = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t + 4) * 64 + 8 * g);
-        // code mt of each 16-bit half (bits 2 mt) moved into bits 6-7 (mt even) or 8-9 (mt odd), fed as the
-        // fp16 value 1024 + c * W_mt (W = 64 or 256): shift left 6, left 2, right 2, right 6 for mt / 2 = 0..3
+        // exact codes (the accumulators stay the size of the result: the tensor cores' fp32
+        // accumulation truncates, so a large constant part would grow the error with the split length)
+        const uint32_t wah = wab.x >> 8, wbh = wab.y >> 8, wch = wcd.x >> 8, wdh = wcd.y >> 8;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int sh = 6 - 4 * i;
-          const uint32_t xa = sh > 0 ? wab.x << sh : wab.x >> -sh, xb = sh > 0 ? wab.y << sh : wab.y >> -sh;
-          const uint32_t xc = sh > 0 ? wcd.x << sh : wcd.x >> -sh, xd = sh > 0 ? wcd.y << sh : wcd.y >> -sh;
+        for (int mt = 0; mt < 8; ++mt) {
+          const int k = mt & 3;
+          const uint32_t m = 0x00030003u << (2 * k);
+          const uint32_t a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
+          const uint32_t a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
+          const uint32_t a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
+          const uint32_t a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
 #pragma unroll
-          for (int odd = 0; odd < 2; ++odd) {
-            const int mt = 2 * i + odd;
-            const uint32_t m = odd ? 0x03000300u : 0x00C000C0u;
-            const uint32_t a0 = and_or(xa, m, kMagic);   // channel 16g + mt, tokens 2t, 2t+1
-            const uint32_t a1 = and_or(xb, m, kMagic);   // channel 16g + 8 + mt
-            const uint32_t a2 = and_or(xc, m, kMagic);   // tokens 2t + 8, 2t + 9
-            const uint32_t a3 = and_or(xd, m, kMagic);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
-          }
+          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
         }
-        // 1024 * (column sums of B), the constant part of every biased code, for the epilogue
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(bacc[nt], kMagic, kMagic, kMagic, kMagic, bf[nt][0], bf[nt][1]);
       }
     } else if (i == 0) {
       issue_rest();                    // page 0 was not requested (bad page id): the rest still is
@@ -421,13 +419,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       cl[w * 8 + head] = lsum[nt];
     }
     const float zs = grp ? zacc[nt][1] : zacc[nt][0];
-    const float bias0 = grp ? bacc[nt][1] : bacc[nt][0], bias1 = grp ? bacc[nt][3] : bacc[nt][2];
     float* dst = ca + (w * 8 + head) * kD;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const float inv_w = (mt & 1) ? 1.f / 256.f : 1.f / 64.f;      // codes were fed as 1024 + c * W
-      dst[16 * g + mt] = fmaf((grp ? acc[nt][mt][1] : acc[nt][mt][0]) - bias0, inv_w, zs);
-      dst[16 * g + 8 + mt] = fmaf((grp ? acc[nt][mt][3] : acc[nt][mt][2]) - bias1, inv_w, zs);
+      dst[16 * g + mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
+      dst[16 * g + 8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
     }
   }
   __syncthreads();

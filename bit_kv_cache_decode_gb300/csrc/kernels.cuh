@@ -7,6 +7,11 @@ namespace oscar {
 
 constexpr int kDefaultDecodeAlgo = OSCAR_DECODE_MMA;
 constexpr int kMaxMmaSplits = 2048;        // history splits of the fused decode
+// History pages one split of the tensor-core decode covers, at most (16 per
+// warp). The tensor cores' fp32 accumulation truncates instead of rounding, so
+// its error grows with the number of MMAs summed into one accumulator; longer
+// contexts take more splits, whose partials the merge adds with rounding.
+constexpr int kMaxPagesPerMmaSplit = 64;
 // partial slots per (request, q head): history splits, then one per BF16 page
 inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA

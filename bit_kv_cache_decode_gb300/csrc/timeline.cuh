@@ -13,11 +13,19 @@ enum TimelineKind : int {
 };
 
 // record i lives at timeline[4 + 4 i]: {kind | layer << 8 | sm << 24 | linear CTA << 32, start, end, mark};
-// timeline[0] counts the records claimed
+// timeline[0] counts the records claimed. The record address is kept in
+// shared memory (thread 0 reads it back), not in a register for the kernel's
+// whole life.
+__device__ __forceinline__ unsigned long long* volatile& timeline_slot() {
+  __shared__ unsigned long long* volatile slot;
+  return slot;
+}
+
 struct TimelineSpan {
-  unsigned long long* rec = nullptr;
   __device__ __forceinline__ TimelineSpan(const LayerView& lv, int kind) {
-    if (lv.timeline != nullptr && threadIdx.x == 0) {
+    if (threadIdx.x != 0) return;
+    unsigned long long* rec = nullptr;
+    if (lv.timeline != nullptr) {
       const unsigned long long i = atomicAdd(lv.timeline, 1ull);
       if (i < (unsigned long long)lv.timeline_cap) {
         const unsigned long long cta = blockIdx.x + gridDim.x * (blockIdx.y + (unsigned long long)gridDim.y * blockIdx.z);
@@ -28,12 +36,17 @@ struct TimelineSpan {
         rec[3] = 0;
       }
     }
+    timeline_slot() = rec;
   }
-  // an intermediate time of the kernel's choosing (the programmatic wait returning)
+  // an intermediate time of the kernel's choosing (the programmatic wait returning); thread 0 only
   __device__ __forceinline__ void mark() {
+    if (threadIdx.x != 0) return;
+    unsigned long long* rec = timeline_slot();
     if (rec != nullptr) rec[3] = global_ns();
   }
   __device__ __forceinline__ ~TimelineSpan() {
+    if (threadIdx.x != 0) return;
+    unsigned long long* rec = timeline_slot();
     if (rec != nullptr) rec[2] = global_ns();
   }
 };

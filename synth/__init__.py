@@ -28,6 +28,8 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass
 
+import functools
+
 import numpy as np
 
 HEAD_DIM = 128
@@ -72,6 +74,7 @@ class HeadStats:
     outliers: np.ndarray       # [N_OUTLIERS] channel indices
 
 
+@functools.lru_cache(maxsize=4096)
 def head_stats(seed: int, layer: int, head: int, d: int = HEAD_DIM) -> HeadStats:
     g = _rng(seed, layer, head, "basis").standard_normal((d, d))
     qm, rm = np.linalg.qr(g)

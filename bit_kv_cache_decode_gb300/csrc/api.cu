@@ -88,6 +88,50 @@ LayerView view(const oscar_cache* c, int layer) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// R = U H P_br (MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法"), composed in
+// double from the float32 U as loaded: (U H)[i][c] = sum_m U[i][m] (-1)^popcount(m & c) / sqrt(128), and
+// column j of R is column bitrev7(j) of U H. R is stored as fp16 hi = fp16(R), lo = fp16(R - hi)
+// (about 22 significant bits) in the B-fragment order of mma.m16n8k16 (k = input channel, n = rotated
+// channel): for k-block kb, n-tile nt and lane (g = lane / 4, t = lane % 4), b0 holds rows 16 kb + 2t,
+// +1 and b1 rows 16 kb + 2t + 8, +9, all of column 8 nt + g.
+void composite_rotation_fragments(const float* U, uint32_t* frag) {
+  std::vector<double> uh((size_t)kD * kD);
+  const double inv = 1.0 / std::sqrt((double)kD);
+  for (int i = 0; i < kD; ++i)
+    for (int c = 0; c < kD; ++c) {
+      double s = 0.0;
+      for (int m = 0; m < kD; ++m) s += (double)U[i * kD + m] * ((__builtin_popcount(m & c) & 1) ? -inv : inv);
+      uh[(size_t)i * kD + c] = s;
+    }
+  auto R = [&](int i, int j) {
+    int rj = 0;
+    for (int bit = 0; bit < 7; ++bit) rj |= ((j >> bit) & 1) << (6 - bit);
+    return uh[(size_t)i * kD + rj];
+  };
+  auto half_bits = [](double x) -> uint32_t {
+    const __half hv = __double2half(x);
+    return (uint32_t)__half_as_ushort(hv);
+  };
+  auto half_val = [](double x) -> double { return (double)__half2float(__double2half(x)); };
+  for (int kb = 0; kb < 8; ++kb)
+    for (int nt = 0; nt < 16; ++nt)
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3, col = 8 * nt + g;
+        const int rows[4] = {16 * kb + 2 * t, 16 * kb + 2 * t + 1, 16 * kb + 2 * t + 8, 16 * kb + 2 * t + 9};
+        uint32_t hi[4], lo[4];
+        for (int e = 0; e < 4; ++e) {
+          const double r = R(rows[e], col);
+          hi[e] = half_bits(r);
+          lo[e] = half_bits(r - half_val(r));
+        }
+        uint32_t* w = frag + (((size_t)kb * 16 + nt) * 32 + lane) * 4;
+        w[0] = hi[0] | (hi[1] << 16);
+        w[1] = hi[2] | (hi[3] << 16);
+        w[2] = lo[0] | (lo[1] << 16);
+        w[3] = lo[2] | (lo[3] << 16);
+      }
+}
+
 int g_configured = 0;
 
 int configure_once() {
@@ -250,11 +294,13 @@ int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float*
   for (int h = 0; h < hkv; ++h) {
     float* dst = host.data() + (size_t)h * kParamFloats;
     std::memcpy(dst + kUKOff, U_K + (size_t)h * kD * kD, kD * kD * sizeof(float));
+    composite_rotation_fragments(U_K + (size_t)h * kD * kD, reinterpret_cast<uint32_t*>(dst + kRKFragOff));
     if (U_V) {
       const float* u = U_V + (size_t)h * kD * kD;
       std::memcpy(dst + kUVOff, u, kD * kD * sizeof(float));
       for (int i = 0; i < kD; ++i)
         for (int j = 0; j < kD; ++j) dst[kUVtOff + j * kD + i] = u[i * kD + j];
+      if (expl) composite_rotation_fragments(u, reinterpret_cast<uint32_t*>(dst + kRVFragOff));
     }
     std::memcpy(dst + kTauKOff, tau_K + (size_t)h * kD, kD * sizeof(float));
     std::memcpy(dst + kTauVOff, tau_V + (size_t)h * kD, kD * sizeof(float));

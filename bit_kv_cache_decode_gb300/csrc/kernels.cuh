@@ -15,7 +15,6 @@ constexpr int kMaxPagesPerMmaSplit = 64;
 // partial slots per (request, q head): history splits, then one per BF16 page
 inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
-constexpr int kPrefillSmem = (kD * kD + 4 * 8 * kD) * 4;           // U + 4 warps x 8 staged rows
 constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;     // U + row + 4 partials + mbarrier
 constexpr int kQprepSmem = (kD * kD + 8 * kD + 8 * 8 * kD) * 4 + 64;   // U_K, 8 query rows, 8 x 8 partial rows, 8 mbarriers
 
@@ -52,6 +51,7 @@ int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, con
 int launch_append(const LayerView& lv, int B, const void* k, const void* v, const int* seq_lens_before,
                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
 int configure_write_path_kernels();
+int configure_prefill_kernel();   // prefill_mma.cu
 
 struct DecodeArgs {
   int B;

@@ -73,91 +73,6 @@ __global__ void k_rotate(LayerView lv, int kind, const __nv_bfloat16* __restrict
 }
 
 // ---------------------------------------------------------------------------
-// Bulk prefill. grid = (ceil(total / kPrefillTok), hkv, 2 kinds); block = 128 threads.
-// Each CTA stages U of (head, kind) in shared memory and handles kPrefillTok
-// consecutive tokens, 8 rows per warp pass. History rows are rotated (V only
-// in explicit mode), clipped, quantised and packed; sink and recent rows are
-// copied as bf16.
-__global__ void __launch_bounds__(128) k_prefill(LayerView lv, const __nv_bfloat16* __restrict__ k,
-                                                 const __nv_bfloat16* __restrict__ v,
-                                                 const int* __restrict__ cu_seqlens, int B, int total,
-                                                 const int* __restrict__ hist_pt, int max_hist_pages,
-                                                 const int* __restrict__ bf16_pt) {
-  TimelineSpan timeline_span(lv, kTlPrefill);
-  extern __shared__ __align__(16) float smem[];
-  float* Us = smem;                       // [128][128]
-  float* xs_all = smem + kD * kD;         // [4 warps][8 rows][128]
-  const int h = blockIdx.y, kind = blockIdx.z;
-  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool rotate = (kind == OSCAR_KIND_K) || lv.v_explicit;
-  const float* prm = lv.params + (size_t)h * kParamFloats;
-  if (rotate) {
-    const float4* src = reinterpret_cast<const float4*>(prm + (kind == OSCAR_KIND_K ? kUKOff : kUVOff));
-    float4* dst = reinterpret_cast<float4*>(Us);
-    for (int i = threadIdx.x; i < kD * kD / 4; i += blockDim.x) dst[i] = src[i];
-  }
-  __syncthreads();
-  const float* tau = prm + (kind == OSCAR_KIND_K ? kTauKOff : kTauVOff);
-  const __nv_bfloat16* src_all = (kind == OSCAR_KIND_K) ? k : v;
-  float* xs = xs_all + wib * 8 * kD;
-  const int bf16_per_req = (lv.sink + lv.recent) / kP;
-  const int tok0 = blockIdx.x * kPrefillTok;
-  const int tok1 = min(tok0 + kPrefillTok, total);
-  for (int base = tok0 + wib * 8; base < tok1; base += 4 * 8) {
-    // classify up to 8 rows; stage the history rows for rotation
-    int where[8];      // -1: nothing, 0: history, 1: bf16
-    int page[8], row[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      where[t] = -1; page[t] = 0; row[t] = 0;
-      const int g = base + t;
-      if (g >= tok1) continue;
-      int lo = 0, hi = B;                         // request r: cu[r] <= g < cu[r+1]
-      while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (cu_seqlens[mid] <= g) lo = mid; else hi = mid; }
-      const int r = lo, pos = g - cu_seqlens[r], L = cu_seqlens[r + 1] - cu_seqlens[r];
-      if (pos < lv.sink) {
-        page[t] = bf16_pt[r * bf16_per_req + pos / kP]; row[t] = pos % kP; where[t] = 1;
-      } else if (pos >= max(lv.sink, L - lv.recent)) {
-        const int slot = (pos - lv.sink) % lv.recent;
-        page[t] = bf16_pt[r * bf16_per_req + lv.sink / kP + slot / kP]; row[t] = slot % kP; where[t] = 1;
-      } else {
-        const int hh = pos - lv.sink;
-        if (hh / kP >= max_hist_pages) { if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN); continue; }
-        page[t] = hist_pt[r * max_hist_pages + hh / kP]; row[t] = hh % kP; where[t] = 0;
-      }
-      const int cap = where[t] == 0 ? lv.n_int2 : lv.n_bf16;
-      if (!valid_page(page[t], cap)) { if (lane == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE); where[t] = -1; }
-    }
-    bool any_hist = false;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const __nv_bfloat16* src = src_all + ((size_t)(base + t) * lv.hkv + h) * kD;
-      if (where[t] == 1) {
-        copy_row_bf16(src, bf16_row(lv, page[t], h, kind, row[t]));
-      } else if (where[t] == 0) {
-        load_row_f32(src, xs + t * kD);
-        any_hist = true;
-      }
-    }
-    if (!any_hist) continue;
-    __syncwarp();
-    float y[8][4];
-    if (rotate) {
-      warp_rotate<8>(Us, xs, y);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 8; ++t)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) y[t][r] = xs[t * kD + rot_channel(lane, r)];
-    }
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-      if (where[t] == 0) quantize_pack_row(y[t], tau, int2_block_w(lv, page[t], h), row[t], kind);
-    __syncwarp();
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Append one token per request with demotion. grid = (B, hkv, 2 kinds); block = 128.
 // The CTA stages U in shared memory by one bulk copy (when a demotion needs
 // it), rotates the demoted row with 4 warps each summing 32 rows of U, then
@@ -283,16 +198,6 @@ int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N,
   return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
-int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, const int* cu_seqlens, int total,
-                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st) {
-  if (total == 0 || B == 0) return OSCAR_OK;
-  dim3 grid((total + kPrefillTok - 1) / kPrefillTok, lv.hkv, 2);
-  k_prefill<<<grid, 128, kPrefillSmem, st>>>(lv, static_cast<const __nv_bfloat16*>(k),
-                                             static_cast<const __nv_bfloat16*>(v), cu_seqlens, B, total, hist_pt,
-                                             max_hist_pages, bf16_pt);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
-}
-
 int launch_append(const LayerView& lv, int B, const void* k, const void* v, const int* seq_lens_before,
                   const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st) {
   if (B == 0) return OSCAR_OK;
@@ -304,8 +209,7 @@ int launch_append(const LayerView& lv, int B, const void* k, const void* v, cons
 }
 
 int configure_write_path_kernels() {
-  if (cudaFuncSetAttribute(k_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem) != cudaSuccess)
-    return OSCAR_ERR_CUDA;
+  if (configure_prefill_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
   if (cudaFuncSetAttribute(k_append, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
   return OSCAR_OK;

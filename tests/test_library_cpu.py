@@ -60,8 +60,8 @@ def _bytes(osc, **kw):
 def test_layout_sizes(osc):
     rc, pb, wb = _bytes(osc)
     assert rc == 0
-    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V per kv head
-    per_layer = (10 * 8 * 5120) + (5 * 8 * 32768) + 8 * (3 * 128 * 128 + 2 * 128) * 4
+    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V, R_K and R_V fragments per kv head
+    per_layer = (10 * 8 * 5120) + (5 * 8 * 32768) + 8 * (5 * 128 * 128 + 2 * 128) * 4
     assert pb >= 2 * per_layer and pb < 2 * per_layer + 2 * 3 * 256
     parts = 2 * 32 * (16 + 5) * 132 * 4          # history splits + 5 BF16 chunks per (request, q head)
     assert wb >= parts

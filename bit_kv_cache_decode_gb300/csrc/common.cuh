@@ -31,7 +31,8 @@ constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D
 // rotation parameters per kv head (float32 words): U_K [D][D], U_V [D][D], U_V transposed [D][D]
 // (for coalesced reads of R_V^T in the merge), tau_K [D], tau_V [D], then the composite
 // rotations R_K = U_K H P_br and R_V (explicit-V mode) as fp16 high + low parts in tensor-core
-// B-fragment order for the prefill (kRFragWords 32-bit words each, see set_rotation)
+// B-fragment order for the prefill and the query prologue (kRFragWords 32-bit words each, see
+// set_rotation)
 constexpr int kRFragWords = 8 * 16 * 32 * 4;  // [k-block 8][n-tile 16][lane 32][hi b0, hi b1, lo b0, lo b1]
 constexpr int kUKOff = 0, kUVOff = kD * kD, kUVtOff = 2 * kD * kD, kTauKOff = 3 * kD * kD,
               kTauVOff = 3 * kD * kD + kD, kRKFragOff = 3 * kD * kD + 2 * kD, kRVFragOff = kRKFragOff + kRFragWords;

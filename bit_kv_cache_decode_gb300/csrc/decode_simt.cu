@@ -71,36 +71,36 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256: U_K arrives in
-// 8 bulk copies of 16 rows and warp w sums the rows of copy w for every query
-// head of the group as soon as that copy lands. Launched as a
-// programmatic dependent of the append kernel: it lets the decode kernel start
-// at once and waits for the append only before it exits.
-__global__ void __launch_bounds__(kQprepWarps * 32) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q,
+// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256: the composite
+// R_K fragments arrive in 8 bulk copies of one k-block each, and every warp
+// multiplies the group's query rows by its 16 rotated channels on the tensor
+// cores as the k-blocks land. Launched as a programmatic dependent of the
+// append kernel: it lets the decode kernel start at once and waits for the
+// append only before it exits.
+__global__ void __launch_bounds__(kQprepWarps * 32, 1) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q,
                                                             DecodeWorkspace ws, float scale_log2) {
   TimelineSpan timeline_span(lv, kTlQprep);
   extern __shared__ __align__(128) float smem[];
-  float* Us = smem;                              // [128][128]
-  float* xs = Us + kD * kD;                      // [8][128]: raw query rows, then rotated rows
-  float* part = xs + 8 * kD;                     // [kQprepWarps][8][128] partial rotations
-  const uint32_t bars = smem_addr(part + kQprepWarps * 8 * kD);
+  uint32_t* frag_s = reinterpret_cast<uint32_t*>(smem);   // [8 k-blocks][16 n-tiles][32 lanes][4]
+  float* xs = smem + kRFragWords;                          // [8][128]: raw query rows, then rotated rows
+  const uint32_t bars = smem_addr(xs + 8 * kD);
   __shared__ int sig[8];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int gq = lv.hq / lv.hkv;
   pdl_launch_dependents();
   if (tid == 0) {
-    // U_K in kQprepWarps chunks of 16 rows, one mbarrier each
-    const float* u = lv.params + (size_t)h * kParamFloats + kUKOff;
+    const float* f = lv.params + (size_t)h * kParamFloats + kRKFragOff;
     const uint64_t keep = l2_evict_last();
-    for (int c = 0; c < kQprepWarps; ++c) {
+    constexpr int chunk = kRFragWords / 8;                 // one k-block: 2,048 words
+    for (int c = 0; c < 8; ++c) {
       mbar_init(bars + 8 * c);
-      bulk_load_hint(smem_addr(Us + c * 16 * kD), u + c * 16 * kD, 16 * kD * 4, bars + 8 * c, keep);
+      bulk_load_hint(smem_addr(frag_s + c * chunk), f + c * chunk, chunk * 4, bars + 8 * c, keep);
     }
   }
   for (int i = tid; i < gq * kD; i += kQprepWarps * 32)
     xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
   __syncthreads();                               // barriers initialised, query rows staged
-  if (!qprep_rotate(lv, ws, Us, xs, part, sig, b, h, bars)) {
+  if (!qprep_rotate(lv, ws, frag_s, xs, sig, b, h, bars)) {
     if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
     mbar_wait(bars + 8 * (tid >> 5), 0);         // one more bounded wait for copies still in flight
     pdl_wait();

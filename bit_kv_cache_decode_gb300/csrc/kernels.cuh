@@ -16,7 +16,7 @@ constexpr int kMaxPagesPerMmaSplit = 64;
 inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
 constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;     // U + row + 4 partials + mbarrier
-constexpr int kQprepSmem = (kD * kD + 8 * kD + 8 * 8 * kD) * 4 + 64;   // U_K, 8 query rows, 8 x 8 partial rows, 8 mbarriers
+constexpr int kQprepSmem = (kRFragWords + 8 * kD) * 4 + 64;        // R_K fragments, 8 query rows, 8 mbarriers
 
 // Decode workspace carved from the caller's workspace buffer.
 struct DecodeWorkspace {

@@ -37,74 +37,97 @@ __device__ __forceinline__ float frag_round(float x) {
   return fabsf(r) < 6.103515625e-05f ? 0.f : r;
 }
 
-// Rotate the raw query rows xs[qi][0..127] (float, shared) of group (b, h)
-// with U (shared, row-major [128][128]), split over kQprepWarps warps: warp w
-// sums rows [16 w, 16 w + 16) of U for every head into part[w][qi][128]; after
-// a block barrier warp qi adds the kQprepWarps partial rows, applies the
-// Hadamard and bit-reversal stages and replaces row qi by q~ in rotated channel
-// order. q~ and its group sums go to the workspace, sigma of head qi to sig[qi].
-// Rows of U are used as they land: chunk w of the copy is waited on through
-// bars + 8 w. Returns false (block-uniform) when a chunk never landed.
+// Rotate the raw query rows xs[qi][0..127] (float, shared) of group (b, h) on
+// the tensor cores: q~ = q R_K with the composite R_K = U_K H P_br that the
+// host stored as fp16 high + low parts in mma.m16n8k16 B-fragment order
+// (frag_s, 64 KB; its 8 k-block chunks of 8 KB complete on mbarriers bars + 8 kb).
+// A = the query rows as fp16 (rows gq .. 15 zero), one fresh accumulator per
+// k-block, added in rounding fp32 (the tensor cores' accumulation truncates);
+// warp w takes n-tiles 2w and 2w + 1, i.e. rotated channels 16 w .. 16 w + 15.
+// Row qi of xs is then replaced by q~ in rotated channel order, q~ and its
+// group sums go to the workspace and sigma of head qi to sig[qi]. Returns false
+// (block-uniform) when a chunk never landed.
 constexpr int kQprepWarps = 8;
-__device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const float* Us,
-                                             float* xs, float* part, int* sig, int b, int h, uint32_t bars) {
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void qp_mma(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1,
+                                       bool zero_c) {
+  if (zero_c)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const uint32_t* frag_s,
+                                             float* xs, int* sig, int b, int h, uint32_t bars) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int gq = lv.hq / lv.hkv;
-  const bool landed = __syncthreads_and(mbar_wait(bars + 8 * w, 0));
-  if (!landed) return false;
-  float acc[8][4];
+  // A fragments: row g (query head g) of each k-block; rows 8..15 are zero
+  uint32_t a[8][2];
 #pragma unroll
-  for (int qi = 0; qi < 8; ++qi)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[qi][r] = 0.f;
-#pragma unroll 4
-  for (int i = 16 * w; i < 16 * w + 16; ++i) {
-    const float* row = Us + i * kD + lane;
-    const float u0 = row[0], u1 = row[32], u2 = row[64], u3 = row[96];
-#pragma unroll
-    for (int qi = 0; qi < 8; ++qi) {
-      if (qi < gq) {
-        const float xi = xs[qi * kD + i];
-        acc[qi][0] = fmaf(xi, u0, acc[qi][0]);
-        acc[qi][1] = fmaf(xi, u1, acc[qi][1]);
-        acc[qi][2] = fmaf(xi, u2, acc[qi][2]);
-        acc[qi][3] = fmaf(xi, u3, acc[qi][3]);
-      }
+  for (int kb = 0; kb < 8; ++kb) {
+    a[kb][0] = a[kb][1] = 0u;
+    if (g < gq) {
+      const float* x = xs + g * kD + 16 * kb + 2 * t;
+      const __half2 lo = __floats2half2_rn(x[0], x[1]), hi = __floats2half2_rn(x[8], x[9]);
+      a[kb][0] = *reinterpret_cast<const uint32_t*>(&lo);
+      a[kb][1] = *reinterpret_cast<const uint32_t*>(&hi);
     }
   }
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  bool landed = true;
 #pragma unroll
-  for (int qi = 0; qi < 8; ++qi)
-    if (qi < gq)
+  for (int kb = 0; kb < 8; ++kb) {
+    landed = landed && mbar_wait(bars + 8 * kb, 0);
+    if (!landed) break;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) part[(w * 8 + qi) * kD + lane + 32 * r] = acc[qi][r];
-  __syncthreads();                                  // all partial rows written, xs no longer read
-  for (int qi = w; qi < gq; qi += kQprepWarps) {
-    float y[4];
+    for (int j = 0; j < 2; ++j) {
+      const uint4 f = *reinterpret_cast<const uint4*>(frag_s + ((kb * 16 + 2 * w + j) * 32 + lane) * 4);
+      float d[4];
+      qp_mma(d, a[kb][0], a[kb][1], f.x, f.y, true);    // q R_hi
+      qp_mma(d, a[kb][0], a[kb][1], f.z, f.w, false);   // + q R_lo
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float v = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < kQprepWarps; ++ww) v += part[(ww * 8 + qi) * kD + lane + 32 * r];
-      y[r] = v;
+      for (int e = 0; e < 4; ++e) acc[j][e] += d[e];
     }
-    fwht128(y);
+  }
+  if (!__syncthreads_and(landed)) return false;        // every warp has also read its query rows
+  if (g < gq) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = 8 * (2 * w + j) + 2 * t;        // rotated channel
+      xs[g * kD + col] = acc[j][0];
+      xs[g * kD + col + 1] = acc[j][1];
+    }
+  }
+  __syncthreads();
+  for (int qi = w; qi < gq; qi += kQprepWarps) {
     const int hq = h * gq + qi;
     float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
-    float s = 0.f, mx = 0.f;
+    float y[4], s0 = 0.f, s1 = 0.f, mx = 0.f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const int ch = rot_channel(lane, r);
-      dst[ch] = y[r];
-      xs[qi * kD + ch] = y[r];
-      s += y[r];
+      y[r] = xs[qi * kD + lane + 32 * r];
+      dst[lane + 32 * r] = y[r];
       mx = fmaxf(mx, fabsf(y[r]));
     }
+    s0 = y[0] + y[1];                                   // channels 0..63: group 0
+    s1 = y[2] + y[3];
 #pragma unroll
-    for (int m = 2; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);   // lanes of equal parity = one group
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    if (lane < 2) ws.qconst[((size_t)b * lv.hq + hq) * kQConst + kQSum0 + lane] = s;
+    for (int m = 1; m < 32; m <<= 1) {
+      s0 += __shfl_xor_sync(0xffffffffu, s0, m);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, m);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    }
     if (lane == 0) {
+      float* qc = ws.qconst + ((size_t)b * lv.hq + hq) * kQConst;
+      qc[kQSum0] = s0;
+      qc[kQSum1] = s1;
       int e = 0;
       if (mx > 0.f && isfinite(mx)) frexpf(mx, &e);  // mx in [2^(e-1), 2^e)
       sig[qi] = min(max(12 - e, -60), 60);

@@ -72,6 +72,9 @@ LayerView view(const oscar_cache* c, int layer) {
   v.int2 = base;
   v.bf16 = base + c->int2_bytes;
   v.params = reinterpret_cast<const float*>(base + c->int2_bytes + c->bf16_bytes);
+  v.next_params = layer + 1 < c->lay.num_layers ? reinterpret_cast<const float*>(
+                                                      reinterpret_cast<const uint8_t*>(v.params) + c->layer_bytes)
+                                                : nullptr;
   v.n_int2 = c->lay.num_int2_pages;
   v.n_bf16 = c->lay.num_bf16_pages;
   v.hkv = c->lay.num_kv_heads;
@@ -330,8 +333,8 @@ int oscar_append_kv(oscar_cache* c, int layer, int B, const void* k, const void*
   if (B == 0) return OSCAR_OK;
   if (!k || !v || !seq_lens_before || !bf16_pt || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
-  return launch_append(view(c, layer), B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt,
-                       static_cast<cudaStream_t>(stream));
+  return launch_prologue(view(c, layer), DecodeWorkspace{}, B, nullptr, k, v, seq_lens_before, hist_pt,
+                         max_hist_pages, bf16_pt, 1.f, static_cast<cudaStream_t>(stream));
 }
 
 int oscar_set_decode_algo(oscar_cache* c, int algo) {
@@ -348,6 +351,7 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
   if (B == 0) return OSCAR_OK;
   if (!q || !seq_lens || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(q)) return OSCAR_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return OSCAR_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DecodeArgs a;
@@ -363,6 +367,7 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.lse = lse;
   a.algo = c->algo;
   a.len_add = 0;
+  a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   {
     int cps, align, extra, mpps;
@@ -388,7 +393,7 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   if (B == 0) return OSCAR_OK;
   if (!q || !k || !v || !seq_lens_before || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt))
     return OSCAR_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return OSCAR_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return OSCAR_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   LayerView lv = view(c, layer);
@@ -397,6 +402,7 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   a.q = q;
   a.seq_lens = seq_lens_before;
   a.len_add = 1;                         // attend over the appended token too
+  a.skip_qprep = 1;                      // the step prologue below rotates the queries
   a.hist_pt = hist_pt;
   a.max_hist_pages = max_hist_pages;
   a.bf16_pt = bf16_pt;
@@ -418,9 +424,10 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
     a.ev1 = c->prof_ev[2 * c->prof_n + 1];
     c->prof_n++;
   }
-  // append, then the decode chain (query prologue, decode, merge), each a
-  // programmatic dependent of the kernel before it
-  const int rc = launch_append(lv, B, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt, st);
+  // one prologue launch (append with demotion, and the query prologue), then the decode and the
+  // merge, each a programmatic dependent of the kernel before it
+  const int rc = launch_prologue(lv, c->dws, B, q, k, v, seq_lens_before, hist_pt, max_hist_pages, bf16_pt,
+                                 sm_scale, st);
   if (rc != OSCAR_OK) return rc;
   return launch_decode(lv, c->dws, a, st);
 }
@@ -552,6 +559,7 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
   out->int2 = base;
   out->bf16 = base + int2b;
   out->params = reinterpret_cast<const float*>(base + int2b + bf16b);
+  out->next_params = nullptr;
   out->n_int2 = L->num_int2_pages;
   out->n_bf16 = L->num_bf16_pages;
   out->hkv = L->num_kv_heads;

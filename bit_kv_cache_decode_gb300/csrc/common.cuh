@@ -46,6 +46,7 @@ struct LayerView {
   uint8_t* int2;          // [n_int2][hkv][kBlockBytes]
   uint8_t* bf16;          // [n_bf16][hkv][kBf16BlockBytes]
   const float* params;    // [hkv][kParamFloats]
+  const float* next_params;   // the next layer's parameters (prefetched into L2 by the prologue), or null
   int n_int2, n_bf16, hkv, hq, sink, recent, v_explicit;
   int* status;            // device status word
   int layer;              // layer index (timeline records only)

@@ -58,6 +58,7 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
   if (B == 0) return OSCAR_OK;
   if (!q || !seq_lens || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q) % 16) return OSCAR_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || sm_scale == INFINITY) return OSCAR_ERR_INVALID_ARG;
   LayerView lv;
   int rc = pool_layer_view(layout, pool, layer, nullptr, &lv);
@@ -108,6 +109,7 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.lse = lse;
   a.algo = kDefaultDecodeAlgo;
   a.len_add = 0;
+  a.skip_qprep = 0;
   a.ev0 = a.ev1 = nullptr;
   a.nbf = nbf;
   decode_split_policy(B, (int)hkv, (int)(hq / hkv), nbf, max_hist_pages, max_splits, sms, a.algo, &a.nsplit,

@@ -18,7 +18,6 @@
 #include "rotate.cuh"
 #include "tma.cuh"
 #include "timeline.cuh"
-#include "qprep.cuh"
 
 namespace oscar {
 
@@ -71,47 +70,6 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Query prologue (see qprep.cuh). grid = (hkv, B), block = 256: the composite
-// R_K fragments arrive in 8 bulk copies of one k-block each, and every warp
-// multiplies the group's query rows by its 16 rotated channels on the tensor
-// cores as the k-blocks land. Launched as a programmatic dependent of the
-// append kernel: it lets the decode kernel start at once and waits for the
-// append only before it exits.
-__global__ void __launch_bounds__(kQprepWarps * 32, 1) k_qprep(LayerView lv, const __nv_bfloat16* __restrict__ q,
-                                                            DecodeWorkspace ws, float scale_log2) {
-  TimelineSpan timeline_span(lv, kTlQprep);
-  extern __shared__ __align__(128) float smem[];
-  uint32_t* frag_s = reinterpret_cast<uint32_t*>(smem);   // [8 k-blocks][16 n-tiles][32 lanes][4]
-  float* xs = smem + kRFragWords;                          // [8][128]: raw query rows, then rotated rows
-  const uint32_t bars = smem_addr(xs + 8 * kD);
-  __shared__ int sig[8];
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
-  const int gq = lv.hq / lv.hkv;
-  pdl_launch_dependents();
-  if (tid == 0) {
-    const float* f = lv.params + (size_t)h * kParamFloats + kRKFragOff;
-    const uint64_t keep = l2_evict_last();
-    constexpr int chunk = kRFragWords / 8;                 // one k-block: 2,048 words
-    for (int c = 0; c < 8; ++c) {
-      mbar_init(bars + 8 * c);
-      bulk_load_hint(smem_addr(frag_s + c * chunk), f + c * chunk, chunk * 4, bars + 8 * c, keep);
-    }
-  }
-  for (int i = tid; i < gq * kD; i += kQprepWarps * 32)
-    xs[i] = __bfloat162float(q[((size_t)b * lv.hq + h * gq) * kD + i]);
-  __syncthreads();                               // barriers initialised, query rows staged
-  if (!qprep_rotate(lv, ws, frag_s, xs, sig, b, h, bars)) {
-    if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
-    mbar_wait(bars + 8 * (tid >> 5), 0);         // one more bounded wait for copies still in flight
-    pdl_wait();
-    return;
-  }
-  __syncthreads();
-  qprep_finish(lv, ws, xs, sig, b, h, scale_log2, kQprepWarps);
-  timeline_span.mark();
-  pdl_wait();                                    // the decode kernel waits on this grid, and through it on the append
-}
-
 // ---------------------------------------------------------------------------
 // INT2 history, CUDA cores. grid = (nsplit, hkv, B), block = 128.
 // A CTA walks its range of history pages; per 64-token page it computes the
@@ -395,19 +353,10 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
 template <int GQ>
 static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st) {
   const float scale_log2 = a.sm_scale * kLog2e;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(lv.hkv, a.B);
-    cfg.blockDim = dim3(kQprepWarps * 32);
-    cfg.dynamicSmemBytes = kQprepSmem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_qprep, lv, static_cast<const __nv_bfloat16*>(a.q), ws, scale_log2) != cudaSuccess)
-      return OSCAR_ERR_CUDA;
+  if (!a.skip_qprep) {
+    const int rc = launch_prologue(lv, ws, a.B, a.q, nullptr, nullptr, a.seq_lens, a.hist_pt, a.max_hist_pages,
+                                   a.bf16_pt, a.sm_scale, st);
+    if (rc != OSCAR_OK) return rc;
   }
   if (a.algo == OSCAR_DECODE_MMA) {
     // one fused launch (history splits and BF16 pages), then the merge kernel; the profiled
@@ -468,8 +417,6 @@ int configure_mma_kernels();   // decode_mma.cu
 
 int configure_decode_kernels() {
   if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
-  cudaError_t e = cudaFuncSetAttribute(k_qprep, cudaFuncAttributeMaxDynamicSharedMemorySize, kQprepSmem);
-  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   return OSCAR_OK;
 }
 

@@ -15,8 +15,6 @@ constexpr int kMaxPagesPerMmaSplit = 64;
 // partial slots per (request, q head): history splits, then one per BF16 page
 inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA
-constexpr int kAppendSmem = (kD * kD + kD + 4 * kD) * 4 + 16;     // U + row + 4 partials + mbarrier
-constexpr int kQprepSmem = (kRFragWords + 8 * kD) * 4 + 64;        // R_K fragments, 8 query rows, 8 mbarriers
 
 // Decode workspace carved from the caller's workspace buffer.
 struct DecodeWorkspace {
@@ -48,8 +46,12 @@ int launch_pack_rotated(const LayerView& lv, int kind, const float* xrot, const 
 int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N, cudaStream_t st);
 int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, const int* cu_seqlens, int total,
                    const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
-int launch_append(const LayerView& lv, int B, const void* k, const void* v, const int* seq_lens_before,
-                  const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
+// Append (k, v non-null: new tokens, demotion) and / or the decode's query prologue (q non-null) in one
+// launch, a programmatic dependent of the kernel before it (prologue.cu).
+int launch_prologue(const LayerView& lv, const DecodeWorkspace& ws, int B, const void* q, const void* k,
+                    const void* v, const int* seq_lens_before, const int* hist_pt, int max_hist_pages,
+                    const int* bf16_pt, float sm_scale, cudaStream_t st);
+int configure_prologue_kernel();
 int configure_write_path_kernels();
 int configure_prefill_kernel();   // prefill_mma.cu
 
@@ -69,6 +71,7 @@ struct DecodeArgs {
   int pages_per_split;
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
+  int skip_qprep;        // the query prologue already ran (with the append, in one launch)
   cudaEvent_t ev0, ev1;  // optional events around the history (fused decode) kernel, may be null
 };
 

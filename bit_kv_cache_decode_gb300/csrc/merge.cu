@@ -10,7 +10,8 @@
 // After the grid it depends on has finished, the merge costs one
 // load round trip per chunk.
 //
-// The kernel must not trigger its dependents early: the next decode call reuses the slots.
+// The kernel triggers its dependents only after its wait: a later decode reuses the slots, and the
+// chain append -> prologue -> decode lets that decode start only after this grid has finished.
 //
 // History slots hold attention over the stored (rotated) value basis. In
 // explicit-V mode their combination is multiplied by R_V^T = P_br H U_V^T
@@ -93,6 +94,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, Decode
   __syncthreads();
   pdl_wait();                                       // the partials are written by the preceding grid
   timeline_span.mark();
+  // The decode grid is complete: the next kernel (typically the next layer's append, which itself waits
+  // for this grid before it starts work) may be scheduled now.
+  pdl_launch_dependents();
   const float* row0 = ws.partials + ((size_t)b * lv.hq + hq) * ws.nslots * kPartFloats;
   const int nslot = nsplit + nbfs;
 

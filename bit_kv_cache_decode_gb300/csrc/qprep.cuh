@@ -37,48 +37,54 @@ __device__ __forceinline__ float frag_round(float x) {
   return fabsf(r) < 6.103515625e-05f ? 0.f : r;
 }
 
-// Rotate the raw query rows xs[qi][0..127] (float, shared) of group (b, h) on
-// the tensor cores: q~ = q R_K with the composite R_K = U_K H P_br that the
-// host stored as fp16 high + low parts in mma.m16n8k16 B-fragment order
-// (frag_s, 64 KB; its 8 k-block chunks of 8 KB complete on mbarriers bars + 8 kb).
-// A = the query rows as fp16 (rows gq .. 15 zero), one fresh accumulator per
-// k-block, added in rounding fp32 (the tensor cores' accumulation truncates);
-// warp w takes n-tiles 2w and 2w + 1, i.e. rotated channels 16 w .. 16 w + 15.
-// Row qi of xs is then replaced by q~ in rotated channel order, q~ and its
-// group sums go to the workspace and sigma of head qi to sig[qi]. Returns false
-// (block-uniform) when a chunk never landed.
-constexpr int kQprepWarps = 8;
-__device__ __forceinline__ void qp_mma(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1,
-                                       bool zero_c) {
+// One 16-row tile of fp32 rows (smem, [16][kTileStride], rows[i * kTileStride + c]) times the
+// composite rotation R = U H P_br on the tensor cores. R arrives in shared
+// memory as fp16 high + low parts in mma.m16n8k16 B-fragment order (frag_s,
+// 64 KB, its 8 k-block chunks of 8 KB completing on mbarriers bars + 8 kb).
+// A = the rows as fp16; one fresh accumulator per k-block, added in rounding
+// fp32 (the tensor cores' accumulation truncates). Warp w of 8 takes n-tiles 2w
+// and 2w + 1, i.e. rotated channels 16 w .. 16 w + 15. On return (after a block
+// barrier) every row of `rows` holds its rotation in rotated channel order.
+// Returns false (block-uniform) when a chunk never landed; rows are then
+// unchanged.
+constexpr int kPrologueWarps = 8;
+__device__ __forceinline__ void qp_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1, bool zero_c) {
   if (zero_c)
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%10,%10,%10};\n"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
   else
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWorkspace& ws, const uint32_t* frag_s,
-                                             float* xs, int* sig, int b, int h, uint32_t bars) {
+// Row stride of the fp32 tiles: 136 floats makes the 64-bit fragment loads of
+// rows g = 0..7 (stride 68 eight-byte words, 68 = 4 mod 16) conflict-free.
+constexpr int kTileStride = kD + 8;
+
+__device__ __forceinline__ uint32_t f16x2_of(const float* x) {
+  const float2 p = *reinterpret_cast<const float2*>(x);
+  const __half2 v = __floats2half2_rn(p.x, p.y);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ bool rotate_tile16(const uint32_t* frag_s, float* rows, uint32_t bars) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int gq = lv.hq / lv.hkv;
-  // A fragments: row g (query head g) of each k-block; rows 8..15 are zero
-  uint32_t a[8][2];
+  uint32_t a[8][4];
 #pragma unroll
   for (int kb = 0; kb < 8; ++kb) {
-    a[kb][0] = a[kb][1] = 0u;
-    if (g < gq) {
-      const float* x = xs + g * kD + 16 * kb + 2 * t;
-      const __half2 lo = __floats2half2_rn(x[0], x[1]), hi = __floats2half2_rn(x[8], x[9]);
-      a[kb][0] = *reinterpret_cast<const uint32_t*>(&lo);
-      a[kb][1] = *reinterpret_cast<const uint32_t*>(&hi);
-    }
+    const float* r0 = rows + g * kTileStride + 16 * kb + 2 * t;
+    const float* r8 = rows + (g + 8) * kTileStride + 16 * kb + 2 * t;
+    a[kb][0] = f16x2_of(r0);           // row g, channels 16 kb + 2t, +1
+    a[kb][1] = f16x2_of(r8);           // row g + 8
+    a[kb][2] = f16x2_of(r0 + 8);       // row g, channels 16 kb + 2t + 8, +9
+    a[kb][3] = f16x2_of(r8 + 8);
   }
   float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
   bool landed = true;
@@ -90,34 +96,41 @@ __device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWo
     for (int j = 0; j < 2; ++j) {
       const uint4 f = *reinterpret_cast<const uint4*>(frag_s + ((kb * 16 + 2 * w + j) * 32 + lane) * 4);
       float d[4];
-      qp_mma(d, a[kb][0], a[kb][1], f.x, f.y, true);    // q R_hi
-      qp_mma(d, a[kb][0], a[kb][1], f.z, f.w, false);   // + q R_lo
+      qp_mma(d, a[kb][0], a[kb][1], a[kb][2], a[kb][3], f.x, f.y, true);    // x R_hi
+      qp_mma(d, a[kb][0], a[kb][1], a[kb][2], a[kb][3], f.z, f.w, false);   // + x R_lo
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[j][e] += d[e];
     }
   }
-  if (!__syncthreads_and(landed)) return false;        // every warp has also read its query rows
-  if (g < gq) {
+  if (!__syncthreads_and(landed)) return false;        // also: every warp has read its A rows
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int col = 8 * (2 * w + j) + 2 * t;        // rotated channel
-      xs[g * kD + col] = acc[j][0];
-      xs[g * kD + col + 1] = acc[j][1];
-    }
+  for (int j = 0; j < 2; ++j) {
+    const int col = 8 * (2 * w + j) + 2 * t;            // rotated channel
+    *reinterpret_cast<float2*>(rows + g * kTileStride + col) = make_float2(acc[j][0], acc[j][1]);
+    *reinterpret_cast<float2*>(rows + (g + 8) * kTileStride + col) = make_float2(acc[j][2], acc[j][3]);
   }
   __syncthreads();
-  for (int qi = w; qi < gq; qi += kQprepWarps) {
+  return true;
+}
+
+// Per query head qi of group (b, h) (warp w takes heads w, w + nwarps, ...):
+// q~ (xs[qi * stride + 0..127], rotated channel order) goes to the workspace with its
+// group sums, and sig[qi] = sigma, the power of two that brings max|q~| near 2^12.
+__device__ __forceinline__ void qprep_stats(const LayerView& lv, const DecodeWorkspace& ws, const float* xs,
+                                            int stride, int* sig, int b, int h, int nwarps) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lv.hq / lv.hkv;
+  for (int qi = w; qi < gq; qi += nwarps) {
     const int hq = h * gq + qi;
     float* dst = ws.qrot + ((size_t)b * lv.hq + hq) * kD;
-    float y[4], s0 = 0.f, s1 = 0.f, mx = 0.f;
+    float y[4], mx = 0.f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      y[r] = xs[qi * kD + lane + 32 * r];
+      y[r] = xs[qi * stride + lane + 32 * r];
       dst[lane + 32 * r] = y[r];
       mx = fmaxf(mx, fabsf(y[r]));
     }
-    s0 = y[0] + y[1];                                   // channels 0..63: group 0
-    s1 = y[2] + y[3];
+    float s0 = y[0] + y[1], s1 = y[2] + y[3];           // channels 0..63: group 0
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
       s0 += __shfl_xor_sync(0xffffffffu, s0, m);
@@ -133,23 +146,27 @@ __device__ __forceinline__ bool qprep_rotate(const LayerView& lv, const DecodeWo
       sig[qi] = min(max(12 - e, -60), 60);
     }
   }
-  return true;
 }
 
-// After qprep_rotate and a block barrier: per-head constants (warp w handles
-// heads w, w + nwarps, ...; lane l owns channels 4l .. 4l + 3) and the
-// fragments (all threads of the block).
+// 2^e for |e| < 126, built from its bits
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// After qprep_stats and a barrier of the participating warps 0 .. nwarps-1:
+// per-head constants (warp w handles heads w, w + nwarps, ...; lane l owns
+// channels 4l .. 4l + 3) and the fragments (all participating threads). q~ of
+// head qi is xs[qi * stride + 0..127].
 __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWorkspace& ws, const float* xs,
-                                             const int* sig, int b, int h, float scale_log2, int nwarps) {
+                                             int stride, const int* sig, int b, int h, float scale_log2,
+                                             int nwarps) {
   const int tid = threadIdx.x, wib = tid >> 5, lane = tid & 31;
   const int gq = lv.hq / lv.hkv;
   for (int qi = wib; qi < gq; qi += nwarps) {
-    const float sc = ldexpf(1.f, sig[qi]);
+    const float sc = pow2i(sig[qi]);
     float offh = 0.f, offl = 0.f, sum = 0.f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e, fragment scale 1 / W = 2^-(6 + 2 (e & 1))
-      const float v = xs[qi * kD + 4 * lane + e];
-      const float x = v * sc * ldexpf(1.f, -6 - 2 * (e & 1));
+      const float v = xs[qi * stride + 4 * lane + e];
+      const float x = v * sc * pow2i(-6 - 2 * (e & 1));
       const float hi = frag_round(x);
       offh += hi;
       offl += frag_round(x - hi);
@@ -169,7 +186,7 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
       qc[g ? kQOff1L : kQOff0L] = 1024.f * offl;
     }
     if (lane == 0) {
-      qc[kQF] = scale_log2 * ldexpf(1.f, -sig[qi]);
+      qc[kQF] = scale_log2 * pow2i(-sig[qi]);
       qc[kQSigma] = (float)sig[qi];
     }
   }
@@ -182,9 +199,9 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
     uint32_t word = 0;
     if (nt < nt_count && head < gq) {
       // r = 0: channels (c0, c0 + 8), even, W = 64; r = 1: (c0 + 1, c0 + 9), odd, W = 256
-      const float sc = ldexpf(1.f, sig[head] - 6 - 2 * r);
+      const float sc = pow2i(sig[head] - 6 - 2 * r);
       const int c0 = 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;
-      float x[2] = {xs[head * kD + c0] * sc, xs[head * kD + c0 + 8] * sc};
+      float x[2] = {xs[head * stride + c0] * sc, xs[head * stride + c0 + 8] * sc};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float hi = frag_round(x[e]);

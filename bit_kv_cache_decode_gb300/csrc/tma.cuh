@@ -42,6 +42,12 @@ __device__ __forceinline__ uint64_t l2_evict_last() {
   return p;
 }
 
+// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2 with a cache policy.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 // bulk_load with an L2 cache policy from l2_evict_first / l2_evict_last
 __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                                uint64_t policy) {

@@ -182,7 +182,7 @@ int oscar_append_kv(oscar_cache* cache, int layer, int B, const void* k, const v
 /* Decode attention for one query token per request (news article, "OSCAR 的设计
  * 思路": BF16 segment and INT2 segment computed separately, combined by an
  * online-softmax merge).
- *  q        : device bf16 [B][Hq][128]; query head i reads kv head i/(Hq/Hkv)
+ *  q        : device bf16 [B][Hq][128], 16-byte aligned; query head i reads kv head i/(Hq/Hkv)
  *  seq_lens : device int32 [B], lengths including the current token (>= 1)
  *  sm_scale : softmax scale (1/sqrt(128) for standard attention)
  *  out      : device [B][Hq][128], bf16 or fp32 per out_dtype. In V-absorbed
@@ -197,11 +197,13 @@ int oscar_decode_attention(oscar_cache* cache, int layer, int B, const void* q, 
 /* One decode step of a layer: oscar_append_kv(k, v at position
  * seq_lens_before[r]) followed by oscar_decode_attention(q) over
  * seq_lens_before[r] + 1 tokens, with the same arguments, layouts and
- * results as those two calls, issued as one chain: the append, then the
- * query prologue, the decode kernel and the merge, each launched as a
- * programmatic dependent of the one before it. The prologue runs while
- * the append does, and the decode kernel prefetches history pages that the
- * append cannot touch before it waits. */
+ * results as those two calls, issued as one chain of three launches, each a
+ * programmatic dependent of the one before it: one step prologue (per
+ * request, kv head and K / V: the demoted row, and for K the query rows, are
+ * rotated together on the tensor cores; the demoted row is quantised into
+ * the history, the queries become the decode's fragments, the new token goes
+ * to its ring slot), the decode kernel and the merge. The decode kernel
+ * prefetches history pages the append cannot touch before it waits. */
 int oscar_decode_step(oscar_cache* cache, int layer, int B, const void* q, const void* k, const void* v,
                       const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
                       const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream);
@@ -331,10 +333,12 @@ int oscar_trace_ctas(oscar_cache* cache, void* buf, int capacity);
  * buf[4 + 4 i .. 4 + 4 i + 3] = {kind | layer << 8 | SM << 24 | linear CTA
  * index << 32, start, end, mark}, times in %globaltimer nanoseconds, taken by
  * thread 0 on entry and when it leaves the kernel; mark is, for the merge, the
- * time its wait for the decode kernel returned and, for the query prologue,
- * the time its work was done (before it waits for the append), else 0. Kinds: 1 append, 2 query
- * prologue, 3 tensor-core decode, 4 merge, 5 CUDA-core history decode,
- * 6 BF16 segment, 7 prefill. Launches issued while a buffer is set keep
+ * time its wait for the decode kernel returned and, for the step prologue,
+ * the time its rotation was done, else 0. Kinds: 1 step prologue
+ * with an append (oscar_append_kv, or append + query prologue in
+ * oscar_decode_step), 2 query prologue alone (oscar_decode_attention),
+ * 3 tensor-core decode, 4 merge, 5 CUDA-core history decode, 6 BF16 segment,
+ * 7 prefill. Launches issued while a buffer is set keep
  * writing to it, also from CUDA graphs captured meanwhile; NULL stops
  * recording for later launches. */
 int oscar_trace_timeline(oscar_cache* cache, void* buf, int capacity);

@@ -174,7 +174,7 @@ void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int c
 
 void algo_policy(int algo, int gq, int nbf, int* ctas_per_sm, int* align, int* extra, int* max_pps) {
   if (algo == OSCAR_DECODE_MMA) {
-    *ctas_per_sm = gq <= 4 ? 4 : 2; *align = 4; *extra = nbf; *max_pps = kMaxPagesPerMmaSplit;
+    *ctas_per_sm = gq <= 4 ? 3 : 2; *align = 4; *extra = nbf; *max_pps = kMaxPagesPerMmaSplit;
   } else {
     *ctas_per_sm = 4; *align = 1; *extra = 0; *max_pps = 0;
   }

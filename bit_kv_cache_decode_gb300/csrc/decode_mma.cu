@@ -552,7 +552,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
 
 // grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
 template <int NT>
-__global__ void __launch_bounds__(128, NT == 1 ? 4 : 2) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
+__global__ void __launch_bounds__(128, NT == 1 ? 3 : 2) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
   TimelineSpan timeline_span(lv, kTlDecodeMma);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);

@@ -5,10 +5,11 @@
 //
 // grid = (Hq, B), block = 256: one CTA per (request, query head). The head's
 // slot rows are contiguous in the workspace, so they arrive in shared memory
-// by bulk copies of up to kMergeChunk slots. A chunk is then combined there:
-// warp w takes slots w, w + 8, ..., lane l owns channels 4l .. 4l + 3.
-// After the grid it depends on has finished, the merge costs one
-// load round trip per chunk.
+// by bulk copies of up to kMergeChunk slots. A chunk is then combined by block
+// reductions: the maxima per part, one weight per slot (one thread each), the
+// l sums, and per output channel one pass over the slots (two threads per
+// channel, one half of the slots each). After the grid it depends on has
+// finished, the merge costs one load round trip per chunk.
 //
 // The kernel triggers its dependents only after its wait: a later decode reuses the slots, and the
 // chain append -> prologue -> decode lets that decode start only after this grid has finished.
@@ -28,64 +29,48 @@ namespace {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWarps = kMergeThreads / 32;
 
-// Fold slots [lo, hi) of the staged chunk (first slot c0) that belong to warp w
-// (s = w mod kMergeWarps) into the warp's running (M, L, A); lane l owns
-// channels 4l .. 4l + 3.
-__device__ __forceinline__ void combine_part(const float* sbuf, int c0, int lo, int hi, int w, int lane, float& M,
-                                             float& L, float4& A) {
-  if (lo >= hi) return;
-  const int first = lo + ((w - lo) % kMergeWarps + kMergeWarps) % kMergeWarps;
-  float mx = -INFINITY;
-  for (int s = first; s < hi; s += kMergeWarps) mx = fmaxf(mx, sbuf[(s - c0) * kPartFloats]);
-  if (mx == -INFINITY) return;
-  const float Mn = fmaxf(M, mx);
-  const float r = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
-  L *= r;
-  A.x *= r; A.y *= r; A.z *= r; A.w *= r;
-  for (int s = first; s < hi; s += kMergeWarps) {
-    const float* row = sbuf + (s - c0) * kPartFloats;
-    const float m = row[0];
-    if (m == -INFINITY) continue;
-    const float wgt = exp2f(m - Mn);
-    const float4 a = reinterpret_cast<const float4*>(row + 4)[lane];
-    L = fmaf(row[1], wgt, L);
-    A.x = fmaf(a.x, wgt, A.x);
-    A.y = fmaf(a.y, wgt, A.y);
-    A.z = fmaf(a.z, wgt, A.z);
-    A.w = fmaf(a.w, wgt, A.w);
-  }
-  M = Mn;
+// 2^x with the SFU (x <= 0 or -inf here)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-// Combine the warps' (M, L, A[c]) of one part; M (the maximum over all warps) is
-// the same in every thread, -inf when the part has no live slot.
-__device__ __forceinline__ void combine_warps(const float* sm, const float* sl, const float (*sa)[kD], int c,
-                                              float& M, float& L, float& A) {
-  M = -INFINITY;
-  L = A = 0.f;
+// Block-wide max (op 0) or sum (op 1) of two values; every thread gets the results.
+template <int OP>
+__device__ __forceinline__ float2 block_reduce2(float2 v, float2* red) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < kMergeWarps; ++i) M = fmaxf(M, sm[i]);
-  if (M == -INFINITY) return;
-#pragma unroll
-  for (int i = 0; i < kMergeWarps; ++i) {
-    if (sm[i] == -INFINITY) continue;
-    const float f = exp2f(sm[i] - M);
-    L = fmaf(sl[i], f, L);
-    if (c < kD) A = fmaf(sa[i][c], f, A);
+  for (int x = 16; x > 0; x >>= 1) {
+    const float a = __shfl_xor_sync(0xffffffffu, v.x, x), b = __shfl_xor_sync(0xffffffffu, v.y, x);
+    v.x = OP == 0 ? fmaxf(v.x, a) : v.x + a;
+    v.y = OP == 0 ? fmaxf(v.y, b) : v.y + b;
   }
+  __syncthreads();                                  // red[] free from its previous use
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float2 r = red[0];
+#pragma unroll
+  for (int i = 1; i < kMergeWarps; ++i) {
+    r.x = OP == 0 ? fmaxf(r.x, red[i].x) : r.x + red[i].x;
+    r.y = OP == 0 ? fmaxf(r.y, red[i].y) : r.y + red[i].y;
+  }
+  return r;
 }
 
 __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, DecodeWorkspace ws, int nsplit, int nbfs,
-                                                         void* out, int out_dtype, float* lse) {
+                                                            void* out, int out_dtype, float* lse) {
   TimelineSpan timeline_span(lv, kTlMerge);
   extern __shared__ __align__(128) float sbuf[];            // [kMergeChunk][kPartFloats]
   __shared__ __align__(8) uint64_t bar_mem;
-  __shared__ float sm[2][kMergeWarps], sl[2][kMergeWarps];
-  __shared__ __align__(16) float sa[2][kMergeWarps][kD];
+  __shared__ float2 red[kMergeWarps];
+  __shared__ float wts[kMergeChunk];
+  __shared__ float ahalf[2][kD];
   __shared__ float zbuf[kD];
   __shared__ int landed;
   const int hq = blockIdx.x, b = blockIdx.y;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int c = tid & (kD - 1), half = tid >> 7;            // output channel, slot half of this thread
   const uint32_t bar = smem_addr(&bar_mem);
   if (tid == 0) {
     mbar_init(bar);
@@ -94,15 +79,15 @@ __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, Decode
   __syncthreads();
   pdl_wait();                                       // the partials are written by the preceding grid
   timeline_span.mark();
-  // The decode grid is complete: the next kernel (typically the next layer's append, which itself waits
+  // The decode grid is complete: the next kernel (typically the next layer's prologue, which itself waits
   // for this grid before it starts work) may be scheduled now.
   pdl_launch_dependents();
   const float* row0 = ws.partials + ((size_t)b * lv.hq + hq) * ws.nslots * kPartFloats;
   const int nslot = nsplit + nbfs;
 
-  // per warp and part (history h, BF16 f): running (M, L, A) with L, A relative to 2^M
-  float Mh = -INFINITY, Lh = 0.f, Mf = -INFINITY, Lf = 0.f;
-  float4 Ah = make_float4(0.f, 0.f, 0.f, 0.f), Af = make_float4(0.f, 0.f, 0.f, 0.f);
+  // running state per part (x: history slots, y: BF16 slots): M and L are block-uniform, A is this
+  // thread's channel c summed over its half of the slots; L and A are relative to 2^M
+  float2 M = make_float2(-INFINITY, -INFINITY), L = make_float2(0.f, 0.f), A = make_float2(0.f, 0.f);
   uint32_t phase = 0;
   for (int c0 = 0; c0 < nslot; c0 += kMergeChunk) {
     const int n = min(kMergeChunk, nslot - c0);
@@ -116,53 +101,71 @@ __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, Decode
       break;
     }
     phase ^= 1u;
-    combine_part(sbuf, c0, c0, min(c0 + n, nsplit), w, lane, Mh, Lh, Ah);       // history slots
-    combine_part(sbuf, c0, max(c0, nsplit), c0 + n, w, lane, Mf, Lf, Af);       // BF16 slots
-    __syncthreads();                                // chunk consumed before the buffer is refilled
+    // 1. the chunk's maxima per part; rescale the running state
+    const bool mine = tid < n;
+    const bool hist = c0 + tid < nsplit;
+    const float m = mine ? sbuf[tid * kPartFloats] : -INFINITY;
+    const float2 cm = block_reduce2<0>(make_float2(hist ? m : -INFINITY, hist ? -INFINITY : m), red);
+    const float2 Mn = make_float2(fmaxf(M.x, cm.x), fmaxf(M.y, cm.y));
+    const float2 r = make_float2(M.x == -INFINITY ? 0.f : ex2(M.x - Mn.x), M.y == -INFINITY ? 0.f : ex2(M.y - Mn.y));
+    L = make_float2(L.x * r.x, L.y * r.y);
+    A = make_float2(A.x * r.x, A.y * r.y);
+    M = Mn;
+    // 2. one weight per slot, and the chunk's l sums
+    float wt = 0.f;
+    if (mine && m != -INFINITY) wt = ex2(m - (hist ? M.x : M.y));
+    if (tid < kMergeChunk) wts[tid] = wt;
+    const float lw = mine ? sbuf[tid * kPartFloats + 1] * wt : 0.f;
+    const float2 cl = block_reduce2<1>(make_float2(hist ? lw : 0.f, hist ? 0.f : lw), red);   // also publishes wts
+    L = make_float2(L.x + cl.x, L.y + cl.y);
+    // 3. channel c over this thread's half of the chunk: history slots [0, nh), BF16 slots [nh, n)
+    const int nh = max(0, min(n, nsplit - c0));
+    const int mid = (n + 1) >> 1, s_lo = half ? mid : 0, s_hi = half ? n : mid;
+    float ax = 0.f, ay = 0.f;
+#pragma unroll 4
+    for (int t = s_lo; t < min(s_hi, nh); ++t) ax = fmaf(wts[t], sbuf[t * kPartFloats + 4 + c], ax);
+#pragma unroll 4
+    for (int t = max(s_lo, nh); t < s_hi; ++t) ay = fmaf(wts[t], sbuf[t * kPartFloats + 4 + c], ay);
+    A = make_float2(A.x + ax, A.y + ay);
+    __syncthreads();                                // the chunk is consumed before the buffer is refilled
   }
-  if (lane == 0) {
-    sm[0][w] = Mh; sl[0][w] = Lh;
-    sm[1][w] = Mf; sl[1][w] = Lf;
+  // the two halves of every channel
+  if (half == 1) {
+    ahalf[0][c] = A.x;
+    ahalf[1][c] = A.y;
   }
-  *reinterpret_cast<float4*>(&sa[0][w][4 * lane]) = Ah;
-  *reinterpret_cast<float4*>(&sa[1][w][4 * lane]) = Af;
   __syncthreads();
-
-  // threads 0..127: channel c of both parts, the warps' states combined
-  const int c = tid;
-  float Mp0, Lp0, Ap0, Mp1, Lp1, Ap1;
-  combine_warps(sm[0], sl[0], sa[0], c, Mp0, Lp0, Ap0);
-  combine_warps(sm[1], sl[1], sa[1], c, Mp1, Lp1, Ap1);
-  if (lv.v_explicit && Mp0 != -INFINITY && landed) {          // block-uniform condition
+  float Ah = A.x + ahalf[0][c], Af = A.y + ahalf[1][c];
+  if (lv.v_explicit && M.x != -INFINITY && landed) {          // block-uniform condition
     // history part: rotated basis -> caller's basis, (a P_br H) U_V^T
-    if (c < kD) zbuf[c] = Ap0;
+    if (half == 0) zbuf[c] = Ah;
     __syncthreads();
     float v[4];
     if (w == 0) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) v[r] = zbuf[rot_channel(lane, r)];   // (a P_br)[lane + 32 r]
+      for (int q = 0; q < 4; ++q) v[q] = zbuf[rot_channel(lane, q)];   // (a P_br)[lane + 32 q]
       fwht128(v);
     }
     __syncthreads();
     if (w == 0) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) zbuf[lane + 32 * r] = v[r];
+      for (int q = 0; q < 4; ++q) zbuf[lane + 32 * q] = v[q];
     }
     __syncthreads();
-    if (c < kD) {
+    if (half == 0) {
       const float* uvt = lv.params + (size_t)(hq / (lv.hq / lv.hkv)) * kParamFloats + kUVtOff;
       float o = 0.f;
 #pragma unroll 8
       for (int i = 0; i < kD; ++i) o = fmaf(zbuf[i], __ldg(uvt + i * kD + c), o);   // (z U_V^T)[c]
-      Ap0 = o;
+      Ah = o;
     }
   }
-  if (c >= kD) return;
-  const float Mx = fmaxf(Mp0, Mp1);
-  const float w0 = (Mp0 == -INFINITY) ? 0.f : exp2f(Mp0 - Mx);
-  const float w1 = (Mp1 == -INFINITY) ? 0.f : exp2f(Mp1 - Mx);
-  const float Ls = Lp0 * w0 + Lp1 * w1;
-  const float o = (Ap0 * w0 + Ap1 * w1) * (1.f / Ls);
+  if (half == 1) return;
+  const float Mx = fmaxf(M.x, M.y);
+  const float w0 = (M.x == -INFINITY) ? 0.f : exp2f(M.x - Mx);
+  const float w1 = (M.y == -INFINITY) ? 0.f : exp2f(M.y - Mx);
+  const float Ls = L.x * w0 + L.y * w1;
+  const float o = (Ah * w0 + Af * w1) * (1.f / Ls);
   const size_t oi = ((size_t)b * lv.hq + hq) * kD + c;
   if (out_dtype == OSCAR_OUT_FP32) static_cast<float*>(out)[oi] = o;
   else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(o);

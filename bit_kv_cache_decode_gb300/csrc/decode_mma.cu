@@ -407,9 +407,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     }
   }
   __syncthreads();
+  // rows of 132 floats: the four 16-byte stores of the 8 lanes of a quarter warp hit distinct banks
+  constexpr int kCaStride = kD + 4;
   float* cm = reinterpret_cast<float*>(smem);     // [kWarps][8] running max
   float* cl = cm + kWarps * 8;                    // [kWarps][8] running sum
-  float* ca = cl + kWarps * 8;                    // [kWarps][8][128] accumulators
+  float* ca = cl + kWarps * 8;                    // [kWarps][8][kCaStride] accumulators
   const int grp = g >> 2;                         // channels 16g .. 16g+15 lie in group g / 4
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -419,12 +421,15 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       cl[w * 8 + head] = lsum[nt];
     }
     const float zs = grp ? zacc[nt][1] : zacc[nt][0];
-    float* dst = ca + (w * 8 + head) * kD;
+    float v[16];                                  // channels 16g .. 16g + 15
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      dst[16 * g + mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
-      dst[16 * g + 8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
+      v[mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
+      v[8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
     }
+    float4* dst = reinterpret_cast<float4*>(ca + (w * 8 + head) * kCaStride + 16 * g);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
   __syncthreads();
   for (int hh = 0; hh < gq; ++hh) {
@@ -439,7 +444,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         if (mw == -INFINITY) continue;
         const float f = exp2f(mw - M);
         Ls = fmaf(cl[ww * 8 + hh], f, Ls);
-        A = fmaf(ca[(ww * 8 + hh) * kD + tid], f, A);
+        A = fmaf(ca[(ww * 8 + hh) * kCaStride + tid], f, A);
       }
     } else {
       M = -INFINITY;

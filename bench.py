@@ -61,7 +61,8 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while running (the first sample is taken
+    before the block starts)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -73,10 +74,13 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t_end = time.time() + 3.0
+            while not self.lines and time.time() < t_end and self.proc.poll() is None:
+                time.sleep(0.01)
         except (FileNotFoundError, OSError):
             self.proc = None
         return self
@@ -93,10 +97,15 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def mark(self):
+        """Samples from here on describe the timed region (earlier ones only prove the sampler runs)."""
+        self.start = len(self.lines)
+
     def summary(self):
         sm, mx, reasons = [], 0.0, set()
+        lines = self.lines[getattr(self, "start", 0):] or self.lines[-1:]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -267,9 +276,9 @@ def run_ours(args, rank: int, world: int, device):
     q_cur = torch.empty_like(q_all[0])            # the step's queries, [layers, B, Hq, 128]
     out = torch.empty(nl, B, hq, 128, dtype=torch.bfloat16, device=device)
     seq = torch.from_numpy(wl["lens"].astype(np.int32)).to(device)
-    # per layer, oscar_decode_step: the append kernel (which also rotates the queries on the tensor-core path)
-    # then one fused decode launch (mma), or append + query rotation + history + BF16 segment + merge (simt)
-    launches_per_layer = 2 if args.algo == 1 else 5
+    # per layer, oscar_decode_step launches the step prologue (append with demotion, query rotation), then
+    # the fused decode and the merge (mma), or the history kernel, the BF16 segment and the merge (simt)
+    launches_per_layer = 3 if args.algo == 1 else 4
 
     def layers():
         for layer in range(nl):
@@ -307,6 +316,7 @@ def run_ours(args, rank: int, world: int, device):
     with ClockSampler(device.index if device.index is not None else 0) as clk:
         torch.cuda.synchronize()
         nvtx_id = torch.cuda.nvtx.range_start("timed_steps")     # profiler filter for the launch list
+        clk.mark()
         ev0.record(stream)
         for i in range(args.warmup, total_steps):
             step(i)
@@ -350,7 +360,7 @@ def run_ours(args, rank: int, world: int, device):
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
                      "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
-        "gpu_launches": (launches_per_layer * nl + 2) * args.steps,
+        "gpu_launches": launches_per_layer * nl * args.steps,
         "clocks": clk.summary(),
     }
     if wl["bf16_pages"] is not None:
@@ -393,8 +403,8 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "e63d824d2155b3840c5f28b5baf92ab3953f911c25082555911e557fc5f21205",
-                      "bytes_per_launch": 66777088 + 500224}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "d753f178da0e315393bf90585905c993920c98fb63a90948f435f15da76cbdc7",
+                      "bytes_per_launch": 66771456 + 374528}
 
 
 def sources_digest() -> str:
@@ -623,7 +633,7 @@ def max_over_ranks(x: float, world: int, device) -> float:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_36l")

@@ -145,39 +145,54 @@ int configure_once() {
   return rc;
 }
 
-// Split policy over the page-table width: choose the number of history splits
-// per (request, kv head) that minimises waves x (pages per CTA + a fixed
-// per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs and every
-// group launches `extra` more CTAs; pages per split are rounded up to `align`
-// and there is no empty trailing split.
-// Splits of the history per (request, kv head): the fewest waves of CTAs, each
-// split at most max_pps pages when the split budget allows (0: no limit).
-void choose_splits(int B, int hkv, int max_pages, int max_splits, int sms, int ctas_per_sm, int align, int extra,
-                   int max_pps, int* nsplit, int* pps) {
+// CUDA-core split policy over the page-table width: the number of history
+// splits per (request, kv head) that minimises waves x (pages per CTA + a fixed
+// per-CTA cost), where a wave is sms * ctas_per_sm resident CTAs; there is no
+// empty trailing split.
+void choose_splits_simt(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps) {
   if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
-  const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
+  const long units = (long)B * hkv, slots = std::max(1L, (long)sms * 4);
   const int nmax = std::min(std::min(max_splits, max_pages), kMaxMmaSplits);
-  const int nmin = max_pps > 0 ? std::min(nmax, (max_pages + max_pps - 1) / max_pps) : 1;
   long best_cost = -1;
   int best_p = max_pages;
-  for (int n = nmin; n <= nmax; ++n) {
-    int p = (max_pages + n - 1) / n;
-    p = (p + align - 1) / align * align;
+  for (int n = 1; n <= nmax; ++n) {
+    const int p = (max_pages + n - 1) / n;
     const int used = (max_pages + p - 1) / p;
-    const long waves = (units * (used + extra) + slots - 1) / slots;
-    const long cost = waves * (p + 2L * align);
+    const long waves = (units * used + slots - 1) / slots;
+    const long cost = waves * (p + 2L);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_p = p; }
   }
   *pps = best_p;
   *nsplit = (max_pages + best_p - 1) / best_p;
 }
 
-void algo_policy(int algo, int gq, int nbf, int* ctas_per_sm, int* align, int* extra, int* max_pps) {
-  if (algo == OSCAR_DECODE_MMA) {
-    *ctas_per_sm = gq <= 4 ? 3 : 2; *align = 4; *extra = nbf; *max_pps = kMaxPagesPerMmaSplit;
-  } else {
-    *ctas_per_sm = 4; *align = 1; *extra = 0; *max_pps = 0;
+// Tensor-core split policy. A request's history pages are spread evenly over n splits of 4 warps,
+// a warp taking every fourth page of its split; the grid has B * hkv * (n + nbf) CTAs (the BF16
+// pages are light ones), ctas_per_sm resident per SM. A CTA's time is about its warps' rounds
+// (pages per warp), so n minimises waves x (rounds + 2 rounds of per-CTA cost: the first page's
+// latency, the warps' combine, one more merge slot), with at most
+// kMaxPagesPerMmaSplit pages per split when the split budget allows. The step prologue, which
+// runs as the decode is scheduled (2 CTAs per request and kv head), holds one decode CTA's
+// registers on each SM it occupies: the first wave has that many fewer slots.
+void choose_splits_mma(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int* nsplit,
+                       int* pps) {
+  if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
+  const int ctas_per_sm = gq <= 4 ? 3 : 2;           // the kernel's resident CTAs at its register count
+  const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
+  const long reserved = std::min((long)sms, 2 * units);
+  const int nmax = std::min(std::min(max_splits, max_pages), kMaxMmaSplits);
+  double best_cost = -1.0;
+  int best_n = nmax;
+  for (int n = 1; n <= nmax; ++n) {
+    const int per = (max_pages + n - 1) / n;
+    if (per > kMaxPagesPerMmaSplit && n < nmax) continue;
+    const long ctas = units * (n + nbf);
+    const long waves = std::max(1L, (ctas + reserved + slots - 1) / slots);
+    const double cost = (double)waves * ((per + 3) / 4 + 2.0);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_n = n; }
   }
+  *nsplit = best_n;
+  *pps = (max_pages + best_n - 1) / best_n;
 }
 
 }  // namespace
@@ -369,12 +384,8 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.len_add = 0;
   a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
-  {
-    int cps, align, extra, mpps;
-    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra, &mpps);
-    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, mpps, &a.nsplit,
-                  &a.pages_per_split);
-  }
+  decode_split_policy(B, c->lay.num_kv_heads, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, max_hist_pages,
+                      c->lay.max_splits, c->sms, a.algo, &a.nsplit, &a.pages_per_split);
   a.ev0 = a.ev1 = nullptr;
   if (c->prof_on && c->prof_n < c->prof_cap) {
     a.ev0 = c->prof_ev[2 * c->prof_n];
@@ -412,12 +423,8 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   a.lse = lse;
   a.algo = c->algo;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
-  {
-    int cps, align, extra, mpps;
-    algo_policy(a.algo, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, &cps, &align, &extra, &mpps);
-    choose_splits(B, c->lay.num_kv_heads, max_hist_pages, c->lay.max_splits, c->sms, cps, align, extra, mpps, &a.nsplit,
-                  &a.pages_per_split);
-  }
+  decode_split_policy(B, c->lay.num_kv_heads, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, max_hist_pages,
+                      c->lay.max_splits, c->sms, a.algo, &a.nsplit, &a.pages_per_split);
   a.ev0 = a.ev1 = nullptr;
   if (c->prof_on && c->prof_n < c->prof_cap) {
     a.ev0 = c->prof_ev[2 * c->prof_n];
@@ -487,7 +494,7 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   int nsplit, pps;
-  choose_splits(B, num_kv_heads, max_pages, max_splits, sms, 4, 1, 0, 0, &nsplit, &pps);
+  choose_splits_simt(B, num_kv_heads, max_pages, max_splits, sms, &nsplit, &pps);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,
@@ -577,9 +584,8 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 // The history split choice of oscar_decode_attention, for at most max_splits splits.
 void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
                          int* nsplit, int* pps) {
-  int cps, align, extra, mpps;
-  algo_policy(algo, gq, nbf, &cps, &align, &extra, &mpps);
-  choose_splits(B, hkv, max_pages, max_splits, sms, cps, align, extra, mpps, nsplit, pps);
+  if (algo == OSCAR_DECODE_MMA) choose_splits_mma(B, hkv, gq, nbf, max_pages, max_splits, sms, nsplit, pps);
+  else choose_splits_simt(B, hkv, max_pages, max_splits, sms, nsplit, pps);
 }
 
 int configure_kernels() { return configure_once(); }

@@ -6,7 +6,8 @@
 // 系统：混合精度缓存布局": packed codes, per-token groups of 64 channels.
 //
 // Work: grid (split, kv head, request); 4 warps per CTA; warp w takes history
-// pages p0 + w, p0 + w + 4, ... of the CTA's split. Each (page, kv head) block
+// pages p0 + w, p0 + w + 4, ... of the CTA's split, a request's pages being
+// spread evenly over the splits. Each (page, kv head) block
 // (5120 B: K codes | V codes | K meta | V meta) is copied into a per-warp
 // 2-stage shared-memory ring by one cp.async.bulk with an mbarrier; waits are
 // bounded and report OSCAR_STATUS_TIMEOUT instead of hanging.
@@ -28,7 +29,7 @@
 // and writes one partial (m, l, acc[128]) per query head and split.
 //
 // The same launch carries the BF16 sink + recent tokens as one extra CTA per
-// BF16 page (bulk-copied, CUDA-core dot products). The log-sum-exp merge of
+// BF16 page (row-wise bulk copies, tensor-core products). The log-sum-exp merge of
 // all slots runs as the next kernel (merge.cu), a programmatic dependent that
 // is scheduled while this grid runs and waits for its completion.
 #include "kernels.cuh"
@@ -104,7 +105,6 @@ struct FusedArgs {
   int len_add;                       // attend over seq_lens[b] + len_add tokens
   const int* hist_pt;
   int max_hist_pages;
-  int pages_per_split;
   int nsplit;                        // history CTAs per group; the next nbf CTAs take one BF16 page each
   int nbf;
   const int* bf16_pt;
@@ -125,7 +125,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
                                            uint8_t* smem, int split, int h, int b, unsigned long long* trace) {
   const int* __restrict__ seq_lens = fa.seq_lens;
   const int* __restrict__ hist_pt = fa.hist_pt;
-  const int max_hist_pages = fa.max_hist_pages, pages_per_split = fa.pages_per_split;
+  const int max_hist_pages = fa.max_hist_pages;
   int& any_timeout = *reinterpret_cast<int*>(smem + kWarps * kStages * kBlockBytes + kWarps * kStages * 8);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -142,8 +142,9 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     npages = max_hist_pages;
     Lh = npages * kP;
   }
-  const int p0 = split * pages_per_split + w;
-  const int p1 = min(split * pages_per_split + pages_per_split, npages);
+  // The request's pages are spread evenly over the splits: split s starts at page floor(s npages / nsplit).
+  const int p0 = (int)((long long)split * npages / fa.nsplit) + w;
+  const int p1 = (int)((long long)(split + 1) * npages / fa.nsplit);
   const int my_pages = p0 < p1 ? (p1 - p0 + kWarps - 1) / kWarps : 0;
   const int* pt = hist_pt + (size_t)b * max_hist_pages;
 
@@ -458,21 +459,59 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   }
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// p = hi + lo as two bf16 pairs (hi the rounded value, lo the rounded remainder), for (x, y)
+__device__ __forceinline__ void split_bf16x2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+constexpr int kBfRow = kD + 8;       // bf16 per staged row: 272 bytes, so the 8 rows of an ldmatrix hit distinct banks
+constexpr int kObStride = kD + 4;    // floats per (warp, head) row of the output combine
+
 // BF16 page c of group (b, h): c = 0 is the sink page, c >= 1 the recent ring
 // pages. Attention is order-independent, so each page is attended as a unit:
-// the (page, kv head) block (K [64][128] then V [64][128], 32 KB) arrives in
-// one bulk copy; row r is live if r < n_sink (sink page) or if its ring slot
-// 64 (c - 1) + r < n_recent (ring pages). Dot products walk the 16-byte
-// columns of a K row in a token-rotated order to avoid bank conflicts.
+// row r is live if r < n_sink (sink page) or if its ring slot 64 (c - 1) + r <
+// n_recent (ring pages). The live rows of K and V arrive by one bulk copy per
+// row into padded rows (the rest are zero), and both products run on the
+// tensor cores (mma.m16n8k16, bf16 in, f32 out), warp w taking tokens
+// 16w .. 16w + 15:
+//  * logits = K q^T: A = K rows (ldmatrix), B = the raw query rows of the
+//    group's heads (8 columns, exact bf16 products);
+//  * P.V: A = V^T (ldmatrix.trans), B = the weights as bf16 hi + lo parts (two
+//    MMAs, so the weights keep about 16 bits), built from the logits'
+//    accumulator layout by movmatrix transposes.
+// The four warps' maxima, sums and outputs are combined through shared memory.
 __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
                                           uint8_t* smem, int c, int h, int b) {
-  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem);                  // K [64][128], V [64][128]
-  float* qs = reinterpret_cast<float*>(smem + kBf16BlockBytes);                 // [8][128]
-  float* pb = qs + 8 * kD;                                                      // [8][64]
-  float* ms = pb + 8 * kP;                                                      // [8]
-  float* ls = ms + 8;                                                           // [8]
-  const uint32_t bar = smem_addr(ls + 8);
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  __nv_bfloat16* ks = reinterpret_cast<__nv_bfloat16*>(smem);                   // [64][kBfRow]
+  __nv_bfloat16* vs = ks + kP * kBfRow;                                         // [64][kBfRow]
+  float* red = reinterpret_cast<float*>(vs + kP * kBfRow);                      // [2][4 warps][8 heads]
+  float* ob = reinterpret_cast<float*>(smem);                                   // [4][8][kObStride], after the MMAs
+  const uint32_t bar = smem_addr(red + 64);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int gq = lv.hq / lv.hkv, hq0 = h * gq;
   pdl_wait();                                      // the append writes into these pages
   const int L = fa.seq_lens[b] + fa.len_add;
@@ -486,72 +525,126 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
   const int page = nrow > 0 ? fa.bf16_pt[(size_t)b * ((lv.sink + lv.recent) / kP) + c] : -1;
   const bool ok = nrow > 0 && page >= 0 && page < lv.n_bf16;
   if (nrow > 0 && !ok && tid == 0) flag(lv.status, OSCAR_STATUS_BAD_PAGE);
-  bool landed = true;
+  bool landed = false;
+  uint32_t qb[8][2];                               // B fragments of the logits: head g, channels of k-step kk
   if (ok) {
     if (tid == 0) {
       mbar_init(bar);
-      bulk_load(smem_addr(kv), lv.bf16 + ((size_t)page * lv.hkv + h) * kBf16BlockBytes, kBf16BlockBytes, bar);
+      mbar_expect_tx(bar, 2u * nrow * kD * 2);
     }
-    for (int i = tid; i < gq * kD; i += 128) qs[i] = __bfloat162float(fa.q[((size_t)b * lv.hq + hq0) * kD + i]);
-    __syncthreads();                               // barrier initialised before anyone waits on it
-    landed = __syncthreads_and(mbar_wait(bar, 0));
+    __syncthreads();                               // barrier armed before any copy is issued
+    {
+      const int r = tid & (kP - 1), kind = tid >> 6;           // one row of K (kind 0) or V (kind 1) per thread
+      __nv_bfloat16* dst = (kind ? vs : ks) + r * kBfRow;
+      if (r < nrow) {
+        const uint8_t* src = lv.bf16 + ((size_t)page * lv.hkv + h) * kBf16BlockBytes + ((size_t)kind * kP + r) * kD * 2;
+        bulk_copy(smem_addr(dst), src, kD * 2, bar);
+      } else {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < kD / 8; ++i) d4[i] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    const __nv_bfloat16* qrow = fa.q + ((size_t)b * lv.hq + hq0 + g) * kD;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      qb[kk][0] = g < gq ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * t) : 0u;
+      qb[kk][1] = g < gq ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * t + 8) : 0u;
+    }
+    landed = __syncthreads_and(mbar_wait(bar, 0));  // also publishes the zeroed rows
     if (!landed && tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
   }
-  const int live = (ok && landed) ? nrow : 0;
-  for (int item = tid; item < gq * kP; item += 128) {
-    const int tk = item % kP, hh = item / kP;
-    float l = -INFINITY;
-    if (tk < live) {
-      const __nv_bfloat16* krow = kv + tk * kD;
-      float dot = 0.f;
-#pragma unroll 4
-      for (int j = 0; j < kD / 8; ++j) {
-        const int i = (j + tk) & (kD / 8 - 1);
-        const uint4 k8 = *reinterpret_cast<const uint4*>(krow + 8 * i);
-        const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&k8);
-        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * kD + 8 * i);
-        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * kD + 8 * i + 4);
-        float2 f;
-        f = __bfloat1622float2(k2[0]); dot = fmaf(f.x, qa.x, fmaf(f.y, qa.y, dot));
-        f = __bfloat1622float2(k2[1]); dot = fmaf(f.x, qa.z, fmaf(f.y, qa.w, dot));
-        f = __bfloat1622float2(k2[2]); dot = fmaf(f.x, qb.x, fmaf(f.y, qb.y, dot));
-        f = __bfloat1622float2(k2[3]); dot = fmaf(f.x, qb.z, fmaf(f.y, qb.w, dot));
-      }
-      l = dot * fa.scale_log2;
+  if (!ok || !landed) {                            // block-uniform: nothing to attend (or the copy never came)
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh) {
+      if (hh >= gq) break;
+      float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.nsplit + c);
+      if (tid == 0) { part[0] = -INFINITY; part[1] = 0.f; }
+      part[4 + tid] = 0.f;
     }
-    pb[hh * kP + tk] = l;
+    return;
+  }
+  // ---- logits of tokens 16w + g (s[0], s[1]) and 16w + g + 8 (s[2], s[3]), heads 2t, 2t + 1 ----
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const uint32_t ka = smem_addr(ks) + ((16 * w + (lane & 7) + 8 * ((lane >> 3) & 1)) * kBfRow + 8 * (lane >> 4)) * 2;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(ka + kk * 32, a0, a1, a2, a3);
+      mma_bf16(s, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    }
+  }
+  const int tok0 = 16 * w + g, tok1 = tok0 + 8;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s[e] = ((e < 2 ? tok0 : tok1) < nrow) ? s[e] * fa.scale_log2 : -INFINITY;
+  // ---- maxima and sums per head over the page ------------------------------------------------------
+  float m0 = fmaxf(s[0], s[2]), m1 = fmaxf(s[1], s[3]);
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, x));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, x));
+  }
+  if (g == 0) { red[w * 8 + 2 * t] = m0; red[w * 8 + 2 * t + 1] = m1; }
+  __syncthreads();
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < 4; ++ww) { M0 = fmaxf(M0, red[ww * 8 + 2 * t]); M1 = fmaxf(M1, red[ww * 8 + 2 * t + 1]); }
+  float p[4];
+  p[0] = M0 == -INFINITY ? 0.f : fast_exp2(s[0] - M0);
+  p[1] = M1 == -INFINITY ? 0.f : fast_exp2(s[1] - M1);
+  p[2] = M0 == -INFINITY ? 0.f : fast_exp2(s[2] - M0);
+  p[3] = M1 == -INFINITY ? 0.f : fast_exp2(s[3] - M1);
+  float l0 = p[0] + p[2], l1 = p[1] + p[3];
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+  }
+  if (g == 0) { red[32 + w * 8 + 2 * t] = l0; red[32 + w * 8 + 2 * t + 1] = l1; }
+  // ---- P.V over the warp's 16 tokens, all 128 channels ------------------------------------------------
+  uint32_t bh0, bl0, bh1, bl1;
+  split_bf16x2(p[0], p[1], bh0, bl0);              // tokens 16w + g: heads 2t, 2t + 1
+  split_bf16x2(p[2], p[3], bh1, bl1);              // tokens 16w + g + 8
+  bh0 = movmatrix_t(bh0); bl0 = movmatrix_t(bl0);  // head g, tokens 2t, 2t + 1
+  bh1 = movmatrix_t(bh1); bl1 = movmatrix_t(bl1);  // head g, tokens 2t + 8, 2t + 9
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  {
+    const uint32_t va = smem_addr(vs) + ((16 * w + (lane & 7) + 8 * (lane >> 4)) * kBfRow + 8 * ((lane >> 3) & 1)) * 2;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(va + mt * 32, a0, a1, a2, a3);     // channels 16 mt .., tokens 16 w ..
+      mma_bf16(o[mt], a0, a1, a2, a3, bh0, bh1);
+      mma_bf16(o[mt], a0, a1, a2, a3, bl0, bl1);
+    }
+  }
+  __syncthreads();                                 // every warp's K / V reads are done: ob may overwrite them
+  // o[mt]: channel 16 mt + g (0, 1) or + 8 (2, 3), head 2t (0, 2) or 2t + 1 (1, 3)
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    float* r0 = ob + (w * 8 + 2 * t) * kObStride + 16 * mt + g;
+    r0[0] = o[mt][0];
+    r0[kObStride] = o[mt][1];
+    r0[8] = o[mt][2];
+    r0[kObStride + 8] = o[mt][3];
   }
   __syncthreads();
-  for (int hh = w; hh < gq; hh += 4) {
-    const float l0 = pb[hh * kP + lane], l1 = pb[hh * kP + lane + 32];
-    float m = fmaxf(l0, l1);
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, x));
-    const float p0 = m == -INFINITY ? 0.f : exp2f(l0 - m), p1 = m == -INFINITY ? 0.f : exp2f(l1 - m);
-    float sum = p0 + p1;
-#pragma unroll
-    for (int x = 16; x > 0; x >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, x);
-    pb[hh * kP + lane] = p0;
-    pb[hh * kP + lane + 32] = p1;
-    if (lane == 0) { ms[hh] = m; ls[hh] = sum; }
-  }
-  __syncthreads();
-  float acc[8];
-#pragma unroll
-  for (int hh = 0; hh < 8; ++hh) acc[hh] = 0.f;
-  const __nv_bfloat16* vcol = kv + kP * kD + tid;
-  for (int tk = 0; tk < live; ++tk) {
-    const float vv = __bfloat162float(vcol[tk * kD]);
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
-      if (hh < gq) acc[hh] = fmaf(pb[hh * kP + tk], vv, acc[hh]);
-  }
 #pragma unroll
   for (int hh = 0; hh < 8; ++hh) {
     if (hh >= gq) break;
+    float M = -INFINITY, Ls = 0.f, A = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < 4; ++ww) {
+      M = fmaxf(M, red[ww * 8 + hh]);
+      Ls += red[32 + ww * 8 + hh];
+      A += ob[(ww * 8 + hh) * kObStride + tid];
+    }
     float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.nsplit + c);
-    if (tid == 0) { part[0] = ms[hh]; part[1] = ls[hh]; }
-    part[4 + tid] = acc[hh];
+    if (tid == 0) { part[0] = M; part[1] = Ls; }
+    part[4 + tid] = A;
   }
 }
 
@@ -592,7 +685,6 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   fa.len_add = a.len_add;
   fa.hist_pt = a.hist_pt;
   fa.max_hist_pages = a.max_hist_pages;
-  fa.pages_per_split = a.pages_per_split;
   fa.nsplit = a.nsplit;
   fa.nbf = a.nbf;
   fa.bf16_pt = a.bf16_pt;
@@ -622,7 +714,8 @@ int configure_mma_kernels() {
     return OSCAR_ERR_CUDA;
   if (cudaFuncSetAttribute(k_decode_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
     return OSCAR_ERR_CUDA;
-  return OSCAR_OK;
+  if (set_max_shared_carveout(reinterpret_cast<const void*>(k_decode_mma<1>)) != OSCAR_OK) return OSCAR_ERR_CUDA;
+  return set_max_shared_carveout(reinterpret_cast<const void*>(k_decode_mma<2>));
 }
 
 }  // namespace oscar

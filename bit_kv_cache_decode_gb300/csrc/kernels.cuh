@@ -68,7 +68,7 @@ struct DecodeArgs {
   float* lse;
   int nsplit;            // history splits launched per (request, kv head)
   int nbf;               // BF16 (sink + recent) chunks of 64 tokens per (request, kv head)
-  int pages_per_split;
+  int pages_per_split;   // history pages per split, at most (the tensor-core path spreads a request evenly)
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
   int skip_qprep;        // the query prologue already ran (with the append, in one launch)
@@ -83,6 +83,15 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
                  int out_dtype, float* lse, cudaStream_t st);
 constexpr int kMergeChunk = 96;            // partial slots staged in shared memory at a time by the merge
 int configure_merge_kernel();
+
+// The kernels of the decode chain all ask for the largest shared-memory carveout: a grid scheduled
+// early beside its predecessor then never waits for an SM to drain and change its L1 / shared split.
+inline int set_max_shared_carveout(const void* fn) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared) == cudaSuccess
+             ? OSCAR_OK
+             : OSCAR_ERR_CUDA;
+}
 int configure_decode_kernels();
 int launch_wait_probe(int* status, cudaStream_t st);   // checks.cu
 

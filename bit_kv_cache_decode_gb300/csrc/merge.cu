@@ -18,6 +18,8 @@
 // explicit-V mode their combination is multiplied by R_V^T = P_br H U_V^T
 // before it meets the BF16 slots, which are in the caller's basis (MarkTechPost
 // article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局").
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
@@ -61,7 +63,7 @@ __device__ __forceinline__ float2 block_reduce2(float2 v, float2* red) {
 __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, DecodeWorkspace ws, int nsplit, int nbfs,
                                                             void* out, int out_dtype, float* lse) {
   TimelineSpan timeline_span(lv, kTlMerge);
-  extern __shared__ __align__(128) float sbuf[];            // [kMergeChunk][kPartFloats]
+  extern __shared__ __align__(128) float sbuf[];            // [min(kMergeChunk, slots)][kPartFloats]
   __shared__ __align__(8) uint64_t bar_mem;
   __shared__ float2 red[kMergeWarps];
   __shared__ float wts[kMergeChunk];
@@ -89,8 +91,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, Decode
   // thread's channel c summed over its half of the slots; L and A are relative to 2^M
   float2 M = make_float2(-INFINITY, -INFINITY), L = make_float2(0.f, 0.f), A = make_float2(0.f, 0.f);
   uint32_t phase = 0;
-  for (int c0 = 0; c0 < nslot; c0 += kMergeChunk) {
-    const int n = min(kMergeChunk, nslot - c0);
+  const int chunk = min(kMergeChunk, nslot);       // slots per bulk copy; the launch sized sbuf for it
+  for (int c0 = 0; c0 < nslot; c0 += chunk) {
+    const int n = min(chunk, nslot - c0);
     if (tid == 0) bulk_load(smem_addr(sbuf), row0 + (size_t)c0 * kPartFloats, n * kPartFloats * 4, bar);
     if (!__syncthreads_and(mbar_wait(bar, phase))) {
       if (tid == 0) {
@@ -182,7 +185,8 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(lv.hq, B);
   cfg.blockDim = dim3(kMergeThreads);
-  cfg.dynamicSmemBytes = kMergeChunk * kPartFloats * sizeof(float);
+  // only the slots one copy brings: a smaller footprint lets the grid sit beside the decode CTAs it waits for
+  cfg.dynamicSmemBytes = std::min(kMergeChunk, nsplit + nbfs) * kPartFloats * sizeof(float);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -192,10 +196,10 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
 }
 
 int configure_merge_kernel() {
-  return cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kMergeChunk * kPartFloats * (int)sizeof(float)) == cudaSuccess
-             ? OSCAR_OK
-             : OSCAR_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kMergeChunk * kPartFloats * (int)sizeof(float)) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  return set_max_shared_carveout(reinterpret_cast<const void*>(k_merge));
 }
 
 }  // namespace oscar

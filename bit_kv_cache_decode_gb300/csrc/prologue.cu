@@ -191,10 +191,10 @@ int launch_prologue(const LayerView& lv, const DecodeWorkspace& ws, int B, const
 }
 
 int configure_prologue_kernel() {
-  return cudaFuncSetAttribute(k_step_prologue, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrologueSmem) ==
-                 cudaSuccess
-             ? OSCAR_OK
-             : OSCAR_ERR_CUDA;
+  if (cudaFuncSetAttribute(k_step_prologue, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrologueSmem) !=
+      cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  return set_max_shared_carveout(reinterpret_cast<const void*>(k_step_prologue));
 }
 
 }  // namespace oscar

@@ -28,6 +28,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// Expect `bytes` of bulk copies on mbarrier `bar` and arrive (arrival count 1): the copies
+// themselves (bulk_copy) may then be issued by any threads of the CTA.
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// One bulk copy global -> shared completing on `bar`, whose bytes an mbar_expect_tx announced.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // L2 eviction policies for bulk copies: data read once per step (streamed cache
 // pages) leaves L2 first, and small data every step needs (rotation matrices)
 // stays, so a step's stream does not push the next layer's matrices out.

@@ -38,8 +38,8 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Block-wide max (op 0) or sum (op 1) of two values; every thread gets the results.
-template <int OP>
+// Block-wide max (op 0) or sum (op 1) of two values over NW warps; every thread gets the results.
+template <int OP, int NW = kMergeWarps>
 __device__ __forceinline__ float2 block_reduce2(float2 v, float2* red) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -53,7 +53,7 @@ __device__ __forceinline__ float2 block_reduce2(float2 v, float2* red) {
   __syncthreads();
   float2 r = red[0];
 #pragma unroll
-  for (int i = 1; i < kMergeWarps; ++i) {
+  for (int i = 1; i < NW; ++i) {
     r.x = OP == 0 ? fmaxf(r.x, red[i].x) : r.x + red[i].x;
     r.y = OP == 0 ? fmaxf(r.y, red[i].y) : r.y + red[i].y;
   }
@@ -175,6 +175,95 @@ __global__ void __launch_bounds__(kMergeThreads, 1) k_merge(LayerView lv, Decode
   if (lse != nullptr && c == 0) lse[(size_t)b * lv.hq + hq] = (Mx + log2f(Ls)) * 0.6931471805599453f;
 }
 
+
+// V-absorbed mode: no rotation follows the combination, so the channels split
+// across kMergeParts CTAs per (request, query head) of 128 threads. Lane l of
+// warp w owns channel 32 part + l and the slots w, w + 4, ... of a chunk of
+// kMergeSplitChunk slots; each slot row's 32 channels are one coalesced 128-byte
+// load, and a chunk's loads (headers and values) are all issued before the first
+// reduction, so a chunk costs one load round trip. 128 threads keep the CTA
+// small enough to be scheduled beside the decode CTAs it waits for.
+constexpr int kMergeParts = 4;
+constexpr int kMergeSplitThreads = 128;
+constexpr int kMergeSplitWarps = kMergeSplitThreads / 32;
+constexpr int kMergeSplitChunk = 64;
+constexpr int kMergeSplitPer = kMergeSplitChunk / kMergeSplitWarps;   // slots per thread and chunk
+
+__global__ void __launch_bounds__(kMergeSplitThreads) k_merge_split(LayerView lv, DecodeWorkspace ws, int nsplit,
+                                                                    int nbfs, void* out, int out_dtype, float* lse) {
+  TimelineSpan timeline_span(lv, kTlMerge);
+  __shared__ float2 red[kMergeSplitWarps];
+  __shared__ float wts[kMergeSplitChunk];
+  __shared__ float2 accs[kMergeSplitWarps][32];
+  const int hq = blockIdx.x, b = blockIdx.y, part = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int c = 32 * part + lane;                   // output channel of this thread
+  pdl_wait();                                       // the partials are written by the preceding grid
+  timeline_span.mark();
+  pdl_launch_dependents();                          // as in k_merge: only after the wait
+  const float* row0 = ws.partials + ((size_t)b * lv.hq + hq) * ws.nslots * kPartFloats;
+  const int nslot = nsplit + nbfs;
+  // running state per part (x: history slots, y: BF16 slots), relative to 2^M
+  float2 M = make_float2(-INFINITY, -INFINITY), L = make_float2(0.f, 0.f), A = make_float2(0.f, 0.f);
+  for (int c0 = 0; c0 < nslot; c0 += kMergeSplitChunk) {
+    const int n = min(kMergeSplitChunk, nslot - c0);
+    float m = -INFINITY, l = 0.f;
+    if (tid < n) {
+      const float2 ml = *reinterpret_cast<const float2*>(row0 + (size_t)(c0 + tid) * kPartFloats);
+      m = ml.x;
+      l = ml.y;
+    }
+    float v[kMergeSplitPer];
+#pragma unroll
+    for (int i = 0; i < kMergeSplitPer; ++i) {
+      const int sl = w + kMergeSplitWarps * i;
+      v[i] = sl < n ? row0[(size_t)(c0 + sl) * kPartFloats + 4 + c] : 0.f;
+    }
+    // the chunk's maxima per part; rescale the running state
+    const bool hist = c0 + tid < nsplit;
+    const float2 cm = block_reduce2<0, kMergeSplitWarps>(make_float2(hist ? m : -INFINITY, hist ? -INFINITY : m), red);
+    const float2 Mn = make_float2(fmaxf(M.x, cm.x), fmaxf(M.y, cm.y));
+    const float2 r = make_float2(M.x == -INFINITY ? 0.f : ex2(M.x - Mn.x), M.y == -INFINITY ? 0.f : ex2(M.y - Mn.y));
+    L = make_float2(L.x * r.x, L.y * r.y);
+    A = make_float2(A.x * r.x, A.y * r.y);
+    M = Mn;
+    // one weight per slot (thread tid < n), and the chunk's l sums
+    float wt = 0.f;
+    if (tid < n && m != -INFINITY) wt = ex2(m - (hist ? M.x : M.y));
+    if (tid < kMergeSplitChunk) wts[tid] = wt;
+    const float lw = tid < n ? l * wt : 0.f;
+    const float2 cl = block_reduce2<1, kMergeSplitWarps>(make_float2(hist ? lw : 0.f, hist ? 0.f : lw), red);
+    L = make_float2(L.x + cl.x, L.y + cl.y);        // the reduction's barriers also published wts
+#pragma unroll
+    for (int i = 0; i < kMergeSplitPer; ++i) {
+      const int sl = w + kMergeSplitWarps * i;
+      if (sl < n) {
+        if (c0 + sl < nsplit) A.x = fmaf(wts[sl], v[i], A.x);
+        else A.y = fmaf(wts[sl], v[i], A.y);
+      }
+    }
+    __syncthreads();                                // wts is rewritten by the next chunk
+  }
+  accs[w][lane] = A;
+  __syncthreads();
+  if (w != 0) return;
+  float Ah = 0.f, Af = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < kMergeSplitWarps; ++ww) {
+    Ah += accs[ww][lane].x;
+    Af += accs[ww][lane].y;
+  }
+  const float Mx = fmaxf(M.x, M.y);
+  const float w0 = (M.x == -INFINITY) ? 0.f : exp2f(M.x - Mx);
+  const float w1 = (M.y == -INFINITY) ? 0.f : exp2f(M.y - Mx);
+  const float Ls = L.x * w0 + L.y * w1;
+  const float o = (Ah * w0 + Af * w1) * (1.f / Ls);
+  const size_t oi = ((size_t)b * lv.hq + hq) * kD + c;
+  if (out_dtype == OSCAR_OUT_FP32) static_cast<float*>(out)[oi] = o;
+  else static_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(o);
+  if (lse != nullptr && c == 0) lse[(size_t)b * lv.hq + hq] = (Mx + log2f(Ls)) * 0.6931471805599453f;
+}
+
 }  // namespace
 
 int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nsplit, int nbfs, void* out,
@@ -183,23 +272,31 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(lv.hq, B);
-  cfg.blockDim = dim3(kMergeThreads);
-  // only the slots one copy brings: a smaller footprint lets the grid sit beside the decode CTAs it waits for
-  cfg.dynamicSmemBytes = std::min(kMergeChunk, nsplit + nbfs) * kPartFloats * sizeof(float);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, k_merge, lv, ws, nsplit, nbfs, out, out_dtype, lse) != cudaSuccess)
-    return OSCAR_ERR_CUDA;
-  return OSCAR_OK;
+  cudaError_t e;
+  if (!lv.v_explicit) {                             // channels split across CTAs
+    cfg.gridDim = dim3(lv.hq, B, kMergeParts);
+    cfg.blockDim = dim3(kMergeSplitThreads);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, k_merge_split, lv, ws, nsplit, nbfs, out, out_dtype, lse);
+  } else {                                          // whole rows: the rotation back needs every channel
+    cfg.gridDim = dim3(lv.hq, B);
+    cfg.blockDim = dim3(kMergeThreads);
+    // only the slots one copy brings: a smaller footprint lets the grid sit beside the decode CTAs it waits for
+    cfg.dynamicSmemBytes = std::min(kMergeChunk, nsplit + nbfs) * kPartFloats * sizeof(float);
+    e = cudaLaunchKernelEx(&cfg, k_merge, lv, ws, nsplit, nbfs, out, out_dtype, lse);
+  }
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_merge_kernel() {
   if (cudaFuncSetAttribute(k_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kMergeChunk * kPartFloats * (int)sizeof(float)) != cudaSuccess)
     return OSCAR_ERR_CUDA;
-  return set_max_shared_carveout(reinterpret_cast<const void*>(k_merge));
+  if (set_max_shared_carveout(reinterpret_cast<const void*>(k_merge)) != OSCAR_OK) return OSCAR_ERR_CUDA;
+  return set_max_shared_carveout(reinterpret_cast<const void*>(k_merge_split));
 }
 
 }  // namespace oscar

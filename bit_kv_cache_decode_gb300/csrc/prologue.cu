@@ -22,7 +22,9 @@
 // * The new token is written to its ring slot, after the slot's old row was
 //   staged.
 // The grid waits for the kernel before it on the stream (programmatic
-// dependent launch) before it reads anything, then lets the decode be scheduled.
+// dependent launch) before it reads q, k and v, then lets the decode be
+// scheduled. Sequence lengths, page tables and the pool's rows (inputs the
+// kernel before does not produce) are read before that wait.
 #include "kernels.cuh"
 #include "rotate.cuh"
 #include "tma.cuh"
@@ -67,27 +69,24 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
       bulk_load_hint(smem_addr(frag_s + c * chunk), f + c * chunk, chunk * 4, bars + 8 * c, keep);
     }
   }
-  // Wait for the grid before (in a model, the kernel that made q, k and v), then let the decode be
-  // scheduled; it waits for this grid before it reads anything this kernel writes.
-  pdl_wait();
-  pdl_launch_dependents();
-
   // --- demotion of the oldest recent token: where it comes from and goes to ---
+  // Sequence lengths, page tables and the pool are not produced by the kernel before this one (the
+  // caller's q, k, v are): they are read before the programmatic wait, so only q, k and v wait for it.
   const int bf16_per_req = (lv.sink + lv.recent) / kP;
   int L_old = 0;
   bool demote = false;
   int slot = 0, spage = -1, hh = 0, hpage = -1;
   if (k != nullptr) {
-    L_old = seq_lens_before[b];
+    L_old = __ldcg(seq_lens_before + b);          // L2 reads: nothing older may sit in this SM's L1
     if (L_old < 0 && tid == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);
     demote = L_old >= lv.sink + lv.recent;
     if (demote) {
       const int old = L_old - lv.recent;
       slot = (old - lv.sink) % lv.recent;
-      spage = bf16_pt[b * bf16_per_req + lv.sink / kP + slot / kP];
+      spage = __ldcg(bf16_pt + b * bf16_per_req + lv.sink / kP + slot / kP);
       hh = old - lv.sink;
       const bool ok_h = hh / kP < max_hist_pages;
-      hpage = ok_h ? hist_pt[b * max_hist_pages + hh / kP] : -1;
+      hpage = ok_h ? __ldcg(hist_pt + (size_t)b * max_hist_pages + hh / kP) : -1;
       if (!ok_h || !valid_page(spage, lv.n_bf16) || !valid_page(hpage, lv.n_int2)) {
         if (tid == 0) flag(lv.status, ok_h ? OSCAR_STATUS_BAD_PAGE : OSCAR_STATUS_BAD_SEQLEN);
         demote = false;
@@ -103,17 +102,18 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
   }
   const bool need_frags = (demote && rotate) || do_q;      // fetch_frags holds whenever this does
   // --- the tile: row 0 the demoted row, rows 1 .. gq the queries, zeros elsewhere ---
-  const __nv_bfloat16* drow = demote ? bf16_row(lv, spage, h, kind, slot % kP) : nullptr;
-  const __nv_bfloat16* qrow = do_q ? q + ((size_t)b * lv.hq + h * gq) * kD : nullptr;
+  // one 16-byte chunk (8 values) per thread: 16 rows x 16 chunks; the demoted row's chunks are loaded
+  // before the wait, the queries' after it
+  static_assert(kPrologueWarps * 32 == 16 * 16, "one chunk per thread");
+  const int r = tid >> 4, c8 = tid & 15;
+  uint4 u = make_uint4(0u, 0u, 0u, 0u);
+  if (r == 0 && demote) u = __ldcg(reinterpret_cast<const uint4*>(bf16_row(lv, spage, h, kind, slot % kP) + 8 * c8));
+  // Wait for the grid before (in a model, the kernel that made q, k and v), then let the decode be
+  // scheduled; it waits for this grid before it reads anything this kernel writes.
+  pdl_wait();
+  pdl_launch_dependents();
+  if (r >= 1 && r <= gq && do_q) u = *reinterpret_cast<const uint4*>(q + ((size_t)b * lv.hq + h * gq + r - 1) * kD + 8 * c8);
   {
-    // one 16-byte chunk (8 values) per thread, all loads in flight at once: 16 rows x 16 chunks
-    static_assert(kPrologueWarps * 32 == 16 * 16, "one chunk per thread");
-    const int r = tid >> 4, c8 = tid & 15;
-    const __nv_bfloat16* src = nullptr;
-    if (r == 0 && demote) src = drow + 8 * c8;
-    else if (r >= 1 && r <= gq && do_q) src = qrow + (r - 1) * kD + 8 * c8;
-    uint4 u = make_uint4(0u, 0u, 0u, 0u);
-    if (src != nullptr) u = *reinterpret_cast<const uint4*>(src);
     const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
     float4* dst = reinterpret_cast<float4*>(rows + r * kTileStride + 8 * c8);
     dst[0] = make_float4(__uint_as_float(wds[0] << 16), __uint_as_float(wds[0] & 0xffff0000u),

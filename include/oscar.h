@@ -174,7 +174,10 @@ int oscar_quantize_prefill(oscar_cache* cache, int layer, int B, const void* k, 
  *  seq_lens_before : device int32 [B], lengths before this token
  * If seq_lens_before[r] >= sink + recent, the token at position
  * seq_lens_before[r] - recent is demoted to history slot
- * seq_lens_before[r] - recent - sink before its ring slot is overwritten. */
+ * seq_lens_before[r] - recent - sink before its ring slot is overwritten.
+ * As in oscar_decode_step, seq_lens_before, the page tables and the pool's
+ * rows are read before the wait for the kernel launched just before; only
+ * k and v may come from that kernel. */
 int oscar_append_kv(oscar_cache* cache, int layer, int B, const void* k, const void* v,
                     const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
                     const int32_t* bf16_pt, void* stream);
@@ -203,7 +206,13 @@ int oscar_decode_attention(oscar_cache* cache, int layer, int B, const void* q, 
  * rotated together on the tensor cores; the demoted row is quantised into
  * the history, the queries become the decode's fragments, the new token goes
  * to its ring slot), the decode kernel and the merge. The decode kernel
- * prefetches history pages the append cannot touch before it waits. */
+ * prefetches history pages the append cannot touch before it waits.
+ * Ordering: only q, k and v may be produced by the kernel launched just
+ * before this call. The prologue is a programmatic dependent of that kernel:
+ * it reads seq_lens_before, the page tables and the pool's BF16 rows before
+ * it waits for it. These inputs must be complete when that kernel starts
+ * (host copies, or any earlier kernel). No kernel of this library writes
+ * them early. */
 int oscar_decode_step(oscar_cache* cache, int layer, int B, const void* q, const void* k, const void* v,
                       const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
                       const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream);

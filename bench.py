@@ -11,6 +11,7 @@ Workloads (synthetic, seeded; Qwen3-shaped random data, no model weights):
   qwen3_8b_36l  (default) 36 layers x (32 q / 8 kv heads, d=128), batch 1,
                 102,400-token context (64 sink + 102,080 history + 256 recent)
   qwen3_4b_b32  36 layers, batch 32 x 102,400 tokens sharing a 92,160-token prefix
+  qwen3_4b_b32_l1   1 layer of qwen3_4b_b32, for profiler captures
   qwen3_8b_l1   1 layer, batch 1, 32,768 tokens
   qwen3_8b_100k_l1  1 layer of qwen3_8b_36l (the same decode launch), for profiler captures
   qwen3_32b_mixed   1 layer x (64 q / 8 kv heads), batch 8, lengths ~ U[98,304, 131,072]: one timed bulk
@@ -45,6 +46,7 @@ BF16_BYTES = 512         # per BF16 token per kv head: K and V, 128 x 2 B each
 WORKLOADS = {
     "qwen3_8b_36l": dict(layers=36, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
     "qwen3_4b_b32": dict(layers=36, hq=32, hkv=8, batch=32, ctx=102400, shared=92160),
+    "qwen3_4b_b32_l1": dict(layers=1, hq=32, hkv=8, batch=32, ctx=102400, shared=92160),
     "qwen3_8b_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=32768, shared=0),
     "qwen3_8b_100k_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
     # ctx as (lo, hi): per-request lengths drawn uniformly, all requests prefilled by one bulk call
@@ -224,7 +226,7 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
     return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, lens=lens, prefill=prefill, B=B, H=H, hq=hq,
                 layers=nl,
                 bf16_pages=bf16_pages, base_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
-                hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared)
+                hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared, shp=shp)
 
 
 def step_inputs(wl, steps: int, device, seed: int):
@@ -278,12 +280,12 @@ def run_ours(args, rank: int, world: int, device):
     seq = torch.from_numpy(wl["lens"].astype(np.int32)).to(device)
     # per layer, oscar_decode_step launches the step prologue (append with demotion, query rotation), then
     # the fused decode and the merge (mma), or the history kernel, the BF16 segment and the merge (simt)
-    launches_per_layer = 3 if args.algo == 1 else 4
+    launches_per_layer = (4 if wl["shp"] else 3) if args.algo == 1 else 4   # + the shared-prefix kernel
 
     def layers():
         for layer in range(nl):
             cache.decode_step(layer, q_cur[layer], kv_cur[layer, 0], kv_cur[layer, 1], seq, wl["hist_pt"],
-                              wl["bf16_pt"], sm, out=out[layer])
+                              wl["bf16_pt"], sm, out=out[layer], shared_hist_pages=wl["shp"])
         seq.add_(1)
 
     # capture one step (all layers) into a CUDA graph
@@ -338,7 +340,8 @@ def run_ours(args, rank: int, world: int, device):
     # dominant kernel: the fused decode kernel, timed per launch with the library's CUDA events in a second
     # timed region that issues the same steps without the graph
     dec_ms, dec_n, lens_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
-    hb = layer_bytes(lens_prof, H, hq)
+    # algorithmic bytes of one layer's decode: with a shared prefix read once for the batch, its pages count once
+    hb = shared_unique_bytes(lens_prof, wl["shared"], H, hq) if wl["shp"] else layer_bytes(lens_prof, H, hq)
     dec_avg_ms = dec_ms / max(dec_n, 1)
     achieved = hb / (dec_avg_ms / 1e3) / 1e9
     res = {
@@ -350,12 +353,15 @@ def run_ours(args, rank: int, world: int, device):
                    "storage": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
                    "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
-                   "launch": "one CUDA graph per step (oscar_decode_step per layer), new tokens copied in"},
+                   "launch": "one CUDA graph per step (oscar_decode_step%s per layer), new tokens copied in"
+                             % ("_shared, %d shared history pages" % wl["shp"] if wl["shp"] else "")},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
                 "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak,
                 "step_unique_bytes": step_unique, "step_unique_gbs": step_unique / (ms_step / 1e3) / 1e9},
-        "roofline": {"bound": "hbm", "kernel": ("k_decode_mma (fused INT2 history + BF16 pages)" if args.algo == 1
-                                                else "k_int2_simt (INT2 history)") +
+        "roofline": {"bound": "hbm", "kernel": ("k_decode_shared (shared-prefix pages, all requests) + "
+                                                if args.algo == 1 and wl["shp"] else "") +
+                     ("k_decode_mma (fused INT2 history + BF16 pages)" if args.algo == 1
+                      else "k_int2_simt (INT2 history)") +
                      ", CUDA events around each launch in an eager copy of the timed steps",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
@@ -394,7 +400,7 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
     for i in range(args.steps):
         for layer in range(nl):
             cache.decode_step(layer, q_all[i, layer], kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"],
-                              wl["bf16_pt"], sm, out=out[layer])
+                              wl["bf16_pt"], sm, out=out[layer], shared_hist_pages=wl["shp"])
         seq.add_(1)
     ms, n = cache.profile_read()
     return ms, n, lens0 + (args.steps - 1) // 2
@@ -510,7 +516,7 @@ def run_e2e_eager(wl, args, device, start_lens):
         dev_in.copy_(host_in, non_blocking=True)
         for layer in range(nl):
             cache.decode_step(layer, qn[layer], kvn[layer, 0], kvn[layer, 1], seq, wl["hist_pt"], wl["bf16_pt"], sm,
-                              out=dev_out[layer])
+                              out=dev_out[layer], shared_hist_pages=wl["shp"])
         host_out.copy_(dev_out.view(-1), non_blocking=True)
         seq.add_(1)
 

@@ -35,6 +35,7 @@ EXPORTS = (
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
     "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
+    "oscar_decode_attention_shared", "oscar_decode_step_shared",
     "oscar_trace_timeline", "oscar_check_wait_timeout",
 )
 
@@ -80,6 +81,10 @@ def _load() -> ctypes.CDLL:
         "oscar_trace_timeline": [vp, vp, c_int],
         "oscar_check_wait_timeout": [vp, vp],
         "oscar_decode_step": [vp, c_int, c_int, vp, vp, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
+        "oscar_decode_attention_shared": [vp, c_int, c_int, vp, i32p, i32p, c_int, c_int, i32p, c_float, vp, c_int,
+                                          vp, vp],
+        "oscar_decode_step_shared": [vp, c_int, c_int, vp, vp, vp, i32p, i32p, c_int, c_int, i32p, c_float, vp,
+                                     c_int, vp, vp],
         "oscar_decode_attention_noalloc": [ctypes.POINTER(Layout), vp, c_int, c_int, vp, i32p, i32p, c_int, i32p,
                                            c_float, vp, c_int, vp, vp, vp],
     }
@@ -232,7 +237,9 @@ class OscarCache:
                "oscar_append_kv")
 
     def decode_attention(self, layer: int, q, seq_lens, hist_pt, bf16_pt, sm_scale: float, out=None,
-                         out_dtype: int = OUT_BF16, lse=None, stream=None):
+                         out_dtype: int = OUT_BF16, lse=None, stream=None, shared_hist_pages: int = 0):
+        """Decode attention; shared_hist_pages > 0 states that history pages [0, shared_hist_pages) of every
+        request are the same pages (oscar_decode_attention_shared)."""
         import torch
         sl = _dev_i32(seq_lens, self.device)
         hp = _dev_i32(hist_pt, self.device)
@@ -240,14 +247,22 @@ class OscarCache:
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
                               device=self.device)
-        _check(_lib.oscar_decode_attention(self._h, layer, sl.numel(), _ptr(q), _ptr(sl), _ptr(hp),
-                                           hp.shape[1] if hp.dim() == 2 else 0, _ptr(bp), float(sm_scale), _ptr(out),
-                                           out_dtype, _ptr(lse), _stream(stream)), "oscar_decode_attention")
+        mhp = hp.shape[1] if hp.dim() == 2 else 0
+        if shared_hist_pages:
+            _check(_lib.oscar_decode_attention_shared(self._h, layer, sl.numel(), _ptr(q), _ptr(sl), _ptr(hp), mhp,
+                                                      int(shared_hist_pages), _ptr(bp), float(sm_scale), _ptr(out),
+                                                      out_dtype, _ptr(lse), _stream(stream)),
+                   "oscar_decode_attention_shared")
+        else:
+            _check(_lib.oscar_decode_attention(self._h, layer, sl.numel(), _ptr(q), _ptr(sl), _ptr(hp), mhp,
+                                               _ptr(bp), float(sm_scale), _ptr(out), out_dtype, _ptr(lse),
+                                               _stream(stream)), "oscar_decode_attention")
         return out
 
     def decode_step(self, layer: int, q, k, v, seq_lens_before, hist_pt, bf16_pt, sm_scale: float, out=None,
-                    out_dtype: int = OUT_BF16, lse=None, stream=None):
-        """append_kv(k, v) then decode_attention(q) over seq_lens_before + 1 tokens, in one call."""
+                    out_dtype: int = OUT_BF16, lse=None, stream=None, shared_hist_pages: int = 0):
+        """append_kv(k, v) then decode_attention(q) over seq_lens_before + 1 tokens, in one call
+        (oscar_decode_step_shared when shared_hist_pages > 0)."""
         import torch
         sl = _dev_i32(seq_lens_before, self.device)
         hp = _dev_i32(hist_pt, self.device)
@@ -255,9 +270,16 @@ class OscarCache:
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32 if out_dtype == OUT_FP32 else torch.bfloat16,
                               device=self.device)
-        _check(_lib.oscar_decode_step(self._h, layer, sl.numel(), _ptr(q), _ptr(k), _ptr(v), _ptr(sl), _ptr(hp),
-                                      hp.shape[1] if hp.dim() == 2 else 0, _ptr(bp), float(sm_scale), _ptr(out),
-                                      out_dtype, _ptr(lse), _stream(stream)), "oscar_decode_step")
+        mhp = hp.shape[1] if hp.dim() == 2 else 0
+        if shared_hist_pages:
+            _check(_lib.oscar_decode_step_shared(self._h, layer, sl.numel(), _ptr(q), _ptr(k), _ptr(v), _ptr(sl),
+                                                 _ptr(hp), mhp, int(shared_hist_pages), _ptr(bp), float(sm_scale),
+                                                 _ptr(out), out_dtype, _ptr(lse), _stream(stream)),
+                   "oscar_decode_step_shared")
+        else:
+            _check(_lib.oscar_decode_step(self._h, layer, sl.numel(), _ptr(q), _ptr(k), _ptr(v), _ptr(sl), _ptr(hp),
+                                          mhp, _ptr(bp), float(sm_scale), _ptr(out), out_dtype, _ptr(lse),
+                                          _stream(stream)), "oscar_decode_step")
         return out
 
     def set_decode_algo(self, algo: int):

@@ -358,11 +358,37 @@ int oscar_set_decode_algo(oscar_cache* c, int algo) {
   return OSCAR_OK;
 }
 
-int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens,
-                           const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, float sm_scale,
-                           void* out, int out_dtype, float* lse, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Splits of a decode call: the request's own history pages (from shared_pages on) by the split
+// policy, and on the tensor-core path the shared-prefix pages in one wave of CTAs (one per SM) over
+// the kv heads and 128-row query tiles, within the max_splits slot budget.
+void set_splits(const oscar_cache* c, int B, int max_hist_pages, int shared_pages, DecodeArgs& a) {
+  const int hkv = c->lay.num_kv_heads, gq = c->lay.num_q_heads / c->lay.num_kv_heads;
+  a.shared_pages = 0;
+  a.nsplit_shared = 0;
+  if (shared_pages > 0 && a.algo == OSCAR_DECODE_MMA && c->lay.max_splits >= 2) {
+    decode_split_policy(B, hkv, gq, a.nbf, max_hist_pages - shared_pages, c->lay.max_splits - 1, c->sms, a.algo,
+                        &a.nsplit, &a.pages_per_split);
+    const int qtiles = (B * gq + kSharedRows - 1) / kSharedRows;
+    int ns = std::max(1, c->sms / (hkv * qtiles));
+    ns = std::min(std::min(ns, shared_pages), c->lay.max_splits - a.nsplit);
+    a.shared_pages = shared_pages;
+    a.nsplit_shared = ns;
+    return;
+  }
+  decode_split_policy(B, hkv, gq, a.nbf, max_hist_pages, c->lay.max_splits, c->sms, a.algo, &a.nsplit,
+                      &a.pages_per_split);
+}
+
+int decode_impl(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens, const int32_t* hist_pt,
+                int max_hist_pages, int shared_pages, const int32_t* bf16_pt, float sm_scale, void* out,
+                int out_dtype, float* lse, void* stream) {
   if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || B > c->lay.max_batch || max_hist_pages < 0)
     return OSCAR_ERR_INVALID_ARG;
+  if (shared_pages < 0 || shared_pages > max_hist_pages) return OSCAR_ERR_INVALID_ARG;
   if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
   if (B == 0) return OSCAR_OK;
   if (!q || !seq_lens || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
@@ -384,8 +410,7 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   a.len_add = 0;
   a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
-  decode_split_policy(B, c->lay.num_kv_heads, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, max_hist_pages,
-                      c->lay.max_splits, c->sms, a.algo, &a.nsplit, &a.pages_per_split);
+  set_splits(c, B, max_hist_pages, shared_pages, a);
   a.ev0 = a.ev1 = nullptr;
   if (c->prof_on && c->prof_n < c->prof_cap) {
     a.ev0 = c->prof_ev[2 * c->prof_n];
@@ -395,11 +420,12 @@ int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, cons
   return launch_decode(view(c, layer), c->dws, a, st);
 }
 
-int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const void* k, const void* v,
-                      const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
-                      const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream) {
+int step_impl(oscar_cache* c, int layer, int B, const void* q, const void* k, const void* v,
+              const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages, int shared_pages,
+              const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream) {
   if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || B > c->lay.max_batch || max_hist_pages < 0)
     return OSCAR_ERR_INVALID_ARG;
+  if (shared_pages < 0 || shared_pages > max_hist_pages) return OSCAR_ERR_INVALID_ARG;
   if (out_dtype != OSCAR_OUT_BF16 && out_dtype != OSCAR_OUT_FP32) return OSCAR_ERR_INVALID_ARG;
   if (B == 0) return OSCAR_OK;
   if (!q || !k || !v || !seq_lens_before || !bf16_pt || !out || (max_hist_pages > 0 && !hist_pt))
@@ -423,8 +449,7 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
   a.lse = lse;
   a.algo = c->algo;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
-  decode_split_policy(B, c->lay.num_kv_heads, c->lay.num_q_heads / c->lay.num_kv_heads, a.nbf, max_hist_pages,
-                      c->lay.max_splits, c->sms, a.algo, &a.nsplit, &a.pages_per_split);
+  set_splits(c, B, max_hist_pages, shared_pages, a);
   a.ev0 = a.ev1 = nullptr;
   if (c->prof_on && c->prof_n < c->prof_cap) {
     a.ev0 = c->prof_ev[2 * c->prof_n];
@@ -437,6 +462,40 @@ int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const voi
                                  sm_scale, st);
   if (rc != OSCAR_OK) return rc;
   return launch_decode(lv, c->dws, a, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int oscar_decode_attention(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens,
+                           const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, float sm_scale,
+                           void* out, int out_dtype, float* lse, void* stream) {
+  return decode_impl(c, layer, B, q, seq_lens, hist_pt, max_hist_pages, 0, bf16_pt, sm_scale, out, out_dtype, lse,
+                     stream);
+}
+
+int oscar_decode_attention_shared(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens,
+                                  const int32_t* hist_pt, int max_hist_pages, int shared_hist_pages,
+                                  const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse,
+                                  void* stream) {
+  return decode_impl(c, layer, B, q, seq_lens, hist_pt, max_hist_pages, shared_hist_pages, bf16_pt, sm_scale, out,
+                     out_dtype, lse, stream);
+}
+
+int oscar_decode_step(oscar_cache* c, int layer, int B, const void* q, const void* k, const void* v,
+                      const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
+                      const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream) {
+  return step_impl(c, layer, B, q, k, v, seq_lens_before, hist_pt, max_hist_pages, 0, bf16_pt, sm_scale, out,
+                   out_dtype, lse, stream);
+}
+
+int oscar_decode_step_shared(oscar_cache* c, int layer, int B, const void* q, const void* k, const void* v,
+                             const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
+                             int shared_hist_pages, const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype,
+                             float* lse, void* stream) {
+  return step_impl(c, layer, B, q, k, v, seq_lens_before, hist_pt, max_hist_pages, shared_hist_pages, bf16_pt,
+                   sm_scale, out, out_dtype, lse, stream);
 }
 
 int oscar_get_status(oscar_cache* c, int* code) {

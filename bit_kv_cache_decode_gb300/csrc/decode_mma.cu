@@ -107,6 +107,8 @@ struct FusedArgs {
   int max_hist_pages;
   int nsplit;                        // history CTAs per group; the next nbf CTAs take one BF16 page each
   int nbf;
+  int hist_start;                    // first history page of the splits (the pages before are shared ones)
+  int bf_slot0;                      // partial slot of BF16 page 0
   const int* bf16_pt;
   const __nv_bfloat16* q;            // raw queries, for the BF16 tokens
   float scale_log2;                  // sm_scale * log2(e)
@@ -142,9 +144,12 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     npages = max_hist_pages;
     Lh = npages * kP;
   }
-  // The request's pages are spread evenly over the splits: split s starts at page floor(s npages / nsplit).
-  const int p0 = (int)((long long)split * npages / fa.nsplit) + w;
-  const int p1 = (int)((long long)(split + 1) * npages / fa.nsplit);
+  // The request's pages from hist_start on are spread evenly over the splits: split s starts at page
+  // hist_start + floor(s n / nsplit), n = npages - hist_start.
+  const int nown = npages - fa.hist_start;
+  if (nown < 0 && tid == 0 && split == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);   // shorter than the shared prefix
+  const int p0 = fa.hist_start + (int)((long long)split * max(nown, 0) / fa.nsplit) + w;
+  const int p1 = fa.hist_start + (int)((long long)(split + 1) * max(nown, 0) / fa.nsplit);
   const int my_pages = p0 < p1 ? (p1 - p0 + kWarps - 1) / kWarps : 0;
   const int* pt = hist_pt + (size_t)b * max_hist_pages;
 
@@ -558,7 +563,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh) {
       if (hh >= gq) break;
-      float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.nsplit + c);
+      float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.bf_slot0 + c);
       if (tid == 0) { part[0] = -INFINITY; part[1] = 0.f; }
       part[4 + tid] = 0.f;
     }
@@ -642,7 +647,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
       Ls += red[32 + ww * 8 + hh];
       A += ob[(ww * 8 + hh) * kObStride + tid];
     }
-    float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.nsplit + c);
+    float* part = part_row(ws, b, lv.hq, hq0 + hh, fa.bf_slot0 + c);
     if (tid == 0) { part[0] = M; part[1] = Ls; }
     part[4 + tid] = A;
   }
@@ -687,6 +692,8 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   fa.max_hist_pages = a.max_hist_pages;
   fa.nsplit = a.nsplit;
   fa.nbf = a.nbf;
+  fa.hist_start = a.shared_pages;
+  fa.bf_slot0 = a.nsplit + a.nsplit_shared;
   fa.bf16_pt = a.bf16_pt;
   fa.q = static_cast<const __nv_bfloat16*>(a.q);
   fa.scale_log2 = scale_log2;

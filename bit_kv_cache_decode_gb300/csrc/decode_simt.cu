@@ -359,13 +359,15 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
     if (rc != OSCAR_OK) return rc;
   }
   if (a.algo == OSCAR_DECODE_MMA) {
-    // one fused launch (history splits and BF16 pages), then the merge kernel; the profiled
-    // span is the fused launch alone (the events make it wait for the query prologue)
+    // the shared-prefix pages for all requests at once (if any), one fused launch for each request's
+    // own history pages and the BF16 pages, then the merge kernel; the profiled span is the decode
+    // launches (the events make them wait for the query prologue)
     if (a.ev0) cudaEventRecord(a.ev0, st);
-    const int rc = launch_decode_mma(lv, ws, a, scale_log2, st);
+    int rc = launch_decode_shared(lv, ws, a, st);
+    if (rc == OSCAR_OK) rc = launch_decode_mma(lv, ws, a, scale_log2, st);
     if (a.ev1) cudaEventRecord(a.ev1, st);
     if (rc != OSCAR_OK) return rc;
-    return launch_merge(lv, ws, a.B, a.nsplit, a.nbf, a.out, a.out_dtype, a.lse, st);
+    return launch_merge(lv, ws, a.B, a.nsplit + a.nsplit_shared, a.nbf, a.out, a.out_dtype, a.lse, st);
   }
   if (a.ev0) cudaEventRecord(a.ev0, st);     // profiled span: the history kernel
   k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
@@ -417,7 +419,7 @@ int configure_mma_kernels();   // decode_mma.cu
 
 int configure_decode_kernels() {
   if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
-  return OSCAR_OK;
+  return configure_shared_kernel();
 }
 
 }  // namespace oscar

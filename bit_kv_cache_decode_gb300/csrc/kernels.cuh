@@ -69,6 +69,8 @@ struct DecodeArgs {
   int nsplit;            // history splits launched per (request, kv head)
   int nbf;               // BF16 (sink + recent) chunks of 64 tokens per (request, kv head)
   int pages_per_split;   // history pages per split, at most (the tensor-core path spreads a request evenly)
+  int shared_pages = 0;  // tensor-core path: history pages [0, shared_pages) are the same for every request
+  int nsplit_shared = 0; // splits of the shared pages per kv head (their slots follow the nsplit history slots)
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
   int skip_qprep;        // the query prologue already ran (with the append, in one launch)
@@ -83,6 +85,9 @@ int launch_merge(const LayerView& lv, const DecodeWorkspace& ws, int B, int nspl
                  int out_dtype, float* lse, cudaStream_t st);
 constexpr int kMergeChunk = 96;            // partial slots staged in shared memory at a time by the merge
 int configure_merge_kernel();
+constexpr int kSharedRows = 128;   // query rows (request x head) per CTA of the shared-prefix decode
+int launch_decode_shared(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
+int configure_shared_kernel();
 
 // The kernels of the decode chain all ask for the largest shared-memory carveout: a grid scheduled
 // early beside its predecessor then never waits for an SM to drain and change its L1 / shared split.

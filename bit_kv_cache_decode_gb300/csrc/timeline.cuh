@@ -9,7 +9,8 @@
 namespace oscar {
 
 enum TimelineKind : int {
-  kTlAppend = 1, kTlQprep = 2, kTlDecodeMma = 3, kTlMerge = 4, kTlInt2Simt = 5, kTlBf16Seg = 6, kTlPrefill = 7
+  kTlAppend = 1, kTlQprep = 2, kTlDecodeMma = 3, kTlMerge = 4, kTlInt2Simt = 5, kTlBf16Seg = 6, kTlPrefill = 7,
+  kTlDecodeShared = 8
 };
 
 // record i lives at timeline[4 + 4 i]: {kind | layer << 8 | sm << 24 | linear CTA << 32, start, end, mark};

@@ -217,6 +217,33 @@ int oscar_decode_step(oscar_cache* cache, int layer, int B, const void* q, const
                       const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
                       const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse, void* stream);
 
+/* Shared-prefix variants (MarkTechPost article "Together AI 开源 OSCAR…",
+ * section "服务系统：混合精度缓存布局": the pool stays compatible with paged
+ * KV and prefix caching). The caller states that history pages
+ * [0, shared_hist_pages) of every request are the same pages: the entries
+ * hist_pt[r][0 .. shared_hist_pages) are equal for all r, and every request
+ * holds at least that many history pages. The result is the same as the
+ * call without the suffix.
+ *
+ * On the tensor-core path one extra kernel then reads each shared page once
+ * per step for all B x Hq / Hkv queries of its kv head, in CTAs of 128 query
+ * rows. Each page is expanded once into shared memory and both products run
+ * as 128-row tensor-core tiles. The per-request kernel covers only each
+ * request's own pages. The CUDA-core path ignores shared_hist_pages.
+ *
+ * With oscar_decode_step_shared, the token each step demotes must land in
+ * the request's own pages, so every request's history must already extend
+ * past the shared pages. Error behaviour is as in the plain calls, and
+ * 0 <= shared_hist_pages <= max_hist_pages is checked on the host. */
+int oscar_decode_attention_shared(oscar_cache* cache, int layer, int B, const void* q, const int32_t* seq_lens,
+                                  const int32_t* hist_pt, int max_hist_pages, int shared_hist_pages,
+                                  const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype, float* lse,
+                                  void* stream);
+int oscar_decode_step_shared(oscar_cache* cache, int layer, int B, const void* q, const void* k, const void* v,
+                             const int32_t* seq_lens_before, const int32_t* hist_pt, int max_hist_pages,
+                             int shared_hist_pages, const int32_t* bf16_pt, float sm_scale, void* out, int out_dtype,
+                             float* lse, void* stream);
+
 /* Choose the INT2 decode kernel (OSCAR_DECODE_MMA by default). */
 int oscar_set_decode_algo(oscar_cache* cache, int algo);
 

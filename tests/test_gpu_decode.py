@@ -68,13 +68,14 @@ def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64):
     return cache, prm, hist_pt, bf16_pt
 
 
-def _check(cache, prm, hist_pt, bf16_pt, lens, gq, v_mode, seed, out_dtype=1, kv_heads=None):
+def _check(cache, prm, hist_pt, bf16_pt, lens, gq, v_mode, seed, out_dtype=1, kv_heads=None, shared_pages=0):
     hkv = cache.cfg.num_kv_heads
     B = len(lens)
     q = queries(seed, 0, hkv, gq, batch=B)
     out = cache.decode_attention(0, to_dev_bf16(q), np.array(lens, np.int32), hist_pt, bf16_pt, synth.sm_scale(),
                                  out_dtype=out_dtype,
-                                 lse=(lse_t := torch.zeros(B, hkv * gq, device=DEV, dtype=torch.float32)))
+                                 lse=(lse_t := torch.zeros(B, hkv * gq, device=DEV, dtype=torch.float32)),
+                                 shared_hist_pages=shared_pages)
     assert cache.get_status() == 0
     got = out.double().cpu().numpy()
     lse = lse_t.double().cpu().numpy()
@@ -126,6 +127,54 @@ def test_shared_prefix_batch(algo):
     cache, prm, hp, bp = _build(lens, 2, 4, 0, seed=14, shared_prefix=64 + 64 * 20, algo=algo)
     assert (hp[0, :20] == hp[1, :20]).all() and (bp[:, 0] == bp[0, 0]).all()
     _check(cache, prm, hp, bp, lens, 4, 0, seed=14)
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_shared_prefix_kernel(v_mode, out_dtype):
+    # 3 requests sharing 20 history pages read once for all 12 query rows per kv head; the third
+    # request has no history pages of its own
+    lens = [64 + 64 * 20 + 300, 64 + 64 * 20 + 700, 64 + 64 * 20 + 256]
+    cache, prm, hp, bp = _build(lens, 2, 4, v_mode, seed=14, shared_prefix=64 + 64 * 20, algo=1)
+    _check(cache, prm, hp, bp, lens, 4, v_mode, seed=14, out_dtype=out_dtype, shared_pages=20)
+
+
+def test_shared_prefix_two_query_tiles():
+    # 20 requests x 8 query heads = 160 rows of one kv head: a full 128-row tile and a partial one;
+    # own history from 0 to 11 pages with ragged last pages
+    lens = [64 + 64 * 10 + 256 + 37 * r for r in range(20)]
+    cache, prm, hp, bp = _build(lens, 1, 8, 0, seed=16, shared_prefix=64 + 64 * 10, algo=1)
+    _check(cache, prm, hp, bp, lens, 8, 0, seed=16, shared_pages=10)
+
+
+def test_shared_prefix_steps():
+    # decode_step with the shared-prefix kernel against the plain decode_step on an identical cache:
+    # the same pools after 40 steps of append and demotion, outputs within the parity bound of each
+    # other at every step and of the oracle at the last one
+    B, hkv, gq, shp, S = 4, 2, 4, 12, 40
+    lens = [64 + 64 * shp + 64 * r + 10 + 256 for r in range(B)]
+    ca, prm, hp, bp = _build(lens, hkv, gq, 0, seed=17, shared_prefix=64 + 64 * shp, algo=1)
+    cb, _, _, _ = _build(lens, hkv, gq, 0, seed=17, shared_prefix=64 + 64 * shp, algo=1)
+    hp_d, bp_d = torch.from_numpy(hp).to(DEV), torch.from_numpy(bp).to(DEV)
+    rng = np.random.default_rng(5)
+    for s in range(S):
+        q = to_dev_bf16(rng.standard_normal((B, hkv * gq, 128)).astype(np.float32))
+        kn = to_dev_bf16(rng.standard_normal((B, hkv, 128)).astype(np.float32))
+        vn = to_dev_bf16(rng.standard_normal((B, hkv, 128)).astype(np.float32))
+        lb = torch.tensor([L + s for L in lens], dtype=torch.int32, device=DEV)
+        oa = ca.decode_step(0, q, kn, vn, lb, hp_d, bp_d, synth.sm_scale(), out_dtype=osc.OUT_FP32,
+                            shared_hist_pages=shp)
+        ob = cb.decode_step(0, q, kn, vn, lb, hp_d, bp_d, synth.sm_scale(), out_dtype=osc.OUT_FP32)
+        err = ((oa - ob).abs().amax(-1) / ob.abs().amax(-1)).max().item()
+        assert err <= 2 * TOL, (s, err)
+    assert ca.get_status() == 0 and cb.get_status() == 0
+    assert torch.equal(ca.pool, cb.pool)
+    pm = pool_from_device(ca, 0)
+    qn = q.float().cpu().numpy().astype(np.float64)
+    got = oa.double().cpu().numpy()
+    for r in range(B):
+        ref, _ = A.decode_request(qn[r], lens[r] + S, pm, hp[r], bp[r], prm, True, synth.sm_scale())
+        assert row_rel_err(got[r], ref).max() <= TOL, r
 
 
 @pytest.mark.parametrize("algo", ALGOS)

@@ -1,4 +1,5 @@
-// Shared-prefix history decode on the tensor cores (sm_103a).
+// Shared-prefix history decode on the 5th-generation tensor cores (sm_103a:
+// tcgen05.mma with TMEM accumulators).
 //
 // MarkTechPost article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存
 // 布局": the pool stays compatible with paged KV and prefix caching, so requests
@@ -6,25 +7,27 @@
 // page tables. This kernel reads each shared page once per step for all the
 // batch's queries of a kv head, instead of once per request.
 //
-// Work: grid (split, kv head, query tile); 8 warps. A CTA takes the shared
-// pages [p0, p1) of its split and the query tile's 128 query rows (request r,
-// head i flattened as r * gq + i), warp w owning rows 16 w .. 16 w + 15.
-//  * Each page (5120 B block: K codes | V codes | K meta | V meta) arrives by
-//    one bulk copy in a 3-stage ring. The CTA expands it once into shared
-//    memory: K as the fp16 numbers 1024 + 256 c (every code moved into mantissa
-//    bits 8-9, so the constant part is 4x the code term at most), V as its
-//    exact codes c. Page i + 1 is expanded while page i is consumed
-//    (double-buffered).
-//  * Logits: mma.m16n8k16 with A = K rows (ldmatrix), B = fragments of the
-//    warp's queries (q~ 2^sigma / 256 as fp16 high + low parts, one column
-//    each), one accumulator per channel group started from minus the
-//    fragments' 1024 * sum, then scale / zero per token and group as in the
-//    per-request kernel.
-//  * P.V: A = the V codes transposed (rows = channels; ldmatrix), B = the
-//    weights times the token's V scale of the tile's channel group (fp16),
-//    built from the logits' accumulator layout with movmatrix transposes; the
-//    zero-point part sum_t p_t z_t is accumulated in fp32 per group, as in the
-//    per-request kernel.
+// Work: grid (split, kv head, query tile); a CTA takes the shared pages
+// [p0, p1) of its split and 128 query rows (request r, head i flattened as
+// r * gq + i). Per page (64 tokens, both products with M = 128 query rows):
+//  * S = Q K^T: A = the rows' fragments q~ 2^sigma / 256 as fp16 high and low
+//    parts (two MMAs into one accumulator), B = the page's K codes expanded to
+//    fp16 1024 + 256 c (every code moved into mantissa bits 8-9); one TMEM
+//    accumulator (64 columns) per channel group. The constant part is
+//    subtracted in fp32 afterwards (1024 * the fragments' sum per group).
+//  * Each row thread reads its row's 64 logits from TMEM, applies the tokens'
+//    scale and zero, and updates its online softmax. Its maximum is updated
+//    lazily: the output accumulator is rescaled only when the maximum grows by
+//    more than 2^8, so the weights stay below 2^8 and fp16-safe.
+//  * O += P V: A = the weights times the token's V scale of each channel group
+//    (fp16), B = the V codes (exact small integers, rows = channels); the
+//    zero-point part sum_t p_t z_t is accumulated in fp32 by the row thread.
+// Operands sit in shared memory in the no-swizzle K-major canonical layout
+// (8-row x 16-byte core matrices). Warp roles: warps 0-3 own the 128 rows (TMEM
+// lanes), warp 4 issues the bulk copies and the MMAs (one thread), warps 5-7
+// expand pages. S is double-buffered in TMEM, so S of page i + 1 runs on the
+// tensor cores while the rows finish page i. Every wait is bounded; a CTA
+// whose wait expires flags OSCAR_STATUS_TIMEOUT and writes empty partials.
 // Each CTA writes one partial (m, l, acc[128]) per query row into the history
 // slot `slot0 + split`; the merge kernel combines it with the request's other
 // slots.
@@ -35,52 +38,98 @@
 namespace oscar {
 namespace {
 
-constexpr int kShWarps = 8;
-constexpr int kShThreads = kShWarps * 32;
-constexpr int kShQ = 16 * kShWarps;                   // query rows per CTA
+constexpr int kRowWarps = 4, kCtlWarp = 4, kExpWarp0 = 5, kExpWarps = 3;
+constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 256
+constexpr int kExpThreads = 32 * kExpWarps;
+constexpr int kShQ = 32 * kRowWarps;                                  // query rows per CTA
 static_assert(kShQ == kSharedRows, "the host's query tiles");
 constexpr int kShStages = 3;
-constexpr int kKhStride = kD + 8;                     // fp16 per expanded K row: 272 B
-constexpr int kVtStride = kP + 8;                     // fp16 per expanded V^T row: 144 B
-constexpr int kKhBytes = kP * kKhStride * 2;          // 17,408
-constexpr int kVtBytes = kD * kVtStride * 2;          // 18,432
-constexpr int kShFragWords = kShWarps * 8 * 4 * 32 * 2;   // [warp][k-block][n-tile][lane][2]: 64 KB
-// per query row: F, the fragment scale 2^sigma / 256, Z0, Z1, and the offsets 1024 sum(high + low) of
-// channel groups 0 and 1; the pairs read as float2 sit at even indices
-constexpr int kShConst = 8;
-constexpr int kCF = 0, kCScale = 1, kCZ = 2, kCOff = 4;
 constexpr uint32_t kMagic = 0x64006400u;              // fp16 1024.0 in both halves
 constexpr uint32_t kCodeMask = 0x03000300u;           // mantissa bits 8-9 of both halves
+constexpr float kLazyRescale = 8.f;                   // log2 growth of a row maximum that forces a rescale
 
-// shared-memory layout (bytes)
+// shared memory (bytes; every operand 1024-byte aligned)
+constexpr int kQBytes = kShQ * kD * 2;                // one part of the rows' fragments: 32 KB
+constexpr int kKhBytes = kP * kD * 2;                 // expanded K of a page: 16 KB
+constexpr int kVtBytes = kD * kP * 2;                 // expanded V^T of a page: 16 KB
+constexpr int kPBytes = kShQ * kP * 2;                // weights of one channel group: 16 KB
 constexpr int kOffRing = 0;
-constexpr int kOffKh = kOffRing + kShStages * kBlockBytes;          // 2 buffers
-constexpr int kOffVt = kOffKh + 2 * kKhBytes;                       // 2 buffers
-constexpr int kOffFrag = kOffVt + 2 * kVtBytes;
-constexpr int kOffConst = kOffFrag + kShFragWords * 4;
-constexpr int kOffBar = kOffConst + kShQ * kShConst * 4;
-constexpr int kShSmem = kOffBar + kShStages * 8 + 8 + 128;          // + a timeout flag, + alignment slack
-static_assert(kShQ * kD * 4 <= 2 * kKhBytes + 2 * kVtBytes, "q~ staging fits in the expansion buffers");
+constexpr int kOffQ = 15360;                          // kShStages * kBlockBytes, 1024-aligned
+constexpr int kOffKh = kOffQ + 2 * kQBytes;           // 2 buffers
+constexpr int kOffVt = kOffKh + 2 * kKhBytes;         // 2 buffers
+constexpr int kOffP = kOffVt + 2 * kVtBytes;          // 2 groups
+constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kNumBars = 14;
+constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
+static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
+static_assert(kShQ * kD * 4 <= 2 * kKhBytes + 2 * kVtBytes + 2 * kPBytes, "q~ staging fits");
+// mbarrier indices
+constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 5, kBarSFree = 7, kBarPReady = 9, kBarODone = 10,
+              kBarBufFree = 11;
+// TMEM columns: S buffers at 0 and 128 (group G at + 64 G), O at 256 (group G at + 64 G)
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
+// UMMA shared-memory descriptor: no swizzle, K-major; lbo = byte step between the core matrices of a row
+// block along K, sbo = byte step between 8-row blocks.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
+// instruction descriptor of kind::f16: D f32, A and B f16, both K-major, M = 128, N = 64
+constexpr uint32_t kIdesc = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, bool accumulate) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mbar_init_n(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(x));
-  return d;
+// 32 columns of this warp's 32 TMEM lanes (one row per thread)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,"
+      "%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
@@ -88,64 +137,64 @@ __device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t m
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
   return d;
 }
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
   const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
                             *reinterpret_cast<const __half2*>(&c));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
 // fp16 rounding of a fragment value, subnormal results flushed to zero
 __device__ __forceinline__ float frag_round16(float x) {
   const float r = __half2float(__float2half_rn(x));
   return fabsf(r) < 6.103515625e-05f ? 0.f : r;
 }
-
-// The 2-bit code i (bits 2i) of both 16-bit halves of x, moved to bits 8-9 and fed as fp16
-// 1024 + 256 c (i is a compile-time constant after unrolling).
+// The 2-bit code i (bits 2i, i may be a run-time value) of both 16-bit halves of x, moved to bits 8-9 and
+// fed as fp16 1024 + 256 c.
 __device__ __forceinline__ uint32_t code_at(uint32_t x, int i) {
   const uint32_t y = i < 4 ? (x << (8 - 2 * i)) : (x >> (2 * i - 8));
   return and_or(y, kCodeMask, kMagic);
 }
-
-// Expanded V^T: row = channel; the fp16 pair of tokens (2p, 2p+1) sits in 16-byte chunk (p / 4) ^ ((row / 8) % 8)
-// of the row, word p % 4. The 8 rows an ldmatrix reads share one swizzle (conflict-free with the padded rows),
-// the expansion's stores spread over the banks, and an ldmatrix address is a per-lane base plus a constant.
-__device__ __forceinline__ int vt_word(int row, int p) {
-  return row * (kVtStride / 2) + 4 * ((p >> 2) ^ ((row >> 3) & 7)) + (p & 3);
+// Byte offset of element (row, k) of a K-major operand in the canonical no-swizzle layout, rows of
+// kcols elements: core matrix (row / 8, k / 8) at (row / 8) * (kcols / 8) * 128 + (k / 8) * 128.
+__device__ __forceinline__ int canon_off(int row, int k, int kcols) {
+  return (row >> 3) * (kcols / 8) * 128 + (k >> 3) * 128 + (row & 7) * 16 + (k & 7) * 2;
 }
 
 
-// Expand one packed page block into the K and V^T buffers (all threads; 2 K words and 2 V words each).
-__device__ __forceinline__ void expand_page(const uint8_t* blk, __half* kh, uint32_t* vt) {
+// Expand one packed page block into K (rows = tokens, K-major over the 128 channel positions) and V^T
+// (rows = channels, K-major over the 64 tokens); et = 0 .. kExpThreads - 1 is the expanding thread.
+// K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel 16u + 8 + q (the
+// query fragments use the same order).
+__device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, int et) {
+  for (int wi = et; wi < kP * (kD / 16); wi += kExpThreads) {   // K: token t, channels 16u .. 16u + 15
+    const int t = (wi & 7) + 8 * (wi >> 6), u = (wi >> 3) & 7;   // a quarter warp: 8 consecutive tokens
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + t * 32 + 4 * u);
+    *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u, kD)) =
+        make_uint4(code_at(x, 0), code_at(x, 1), code_at(x, 2), code_at(x, 3));
+    *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u + 8, kD)) =
+        make_uint4(code_at(x, 4), code_at(x, 5), code_at(x, 6), code_at(x, 7));
+  }
+  for (int vi = et; vi < (kD / 8) * (kP / 8); vi += kExpThreads) {   // V: octet o (channels 8o ..), tokens 8 kb ..
+    const int o = vi >> 3, kb = vi & 7;
+    uint32_t x[4];
 #pragma unroll
-  for (int k2 = 0; k2 < 2; ++k2) {
-    const int wi = threadIdx.x + kShThreads * k2;              // 0 .. 511
-    {                                                          // K: token tk, channels 16 u .. 16 u + 15
-      const int tk = wi >> 3, u = wi & 7;
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + tk * 32 + 4 * u);
-      // fp16 pair r_i = (channel 16u + i, channel 16u + 8 + i) goes to positions 2i, 2i + 1 of the block
-      uint4* dst = reinterpret_cast<uint4*>(kh + tk * kKhStride + 16 * u);
-      dst[0] = make_uint4(code_at(x, 0), code_at(x, 1), code_at(x, 2), code_at(x, 3));
-      dst[1] = make_uint4(code_at(x, 4), code_at(x, 5), code_at(x, 6), code_at(x, 7));
-    }
-    {                                                          // V: tokens 2p, 2p + 1, channels 8 o .. 8 o + 7
-      const int p = wi >> 4, o = wi & 15;
-      const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kVCodesOff + p * 64 + 4 * o);
+    for (int pp = 0; pp < 4; ++pp)
+      x[pp] = *reinterpret_cast<const uint32_t*>(blk + kVCodesOff + (4 * kb + pp) * 64 + 4 * o);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)                              // the exact codes: (1024 + 256 c) / 256 - 4 = c
-        vt[vt_word(8 * o + i, p)] = hfma2_u(code_at(x, i), 0x1C001C00u, 0xC400C400u);
+    for (int ii = 0; ii < 8; ++ii) {
+      const int i = (ii + kb) & 7;                 // staggered: the quarter warp's stores hit distinct banks
+      uint32_t c[4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) c[pp] = hfma2_u(code_at(x[pp], i), 0x1C001C00u, 0xC400C400u);   // exact c
+      *reinterpret_cast<uint4*>(vt + canon_off(8 * o + i, 8 * kb, kP)) = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
 }
@@ -160,329 +209,342 @@ struct SharedArgs {
 
 __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, DecodeWorkspace ws, SharedArgs sa) {
   TimelineSpan timeline_span(lv, kTlDecodeShared);
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
-  __shared__ int page_ok[kShStages];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int split = blockIdx.x, h = blockIdx.y, qt = blockIdx.z;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int gq = lv.hq / lv.hkv, nq = sa.B * gq;
   uint8_t* ring = smem + kOffRing;
-  uint32_t* frag_s = reinterpret_cast<uint32_t*>(smem + kOffFrag);
-  float* qc_s = reinterpret_cast<float*>(smem + kOffConst);
-  const uint32_t bar0 = smem_addr(smem + kOffBar);
+  const uint32_t bar = smem_addr(smem + kOffBar);
+  auto B_ = [&](int k) { return bar + 8 * k; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + kNumBars * 8);
+  volatile int* failed = reinterpret_cast<volatile int*>(smem + kOffBar + kNumBars * 8 + 4);
 
   const int np = sa.shared_pages;
   const int p0 = (int)((long long)split * np / sa.nsplit);
   const int n = (int)((long long)(split + 1) * np / sa.nsplit) - p0;
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < kShStages; ++s) mbar_init(bar0 + 8 * s);
-  }
-  __syncthreads();
-  // page k of the split into stage k % 3 (thread 0); the step prologue never writes shared pages, so
-  // the first ones are requested before the programmatic wait
-  int issued_n = 0;                                // pages requested so far (thread 0)
-  auto issue = [&](int k) {
-    issued_n = k + 1;
+  // page k of the split into ring stage k % 3 (the control thread); the step prologue never writes
+  // shared pages, so the first ones are requested before the programmatic wait
+  auto issue = [&](int k) -> bool {
     const int pid = __ldcg(sa.hist_pt + p0 + k);
-    const bool ok = pid >= 0 && pid < lv.n_int2;
-    if (ok) {
-      bulk_load_hint(smem_addr(ring + (k % kShStages) * kBlockBytes), int2_block(lv, pid, h), kBlockBytes,
-                     bar0 + 8 * (k % kShStages), l2_evict_first());
-    } else {
+    if (pid < 0 || pid >= lv.n_int2) {
       flag(lv.status, OSCAR_STATUS_BAD_PAGE);
+      return false;
     }
-    page_ok[k % kShStages] = ok;
+    bulk_load_hint(smem_addr(ring + (k % kShStages) * kBlockBytes), int2_block(lv, pid, h), kBlockBytes,
+                   B_(kBarRing + k % kShStages), l2_evict_first());
+    return true;
   };
-  if (tid == 0) {
-    for (int k = 0; k < kShStages && k < n; ++k) issue(k);
+  if (w == kCtlWarp) {
+    if (lane == 0) {
+      mbar_init_n(B_(kBarRing + 0), 1);
+      mbar_init_n(B_(kBarRing + 1), 1);
+      mbar_init_n(B_(kBarRing + 2), 1);
+      mbar_init_n(B_(kBarExp + 0), kExpThreads);
+      mbar_init_n(B_(kBarExp + 1), kExpThreads);
+      mbar_init_n(B_(kBarSDone + 0), 1);
+      mbar_init_n(B_(kBarSDone + 1), 1);
+      mbar_init_n(B_(kBarSFree + 0), 32 * kRowWarps);
+      mbar_init_n(B_(kBarSFree + 1), 32 * kRowWarps);
+      mbar_init_n(B_(kBarPReady), 32 * kRowWarps);
+      mbar_init_n(B_(kBarODone), 1);
+      mbar_init_n(B_(kBarBufFree + 0), 1);
+      mbar_init_n(B_(kBarBufFree + 1), 1);
+      mbar_init_n(B_(13), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      *failed = 0;
+      bool ok = true;
+      for (int k = 0; k < kShStages && k < n; ++k) ok = issue(k) && ok;
+      if (!ok) *failed = 1;
+    }
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   pdl_launch_dependents();
   pdl_wait();                                      // q~ and its constants come from the step prologue
-
-  // ---- the tile's query rows: q~ staged in the expansion buffers, then fragments and constants ----
-  float* qs = reinterpret_cast<float*>(smem + kOffKh);          // [kShQ][kD]
-  for (int e = tid; e < kShQ * kD / 4; e += kShThreads) {
-    const int ql = e / (kD / 4), c4 = e % (kD / 4), Q = qt * kShQ + ql;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (Q < nq) {
-      const int r = Q / gq, hq = h * gq + Q % gq;
-      v = *reinterpret_cast<const float4*>(ws.qrot + ((size_t)r * lv.hq + hq) * kD + 4 * c4);
-    }
-    reinterpret_cast<float4*>(qs)[e] = v;
-  }
+  tc_fence_before();
   __syncthreads();
-  // per row (warp w: rows w, w + 8, ...): F, Z0, Z1 and the fragment offsets 1024 * sum(part) per group
-  for (int ql = w; ql < kShQ; ql += kShWarps) {
-    const int Q = qt * kShQ + ql;
-    float F = 0.f, Z0 = 0.f, Z1 = 0.f, sig = 0.f;
-    if (Q < nq) {
-      const float* qc = ws.qconst + ((size_t)(Q / gq) * lv.hq + h * gq + Q % gq) * kQConst;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- the rows' fragments (row warps: thread = row): q~ 2^sigma / 256 as fp16 high and low parts ----
+  const int q = tid;                               // row of this thread (row warps)
+  const int Q = qt * kShQ + q;
+  const bool valid = w < kRowWarps && Q < nq;
+  float F = 0.f, Z0 = 0.f, Z1 = 0.f, off0 = 0.f, off1 = 0.f;
+  if (w < kRowWarps) {
+    float sig = 0.f;
+    const float* qrow = nullptr;
+    if (valid) {
+      const size_t row = (size_t)(Q / gq) * lv.hq + h * gq + Q % gq;
+      const float* qc = ws.qconst + row * kQConst;
       F = qc[kQF];
       Z0 = qc[kQZ0];
       Z1 = qc[kQZ1];
       sig = qc[kQSigma];
+      qrow = ws.qrot + row * kD;
     }
-    const float sc = exp2f(sig - 8.f);             // fragment value x = q~ 2^sigma / 256
-    float offh = 0.f, offl = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {                  // lane l: channels 4l .. 4l + 3 (group l / 16)
-      const float x = qs[ql * kD + 4 * lane + e] * sc;
-      const float hi = frag_round16(x);
-      offh += hi;
-      offl += frag_round16(x - hi);
-    }
-#pragma unroll
-    for (int m = 1; m < 16; m <<= 1) {
-      offh += __shfl_xor_sync(0xffffffffu, offh, m);
-      offl += __shfl_xor_sync(0xffffffffu, offl, m);
-    }
-    if (lane == 0) {
-      qc_s[ql * kShConst + kCF] = F;
-      qc_s[ql * kShConst + kCScale] = sc;
-      qc_s[ql * kShConst + kCZ] = Z0;
-      qc_s[ql * kShConst + kCZ + 1] = Z1;
-    }
-    if (lane == 0 || lane == 16) qc_s[ql * kShConst + kCOff + (lane >> 4)] = 1024.f * offh + 1024.f * offl;
-  }
-  __syncthreads();
-  // B fragments: word (warp ww, k-block kb, n-tile nb, part, lane (g', t'), r) holds, for row
-  // 16 ww + 8 nb + g' and its high (part 0) or low (part 1) fp16 parts, the channels at k rows 2t' + 8r
-  // and 2t' + 8r + 1 of the k-block: 16 kb + t' + 4r and 16 kb + 8 + t' + 4r (the expanded K rows hold
-  // channel i of a 16-channel block at position 2i, channel 8 + i at 2i + 1). Both parts accumulate
-  // into the same column.
-  for (int wi = tid; wi < kShFragWords; wi += kShThreads) {
-    const int r = wi & 1, lp = (wi >> 1) & 31, part = (wi >> 6) & 1, nb = (wi >> 7) & 1, kb = (wi >> 8) & 7,
-              ww = wi >> 11;
-    const int ql = 16 * ww + 8 * nb + (lp >> 2), tp = lp & 3;
-    const float sc = qc_s[ql * kShConst + kCScale];
-    const int c0 = 16 * kb + tp + 4 * r;
-    float x[2] = {qs[ql * kD + c0] * sc, qs[ql * kD + c0 + 8] * sc};
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float hi = frag_round16(x[e]);
-      x[e] = part ? frag_round16(x[e] - hi) : hi;
-    }
-    frag_s[wi] = pack_f16x2(x[0], x[1]);
-  }
-  __syncthreads();
-  // the lane's 4 query rows j = 2 nb + e: row 16 w + 8 nb + 2t + e (n-tile nb, accumulator column 2t + e)
-  auto qrow = [&](int j) { return 16 * w + 8 * (j >> 1) + 2 * t + (j & 1); };
-  float cF[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) cF[j] = qc_s[qrow(j) * kShConst + kCF];
-  __syncthreads();                                 // q~ staging is done: the buffers take pages now
-
-  // ---- running state: vacc[b][mt] = channels 16 mt + g (+ 8), rows 8b + 2t (+ 1) --------------------
-  float vacc[2][8][4];
-#pragma unroll
-  for (int b = 0; b < 2; ++b)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) vacc[b][mt][e] = 0.f;
-  float mrun[4], lsum[4], zacc[4][2];             // zacc[j][G]: sum of p z over the lane's tokens, group G
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    mrun[j] = -INFINITY;
-    lsum[j] = 0.f;
-    zacc[j][0] = zacc[j][1] = 0.f;
-  }
-  bool timed_out = false;
-  auto wait_page = [&](int k) {                    // every thread; page k was issued if page_ok says so
-    const int s = k % kShStages;
-    if (page_ok[s] && !mbar_wait(bar0 + 8 * s, (k / kShStages) & 1)) timed_out = true;
-  };
-  auto kh_of = [&](int buf) { return reinterpret_cast<__half*>(smem + kOffKh + buf * kKhBytes); };
-  auto vt_of = [&](int buf) { return reinterpret_cast<uint32_t*>(smem + kOffVt + buf * kVtBytes); };
-  if (n > 0) {
-    wait_page(0);
-    if (page_ok[0] && !timed_out) expand_page(ring, kh_of(0), vt_of(0));
-  }
-  timed_out = __syncthreads_or(timed_out);
-
-  for (int i = 0; i < n && !timed_out; ++i) {
-    const int s = i % kShStages, s1 = (i + 1) % kShStages;
-    const bool ok_i = page_ok[s];
-    if (i + 1 < n) {                               // expand page i + 1 while page i is consumed
-      wait_page(i + 1);
-      if (page_ok[s1] && !timed_out) expand_page(ring + s1 * kBlockBytes, kh_of((i + 1) & 1), vt_of((i + 1) & 1));
-    }
-    if (ok_i) {
-      const uint8_t* blk = ring + s * kBlockBytes;
-      const uint32_t kh_a = smem_addr(kh_of(i & 1)), vt_a = smem_addr(vt_of(i & 1));
-      // this lane's ldmatrix row of V^T (vrow = lane % 8 + 8 hr) and chunk parity (token half h)
-      const int hr = (lane >> 3) & 1, hh = lane >> 4;
-      const uint32_t vt_lane = vt_a + ((lane & 7) + 8 * hr) * kVtStride * 2 + 16 * (hh ^ hr);
-      // ---- logits of the page's 64 tokens for the warp's 16 rows -----------------------------------
-      float lg[4][4][2];                           // [token tile m][query j][token 16m + g, 16m + g + 8]
+    const float sc = exp2f(sig - 8.f);
+    uint8_t* qh = smem + kOffQ;
+    uint8_t* qlo = smem + kOffQ + kQBytes;
+    float oh0 = 0.f, oh1 = 0.f, ol0 = 0.f, ol1 = 0.f;   // sums of the high and low parts per group
 #pragma unroll 1
-      for (int G = 0; G < 2; ++G) {
-        uint32_t bq[4][2][2][2];                   // [k-block 4G + kk][n-tile][part][reg]
+    for (int cc = 0; cc < 4; ++cc) {               // channels 32 cc .. 32 cc + 31: 16-channel blocks 2cc, 2cc + 1
+      float x[32];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+      for (int e = 0; e < 8; ++e) {
+        const float4 v = valid ? *reinterpret_cast<const float4*>(qrow + 32 * cc + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[4 * e] = v.x * sc;
+        x[4 * e + 1] = v.y * sc;
+        x[4 * e + 2] = v.z * sc;
+        x[4 * e + 3] = v.w * sc;
+      }
 #pragma unroll
-          for (int nb = 0; nb < 2; ++nb)
+      for (int ub = 0; ub < 2; ++ub) {
+        const int u = 2 * cc + ub, G = u >> 2;
 #pragma unroll
-            for (int pt = 0; pt < 2; ++pt) {
-              const uint2 v = *reinterpret_cast<const uint2*>(
-                  frag_s + (((((w * 8 + 4 * G + kk) * 2 + nb) * 2 + pt) * 32 + lane) * 2));
-              bq[kk][nb][pt][0] = v.x;
-              bq[kk][nb][pt][1] = v.y;
+        for (int half = 0; half < 2; ++half) {     // k-block 2u + half: channel pairs (16u + j, 16u + 8 + j)
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            const int j = 4 * half + pr;
+            const float xa = x[16 * ub + j], xb = x[16 * ub + 8 + j];
+            const float ha = frag_round16(xa), hb = frag_round16(xb);
+            const float la = frag_round16(xa - ha), lb = frag_round16(xb - hb);
+            if (G == 0) {
+              oh0 += ha + hb;
+              ol0 += la + lb;
+            } else {
+              oh1 += ha + hb;
+              ol1 += la + lb;
             }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float acc[2][4];                         // n-tile nb: rows 8 nb + 2t (0, 2), + 1 (1, 3)
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-            const float o0 = qc_s[qrow(2 * nb) * kShConst + kCOff + G];
-            const float o1 = qc_s[qrow(2 * nb + 1) * kShConst + kCOff + G];
-            acc[nb][0] = acc[nb][2] = -o0;
-            acc[nb][1] = acc[nb][3] = -o1;
+            hw[pr] = pack_f16x2(ha, hb);
+            lw[pr] = pack_f16x2(la, lb);
           }
-          const uint32_t arow = kh_a + ((16 * m + (lane & 7) + 8 * ((lane >> 3) & 1)) * kKhStride + 8 * (lane >> 4)) * 2;
+          *reinterpret_cast<uint4*>(qh + canon_off(q, 16 * u + 8 * half, kD)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(qlo + canon_off(q, 16 * u + 8 * half, kD)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+    }
+    off0 = 1024.f * oh0 + 1024.f * ol0;            // the constant part 1024 * sum(high + low) per group
+    off1 = 1024.f * oh1 + 1024.f * ol1;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the fragments
+  }
+  __syncthreads();
+
+  if (w == kCtlWarp) {
+    // ---- control: the MMAs of every page and the ring's bulk copies (one thread) ----------------------
+    if (lane == 0) {
+      const uint32_t qh_a = smem_addr(smem + kOffQ), ql_a = qh_a + kQBytes, p_a = smem_addr(smem + kOffP);
+      const uint32_t kh_a = smem_addr(smem + kOffKh), vt_a = smem_addr(smem + kOffVt);
+      auto issue_s = [&](int i) {                  // S_G = Q_G K_G^T into TMEM columns 128 (i % 2) + 64 G
+        const int b = i & 1;
+#pragma unroll
+        for (int G = 0; G < 2; ++G)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(arow + (16 * (4 * G + kk)) * 2, a0, a1, a2, a3);
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-              mma16816(acc[nb], a0, a1, a2, a3, bq[kk][nb][0][0], bq[kk][nb][0][1]);   // high parts
-              mma16816(acc[nb], a0, a1, a2, a3, bq[kk][nb][1][0], bq[kk][nb][1][1]);   // low parts
-            }
+            const uint32_t koff = (8 * G + 2 * kk) * 128;                 // k-blocks 8G + 2kk and + 1
+            const uint64_t bd = umma_desc(kh_a + b * kKhBytes + koff, 128, (kD / 8) * 128);
+            const uint32_t d = tmem + kColS + 128 * b + 64 * G;
+            umma(d, umma_desc(qh_a + koff, 128, (kD / 8) * 128), bd, kk > 0);
+            umma(d, umma_desc(ql_a + koff, 128, (kD / 8) * 128), bd, true);
           }
-          const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + (16 * m + g) * 8);
-          const uint2 mk1 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + (16 * m + g + 8) * 8);
-          const float2 sz0 = __half22float2(*reinterpret_cast<const __half2*>(G == 0 ? &mk0.x : &mk0.y));
-          const float2 sz1 = __half22float2(*reinterpret_cast<const __half2*>(G == 0 ? &mk1.x : &mk1.y));
-          if (G == 0) {
-            const float2 zz0 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.y));   // group 1 of row g
-            const float2 zz1 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
+        umma_commit(B_(kBarSDone + b));
+      };
+      bool ok = !*failed;
+      if (ok && n > 0) {
+        ok = mbar_wait(B_(kBarExp + 0), 0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int i = 0; i < n && ok; ++i) {
+        if (*failed) {
+          ok = false;
+          break;
+        }
+        const int b = i & 1;
+        if (i + 1 < n) {                           // S of page i + 1 runs while the rows finish page i
+          const int b1 = (i + 1) & 1;
+          ok = mbar_wait(B_(kBarExp + b1), ((i + 1) >> 1) & 1);
+          if (ok && i + 1 >= 2) ok = mbar_wait(B_(kBarSFree + b1), ((i - 1) >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        ok = mbar_wait(B_(kBarPReady), i & 1);     // the rows' weights of page i
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 zc = *reinterpret_cast<const float2*>(qc_s + qrow(j) * kShConst + kCZ);   // Z0, Z1
-              lg[m][j][0] = fmaf(cF[j] * sz0.x, acc[j >> 1][j & 1], fmaf(sz0.y, zc.x, zz0.y * zc.y));
-              lg[m][j][1] = fmaf(cF[j] * sz1.x, acc[j >> 1][2 + (j & 1)], fmaf(sz1.y, zc.x, zz1.y * zc.y));
-            }
-          } else {
+        for (int G = 0; G < 2; ++G)                // O_G += P_G V_G^T, TMEM columns 256 + 64 G
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              lg[m][j][0] = fmaf(cF[j] * sz0.x, acc[j >> 1][j & 1], lg[m][j][0]);
-              lg[m][j][1] = fmaf(cF[j] * sz1.x, acc[j >> 1][2 + (j & 1)], lg[m][j][1]);
-            }
+          for (int kk = 0; kk < 4; ++kk)
+            umma(tmem + kColO + 64 * G, umma_desc(p_a + G * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
+                 umma_desc(vt_a + b * kVtBytes + G * 8 * (kP / 8) * 128 + 2 * kk * 128, 128, (kP / 8) * 128),
+                 i > 0 || kk > 0);
+        umma_commit(B_(kBarODone));
+        umma_commit(B_(kBarBufFree + b));
+        if (i + kShStages < n && !issue(i + kShStages)) ok = false;   // ring stage i % 3 is free
+      }
+      if (!ok) {
+        if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+        *failed = 1;
+      }
+      umma_commit(B_(13));                         // every MMA of this thread completes before TMEM is released
+      mbar_wait(B_(13), 0);
+    }
+    __syncwarp();
+  } else if (w >= kExpWarp0) {
+    // ---- expansion: page i into the K and V^T buffers i % 2 -------------------------------------------
+    const int et = tid - 32 * kExpWarp0;
+    for (int i = 0; i < n; ++i) {
+      if (__any_sync(0xffffffffu, *failed != 0)) break;
+      const int b = i & 1;
+      bool ok = mbar_wait(B_(kBarRing + i % kShStages), (i / kShStages) & 1);
+      if (ok && i >= 2) ok = mbar_wait(B_(kBarBufFree + b), ((i - 2) >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) {
+          flag(lv.status, OSCAR_STATUS_TIMEOUT);
+          *failed = 1;
+        }
+        break;
+      }
+      expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes, et);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the buffers
+      mbar_arrive(B_(kBarExp + b));
+    }
+  } else {
+    // ---- rows: logits, online softmax, weights; thread = row q, TMEM lane 32 w + lane ------------------
+    const uint32_t trow = tmem + ((uint32_t)(32 * w) << 16);
+    uint8_t* pbase = smem + kOffP;
+    float m = -INFINITY, lsum = 0.f, zacc0 = 0.f, zacc1 = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      if (__any_sync(0xffffffffu, *failed != 0)) {
+        ok = false;
+        break;
+      }
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarSDone + b), (i >> 1) & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint8_t* blk = ring + (i % kShStages) * kBlockBytes;
+      float l[kP];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        float s0[32], s1[32];
+        tmem_ld32(trow + kColS + 128 * b + 32 * hf, s0);
+        tmem_ld32(trow + kColS + 128 * b + 64 + 32 * hf, s1);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int t = 32 * hf + c;
+          const uint2 mk = *reinterpret_cast<const uint2*>(blk + kKMetaOff + 8 * t);   // (s0, z0), (s1, z1)
+          const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&mk.x));
+          const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&mk.y));
+          l[t] = fmaf(F, fmaf(k0.x, s0[c] - off0, k1.x * (s1[c] - off1)), fmaf(k0.y, Z0, k1.y * Z1));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(B_(kBarSFree + b));
+      // lazy maximum: rescale only when it grows by more than 2^8
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < kP; ++t) mx = fmaxf(mx, l[t]);
+      float al = 1.f;
+      const bool grow = mx > m + kLazyRescale;
+      if (grow) {
+        al = (m == -INFINITY) ? 0.f : exp2f(m - mx);
+        m = mx;
+      }
+      lsum *= al;
+      zacc0 *= al;
+      zacc1 *= al;
+      if (i > 0) {                                 // O of page i - 1 is complete and the weights buffer free
+        if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (i - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {       // rescale this warp's rows of O (al = 1 for the others)
+#pragma unroll 1
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float o[32];
+            tmem_ld32(trow + kColO + 32 * c4, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= al;
+            tmem_st32(trow + kColO + 32 * c4, o);
           }
         }
       }
-      // ---- online softmax update (shared pages are full: all 64 tokens are live) -------------------
-      float mref[4];
-      bool grow = false;
+      // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float mx = -INFINITY;
+      for (int j = 0; j < kP / 8; ++j) {
+        uint32_t w0[4], w1[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) mx = fmaxf(mx, fmaxf(lg[m][j][0], lg[m][j][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mref[j] = fmaxf(mrun[j], mx);
-        grow |= mref[j] > mrun[j];
-      }
-      if (__any_sync(0xffffffffu, grow)) {
-        float al[4];
+        for (int pr = 0; pr < 4; ++pr) {
+          float a0[2], a1[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          al[j] = mref[j] > mrun[j] ? exp2f(mrun[j] - mref[j]) : 1.f;
-          lsum[j] *= al[j];
-          zacc[j][0] *= al[j];
-          zacc[j][1] *= al[j];
-          mrun[j] = mref[j];
-        }
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            vacc[b][mt][0] *= al[2 * b];
-            vacc[b][mt][2] *= al[2 * b];
-            vacc[b][mt][1] *= al[2 * b + 1];
-            vacc[b][mt][3] *= al[2 * b + 1];
+          for (int e = 0; e < 2; ++e) {
+            const int t = 8 * j + 2 * pr + e;
+            const uint2 mv = *reinterpret_cast<const uint2*>(blk + kVMetaOff + 8 * t);   // (s0, z0), (s1, z1)
+            const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&mv.x));
+            const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&mv.y));
+            const float p = fast_exp2(l[t] - m);
+            lsum += p;
+            zacc0 = fmaf(p, v0.y, zacc0);
+            zacc1 = fmaf(p, v1.y, zacc1);
+            a0[e] = p * v0.x;
+            a1[e] = p * v1.x;
           }
+          w0[pr] = pack_f16x2(a0[0], a0[1]);
+          w1[pr] = pack_f16x2(a1[0], a1[1]);
+        }
+        *reinterpret_cast<uint4*>(pbase + canon_off(q, 8 * j, kP)) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4*>(pbase + kPBytes + canon_off(q, 8 * j, kP)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
       }
-      // ---- P.V over the page's four 16-token tiles --------------------------------------------------
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the weights
+      tc_fence_before();
+      mbar_arrive(B_(kBarPReady));
+    }
+    if (ok && n > 0 && !__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (n - 1) & 1))) ok = false;
+    if (!ok && lane == 0) {
+      if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+      *failed = 1;
+    }
+    tc_fence_after();
+    // ---- partial of this row: (m, l, O + the zero-point sums) ------------------------------------------
+    const bool live = __all_sync(0xffffffffu, ok) && n > 0;
+    float* part = valid ? ws.partials + (((size_t)(Q / gq) * lv.hq + h * gq + Q % gq) * ws.nslots + sa.slot0 + split) *
+                                            kPartFloats
+                        : nullptr;
+    if (part != nullptr) {
+      part[0] = live ? m : -INFINITY;
+      part[1] = live ? lsum : 0.f;
+    }
+#pragma unroll 1
+    for (int c4 = 0; c4 < 4; ++c4) {
+      float o[32];
+      if (live) tmem_ld32(trow + kColO + 32 * c4, o);   // warp-uniform condition
+      const float zs = c4 < 2 ? zacc0 : zacc1;
+      if (part != nullptr) {
 #pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        // V scale and zero of tokens 16 kt + g (x: group 0, y: group 1) and 16 kt + g + 8
-        const uint2 mv0 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + (16 * kt + g) * 8);
-        const uint2 mv1 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + (16 * kt + g + 8) * 8);
-        const float2 v00 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.x));   // (s, z), token g, group 0
-        const float2 v01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));   // group 1
-        const float2 v10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));   // token g + 8
-        const float2 v11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
-        float p[4][2];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          p[j][0] = fast_exp2(lg[kt][j][0] - mrun[j]);
-          p[j][1] = fast_exp2(lg[kt][j][1] - mrun[j]);
-          lsum[j] += p[j][0] + p[j][1];
-          zacc[j][0] = fmaf(p[j][0], v00.y, fmaf(p[j][1], v10.y, zacc[j][0]));
-          zacc[j][1] = fmaf(p[j][0], v01.y, fmaf(p[j][1], v11.y, zacc[j][1]));
-        }
-        uint32_t b0[2][2], b1[2][2];                  // [b][G]
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {                 // row 8b + g, tokens 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1)
-          b0[b][0] = movmatrix_t(pack_f16x2(p[2 * b][0] * v00.x, p[2 * b + 1][0] * v00.x));
-          b1[b][0] = movmatrix_t(pack_f16x2(p[2 * b][1] * v10.x, p[2 * b + 1][1] * v10.x));
-          b0[b][1] = movmatrix_t(pack_f16x2(p[2 * b][0] * v01.x, p[2 * b + 1][0] * v01.x));
-          b1[b][1] = movmatrix_t(pack_f16x2(p[2 * b][1] * v11.x, p[2 * b + 1][1] * v11.x));
-        }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {               // channels 16 mt ..: group mt / 4
-          // row 16 mt + vrow, token pairs 8 kt + 4h ..: chunk (2 kt + h) ^ (2 (mt % 4) + hr) = 2 (kt ^ mt % 4) + (h ^ hr)
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(vt_lane + 16 * mt * kVtStride * 2 + 32 * (kt ^ (mt & 3)), a0, a1, a2, a3);
-#pragma unroll
-          for (int b = 0; b < 2; ++b) mma16816(vacc[b][mt], a0, a1, a2, a3, b0[b][mt >> 2], b1[b][mt >> 2]);
-        }
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(part + 4 + 32 * c4 + e) =
+              live ? make_float4(o[e] + zs, o[e + 1] + zs, o[e + 2] + zs, o[e + 3] + zs) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    timed_out = __syncthreads_or(timed_out);      // page i's buffers and ring stage are free
-    if (!timed_out && tid == 0 && i + kShStages < n) issue(i + kShStages);
   }
-
-  if (timed_out) {
-    // give the copies still in flight a bounded chance to land before the CTA's memory is released
-    if (tid == 0) {                                // only the last use of each stage can be outstanding
-      flag(lv.status, OSCAR_STATUS_TIMEOUT);
-      for (int k = max(0, issued_n - kShStages); k < issued_n; ++k)
-        if (page_ok[k % kShStages]) mbar_wait(bar0 + 8 * (k % kShStages), (k / kShStages) & 1);
-    }
-  }
-  // ---- partials: one slot per query row ----------------------------------------------------------------
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int x = 4; x < 32; x <<= 1) {
-      lsum[j] += __shfl_xor_sync(0xffffffffu, lsum[j], x);
-      zacc[j][0] += __shfl_xor_sync(0xffffffffu, zacc[j][0], x);
-      zacc[j][1] += __shfl_xor_sync(0xffffffffu, zacc[j][1], x);
-    }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int Q = qt * kShQ + qrow(j);
-    if (Q >= nq) continue;
-    float* part = ws.partials + (((size_t)(Q / gq) * lv.hq + h * gq + Q % gq) * ws.nslots + sa.slot0 + split) *
-                                    kPartFloats;
-    const bool live = !timed_out && mrun[j] != -INFINITY;
-    if (g == 0) {
-      part[0] = live ? mrun[j] : -INFINITY;
-      part[1] = live ? lsum[j] : 0.f;
-    }
-    const int b = j >> 1, e0 = j & 1;              // vacc elements e0 (channel 16mt + g), e0 + 2 (+ 8)
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const float zs = zacc[j][mt >> 2];
-      part[4 + 16 * mt + g] = live ? vacc[b][mt][e0] + zs : 0.f;
-      part[4 + 16 * mt + g + 8] = live ? vacc[b][mt][e0 + 2] + zs : 0.f;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (w == kCtlWarp) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 

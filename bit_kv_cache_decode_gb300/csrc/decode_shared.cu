@@ -10,11 +10,10 @@
 // Work: grid (split, kv head, query tile); a CTA takes the shared pages
 // [p0, p1) of its split and 128 query rows (request r, head i flattened as
 // r * gq + i). Per page (64 tokens, both products with M = 128 query rows):
-//  * S = Q K^T: A = the rows' fragments q~ 2^sigma / 256 as fp16 high and low
-//    parts (two MMAs into one accumulator), B = the page's K codes expanded to
-//    fp16 1024 + 256 c (every code moved into mantissa bits 8-9); one TMEM
-//    accumulator (64 columns) per channel group. The constant part is
-//    subtracted in fp32 afterwards (1024 * the fragments' sum per group).
+//  * S = Q K^T: A = the rows' fragments q~ 2^sigma as fp16 high and low parts
+//    (two MMAs into one accumulator), B = the page's K codes expanded to their
+//    exact fp16 values c; one TMEM accumulator (64 columns) per channel group,
+//    holding 2^sigma sum_{ch in group} c q~ (exact products, fp32 sums).
 //  * Each row thread reads its row's 64 logits from TMEM, applies the tokens'
 //    scale and zero, and updates its online softmax. Its maximum is updated
 //    lazily: the output accumulator is rescaled only when the maximum grows by
@@ -24,8 +23,10 @@
 //    zero-point part sum_t p_t z_t is accumulated in fp32 by the row thread.
 // Operands sit in shared memory in the no-swizzle K-major canonical layout
 // (8-row x 16-byte core matrices). Warp roles: warps 0-3 own the 128 rows (TMEM
-// lanes), warp 4 issues the bulk copies and the MMAs (one thread), warps 5-7
-// expand pages. S is double-buffered in TMEM, so S of page i + 1 runs on the
+// lanes; four warps per lane quarter, one for each 16-token slice of a page,
+// which agree on each row's maximum through shared memory), warp 16 issues the
+// bulk copies and the MMAs (one thread), warps 17-19 expand pages and convert
+// their scale / zero metadata to floats. S is double-buffered in TMEM, so S of page i + 1 runs on the
 // tensor cores while the rows finish page i. Every wait is bounded; a CTA
 // whose wait expires flags OSCAR_STATUS_TIMEOUT and writes empty partials.
 // Each CTA writes one partial (m, l, acc[128]) per query row into the history
@@ -38,10 +39,12 @@
 namespace oscar {
 namespace {
 
-constexpr int kRowWarps = 4, kCtlWarp = 4, kExpWarp0 = 5, kExpWarps = 3;
-constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 256
+// row warps w = 0 .. 15: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), 16-token slice w / 4 of every page
+constexpr int kRowWarps = 16, kSlices = 4, kSliceTok = kP / kSlices, kCtlWarp = 16, kExpWarp0 = 17, kExpWarps = 3;
+constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 640
 constexpr int kExpThreads = 32 * kExpWarps;
-constexpr int kShQ = 32 * kRowWarps;                                  // query rows per CTA
+constexpr int kRowThreads = 32 * kRowWarps;
+constexpr int kShQ = 128;                                             // query rows per CTA (TMEM lanes)
 static_assert(kShQ == kSharedRows, "the host's query tiles");
 constexpr int kShStages = 3;
 constexpr uint32_t kMagic = 0x64006400u;              // fp16 1024.0 in both halves
@@ -58,14 +61,17 @@ constexpr int kOffQ = 15360;                          // kShStages * kBlockBytes
 constexpr int kOffKh = kOffQ + 2 * kQBytes;           // 2 buffers
 constexpr int kOffVt = kOffKh + 2 * kKhBytes;         // 2 buffers
 constexpr int kOffP = kOffVt + 2 * kVtBytes;          // 2 groups
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kNumBars = 14;
+constexpr int kOffMeta = kOffP + 2 * kPBytes;        // [2 buffers][K, V][64 tokens] (s0, z0, s1, z1) as float4
+constexpr int kRowc = 16;                             // per row: F, Z0, Z1, then (l, z0, z1) sums of slices 1-3
+constexpr int kOffRowc = kOffMeta + 2 * 2 * kP * 16;  // [128 rows][kRowc]
+constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128 rows] partial maxima
+constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
+constexpr int kNumBars = 15;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
 static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
-static_assert(kShQ * kD * 4 <= 2 * kKhBytes + 2 * kVtBytes + 2 * kPBytes, "q~ staging fits");
 // mbarrier indices
 constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 5, kBarSFree = 7, kBarPReady = 9, kBarODone = 10,
-              kBarBufFree = 11;
+              kBarBufFree = 11, kBarFinal = 13, kBarMx = 14;
 // TMEM columns: S buffers at 0 and 128 (group G at + 64 G), O at 256 (group G at + 64 G)
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
@@ -112,6 +118,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 16 columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -162,6 +180,10 @@ __device__ __forceinline__ uint32_t code_at(uint32_t x, int i) {
   const uint32_t y = i < 4 ? (x << (8 - 2 * i)) : (x >> (2 * i - 8));
   return and_or(y, kCodeMask, kMagic);
 }
+// The same code as its exact fp16 value c: (1024 + 256 c) / 256 - 4.
+__device__ __forceinline__ uint32_t exact_at(uint32_t x, int i) {
+  return hfma2_u(code_at(x, i), 0x1C001C00u, 0xC400C400u);
+}
 // Byte offset of element (row, k) of a K-major operand in the canonical no-swizzle layout, rows of
 // kcols elements: core matrix (row / 8, k / 8) at (row / 8) * (kcols / 8) * 128 + (k / 8) * 128.
 __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
@@ -171,16 +193,23 @@ __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
 
 // Expand one packed page block into K (rows = tokens, K-major over the 128 channel positions) and V^T
 // (rows = channels, K-major over the 64 tokens); et = 0 .. kExpThreads - 1 is the expanding thread.
-// K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel 16u + 8 + q (the
-// query fragments use the same order).
-__device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, int et) {
+// Both hold exact codes. K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel
+// 16u + 8 + q (the query fragments use the same order).
+__device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, uint8_t* meta, int et) {
   for (int wi = et; wi < kP * (kD / 16); wi += kExpThreads) {   // K: token t, channels 16u .. 16u + 15
     const int t = (wi & 7) + 8 * (wi >> 6), u = (wi >> 3) & 7;   // a quarter warp: 8 consecutive tokens
     const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + t * 32 + 4 * u);
     *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u, kD)) =
-        make_uint4(code_at(x, 0), code_at(x, 1), code_at(x, 2), code_at(x, 3));
+        make_uint4(exact_at(x, 0), exact_at(x, 1), exact_at(x, 2), exact_at(x, 3));
     *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u + 8, kD)) =
-        make_uint4(code_at(x, 4), code_at(x, 5), code_at(x, 6), code_at(x, 7));
+        make_uint4(exact_at(x, 4), exact_at(x, 5), exact_at(x, 6), exact_at(x, 7));
+  }
+  for (int mi = et; mi < 2 * kP; mi += kExpThreads) {  // metadata rows as floats: (s0, z0, s1, z1)
+    const int kind = mi / kP, t = mi % kP;
+    const uint2 mw = *reinterpret_cast<const uint2*>(blk + (kind ? kVMetaOff : kKMetaOff) + 8 * t);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
+    reinterpret_cast<float4*>(meta)[mi] = make_float4(a.x, a.y, b.x, b.y);
   }
   for (int vi = et; vi < (kD / 8) * (kP / 8); vi += kExpThreads) {   // V: octet o (channels 8o ..), tokens 8 kb ..
     const int o = vi >> 3, kb = vi & 7;
@@ -193,7 +222,7 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
       const int i = (ii + kb) & 7;                 // staggered: the quarter warp's stores hit distinct banks
       uint32_t c[4];
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) c[pp] = hfma2_u(code_at(x[pp], i), 0x1C001C00u, 0xC400C400u);   // exact c
+      for (int pp = 0; pp < 4; ++pp) c[pp] = exact_at(x[pp], i);
       *reinterpret_cast<uint4*>(vt + canon_off(8 * o + i, 8 * kb, kP)) = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
@@ -244,13 +273,14 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarExp + 1), kExpThreads);
       mbar_init_n(B_(kBarSDone + 0), 1);
       mbar_init_n(B_(kBarSDone + 1), 1);
-      mbar_init_n(B_(kBarSFree + 0), 32 * kRowWarps);
-      mbar_init_n(B_(kBarSFree + 1), 32 * kRowWarps);
-      mbar_init_n(B_(kBarPReady), 32 * kRowWarps);
+      mbar_init_n(B_(kBarSFree + 0), kRowThreads);
+      mbar_init_n(B_(kBarSFree + 1), kRowThreads);
+      mbar_init_n(B_(kBarPReady), kRowThreads);
+      mbar_init_n(B_(kBarMx), kRowThreads);
       mbar_init_n(B_(kBarODone), 1);
       mbar_init_n(B_(kBarBufFree + 0), 1);
       mbar_init_n(B_(kBarBufFree + 1), 1);
-      mbar_init_n(B_(13), 1);
+      mbar_init_n(B_(kBarFinal), 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       *failed = 0;
       bool ok = true;
@@ -270,13 +300,12 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- the rows' fragments (row warps: thread = row): q~ 2^sigma / 256 as fp16 high and low parts ----
-  const int q = tid;                               // row of this thread (row warps)
-  const int Q = qt * kShQ + q;
-  const bool valid = w < kRowWarps && Q < nq;
-  float F = 0.f, Z0 = 0.f, Z1 = 0.f, off0 = 0.f, off1 = 0.f;
-  if (w < kRowWarps) {
-    float sig = 0.f;
+  // ---- the rows' fragments (warps 0-3: thread = row): q~ 2^sigma as fp16 high and low parts ----------
+  float* rowc = reinterpret_cast<float*>(smem + kOffRowc);
+  if (w < 4) {
+    const int q = tid, Q = qt * kShQ + q;
+    const bool valid = Q < nq;
+    float F = 0.f, Z0 = 0.f, Z1 = 0.f, sig = 0.f;
     const float* qrow = nullptr;
     if (valid) {
       const size_t row = (size_t)(Q / gq) * lv.hq + h * gq + Q % gq;
@@ -287,10 +316,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       sig = qc[kQSigma];
       qrow = ws.qrot + row * kD;
     }
-    const float sc = exp2f(sig - 8.f);
+    const float sc = exp2f(sig);                   // max |q~| 2^sigma is near 2^12: fp16-safe
     uint8_t* qh = smem + kOffQ;
     uint8_t* qlo = smem + kOffQ + kQBytes;
-    float oh0 = 0.f, oh1 = 0.f, ol0 = 0.f, ol1 = 0.f;   // sums of the high and low parts per group
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {               // channels 32 cc .. 32 cc + 31: 16-channel blocks 2cc, 2cc + 1
       float x[32];
@@ -304,7 +332,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       }
 #pragma unroll
       for (int ub = 0; ub < 2; ++ub) {
-        const int u = 2 * cc + ub, G = u >> 2;
+        const int u = 2 * cc + ub;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {     // k-block 2u + half: channel pairs (16u + j, 16u + 8 + j)
           uint32_t hw[4], lw[4];
@@ -314,13 +342,6 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
             const float xa = x[16 * ub + j], xb = x[16 * ub + 8 + j];
             const float ha = frag_round16(xa), hb = frag_round16(xb);
             const float la = frag_round16(xa - ha), lb = frag_round16(xb - hb);
-            if (G == 0) {
-              oh0 += ha + hb;
-              ol0 += la + lb;
-            } else {
-              oh1 += ha + hb;
-              ol1 += la + lb;
-            }
             hw[pr] = pack_f16x2(ha, hb);
             lw[pr] = pack_f16x2(la, lb);
           }
@@ -329,12 +350,15 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         }
       }
     }
-    off0 = 1024.f * oh0 + 1024.f * ol0;            // the constant part 1024 * sum(high + low) per group
-    off1 = 1024.f * oh1 + 1024.f * ol1;
+    rowc[q * kRowc + 0] = F;
+    rowc[q * kRowc + 1] = Z0;
+    rowc[q * kRowc + 2] = Z1;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the fragments
   }
   __syncthreads();
 
+  // running softmax state of a row warp's rows over its half of the tokens (warps 0-3 write the partials)
+  float m = -INFINITY, lsum = 0.f, zacc0 = 0.f, zacc1 = 0.f;
   if (w == kCtlWarp) {
     // ---- control: the MMAs of every page and the ring's bulk copies (one thread) ----------------------
     if (lane == 0) {
@@ -394,8 +418,8 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
         *failed = 1;
       }
-      umma_commit(B_(13));                         // every MMA of this thread completes before TMEM is released
-      mbar_wait(B_(13), 0);
+      umma_commit(B_(kBarFinal));                  // every MMA of this thread completes before TMEM is released
+      mbar_wait(B_(kBarFinal), 0);
     }
     __syncwarp();
   } else if (w >= kExpWarp0) {
@@ -413,15 +437,18 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         }
         break;
       }
-      expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes, et);
+      expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes,
+                  smem + kOffMeta + b * 2 * kP * 16, et);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the buffers
       mbar_arrive(B_(kBarExp + b));
     }
   } else {
-    // ---- rows: logits, online softmax, weights; thread = row q, TMEM lane 32 w + lane ------------------
-    const uint32_t trow = tmem + ((uint32_t)(32 * w) << 16);
+    // ---- rows: logits, online softmax, weights. Thread = row q (TMEM lane), tokens 16 sl .. 16 sl + 15 ----
+    const int quarter = w & 3, sl = w >> 2, q = 32 * quarter + lane;
+    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
     uint8_t* pbase = smem + kOffP;
-    float m = -INFINITY, lsum = 0.f, zacc0 = 0.f, zacc1 = 0.f;
+    float* mxs = reinterpret_cast<float*>(smem + kOffMx);   // [page % 2][slice][row]
+    const float F = rowc[q * kRowc + 0], Z0 = rowc[q * kRowc + 1], Z1 = rowc[q * kRowc + 2];
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       if (__any_sync(0xffffffffu, *failed != 0)) {
@@ -429,33 +456,41 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         break;
       }
       const int b = i & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarSDone + b), (i >> 1) & 1))) {
+      // S of page i, and its metadata (written by the expansion of page i)
+      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarSDone + b), (i >> 1) & 1) &&
+                                       mbar_wait(B_(kBarExp + b), (i >> 1) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint8_t* blk = ring + (i % kShStages) * kBlockBytes;
-      float l[kP];
+      const float4* km = reinterpret_cast<const float4*>(smem + kOffMeta + b * 2 * kP * 16) + kSliceTok * sl;
+      const float4* vm = km + kP;
+      float l[kSliceTok];
+      {
+        float s0[kSliceTok], s1[kSliceTok];
+        tmem_ld16(trow + kColS + 128 * b + kSliceTok * sl, s0);
+        tmem_ld16(trow + kColS + 128 * b + 64 + kSliceTok * sl, s1);
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        float s0[32], s1[32];
-        tmem_ld32(trow + kColS + 128 * b + 32 * hf, s0);
-        tmem_ld32(trow + kColS + 128 * b + 64 + 32 * hf, s1);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int t = 32 * hf + c;
-          const uint2 mk = *reinterpret_cast<const uint2*>(blk + kKMetaOff + 8 * t);   // (s0, z0), (s1, z1)
-          const float2 k0 = __half22float2(*reinterpret_cast<const __half2*>(&mk.x));
-          const float2 k1 = __half22float2(*reinterpret_cast<const __half2*>(&mk.y));
-          l[t] = fmaf(F, fmaf(k0.x, s0[c] - off0, k1.x * (s1[c] - off1)), fmaf(k0.y, Z0, k1.y * Z1));
+        for (int c = 0; c < kSliceTok; ++c) {
+          const float4 k = km[c];                 // (s0, z0, s1, z1) of the token
+          l[c] = fmaf(F, fmaf(k.x, s0[c], k.z * s1[c]), fmaf(k.y, Z0, k.w * Z1));
         }
       }
       tc_fence_before();
       mbar_arrive(B_(kBarSFree + b));
-      // lazy maximum: rescale only when it grows by more than 2^8
+      // the row's maximum over the page's four slices
       float mx = -INFINITY;
 #pragma unroll
-      for (int t = 0; t < kP; ++t) mx = fmaxf(mx, l[t]);
+      for (int c = 0; c < kSliceTok; ++c) mx = fmaxf(mx, l[c]);
+      mxs[(b * kSlices + sl) * kShQ + q] = mx;
+      mbar_arrive(B_(kBarMx));
+      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarMx), i & 1))) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int o = 0; o < kSlices; ++o) mx = fmaxf(mx, mxs[(b * kSlices + o) * kShQ + q]);
+      // lazy maximum (the same in every slice): rescale only when it grows by more than 2^8
       float al = 1.f;
       const bool grow = mx > m + kLazyRescale;
       if (grow) {
@@ -471,7 +506,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {       // rescale this warp's rows of O (al = 1 for the others)
+        if (sl == 0 && __any_sync(0xffffffffu, grow)) {   // rescale these rows of O (al = 1 for the others)
 #pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
             float o[32];
@@ -484,54 +519,71 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       }
       // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout
 #pragma unroll
-      for (int j = 0; j < kP / 8; ++j) {
+      for (int j = 0; j < kSliceTok / 8; ++j) {   // tokens 16 sl + 8j .. + 7
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {
           float a0[2], a1[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int t = 8 * j + 2 * pr + e;
-            const uint2 mv = *reinterpret_cast<const uint2*>(blk + kVMetaOff + 8 * t);   // (s0, z0), (s1, z1)
-            const float2 v0 = __half22float2(*reinterpret_cast<const __half2*>(&mv.x));
-            const float2 v1 = __half22float2(*reinterpret_cast<const __half2*>(&mv.y));
-            const float p = fast_exp2(l[t] - m);
+            const int c = 8 * j + 2 * pr + e;
+            const float4 v = vm[c];               // (s0, z0, s1, z1) of the token's V
+            const float p = fast_exp2(l[c] - m);
             lsum += p;
-            zacc0 = fmaf(p, v0.y, zacc0);
-            zacc1 = fmaf(p, v1.y, zacc1);
-            a0[e] = p * v0.x;
-            a1[e] = p * v1.x;
+            zacc0 = fmaf(p, v.y, zacc0);
+            zacc1 = fmaf(p, v.w, zacc1);
+            a0[e] = p * v.x;
+            a1[e] = p * v.z;
           }
           w0[pr] = pack_f16x2(a0[0], a0[1]);
           w1[pr] = pack_f16x2(a1[0], a1[1]);
         }
-        *reinterpret_cast<uint4*>(pbase + canon_off(q, 8 * j, kP)) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        *reinterpret_cast<uint4*>(pbase + kPBytes + canon_off(q, 8 * j, kP)) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        const int off = canon_off(q, kSliceTok * sl + 8 * j, kP);
+        *reinterpret_cast<uint4*>(pbase + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        *reinterpret_cast<uint4*>(pbase + kPBytes + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the weights
       tc_fence_before();
       mbar_arrive(B_(kBarPReady));
     }
-    if (ok && n > 0 && !__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (n - 1) & 1))) ok = false;
+    if (ok && n > 0 && sl == 0 && !__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (n - 1) & 1))) ok = false;
     if (!ok && lane == 0) {
       if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
       *failed = 1;
     }
+    if (sl > 0) {                                  // this slice's sums, for the slice-0 warp of these rows
+      rowc[q * kRowc + 3 * sl + 0] = lsum;
+      rowc[q * kRowc + 3 * sl + 1] = zacc0;
+      rowc[q * kRowc + 3 * sl + 2] = zacc1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // ---- partials (warps 0-3: thread = row): (m, l, O + the zero-point sums) --------------------------------
+  if (w < 4) {
     tc_fence_after();
-    // ---- partial of this row: (m, l, O + the zero-point sums) ------------------------------------------
-    const bool live = __all_sync(0xffffffffu, ok) && n > 0;
-    float* part = valid ? ws.partials + (((size_t)(Q / gq) * lv.hq + h * gq + Q % gq) * ws.nslots + sa.slot0 + split) *
-                                            kPartFloats
-                        : nullptr;
+    const int q = tid, Q = qt * kShQ + q;
+    const uint32_t trow = tmem + ((uint32_t)(32 * w) << 16);
+    const bool live = *failed == 0 && n > 0;       // block-uniform after the barrier
+    float L = lsum, zz0 = zacc0, zz1 = zacc1;
+#pragma unroll
+    for (int o = 1; o < kSlices; ++o) {
+      L += rowc[q * kRowc + 3 * o];
+      zz0 += rowc[q * kRowc + 3 * o + 1];
+      zz1 += rowc[q * kRowc + 3 * o + 2];
+    }
+    float* part = Q < nq ? ws.partials + (((size_t)(Q / gq) * lv.hq + h * gq + Q % gq) * ws.nslots + sa.slot0 + split) *
+                                             kPartFloats
+                         : nullptr;
     if (part != nullptr) {
       part[0] = live ? m : -INFINITY;
-      part[1] = live ? lsum : 0.f;
+      part[1] = live ? L : 0.f;
     }
 #pragma unroll 1
     for (int c4 = 0; c4 < 4; ++c4) {
       float o[32];
-      if (live) tmem_ld32(trow + kColO + 32 * c4, o);   // warp-uniform condition
-      const float zs = c4 < 2 ? zacc0 : zacc1;
+      if (live) tmem_ld32(trow + kColO + 32 * c4, o);
+      const float zs = c4 < 2 ? zz0 : zz1;
       if (part != nullptr) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4)

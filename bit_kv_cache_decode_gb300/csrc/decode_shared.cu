@@ -22,10 +22,11 @@
 //    (fp16), B = the V codes (exact small integers, rows = channels); the
 //    zero-point part sum_t p_t z_t is accumulated in fp32 by the row thread.
 // Operands sit in shared memory in the no-swizzle K-major canonical layout
-// (8-row x 16-byte core matrices). Warp roles: warps 0-3 own the 128 rows (TMEM
-// lanes; four warps per lane quarter, one for each 16-token slice of a page,
-// which agree on each row's maximum through shared memory), warp 16 issues the
-// bulk copies and the MMAs (one thread), warps 17-19 expand pages and convert
+// (8-row x 16-byte core matrices); expanded pages are triple-buffered. Warp
+// roles: warps 0-3 own the 128 rows (TMEM
+// lanes; two warps per lane quarter, one for each half of a page's tokens,
+// which agree on each row's maximum through shared memory), warp 8 issues the
+// bulk copies and the MMAs (one thread), warps 9-15 expand pages and convert
 // their scale / zero metadata to floats. S is double-buffered in TMEM, so S of page i + 1 runs on the
 // tensor cores while the rows finish page i. Every wait is bounded; a CTA
 // whose wait expires flags OSCAR_STATUS_TIMEOUT and writes empty partials.
@@ -39,9 +40,9 @@
 namespace oscar {
 namespace {
 
-// row warps w = 0 .. 15: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), 16-token slice w / 4 of every page
-constexpr int kRowWarps = 16, kSlices = 4, kSliceTok = kP / kSlices, kCtlWarp = 16, kExpWarp0 = 17, kExpWarps = 3;
-constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 640
+// row warps w = 0 .. 7: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), 32-token slice w / 4 of every page
+constexpr int kRowWarps = 8, kSlices = 2, kSliceTok = kP / kSlices, kCtlWarp = 8, kExpWarp0 = 9, kExpWarps = 7;
+constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 512
 constexpr int kExpThreads = 32 * kExpWarps;
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kShQ = 128;                                             // query rows per CTA (TMEM lanes)
@@ -58,20 +59,22 @@ constexpr int kVtBytes = kD * kP * 2;                 // expanded V^T of a page:
 constexpr int kPBytes = kShQ * kP * 2;                // weights of one channel group: 16 KB
 constexpr int kOffRing = 0;
 constexpr int kOffQ = 15360;                          // kShStages * kBlockBytes, 1024-aligned
-constexpr int kOffKh = kOffQ + 2 * kQBytes;           // 2 buffers
-constexpr int kOffVt = kOffKh + 2 * kKhBytes;         // 2 buffers
-constexpr int kOffP = kOffVt + 2 * kVtBytes;          // 2 groups
-constexpr int kOffMeta = kOffP + 2 * kPBytes;        // [2 buffers][K, V][64 tokens] (s0, z0, s1, z1) as float4
+constexpr int kBufs = 3;                              // expanded pages in flight
+constexpr int kOffKh = kOffQ + 2 * kQBytes;           // kBufs buffers
+constexpr int kOffVt = kOffKh + kBufs * kKhBytes;     // kBufs buffers
+constexpr int kOffP = kOffVt + kBufs * kVtBytes;      // 2 groups
+constexpr int kMetaBytes = 2 * kP * 16;               // [K, V][64 tokens] (s0, z0, s1, z1) as float4
+constexpr int kOffMeta = kOffP + 2 * kPBytes;         // kBufs buffers
 constexpr int kRowc = 16;                             // per row: F, Z0, Z1, then (l, z0, z1) sums of slices 1-3
-constexpr int kOffRowc = kOffMeta + 2 * 2 * kP * 16;  // [128 rows][kRowc]
+constexpr int kOffRowc = kOffMeta + kBufs * kMetaBytes;   // [128 rows][kRowc]
 constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128 rows] partial maxima
 constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
-constexpr int kNumBars = 15;
+constexpr int kNumBars = 17;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
 static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
 // mbarrier indices
-constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 5, kBarSFree = 7, kBarPReady = 9, kBarODone = 10,
-              kBarBufFree = 11, kBarFinal = 13, kBarMx = 14;
+constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 6, kBarSFree = 8, kBarPReady = 10, kBarODone = 11,
+              kBarBufFree = 12, kBarFinal = 15, kBarMx = 16;
 // TMEM columns: S buffers at 0 and 128 (group G at + 64 G), O at 256 (group G at + 64 G)
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
@@ -212,14 +215,14 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     reinterpret_cast<float4*>(meta)[mi] = make_float4(a.x, a.y, b.x, b.y);
   }
   for (int vi = et; vi < (kD / 8) * (kP / 8); vi += kExpThreads) {   // V: octet o (channels 8o ..), tokens 8 kb ..
-    const int o = vi >> 3, kb = vi & 7;
+    const int o = vi & 15, kb = vi >> 4;          // a quarter warp: 8 consecutive octets (consecutive code words)
     uint32_t x[4];
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp)
       x[pp] = *reinterpret_cast<const uint32_t*>(blk + kVCodesOff + (4 * kb + pp) * 64 + 4 * o);
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
-      const int i = (ii + kb) & 7;                 // staggered: the quarter warp's stores hit distinct banks
+      const int i = (ii + o) & 7;                  // staggered: the quarter warp's stores hit distinct banks
       uint32_t c[4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) c[pp] = exact_at(x[pp], i);
@@ -271,6 +274,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarRing + 2), 1);
       mbar_init_n(B_(kBarExp + 0), kExpThreads);
       mbar_init_n(B_(kBarExp + 1), kExpThreads);
+      mbar_init_n(B_(kBarExp + 2), kExpThreads);
       mbar_init_n(B_(kBarSDone + 0), 1);
       mbar_init_n(B_(kBarSDone + 1), 1);
       mbar_init_n(B_(kBarSFree + 0), kRowThreads);
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarODone), 1);
       mbar_init_n(B_(kBarBufFree + 0), 1);
       mbar_init_n(B_(kBarBufFree + 1), 1);
+      mbar_init_n(B_(kBarBufFree + 2), 1);
       mbar_init_n(B_(kBarFinal), 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       *failed = 0;
@@ -365,13 +370,13 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       const uint32_t qh_a = smem_addr(smem + kOffQ), ql_a = qh_a + kQBytes, p_a = smem_addr(smem + kOffP);
       const uint32_t kh_a = smem_addr(smem + kOffKh), vt_a = smem_addr(smem + kOffVt);
       auto issue_s = [&](int i) {                  // S_G = Q_G K_G^T into TMEM columns 128 (i % 2) + 64 G
-        const int b = i & 1;
+        const int b = i & 1, kb3 = i % kBufs;
 #pragma unroll
         for (int G = 0; G < 2; ++G)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t koff = (8 * G + 2 * kk) * 128;                 // k-blocks 8G + 2kk and + 1
-            const uint64_t bd = umma_desc(kh_a + b * kKhBytes + koff, 128, (kD / 8) * 128);
+            const uint64_t bd = umma_desc(kh_a + kb3 * kKhBytes + koff, 128, (kD / 8) * 128);
             const uint32_t d = tmem + kColS + 128 * b + 64 * G;
             umma(d, umma_desc(qh_a + koff, 128, (kD / 8) * 128), bd, kk > 0);
             umma(d, umma_desc(ql_a + koff, 128, (kD / 8) * 128), bd, true);
@@ -391,10 +396,15 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           ok = false;
           break;
         }
-        const int b = i & 1;
+        const int kb3 = i % kBufs;
+        // page i is expanded (its wait preceded S of page i): its ring stage takes page i + 3
+        if (i + kShStages < n && !issue(i + kShStages)) {
+          ok = false;
+          break;
+        }
         if (i + 1 < n) {                           // S of page i + 1 runs while the rows finish page i
           const int b1 = (i + 1) & 1;
-          ok = mbar_wait(B_(kBarExp + b1), ((i + 1) >> 1) & 1);
+          ok = mbar_wait(B_(kBarExp + (i + 1) % kBufs), ((i + 1) / kBufs) & 1);
           if (ok && i + 1 >= 2) ok = mbar_wait(B_(kBarSFree + b1), ((i - 1) >> 1) & 1);
           if (!ok) break;
           tc_fence_after();
@@ -408,11 +418,10 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma(tmem + kColO + 64 * G, umma_desc(p_a + G * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
-                 umma_desc(vt_a + b * kVtBytes + G * 8 * (kP / 8) * 128 + 2 * kk * 128, 128, (kP / 8) * 128),
+                 umma_desc(vt_a + kb3 * kVtBytes + G * 8 * (kP / 8) * 128 + 2 * kk * 128, 128, (kP / 8) * 128),
                  i > 0 || kk > 0);
         umma_commit(B_(kBarODone));
-        umma_commit(B_(kBarBufFree + b));
-        if (i + kShStages < n && !issue(i + kShStages)) ok = false;   // ring stage i % 3 is free
+        umma_commit(B_(kBarBufFree + kb3));
       }
       if (!ok) {
         if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
@@ -423,13 +432,13 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
     }
     __syncwarp();
   } else if (w >= kExpWarp0) {
-    // ---- expansion: page i into the K and V^T buffers i % 2 -------------------------------------------
+    // ---- expansion: page i into the K, V^T and metadata buffers i % 3 ---------------------------------
     const int et = tid - 32 * kExpWarp0;
     for (int i = 0; i < n; ++i) {
       if (__any_sync(0xffffffffu, *failed != 0)) break;
-      const int b = i & 1;
+      const int b = i % kBufs;
       bool ok = mbar_wait(B_(kBarRing + i % kShStages), (i / kShStages) & 1);
-      if (ok && i >= 2) ok = mbar_wait(B_(kBarBufFree + b), ((i - 2) >> 1) & 1);
+      if (ok && i >= kBufs) ok = mbar_wait(B_(kBarBufFree + b), ((i - kBufs) / kBufs) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) {
           flag(lv.status, OSCAR_STATUS_TIMEOUT);
@@ -438,12 +447,12 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         break;
       }
       expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes,
-                  smem + kOffMeta + b * 2 * kP * 16, et);
+                  smem + kOffMeta + b * kMetaBytes, et);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the buffers
       mbar_arrive(B_(kBarExp + b));
     }
   } else {
-    // ---- rows: logits, online softmax, weights. Thread = row q (TMEM lane), tokens 16 sl .. 16 sl + 15 ----
+    // ---- rows: logits, online softmax, weights. Thread = row q (TMEM lane), tokens kSliceTok sl .. --------
     const int quarter = w & 3, sl = w >> 2, q = 32 * quarter + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
     uint8_t* pbase = smem + kOffP;
@@ -458,27 +467,28 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       const int b = i & 1;
       // S of page i, and its metadata (written by the expansion of page i)
       if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarSDone + b), (i >> 1) & 1) &&
-                                       mbar_wait(B_(kBarExp + b), (i >> 1) & 1))) {
+                                       mbar_wait(B_(kBarExp + i % kBufs), (i / kBufs) & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float4* km = reinterpret_cast<const float4*>(smem + kOffMeta + b * 2 * kP * 16) + kSliceTok * sl;
+      const float4* km = reinterpret_cast<const float4*>(smem + kOffMeta + (i % kBufs) * kMetaBytes) + kSliceTok * sl;
       const float4* vm = km + kP;
       float l[kSliceTok];
-      {
-        float s0[kSliceTok], s1[kSliceTok];
-        tmem_ld16(trow + kColS + 128 * b + kSliceTok * sl, s0);
-        tmem_ld16(trow + kColS + 128 * b + 64 + kSliceTok * sl, s1);
 #pragma unroll
-        for (int c = 0; c < kSliceTok; ++c) {
-          const float4 k = km[c];                 // (s0, z0, s1, z1) of the token
-          l[c] = fmaf(F, fmaf(k.x, s0[c], k.z * s1[c]), fmaf(k.y, Z0, k.w * Z1));
+      for (int c16 = 0; c16 < kSliceTok / 16; ++c16) {
+        float s0[16], s1[16];
+        tmem_ld16(trow + kColS + 128 * b + kSliceTok * sl + 16 * c16, s0);
+        tmem_ld16(trow + kColS + 128 * b + 64 + kSliceTok * sl + 16 * c16, s1);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 k = km[16 * c16 + c];      // (s0, z0, s1, z1) of the token
+          l[16 * c16 + c] = fmaf(F, fmaf(k.x, s0[c], k.z * s1[c]), fmaf(k.y, Z0, k.w * Z1));
         }
       }
       tc_fence_before();
       mbar_arrive(B_(kBarSFree + b));
-      // the row's maximum over the page's four slices
+      // the row's maximum over the page's slices
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kSliceTok; ++c) mx = fmaxf(mx, l[c]);
@@ -519,7 +529,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       }
       // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout
 #pragma unroll
-      for (int j = 0; j < kSliceTok / 8; ++j) {   // tokens 16 sl + 8j .. + 7
+      for (int j = 0; j < kSliceTok / 8; ++j) {   // tokens kSliceTok sl + 8j .. + 7
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {

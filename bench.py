@@ -409,8 +409,8 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "d753f178da0e315393bf90585905c993920c98fb63a90948f435f15da76cbdc7",
-                      "bytes_per_launch": 66771456 + 374528}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "69c0b4e14a7971e7a3e64440f4787809fe7f3a1a04d0f0be9a9b90cb00a5262d",
+                      "bytes_per_launch": 66764288 + 289280}
 
 
 def sources_digest() -> str:

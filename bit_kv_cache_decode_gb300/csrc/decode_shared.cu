@@ -63,7 +63,7 @@ constexpr int kBufs = 3;                              // expanded pages in fligh
 constexpr int kOffKh = kOffQ + 2 * kQBytes;           // kBufs buffers
 constexpr int kOffVt = kOffKh + kBufs * kKhBytes;     // kBufs buffers
 constexpr int kOffP = kOffVt + kBufs * kVtBytes;      // 2 groups
-constexpr int kMetaBytes = 2 * kP * 16;               // [K, V][64 tokens] (s0, z0, s1, z1) as float4
+constexpr int kMetaBytes = 2 * kP * 16;               // [K, V][s0, z0, s1, z1][64 tokens] as floats
 constexpr int kOffMeta = kOffP + 2 * kPBytes;         // kBufs buffers
 constexpr int kRowc = 16;                             // per row: F, Z0, Z1, then (l, z0, z1) sums of slices 1-3
 constexpr int kOffRowc = kOffMeta + kBufs * kMetaBytes;   // [128 rows][kRowc]
@@ -207,12 +207,16 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u + 8, kD)) =
         make_uint4(exact_at(x, 4), exact_at(x, 5), exact_at(x, 6), exact_at(x, 7));
   }
-  for (int mi = et; mi < 2 * kP; mi += kExpThreads) {  // metadata rows as floats: (s0, z0, s1, z1)
+  for (int mi = et; mi < 2 * kP; mi += kExpThreads) {  // metadata as float arrays: s0, z0, s1, z1 per token
     const int kind = mi / kP, t = mi % kP;
     const uint2 mw = *reinterpret_cast<const uint2*>(blk + (kind ? kVMetaOff : kKMetaOff) + 8 * t);
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
     const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
-    reinterpret_cast<float4*>(meta)[mi] = make_float4(a.x, a.y, b.x, b.y);
+    float* mk = reinterpret_cast<float*>(meta) + kind * 4 * kP + t;
+    mk[0] = a.x;
+    mk[kP] = a.y;
+    mk[2 * kP] = b.x;
+    mk[3 * kP] = b.y;
   }
   for (int vi = et; vi < (kD / 8) * (kP / 8); vi += kExpThreads) {   // V: octet o (channels 8o ..), tokens 8 kb ..
     const int o = vi & 15, kb = vi >> 4;          // a quarter warp: 8 consecutive octets (consecutive code words)
@@ -458,6 +462,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
     uint8_t* pbase = smem + kOffP;
     float* mxs = reinterpret_cast<float*>(smem + kOffMx);   // [page % 2][slice][row]
     const float F = rowc[q * kRowc + 0], Z0 = rowc[q * kRowc + 1], Z1 = rowc[q * kRowc + 2];
+    const float2 Fv = make_float2(F, F), Z0v = make_float2(Z0, Z0), Z1v = make_float2(Z1, Z1);
+    // sums over this slice's tokens, even tokens in x and odd ones in y
+    float2 lsum2 = make_float2(0.f, 0.f), zacc02 = make_float2(0.f, 0.f), zacc12 = make_float2(0.f, 0.f);
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       if (__any_sync(0xffffffffu, *failed != 0)) {
@@ -472,8 +479,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         break;
       }
       tc_fence_after();
-      const float4* km = reinterpret_cast<const float4*>(smem + kOffMeta + (i % kBufs) * kMetaBytes) + kSliceTok * sl;
-      const float4* vm = km + kP;
+      // the page's metadata: [K, V][s0, z0, s1, z1][64 tokens]; this slice starts at token kSliceTok sl
+      const float* md = reinterpret_cast<const float*>(smem + kOffMeta + (i % kBufs) * kMetaBytes) + kSliceTok * sl;
+      auto pair = [&](int arr, int c) { return *reinterpret_cast<const float2*>(md + arr * kP + c); };
       float l[kSliceTok];
 #pragma unroll
       for (int c16 = 0; c16 < kSliceTok / 16; ++c16) {
@@ -481,9 +489,15 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         tmem_ld16(trow + kColS + 128 * b + kSliceTok * sl + 16 * c16, s0);
         tmem_ld16(trow + kColS + 128 * b + 64 + kSliceTok * sl + 16 * c16, s1);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 k = km[16 * c16 + c];      // (s0, z0, s1, z1) of the token
-          l[16 * c16 + c] = fmaf(F, fmaf(k.x, s0[c], k.z * s1[c]), fmaf(k.y, Z0, k.w * Z1));
+        for (int c = 0; c < 16; c += 2) {        // two tokens per packed fp32 op: F (s0 S0 + s1 S1) + z0 Z0 + z1 Z1
+          const int t = 16 * c16 + c;
+          float2 a = __fmul2_rn(pair(2, t), make_float2(s1[c], s1[c + 1]));
+          a = __ffma2_rn(pair(0, t), make_float2(s0[c], s0[c + 1]), a);
+          float2 zt = __fmul2_rn(pair(3, t), Z1v);
+          zt = __ffma2_rn(pair(1, t), Z0v, zt);
+          const float2 lv = __ffma2_rn(Fv, a, zt);
+          l[t] = lv.x;
+          l[t + 1] = lv.y;
         }
       }
       tc_fence_before();
@@ -507,9 +521,10 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         al = (m == -INFINITY) ? 0.f : exp2f(m - mx);
         m = mx;
       }
-      lsum *= al;
-      zacc0 *= al;
-      zacc1 *= al;
+      const float2 al2 = make_float2(al, al);
+      lsum2 = __fmul2_rn(lsum2, al2);
+      zacc02 = __fmul2_rn(zacc02, al2);
+      zacc12 = __fmul2_rn(zacc12, al2);
       if (i > 0) {                                 // O of page i - 1 is complete and the weights buffer free
         if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (i - 1) & 1))) {
           ok = false;
@@ -527,26 +542,22 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           }
         }
       }
-      // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout
+      // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout; two tokens per op
+      const float2 negm = make_float2(-m, -m);
 #pragma unroll
       for (int j = 0; j < kSliceTok / 8; ++j) {   // tokens kSliceTok sl + 8j .. + 7
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {
-          float a0[2], a1[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 8 * j + 2 * pr + e;
-            const float4 v = vm[c];               // (s0, z0, s1, z1) of the token's V
-            const float p = fast_exp2(l[c] - m);
-            lsum += p;
-            zacc0 = fmaf(p, v.y, zacc0);
-            zacc1 = fmaf(p, v.w, zacc1);
-            a0[e] = p * v.x;
-            a1[e] = p * v.z;
-          }
-          w0[pr] = pack_f16x2(a0[0], a0[1]);
-          w1[pr] = pack_f16x2(a1[0], a1[1]);
+          const int c = 8 * j + 2 * pr;
+          const float2 d = __fadd2_rn(make_float2(l[c], l[c + 1]), negm);
+          const float2 pv = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+          lsum2 = __fadd2_rn(lsum2, pv);
+          zacc02 = __ffma2_rn(pv, pair(4 + 1, c), zacc02);              // V zero, group 0
+          zacc12 = __ffma2_rn(pv, pair(4 + 3, c), zacc12);              // V zero, group 1
+          const float2 a0 = __fmul2_rn(pv, pair(4 + 0, c)), a1 = __fmul2_rn(pv, pair(4 + 2, c));
+          w0[pr] = pack_f16x2(a0.x, a0.y);
+          w1[pr] = pack_f16x2(a1.x, a1.y);
         }
         const int off = canon_off(q, kSliceTok * sl + 8 * j, kP);
         *reinterpret_cast<uint4*>(pbase + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
@@ -561,6 +572,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
       *failed = 1;
     }
+    lsum = lsum2.x + lsum2.y;
+    zacc0 = zacc02.x + zacc02.y;
+    zacc1 = zacc12.x + zacc12.y;
     if (sl > 0) {                                  // this slice's sums, for the slice-0 warp of these rows
       rowc[q * kRowc + 3 * sl + 0] = lsum;
       rowc[q * kRowc + 3 * sl + 1] = zacc0;

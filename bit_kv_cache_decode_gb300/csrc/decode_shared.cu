@@ -55,7 +55,10 @@ constexpr float kLazyRescale = 8.f;                   // log2 growth of a row ma
 // shared memory (bytes; every operand 1024-byte aligned)
 constexpr int kQBytes = kShQ * kD * 2;                // one part of the rows' fragments: 32 KB
 constexpr int kKhBytes = kP * kD * 2;                 // expanded K of a page: 16 KB
-constexpr int kVtBytes = kD * kP * 2;                 // expanded V^T of a page: 16 KB
+// expanded V^T of a page: 16 blocks of 8 channel rows, each block 8 core matrices of 128 B plus 16 B of
+// padding, so the eight blocks a quarter warp writes at once start in distinct 16-byte bank slots
+constexpr int kVtSbo = (kP / 8) * 128 + 16;           // 1,040 B between 8-channel blocks
+constexpr int kVtBytes = (kD / 8) * kVtSbo;           // 16,640 B
 constexpr int kPBytes = kShQ * kP * 2;                // weights of one channel group: 16 KB
 constexpr int kOffRing = 0;
 constexpr int kOffQ = 15360;                          // kShStages * kBlockBytes, 1024-aligned
@@ -225,12 +228,11 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     for (int pp = 0; pp < 4; ++pp)
       x[pp] = *reinterpret_cast<const uint32_t*>(blk + kVCodesOff + (4 * kb + pp) * 64 + 4 * o);
 #pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = (ii + o) & 7;                  // staggered: the quarter warp's stores hit distinct banks
+    for (int i = 0; i < 8; ++i) {                // row i of core matrix (o, kb): channel 8o + i, tokens 8kb ..
       uint32_t c[4];
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) c[pp] = exact_at(x[pp], i);
-      *reinterpret_cast<uint4*>(vt + canon_off(8 * o + i, 8 * kb, kP)) = make_uint4(c[0], c[1], c[2], c[3]);
+      *reinterpret_cast<uint4*>(vt + o * kVtSbo + kb * 128 + i * 16) = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
 }
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma(tmem + kColO + 64 * G, umma_desc(p_a + G * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
-                 umma_desc(vt_a + kb3 * kVtBytes + G * 8 * (kP / 8) * 128 + 2 * kk * 128, 128, (kP / 8) * 128),
+                 umma_desc(vt_a + kb3 * kVtBytes + G * 8 * kVtSbo + 2 * kk * 128, 128, kVtSbo),
                  i > 0 || kk > 0);
         umma_commit(B_(kBarODone));
         umma_commit(B_(kBarBufFree + kb3));

@@ -175,24 +175,35 @@ void choose_splits_simt(int B, int hkv, int max_pages, int max_splits, int sms, 
 // runs as the decode is scheduled (2 CTAs per request and kv head), holds one decode CTA's
 // registers on each SM it occupies: the first wave has that many fewer slots.
 void choose_splits_mma(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int* nsplit,
-                       int* pps) {
+                       int* pps, int* occupancy) {
+  *occupancy = gq <= 4 ? 3 : 2;                      // the kernel variants' resident CTAs per SM
   if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
-  const int ctas_per_sm = gq <= 4 ? 3 : 2;           // the kernel's resident CTAs at its register count
-  const long units = (long)B * hkv, slots = std::max(1L, (long)sms * ctas_per_sm);
-  const long reserved = std::min((long)sms, 2 * units);
+  const long units = (long)B * hkv, reserved = std::min((long)sms, 2 * units);
   const int nmax = std::min(std::min(max_splits, max_pages), kMaxMmaSplits);
-  double best_cost = -1.0;
-  int best_n = nmax;
-  for (int n = 1; n <= nmax; ++n) {
-    const int per = (max_pages + n - 1) / n;
-    if (per > kMaxPagesPerMmaSplit && n < nmax) continue;
-    const long ctas = units * (n + nbf);
-    const long waves = std::max(1L, (ctas + reserved + slots - 1) / slots);
-    const double cost = (double)waves * ((per + 3) / 4 + 2.0);
-    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_n = n; }
+  auto best = [&](int ctas_per_sm, long* waves_out) {
+    const long slots = std::max(1L, (long)sms * ctas_per_sm);
+    double best_cost = -1.0;
+    int best_n = nmax;
+    long best_waves = 1;
+    for (int n = 1; n <= nmax; ++n) {
+      const int per = (max_pages + n - 1) / n;
+      if (per > kMaxPagesPerMmaSplit && n < nmax) continue;
+      const long ctas = units * (n + nbf);
+      const long waves = std::max(1L, (ctas + reserved + slots - 1) / slots);
+      const double cost = (double)waves * ((per + 3) / 4 + 2.0);
+      if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_n = n; best_waves = waves; }
+    }
+    *waves_out = best_waves;
+    return best_n;
+  };
+  long waves = 1;
+  int n = best(*occupancy, &waves);
+  if (gq <= 4 && waves > 2) {                        // many waves: the 4-CTA variant hides latency better
+    *occupancy = 4;
+    n = best(4, &waves);
   }
-  *nsplit = best_n;
-  *pps = (max_pages + best_n - 1) / best_n;
+  *nsplit = n;
+  *pps = (max_pages + n - 1) / n;
 }
 
 }  // namespace
@@ -371,7 +382,7 @@ void set_splits(const oscar_cache* c, int B, int max_hist_pages, int shared_page
   a.nsplit_shared = 0;
   if (shared_pages > 0 && a.algo == OSCAR_DECODE_MMA && c->lay.max_splits >= 2) {
     decode_split_policy(B, hkv, gq, a.nbf, max_hist_pages - shared_pages, c->lay.max_splits - 1, c->sms, a.algo,
-                        &a.nsplit, &a.pages_per_split);
+                        &a.nsplit, &a.pages_per_split, &a.mma_occupancy);
     const int qtiles = (B * gq + kSharedRows - 1) / kSharedRows;
     int ns = std::max(1, c->sms / (hkv * qtiles));
     ns = std::min(std::min(ns, shared_pages), c->lay.max_splits - a.nsplit);
@@ -380,7 +391,7 @@ void set_splits(const oscar_cache* c, int B, int max_hist_pages, int shared_page
     return;
   }
   decode_split_policy(B, hkv, gq, a.nbf, max_hist_pages, c->lay.max_splits, c->sms, a.algo, &a.nsplit,
-                      &a.pages_per_split);
+                      &a.pages_per_split, &a.mma_occupancy);
 }
 
 int decode_impl(oscar_cache* c, int layer, int B, const void* q, const int32_t* seq_lens, const int32_t* hist_pt,
@@ -642,8 +653,9 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 
 // The history split choice of oscar_decode_attention, for at most max_splits splits.
 void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
-                         int* nsplit, int* pps) {
-  if (algo == OSCAR_DECODE_MMA) choose_splits_mma(B, hkv, gq, nbf, max_pages, max_splits, sms, nsplit, pps);
+                         int* nsplit, int* pps, int* occupancy) {
+  *occupancy = 3;
+  if (algo == OSCAR_DECODE_MMA) choose_splits_mma(B, hkv, gq, nbf, max_pages, max_splits, sms, nsplit, pps, occupancy);
   else choose_splits_simt(B, hkv, max_pages, max_splits, sms, nsplit, pps);
 }
 

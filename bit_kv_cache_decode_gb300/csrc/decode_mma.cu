@@ -654,8 +654,10 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
 }
 
 // grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
-template <int NT>
-__global__ void __launch_bounds__(128, NT == 1 ? 3 : 2) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
+// MINB resident CTAs per SM (the register budget): 3 for grids of one or two waves (more registers, more
+// independent work per warp), 4 for grids of many waves (more warps to hide latency).
+template <int NT, int MINB>
+__global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
   TimelineSpan timeline_span(lv, kTlDecodeMma);
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
@@ -711,18 +713,22 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = (lv.hq / lv.hkv <= 4) ? cudaLaunchKernelEx(&cfg, k_decode_mma<1>, lv, ws, fa)
-                                              : cudaLaunchKernelEx(&cfg, k_decode_mma<2>, lv, ws, fa);
+  cudaError_t e;
+  if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2>, lv, ws, fa);
+  else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4>, lv, ws, fa);
+  else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3>, lv, ws, fa);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels() {
-  if (cudaFuncSetAttribute(k_decode_mma<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
-    return OSCAR_ERR_CUDA;
-  if (cudaFuncSetAttribute(k_decode_mma<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
-    return OSCAR_ERR_CUDA;
-  if (set_max_shared_carveout(reinterpret_cast<const void*>(k_decode_mma<1>)) != OSCAR_OK) return OSCAR_ERR_CUDA;
-  return set_max_shared_carveout(reinterpret_cast<const void*>(k_decode_mma<2>));
+  const void* fns[3] = {reinterpret_cast<const void*>(k_decode_mma<1, 3>), reinterpret_cast<const void*>(k_decode_mma<1, 4>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2>)};
+  for (const void* f : fns) {
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
+      return OSCAR_ERR_CUDA;
+    if (set_max_shared_carveout(f) != OSCAR_OK) return OSCAR_ERR_CUDA;
+  }
+  return OSCAR_OK;
 }
 
 }  // namespace oscar

@@ -113,7 +113,7 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.ev0 = a.ev1 = nullptr;
   a.nbf = nbf;
   decode_split_policy(B, (int)hkv, (int)(hq / hkv), nbf, max_hist_pages, max_splits, sms, a.algo, &a.nsplit,
-                      &a.pages_per_split);
+                      &a.pages_per_split, &a.mma_occupancy);
   ws.max_splits = a.nsplit;
   ws.nslots = partial_slots(a.nsplit, nbf);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

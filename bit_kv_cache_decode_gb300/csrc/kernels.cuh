@@ -71,6 +71,7 @@ struct DecodeArgs {
   int pages_per_split;   // history pages per split, at most (the tensor-core path spreads a request evenly)
   int shared_pages = 0;  // tensor-core path: history pages [0, shared_pages) are the same for every request
   int nsplit_shared = 0; // splits of the shared pages per kv head (their slots follow the nsplit history slots)
+  int mma_occupancy = 3; // tensor-core path, gq <= 4: resident CTAs per SM of the decode kernel variant (3 or 4)
   int algo;              // OSCAR_DECODE_SIMT / OSCAR_DECODE_MMA
   int len_add;           // the kernels attend over seq_lens[b] + len_add tokens
   int skip_qprep;        // the query prologue already ran (with the append, in one launch)
@@ -111,6 +112,6 @@ namespace oscar {
 // api.cu helpers for entry points that work without a cache handle
 int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, LayerView* out);
 void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
-                         int* nsplit, int* pps);
+                         int* nsplit, int* pps, int* occupancy);
 int configure_kernels();
 }  // namespace oscar

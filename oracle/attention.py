@@ -84,7 +84,7 @@ def decode_request(q: np.ndarray, seq_len: int, pool: poolmod.PoolModel, hist_pt
     hq = q.shape[0]
     gq = hq // geo.hkv
     kv_heads = list(range(geo.hkv)) if kv_heads is None else list(kv_heads)
-    seg, kk, vv = poolmod.gather_request(pool, seq_len, hist_pt, bf16_pt, heads=kv_heads)
+    seg, kk, vv = poolmod.gather_request(pool, seq_len, hist_pt, bf16_pt, heads=kv_heads, params=params)
     hist = np.array([s == "history" for s in seg], dtype=bool)
     o = np.full((hq, geo.d), np.nan)
     lse = np.full(hq, np.nan)

@@ -33,7 +33,10 @@ bytes (5120 for P = 64, d = 128, G = 64), in this order:
    [row 2p bytes (2o, 2o+1) | row 2p+1 bytes (2o, 2o+1)] of the same packed
    form, i.e. one little-endian 32-bit word whose low half is row 2p and high
    half row 2p+1.
-3. K metadata: row t at t*(d/G)*4: for each group g, fp16 scale then fp16 zero.
+3. K metadata: row t at t*(d/G)*m, m = 4 (fp16 format, the default): for each
+   group g, fp16 scale then fp16 zero; m = 2 (compact u8 format): for each group
+   g, the byte mn8 then the byte mx8 (see ``quant``: indices on the group's grid
+   over [-T, T]); the block is then 4608 bytes.
 4. V metadata: same layout.
 
 BF16 page block, one per (page, kv-head): K [P][d] bf16 then V [P][d] bf16.
@@ -55,6 +58,11 @@ class PoolGeometry:
     page: int = 64
     sink: int = 64
     recent: int = 256
+    meta_format: str = "f16"     # "f16": fp16 (scale, zero); "u8": 8-bit (mn8, mx8) on [-T, T]
+
+    @property
+    def meta_per_group(self) -> int:   # metadata bytes per group of one row
+        return {"f16": 4, "u8": 2}[self.meta_format]
 
     @property
     def codes_bytes(self) -> int:      # K (or V) codes per page block
@@ -62,7 +70,7 @@ class PoolGeometry:
 
     @property
     def meta_bytes(self) -> int:       # K (or V) metadata per page block
-        return self.page * (self.d // self.group) * 4
+        return self.page * (self.d // self.group) * self.meta_per_group
 
     @property
     def block_bytes(self) -> int:
@@ -108,23 +116,27 @@ class PoolModel:
         return g.codes_bytes + p[:, None] * (g.d // 2) + (4 * o + b)[None, :] + 2 * e[:, None]
 
     def _meta_index(self, rows: np.ndarray, which: int) -> np.ndarray:
-        """[n, (d/G)*4] byte offsets of rows' metadata; which = 0 for K, 1 for V."""
+        """[n, (d/G)*m] byte offsets of rows' metadata; which = 0 for K, 1 for V."""
         g = self.geo
-        per = (g.d // g.group) * 4
+        per = (g.d // g.group) * g.meta_per_group
         base = 2 * g.codes_bytes + which * g.meta_bytes
         return base + rows[:, None] * per + np.arange(per)[None, :]
 
-    @staticmethod
-    def _meta_bytes(s, z) -> np.ndarray:
-        s = np.asarray(s, dtype=np.float16)
-        z = np.asarray(z, dtype=np.float16)
-        sz = np.empty(s.shape[:-1] + (2 * s.shape[-1],), dtype=np.float16)
-        sz[..., 0::2] = s
-        sz[..., 1::2] = z
-        return np.ascontiguousarray(sz).view(np.uint8)
+    def _meta_dtype(self):
+        return np.float16 if self.geo.meta_format == "f16" else np.uint8
+
+    def _meta_bytes(self, a, b) -> np.ndarray:
+        """Interleave the two stored metadata fields of each group: (scale, zero) or (mn8, mx8)."""
+        a = np.asarray(a, dtype=self._meta_dtype())
+        b = np.asarray(b, dtype=self._meta_dtype())
+        ab = np.empty(a.shape[:-1] + (2 * a.shape[-1],), dtype=a.dtype)
+        ab[..., 0::2] = a
+        ab[..., 1::2] = b
+        return np.ascontiguousarray(ab).view(np.uint8)
 
     def write_history(self, page: int, rows, head: int, k_pack, k_s, k_z, v_pack, v_s, v_z):
-        """Write rows (int array [n]) of one (page, head): packed codes [n, d/4], scale/zero [n, d/G]."""
+        """Write rows (int array [n]) of one (page, head): packed codes [n, d/4] and the stored
+        metadata [n, d/G]: fp16 scale / zero, or u8 mn8 / mx8 in the compact format."""
         rows = np.atleast_1d(np.asarray(rows, dtype=np.int64))
         blk = self.int2[page, head]
         blk[self._k_byte_index(rows)] = np.asarray(k_pack).reshape(len(rows), -1)
@@ -133,14 +145,15 @@ class PoolModel:
         blk[self._meta_index(rows, 1)] = self._meta_bytes(np.reshape(v_s, (len(rows), -1)), np.reshape(v_z, (len(rows), -1)))
 
     def read_history(self, page: int, rows, head: int):
-        """(k_codes [n,d], k_s, k_z [n,d/G], v_codes, v_s, v_z) of rows of one (page, head)."""
+        """(k_codes [n,d], k_s, k_z [n,d/G], v_codes, v_s, v_z) of rows of one (page, head); the
+        metadata as stored (fp16 scale / zero, or u8 mn8 / mx8)."""
         rows = np.atleast_1d(np.asarray(rows, dtype=np.int64))
         blk = self.int2[page, head]
         kc = quant.unpack_codes(blk[self._k_byte_index(rows)])
         vc = quant.unpack_codes(blk[self._v_byte_index(rows)])
         out = []
         for which in (0, 1):
-            sz = np.ascontiguousarray(blk[self._meta_index(rows, which)]).view(np.float16)
+            sz = np.ascontiguousarray(blk[self._meta_index(rows, which)]).view(self._meta_dtype())
             out.append((sz[:, 0::2].copy(), sz[:, 1::2].copy()))
         return kc, out[0][0], out[0][1], vc, out[1][0], out[1][1]
 
@@ -181,13 +194,24 @@ def rotated_f32(x: np.ndarray, u32: np.ndarray) -> np.ndarray:
     return (np.asarray(x, dtype=np.float64) @ r).astype(np.float32)
 
 
-def quantize_history_tokens(k_f32, v_f32, prm: HeadParams, v_absorbed: bool, group: int):
-    """Rotate (K always; V unless absorbed), clip, quantise and pack tokens [n, d] of one head."""
+def quantize_history_tokens(k_f32, v_f32, prm: HeadParams, v_absorbed: bool, group: int,
+                            meta_format: str = "f16"):
+    """Rotate (K always; V unless absorbed), clip, quantise and pack tokens [n, d] of one head.
+
+    Returns (k_pack, k_a, k_b, v_pack, v_a, v_b), (a, b) the stored metadata of the format."""
     kr = rotated_f32(k_f32, prm.u_k)
     vr = np.asarray(v_f32, dtype=np.float32) if v_absorbed else rotated_f32(v_f32, prm.u_v)
-    kc, ks, kz = quant.quantize_token(kr, prm.tau_k, group)
-    vc, vs, vz = quant.quantize_token(vr, prm.tau_v, group)
+    qt = quant.quantize_token if meta_format == "f16" else quant.quantize_token_u8
+    kc, ks, kz = qt(kr, prm.tau_k, group)
+    vc, vs, vz = qt(vr, prm.tau_v, group)
     return quant.pack_codes(kc), ks, kz, quant.pack_codes(vc), vs, vz
+
+
+def dequant_params(a, b, tau, geo: PoolGeometry):
+    """Float (scale, zero) per group from the stored metadata (a, b) of the pool's format."""
+    if geo.meta_format == "f16":
+        return np.asarray(a, dtype=np.float16), np.asarray(b, dtype=np.float16)
+    return quant.u8_scale_zero(a, b, quant.group_bounds(tau, geo.group))
 
 
 def bf16_location(pos: int, seg: str, bf16_pt, geo: PoolGeometry):
@@ -205,7 +229,8 @@ def place(pool: PoolModel, pos: int, seq_len: int, head: int, k_f32, v_f32, prm:
     seg = segment_of(pos, seq_len, geo)
     if seg == "history":
         h = pos - geo.sink
-        pk = quantize_history_tokens(np.asarray(k_f32)[None], np.asarray(v_f32)[None], prm, v_absorbed, geo.group)
+        pk = quantize_history_tokens(np.asarray(k_f32)[None], np.asarray(v_f32)[None], prm, v_absorbed, geo.group,
+                                     geo.meta_format)
         pool.write_history(int(hist_pt[h // geo.page]), [h % geo.page], head, *pk)
         return
     page, row = bf16_location(pos, seg, bf16_pt, geo)
@@ -224,7 +249,7 @@ def prefill(pool: PoolModel, k, v, hist_pt, bf16_pt, params, v_absorbed: bool):
     for hd in range(geo.hkv):
         if lh > 0:
             pk = quantize_history_tokens(k[geo.sink: geo.sink + lh, hd], v[geo.sink: geo.sink + lh, hd],
-                                         params[hd], v_absorbed, geo.group)
+                                         params[hd], v_absorbed, geo.group, geo.meta_format)
             for i in range((lh + geo.page - 1) // geo.page):
                 a, b = i * geo.page, min((i + 1) * geo.page, lh)
                 pool.write_history(int(hist_pt[i]), np.arange(b - a), hd, *(x[a:b] for x in pk))
@@ -249,22 +274,26 @@ def append(pool: PoolModel, k_new, v_new, seq_len_before: int, hist_pt, bf16_pt,
         for hd in range(geo.hkv):
             kb, vb = pool.read_bf16(page, row, hd)
             pk = quantize_history_tokens(bits_to_f64(kb)[None].astype(np.float32),
-                                         bits_to_f64(vb)[None].astype(np.float32), params[hd], v_absorbed, geo.group)
+                                         bits_to_f64(vb)[None].astype(np.float32), params[hd], v_absorbed, geo.group,
+                                         geo.meta_format)
             pool.write_history(int(hist_pt[h // geo.page]), [h % geo.page], hd, *pk)
     for hd in range(geo.hkv):
         place(pool, L_old, L_old + 1, hd, k_new[hd], v_new[hd], params[hd], v_absorbed, hist_pt, bf16_pt)
 
 
-def gather_request(pool: PoolModel, seq_len: int, hist_pt, bf16_pt, heads=None):
+def gather_request(pool: PoolModel, seq_len: int, hist_pt, bf16_pt, heads=None, params=None):
     """Decode one request's cache from the pool bytes.
 
     Returns (seg, k, v): seg is a list of segment names per position; k, v are
     [L, n_heads, d] fp64 arrays where BF16 rows hold the stored bf16 values and
     history rows hold the dequantised values (rotated basis). ``heads`` selects
-    kv heads (default: all).
+    kv heads (default: all). ``params`` (the heads' HeadParams, indexed by kv head) is required
+    by the compact metadata format, whose grid depends on the clip thresholds.
     """
     geo = pool.geo
     heads = list(range(geo.hkv)) if heads is None else list(heads)
+    if geo.meta_format != "f16" and params is None:
+        raise ValueError("the compact metadata format needs the heads' clip thresholds")
     L = seq_len
     kk = np.zeros((L, len(heads), geo.d))
     vv = np.zeros((L, len(heads), geo.d))
@@ -273,9 +302,11 @@ def gather_request(pool: PoolModel, seq_len: int, hist_pt, bf16_pt, heads=None):
     for j, hd in enumerate(heads):
         for i in range((lh + geo.page - 1) // geo.page):
             a, b = i * geo.page, min((i + 1) * geo.page, lh)
-            kc, ks, kz, vc, vs, vz = pool.read_history(int(hist_pt[i]), np.arange(b - a), hd)
-            kk[geo.sink + a: geo.sink + b, j] = quant.dequantize(kc, ks, kz, geo.group)
-            vv[geo.sink + a: geo.sink + b, j] = quant.dequantize(vc, vs, vz, geo.group)
+            kc, ka, kb, vc, va, vb = pool.read_history(int(hist_pt[i]), np.arange(b - a), hd)
+            tk = params[hd].tau_k if params is not None else None
+            tv = params[hd].tau_v if params is not None else None
+            kk[geo.sink + a: geo.sink + b, j] = quant.dequantize_sz(kc, *dequant_params(ka, kb, tk, geo), geo.group)
+            vv[geo.sink + a: geo.sink + b, j] = quant.dequantize_sz(vc, *dequant_params(va, vb, tv, geo), geo.group)
         for pos in range(L):
             if seg[pos] != "history":
                 page, row = bf16_location(pos, seg[pos], bf16_pt, geo)

@@ -20,6 +20,15 @@ Readings taken where the pages are silent (each is listed in the design doc):
   in the order written, so that a GPU implementation can reproduce the codes
   bit for bit.
 
+Compact metadata (16 bits per group, the pages' 2.25 bits per history element; row f2 of the scope
+table, a format of this library's choosing): the group's minimum and maximum are stored as 8-bit
+indices on a fixed grid over [-T, T], T the group's largest clip threshold (every clipped value lies
+within it). With step D = (2 T) / 255: mn8 = clamp(floor((mn + T) / D), 0, 255), mx8 = clamp(ceil((mx
++ T) / D), 0, 255); the dequantisation parameters are zero' = mn8 D - T and scale' = (mx8 - mn8) D / 3,
+each operation a single float32 rounding in the order written (no fused multiply-add), and the codes
+are computed from them exactly as in the fp16 format. Rounding mn down and mx up keeps [mn, mx] inside
+[zero', zero' + 3 scale'] (up to float32 rounding), so |y - xhat| <= scale' / 2 still holds.
+
 Packing: channel j of a token goes to byte j // 4 at bits 2*(j % 4)
 (little-endian within the byte). How tokens of one page are arranged in
 memory is the pool's business (see ``oracle.pool``).
@@ -74,9 +83,76 @@ def quantize_groups(y: np.ndarray, group: int):
     return code.astype(np.uint8).reshape(y.shape), s16, z16
 
 
+def _codes(yg: np.ndarray, s32: np.ndarray, z32: np.ndarray) -> np.ndarray:
+    """code = clamp(rint((y - zero') / scale'), 0, 3), 0 where scale' == 0; float32 op by op."""
+    diff = (yg - z32).astype(F32)             # one fp32 subtraction
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (diff / s32).astype(F32)          # one fp32 division
+    code = np.clip(np.rint(t), 0.0, 3.0)      # round half to even
+    code = np.where(s32 == 0, 0.0, code)
+    return np.nan_to_num(code, nan=0.0)
+
+
+def group_bounds(tau: np.ndarray, group: int) -> np.ndarray:
+    """T per group of ``group`` consecutive channels: the largest clip threshold of the group (float32)."""
+    t = np.asarray(tau, dtype=F32)
+    return t.reshape(t.shape[:-1] + (t.shape[-1] // group, group)).max(axis=-1)
+
+
+def u8_scale_zero(mn8: np.ndarray, mx8: np.ndarray, T: np.ndarray):
+    """(scale', zero') in float32 of the compact format: D = 2T / 255, zero' = mn8 D - T,
+    scale' = (mx8 - mn8) D / 3, one rounding per operation (T broadcast over leading axes)."""
+    T = np.asarray(T, dtype=F32)
+    D = ((T + T).astype(F32) / F32(255.0)).astype(F32)
+    a = np.asarray(mn8).astype(F32)
+    b = np.asarray(mx8).astype(F32)
+    z = ((a * D).astype(F32) - T).astype(F32)
+    s = (((b - a).astype(F32) * D).astype(F32) / F32(3.0)).astype(F32)
+    return s, z
+
+
+def quantize_groups_u8(y: np.ndarray, group: int, T: np.ndarray):
+    """Quantise clipped float32 values y [..., d] with the compact (8 + 8 bit) metadata.
+
+    T [d/group]: the groups' bounds (``group_bounds`` of the clip thresholds).
+    Returns (codes uint8 [..., d], mn8 uint8 [..., d/group], mx8 uint8 [..., d/group]).
+    """
+    y = np.asarray(y, dtype=F32)
+    d = y.shape[-1]
+    assert d % group == 0
+    yg = y.reshape(y.shape[:-1] + (d // group, group))
+    mn = yg.min(axis=-1)
+    mx = yg.max(axis=-1)
+    T = np.broadcast_to(np.asarray(T, dtype=F32), mn.shape)
+    D = ((T + T).astype(F32) / F32(255.0)).astype(F32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lo = (((mn + T).astype(F32)) / D).astype(F32)
+        hi = (((mx + T).astype(F32)) / D).astype(F32)
+    mn8 = np.where(D > 0, np.clip(np.floor(np.nan_to_num(lo, nan=0.0)), 0, 255), 0).astype(np.uint8)
+    mx8 = np.where(D > 0, np.clip(np.ceil(np.nan_to_num(hi, nan=0.0)), 0, 255), 0).astype(np.uint8)
+    s, z = u8_scale_zero(mn8, mx8, T)
+    code = _codes(yg, s[..., None], z[..., None])
+    return code.astype(np.uint8).reshape(y.shape), mn8, mx8
+
+
 def quantize_token(x_rot: np.ndarray, tau: np.ndarray, group: int = 64):
     """Clip then quantise rotated float32 tokens x_rot [..., d]."""
     return quantize_groups(clip(x_rot, tau), group)
+
+
+def quantize_token_u8(x_rot: np.ndarray, tau: np.ndarray, group: int = 64):
+    """Clip then quantise rotated float32 tokens x_rot [..., d] with the compact metadata."""
+    return quantize_groups_u8(clip(x_rot, tau), group, group_bounds(tau, group))
+
+
+def dequantize_sz(codes: np.ndarray, s: np.ndarray, z: np.ndarray, group: int = 64) -> np.ndarray:
+    """xhat = zero + scale * code in fp64 for any float scale / zero per group of ``group`` channels."""
+    codes = np.asarray(codes)
+    d = codes.shape[-1]
+    c = codes.astype(np.float64).reshape(codes.shape[:-1] + (d // group, group))
+    sf = np.asarray(s).astype(np.float64)[..., None]
+    zf = np.asarray(z).astype(np.float64)[..., None]
+    return (zf + sf * c).reshape(codes.shape)
 
 
 def dequantize(codes: np.ndarray, s16: np.ndarray, z16: np.ndarray, group: int = 64) -> np.ndarray:

@@ -24,9 +24,10 @@ Compact metadata (16 bits per group, the pages' 2.25 bits per history element; r
 table, a format of this library's choosing): the group's minimum and maximum are stored as 8-bit
 indices on a fixed grid over [-T, T], T the group's largest clip threshold (every clipped value lies
 within it). With step D = (2 T) / 255: mn8 = clamp(floor((mn + T) / D), 0, 255), mx8 = clamp(ceil((mx
-+ T) / D), 0, 255); the dequantisation parameters are zero' = mn8 D - T and scale' = (mx8 - mn8) D / 3,
-each operation a single float32 rounding in the order written (no fused multiply-add), and the codes
-are computed from them exactly as in the fp16 format. Rounding mn down and mx up keeps [mn, mx] inside
++ T) / D), 0, 255), each operation of the two quotients rounded to float32 in the order written; the
+dequantisation parameters are zero' = fl32(mn8 D - T) (one rounding of the exact value, a fused
+multiply-add) and scale' = fl32((mx8 - mn8) E) with E = fl32(D / 3), and the codes are computed from
+them exactly as in the fp16 format. Rounding mn down and mx up keeps [mn, mx] inside
 [zero', zero' + 3 scale'] (up to float32 rounding), so |y - xhat| <= scale' / 2 still holds.
 
 Packing: channel j of a token goes to byte j // 4 at bits 2*(j % 4)
@@ -99,15 +100,23 @@ def group_bounds(tau: np.ndarray, group: int) -> np.ndarray:
     return t.reshape(t.shape[:-1] + (t.shape[-1] // group, group)).max(axis=-1)
 
 
-def u8_scale_zero(mn8: np.ndarray, mx8: np.ndarray, T: np.ndarray):
-    """(scale', zero') in float32 of the compact format: D = 2T / 255, zero' = mn8 D - T,
-    scale' = (mx8 - mn8) D / 3, one rounding per operation (T broadcast over leading axes)."""
+def u8_steps(T: np.ndarray):
+    """(D, E) in float32 of the compact format: D = fl32(2T / 255), E = fl32(D / 3)."""
     T = np.asarray(T, dtype=F32)
     D = ((T + T).astype(F32) / F32(255.0)).astype(F32)
-    a = np.asarray(mn8).astype(F32)
-    b = np.asarray(mx8).astype(F32)
-    z = ((a * D).astype(F32) - T).astype(F32)
-    s = (((b - a).astype(F32) * D).astype(F32) / F32(3.0)).astype(F32)
+    return D, (D / F32(3.0)).astype(F32)
+
+
+def u8_scale_zero(mn8: np.ndarray, mx8: np.ndarray, T: np.ndarray):
+    """(scale', zero') in float32 of the compact format (T broadcast over leading axes):
+    zero' = fl32(mn8 D - T), the exact value rounded once (mn8 D has at most 32 significant bits and
+    lies within a factor 2 of T, so the fp64 difference is exact); scale' = fl32((mx8 - mn8) E)."""
+    T = np.asarray(T, dtype=F32)
+    D, E = u8_steps(T)
+    a = np.asarray(mn8).astype(np.float64)
+    b = np.asarray(mx8).astype(np.float64)
+    z = (a * D.astype(np.float64) - T.astype(np.float64)).astype(F32)
+    s = ((b - a).astype(F32) * E).astype(F32)
     return s, z
 
 
@@ -124,7 +133,7 @@ def quantize_groups_u8(y: np.ndarray, group: int, T: np.ndarray):
     mn = yg.min(axis=-1)
     mx = yg.max(axis=-1)
     T = np.broadcast_to(np.asarray(T, dtype=F32), mn.shape)
-    D = ((T + T).astype(F32) / F32(255.0)).astype(F32)
+    D, _ = u8_steps(T)
     with np.errstate(divide="ignore", invalid="ignore"):
         lo = (((mn + T).astype(F32)) / D).astype(F32)
         hi = (((mx + T).astype(F32)) / D).astype(F32)

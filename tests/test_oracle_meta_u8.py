@@ -188,3 +188,19 @@ def test_compact_gather_needs_thresholds_and_stays_within_half_a_step():
         s, z = quant.u8_scale_zero(mn8, mx8, quant.group_bounds(tau, 64))
         step = s.astype(np.float64).repeat(64, axis=1)
         assert np.all(np.abs(got[hist, 0] - y) <= 0.5 * step * (1 + 1e-5) + 1e-6)
+
+
+def test_zero_point_is_the_once_rounded_exact_value():
+    rng = np.random.default_rng(9)
+    for _ in range(2000):
+        T = F32(rng.uniform(1e-3, 50.0) * 10.0 ** int(rng.integers(-3, 3)))
+        a = int(rng.integers(0, 256))
+        b = int(rng.integers(a, 256))
+        s, z = quant.u8_scale_zero(np.uint8(a), np.uint8(b), T)
+        D, E = quant.u8_steps(T)
+        exact = Fraction(a) * Fraction(float(D)) - Fraction(float(T))
+        zf = float(z)
+        ulp = float(np.spacing(np.abs(F32(zf)))) if zf != 0 else float(np.spacing(F32(0)))
+        assert abs(Fraction(zf) - exact) <= Fraction(ulp) / 2
+        assert float(s) == float(F32(F32(b - a) * E))
+        assert float(E) == float(F32(D / F32(3)))

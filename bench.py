@@ -41,6 +41,9 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV tokens/s and achieved HBM GB/s vs GB300 peak, 100K ctx"
 UNIT = "KV tokens/s"
 HIST_BYTES = 80          # per history token per kv head: 32 B K codes + 32 B V codes + 16 B fp16 scale/zero
+HIST_BYTES_BY_META = {"f16": 80, "u8": 72}     # the compact format stores 8 B of (mn8, mx8) per token
+STORAGE = {"f16": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
+           "u8": "int2 history (8-bit min/max grid indices per 64-group, 2.25 bits per element) + bf16 sink/recent"}
 BF16_BYTES = 512         # per BF16 token per kv head: K and V, 128 x 2 B each
 
 WORKLOADS = {
@@ -127,7 +130,8 @@ class ClockSampler:
 # workload construction
 
 
-def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_capacity: int = 64, algo: int = 1):
+def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_capacity: int = 64, algo: int = 1,
+                   meta: str = "f16"):
     import torch
     import bit_kv_cache_decode_gb300 as osc
     import synth
@@ -155,7 +159,8 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
         else:
             bf16_pt[r] = 5 * r + np.arange(5)
     cfg = osc.CacheConfig(num_layers=nl, num_kv_heads=H, num_q_heads=hq, num_int2_pages=n_int2,
-                          num_bf16_pages=n_bf16, max_batch=B, max_splits=512, v_mode=osc.V_ABSORBED)
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=512, v_mode=osc.V_ABSORBED,
+                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
     cache = osc.OscarCache(cfg, device=device)
     cache.set_decode_algo(algo)
     # offline calibration on the host (library routine), one per (layer, kv head)
@@ -269,7 +274,7 @@ def run_ours(args, rank: int, world: int, device):
     total_steps = args.warmup + args.steps
     mixed = isinstance(WORKLOADS[args.workload]["ctx"], tuple)
     wl = build_workload(args.workload, seed, device, with_bf16=not (args.no_bf16 or mixed),
-                        steps_capacity=3 * total_steps + 16, algo=args.algo)
+                        steps_capacity=3 * total_steps + 16, algo=args.algo, meta=args.meta_format)
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
     stream = torch.cuda.current_stream()
     sm = synth.sm_scale()
@@ -350,7 +355,7 @@ def run_ours(args, rank: int, world: int, device):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items()},
                    "head_dim": 128, "sink": 64, "recent": 256, "group": 64, "page": 64, "v_mode": "absorbed",
-                   "storage": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
+                   "storage": STORAGE[args.meta_format], "meta_format": args.meta_format,
                    "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
                    "launch": "one CUDA graph per step (oscar_decode_step%s per layer), new tokens copied in"
@@ -546,7 +551,9 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
     import torch
     torch.cuda.synchronize()
     cfg = wl["cfg"]
-    pm = P.PoolModel(P.PoolGeometry(hkv=H), cfg.num_int2_pages, cfg.num_bf16_pages)
+    import bit_kv_cache_decode_gb300 as osc
+    geo = P.PoolGeometry(hkv=H, meta_format="u8" if cfg.meta_format == osc.META_U8 else "f16")
+    pm = P.PoolModel(geo, cfg.num_int2_pages, cfg.num_bf16_pages)
     pm.int2[:] = cache.int2_pages(0).cpu().numpy()
     pm.bf16[:] = cache.bf16_pages(0).cpu().numpy().view(np.uint16).reshape(pm.bf16.shape)
     prm = [P.HeadParams(c["U_K"], c["U_V"], c["tau_K"], c["tau_V"]) for c in wl["cals"][:H]]
@@ -580,7 +587,7 @@ def run_reference(args, rank, world):
     L, H, hq = w["ctx"], w["hkv"], w["hq"]
     seed = 1234
     # build layer 0 of the workload with the oracle itself (one kv head per step sample)
-    geo = P.PoolGeometry(hkv=1)
+    geo = P.PoolGeometry(hkv=1, meta_format=args.meta_format)
     nh = (L - 320 + 63) // 64
     pm = P.PoolModel(geo, nh, 5)
     qc, kc, vc = synth.calibration(seed, 0, 0)
@@ -647,7 +654,11 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--meta-format", choices=["f16", "u8"], default="f16",
+                    help="INT2 group metadata: fp16 scale/zero (default) or the compact 16-bit format")
     args = ap.parse_args()
+    global HIST_BYTES
+    HIST_BYTES = HIST_BYTES_BY_META[args.meta_format]
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))

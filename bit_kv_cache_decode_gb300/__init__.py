@@ -27,6 +27,7 @@ V_ABSORBED, V_EXPLICIT = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 KIND_K, KIND_V = 0, 1
 DECODE_SIMT, DECODE_MMA = 0, 1
+META_F16, META_U8 = 0, 1
 
 # every symbol include/oscar.h declares
 EXPORTS = (
@@ -49,7 +50,7 @@ class OscarError(RuntimeError):
 class Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "num_layers", "num_kv_heads", "num_q_heads", "head_dim", "group", "page_size", "sink", "recent",
-        "num_int2_pages", "num_bf16_pages", "v_mode", "max_batch", "max_splits")]
+        "num_int2_pages", "num_bf16_pages", "v_mode", "max_batch", "max_splits", "meta_format")]
 
 
 def _load() -> ctypes.CDLL:
@@ -146,11 +147,12 @@ class CacheConfig:
     page_size: int = 64
     sink: int = 64
     recent: int = 256
+    meta_format: int = META_F16        # META_U8: 16-bit (mn8, mx8) group metadata, 4608-byte INT2 blocks
 
     def layout(self) -> Layout:
         return Layout(self.num_layers, self.num_kv_heads, self.num_q_heads, self.head_dim, self.group,
                       self.page_size, self.sink, self.recent, self.num_int2_pages, self.num_bf16_pages, self.v_mode,
-                      self.max_batch, self.max_splits)
+                      self.max_batch, self.max_splits, self.meta_format)
 
 
 def cache_bytes(cfg: CacheConfig) -> tuple[int, int]:
@@ -199,10 +201,12 @@ class OscarCache:
         return a.value, b.value, c.value
 
     def int2_pages(self, layer: int):
-        """uint8 view [num_int2_pages, Hkv, 5120] of a layer's INT2 page blocks."""
+        """uint8 view [num_int2_pages, Hkv, block] of a layer's INT2 page blocks (block = 5120 bytes,
+        or 4608 with the compact META_U8 metadata)."""
         o, _, _ = self.layer_offsets(layer)
-        n = self.cfg.num_int2_pages * self.cfg.num_kv_heads * 5120
-        return self.pool[o:o + n].view(self.cfg.num_int2_pages, self.cfg.num_kv_heads, 5120)
+        blk = 4608 if self.cfg.meta_format == META_U8 else 5120
+        n = self.cfg.num_int2_pages * self.cfg.num_kv_heads * blk
+        return self.pool[o:o + n].view(self.cfg.num_int2_pages, self.cfg.num_kv_heads, blk)
 
     def bf16_pages(self, layer: int):
         """uint8 view [num_bf16_pages, Hkv, 32768] of a layer's BF16 page blocks."""

@@ -45,6 +45,7 @@ int check_layout(const oscar_layout* L) {
   if (L->page_size < 1 || L->sink % L->page_size != 0 || L->recent % L->page_size != 0) return OSCAR_ERR_INVALID_ARG;
   if (L->group < 1 || L->head_dim % L->group != 0) return OSCAR_ERR_INVALID_ARG;
   if (L->v_mode != OSCAR_V_ABSORBED && L->v_mode != OSCAR_V_EXPLICIT) return OSCAR_ERR_INVALID_ARG;
+  if (L->meta_format != OSCAR_META_F16 && L->meta_format != OSCAR_META_U8) return OSCAR_ERR_INVALID_ARG;
   if (L->head_dim != kD || L->group != kG || L->page_size != kP) return OSCAR_ERR_UNSUPPORTED;
   if (!is_pow2_le8(L->num_q_heads / L->num_kv_heads)) return OSCAR_ERR_UNSUPPORTED;
   if (L->max_splits > 4096) return OSCAR_ERR_UNSUPPORTED;
@@ -53,7 +54,8 @@ int check_layout(const oscar_layout* L) {
 
 void sizes(const oscar_layout* L, size_t* int2b, size_t* bf16b, size_t* prmb, size_t* layerb, size_t* poolb,
            size_t* wsb) {
-  *int2b = align_up((size_t)L->num_int2_pages * L->num_kv_heads * kBlockBytes);
+  *int2b = align_up((size_t)L->num_int2_pages * L->num_kv_heads *
+                    (L->meta_format == OSCAR_META_U8 ? kBlockBytesU8 : kBlockBytes));
   *bf16b = align_up((size_t)L->num_bf16_pages * L->num_kv_heads * kBf16BlockBytes);
   *prmb = align_up((size_t)L->num_kv_heads * kParamFloats * sizeof(float));
   *layerb = *int2b + *bf16b + *prmb;
@@ -82,6 +84,8 @@ LayerView view(const oscar_cache* c, int layer) {
   v.sink = c->lay.sink;
   v.recent = c->lay.recent;
   v.v_explicit = c->lay.v_mode == OSCAR_V_EXPLICIT;
+  v.meta_u8 = c->lay.meta_format == OSCAR_META_U8;
+  v.blk_bytes = v.meta_u8 ? kBlockBytesU8 : kBlockBytes;
   v.status = c->status;
   v.layer = layer;
   v.timeline = c->timeline;
@@ -333,6 +337,21 @@ int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float*
     }
     std::memcpy(dst + kTauKOff, tau_K + (size_t)h * kD, kD * sizeof(float));
     std::memcpy(dst + kTauVOff, tau_V + (size_t)h * kD, kD * sizeof(float));
+    // compact-format grid per (kind, group): T = the group's largest threshold, D = fl32(2T / 255),
+    // E = fl32(D / 3) (single-precision operations, each correctly rounded)
+    for (int kind = 0; kind < 2; ++kind)
+      for (int g = 0; g < kNG; ++g) {
+        const float* t = (kind == 0 ? tau_K : tau_V) + (size_t)h * kD + g * kG;
+        float T = t[0];
+        for (int j = 1; j < kG; ++j) T = t[j] > T ? t[j] : T;
+        const float D = (T + T) / 255.0f;
+        const float E = D / 3.0f;
+        float* mc = dst + kMetaCOff + kind * 8 + g * 4;
+        mc[0] = T;
+        mc[1] = D;
+        mc[2] = E;
+        mc[3] = 0.f;
+      }
   }
   LayerView v = view(c, layer);
   cudaError_t e = cudaMemcpyAsync(const_cast<float*>(v.params), host.data(), host.size() * sizeof(float),
@@ -644,6 +663,8 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
   out->sink = L->sink;
   out->recent = L->recent;
   out->v_explicit = L->v_mode == OSCAR_V_EXPLICIT;
+  out->meta_u8 = L->meta_format == OSCAR_META_U8;
+  out->blk_bytes = out->meta_u8 ? kBlockBytesU8 : kBlockBytes;
   out->status = status;
   out->layer = layer;
   out->timeline = nullptr;

@@ -27,6 +27,12 @@ constexpr int kVCodesOff = kCodeBytes;
 constexpr int kKMetaOff = 2 * kCodeBytes;
 constexpr int kVMetaOff = 2 * kCodeBytes + kMetaBytes;
 constexpr int kBlockBytes = 2 * kCodeBytes + 2 * kMetaBytes;   // 5120
+// Compact metadata (OSCAR_META_U8, 16 bits per group: the pages' 2.25 bits per history element):
+// per row and group the bytes (mn8, mx8), indices on a grid of 255 steps over [-T, T], T the
+// group's largest clip threshold. K metadata at kKMetaOff, V metadata right after it.
+constexpr int kMetaBytesU8 = kP * kNG * 2;                       // 256
+constexpr int kVMetaOffU8 = 2 * kCodeBytes + kMetaBytesU8;       // 4352
+constexpr int kBlockBytesU8 = 2 * kCodeBytes + 2 * kMetaBytesU8; // 4608
 constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D] then V [P][D]
 // rotation parameters per kv head (float32 words): U_K [D][D], U_V [D][D], U_V transposed [D][D]
 // (for coalesced reads of R_V^T in the merge), tau_K [D], tau_V [D], then the composite
@@ -36,7 +42,10 @@ constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D
 constexpr int kRFragWords = 8 * 16 * 32 * 4;  // [k-block 8][n-tile 16][lane 32][hi b0, hi b1, lo b0, lo b1]
 constexpr int kUKOff = 0, kUVOff = kD * kD, kUVtOff = 2 * kD * kD, kTauKOff = 3 * kD * kD,
               kTauVOff = 3 * kD * kD + kD, kRKFragOff = 3 * kD * kD + 2 * kD, kRVFragOff = kRKFragOff + kRFragWords;
-constexpr int kParamFloats = kRVFragOff + kRFragWords;
+// then, per kind and group, the compact format's grid constants {T, D = fl32(2T / 255), E = fl32(D / 3),
+// 0} (kMetaCFloats words, padded so that a head's parameters stay 128-byte aligned)
+constexpr int kMetaCOff = kRVFragOff + kRFragWords, kMetaCFloats = 32;
+constexpr int kParamFloats = kMetaCOff + kMetaCFloats;
 // one split partial: m (log2 units), l, then acc[D]; padded to 132 floats (528 B, 16 B aligned)
 constexpr int kPartFloats = kD + 4;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -48,6 +57,8 @@ struct LayerView {
   const float* params;    // [hkv][kParamFloats]
   const float* next_params;   // the next layer's parameters (prefetched into L2 by the prologue), or null
   int n_int2, n_bf16, hkv, hq, sink, recent, v_explicit;
+  int meta_u8;            // OSCAR_META_U8 pool: 8-bit (mn8, mx8) metadata, 4608-byte INT2 blocks
+  int blk_bytes;          // INT2 block bytes: kBlockBytes or kBlockBytesU8
   int* status;            // device status word
   int layer;              // layer index (timeline records only)
   unsigned long long* timeline;   // optional kernel timeline (see oscar_trace_timeline), or null
@@ -57,10 +68,34 @@ struct LayerView {
 __device__ __forceinline__ void flag(int* status, int bits) { atomicOr(status, bits); }
 
 __device__ __forceinline__ const uint8_t* int2_block(const LayerView& lv, int page, int head) {
-  return lv.int2 + ((size_t)page * lv.hkv + head) * kBlockBytes;
+  return lv.int2 + ((size_t)page * lv.hkv + head) * lv.blk_bytes;
 }
 __device__ __forceinline__ uint8_t* int2_block_w(const LayerView& lv, int page, int head) {
-  return lv.int2 + ((size_t)page * lv.hkv + head) * kBlockBytes;
+  return lv.int2 + ((size_t)page * lv.hkv + head) * lv.blk_bytes;
+}
+// Grid constants {T, D, E, 0} of (kv head h, kind, group G) of the compact format.
+__device__ __forceinline__ const float* meta_consts(const LayerView& lv, int h, int kind) {
+  return lv.params + (size_t)h * kParamFloats + kMetaCOff + kind * 8;
+}
+
+// Compact format, write side: the group's grid indices from its clipped min / max, and the
+// dequantisation parameters the codes are computed with. Every operation rounds as written: the
+// quotients with __fadd_rn / __fdiv_rn, zero' = fma(mn8, D, -T), scale' = (mx8 - mn8) * E.
+__device__ __forceinline__ void u8_quant_params(float mn, float mx, float T, float D, float E, unsigned& mn8,
+                                                unsigned& mx8, float& scale, float& zero) {
+  mn8 = mx8 = 0u;
+  if (D > 0.f) {
+    const float lo = floorf(__fdiv_rn(__fadd_rn(mn, T), D));
+    const float hi = ceilf(__fdiv_rn(__fadd_rn(mx, T), D));
+    mn8 = (unsigned)fminf(fmaxf(lo, 0.f), 255.f);
+    mx8 = (unsigned)fminf(fmaxf(hi, 0.f), 255.f);
+  }
+  scale = __fmul_rn((float)(mx8 - mn8), E);
+  zero = __fmaf_rn((float)mn8, D, -T);
+}
+// Compact format, read side: (scale', zero') of one group from its two index bytes.
+__device__ __forceinline__ float2 u8_scale_zero(unsigned mn8, unsigned mx8, float T, float D, float E) {
+  return make_float2(__fmul_rn((float)(int)(mx8 - mn8), E), __fmaf_rn((float)mn8, D, -T));
 }
 __device__ __forceinline__ __nv_bfloat16* bf16_row(const LayerView& lv, int page, int head, int kind, int row) {
   return reinterpret_cast<__nv_bfloat16*>(lv.bf16 + ((size_t)page * lv.hkv + head) * kBf16BlockBytes) +

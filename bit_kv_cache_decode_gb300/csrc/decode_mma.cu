@@ -121,8 +121,15 @@ __device__ __forceinline__ float* part_row(const DecodeWorkspace& ws, int b, int
   return ws.partials + (((size_t)b * hq_total + hq) * ws.nslots + slot) * kPartFloats;
 }
 
-// History split `split` of group (b, h): see the file comment.
-template <int NT>
+// (scale', zero') of both groups of one row from its four compact-format index bytes.
+__device__ __forceinline__ void u8_row_meta(uint32_t m, const float (&c)[6], float2& g0, float2& g1) {
+  g0 = u8_scale_zero(m & 0xffu, (m >> 8) & 0xffu, c[0], c[1], c[2]);
+  g1 = u8_scale_zero((m >> 16) & 0xffu, m >> 24, c[3], c[4], c[5]);
+}
+
+// History split `split` of group (b, h): see the file comment. U8: the pool holds the compact
+// (mn8, mx8) metadata (4608-byte blocks, staged in the same 5120-byte slots).
+template <int NT, bool U8>
 __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
                                            uint8_t* smem, int split, int h, int b, unsigned long long* trace) {
   const int* __restrict__ seq_lens = fa.seq_lens;
@@ -170,7 +177,8 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     }
     if (lane == 0) {
       const int s = i % kStages;
-      bulk_load_hint(stage_s + s * kBlockBytes, int2_block(lv, pid, h), kBlockBytes, bar_s + 8 * s, l2_evict_first());
+      bulk_load_hint(stage_s + s * kBlockBytes, int2_block(lv, pid, h), U8 ? kBlockBytesU8 : kBlockBytes, bar_s + 8 * s,
+                     l2_evict_first());
     }
     return true;
   };
@@ -192,6 +200,18 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   };
 
   // ---- per-lane constants -------------------------------------------------------
+  float kmc[6], vmc[6];                // compact format: {T, D, E} of groups 0, 1 for K and for V
+  if constexpr (U8) {
+    const float* mk = meta_consts(lv, h, OSCAR_KIND_K);
+    const float* mv = meta_consts(lv, h, OSCAR_KIND_V);
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      kmc[i] = mk[i];
+      kmc[3 + i] = mk[4 + i];
+      vmc[i] = mv[i];
+      vmc[3 + i] = mv[4 + i];
+    }
+  }
   uint32_t qf[8][NT][2];
   {
     const uint32_t* frag = ws.qfrag + ((size_t)b * lv.hkv + h) * kFragWords;
@@ -292,12 +312,18 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             }
           }
         }
-        const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r0 * 8);
-        const uint2 mk1 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r1 * 8);
-        const float2 sz00 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.x));   // scale0, zero0 of row r0
-        const float2 sz01 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.y));   // scale1, zero1
-        const float2 sz10 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.x));
-        const float2 sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
+        float2 sz00, sz01, sz10, sz11;             // (scale, zero) of groups 0, 1 of rows r0, r1
+        if constexpr (U8) {
+          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kKMetaOff + r0 * 4), kmc, sz00, sz01);
+          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kKMetaOff + r1 * 4), kmc, sz10, sz11);
+        } else {
+          const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r0 * 8);
+          const uint2 mk1 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r1 * 8);
+          sz00 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.x));
+          sz01 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.y));
+          sz10 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.x));
+          sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float a00 = c[0][nt][0] + c[0][nt][1], a01 = c[1][nt][0] + c[1][nt][1];   // row r0: hi + lo per group
@@ -347,12 +373,18 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const int r0 = 16 * kt + g, r1 = r0 + 8;
-        const uint2 mv0 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r0 * 8);
-        const uint2 mv1 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r1 * 8);
-        float2 sv00 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.x));
-        float2 sv01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));
-        float2 sv10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));
-        float2 sv11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
+        float2 sv00, sv01, sv10, sv11;
+        if constexpr (U8) {
+          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kVMetaOffU8 + r0 * 4), vmc, sv00, sv01);
+          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kVMetaOffU8 + r1 * 4), vmc, sv10, sv11);
+        } else {
+          const uint2 mv0 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r0 * 8);
+          const uint2 mv1 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r1 * 8);
+          sv00 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.x));
+          sv01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));
+          sv10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));
+          sv11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
+        }
         if (ntok < kP) {                           // rows past the end: no stale metadata
           if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);
           if (r1 >= ntok) sv10 = sv11 = make_float2(0.f, 0.f);
@@ -656,7 +688,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
 // grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
 // MINB resident CTAs per SM (the register budget): 3 for grids of one or two waves (more registers, more
 // independent work per warp), 4 for grids of many waves (more warps to hide latency).
-template <int NT, int MINB>
+template <int NT, int MINB, bool U8>
 __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
   TimelineSpan timeline_span(lv, kTlDecodeMma);
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -678,7 +710,7 @@ __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWo
     __syncthreads();
   }
   pdl_launch_dependents();                         // the merge kernel may be scheduled now; it waits for this grid
-  if (blockIdx.x < fa.nsplit) int2_split<NT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
+  if (blockIdx.x < fa.nsplit) int2_split<NT, U8>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
   else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
   if (trace != nullptr && threadIdx.x == 0) trace[5] = global_ns();
 }
@@ -714,15 +746,25 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2>, lv, ws, fa);
-  else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4>, lv, ws, fa);
-  else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3>, lv, ws, fa);
+  if (lv.meta_u8) {
+    if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2, true>, lv, ws, fa);
+    else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4, true>, lv, ws, fa);
+    else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3, true>, lv, ws, fa);
+  } else {
+    if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2, false>, lv, ws, fa);
+    else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4, false>, lv, ws, fa);
+    else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3, false>, lv, ws, fa);
+  }
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels() {
-  const void* fns[3] = {reinterpret_cast<const void*>(k_decode_mma<1, 3>), reinterpret_cast<const void*>(k_decode_mma<1, 4>),
-                        reinterpret_cast<const void*>(k_decode_mma<2, 2>)};
+  const void* fns[6] = {reinterpret_cast<const void*>(k_decode_mma<1, 3, false>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 4, false>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2, false>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 3, true>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 4, true>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2, true>)};
   for (const void* f : fns) {
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
       return OSCAR_ERR_CUDA;

@@ -200,8 +200,10 @@ __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
 // Expand one packed page block into K (rows = tokens, K-major over the 128 channel positions) and V^T
 // (rows = channels, K-major over the 64 tokens); et = 0 .. kExpThreads - 1 is the expanding thread.
 // Both hold exact codes. K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel
-// 16u + 8 + q (the query fragments use the same order).
-__device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, uint8_t* meta, int et) {
+// 16u + 8 + q (the query fragments use the same order). mc: null for the fp16 metadata, else the compact
+// format's grid constants {T, D, E, 0} per (kind, group) (16 floats).
+__device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, uint8_t* meta, int et,
+                                            const float* __restrict__ mc) {
   for (int wi = et; wi < kP * (kD / 16); wi += kExpThreads) {   // K: token t, channels 16u .. 16u + 15
     const int t = (wi & 7) + 8 * (wi >> 6), u = (wi >> 3) & 7;   // a quarter warp: 8 consecutive tokens
     const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + t * 32 + 4 * u);
@@ -212,9 +214,17 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
   }
   for (int mi = et; mi < 2 * kP; mi += kExpThreads) {  // metadata as float arrays: s0, z0, s1, z1 per token
     const int kind = mi / kP, t = mi % kP;
-    const uint2 mw = *reinterpret_cast<const uint2*>(blk + (kind ? kVMetaOff : kKMetaOff) + 8 * t);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
+    float2 a, b;
+    if (mc == nullptr) {
+      const uint2 mw = *reinterpret_cast<const uint2*>(blk + (kind ? kVMetaOff : kKMetaOff) + 8 * t);
+      a = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
+      b = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
+    } else {
+      const uint32_t mw = *reinterpret_cast<const uint32_t*>(blk + (kind ? kVMetaOffU8 : kKMetaOff) + 4 * t);
+      const float* c = mc + 8 * kind;
+      a = u8_scale_zero(mw & 0xffu, (mw >> 8) & 0xffu, c[0], c[1], c[2]);
+      b = u8_scale_zero((mw >> 16) & 0xffu, mw >> 24, c[4], c[5], c[6]);
+    }
     float* mk = reinterpret_cast<float*>(meta) + kind * 4 * kP + t;
     mk[0] = a.x;
     mk[kP] = a.y;
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       flag(lv.status, OSCAR_STATUS_BAD_PAGE);
       return false;
     }
-    bulk_load_hint(smem_addr(ring + (k % kShStages) * kBlockBytes), int2_block(lv, pid, h), kBlockBytes,
+    bulk_load_hint(smem_addr(ring + (k % kShStages) * kBlockBytes), int2_block(lv, pid, h), lv.blk_bytes,
                    B_(kBarRing + k % kShStages), l2_evict_first());
     return true;
   };
@@ -440,6 +450,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
   } else if (w >= kExpWarp0) {
     // ---- expansion: page i into the K, V^T and metadata buffers i % 3 ---------------------------------
     const int et = tid - 32 * kExpWarp0;
+    const float* mc = lv.meta_u8 ? lv.params + (size_t)h * kParamFloats + kMetaCOff : nullptr;
     for (int i = 0; i < n; ++i) {
       if (__any_sync(0xffffffffu, *failed != 0)) break;
       const int b = i % kBufs;
@@ -453,7 +464,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         break;
       }
       expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes,
-                  smem + kOffMeta + b * kMetaBytes, et);
+                  smem + kOffMeta + b * kMetaBytes, et, mc);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the buffers
       mbar_arrive(B_(kBarExp + b));
     }

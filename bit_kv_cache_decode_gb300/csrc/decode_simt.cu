@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
                                                    int pages_per_split, float scale_log2, int len_add) {
   TimelineSpan timeline_span(lv, kTlInt2Simt);
   __shared__ __align__(16) uint8_t blk[kBlockBytes];
+  __shared__ float2 msz[2][kP][kNG];     // [K, V][token][group] (scale', zero') of the staged page
+  __shared__ float mcs[16];              // compact format: {T, D, E, 0} per (kind, group)
   __shared__ float qs[GQ][kD];
   __shared__ float qg[GQ][kNG];
   __shared__ float pbuf[GQ][kP];
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
   for (int i = tid; i < GQ * kD; i += 128) qs[i / kD][i % kD] = ws.qrot[((size_t)b * lv.hq + hq0) * kD + i];
   if (tid < GQ * kNG) qg[tid / kNG][tid % kNG] = ws.qconst[((size_t)b * lv.hq + hq0 + tid / kNG) * kQConst + kQSum0 + tid % kNG];
   if (tid < GQ) { mrow[tid] = -INFINITY; lrow[tid] = 0.f; }
+  if (tid < 16) mcs[tid] = lv.params[(size_t)h * kParamFloats + kMetaCOff + tid];
   float acc[GQ];
 #pragma unroll
   for (int i = 0; i < GQ; ++i) acc[i] = 0.f;
@@ -112,14 +115,27 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
     const int ntok = min(kP, Lh - page * kP);
     const uint4* src = reinterpret_cast<const uint4*>(int2_block(lv, pid, h));
     uint4* dst = reinterpret_cast<uint4*>(blk);
-    for (int i = tid; i < kBlockBytes / 16; i += 128) dst[i] = src[i];
+    for (int i = tid; i < lv.blk_bytes / 16; i += 128) dst[i] = src[i];
+    __syncthreads();
+    for (int i = tid; i < 2 * kP * kNG; i += 128) {     // metadata of both kinds as float pairs
+      const int kind = i / (kP * kNG), tk = (i / kNG) % kP, g = i % kNG;
+      float2 sz;
+      if (!lv.meta_u8) {
+        const __half* m = reinterpret_cast<const __half*>(blk + (kind ? kVMetaOff : kKMetaOff) + tk * kNG * 4) + 2 * g;
+        sz = make_float2(__half2float(m[0]), __half2float(m[1]));
+      } else {
+        const uint8_t* m = blk + (kind ? kVMetaOffU8 : kKMetaOff) + tk * kNG * 2 + 2 * g;
+        const float* c = mcs + 8 * kind + 4 * g;
+        sz = u8_scale_zero(m[0], m[1], c[0], c[1], c[2]);
+      }
+      msz[kind][tk][g] = sz;
+    }
     __syncthreads();
     for (int item = tid; item < GQ * kP; item += 128) {
       const int tk = item % kP, hh = item / kP;
       float l = -INFINITY;
       if (tk < ntok) {
         const uint32_t* kw = reinterpret_cast<const uint32_t*>(blk + kKCodesOff + tk * (kD / 4));
-        const __half* meta = reinterpret_cast<const __half*>(blk + kKMetaOff + tk * kNG * 4);
         float dot = 0.f;
 #pragma unroll
         for (int g = 0; g < kNG; ++g) {
@@ -130,8 +146,8 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
 #pragma unroll
             for (int i = 0; i < 16; ++i) a = fmaf((float)((word >> (2 * i)) & 3u), qs[hh][g * 64 + w * 16 + i], a);
           }
-          dot = fmaf(__half2float(meta[2 * g]), a, dot);
-          dot = fmaf(__half2float(meta[2 * g + 1]), qg[hh][g], dot);
+          dot = fmaf(msz[0][tk][g].x, a, dot);
+          dot = fmaf(msz[0][tk][g].y, qg[hh][g], dot);
         }
         l = dot * scale_log2;
       }
@@ -148,8 +164,7 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
       for (int tk = 0; tk < ntok; ++tk) {
         const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + (tk >> 1) * 64);
         const float code = (float)((word >> ((tk & 1) * 16 + sh)) & 3u);
-        const __half* vm = reinterpret_cast<const __half*>(blk + kVMetaOff + tk * kNG * 4);
-        const float vhat = fmaf(__half2float(vm[2 * g]), code, __half2float(vm[2 * g + 1]));
+        const float vhat = fmaf(msz[1][tk][g].x, code, msz[1][tk][g].y);
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) acc[hh] = fmaf(pbuf[hh][tk], vhat, acc[hh]);
       }

@@ -143,7 +143,8 @@ __device__ __forceinline__ uint32_t pack16(uint4 b) {
 // time; codes and fp16 metadata of every row go to codes_s [16][128] (one code per byte) and
 // meta_s [16][2] (fp16 scale, zero per group).
 __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotate, const __nv_bfloat16* xs,
-                                              const float* tau_s, uint8_t* codes_s, uint32_t* meta_s) {
+                                              const float* tau_s, const float* mc, uint8_t* codes_s,
+                                              uint32_t* meta_s) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   uint32_t a[8][4];
   if (rotate) {
@@ -211,10 +212,19 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, s));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
       }
-      const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
-      const __half s16 = __float2half_rn(sat_fp16(scale));
-      const __half z16 = __float2half_rn(sat_fp16(mn));
-      const float sq = __half2float(s16), zq = __half2float(z16);
+      float sq, zq;
+      uint32_t meta;
+      if (mc == nullptr) {                          // fp16 (scale, zero)
+        const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+        const __half2 sz = __halves2half2(__float2half_rn(sat_fp16(scale)), __float2half_rn(sat_fp16(mn)));
+        sq = __low2float(sz);
+        zq = __high2float(sz);
+        meta = *reinterpret_cast<const uint32_t*>(&sz);
+      } else {                                      // compact (mn8, mx8)
+        unsigned mn8, mx8;
+        u8_quant_params(mn, mx, mc[4 * G], mc[4 * G + 1], mc[4 * G + 2], mn8, mx8, sq, zq);
+        meta = mn8 | (mx8 << 8);
+      }
       const int row = g + 8 * rr;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -230,17 +240,14 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
         }
         *reinterpret_cast<uint16_t*>(codes_s + row * kD + 8 * (8 * G + j) + 2 * t) = (uint16_t)pair;
       }
-      if (t == 0) {
-        const __half2 sz = __halves2half2(s16, z16);
-        meta_s[row * 2 + G] = *reinterpret_cast<const uint32_t*>(&sz);
-      }
+      if (t == 0) meta_s[row * 2 + G] = meta;
     }
   }
 }
 
 // smem layout of one CTA (bytes): rotation fragments | tau | per warp: 2 staged tiles, codes, metadata
 constexpr int kFragBytes = kRFragWords * 4;                               // 64 KB
-constexpr int kTauBytes = kD * 4;
+constexpr int kTauBytes = kD * 4 + 32;           // tau, then the compact format's 8 grid constants
 constexpr int kXTileBytes = kTileRows * kXStride * 2;                     // 4,352
 constexpr int kWarpBytes = 2 * kXTileBytes + kTileRows * kD + kTileRows * 2 * 4;
 constexpr int kPrefillMmaSmem = kFragBytes + kTauBytes + kPrefillWarps * kWarpBytes + 16;
@@ -269,6 +276,8 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     }
   }
   for (int i = tid; i < kD; i += blockDim.x) tau_s[i] = prm[(kind == OSCAR_KIND_K ? kTauKOff : kTauVOff) + i];
+  if (tid < 8) tau_s[kD + tid] = prm[kMetaCOff + kind * 8 + tid];      // compact-format grid constants
+  const float* mc = lv.meta_u8 ? tau_s + kD : nullptr;
   __syncthreads();
   if (rotate && !__syncthreads_and(mbar_wait(bar, 0))) {
     if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
@@ -305,7 +314,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
       reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(xs + r * kXStride)[lane];
     }
     if (hist_rows != 0) {
-      quantize_tile(frag_s, rotate, xs, tau_s, codes_s, meta_s);
+      quantize_tile(frag_s, rotate, xs, tau_s, mc, codes_s, meta_s);
       __syncwarp();
       // packed codes: 16 rows x 8 words of 16 codes; word idx = lane + 32 j
 #pragma unroll
@@ -328,8 +337,13 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
         const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
         if ((hist_rows >> r) & 1u) {
           uint8_t* blk = int2_block_w(lv, page, h);
-          const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOff) + row * (kNG * 4) + G * 4;
-          *reinterpret_cast<uint32_t*>(blk + off) = meta_s[r * 2 + G];
+          if (mc == nullptr) {
+            const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOff) + row * (kNG * 4) + G * 4;
+            *reinterpret_cast<uint32_t*>(blk + off) = meta_s[r * 2 + G];
+          } else {
+            const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOffU8) + row * (kNG * 2) + G * 2;
+            *reinterpret_cast<uint16_t*>(blk + off) = (uint16_t)meta_s[r * 2 + G];
+          }
         }
       }
     }

@@ -80,9 +80,10 @@ __device__ __forceinline__ float sat_fp16(float x) { return fminf(fmaxf(x, -6550
 // Quantise one rotated row held as y[r] (channel rot_channel(lane, r)) and
 // write its packed byte and group metadata into the page block `blk`, row
 // `row`, half `kind` (OSCAR_KIND_K / OSCAR_KIND_V). tau: float [128] clip
-// thresholds indexed by rotated channel.
+// thresholds indexed by rotated channel. mc: null for the fp16 (scale, zero) metadata, else the
+// kind's compact-format constants {T, D, E, 0} for groups 0 and 1 (8 floats).
 __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const float* __restrict__ tau,
-                                                  uint8_t* blk, int row, int kind) {
+                                                  uint8_t* blk, int row, int kind, const float* __restrict__ mc) {
   const int lane = threadIdx.x & 31;
   float y[4];
 #pragma unroll
@@ -97,10 +98,19 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, s));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
   }
-  const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
-  const __half s16 = __float2half_rn(sat_fp16(scale));
-  const __half z16 = __float2half_rn(sat_fp16(mn));
-  const float sq = __half2float(s16), zq = __half2float(z16);
+  float sq, zq;
+  __half s16, z16;
+  unsigned mn8 = 0, mx8 = 0;
+  if (mc == nullptr) {
+    const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+    s16 = __float2half_rn(sat_fp16(scale));
+    z16 = __float2half_rn(sat_fp16(mn));
+    sq = __half2float(s16);
+    zq = __half2float(z16);
+  } else {
+    const float* c = mc + 4 * (lane & 1);           // lanes of group (lane & 1)
+    u8_quant_params(mn, mx, c[0], c[1], c[2], mn8, mx8, sq, zq);
+  }
   unsigned byte = 0;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -115,9 +125,14 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
   if (kind == OSCAR_KIND_K) blk[kKCodesOff + row * (kD / 4) + b] = (uint8_t)byte;
   else blk[v_byte_off(row, b)] = (uint8_t)byte;
   if (lane < 2) {                                // lane 0: group 0, lane 1: group 1
-    __half2 sz = __halves2half2(s16, z16);
-    const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOff) + row * (kNG * 4) + lane * 4;
-    *reinterpret_cast<__half2*>(blk + off) = sz;
+    if (mc == nullptr) {
+      __half2 sz = __halves2half2(s16, z16);
+      const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOff) + row * (kNG * 4) + lane * 4;
+      *reinterpret_cast<__half2*>(blk + off) = sz;
+    } else {
+      const int off = (kind == OSCAR_KIND_K ? kKMetaOff : kVMetaOffU8) + row * (kNG * 2) + lane * 2;
+      *reinterpret_cast<uint16_t*>(blk + off) = (uint16_t)(mn8 | (mx8 << 8));
+    }
   }
 }
 

@@ -48,7 +48,9 @@
  *                                           hist_pt[h / P], row h % P
  *    Requests may share sink and history pages (prefix caching); recent pages
  *    must be private to one request.
- *  - INT2 page block, one per (page, kv head), 5120 bytes:
+ *  - INT2 page block, one per (page, kv head), 5120 bytes in the default
+ *    OSCAR_META_F16 format (the compact OSCAR_META_U8 format is described with
+ *    its define below):
  *      [0, 2048)    K codes, row t at 32 t: channel j in byte j/4, bits 2(j%4)
  *      [2048, 4096) V codes, rows (2p, 2p+1) at 2048 + 64 p; channel octet o
  *                   (channels 8o..8o+7) is the 32-bit word at +4 o whose low
@@ -105,6 +107,24 @@ extern "C" {
 #define OSCAR_DECODE_SIMT 0  /* CUDA-core INT2 decode                          */
 #define OSCAR_DECODE_MMA  1  /* tensor-core (mma.sync) INT2 decode, default    */
 
+/* INT2 group metadata format (oscar_layout.meta_format). The pages budget the
+ * history at 2.25 bits per element (news article "超越 TurboQuant…", section
+ * "精度表现": rotation baselines at about 2.25 BPE; 2 bits per code plus 16
+ * bits per group of 64) without fixing how the 16 bits are split.
+ *  OSCAR_META_F16: per (row, group) an fp16 scale and an fp16 zero (32 bits:
+ *    2.5 bits per element, 5120-byte page blocks). The default.
+ *  OSCAR_META_U8: per (row, group) two bytes mn8, mx8 (16 bits: 2.25 bits per
+ *    element, 4608-byte page blocks): the clipped group's minimum and maximum
+ *    rounded down / up to a grid of 255 steps over [-T, T], T the group's
+ *    largest clip threshold. With D = fl32(2T / 255) and E = fl32(D / 3),
+ *    zero' = fma(mn8, D, -T) and scale' = (mx8 - mn8) * E (float32); codes are
+ *    round-to-nearest-even((y - zero') / scale') clamped to [0, 3], 0 where
+ *    scale' = 0. Block layout: K codes [0, 2048), V codes [2048, 4096), K
+ *    metadata [4096, 4352) at 4 bytes per row (mn8, mx8 of group 0, then of
+ *    group 1), V metadata [4352, 4608). */
+#define OSCAR_META_F16 0
+#define OSCAR_META_U8  1
+
 typedef struct oscar_layout {
   int num_layers;      /* >= 1                                                */
   int num_kv_heads;    /* Hkv >= 1                                            */
@@ -119,6 +139,7 @@ typedef struct oscar_layout {
   int v_mode;          /* OSCAR_V_ABSORBED or OSCAR_V_EXPLICIT                */
   int max_batch;       /* largest B any call will pass                        */
   int max_splits;      /* largest number of history splits per (request, kv head) */
+  int meta_format;     /* OSCAR_META_F16 (0) or OSCAR_META_U8 (1), see below   */
 } oscar_layout;
 
 typedef struct oscar_cache oscar_cache;

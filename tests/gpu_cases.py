@@ -32,7 +32,8 @@ def upload_params(cache: osc.OscarCache, layer: int, prm: list[P.HeadParams]):
 
 def pool_from_device(cache: osc.OscarCache, layer: int) -> P.PoolModel:
     cfg = cache.cfg
-    pm = P.PoolModel(P.PoolGeometry(hkv=cfg.num_kv_heads), cfg.num_int2_pages, cfg.num_bf16_pages)
+    geo = P.PoolGeometry(hkv=cfg.num_kv_heads, meta_format="u8" if cfg.meta_format == osc.META_U8 else "f16")
+    pm = P.PoolModel(geo, cfg.num_int2_pages, cfg.num_bf16_pages)
     torch.cuda.synchronize()
     pm.int2[:] = cache.int2_pages(layer).cpu().numpy()
     pm.bf16[:] = cache.bf16_pages(layer).cpu().numpy().view(np.uint16).reshape(pm.bf16.shape)
@@ -59,14 +60,16 @@ def to_dev_bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(DEV).to(torch.bfloat16)
 
 
-def compare_int2_pools(got: P.PoolModel, ref: P.PoolModel, rows_written, tol_frac: float = 1e-3):
+def compare_int2_pools(got: P.PoolModel, ref: P.PoolModel, rows_written, tol_frac: float = 1e-3, params=None):
     """Compare history rows written by a GPU path that rotated on the device with
     the oracle's (fp64-rotated) rows.
 
     rows_written: iterable of (page, row). Codes and metadata must agree except
     where float32 rotation rounding moves a value across a rounding boundary: at
     most ``tol_frac`` of the dequantised values may differ, each by at most one
-    quantisation step (plus a 1-ulp change of the fp16 scale/zero).
+    quantisation step (plus a 1-ulp change of the fp16 scale/zero, or one grid step of
+    the compact format's indices). ``params`` (HeadParams per kv head) is needed for
+    the compact format.
     """
     geo = ref.geo
     by_page = {}
@@ -78,8 +81,11 @@ def compare_int2_pools(got: P.PoolModel, ref: P.PoolModel, rows_written, tol_fra
         for h in range(geo.hkv):
             a = got.read_history(page, rows, h)
             b = ref.read_history(page, rows, h)
-            for (ca, sa, za), (cb, sb, zb) in (((a[0], a[1], a[2]), (b[0], b[1], b[2])),
-                                               ((a[3], a[4], a[5]), (b[3], b[4], b[5]))):
+            taus = (params[h].tau_k, params[h].tau_v) if params is not None else (None, None)
+            for kind, (ca, sa, za), (cb, sb, zb) in ((0, (a[0], a[1], a[2]), (b[0], b[1], b[2])),
+                                                     (1, (a[3], a[4], a[5]), (b[3], b[4], b[5]))):
+                sa, za = P.dequant_params(sa, za, taus[kind], geo)
+                sb, zb = P.dequant_params(sb, zb, taus[kind], geo)
                 xa = (za.astype(np.float64).repeat(64, 1) + sa.astype(np.float64).repeat(64, 1) * ca)
                 xb = (zb.astype(np.float64).repeat(64, 1) + sb.astype(np.float64).repeat(64, 1) * cb)
                 step = np.maximum(sa, sb).astype(np.float64).repeat(64, 1)

@@ -23,7 +23,7 @@ TOL = 2e-3
 ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma")]
 
 
-def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64):
+def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64, meta="f16"):
     """Prefill B requests on the GPU. With shared_prefix > 0 all requests share their first
     `shared_prefix` tokens (sink page and the history pages covering them)."""
     B = len(lens)
@@ -49,7 +49,8 @@ def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64):
             bf16_pt[r] = perm_b[ob:ob + 5]
             ob += 5
     cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=n_int2,
-                          num_bf16_pages=n_bf16, max_batch=B, max_splits=max_splits, v_mode=v_mode)
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=max_splits, v_mode=v_mode,
+                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
     cache = osc.OscarCache(cfg, device=DEV)
     cache.set_decode_algo(algo)
     prm = head_params(seed, 0, hkv)
@@ -175,6 +176,33 @@ def test_shared_prefix_steps():
     for r in range(B):
         ref, _ = A.decode_request(qn[r], lens[r] + S, pm, hp[r], bp[r], prm, True, synth.sm_scale())
         assert row_rel_err(got[r], ref).max() <= TOL, r
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("gq", [4, 8])
+def test_compact_metadata_decode(algo, v_mode, gq):
+    # the 16-bit-per-group metadata format: both decoders, both V modes, the one- and two-n-tile variants
+    lens = [1024, 64 + 64 * 13 + 29 + 256, 300]
+    cache, prm, hp, bp = _build(lens, 2, gq, v_mode, seed=18, algo=algo, meta="u8")
+    assert cache.pool.numel() > 0 and cache.int2_pages(0).shape[-1] == 4608
+    _check(cache, prm, hp, bp, lens, gq, v_mode, seed=18)
+
+
+@pytest.mark.parametrize("meta", ["f16", "u8"])
+def test_many_waves_kernel_variant(meta):
+    # 32 requests x 8 kv heads: a grid of more than two waves, where the split policy takes the
+    # 4-CTAs-per-SM build of the tensor-core decode
+    lens = [64 + 64 * 8 + 256 + 17 * r for r in range(32)]
+    cache, prm, hp, bp = _build(lens, 8, 4, 0, seed=19, algo=1, meta=meta)
+    _check(cache, prm, hp, bp, lens, 4, 0, seed=19)
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_compact_metadata_shared_prefix_kernel(v_mode):
+    lens = [64 + 64 * 20 + 300, 64 + 64 * 20 + 700, 64 + 64 * 20 + 256]
+    cache, prm, hp, bp = _build(lens, 2, 4, v_mode, seed=20, shared_prefix=64 + 64 * 20, algo=1, meta="u8")
+    _check(cache, prm, hp, bp, lens, 4, v_mode, seed=20, shared_pages=20)
 
 
 @pytest.mark.parametrize("algo", ALGOS)

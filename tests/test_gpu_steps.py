@@ -19,10 +19,10 @@ from oracle import pool as P
 TOL = 2e-3
 
 
-def _cache(hkv, gq, L_final, v_mode, algo, B=1):
+def _cache(hkv, gq, L_final, v_mode, algo, B=1, meta=0):
     nh = max(1, (L_final - 320 + 63) // 64)
     cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=B * nh,
-                          num_bf16_pages=5 * B, max_batch=B, max_splits=256, v_mode=v_mode)
+                          num_bf16_pages=5 * B, max_batch=B, max_splits=256, v_mode=v_mode, meta_format=meta)
     cache = osc.OscarCache(cfg, device=DEV)
     cache.set_decode_algo(algo)
     hist_pt = np.arange(B * nh, dtype=np.int32).reshape(B, nh)[:, ::-1].copy()
@@ -53,6 +53,36 @@ def test_decode_step_equals_append_then_decode(algo, v_mode):
         assert torch.equal(o1, o2), s
     assert caches[0].get_status() == 0 and caches[1].get_status() == 0
     assert torch.equal(caches[0].pool, caches[1].pool)
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_compact_metadata_8k_then_64_steps(v_mode):
+    # the 16-bit-per-group format through prefill, 64 fused append + demotion + decode steps
+    hkv, gq, L0, steps = 8, 4, 8192, 64
+    cache, hp, bp = _cache(hkv, gq, L0 + steps, v_mode, 1, meta=osc.META_U8)
+    prm = head_params(33, 0, hkv)
+    upload_params(cache, 0, prm)
+    k, v = tokens(33, 0, hkv, L0 + steps)
+    cache.quantize_prefill(0, to_dev_bf16(k[:L0]), to_dev_bf16(v[:L0]), np.array([0, L0], np.int32), hp, bp)
+    hp_d, bp_d = torch.from_numpy(hp).to(DEV), torch.from_numpy(bp).to(DEV)
+    for s in range(1, steps + 1):
+        q = queries(33, 0, hkv, gq, extra=s)
+        lb = torch.tensor([L0 + s - 1], dtype=torch.int32, device=DEV)
+        out = cache.decode_step(0, to_dev_bf16(q), to_dev_bf16(k[L0 + s - 1][None]), to_dev_bf16(v[L0 + s - 1][None]),
+                                lb, hp_d, bp_d, synth.sm_scale(), out_dtype=osc.OUT_FP32)
+        if s in (1, steps):
+            assert cache.get_status() == 0
+            pm = pool_from_device(cache, 0)
+            ref, _ = A.decode_request(q[0], L0 + s, pm, hp[0], bp[0], prm, v_mode == osc.V_ABSORBED,
+                                      synth.sm_scale())
+            err = row_rel_err(out[0].double().cpu().numpy(), ref)
+            assert err.max() <= TOL, (s, err.max())
+    ref_pool = P.PoolModel(P.PoolGeometry(hkv=hkv, meta_format="u8"), cache.cfg.num_int2_pages,
+                           cache.cfg.num_bf16_pages)
+    P.prefill(ref_pool, k, v, hp[0], bp[0], prm, v_mode == osc.V_ABSORBED)
+    got = pool_from_device(cache, 0)
+    assert np.array_equal(got.bf16, ref_pool.bf16)
+    compare_int2_pools(got, ref_pool, [(int(hp[0, h // 64]), h % 64) for h in range(L0 + steps - 320)], params=prm)
 
 
 @pytest.mark.parametrize("algo", [pytest.param(0, id="simt"), pytest.param(1, id="mma")])

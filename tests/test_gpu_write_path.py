@@ -14,15 +14,20 @@ from oracle import pool as P
 from oracle import quant
 
 
-def _cache(hkv, hq, n_int2, n_bf16, v_mode=0, layers=1, max_batch=2):
+META = [pytest.param("f16", id="meta_f16"), pytest.param("u8", id="meta_u8")]
+
+
+def _cache(hkv, hq, n_int2, n_bf16, v_mode=0, layers=1, max_batch=2, meta="f16"):
     cfg = osc.CacheConfig(num_layers=layers, num_kv_heads=hkv, num_q_heads=hq, num_int2_pages=n_int2,
-                          num_bf16_pages=n_bf16, max_batch=max_batch, max_splits=32, v_mode=v_mode)
+                          num_bf16_pages=n_bf16, max_batch=max_batch, max_splits=32, v_mode=v_mode,
+                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
     return osc.OscarCache(cfg, device=DEV)
 
 
-def test_pack_rotated_bit_exact():
+@pytest.mark.parametrize("meta", META)
+def test_pack_rotated_bit_exact(meta):
     hkv, layer = 2, 1
-    cache = _cache(hkv, 8, 5, 1, layers=2)
+    cache = _cache(hkv, 8, 5, 1, layers=2, meta=meta)
     prm = head_params(3, layer, hkv)
     upload_params(cache, layer, prm)
     N = 300
@@ -42,11 +47,12 @@ def test_pack_rotated_bit_exact():
     cache.pack_rotated(layer, osc.KIND_V, torch.from_numpy(xv).to(DEV), pages, rows)
     assert cache.get_status() == 0
     got = pool_from_device(cache, layer)
-    ref = P.PoolModel(P.PoolGeometry(hkv=hkv), 5, 1)
+    ref = P.PoolModel(P.PoolGeometry(hkv=hkv, meta_format=meta), 5, 1)
+    qt = quant.quantize_token if meta == "f16" else quant.quantize_token_u8
     for n in range(N):
         for h in range(hkv):
-            kc, ks, kz = quant.quantize_token(xk[n, h], prm[h].tau_k, 64)
-            vc, vs, vz = quant.quantize_token(xv[n, h], prm[h].tau_v, 64)
+            kc, ks, kz = qt(xk[n, h], prm[h].tau_k, 64)
+            vc, vs, vz = qt(xv[n, h], prm[h].tau_v, 64)
             ref.write_history(int(pages[n]), [int(rows[n])], h, quant.pack_codes(kc), ks, kz, quant.pack_codes(vc), vs, vz)
     assert np.array_equal(got.int2, ref.int2)
     # layer 0 untouched
@@ -71,8 +77,8 @@ def test_rotate_matches_fp64(kind):
         assert np.abs(y[:, h] - ref).max() <= 1e-5 * nrm.max()
 
 
-def _prefill_case(v_mode, lens, hkv=2, seed=5):
-    geo = P.PoolGeometry(hkv=hkv)
+def _prefill_case(v_mode, lens, hkv=2, seed=5, meta="f16"):
+    geo = P.PoolGeometry(hkv=hkv, meta_format=meta)
     B = len(lens)
     nh = [max(0, (L - 320 + 63) // 64) for L in lens]
     mhp = max(1, max(nh))
@@ -85,7 +91,7 @@ def _prefill_case(v_mode, lens, hkv=2, seed=5):
     for r in range(B):
         hist_pt[r, :nh[r]] = perm_i[o:o + nh[r]]
         o += nh[r]
-    cache = _cache(hkv, hkv * 4, n_int2, n_bf16, v_mode=v_mode, max_batch=B)
+    cache = _cache(hkv, hkv * 4, n_int2, n_bf16, v_mode=v_mode, max_batch=B, meta=meta)
     prm = head_params(seed, 0, hkv)
     upload_params(cache, 0, prm)
     ks, vs = zip(*[tokens(seed, 0, hkv, L, extra=r) for r, L in enumerate(lens)])
@@ -101,21 +107,25 @@ def _prefill_case(v_mode, lens, hkv=2, seed=5):
     return cache, ref, rows, prm, (hist_pt, bf16_pt, ks, vs)
 
 
+@pytest.mark.parametrize("meta", META)
 @pytest.mark.parametrize("v_mode", [0, 1])
-def test_prefill_matches_oracle(v_mode):
-    cache, ref, rows, _, _ = _prefill_case(v_mode, [1, 63, 64, 65, 320, 321, 1024, 1400])
+def test_prefill_matches_oracle(v_mode, meta):
+    cache, ref, rows, prm, _ = _prefill_case(v_mode, [1, 63, 64, 65, 320, 321, 1024, 1400], meta=meta)
     got = pool_from_device(cache, 0)
     assert np.array_equal(got.bf16, ref.bf16)
-    compare_int2_pools(got, ref, rows)
+    compare_int2_pools(got, ref, rows, params=prm)
 
 
+@pytest.mark.parametrize("meta", META)
 @pytest.mark.parametrize("v_mode", [0, 1])
-def test_append_demotion_sequence_matches_oracle(v_mode):
+def test_append_demotion_sequence_matches_oracle(v_mode, meta):
     hkv, seed = 2, 6
     L0, steps = 64 + 256 + 40, 150
-    cache, ref, rows, prm, (hist_pt, bf16_pt, ks, vs) = _prefill_case(v_mode, [L0 + steps, 0 + 450], hkv, seed)
+    cache, ref, rows, prm, (hist_pt, bf16_pt, ks, vs) = _prefill_case(v_mode, [L0 + steps, 0 + 450], hkv, seed,
+                                                                      meta=meta)
     # rebuild from scratch by appending: request 0 from L0, request 1 from an empty pool
-    cache2 = _cache(hkv, hkv * 4, cache.cfg.num_int2_pages, cache.cfg.num_bf16_pages, v_mode=v_mode, max_batch=2)
+    cache2 = _cache(hkv, hkv * 4, cache.cfg.num_int2_pages, cache.cfg.num_bf16_pages, v_mode=v_mode, max_batch=2,
+                    meta=meta)
     upload_params(cache2, 0, prm)
     cu = np.array([0, L0], np.int32)
     cache2.quantize_prefill(0, to_dev_bf16(ks[0][:L0]), to_dev_bf16(vs[0][:L0]), cu, hist_pt[:1], bf16_pt[:1])
@@ -133,7 +143,7 @@ def test_append_demotion_sequence_matches_oracle(v_mode):
     got = pool_from_device(cache2, 0)
     # the oracle's prefill of the final lengths equals its token-by-token append (pinned on CPU)
     assert np.array_equal(got.bf16, ref.bf16)
-    compare_int2_pools(got, ref, rows)
+    compare_int2_pools(got, ref, rows, params=prm)
 
 
 def test_bad_page_ids_are_reported_not_faulted():

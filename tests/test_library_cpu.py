@@ -57,11 +57,13 @@ def _bytes(osc, **kw):
     return rc, pb.value, wb.value
 
 
-def test_layout_sizes(osc):
-    rc, pb, wb = _bytes(osc)
+@pytest.mark.parametrize("meta,block", [(0, 5120), (1, 4608)])
+def test_layout_sizes(osc, meta, block):
+    rc, pb, wb = _bytes(osc, meta_format=meta)
     assert rc == 0
-    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V, R_K and R_V fragments per kv head
-    per_layer = (10 * 8 * 5120) + (5 * 8 * 32768) + 8 * (5 * 128 * 128 + 2 * 128) * 4
+    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V, R_K and R_V fragments and
+    # the compact format's 32 grid constants per kv head
+    per_layer = (10 * 8 * block) + (5 * 8 * 32768) + 8 * (5 * 128 * 128 + 2 * 128 + 32) * 4
     assert pb >= 2 * per_layer and pb < 2 * per_layer + 2 * 3 * 256
     parts = 2 * 32 * (16 + 5) * 132 * 4          # history splits + 5 BF16 chunks per (request, q head)
     assert wb >= parts
@@ -70,7 +72,7 @@ def test_layout_sizes(osc):
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=64), -2), (dict(group=32), -2), (dict(page_size=32), -2),
     (dict(num_q_heads=24), -2), (dict(num_q_heads=30), -1), (dict(sink=65), -1), (dict(recent=0), -1),
-    (dict(max_batch=0), -1), (dict(v_mode=7), -1), (dict(num_layers=0), -1),
+    (dict(max_batch=0), -1), (dict(v_mode=7), -1), (dict(num_layers=0), -1), (dict(meta_format=2), -1),
 ])
 def test_layout_validation(osc, kw, code):
     rc, _, _ = _bytes(osc, **kw)

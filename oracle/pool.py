@@ -47,7 +47,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from . import quant
+from . import codebook, quant
 
 
 @dataclass(frozen=True)
@@ -58,11 +58,13 @@ class PoolGeometry:
     page: int = 64
     sink: int = 64
     recent: int = 256
-    meta_format: str = "f16"     # "f16": fp16 (scale, zero); "u8": 8-bit (mn8, mx8) on [-T, T]
+    # "f16": fp16 (scale, zero); "u8": 8-bit (mn8, mx8) on [-T, T]; "cb": fp16 (range, zero) with a
+    # Lloyd-Max codebook per (kv head, kind) (see ``codebook``)
+    meta_format: str = "f16"
 
     @property
     def meta_per_group(self) -> int:   # metadata bytes per group of one row
-        return {"f16": 4, "u8": 2}[self.meta_format]
+        return {"f16": 4, "u8": 2, "cb": 4}[self.meta_format]
 
     @property
     def codes_bytes(self) -> int:      # K (or V) codes per page block
@@ -123,7 +125,7 @@ class PoolModel:
         return base + rows[:, None] * per + np.arange(per)[None, :]
 
     def _meta_dtype(self):
-        return np.float16 if self.geo.meta_format == "f16" else np.uint8
+        return np.uint8 if self.geo.meta_format == "u8" else np.float16
 
     def _meta_bytes(self, a, b) -> np.ndarray:
         """Interleave the two stored metadata fields of each group: (scale, zero) or (mn8, mx8)."""
@@ -183,6 +185,8 @@ class HeadParams:
     u_v: np.ndarray      # [d, d] float32 (ignored when V is absorbed)
     tau_k: np.ndarray    # [d] float32, rotated basis
     tau_v: np.ndarray    # [d] float32
+    cb_k: np.ndarray | None = None   # codebook bytes [4] (the "cb" metadata format)
+    cb_v: np.ndarray | None = None
 
 
 def rotated_f32(x: np.ndarray, u32: np.ndarray) -> np.ndarray:
@@ -201,17 +205,30 @@ def quantize_history_tokens(k_f32, v_f32, prm: HeadParams, v_absorbed: bool, gro
     Returns (k_pack, k_a, k_b, v_pack, v_a, v_b), (a, b) the stored metadata of the format."""
     kr = rotated_f32(k_f32, prm.u_k)
     vr = np.asarray(v_f32, dtype=np.float32) if v_absorbed else rotated_f32(v_f32, prm.u_v)
-    qt = quant.quantize_token if meta_format == "f16" else quant.quantize_token_u8
-    kc, ks, kz = qt(kr, prm.tau_k, group)
-    vc, vs, vz = qt(vr, prm.tau_v, group)
+    if meta_format == "cb":
+        kc, ks, kz = codebook.quantize_token(kr, prm.tau_k, prm.cb_k, group)
+        vc, vs, vz = codebook.quantize_token(vr, prm.tau_v, prm.cb_v, group)
+    else:
+        qt = quant.quantize_token if meta_format == "f16" else quant.quantize_token_u8
+        kc, ks, kz = qt(kr, prm.tau_k, group)
+        vc, vs, vz = qt(vr, prm.tau_v, group)
     return quant.pack_codes(kc), ks, kz, quant.pack_codes(vc), vs, vz
 
 
 def dequant_params(a, b, tau, geo: PoolGeometry):
-    """Float (scale, zero) per group from the stored metadata (a, b) of the pool's format."""
+    """Float (scale, zero) per group from the stored metadata (a, b) of the "f16" or "u8" format."""
     if geo.meta_format == "f16":
         return np.asarray(a, dtype=np.float16), np.asarray(b, dtype=np.float16)
+    assert geo.meta_format == "u8"
     return quant.u8_scale_zero(a, b, quant.group_bounds(tau, geo.group))
+
+
+def dequant_rows(codes, a, b, prm, kind: int, geo: PoolGeometry) -> np.ndarray:
+    """Dequantised fp64 rows [n, d] of one kind (0 K, 1 V) from codes and stored metadata."""
+    if geo.meta_format == "cb":
+        return codebook.dequantize(codes, a, b, prm.cb_k if kind == 0 else prm.cb_v, geo.group)
+    tau = None if prm is None else (prm.tau_k if kind == 0 else prm.tau_v)
+    return quant.dequantize_sz(codes, *dequant_params(a, b, tau, geo), geo.group)
 
 
 def bf16_location(pos: int, seg: str, bf16_pt, geo: PoolGeometry):
@@ -293,7 +310,7 @@ def gather_request(pool: PoolModel, seq_len: int, hist_pt, bf16_pt, heads=None, 
     geo = pool.geo
     heads = list(range(geo.hkv)) if heads is None else list(heads)
     if geo.meta_format != "f16" and params is None:
-        raise ValueError("the compact metadata format needs the heads' clip thresholds")
+        raise ValueError("the compact and codebook metadata formats need the heads' parameters")
     L = seq_len
     kk = np.zeros((L, len(heads), geo.d))
     vv = np.zeros((L, len(heads), geo.d))
@@ -303,10 +320,9 @@ def gather_request(pool: PoolModel, seq_len: int, hist_pt, bf16_pt, heads=None, 
         for i in range((lh + geo.page - 1) // geo.page):
             a, b = i * geo.page, min((i + 1) * geo.page, lh)
             kc, ka, kb, vc, va, vb = pool.read_history(int(hist_pt[i]), np.arange(b - a), hd)
-            tk = params[hd].tau_k if params is not None else None
-            tv = params[hd].tau_v if params is not None else None
-            kk[geo.sink + a: geo.sink + b, j] = quant.dequantize_sz(kc, *dequant_params(ka, kb, tk, geo), geo.group)
-            vv[geo.sink + a: geo.sink + b, j] = quant.dequantize_sz(vc, *dequant_params(va, vb, tv, geo), geo.group)
+            prm = params[hd] if params is not None else None
+            kk[geo.sink + a: geo.sink + b, j] = dequant_rows(kc, ka, kb, prm, 0, geo)
+            vv[geo.sink + a: geo.sink + b, j] = dequant_rows(vc, va, vb, prm, 1, geo)
         for pos in range(L):
             if seg[pos] != "history":
                 page, row = bf16_location(pos, seg[pos], bf16_pt, geo)

@@ -41,9 +41,12 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV tokens/s and achieved HBM GB/s vs GB300 peak, 100K ctx"
 UNIT = "KV tokens/s"
 HIST_BYTES = 80          # per history token per kv head: 32 B K codes + 32 B V codes + 16 B fp16 scale/zero
-HIST_BYTES_BY_META = {"f16": 80, "u8": 72}     # the compact format stores 8 B of (mn8, mx8) per token
+HIST_BYTES_BY_META = {"f16": 80, "u8": 72, "cb": 80}   # the compact format stores 8 B of (mn8, mx8) per token
 STORAGE = {"f16": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recent",
-           "u8": "int2 history (8-bit min/max grid indices per 64-group, 2.25 bits per element) + bf16 sink/recent"}
+           "u8": "int2 history (8-bit min/max grid indices per 64-group, 2.25 bits per element) + bf16 sink/recent",
+           "cb": "int2 history (Lloyd-Max 4-level codebook per kv head, fp16 range/zero per 64-group) + bf16 "
+                 "sink/recent"}
+META_FORMATS = {"f16": 0, "u8": 1, "cb": 2}
 BF16_BYTES = 512         # per BF16 token per kv head: K and V, 128 x 2 B each
 
 WORKLOADS = {
@@ -160,7 +163,7 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
             bf16_pt[r] = 5 * r + np.arange(5)
     cfg = osc.CacheConfig(num_layers=nl, num_kv_heads=H, num_q_heads=hq, num_int2_pages=n_int2,
                           num_bf16_pages=n_bf16, max_batch=B, max_splits=512, v_mode=osc.V_ABSORBED,
-                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
+                          meta_format=META_FORMATS[meta])
     cache = osc.OscarCache(cfg, device=device)
     cache.set_decode_algo(algo)
     # offline calibration on the host (library routine), one per (layer, kv head)
@@ -169,7 +172,10 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
     def cal(lh):
         layer, h = lh
         qc, kc, vc = synth.calibration(seed, layer, h)
-        return osc.calibrate(qc, kc, vc, sm)
+        c = osc.calibrate(qc, kc, vc, sm)
+        if meta == "cb":
+            c["kc"], c["vc"] = kc, vc
+        return c
 
     with ThreadPoolExecutor(max_workers=os.cpu_count() or 8) as ex:
         cals = list(ex.map(cal, [(l, h) for l in range(nl) for h in range(H)]))
@@ -191,6 +197,15 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
         cs = cals[layer * H:(layer + 1) * H]
         cache.set_rotation(layer, np.stack([c["U_K"] for c in cs]), np.stack([c["U_V"] for c in cs]),
                            np.stack([c["tau_K"] for c in cs]), np.stack([c["tau_V"] for c in cs]))
+        if meta == "cb":
+            # Lloyd-Max codebooks from the calibration rows: keys rotated by the library, V as stored
+            # (V-absorbed layout)
+            kcal = torch.from_numpy(np.stack([c["kc"] for c in cs], axis=1)).to(device).to(torch.bfloat16)
+            krot = cache.rotate(layer, osc.KIND_K, kcal).cpu().numpy()
+            for h in range(H):
+                cs[h]["cb_k"] = osc.calibrate_codebook(krot[:, h], cs[h]["tau_K"])
+                cs[h]["cb_v"] = osc.calibrate_codebook(cs[h]["vc"], cs[h]["tau_V"])
+            cache.set_codebook(layer, np.stack([c["cb_k"] for c in cs]), np.stack([c["cb_v"] for c in cs]))
         outl = np.stack([synth.head_stats(seed, layer, h).outliers for h in range(H)])
         gen.manual_seed(seed * 1000003 + layer)
         if mixed:
@@ -552,11 +567,12 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
     torch.cuda.synchronize()
     cfg = wl["cfg"]
     import bit_kv_cache_decode_gb300 as osc
-    geo = P.PoolGeometry(hkv=H, meta_format="u8" if cfg.meta_format == osc.META_U8 else "f16")
+    geo = P.PoolGeometry(hkv=H, meta_format={v: k for k, v in META_FORMATS.items()}[cfg.meta_format])
     pm = P.PoolModel(geo, cfg.num_int2_pages, cfg.num_bf16_pages)
     pm.int2[:] = cache.int2_pages(0).cpu().numpy()
     pm.bf16[:] = cache.bf16_pages(0).cpu().numpy().view(np.uint16).reshape(pm.bf16.shape)
-    prm = [P.HeadParams(c["U_K"], c["U_V"], c["tau_K"], c["tau_V"]) for c in wl["cals"][:H]]
+    prm = [P.HeadParams(c["U_K"], c["U_V"], c["tau_K"], c["tau_V"], c.get("cb_k"), c.get("cb_v"))
+           for c in wl["cals"][:H]]
     q = np.random.default_rng(seed).standard_normal((hq, 128)).astype(np.float32)
     Lnow = int(L)
     t0 = time.perf_counter()
@@ -594,6 +610,10 @@ def run_reference(args, rank, world):
     cal = rotation.calibrate(qc, kc, vc, synth.sm_scale())
     prm = [P.HeadParams(cal["U_K"].astype(np.float32), cal["U_V"].astype(np.float32),
                         cal["tau_K"].astype(np.float32), cal["tau_V"].astype(np.float32))]
+    if args.meta_format == "cb":
+        from oracle import codebook as CB
+        prm[0].cb_k = CB.calibrate_codebook(P.rotated_f32(kc, prm[0].u_k), prm[0].tau_k)
+        prm[0].cb_v = CB.calibrate_codebook(vc.astype(np.float32), prm[0].tau_v)
     k, v = synth.kv_tokens(seed, 0, 0, L)
     P.prefill(pm, k[:, None], v[:, None], np.arange(nh), np.arange(5), prm, True)
     q = synth.queries(seed, 0, 0, hq // H)
@@ -654,8 +674,9 @@ def main():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
-    ap.add_argument("--meta-format", choices=["f16", "u8"], default="f16",
-                    help="INT2 group metadata: fp16 scale/zero (default) or the compact 16-bit format")
+    ap.add_argument("--meta-format", choices=["f16", "u8", "cb"], default="f16",
+                    help="INT2 group metadata: fp16 scale/zero (default), the compact 16-bit format, or the "
+                         "Lloyd-Max codebook format")
     args = ap.parse_args()
     global HIST_BYTES
     HIST_BYTES = HIST_BYTES_BY_META[args.meta_format]

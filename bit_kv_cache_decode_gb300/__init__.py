@@ -27,7 +27,7 @@ V_ABSORBED, V_EXPLICIT = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 KIND_K, KIND_V = 0, 1
 DECODE_SIMT, DECODE_MMA = 0, 1
-META_F16, META_U8 = 0, 1
+META_F16, META_U8, META_CB = 0, 1, 2
 
 # every symbol include/oscar.h declares
 EXPORTS = (
@@ -37,7 +37,7 @@ EXPORTS = (
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
     "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
     "oscar_decode_attention_shared", "oscar_decode_step_shared",
-    "oscar_trace_timeline", "oscar_check_wait_timeout",
+    "oscar_trace_timeline", "oscar_check_wait_timeout", "oscar_set_codebook", "oscar_calibrate_codebook",
 )
 
 
@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
         "oscar_cache_destroy": [vp],
         "oscar_layer_offsets": [vp, c_int, sz, sz, sz],
         "oscar_set_rotation": [vp, c_int, vp, vp, vp, vp, vp],
+        "oscar_set_codebook": [vp, c_int, vp, vp, vp],
+        "oscar_calibrate_codebook": [vp, c_int, vp, vp],
         "oscar_quantize_prefill": [vp, c_int, c_int, vp, vp, i32p, c_int, i32p, c_int, i32p, vp],
         "oscar_append_kv": [vp, c_int, c_int, vp, vp, i32p, i32p, c_int, i32p, vp],
         "oscar_decode_attention": [vp, c_int, c_int, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
@@ -147,7 +149,8 @@ class CacheConfig:
     page_size: int = 64
     sink: int = 64
     recent: int = 256
-    meta_format: int = META_F16        # META_U8: 16-bit (mn8, mx8) group metadata, 4608-byte INT2 blocks
+    meta_format: int = META_F16        # META_U8: 16-bit (mn8, mx8) group metadata, 4608-byte INT2 blocks;
+    #                                    META_CB: Lloyd-Max codebook levels with fp16 (range, zero) metadata
 
     def layout(self) -> Layout:
         return Layout(self.num_layers, self.num_kv_heads, self.num_q_heads, self.head_dim, self.group,
@@ -220,6 +223,12 @@ class OscarCache:
         uk, uv, tk, tv = f32(U_K), f32(U_V), f32(tau_K), f32(tau_V)
         _check(_lib.oscar_set_rotation(self._h, layer, _ptr(uk), _ptr(uv), _ptr(tk), _ptr(tv), _stream(stream)),
                "oscar_set_rotation")
+
+    def set_codebook(self, layer: int, cb_K, cb_V, stream=None):
+        """Codebook bytes uint8 [Hkv][4] of K and V (META_CB layouts); call after set_rotation."""
+        ck = np.ascontiguousarray(cb_K, dtype=np.uint8)
+        cv = np.ascontiguousarray(cb_V, dtype=np.uint8)
+        _check(_lib.oscar_set_codebook(self._h, layer, _ptr(ck), _ptr(cv), _stream(stream)), "oscar_set_codebook")
 
     def quantize_prefill(self, layer: int, k, v, cu_seqlens, hist_pt, bf16_pt, total_tokens: int | None = None,
                          stream=None):
@@ -355,6 +364,16 @@ def bf16_decode(kv_pages, q, seq_lens, page_table, sm_scale: float, num_kv_heads
                                   _ptr(pt), int(pt.shape[1]), float(sm_scale), _ptr(out), out_dtype, _ptr(lse),
                                   _ptr(workspace), workspace.numel() * workspace.element_size(), max_splits,
                                   _stream(stream)), "oscar_bf16_decode")
+    return out
+
+
+def calibrate_codebook(x_rot, tau) -> np.ndarray:
+    """Host Lloyd-Max calibration of one codebook from rotated float32 rows x_rot [N, 128] and clip
+    thresholds tau [128]: returns the codebook bytes uint8 [4]."""
+    x = np.ascontiguousarray(x_rot, dtype=np.float32)
+    t = np.ascontiguousarray(tau, dtype=np.float32)
+    out = np.zeros(4, np.uint8)
+    _check(_lib.oscar_calibrate_codebook(_ptr(x), x.shape[0], _ptr(t), _ptr(out)), "oscar_calibrate_codebook")
     return out
 
 

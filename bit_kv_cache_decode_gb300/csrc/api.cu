@@ -45,7 +45,8 @@ int check_layout(const oscar_layout* L) {
   if (L->page_size < 1 || L->sink % L->page_size != 0 || L->recent % L->page_size != 0) return OSCAR_ERR_INVALID_ARG;
   if (L->group < 1 || L->head_dim % L->group != 0) return OSCAR_ERR_INVALID_ARG;
   if (L->v_mode != OSCAR_V_ABSORBED && L->v_mode != OSCAR_V_EXPLICIT) return OSCAR_ERR_INVALID_ARG;
-  if (L->meta_format != OSCAR_META_F16 && L->meta_format != OSCAR_META_U8) return OSCAR_ERR_INVALID_ARG;
+  if (L->meta_format != OSCAR_META_F16 && L->meta_format != OSCAR_META_U8 && L->meta_format != OSCAR_META_CB)
+    return OSCAR_ERR_INVALID_ARG;
   if (L->head_dim != kD || L->group != kG || L->page_size != kP) return OSCAR_ERR_UNSUPPORTED;
   if (!is_pow2_le8(L->num_q_heads / L->num_kv_heads)) return OSCAR_ERR_UNSUPPORTED;
   if (L->max_splits > 4096) return OSCAR_ERR_UNSUPPORTED;
@@ -85,6 +86,7 @@ LayerView view(const oscar_cache* c, int layer) {
   v.recent = c->lay.recent;
   v.v_explicit = c->lay.v_mode == OSCAR_V_EXPLICIT;
   v.meta_u8 = c->lay.meta_format == OSCAR_META_U8;
+  v.meta_cb = c->lay.meta_format == OSCAR_META_CB;
   v.blk_bytes = v.meta_u8 ? kBlockBytesU8 : kBlockBytes;
   v.status = c->status;
   v.layer = layer;
@@ -210,6 +212,14 @@ void choose_splits_mma(int B, int hkv, int gq, int nbf, int max_pages, int max_s
   *pps = (max_pages + n - 1) / n;
 }
 
+// Codebook levels and decision thresholds as the kernels read them: k_i as floats, then
+// theta_i = fl32((k_i + k_{i+1}) / 510).
+void codebook_consts(const uint8_t* k, float* out) {
+  for (int i = 0; i < 4; ++i) out[i] = (float)k[i];
+  for (int i = 0; i < 3; ++i) out[4 + i] = (float)(k[i] + k[i + 1]) / 510.0f;
+  out[7] = 0.f;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,6 +313,28 @@ int oscar_layer_offsets(const oscar_cache* c, int layer, size_t* int2_off, size_
   return OSCAR_OK;
 }
 
+int oscar_set_codebook(oscar_cache* c, int layer, const uint8_t* cb_K, const uint8_t* cb_V, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || !cb_K || !cb_V) return OSCAR_ERR_INVALID_ARG;
+  if (c->lay.meta_format != OSCAR_META_CB) return OSCAR_ERR_UNSUPPORTED;
+  const int hkv = c->lay.num_kv_heads;
+  for (int h = 0; h < hkv; ++h)
+    for (int i = 0; i < 3; ++i)
+      if (cb_K[4 * h + i] > cb_K[4 * h + i + 1] || cb_V[4 * h + i] > cb_V[4 * h + i + 1]) return OSCAR_ERR_INVALID_ARG;
+  LayerView v = view(c, layer);
+  std::vector<float> host((size_t)hkv * 16, 0.f);
+  for (int h = 0; h < hkv; ++h) {
+    codebook_consts(cb_K + 4 * h, host.data() + 16 * h);
+    codebook_consts(cb_V + 4 * h, host.data() + 16 * h + 8);
+  }
+  for (int h = 0; h < hkv; ++h) {
+    float* dst = const_cast<float*>(v.params) + (size_t)h * kParamFloats + kCbOff;
+    if (cudaMemcpyAsync(dst, host.data() + 16 * h, 16 * sizeof(float), cudaMemcpyHostToDevice,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return OSCAR_ERR_CUDA;
+  }
+  return OSCAR_OK;
+}
+
 int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float* U_V, const float* tau_K,
                        const float* tau_V, void* stream) {
   if (!c || layer < 0 || layer >= c->lay.num_layers || !U_K || !tau_K || !tau_V) return OSCAR_ERR_INVALID_ARG;
@@ -352,6 +384,9 @@ int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float*
         mc[2] = E;
         mc[3] = 0.f;
       }
+    static const uint8_t kUniform[4] = {0, 85, 170, 255};
+    codebook_consts(kUniform, dst + kCbOff);
+    codebook_consts(kUniform, dst + kCbOff + 8);
   }
   LayerView v = view(c, layer);
   cudaError_t e = cudaMemcpyAsync(const_cast<float*>(v.params), host.data(), host.size() * sizeof(float),
@@ -664,6 +699,7 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
   out->recent = L->recent;
   out->v_explicit = L->v_mode == OSCAR_V_EXPLICIT;
   out->meta_u8 = L->meta_format == OSCAR_META_U8;
+  out->meta_cb = L->meta_format == OSCAR_META_CB;
   out->blk_bytes = out->meta_u8 ? kBlockBytesU8 : kBlockBytes;
   out->status = status;
   out->layer = layer;

@@ -173,3 +173,51 @@ extern "C" int oscar_calibrate(const float* Q, const float* K, const float* V, i
   thresholds(V, N, uv, c_V, tau_V);
   return OSCAR_OK;
 }
+
+// Lloyd-Max codebook of one (layer, kv head, kind) (news article "超越 TurboQuant…", section "总结与展望":
+// a Lloyd-Max codebook inside the attention-aware rotation). Lloyd's iteration on the pooled normalised
+// group values u = (y - min) / (max - min) of the clipped calibration rows; cell i holds the u in
+// (t_{i-1}, t_i], t the midpoints between neighbouring levels, and each level moves to its cell's mean.
+extern "C" int oscar_calibrate_codebook(const float* x_rot, int N, const float* tau, uint8_t* cb) {
+  if (!x_rot || !tau || !cb || N < 1) return OSCAR_ERR_INVALID_ARG;
+  constexpr int G = 64;
+  std::vector<double> u;
+  u.reserve((size_t)N * D);
+  float y[G];
+  for (int n = 0; n < N; ++n)
+    for (int g = 0; g < D / G; ++g) {
+      float mn = INFINITY, mx = -INFINITY;
+      for (int j = 0; j < G; ++j) {
+        const float t = tau[g * G + j];
+        y[j] = std::min(std::max(x_rot[(size_t)n * D + g * G + j], -t), t);
+        mn = std::min(mn, y[j]);
+        mx = std::max(mx, y[j]);
+      }
+      if (!(mx > mn)) continue;
+      const double range = (double)mx - (double)mn;
+      for (int j = 0; j < G; ++j) u.push_back(((double)y[j] - (double)mn) / range);
+    }
+  std::sort(u.begin(), u.end());
+  std::vector<double> csum(u.size() + 1, 0.0);
+  for (size_t i = 0; i < u.size(); ++i) csum[i + 1] = csum[i] + u[i];
+  double c[4] = {0.0, 1.0 / 3.0, 2.0 / 3.0, 1.0};
+  for (int it = 0; it < 1000; ++it) {
+    size_t edge[5];
+    edge[0] = 0;
+    edge[4] = u.size();
+    for (int i = 0; i < 3; ++i)
+      edge[i + 1] = (size_t)(std::upper_bound(u.begin(), u.end(), 0.5 * (c[i] + c[i + 1])) - u.begin());
+    double nc[4], moved = 0.0;
+    for (int i = 0; i < 4; ++i) {
+      nc[i] = edge[i + 1] > edge[i] ? (csum[edge[i + 1]] - csum[edge[i]]) / (double)(edge[i + 1] - edge[i]) : c[i];
+      moved = std::max(moved, std::fabs(nc[i] - c[i]));
+    }
+    std::copy(nc, nc + 4, c);
+    if (moved <= 1e-12) break;
+  }
+  int k[4];
+  for (int i = 0; i < 4; ++i) k[i] = (int)std::min(std::max(std::rint(255.0 * c[i]), 0.0), 255.0);
+  std::sort(k, k + 4);
+  for (int i = 0; i < 4; ++i) cb[i] = (uint8_t)k[i];
+  return OSCAR_OK;
+}

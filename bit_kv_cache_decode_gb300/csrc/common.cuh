@@ -33,6 +33,8 @@ constexpr int kBlockBytes = 2 * kCodeBytes + 2 * kMetaBytes;   // 5120
 constexpr int kMetaBytesU8 = kP * kNG * 2;                       // 256
 constexpr int kVMetaOffU8 = 2 * kCodeBytes + kMetaBytesU8;       // 4352
 constexpr int kBlockBytesU8 = 2 * kCodeBytes + 2 * kMetaBytesU8; // 4608
+// metadata formats as kernel template arguments (OSCAR_META_F16 / _U8 / _CB)
+constexpr int kFmtF16 = 0, kFmtU8 = 1, kFmtCB = 2;
 constexpr int kBf16BlockBytes = 2 * kP * kD * 2;               // 32768: K [P][D] then V [P][D]
 // rotation parameters per kv head (float32 words): U_K [D][D], U_V [D][D], U_V transposed [D][D]
 // (for coalesced reads of R_V^T in the merge), tau_K [D], tau_V [D], then the composite
@@ -43,8 +45,9 @@ constexpr int kRFragWords = 8 * 16 * 32 * 4;  // [k-block 8][n-tile 16][lane 32]
 constexpr int kUKOff = 0, kUVOff = kD * kD, kUVtOff = 2 * kD * kD, kTauKOff = 3 * kD * kD,
               kTauVOff = 3 * kD * kD + kD, kRKFragOff = 3 * kD * kD + 2 * kD, kRVFragOff = kRKFragOff + kRFragWords;
 // then, per kind and group, the compact format's grid constants {T, D = fl32(2T / 255), E = fl32(D / 3),
-// 0} (kMetaCFloats words, padded so that a head's parameters stay 128-byte aligned)
-constexpr int kMetaCOff = kRVFragOff + kRFragWords, kMetaCFloats = 32;
+// 0}, and per kind the codebook {k_0, k_1, k_2, k_3, theta_0, theta_1, theta_2, 0} as floats
+// (kMetaCFloats words, padded so that a head's parameters stay 128-byte aligned)
+constexpr int kMetaCOff = kRVFragOff + kRFragWords, kCbOff = kMetaCOff + 16, kMetaCFloats = 32;
 constexpr int kParamFloats = kMetaCOff + kMetaCFloats;
 // one split partial: m (log2 units), l, then acc[D]; padded to 132 floats (528 B, 16 B aligned)
 constexpr int kPartFloats = kD + 4;
@@ -58,6 +61,7 @@ struct LayerView {
   const float* next_params;   // the next layer's parameters (prefetched into L2 by the prologue), or null
   int n_int2, n_bf16, hkv, hq, sink, recent, v_explicit;
   int meta_u8;            // OSCAR_META_U8 pool: 8-bit (mn8, mx8) metadata, 4608-byte INT2 blocks
+  int meta_cb;            // OSCAR_META_CB pool: codebook levels, fp16 (range, zero) metadata
   int blk_bytes;          // INT2 block bytes: kBlockBytes or kBlockBytesU8
   int* status;            // device status word
   int layer;              // layer index (timeline records only)
@@ -76,6 +80,15 @@ __device__ __forceinline__ uint8_t* int2_block_w(const LayerView& lv, int page, 
 // Grid constants {T, D, E, 0} of (kv head h, kind, group G) of the compact format.
 __device__ __forceinline__ const float* meta_consts(const LayerView& lv, int h, int kind) {
   return lv.params + (size_t)h * kParamFloats + kMetaCOff + kind * 8;
+}
+
+// Codebook constants {k_0..k_3, theta_0..theta_2, 0} of (kv head h, kind).
+__device__ __forceinline__ const float* cb_consts(const LayerView& lv, int h, int kind) {
+  return lv.params + (size_t)h * kParamFloats + kCbOff + kind * 8;
+}
+// Codebook format, write side: the code of t = (y - zero') / range' (0 .. 3, ties to the lower level).
+__device__ __forceinline__ float cb_code(float t, const float* cb) {
+  return (float)((t > cb[4]) + (t > cb[5]) + (t > cb[6]));
 }
 
 // Compact format, write side: the group's grid indices from its clipped min / max, and the

@@ -127,9 +127,17 @@ __device__ __forceinline__ void u8_row_meta(uint32_t m, const float (&c)[6], flo
   g1 = u8_scale_zero((m >> 16) & 0xffu, m >> 24, c[3], c[4], c[5]);
 }
 
-// History split `split` of group (b, h): see the file comment. U8: the pool holds the compact
-// (mn8, mx8) metadata (4608-byte blocks, staged in the same 5120-byte slots).
-template <int NT, bool U8>
+// Codebook format: the fp16 value 1024 + k_c of code c from the codebook bytes `lut` (k_0 .. k_3):
+// one byte permute per register. sel holds two codes in its bits 0-1 and 8-9 (results in the low and
+// the high half); the other selector nibbles pick the constant byte 0x64, fp16 1024's high byte.
+__device__ __forceinline__ uint32_t cb_lookup(uint32_t lut, uint32_t sel) {
+  return __byte_perm(lut, 0x64646464u, (sel & 0x0303u) | 0x4040u);
+}
+
+// History split `split` of group (b, h): see the file comment. FMT: the pool's metadata format,
+// kFmtF16, kFmtU8 (compact (mn8, mx8) metadata, 4608-byte blocks staged in the same 5120-byte slots) or
+// kFmtCB (codebook levels k_c instead of the codes, fp16 range / 255 as the scale).
+template <int NT, int FMT>
 __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWorkspace& ws, const FusedArgs& fa,
                                            uint8_t* smem, int split, int h, int b, unsigned long long* trace) {
   const int* __restrict__ seq_lens = fa.seq_lens;
@@ -139,6 +147,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gq = lv.hq / lv.hkv;
+  constexpr bool U8 = FMT == kFmtU8, CB = FMT == kFmtCB;
   if (tid == 0) any_timeout = 0;
   __syncthreads();
 
@@ -201,6 +210,16 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
 
   // ---- per-lane constants -------------------------------------------------------
   float kmc[6], vmc[6];                // compact format: {T, D, E} of groups 0, 1 for K and for V
+  uint32_t klut = 0, vlut = 0;         // codebook format: the bytes k_0 .. k_3 of K and of V
+  if constexpr (CB) {
+    const float* ck = cb_consts(lv, h, OSCAR_KIND_K);
+    const float* cv = cb_consts(lv, h, OSCAR_KIND_V);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      klut |= (uint32_t)ck[i] << (8 * i);
+      vlut |= (uint32_t)cv[i] << (8 * i);
+    }
+  }
   if constexpr (U8) {
     const float* mk = meta_consts(lv, h, OSCAR_KIND_K);
     const float* mv = meta_consts(lv, h, OSCAR_KIND_V);
@@ -301,10 +320,20 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           const uint32_t wy[4] = {ky[G] << 6, ky[G] << 2, ky[G] >> 2, ky[G] >> 6};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint32_t a0 = and_or(wx[j], 0x00C000C0u, kMagic);   // row r0, codes 2j (k rows 2t, 2t+1)
-            const uint32_t a1 = and_or(wy[j], 0x00C000C0u, kMagic);   // row r1
-            const uint32_t a2 = and_or(wx[j], 0x03000300u, kMagic);   // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
-            const uint32_t a3 = and_or(wy[j], 0x03000300u, kMagic);   // row r1
+            uint32_t a0, a1, a2, a3;
+            if constexpr (CB) {
+              // k rows (2t, 2t+1): channels (16t + j, 16t + 4 + j) of the word (bytes 0, 1 at bits 2j);
+              // (2t+8, 2t+9): channels (16t + 8 + j, 16t + 12 + j) (bytes 2, 3)
+              a0 = cb_lookup(klut, kx[G] >> (2 * j));
+              a1 = cb_lookup(klut, ky[G] >> (2 * j));
+              a2 = cb_lookup(klut, kx[G] >> (2 * j + 16));
+              a3 = cb_lookup(klut, ky[G] >> (2 * j + 16));
+            } else {
+              a0 = and_or(wx[j], 0x00C000C0u, kMagic);   // row r0, codes 2j (k rows 2t, 2t+1)
+              a1 = and_or(wy[j], 0x00C000C0u, kMagic);   // row r1
+              a2 = and_or(wx[j], 0x03000300u, kMagic);   // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
+              a3 = and_or(wy[j], 0x03000300u, kMagic);   // row r1
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               if (j == 0) mma16816_c(c[G][nt], a0, a1, a2, a3, qf[4 * G][nt][0], qf[4 * G][nt][1], cOff[G][nt]);
@@ -323,6 +352,12 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           sz01 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.y));
           sz10 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.x));
           sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
+          if constexpr (CB) {                      // range / 255: the dequantised value is zero + that * k_c
+            sz00.x = __fmul_rn(sz00.x, 1.f / 255.f);
+            sz01.x = __fmul_rn(sz01.x, 1.f / 255.f);
+            sz10.x = __fmul_rn(sz10.x, 1.f / 255.f);
+            sz11.x = __fmul_rn(sz11.x, 1.f / 255.f);
+          }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -384,6 +419,12 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           sv01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));
           sv10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));
           sv11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
+          if constexpr (CB) {                      // range * 256 / 255: the V operand holds k_c / 256
+            sv00.x = __fmul_rn(sv00.x, 256.f / 255.f);
+            sv01.x = __fmul_rn(sv01.x, 256.f / 255.f);
+            sv10.x = __fmul_rn(sv10.x, 256.f / 255.f);
+            sv11.x = __fmul_rn(sv11.x, 256.f / 255.f);
+          }
         }
         if (ntok < kP) {                           // rows past the end: no stale metadata
           if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);
@@ -405,14 +446,34 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         // exact codes (the accumulators stay the size of the result: the tensor cores' fp32
         // accumulation truncates, so a large constant part would grow the error with the split length)
         const uint32_t wah = wab.x >> 8, wbh = wab.y >> 8, wch = wcd.x >> 8, wdh = wcd.y >> 8;
+        // codebook format: each word's bytes reordered to (row 2p, row 2p+1) pairs per channel quartet,
+        // so that one shift puts a channel's two codes 8 bits apart, as the lookup's selector wants them
+        uint32_t vw[4];
+        if constexpr (CB) {
+          vw[0] = __byte_perm(wab.x, 0u, 0x3120u);
+          vw[1] = __byte_perm(wab.y, 0u, 0x3120u);
+          vw[2] = __byte_perm(wcd.x, 0u, 0x3120u);
+          vw[3] = __byte_perm(wcd.y, 0u, 0x3120u);
+        }
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           const int k = mt & 3;
-          const uint32_t m = 0x00030003u << (2 * k);
-          const uint32_t a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
-          const uint32_t a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
-          const uint32_t a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
-          const uint32_t a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
+          uint32_t a0, a1, a2, a3;
+          if constexpr (CB) {
+            // k_c / 256 exactly: (1024 + k_c) / 256 - 4 (the P operand carries range * 256 / 255, which keeps
+            // it clear of fp16 subnormals)
+            const int sh = 2 * k + (mt < 4 ? 0 : 16);
+            a0 = exact_codes(cb_lookup(vlut, vw[0] >> sh), 4);
+            a1 = exact_codes(cb_lookup(vlut, vw[1] >> sh), 4);
+            a2 = exact_codes(cb_lookup(vlut, vw[2] >> sh), 4);
+            a3 = exact_codes(cb_lookup(vlut, vw[3] >> sh), 4);
+          } else {
+            const uint32_t m = 0x00030003u << (2 * k);
+            a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
+            a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
+            a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
+            a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
         }
@@ -688,7 +749,7 @@ __device__ __forceinline__ void bf16_page(const LayerView& lv, const DecodeWorks
 // grid = (nsplit + nbf, hkv, B), block = 128: history splits, then one CTA per BF16 page.
 // MINB resident CTAs per SM (the register budget): 3 for grids of one or two waves (more registers, more
 // independent work per warp), 4 for grids of many waves (more warps to hide latency).
-template <int NT, int MINB, bool U8>
+template <int NT, int MINB, int FMT>
 __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWorkspace ws, FusedArgs fa) {
   TimelineSpan timeline_span(lv, kTlDecodeMma);
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -710,12 +771,21 @@ __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWo
     __syncthreads();
   }
   pdl_launch_dependents();                         // the merge kernel may be scheduled now; it waits for this grid
-  if (blockIdx.x < fa.nsplit) int2_split<NT, U8>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
+  if (blockIdx.x < fa.nsplit) int2_split<NT, FMT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
   else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
   if (trace != nullptr && threadIdx.x == 0) trace[5] = global_ns();
 }
 
 }  // namespace
+
+// the kernel build for the layout's metadata format, the GQA width and the occupancy the split policy chose
+template <int FMT>
+static cudaError_t launch_fmt(cudaLaunchConfig_t& cfg, const LayerView& lv, const DecodeWorkspace& ws,
+                              const FusedArgs& fa, int occupancy) {
+  if (lv.hq / lv.hkv > 4) return cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2, FMT>, lv, ws, fa);
+  if (occupancy == 4) return cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4, FMT>, lv, ws, fa);
+  return cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3, FMT>, lv, ws, fa);
+}
 
 int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
                       cudaStream_t st) {
@@ -746,25 +816,22 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (lv.meta_u8) {
-    if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2, true>, lv, ws, fa);
-    else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4, true>, lv, ws, fa);
-    else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3, true>, lv, ws, fa);
-  } else {
-    if (lv.hq / lv.hkv > 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<2, 2, false>, lv, ws, fa);
-    else if (a.mma_occupancy == 4) e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 4, false>, lv, ws, fa);
-    else e = cudaLaunchKernelEx(&cfg, k_decode_mma<1, 3, false>, lv, ws, fa);
-  }
+  if (lv.meta_u8) e = launch_fmt<kFmtU8>(cfg, lv, ws, fa, a.mma_occupancy);
+  else if (lv.meta_cb) e = launch_fmt<kFmtCB>(cfg, lv, ws, fa, a.mma_occupancy);
+  else e = launch_fmt<kFmtF16>(cfg, lv, ws, fa, a.mma_occupancy);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels() {
-  const void* fns[6] = {reinterpret_cast<const void*>(k_decode_mma<1, 3, false>),
-                        reinterpret_cast<const void*>(k_decode_mma<1, 4, false>),
-                        reinterpret_cast<const void*>(k_decode_mma<2, 2, false>),
-                        reinterpret_cast<const void*>(k_decode_mma<1, 3, true>),
-                        reinterpret_cast<const void*>(k_decode_mma<1, 4, true>),
-                        reinterpret_cast<const void*>(k_decode_mma<2, 2, true>)};
+  const void* fns[9] = {reinterpret_cast<const void*>(k_decode_mma<1, 3, kFmtF16>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 4, kFmtF16>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2, kFmtF16>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 3, kFmtU8>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 4, kFmtU8>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2, kFmtU8>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 3, kFmtCB>),
+                        reinterpret_cast<const void*>(k_decode_mma<1, 4, kFmtCB>),
+                        reinterpret_cast<const void*>(k_decode_mma<2, 2, kFmtCB>)};
   for (const void* f : fns) {
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kMmaSmem) != cudaSuccess)
       return OSCAR_ERR_CUDA;

@@ -190,6 +190,15 @@ __device__ __forceinline__ uint32_t code_at(uint32_t x, int i) {
 __device__ __forceinline__ uint32_t exact_at(uint32_t x, int i) {
   return hfma2_u(code_at(x, i), 0x1C001C00u, 0xC400C400u);
 }
+// Codebook format: the level k_c of code i of both 16-bit halves of x as an exact fp16 value, from the
+// codebook bytes `lut`: one byte permute builds fp16 1024 + k_c; then k_c = (1024 + k_c) - 1024 (K) or
+// k_c / 256 = (1024 + k_c) / 256 - 4 (V, whose P operand then carries range * 256 / 255 and stays
+// clear of fp16 subnormals).
+__device__ __forceinline__ uint32_t cb_level_at(uint32_t x, int i, uint32_t lut, bool div256) {
+  const uint32_t y = (x >> (2 * i)) & 0x00030003u;
+  const uint32_t v = __byte_perm(lut, 0x64646464u, ((y | (y >> 8)) & 0x0303u) | 0x4040u);
+  return div256 ? hfma2_u(v, 0x1C001C00u, 0xC400C400u) : hfma2_u(v, 0x3C003C00u, 0xE400E400u);
+}
 // Byte offset of element (row, k) of a K-major operand in the canonical no-swizzle layout, rows of
 // kcols elements: core matrix (row / 8, k / 8) at (row / 8) * (kcols / 8) * 128 + (k / 8) * 128.
 __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
@@ -201,16 +210,19 @@ __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
 // (rows = channels, K-major over the 64 tokens); et = 0 .. kExpThreads - 1 is the expanding thread.
 // Both hold exact codes. K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel
 // 16u + 8 + q (the query fragments use the same order). mc: null for the fp16 metadata, else the compact
-// format's grid constants {T, D, E, 0} per (kind, group) (16 floats).
+// format's grid constants {T, D, E, 0} per (kind, group) (16 floats). cb: codebook format, whose K and V
+// operands hold the levels k_c (bytes of klut, vlut) instead of the codes and whose scale is range / 255.
 __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uint8_t* vt, uint8_t* meta, int et,
-                                            const float* __restrict__ mc) {
+                                            const float* __restrict__ mc, bool cb, uint32_t klut, uint32_t vlut) {
+  auto kval = [&](uint32_t x, int i) { return cb ? cb_level_at(x, i, klut, false) : exact_at(x, i); };
+  auto vval = [&](uint32_t x, int i) { return cb ? cb_level_at(x, i, vlut, true) : exact_at(x, i); };
   for (int wi = et; wi < kP * (kD / 16); wi += kExpThreads) {   // K: token t, channels 16u .. 16u + 15
     const int t = (wi & 7) + 8 * (wi >> 6), u = (wi >> 3) & 7;   // a quarter warp: 8 consecutive tokens
     const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + t * 32 + 4 * u);
     *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u, kD)) =
-        make_uint4(exact_at(x, 0), exact_at(x, 1), exact_at(x, 2), exact_at(x, 3));
+        make_uint4(kval(x, 0), kval(x, 1), kval(x, 2), kval(x, 3));
     *reinterpret_cast<uint4*>(kh + canon_off(t, 16 * u + 8, kD)) =
-        make_uint4(exact_at(x, 4), exact_at(x, 5), exact_at(x, 6), exact_at(x, 7));
+        make_uint4(kval(x, 4), kval(x, 5), kval(x, 6), kval(x, 7));
   }
   for (int mi = et; mi < 2 * kP; mi += kExpThreads) {  // metadata as float arrays: s0, z0, s1, z1 per token
     const int kind = mi / kP, t = mi % kP;
@@ -219,6 +231,11 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
       const uint2 mw = *reinterpret_cast<const uint2*>(blk + (kind ? kVMetaOff : kKMetaOff) + 8 * t);
       a = __half22float2(*reinterpret_cast<const __half2*>(&mw.x));
       b = __half22float2(*reinterpret_cast<const __half2*>(&mw.y));
+      if (cb) {                                  // K: range / 255 (levels k_c); V: range * 256 / 255 (k_c / 256)
+        const float f = kind ? 256.f / 255.f : 1.f / 255.f;
+        a.x = __fmul_rn(a.x, f);
+        b.x = __fmul_rn(b.x, f);
+      }
     } else {
       const uint32_t mw = *reinterpret_cast<const uint32_t*>(blk + (kind ? kVMetaOffU8 : kKMetaOff) + 4 * t);
       const float* c = mc + 8 * kind;
@@ -241,7 +258,7 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     for (int i = 0; i < 8; ++i) {                // row i of core matrix (o, kb): channel 8o + i, tokens 8kb ..
       uint32_t c[4];
 #pragma unroll
-      for (int pp = 0; pp < 4; ++pp) c[pp] = exact_at(x[pp], i);
+      for (int pp = 0; pp < 4; ++pp) c[pp] = vval(x[pp], i);
       *reinterpret_cast<uint4*>(vt + o * kVtSbo + kb * 128 + i * 16) = make_uint4(c[0], c[1], c[2], c[3]);
     }
   }
@@ -451,6 +468,15 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
     // ---- expansion: page i into the K, V^T and metadata buffers i % 3 ---------------------------------
     const int et = tid - 32 * kExpWarp0;
     const float* mc = lv.meta_u8 ? lv.params + (size_t)h * kParamFloats + kMetaCOff : nullptr;
+    uint32_t klut = 0, vlut = 0;
+    if (lv.meta_cb) {
+      const float* ck = cb_consts(lv, h, OSCAR_KIND_K);
+      const float* cv = cb_consts(lv, h, OSCAR_KIND_V);
+      for (int i = 0; i < 4; ++i) {
+        klut |= (uint32_t)ck[i] << (8 * i);
+        vlut |= (uint32_t)cv[i] << (8 * i);
+      }
+    }
     for (int i = 0; i < n; ++i) {
       if (__any_sync(0xffffffffu, *failed != 0)) break;
       const int b = i % kBufs;
@@ -464,7 +490,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         break;
       }
       expand_page(ring + (i % kShStages) * kBlockBytes, smem + kOffKh + b * kKhBytes, smem + kOffVt + b * kVtBytes,
-                  smem + kOffMeta + b * kMetaBytes, et, mc);
+                  smem + kOffMeta + b * kMetaBytes, et, mc, lv.meta_cb != 0, klut, vlut);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the buffers
       mbar_arrive(B_(kBarExp + b));
     }

@@ -75,14 +75,14 @@ __device__ __forceinline__ void softmax_chunk(float (&pbuf)[GQ][kP], float* mrow
 // A CTA walks its range of history pages; per 64-token page it computes the
 // logits of all GQ heads (thread per (token, head)), updates the online
 // softmax, then accumulates P.Vhat (thread per rotated channel).
-template <int GQ>
+template <int GQ, bool CB>
 __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace ws, const int* __restrict__ seq_lens,
                                                    const int* __restrict__ hist_pt, int max_hist_pages,
                                                    int pages_per_split, float scale_log2, int len_add) {
   TimelineSpan timeline_span(lv, kTlInt2Simt);
   __shared__ __align__(16) uint8_t blk[kBlockBytes];
   __shared__ float2 msz[2][kP][kNG];     // [K, V][token][group] (scale', zero') of the staged page
-  __shared__ float mcs[16];              // compact format: {T, D, E, 0} per (kind, group)
+  __shared__ float mcs[32];              // compact format {T, D, E, 0} per (kind, group); codebook per kind
   __shared__ float qs[GQ][kD];
   __shared__ float qg[GQ][kNG];
   __shared__ float pbuf[GQ][kP];
@@ -101,7 +101,8 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
   for (int i = tid; i < GQ * kD; i += 128) qs[i / kD][i % kD] = ws.qrot[((size_t)b * lv.hq + hq0) * kD + i];
   if (tid < GQ * kNG) qg[tid / kNG][tid % kNG] = ws.qconst[((size_t)b * lv.hq + hq0 + tid / kNG) * kQConst + kQSum0 + tid % kNG];
   if (tid < GQ) { mrow[tid] = -INFINITY; lrow[tid] = 0.f; }
-  if (tid < 16) mcs[tid] = lv.params[(size_t)h * kParamFloats + kMetaCOff + tid];
+  if (tid < 32) mcs[tid] = lv.params[(size_t)h * kParamFloats + kMetaCOff + tid];
+  const float* lvk = mcs + 16;            // codebook levels k_0..k_3 of K (then thresholds), V at + 8
   float acc[GQ];
 #pragma unroll
   for (int i = 0; i < GQ; ++i) acc[i] = 0.f;
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
       if (!lv.meta_u8) {
         const __half* m = reinterpret_cast<const __half*>(blk + (kind ? kVMetaOff : kKMetaOff) + tk * kNG * 4) + 2 * g;
         sz = make_float2(__half2float(m[0]), __half2float(m[1]));
+        if (CB) sz.x = __fmul_rn(sz.x, 1.f / 255.f);     // range / 255: the dequantised value is zero + that * k
       } else {
         const uint8_t* m = blk + (kind ? kVMetaOffU8 : kKMetaOff) + tk * kNG * 2 + 2 * g;
         const float* c = mcs + 8 * kind + 4 * g;
@@ -144,7 +146,10 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
           for (int w = 0; w < 4; ++w) {
             const uint32_t word = kw[g * 4 + w];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) a = fmaf((float)((word >> (2 * i)) & 3u), qs[hh][g * 64 + w * 16 + i], a);
+            for (int i = 0; i < 16; ++i) {
+              const unsigned c = (word >> (2 * i)) & 3u;
+              a = fmaf(CB ? lvk[c] : (float)c, qs[hh][g * 64 + w * 16 + i], a);
+            }
           }
           dot = fmaf(msz[0][tk][g].x, a, dot);
           dot = fmaf(msz[0][tk][g].y, qg[hh][g], dot);
@@ -163,7 +168,8 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
       for (int hh = 0; hh < GQ; ++hh) acc[hh] *= alpha[hh];
       for (int tk = 0; tk < ntok; ++tk) {
         const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + (tk >> 1) * 64);
-        const float code = (float)((word >> ((tk & 1) * 16 + sh)) & 3u);
+        const unsigned ci = (word >> ((tk & 1) * 16 + sh)) & 3u;
+        const float code = CB ? lvk[8 + ci] : (float)ci;
         const float vhat = fmaf(msz[1][tk][g].x, code, msz[1][tk][g].y);
 #pragma unroll
         for (int hh = 0; hh < GQ; ++hh) acc[hh] = fmaf(pbuf[hh][tk], vhat, acc[hh]);
@@ -385,8 +391,13 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
     return launch_merge(lv, ws, a.B, a.nsplit + a.nsplit_shared, a.nbf, a.out, a.out_dtype, a.lse, st);
   }
   if (a.ev0) cudaEventRecord(a.ev0, st);     // profiled span: the history kernel
-  k_int2_simt<GQ><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
-                                                               a.pages_per_split, scale_log2, a.len_add);
+  if (lv.meta_cb)
+    k_int2_simt<GQ, true><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt, a.max_hist_pages,
+                                                                       a.pages_per_split, scale_log2, a.len_add);
+  else
+    k_int2_simt<GQ, false><<<dim3(a.nsplit, lv.hkv, a.B), 128, 0, st>>>(lv, ws, a.seq_lens, a.hist_pt,
+                                                                        a.max_hist_pages, a.pages_per_split,
+                                                                        scale_log2, a.len_add);
   if (a.ev1) cudaEventRecord(a.ev1, st);
   k_bf16_seg<GQ><<<dim3(lv.hkv, a.B), 128, 0, st>>>(lv, ws, static_cast<const __nv_bfloat16*>(a.q), a.seq_lens,
                                                     a.bf16_pt, scale_log2, a.nsplit, a.len_add);

@@ -143,8 +143,8 @@ __device__ __forceinline__ uint32_t pack16(uint4 b) {
 // time; codes and fp16 metadata of every row go to codes_s [16][128] (one code per byte) and
 // meta_s [16][2] (fp16 scale, zero per group).
 __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotate, const __nv_bfloat16* xs,
-                                              const float* tau_s, const float* mc, uint8_t* codes_s,
-                                              uint32_t* meta_s) {
+                                              const float* tau_s, const float* mc, const float* cb,
+                                              uint8_t* codes_s, uint32_t* meta_s) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   uint32_t a[8][4];
   if (rotate) {
@@ -214,8 +214,9 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
       }
       float sq, zq;
       uint32_t meta;
-      if (mc == nullptr) {                          // fp16 (scale, zero)
-        const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      if (mc == nullptr) {                          // fp16 (scale, zero), or (range, zero) with a codebook
+        const float diff = __fsub_rn(mx, mn);
+        const float scale = cb != nullptr ? diff : __fdiv_rn(diff, 3.0f);
         const __half2 sz = __halves2half2(__float2half_rn(sat_fp16(scale)), __float2half_rn(sat_fp16(mn)));
         sq = __low2float(sz);
         zq = __high2float(sz);
@@ -233,8 +234,8 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
         for (int e = 0; e < 2; ++e) {
           float c = 0.f;
           if (sq != 0.f) {
-            c = rintf(__fdiv_rn(__fsub_rn(acc[j][2 * rr + e], zq), sq));
-            c = fminf(fmaxf(c, 0.f), 3.f);
+            const float t = __fdiv_rn(__fsub_rn(acc[j][2 * rr + e], zq), sq);
+            c = cb != nullptr ? cb_code(t, cb) : fminf(fmaxf(rintf(t), 0.f), 3.f);
           }
           pair |= ((uint32_t)c) << (8 * e);
         }
@@ -276,8 +277,9 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     }
   }
   for (int i = tid; i < kD; i += blockDim.x) tau_s[i] = prm[(kind == OSCAR_KIND_K ? kTauKOff : kTauVOff) + i];
-  if (tid < 8) tau_s[kD + tid] = prm[kMetaCOff + kind * 8 + tid];      // compact-format grid constants
+  if (tid < 8) tau_s[kD + tid] = prm[(lv.meta_cb ? kCbOff : kMetaCOff) + kind * 8 + tid];   // format constants
   const float* mc = lv.meta_u8 ? tau_s + kD : nullptr;
+  const float* cbc = lv.meta_cb ? tau_s + kD : nullptr;
   __syncthreads();
   if (rotate && !__syncthreads_and(mbar_wait(bar, 0))) {
     if (tid == 0) flag(lv.status, OSCAR_STATUS_TIMEOUT);
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
       reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(xs + r * kXStride)[lane];
     }
     if (hist_rows != 0) {
-      quantize_tile(frag_s, rotate, xs, tau_s, mc, codes_s, meta_s);
+      quantize_tile(frag_s, rotate, xs, tau_s, mc, cbc, codes_s, meta_s);
       __syncwarp();
       // packed codes: 16 rows x 8 words of 16 codes; word idx = lane + 32 j
 #pragma unroll

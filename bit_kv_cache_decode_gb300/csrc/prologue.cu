@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
 #pragma unroll
       for (int r = 0; r < 4; ++r) y[r] = rows[rot_channel(lane, r)];
       quantize_pack_row(y, tau_s, int2_block_w(lv, hpage, h), hh % kP, kind,
-                        lv.meta_u8 ? meta_consts(lv, h, kind) : nullptr);
+                        lv.meta_u8 ? meta_consts(lv, h, kind) : nullptr, lv.meta_cb ? cb_consts(lv, h, kind) : nullptr);
     }
   } else if (do_q) {
     constexpr int kQWarps = kPrologueWarps - 1;

@@ -22,6 +22,9 @@
 //               k rows (2t', 2t'+1) -> channels (c0, c0 + 8) and (2t'+8, 2t'+9) ->
 //               channels (c0 + 1, c0 + 9), c0 = 16 (t' + 4 G) + 2 j; column g' is
 //               (head 4 nt + g'/2, part g'%2). sigma puts max|q~| near 2^12.
+//               Codebook pools (OSCAR_META_CB): the kernel feeds level k_c as 1024 + k_c
+//               (W = 1 for every channel), k rows (2t', 2t'+1) -> channels (c0, c0 + 4) and
+//               (2t'+8, 2t'+9) -> channels (c0 + 8, c0 + 12), c0 = 16 (t' + 4 G) + j.
 #pragma once
 
 #include "kernels.cuh"
@@ -166,7 +169,7 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
 #pragma unroll
     for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e, fragment scale 1 / W = 2^-(6 + 2 (e & 1))
       const float v = xs[qi * stride + 4 * lane + e];
-      const float x = v * sc * pow2i(-6 - 2 * (e & 1));
+      const float x = v * sc * (lv.meta_cb ? 1.f : pow2i(-6 - 2 * (e & 1)));
       const float hi = frag_round(x);
       offh += hi;
       offl += frag_round(x - hi);
@@ -199,9 +202,12 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
     uint32_t word = 0;
     if (nt < nt_count && head < gq) {
       // r = 0: channels (c0, c0 + 8), even, W = 64; r = 1: (c0 + 1, c0 + 9), odd, W = 256
-      const float sc = pow2i(sig[head] - 6 - 2 * r);
-      const int c0 = 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;
-      float x[2] = {xs[head * stride + c0] * sc, xs[head * stride + c0 + 8] * sc};
+      // (codebook pools: r = 0: (c0, c0 + 4), r = 1: (c0 + 8, c0 + 12), W = 1)
+      const float sc = lv.meta_cb ? pow2i(sig[head]) : pow2i(sig[head] - 6 - 2 * r);
+      const int c0 = lv.meta_cb ? 16 * (tp + 4 * (kb >> 2)) + (kb & 3) + 8 * r
+                                : 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;
+      const int c1 = c0 + (lv.meta_cb ? 4 : 8);
+      float x[2] = {xs[head * stride + c0] * sc, xs[head * stride + c1] * sc};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float hi = frag_round(x[e]);

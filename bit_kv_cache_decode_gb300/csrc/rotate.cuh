@@ -81,9 +81,11 @@ __device__ __forceinline__ float sat_fp16(float x) { return fminf(fmaxf(x, -6550
 // write its packed byte and group metadata into the page block `blk`, row
 // `row`, half `kind` (OSCAR_KIND_K / OSCAR_KIND_V). tau: float [128] clip
 // thresholds indexed by rotated channel. mc: null for the fp16 (scale, zero) metadata, else the
-// kind's compact-format constants {T, D, E, 0} for groups 0 and 1 (8 floats).
+// kind's compact-format constants {T, D, E, 0} for groups 0 and 1 (8 floats). cb: null, or the kind's
+// codebook constants {k_0..k_3, theta_0..theta_2, 0} (codebook format: fp16 range and zero).
 __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const float* __restrict__ tau,
-                                                  uint8_t* blk, int row, int kind, const float* __restrict__ mc) {
+                                                  uint8_t* blk, int row, int kind, const float* __restrict__ mc,
+                                                  const float* __restrict__ cb = nullptr) {
   const int lane = threadIdx.x & 31;
   float y[4];
 #pragma unroll
@@ -102,7 +104,8 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
   __half s16, z16;
   unsigned mn8 = 0, mx8 = 0;
   if (mc == nullptr) {
-    const float scale = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+    const float diff = __fsub_rn(mx, mn);
+    const float scale = cb != nullptr ? diff : __fdiv_rn(diff, 3.0f);   // codebook format: the range
     s16 = __float2half_rn(sat_fp16(scale));
     z16 = __float2half_rn(sat_fp16(mn));
     sq = __half2float(s16);
@@ -116,8 +119,8 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
   for (int r = 0; r < 4; ++r) {
     float c = 0.f;
     if (sq != 0.f) {
-      c = rintf(__fdiv_rn(__fsub_rn(y[r], zq), sq));
-      c = fminf(fmaxf(c, 0.f), 3.f);
+      const float t = __fdiv_rn(__fsub_rn(y[r], zq), sq);
+      c = cb != nullptr ? cb_code(t, cb) : fminf(fmaxf(rintf(t), 0.f), 3.f);
     }
     byte |= ((unsigned)c) << (2 * rev2(r));
   }

@@ -124,6 +124,19 @@ extern "C" {
  *    group 1), V metadata [4352, 4608). */
 #define OSCAR_META_F16 0
 #define OSCAR_META_U8  1
+/* OSCAR_META_CB: the Lloyd-Max codebook variant (news article "超越 TurboQuant…",
+ * section "总结与展望": the latest code adds a Lloyd-Max codebook to the
+ * attention-aware rotation). The 2-bit code indexes a codebook of 4 levels
+ * c_i = k_i / 255 (bytes 0 <= k_0 <= k_1 <= k_2 <= k_3 <= 255, one codebook
+ * per (layer, kv head, K / V), set by oscar_set_codebook) on each group's
+ * normalised range. Per (row, group) the metadata are fp16 range' =
+ * fp16(max - min) and zero' = fp16(min) (RNE, saturating), in the bytes and
+ * the 5120-byte block layout of OSCAR_META_F16 (range' in the scale slot).
+ * Encoding in float32: t = (y - zero') / range', theta_i = (k_i + k_{i+1}) /
+ * 510, code = number of i with t > theta_i (0 where range' = 0). Dequantised
+ * value: zero' + range' * k_code / 255. (0, 85, 170, 255) gives the uniform
+ * levels. */
+#define OSCAR_META_CB  2
 
 typedef struct oscar_layout {
   int num_layers;      /* >= 1                                                */
@@ -175,6 +188,25 @@ int oscar_layer_offsets(const oscar_cache* cache, int layer, size_t* int2_off, s
  * `stream`. */
 int oscar_set_rotation(oscar_cache* cache, int layer, const float* U_K, const float* U_V,
                        const float* tau_K, const float* tau_V, void* stream);
+
+/* Load a layer's codebooks (OSCAR_META_CB layouts; see OSCAR_META_CB).
+ *  cb_K, cb_V : host uint8 [Hkv][4], each codebook non-decreasing.
+ * oscar_set_rotation resets both to the uniform (0, 85, 170, 255), so call this
+ * after it. Errors: INVALID_ARG (null pointer, bad layer, a decreasing
+ * codebook), UNSUPPORTED (the layout is not OSCAR_META_CB), CUDA. The copy is
+ * enqueued on `stream`. */
+int oscar_set_codebook(oscar_cache* cache, int layer, const uint8_t* cb_K, const uint8_t* cb_V, void* stream);
+
+/* Lloyd-Max calibration of one codebook on the host (news article "超越
+ * TurboQuant…", section "总结与展望"): from rotated float32 calibration rows
+ * x_rot [N][128] (host), clipped to tau [128], every 64-channel group with
+ * max > min contributes its values normalised to u = (y - min) / (max - min).
+ * Lloyd's iteration from the levels (0, 1/3, 2/3, 1): thresholds at the
+ * midpoints, each level the mean of its cell (u <= t_0, t_0 < u <= t_1, ...;
+ * an empty cell keeps its level), until no level moves by more than 1e-12 or
+ * 1000 iterations; then cb[i] = rint(255 level_i) clamped and sorted.
+ * Errors: INVALID_ARG (null pointer, N < 1). */
+int oscar_calibrate_codebook(const float* x_rot, int N, const float* tau, uint8_t* cb);
 
 /* Bulk write of B requests' prompt tokens (MarkTechPost article, "服务系统：
  * 混合精度缓存布局", write path: rotate, clip, quantise, pack).

@@ -9,6 +9,7 @@ import torch
 
 import bit_kv_cache_decode_gb300 as osc
 import synth
+from oracle import codebook as CB
 from oracle import pool as P
 from oracle import rotation
 
@@ -25,14 +26,30 @@ def head_params(seed: int, layer: int, hkv: int) -> list[P.HeadParams]:
     return out
 
 
+def with_codebooks(seed: int, layer: int, prm: list[P.HeadParams]) -> list[P.HeadParams]:
+    """The heads' parameters with codebooks: K's from the oracle's Lloyd-Max calibration on the head's
+    calibration keys, V's a fixed uneven one (so that a K / V mix-up shows)."""
+    out = []
+    for h, p in enumerate(prm):
+        _, kc, _ = synth.calibration(seed, layer, h)
+        cbk = CB.calibrate_codebook(P.rotated_f32(kc, p.u_k), p.tau_k)
+        out.append(P.HeadParams(p.u_k, p.u_v, p.tau_k, p.tau_v, cbk, np.array([5, 90, 141, 240], np.uint8)))
+    return out
+
+
 def upload_params(cache: osc.OscarCache, layer: int, prm: list[P.HeadParams]):
     cache.set_rotation(layer, np.stack([p.u_k for p in prm]), np.stack([p.u_v for p in prm]),
                        np.stack([p.tau_k for p in prm]), np.stack([p.tau_v for p in prm]))
+    if cache.cfg.meta_format == osc.META_CB:
+        cache.set_codebook(layer, np.stack([p.cb_k for p in prm]), np.stack([p.cb_v for p in prm]))
+
+
+META_NAMES = {osc.META_F16: "f16", osc.META_U8: "u8", osc.META_CB: "cb"}
 
 
 def pool_from_device(cache: osc.OscarCache, layer: int) -> P.PoolModel:
     cfg = cache.cfg
-    geo = P.PoolGeometry(hkv=cfg.num_kv_heads, meta_format="u8" if cfg.meta_format == osc.META_U8 else "f16")
+    geo = P.PoolGeometry(hkv=cfg.num_kv_heads, meta_format=META_NAMES[cfg.meta_format])
     pm = P.PoolModel(geo, cfg.num_int2_pages, cfg.num_bf16_pages)
     torch.cuda.synchronize()
     pm.int2[:] = cache.int2_pages(layer).cpu().numpy()
@@ -81,13 +98,19 @@ def compare_int2_pools(got: P.PoolModel, ref: P.PoolModel, rows_written, tol_fra
         for h in range(geo.hkv):
             a = got.read_history(page, rows, h)
             b = ref.read_history(page, rows, h)
-            taus = (params[h].tau_k, params[h].tau_v) if params is not None else (None, None)
+            prm = params[h] if params is not None else None
             for kind, (ca, sa, za), (cb, sb, zb) in ((0, (a[0], a[1], a[2]), (b[0], b[1], b[2])),
                                                      (1, (a[3], a[4], a[5]), (b[3], b[4], b[5]))):
-                sa, za = P.dequant_params(sa, za, taus[kind], geo)
-                sb, zb = P.dequant_params(sb, zb, taus[kind], geo)
-                xa = (za.astype(np.float64).repeat(64, 1) + sa.astype(np.float64).repeat(64, 1) * ca)
-                xb = (zb.astype(np.float64).repeat(64, 1) + sb.astype(np.float64).repeat(64, 1) * cb)
+                xa = P.dequant_rows(ca, sa, za, prm, kind, geo)
+                xb = P.dequant_rows(cb, sb, zb, prm, kind, geo)
+                if geo.meta_format == "cb":          # one step = the widest gap between neighbouring levels
+                    lev = (prm.cb_k if kind == 0 else prm.cb_v).astype(np.float64)
+                    sa = sa.astype(np.float64) * max(np.diff(lev).max(), lev[0], 255 - lev[3]) / 255.0
+                    sb = sb.astype(np.float64) * max(np.diff(lev).max(), lev[0], 255 - lev[3]) / 255.0
+                else:
+                    tau = None if prm is None else (prm.tau_k if kind == 0 else prm.tau_v)
+                    sa = P.dequant_params(sa, za, tau, geo)[0]
+                    sb = P.dequant_params(sb, zb, tau, geo)[0]
                 step = np.maximum(sa, sb).astype(np.float64).repeat(64, 1)
                 d = np.abs(xa - xb)
                 assert np.all(d <= 1.01 * step + 2e-3 * np.abs(xb) + 1e-6), (page, h, d.max())

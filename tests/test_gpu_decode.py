@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import bit_kv_cache_decode_gb300 as osc
     from gpu_cases import (DEV, bf16_ulp, head_params, pool_from_device, queries, row_rel_err, to_dev_bf16, tokens,
-                           upload_params)
+                           upload_params, with_codebooks)
 import synth
 from oracle import attention as A
 from oracle import pool as P
@@ -50,10 +50,12 @@ def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64, 
             ob += 5
     cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=n_int2,
                           num_bf16_pages=n_bf16, max_batch=B, max_splits=max_splits, v_mode=v_mode,
-                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
+                          meta_format={"f16": 0, "u8": 1, "cb": 2}[meta])
     cache = osc.OscarCache(cfg, device=DEV)
     cache.set_decode_algo(algo)
     prm = head_params(seed, 0, hkv)
+    if meta == "cb":
+        prm = with_codebooks(seed, 0, prm)
     upload_params(cache, 0, prm)
     ks, vs = [], []
     for r, L in enumerate(lens):
@@ -189,7 +191,24 @@ def test_compact_metadata_decode(algo, v_mode, gq):
     _check(cache, prm, hp, bp, lens, gq, v_mode, seed=18)
 
 
-@pytest.mark.parametrize("meta", ["f16", "u8"])
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("v_mode", [0, 1])
+@pytest.mark.parametrize("gq", [4, 8])
+def test_codebook_decode(algo, v_mode, gq):
+    # the Lloyd-Max codebook format: both decoders, both V modes, the one- and two-n-tile variants
+    lens = [1024, 64 + 64 * 13 + 29 + 256, 300]
+    cache, prm, hp, bp = _build(lens, 2, gq, v_mode, seed=21, algo=algo, meta="cb")
+    _check(cache, prm, hp, bp, lens, gq, v_mode, seed=21)
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_codebook_shared_prefix_kernel(v_mode):
+    lens = [64 + 64 * 20 + 300, 64 + 64 * 20 + 700, 64 + 64 * 20 + 256]
+    cache, prm, hp, bp = _build(lens, 2, 4, v_mode, seed=22, shared_prefix=64 + 64 * 20, algo=1, meta="cb")
+    _check(cache, prm, hp, bp, lens, 4, v_mode, seed=22, shared_pages=20)
+
+
+@pytest.mark.parametrize("meta", ["f16", "u8", "cb"])
 def test_many_waves_kernel_variant(meta):
     # 32 requests x 8 kv heads: a grid of more than two waves, where the split policy takes the
     # 4-CTAs-per-SM build of the tensor-core decode

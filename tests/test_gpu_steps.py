@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import bit_kv_cache_decode_gb300 as osc
     from gpu_cases import (DEV, compare_int2_pools, head_params, pool_from_device, queries, row_rel_err, to_dev_bf16,
-                           tokens, upload_params)
+                           tokens, upload_params, with_codebooks)
 import synth
 from oracle import attention as A
 from oracle import pool as P
@@ -55,12 +55,16 @@ def test_decode_step_equals_append_then_decode(algo, v_mode):
     assert torch.equal(caches[0].pool, caches[1].pool)
 
 
+@pytest.mark.parametrize("meta", [pytest.param("u8", id="meta_u8"), pytest.param("cb", id="meta_cb")])
 @pytest.mark.parametrize("v_mode", [0, 1])
-def test_compact_metadata_8k_then_64_steps(v_mode):
-    # the 16-bit-per-group format through prefill, 64 fused append + demotion + decode steps
+def test_metadata_formats_8k_then_64_steps(v_mode, meta):
+    # the 16-bit-per-group and the codebook formats through prefill, 64 fused append + demotion +
+    # decode steps
     hkv, gq, L0, steps = 8, 4, 8192, 64
-    cache, hp, bp = _cache(hkv, gq, L0 + steps, v_mode, 1, meta=osc.META_U8)
+    cache, hp, bp = _cache(hkv, gq, L0 + steps, v_mode, 1, meta=osc.META_U8 if meta == "u8" else osc.META_CB)
     prm = head_params(33, 0, hkv)
+    if meta == "cb":
+        prm = with_codebooks(33, 0, prm)
     upload_params(cache, 0, prm)
     k, v = tokens(33, 0, hkv, L0 + steps)
     cache.quantize_prefill(0, to_dev_bf16(k[:L0]), to_dev_bf16(v[:L0]), np.array([0, L0], np.int32), hp, bp)
@@ -77,7 +81,7 @@ def test_compact_metadata_8k_then_64_steps(v_mode):
                                       synth.sm_scale())
             err = row_rel_err(out[0].double().cpu().numpy(), ref)
             assert err.max() <= TOL, (s, err.max())
-    ref_pool = P.PoolModel(P.PoolGeometry(hkv=hkv, meta_format="u8"), cache.cfg.num_int2_pages,
+    ref_pool = P.PoolModel(P.PoolGeometry(hkv=hkv, meta_format=meta), cache.cfg.num_int2_pages,
                            cache.cfg.num_bf16_pages)
     P.prefill(ref_pool, k, v, hp[0], bp[0], prm, v_mode == osc.V_ABSORBED)
     got = pool_from_device(cache, 0)

@@ -9,18 +9,25 @@ pytestmark = pytest.mark.gpu
 if torch.cuda.is_available():
     import bit_kv_cache_decode_gb300 as osc
     from gpu_cases import (DEV, compare_int2_pools, head_params, pool_from_device, to_dev_bf16, tokens,
-                           upload_params)
+                           upload_params, with_codebooks)
+from oracle import codebook as CB
 from oracle import pool as P
 from oracle import quant
 
 
-META = [pytest.param("f16", id="meta_f16"), pytest.param("u8", id="meta_u8")]
+META = [pytest.param("f16", id="meta_f16"), pytest.param("u8", id="meta_u8"), pytest.param("cb", id="meta_cb")]
+FMT = {"f16": 0, "u8": 1, "cb": 2}
+
+
+def _params(seed, layer, hkv, meta):
+    prm = head_params(seed, layer, hkv)
+    return with_codebooks(seed, layer, prm) if meta == "cb" else prm
 
 
 def _cache(hkv, hq, n_int2, n_bf16, v_mode=0, layers=1, max_batch=2, meta="f16"):
     cfg = osc.CacheConfig(num_layers=layers, num_kv_heads=hkv, num_q_heads=hq, num_int2_pages=n_int2,
                           num_bf16_pages=n_bf16, max_batch=max_batch, max_splits=32, v_mode=v_mode,
-                          meta_format=osc.META_U8 if meta == "u8" else osc.META_F16)
+                          meta_format=FMT[meta])
     return osc.OscarCache(cfg, device=DEV)
 
 
@@ -28,7 +35,7 @@ def _cache(hkv, hq, n_int2, n_bf16, v_mode=0, layers=1, max_batch=2, meta="f16")
 def test_pack_rotated_bit_exact(meta):
     hkv, layer = 2, 1
     cache = _cache(hkv, 8, 5, 1, layers=2, meta=meta)
-    prm = head_params(3, layer, hkv)
+    prm = _params(3, layer, hkv, meta)
     upload_params(cache, layer, prm)
     N = 300
     k, v = tokens(3, layer, hkv, N)
@@ -48,11 +55,15 @@ def test_pack_rotated_bit_exact(meta):
     assert cache.get_status() == 0
     got = pool_from_device(cache, layer)
     ref = P.PoolModel(P.PoolGeometry(hkv=hkv, meta_format=meta), 5, 1)
-    qt = quant.quantize_token if meta == "f16" else quant.quantize_token_u8
     for n in range(N):
         for h in range(hkv):
-            kc, ks, kz = qt(xk[n, h], prm[h].tau_k, 64)
-            vc, vs, vz = qt(xv[n, h], prm[h].tau_v, 64)
+            if meta == "cb":
+                kc, ks, kz = CB.quantize_token(xk[n, h], prm[h].tau_k, prm[h].cb_k)
+                vc, vs, vz = CB.quantize_token(xv[n, h], prm[h].tau_v, prm[h].cb_v)
+            else:
+                qt = quant.quantize_token if meta == "f16" else quant.quantize_token_u8
+                kc, ks, kz = qt(xk[n, h], prm[h].tau_k, 64)
+                vc, vs, vz = qt(xv[n, h], prm[h].tau_v, 64)
             ref.write_history(int(pages[n]), [int(rows[n])], h, quant.pack_codes(kc), ks, kz, quant.pack_codes(vc), vs, vz)
     assert np.array_equal(got.int2, ref.int2)
     # layer 0 untouched
@@ -92,7 +103,7 @@ def _prefill_case(v_mode, lens, hkv=2, seed=5, meta="f16"):
         hist_pt[r, :nh[r]] = perm_i[o:o + nh[r]]
         o += nh[r]
     cache = _cache(hkv, hkv * 4, n_int2, n_bf16, v_mode=v_mode, max_batch=B, meta=meta)
-    prm = head_params(seed, 0, hkv)
+    prm = _params(seed, 0, hkv, meta)
     upload_params(cache, 0, prm)
     ks, vs = zip(*[tokens(seed, 0, hkv, L, extra=r) for r, L in enumerate(lens)])
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)

@@ -72,7 +72,7 @@ def test_layout_sizes(osc, meta, block):
 @pytest.mark.parametrize("kw,code", [
     (dict(head_dim=64), -2), (dict(group=32), -2), (dict(page_size=32), -2),
     (dict(num_q_heads=24), -2), (dict(num_q_heads=30), -1), (dict(sink=65), -1), (dict(recent=0), -1),
-    (dict(max_batch=0), -1), (dict(v_mode=7), -1), (dict(num_layers=0), -1), (dict(meta_format=2), -1),
+    (dict(max_batch=0), -1), (dict(v_mode=7), -1), (dict(num_layers=0), -1), (dict(meta_format=3), -1),
 ])
 def test_layout_validation(osc, kw, code):
     rc, _, _ = _bytes(osc, **kw)
@@ -99,3 +99,31 @@ def test_host_calibration_matches_oracle(osc, head):
     assert np.abs(got["U_V"] - ref["U_V"]).max() < 1e-4
     assert np.abs(got["tau_K"] - ref["tau_K"]).max() <= 1e-5 * np.abs(ref["tau_K"]).max()
     assert np.abs(got["tau_V"] - ref["tau_V"]).max() <= 1e-4 * np.abs(ref["tau_V"]).max()
+
+
+@pytest.mark.parametrize("head", [0, 1])
+def test_host_codebook_calibration_matches_oracle(osc, head):
+    from oracle import codebook as CB
+    from oracle import pool as P
+    qc, kc, vc = synth.calibration(51, 0, head)
+    cal = rotation.calibrate(qc, kc, vc, synth.sm_scale())
+    xk = P.rotated_f32(kc, cal["U_K"].astype(np.float32))
+    tk = cal["tau_K"].astype(np.float32)
+    got = osc.calibrate_codebook(xk, tk)
+    ref = CB.calibrate_codebook(xk, tk)
+    assert np.array_equal(got, ref), (got, ref)
+    # heavy-tailed rows with clipping and constant groups mixed in
+    rng = np.random.default_rng(7 + head)
+    x = (rng.standard_t(3, size=(3000, 128)) * rng.uniform(0.1, 3.0, size=(3000, 1))).astype(np.float32)
+    x[::17, :64] = 0.5
+    tau = rng.uniform(0.5, 4.0, 128).astype(np.float32)
+    assert np.array_equal(osc.calibrate_codebook(x, tau), CB.calibrate_codebook(x, tau))
+
+
+def test_codebook_layout_and_argument_checks(osc):
+    rc, pb, _ = _bytes(osc, meta_format=2)
+    rc0, pb0, _ = _bytes(osc, meta_format=0)
+    assert rc == 0 and pb == pb0                   # same blocks as the fp16 format
+    lib = osc.lib()
+    assert lib.oscar_set_codebook(None, 0, None, None, None) == osc.ERR_INVALID_ARG
+    assert lib.oscar_calibrate_codebook(None, 1, None, None) == osc.ERR_INVALID_ARG

@@ -253,7 +253,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     cF[nt] = cZ0[nt] = cZ1[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
-      cF[nt] = qc[kQF];
+      cF[nt] = CB ? qc[kQF] : qc[kQF] * 16777216.f;   // 2^24: the codes were fed as subnormals
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
       o0h = qc[kQOff0H];
@@ -314,10 +314,9 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         float c[2][NT][4];                         // per group; starts from -offset: the MMAs add the biased sums
 #pragma unroll
         for (int G = 0; G < 2; ++G) {
-          // code i (bits 2i of each 16-bit half) is moved into bits 6-7 (i even) or 8-9 (i odd):
-          // shift left 6 for i = 0, 1; left 2 for i = 2, 3; right 2 for i = 4, 5; right 6 for i = 6, 7
-          const uint32_t wx[4] = {kx[G] << 6, kx[G] << 2, kx[G] >> 2, kx[G] >> 6};
-          const uint32_t wy[4] = {ky[G] << 6, ky[G] << 2, ky[G] >> 2, ky[G] >> 6};
+          // codes 0-3 of each 16-bit half from the word, codes 4-7 from the word shifted right by 8
+          const uint32_t wx[2] = {kx[G], kx[G] >> 8};
+          const uint32_t wy[2] = {ky[G], ky[G] >> 8};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint32_t a0, a1, a2, a3;
@@ -329,10 +328,13 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
               a2 = cb_lookup(klut, kx[G] >> (2 * j + 16));
               a3 = cb_lookup(klut, ky[G] >> (2 * j + 16));
             } else {
-              a0 = and_or(wx[j], 0x00C000C0u, kMagic);   // row r0, codes 2j (k rows 2t, 2t+1)
-              a1 = and_or(wy[j], 0x00C000C0u, kMagic);   // row r1
-              a2 = and_or(wx[j], 0x03000300u, kMagic);   // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
-              a3 = and_or(wy[j], 0x03000300u, kMagic);   // row r1
+              // the masked bits as fp16 subnormals c 4^(p mod 4) 2^-24, p the code's position (no bias, no
+              // conversion; the query fragments carry 4^-(p mod 4))
+              const uint32_t m0 = 0x00030003u << (4 * (j & 1)), m1 = 0x000C000Cu << (4 * (j & 1));
+              a0 = wx[j >> 1] & m0;                    // row r0, codes 2j (k rows 2t, 2t+1)
+              a1 = wy[j >> 1] & m0;                    // row r1
+              a2 = wx[j >> 1] & m1;                    // row r0, codes 2j+1 (k rows 2t+8, 2t+9)
+              a3 = wy[j >> 1] & m1;                    // row r1
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -468,6 +470,9 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             a2 = exact_codes(cb_lookup(vlut, vw[2] >> sh), 4);
             a3 = exact_codes(cb_lookup(vlut, vw[3] >> sh), 4);
           } else {
+            // the masked code bits as an fp16 subnormal, exactly c 4^k 2^-24: no bias (the accumulators stay
+            // the size of the result) and no conversion; the power of two 2^24 4^-k is applied to the
+            // accumulators once, after the loop
             const uint32_t m = 0x00030003u << (2 * k);
             a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
             a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
@@ -523,8 +528,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     float v[16];                                  // channels 16g .. 16g + 15
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      v[mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
-      v[8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
+      // codes were fed as c 4^k 2^-24, k = mt & 3 (the codebook build feeds its levels / 256 and its
+      // P operand carries the 256)
+      const float un = 1.f;
+      v[mt] = fmaf(grp ? acc[nt][mt][1] : acc[nt][mt][0], un, zs);
+      v[8 + mt] = fmaf(grp ? acc[nt][mt][3] : acc[nt][mt][2], un, zs);
     }
     float4* dst = reinterpret_cast<float4*>(ca + (w * 8 + head) * kCaStride + 16 * g);
 #pragma unroll

@@ -9,15 +9,16 @@
 //  * ws.qconst: group sums of q~, F = sm_scale log2(e) 2^-sigma, the scaled group
 //               sums (zero-point terms), the fragment offsets and sigma;
 //  * ws.qfrag : fp16 B fragments of the tensor-core logits. The tensor-core
-//               kernel feeds code c of channel ch as 1024 + c W(ch), the code
-//               sitting in mantissa bits 6-7 (W = 64, ch even) or 8-9 (W = 256,
-//               ch odd). With x(ch) = q~[ch] 2^sigma / W(ch) split into two fp16
-//               parts hi = fp16(x), lo = fp16(x - hi), the fragments carry hi
-//               and lo in separate columns and off_{g,part} = 1024 * sum_{ch in g}
-//               part(ch); then summing both columns,
-//               sum_{ch in g} (1024 + c W(ch)) (hi + lo)(ch) - off_g = 2^sigma sum c q~
-//               to about 22 bits. Keeping the codes in the top mantissa bits keeps
-//               the constant 1024 within 16/c of the code term.
+//               kernel feeds code c of channel ch as the fp16 subnormal
+//               c W(ch) 2^-24, W(ch) = 4^(p mod 4) for the code's position p in
+//               its 16-bit half of the packed word (the masked bits themselves,
+//               after a shift by 8 for p >= 4). With x(ch) = q~[ch] 2^sigma / W(ch)
+//               split into two fp16 parts hi = fp16(x), lo = fp16(x - hi), the
+//               fragments carry hi and lo in separate columns; summing both,
+//               sum_{ch in g} c W(ch) 2^-24 (hi + lo)(ch) = 2^(sigma - 24) sum c q~
+//               to about 22 bits, with no constant part to cancel (the offsets
+//               below are 0). Codebook pools feed 1024 + k_c instead and use the
+//               offsets off_{g,part} = 1024 * sum_{ch in g} part(ch).
 //               k-block kb = 4 G + j (G the channel group) at lane (g', t') holds
 //               k rows (2t', 2t'+1) -> channels (c0, c0 + 8) and (2t'+8, 2t'+9) ->
 //               channels (c0 + 1, c0 + 9), c0 = 16 (t' + 4 G) + 2 j; column g' is
@@ -167,12 +168,14 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
     const float sc = pow2i(sig[qi]);
     float offh = 0.f, offl = 0.f, sum = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e, fragment scale 1 / W = 2^-(6 + 2 (e & 1))
+    for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e
       const float v = xs[qi * stride + 4 * lane + e];
-      const float x = v * sc * (lv.meta_cb ? 1.f : pow2i(-6 - 2 * (e & 1)));
-      const float hi = frag_round(x);
-      offh += hi;
-      offl += frag_round(x - hi);
+      if (lv.meta_cb) {                             // offsets of the biased codebook levels 1024 + k_c
+        const float x = v * sc;
+        const float hi = frag_round(x);
+        offh += hi;
+        offl += frag_round(x - hi);
+      }
       sum += v;
     }
 #pragma unroll
@@ -201,9 +204,11 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
     const int head = 4 * nt + (gp >> 1), part = gp & 1;
     uint32_t word = 0;
     if (nt < nt_count && head < gq) {
-      // r = 0: channels (c0, c0 + 8), even, W = 64; r = 1: (c0 + 1, c0 + 9), odd, W = 256
-      // (codebook pools: r = 0: (c0, c0 + 4), r = 1: (c0 + 8, c0 + 12), W = 1)
-      const float sc = lv.meta_cb ? pow2i(sig[head]) : pow2i(sig[head] - 6 - 2 * r);
+      // r = 0: channels (c0, c0 + 8), code position p = 2 (kb & 3) in its 16-bit half; r = 1: (c0 + 1,
+      // c0 + 9), p + 1. The code of position p is fed as c 4^(p mod 4) 2^-24, so the fragment carries
+      // q~ 2^sigma / 4^(p mod 4) (the kernel's F takes the 2^24). Codebook pools: r = 0: (c0, c0 + 4),
+      // r = 1: (c0 + 8, c0 + 12), levels fed as 1024 + k_c (W = 1).
+      const float sc = lv.meta_cb ? pow2i(sig[head]) : pow2i(sig[head] - 2 * ((2 * (kb & 3) + r) & 3));
       const int c0 = lv.meta_cb ? 16 * (tp + 4 * (kb >> 2)) + (kb & 3) + 8 * r
                                 : 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;
       const int c1 = c0 + (lv.meta_cb ? 4 : 8);

@@ -429,8 +429,8 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "69c0b4e14a7971e7a3e64440f4787809fe7f3a1a04d0f0be9a9b90cb00a5262d",
-                      "bytes_per_launch": 66764288 + 289280}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "7b0042ad2e7bba040280cfa9a896eb39522e75f9adbb292c62ce551c885a87c7",
+                      "bytes_per_launch": 66763776 + 270592}
 
 
 def sources_digest() -> str:
@@ -446,7 +446,7 @@ def sources_digest() -> str:
 
 
 def decode_traffic(args):
-    if args.algo != 1 or args.workload not in ("qwen3_8b_36l", "qwen3_8b_100k_l1"):
+    if args.algo != 1 or args.workload not in ("qwen3_8b_36l", "qwen3_8b_100k_l1") or args.meta_format != "f16":
         return None
     if NCU_DECODE_TRAFFIC["sources_sha256"] != sources_digest():
         return None

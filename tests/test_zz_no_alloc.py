@@ -19,13 +19,13 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import bit_kv_cache_decode_gb300 as osc
-    from gpu_cases import DEV, head_params, queries, row_rel_err, to_dev_bf16, tokens, upload_params
+    from gpu_cases import DEV, head_params, queries, row_rel_err, to_dev_bf16, tokens, upload_params, with_codebooks
 import synth
 
 TOL = 2e-3
 
 
-def _cache(lens, hkv, gq, v_mode, seed):
+def _cache(lens, hkv, gq, v_mode, seed, meta=0):
     B = len(lens)
     nh = [max(0, (L - 320 + 63) // 64) for L in lens]
     mhp = max(1, max(nh))
@@ -36,10 +36,11 @@ def _cache(lens, hkv, gq, v_mode, seed):
         o += nh[r]
     bf16_pt = np.arange(5 * B, dtype=np.int32).reshape(B, 5)
     cfg = osc.CacheConfig(num_layers=2, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=o + 1,
-                          num_bf16_pages=5 * B, max_batch=B, max_splits=64, v_mode=v_mode)
+                          num_bf16_pages=5 * B, max_batch=B, max_splits=64, v_mode=v_mode, meta_format=meta)
     cache = osc.OscarCache(cfg, device=DEV)
     for layer in range(2):
-        upload_params(cache, layer, head_params(seed + layer, layer, hkv))
+        prm = head_params(seed + layer, layer, hkv)
+        upload_params(cache, layer, with_codebooks(seed + layer, layer, prm) if meta == osc.META_CB else prm)
         ks, vs = zip(*[tokens(seed, layer, hkv, L, extra=r) for r, L in enumerate(lens)])
         cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
         cache.quantize_prefill(layer, to_dev_bf16(np.concatenate(ks)), to_dev_bf16(np.concatenate(vs)), cu,
@@ -48,10 +49,11 @@ def _cache(lens, hkv, gq, v_mode, seed):
     return cache, hist_pt, bf16_pt
 
 
+@pytest.mark.parametrize("meta", [0, 1, 2], ids=["meta_f16", "meta_u8", "meta_cb"])
 @pytest.mark.parametrize("v_mode", [0, 1])
-def test_noalloc_matches_decode_attention_on_two_calls(v_mode):
+def test_noalloc_matches_decode_attention_on_two_calls(v_mode, meta):
     lens, hkv, gq = [1024, 5000, 300], 2, 4
-    cache, hp, bp = _cache(lens, hkv, gq, v_mode, seed=41)
+    cache, hp, bp = _cache(lens, hkv, gq, v_mode, seed=41, meta=meta)
     seq = torch.tensor(lens, dtype=torch.int32, device=DEV)
     hp_d, bp_d = torch.from_numpy(hp).to(DEV), torch.from_numpy(bp).to(DEV)
     status = torch.full((1,), -1, dtype=torch.int32, device=DEV)

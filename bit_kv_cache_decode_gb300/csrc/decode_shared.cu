@@ -72,7 +72,7 @@ constexpr int kRowc = 16;                             // per row: F, Z0, Z1, the
 constexpr int kOffRowc = kOffMeta + kBufs * kMetaBytes;   // [128 rows][kRowc]
 constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128 rows] partial maxima
 constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
-constexpr int kNumBars = 17;
+constexpr int kNumBars = 20;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
 static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
 // mbarrier indices
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarSFree + 0), kRowThreads);
       mbar_init_n(B_(kBarSFree + 1), kRowThreads);
       mbar_init_n(B_(kBarPReady), kRowThreads);
-      mbar_init_n(B_(kBarMx), kRowThreads);
+      for (int qq = 0; qq < 4; ++qq) mbar_init_n(B_(kBarMx + qq), kRowThreads / 4);   // per row quarter
       mbar_init_n(B_(kBarODone), 1);
       mbar_init_n(B_(kBarBufFree + 0), 1);
       mbar_init_n(B_(kBarBufFree + 1), 1);
@@ -546,8 +546,8 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
 #pragma unroll
       for (int c = 0; c < kSliceTok; ++c) mx = fmaxf(mx, l[c]);
       mxs[(b * kSlices + sl) * kShQ + q] = mx;
-      mbar_arrive(B_(kBarMx));
-      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarMx), i & 1))) {
+      mbar_arrive(B_(kBarMx + quarter));            // only the two slice warps of these rows exchange maxima
+      if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarMx + quarter), i & 1))) {
         ok = false;
         break;
       }

@@ -429,18 +429,21 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "7b0042ad2e7bba040280cfa9a896eb39522e75f9adbb292c62ce551c885a87c7",
+NCU_DECODE_TRAFFIC = {"sources_sha256": "ea02d410d368d7a4fd543f7aacffa647af8afa777de0c45586fa668e24b0a984",
                       "bytes_per_launch": 66763776 + 270592}
+
+
+# the sources the fused decode kernel is compiled from (its file and the headers it includes)
+DECODE_KERNEL_SOURCES = ("decode_mma.cu", "kernels.cuh", "common.cuh", "rotate.cuh", "tma.cuh", "timeline.cuh")
 
 
 def sources_digest() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_decode_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".cpp", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in DECODE_KERNEL_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "oscar.h"), "rb").read())
     return h.hexdigest()
 

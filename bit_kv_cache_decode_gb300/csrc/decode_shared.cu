@@ -79,7 +79,9 @@ static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
 constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 6, kBarSFree = 8, kBarPReady = 10, kBarODone = 11,
               kBarBufFree = 12, kBarFinal = 15, kBarMx = 16;
 // TMEM columns: S buffers at 0 and 128 (group G at + 64 G), O at 256 (group G at + 64 G)
-constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
+// TMEM columns: S of two pages (fp32) at 0 and 128, O (fp32) at 256, the rows' query fragments (fp16 pairs,
+// the S MMAs' A operand) at 384 (high parts) and 448 (low parts)
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256, kColQh = 384, kColQl = 448;
 
 // UMMA shared-memory descriptor: no swizzle, K-major; lbo = byte step between the core matrices of a row
 // block along K, sbo = byte step between 8-row blocks.
@@ -95,6 +97,14 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, bo
       "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// The same with A in tensor memory (its M rows in the TMEM lanes, K along the columns, two fp16 per column).
+__device__ __forceinline__ void umma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, bool accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(kIdesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -125,17 +135,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 16 columns of this warp's 32 TMEM lanes
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 32 columns at each of two TMEM addresses: both loads in flight, then one wait
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32], float (&vb)[32]) {
+  uint32_t r[32], q[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
+      "%28,%29,%30,%31}, [%32];"
+      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]),
+        "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]),
+        "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]),
+        "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+      : "r"(tb));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) {
+    va[i] = __uint_as_float(r[i]);
+    vb[i] = __uint_as_float(q[i]);
+  }
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
@@ -355,43 +381,42 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       qrow = ws.qrot + row * kD;
     }
     const float sc = exp2f(sig);                   // max |q~| 2^sigma is near 2^12: fp16-safe
-    uint8_t* qh = smem + kOffQ;
-    uint8_t* qlo = smem + kOffQ + kQBytes;
+    // the row's fragments go to its TMEM lane: column 8u + j holds the fp16 pair (16u + j, 16u + 8 + j) of
+    // 16-channel block u (high parts from column kColQh, low parts from kColQl), the S MMAs' A operand
+    const uint32_t tq = tmem + ((uint32_t)(32 * w) << 16);
 #pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {               // channels 32 cc .. 32 cc + 31: 16-channel blocks 2cc, 2cc + 1
-      float x[32];
+    for (int c2 = 0; c2 < 2; ++c2) {               // channels 64 c2 .. 64 c2 + 63: TMEM columns 32 c2 ..
+      float hw[32], lw[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float4 v = valid ? *reinterpret_cast<const float4*>(qrow + 32 * cc + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x[4 * e] = v.x * sc;
-        x[4 * e + 1] = v.y * sc;
-        x[4 * e + 2] = v.z * sc;
-        x[4 * e + 3] = v.w * sc;
-      }
+      for (int cl = 0; cl < 2; ++cl) {
+        const int cc = 2 * c2 + cl;                // channels 32 cc .. 32 cc + 31: 16-channel blocks 2cc, 2cc + 1
+        float x[32];
 #pragma unroll
-      for (int ub = 0; ub < 2; ++ub) {
-        const int u = 2 * cc + ub;
+        for (int e = 0; e < 8; ++e) {
+          const float4 v = valid ? *reinterpret_cast<const float4*>(qrow + 32 * cc + 4 * e) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[4 * e] = v.x * sc;
+          x[4 * e + 1] = v.y * sc;
+          x[4 * e + 2] = v.z * sc;
+          x[4 * e + 3] = v.w * sc;
+        }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {     // k-block 2u + half: channel pairs (16u + j, 16u + 8 + j)
-          uint32_t hw[4], lw[4];
+        for (int ub = 0; ub < 2; ++ub)
 #pragma unroll
-          for (int pr = 0; pr < 4; ++pr) {
-            const int j = 4 * half + pr;
+          for (int j = 0; j < 8; ++j) {
             const float xa = x[16 * ub + j], xb = x[16 * ub + 8 + j];
             const float ha = frag_round16(xa), hb = frag_round16(xb);
             const float la = frag_round16(xa - ha), lb = frag_round16(xb - hb);
-            hw[pr] = pack_f16x2(ha, hb);
-            lw[pr] = pack_f16x2(la, lb);
+            hw[16 * cl + 8 * ub + j] = __uint_as_float(pack_f16x2(ha, hb));
+            lw[16 * cl + 8 * ub + j] = __uint_as_float(pack_f16x2(la, lb));
           }
-          *reinterpret_cast<uint4*>(qh + canon_off(q, 16 * u + 8 * half, kD)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(qlo + canon_off(q, 16 * u + 8 * half, kD)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
       }
+      tmem_st32(tq + kColQh + 32 * c2, hw);
+      tmem_st32(tq + kColQl + 32 * c2, lw);
     }
     rowc[q * kRowc + 0] = F;
     rowc[q * kRowc + 1] = Z0;
     rowc[q * kRowc + 2] = Z1;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the MMAs read the fragments
+    tc_fence_before();                             // the MMAs read the fragments from TMEM after the barrier
   }
   __syncthreads();
 
@@ -400,7 +425,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
   if (w == kCtlWarp) {
     // ---- control: the MMAs of every page and the ring's bulk copies (one thread) ----------------------
     if (lane == 0) {
-      const uint32_t qh_a = smem_addr(smem + kOffQ), ql_a = qh_a + kQBytes, p_a = smem_addr(smem + kOffP);
+      const uint32_t p_a = smem_addr(smem + kOffP);
       const uint32_t kh_a = smem_addr(smem + kOffKh), vt_a = smem_addr(smem + kOffVt);
       auto issue_s = [&](int i) {                  // S_G = Q_G K_G^T into TMEM columns 128 (i % 2) + 64 G
         const int b = i & 1, kb3 = i % kBufs;
@@ -411,8 +436,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
             const uint32_t koff = (8 * G + 2 * kk) * 128;                 // k-blocks 8G + 2kk and + 1
             const uint64_t bd = umma_desc(kh_a + kb3 * kKhBytes + koff, 128, (kD / 8) * 128);
             const uint32_t d = tmem + kColS + 128 * b + 64 * G;
-            umma(d, umma_desc(qh_a + koff, 128, (kD / 8) * 128), bd, kk > 0);
-            umma(d, umma_desc(ql_a + koff, 128, (kD / 8) * 128), bd, true);
+            const uint32_t qcol = 8 * (4 * G + kk);                      // K = 16 channels: 8 TMEM columns
+            umma_ta(d, tmem + kColQh + qcol, bd, kk > 0);
+            umma_ta(d, tmem + kColQl + qcol, bd, true);
           }
         umma_commit(B_(kBarSDone + b));
       };
@@ -522,16 +548,14 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       const float* md = reinterpret_cast<const float*>(smem + kOffMeta + (i % kBufs) * kMetaBytes) + kSliceTok * sl;
       auto pair = [&](int arr, int c) { return *reinterpret_cast<const float2*>(md + arr * kP + c); };
       float l[kSliceTok];
+      {
+        static_assert(kSliceTok == 32, "one 32-column load per group");
+        float s0[32], s1[32];                      // S of groups 0 and 1: both loads in flight, one wait
+        tmem_ld32x2(trow + kColS + 128 * b + kSliceTok * sl, trow + kColS + 128 * b + 64 + kSliceTok * sl, s0, s1);
 #pragma unroll
-      for (int c16 = 0; c16 < kSliceTok / 16; ++c16) {
-        float s0[16], s1[16];
-        tmem_ld16(trow + kColS + 128 * b + kSliceTok * sl + 16 * c16, s0);
-        tmem_ld16(trow + kColS + 128 * b + 64 + kSliceTok * sl + 16 * c16, s1);
-#pragma unroll
-        for (int c = 0; c < 16; c += 2) {        // two tokens per packed fp32 op: F (s0 S0 + s1 S1) + z0 Z0 + z1 Z1
-          const int t = 16 * c16 + c;
-          float2 a = __fmul2_rn(pair(2, t), make_float2(s1[c], s1[c + 1]));
-          a = __ffma2_rn(pair(0, t), make_float2(s0[c], s0[c + 1]), a);
+        for (int t = 0; t < kSliceTok; t += 2) {   // two tokens per packed fp32 op: F (s0 S0 + s1 S1) + z0 Z0 + z1 Z1
+          float2 a = __fmul2_rn(pair(2, t), make_float2(s1[t], s1[t + 1]));
+          a = __ffma2_rn(pair(0, t), make_float2(s0[t], s0[t + 1]), a);
           float2 zt = __fmul2_rn(pair(3, t), Z1v);
           zt = __ffma2_rn(pair(1, t), Z0v, zt);
           const float2 lv = __ffma2_rn(Fv, a, zt);

@@ -53,7 +53,6 @@ constexpr uint32_t kCodeMask = 0x03000300u;           // mantissa bits 8-9 of bo
 constexpr float kLazyRescale = 8.f;                   // log2 growth of a row maximum that forces a rescale
 
 // shared memory (bytes; every operand 1024-byte aligned)
-constexpr int kQBytes = kShQ * kD * 2;                // one part of the rows' fragments: 32 KB
 constexpr int kKhBytes = kP * kD * 2;                 // expanded K of a page: 16 KB
 // expanded V^T of a page: 16 blocks of 8 channel rows, each block 8 core matrices of 128 B plus 16 B of
 // padding, so the eight blocks a quarter warp writes at once start in distinct 16-byte bank slots
@@ -61,9 +60,8 @@ constexpr int kVtSbo = (kP / 8) * 128 + 16;           // 1,040 B between 8-chann
 constexpr int kVtBytes = (kD / 8) * kVtSbo;           // 16,640 B
 constexpr int kPBytes = kShQ * kP * 2;                // weights of one channel group: 16 KB
 constexpr int kOffRing = 0;
-constexpr int kOffQ = 15360;                          // kShStages * kBlockBytes, 1024-aligned
 constexpr int kBufs = 3;                              // expanded pages in flight
-constexpr int kOffKh = kOffQ + 2 * kQBytes;           // kBufs buffers
+constexpr int kOffKh = 15360;                         // kShStages * kBlockBytes, 1024-aligned; kBufs buffers
 constexpr int kOffVt = kOffKh + kBufs * kKhBytes;     // kBufs buffers
 constexpr int kOffP = kOffVt + kBufs * kVtBytes;      // 2 groups
 constexpr int kMetaBytes = 2 * kP * 16;               // [K, V][s0, z0, s1, z1][64 tokens] as floats
@@ -74,7 +72,7 @@ constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128
 constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
 constexpr int kNumBars = 20;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
-static_assert(kOffQ >= kShStages * kBlockBytes, "ring fits");
+static_assert(kOffKh >= kShStages * kBlockBytes, "ring fits");
 // mbarrier indices
 constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 6, kBarSFree = 8, kBarPReady = 10, kBarODone = 11,
               kBarBufFree = 12, kBarFinal = 15, kBarMx = 16;

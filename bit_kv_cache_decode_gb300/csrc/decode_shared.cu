@@ -63,19 +63,19 @@ constexpr int kOffRing = 0;
 constexpr int kBufs = 3;                              // expanded pages in flight
 constexpr int kOffKh = 15360;                         // kShStages * kBlockBytes, 1024-aligned; kBufs buffers
 constexpr int kOffVt = kOffKh + kBufs * kKhBytes;     // kBufs buffers
-constexpr int kOffP = kOffVt + kBufs * kVtBytes;      // 2 groups
+constexpr int kOffP = kOffVt + kBufs * kVtBytes;      // 2 buffers (page parity) x 2 groups
 constexpr int kMetaBytes = 2 * kP * 16;               // [K, V][s0, z0, s1, z1][64 tokens] as floats
-constexpr int kOffMeta = kOffP + 2 * kPBytes;         // kBufs buffers
+constexpr int kOffMeta = kOffP + 4 * kPBytes;         // kBufs buffers
 constexpr int kRowc = 16;                             // per row: F, Z0, Z1, then (l, z0, z1) sums of slices 1-3
 constexpr int kOffRowc = kOffMeta + kBufs * kMetaBytes;   // [128 rows][kRowc]
 constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128 rows] partial maxima
 constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 21;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
 static_assert(kOffKh >= kShStages * kBlockBytes, "ring fits");
 // mbarrier indices
 constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 6, kBarSFree = 8, kBarPReady = 10, kBarODone = 11,
-              kBarBufFree = 12, kBarFinal = 15, kBarMx = 16;
+              kBarBufFree = 13, kBarFinal = 16, kBarMx = 17;   // O done: one barrier per weights buffer
 // TMEM columns: S buffers at 0 and 128 (group G at + 64 G), O at 256 (group G at + 64 G)
 // TMEM columns: S of two pages (fp32) at 0 and 128, O (fp32) at 256, the rows' query fragments (fp16 pairs,
 // the S MMAs' A operand) at 384 (high parts) and 448 (low parts)
@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarSFree + 1), kRowThreads);
       mbar_init_n(B_(kBarPReady), kRowThreads);
       for (int qq = 0; qq < 4; ++qq) mbar_init_n(B_(kBarMx + qq), kRowThreads / 4);   // per row quarter
-      mbar_init_n(B_(kBarODone), 1);
+      mbar_init_n(B_(kBarODone + 0), 1);
+      mbar_init_n(B_(kBarODone + 1), 1);
       mbar_init_n(B_(kBarBufFree + 0), 1);
       mbar_init_n(B_(kBarBufFree + 1), 1);
       mbar_init_n(B_(kBarBufFree + 2), 1);
@@ -474,10 +475,10 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
         for (int G = 0; G < 2; ++G)                // O_G += P_G V_G^T, TMEM columns 256 + 64 G
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma(tmem + kColO + 64 * G, umma_desc(p_a + G * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
+            umma(tmem + kColO + 64 * G, umma_desc(p_a + ((i & 1) * 2 + G) * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
                  umma_desc(vt_a + kb3 * kVtBytes + G * 8 * kVtSbo + 2 * kk * 128, 128, kVtSbo),
                  i > 0 || kk > 0);
-        umma_commit(B_(kBarODone));
+        umma_commit(B_(kBarODone + (i & 1)));
         umma_commit(B_(kBarBufFree + kb3));
       }
       if (!ok) {
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
     // ---- rows: logits, online softmax, weights. Thread = row q (TMEM lane), tokens kSliceTok sl .. --------
     const int quarter = w & 3, sl = w >> 2, q = 32 * quarter + lane;
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
-    uint8_t* pbase = smem + kOffP;
+    uint8_t* const pbuf = smem + kOffP;                      // [page parity][group]
     float* mxs = reinterpret_cast<float*>(smem + kOffMx);   // [page % 2][slice][row]
     const float F = rowc[q * kRowc + 0], Z0 = rowc[q * kRowc + 1], Z1 = rowc[q * kRowc + 2];
     const float2 Fv = make_float2(F, F), Z0v = make_float2(Z0, Z0), Z1v = make_float2(Z1, Z1);
@@ -586,13 +587,22 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       lsum2 = __fmul2_rn(lsum2, al2);
       zacc02 = __fmul2_rn(zacc02, al2);
       zacc12 = __fmul2_rn(zacc12, al2);
-      if (i > 0) {                                 // O of page i - 1 is complete and the weights buffer free
-        if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (i - 1) & 1))) {
+      // the weights buffer of page i (parity i & 1) is free once O of page i - 2 is complete; O itself is
+      // rescaled (when the maximum grows) once O of page i - 1 is
+      if (i >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarODone + (i & 1)), ((i - 2) >> 1) & 1))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (sl == 0 && __any_sync(0xffffffffu, grow)) {   // rescale these rows of O (al = 1 for the others)
+      }
+      if (i > 0 && sl == 0 && __any_sync(0xffffffffu, grow)) {   // rescale these rows of O (al = 1 for the others)
+        if (!__all_sync(0xffffffffu, mbar_wait(B_(kBarODone + ((i - 1) & 1)), ((i - 1) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        {
 #pragma unroll 1
           for (int c4 = 0; c4 < 4; ++c4) {
             float o[32];
@@ -621,6 +631,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           w1[pr] = pack_f16x2(a1.x, a1.y);
         }
         const int off = canon_off(q, kSliceTok * sl + 8 * j, kP);
+        uint8_t* const pbase = pbuf + (i & 1) * 2 * kPBytes;
         *reinterpret_cast<uint4*>(pbase + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
         *reinterpret_cast<uint4*>(pbase + kPBytes + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
       }
@@ -628,7 +639,8 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       tc_fence_before();
       mbar_arrive(B_(kBarPReady));
     }
-    if (ok && n > 0 && sl == 0 && !__all_sync(0xffffffffu, mbar_wait(B_(kBarODone), (n - 1) & 1))) ok = false;
+    if (ok && n > 0 && sl == 0 && !__all_sync(0xffffffffu, mbar_wait(B_(kBarODone + ((n - 1) & 1)), ((n - 1) >> 1) & 1)))
+      ok = false;
     if (!ok && lane == 0) {
       if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
       *failed = 1;

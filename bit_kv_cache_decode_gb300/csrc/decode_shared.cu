@@ -41,8 +41,11 @@ namespace oscar {
 namespace {
 
 // row warps w = 0 .. 7: TMEM lane quarter w % 4 (rows 32 (w % 4) ..), 32-token slice w / 4 of every page
-constexpr int kRowWarps = 8, kSlices = 2, kSliceTok = kP / kSlices, kCtlWarp = 8, kExpWarp0 = 9, kExpWarps = 7;
-constexpr int kShThreads = (kRowWarps + 1 + kExpWarps) * 32;          // 512
+// warp 8: the bulk copies and the S MMAs; warps 9 .. 14: expansion; warp 15: the O MMAs (two issuing
+// threads, so that neither MMA stream waits behind the other's issue)
+constexpr int kRowWarps = 8, kSlices = 2, kSliceTok = kP / kSlices, kCtlWarp = 8, kExpWarp0 = 9, kExpWarps = 6;
+constexpr int kOWarp = kExpWarp0 + kExpWarps;
+constexpr int kShThreads = (kRowWarps + 2 + kExpWarps) * 32;          // 512
 constexpr int kExpThreads = 32 * kExpWarps;
 constexpr int kRowThreads = 32 * kRowWarps;
 constexpr int kShQ = 128;                                             // query rows per CTA (TMEM lanes)
@@ -314,8 +317,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
   const int n = (int)((long long)(split + 1) * np / sa.nsplit) - p0;
   // page k of the split into ring stage k % 3 (the control thread); the step prologue never writes
   // shared pages, so the first ones are requested before the programmatic wait
-  auto issue = [&](int k) -> bool {
-    const int pid = __ldcg(sa.hist_pt + p0 + k);
+  auto issue_pid = [&](int k, int pid) -> bool {
     if (pid < 0 || pid >= lv.n_int2) {
       flag(lv.status, OSCAR_STATUS_BAD_PAGE);
       return false;
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
                    B_(kBarRing + k % kShStages), l2_evict_first());
     return true;
   };
+  auto issue = [&](int k) -> bool { return issue_pid(k, __ldcg(sa.hist_pt + p0 + k)); };
   if (w == kCtlWarp) {
     if (lane == 0) {
       mbar_init_n(B_(kBarRing + 0), 1);
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       mbar_init_n(B_(kBarBufFree + 0), 1);
       mbar_init_n(B_(kBarBufFree + 1), 1);
       mbar_init_n(B_(kBarBufFree + 2), 1);
-      mbar_init_n(B_(kBarFinal), 1);
+      mbar_init_n(B_(kBarFinal), 2);                // both issuing threads
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       *failed = 0;
       bool ok = true;
@@ -422,10 +425,9 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
   // running softmax state of a row warp's rows over its half of the tokens (warps 0-3 write the partials)
   float m = -INFINITY, lsum = 0.f, zacc0 = 0.f, zacc1 = 0.f;
   if (w == kCtlWarp) {
-    // ---- control: the MMAs of every page and the ring's bulk copies (one thread) ----------------------
+    // ---- control: the S MMAs of every page and the ring's bulk copies (one thread) --------------------
     if (lane == 0) {
-      const uint32_t p_a = smem_addr(smem + kOffP);
-      const uint32_t kh_a = smem_addr(smem + kOffKh), vt_a = smem_addr(smem + kOffVt);
+      const uint32_t kh_a = smem_addr(smem + kOffKh);
       auto issue_s = [&](int i) {                  // S_G = Q_G K_G^T into TMEM columns 128 (i % 2) + 64 G
         const int b = i & 1, kb3 = i % kBufs;
 #pragma unroll
@@ -449,14 +451,17 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           issue_s(0);
         }
       }
+      int pid_ahead = kShStages < n ? __ldcg(sa.hist_pt + p0 + kShStages) : 0;
       for (int i = 0; i < n && ok; ++i) {
         if (*failed) {
           ok = false;
           break;
         }
-        const int kb3 = i % kBufs;
         // page i is expanded (its wait preceded S of page i): its ring stage takes page i + 3
-        if (i + kShStages < n && !issue(i + kShStages)) {
+        // the page id was loaded one iteration ahead: its global-memory latency stays off this thread's path
+        const int pid = pid_ahead;
+        pid_ahead = i + kShStages + 1 < n ? __ldcg(sa.hist_pt + p0 + i + kShStages + 1) : 0;
+        if (i + kShStages < n && !issue_pid(i + kShStages, pid)) {
           ok = false;
           break;
         }
@@ -468,7 +473,27 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           tc_fence_after();
           issue_s(i + 1);
         }
-        ok = mbar_wait(B_(kBarPReady), i & 1);     // the rows' weights of page i
+      }
+      if (!ok) {
+        if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);
+        *failed = 1;
+      }
+      umma_commit(B_(kBarFinal));                  // every MMA of this thread completes before TMEM is released
+      mbar_wait(B_(kBarFinal), 0);
+    }
+    __syncwarp();
+  } else if (w == kOWarp) {
+    // ---- O += P V^T of every page, once the rows' weights are in (one thread) -----------------------------
+    if (lane == 0) {
+      const uint32_t p_a = smem_addr(smem + kOffP), vt_a = smem_addr(smem + kOffVt);
+      bool ok = !*failed;
+      for (int i = 0; i < n && ok; ++i) {
+        if (*failed) {
+          ok = false;
+          break;
+        }
+        const int kb3 = i % kBufs;
+        ok = mbar_wait(B_(kBarPReady), i & 1);     // the rows' weights of page i (S of page i is complete)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -479,7 +504,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
                  umma_desc(vt_a + kb3 * kVtBytes + G * 8 * kVtSbo + 2 * kk * 128, 128, kVtSbo),
                  i > 0 || kk > 0);
         umma_commit(B_(kBarODone + (i & 1)));
-        umma_commit(B_(kBarBufFree + kb3));
+        umma_commit(B_(kBarBufFree + kb3));      // S of page i completed before its weights were written
       }
       if (!ok) {
         if (!*failed) flag(lv.status, OSCAR_STATUS_TIMEOUT);

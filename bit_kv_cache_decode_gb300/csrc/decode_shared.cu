@@ -72,7 +72,9 @@ constexpr int kOffMeta = kOffP + 4 * kPBytes;         // kBufs buffers
 constexpr int kRowc = 16;                             // per row: F, Z0, Z1, then (l, z0, z1) sums of slices 1-3
 constexpr int kOffRowc = kOffMeta + kBufs * kMetaBytes;   // [128 rows][kRowc]
 constexpr int kOffMx = kOffRowc + kShQ * kRowc * 4;   // [2 pages][4 slices][128 rows] partial maxima
-constexpr int kOffBar = kOffMx + 2 * kSlices * kShQ * 4;
+constexpr int kPidTable = 256;                        // page ids of a split held in shared memory
+constexpr int kOffPid = kOffMx + 2 * kSlices * kShQ * 4;
+constexpr int kOffBar = kOffPid + kPidTable * 4;
 constexpr int kNumBars = 21;
 constexpr int kShSmem = kOffBar + kNumBars * 8 + 16 + 1024;          // + TMEM address, flag, alignment slack
 static_assert(kOffKh >= kShStages * kBlockBytes, "ring fits");
@@ -326,8 +328,14 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
                    B_(kBarRing + k % kShStages), l2_evict_first());
     return true;
   };
-  auto issue = [&](int k) -> bool { return issue_pid(k, __ldcg(sa.hist_pt + p0 + k)); };
+  // the split's page ids, read once by the control warp (beyond the table: from global memory)
+  const int* pid_s = reinterpret_cast<const int*>(smem + kOffPid);
+  auto page_id = [&](int k) -> int { return k < kPidTable ? pid_s[k] : __ldcg(sa.hist_pt + p0 + k); };
+  auto issue = [&](int k) -> bool { return issue_pid(k, page_id(k)); };
   if (w == kCtlWarp) {
+    for (int k = lane; k < n && k < kPidTable; k += 32)
+      const_cast<int*>(pid_s)[k] = __ldcg(sa.hist_pt + p0 + k);
+    __syncwarp();
     if (lane == 0) {
       mbar_init_n(B_(kBarRing + 0), 1);
       mbar_init_n(B_(kBarRing + 1), 1);
@@ -451,17 +459,14 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           issue_s(0);
         }
       }
-      int pid_ahead = kShStages < n ? __ldcg(sa.hist_pt + p0 + kShStages) : 0;
       for (int i = 0; i < n && ok; ++i) {
         if (*failed) {
           ok = false;
           break;
         }
         // page i is expanded (its wait preceded S of page i): its ring stage takes page i + 3
-        // the page id was loaded one iteration ahead: its global-memory latency stays off this thread's path
-        const int pid = pid_ahead;
-        pid_ahead = i + kShStages + 1 < n ? __ldcg(sa.hist_pt + p0 + i + kShStages + 1) : 0;
-        if (i + kShStages < n && !issue_pid(i + kShStages, pid)) {
+        // (the page id comes from the shared-memory table: no global-memory latency on this thread's path)
+        if (i + kShStages < n && !issue(i + kShStages)) {
           ok = false;
           break;
         }

@@ -122,9 +122,15 @@ __device__ __forceinline__ float* part_row(const DecodeWorkspace& ws, int b, int
 }
 
 // (scale', zero') of both groups of one row from its four compact-format index bytes.
+// Byte k of m as an exact float, without an integer conversion: the float 2^23 + byte, minus 2^23.
+__device__ __forceinline__ float byte_f(uint32_t m, int k) {
+  return __uint_as_float(__byte_perm(m, 0x4B000000u, 0x7540u | (uint32_t)k)) - 8388608.f;
+}
 __device__ __forceinline__ void u8_row_meta(uint32_t m, const float (&c)[6], float2& g0, float2& g1) {
-  g0 = u8_scale_zero(m & 0xffu, (m >> 8) & 0xffu, c[0], c[1], c[2]);
-  g1 = u8_scale_zero((m >> 16) & 0xffu, m >> 24, c[3], c[4], c[5]);
+  // the same values as u8_scale_zero: scale' = (mx8 - mn8) E (an exact difference), zero' = fma(mn8, D, -T)
+  const float mn0 = byte_f(m, 0), mx0 = byte_f(m, 1), mn1 = byte_f(m, 2), mx1 = byte_f(m, 3);
+  g0 = make_float2(__fmul_rn(mx0 - mn0, c[2]), __fmaf_rn(mn0, c[1], -c[0]));
+  g1 = make_float2(__fmul_rn(mx1 - mn1, c[5]), __fmaf_rn(mn1, c[4], -c[3]));
 }
 
 // Codebook format: the fp16 value 1024 + k_c of code c from the codebook bytes `lut` (k_0 .. k_3):

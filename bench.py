@@ -593,9 +593,13 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
                       f"{dt:.1f} s; numpy fp64 unpack + dequantise + exact softmax"}
 
 
+REFERENCE_SAMPLE_TOKENS = 32768
+
+
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: one step = the oracle's decode of one layer of the workload for a
-    bounded sample of kv heads (host cores)."""
+    """The oracle as the reference arm: one step = the oracle's decode of a bounded sample of the workload
+    on the host cores: one kv head of layer 0 over at most the first 32,768 tokens of the context (a request
+    of that length), so that a run of --steps K stays within minutes."""
     if rank != 0:
         return None
     from oracle import attention as A
@@ -603,7 +607,8 @@ def run_reference(args, rank, world):
     from oracle import rotation
     import synth
     w = WORKLOADS[args.workload]
-    L, H, hq = w["ctx"], w["hkv"], w["hq"]
+    ctx = w["ctx"][1] if isinstance(w["ctx"], tuple) else w["ctx"]
+    L, H, hq = min(ctx, REFERENCE_SAMPLE_TOKENS), w["hkv"], w["hq"]
     seed = 1234
     # build layer 0 of the workload with the oracle itself (one kv head per step sample)
     geo = P.PoolGeometry(hkv=1, meta_format=args.meta_format)
@@ -632,7 +637,9 @@ def run_reference(args, rank, world):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, **w},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"layer 0, 1 of {H} kv heads, context {L}, per step"},
+                             "sample": f"layer 0, 1 of {H} kv heads ({hq // H} q heads), the first {L} tokens of "
+                                       f"the {ctx}-token context as one request, per step; numpy fp64 unpack + "
+                                       f"dequantise + exact softmax"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -7,7 +7,7 @@ Sources:
 * Page A, "OSCAR 的设计思路": four 2-bit values are packed into one byte; the
   INT2 read path restores values from scale and zero point.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 * Asymmetric INT2 with 4 levels: zero = group minimum (a float offset, not an
   integer zero point), scale = (max - min) / 3, code = round((y - zero)/scale)
   clamped to [0, 3], round half to even.

@@ -1,5 +1,5 @@
 // Log-sum-exp merge of a decode call's partial results (sm_103a), shared by
-// both decode algorithms (the online-softmax merge of split partials: Page A of
+// both decode algorithms (the online-softmax merge of split partials: the news article "超越 TurboQuant…" of
 // the OSCAR write-ups, "online softmax"; partial = (m, l, acc) with l and acc
 // relative to 2^m, m in log2 units).
 //

@@ -8,12 +8,12 @@ reader can check each step against it by eye.
 
 Sources (cited by page title and section throughout):
 
-* Page A -- "超越 TurboQuant，显存压力终于得到缓解！Together AI 最新论文 OSCAR
-  直接挑战 TurboQuant…" (news article, m.youleyou.com). Sections used:
+* the news article "超越 TurboQuant，显存压力终于得到缓解！Together AI 最新论文 OSCAR
+  直接挑战 TurboQuant…" (m.youleyou.com), cited as news article "超越 TurboQuant…". Sections used:
   "OSCAR 的出发点", "OSCAR 的设计思路" (token pool, write/read path),
   "精度表现" (bits-per-element budget).
-* Page B -- "Together AI 开源 OSCAR：一种用于长上下文 LLM 服务的注意力感知 2
-  位 KV 缓存量化系统" (MarkTechPost article, Chinese translation). Sections
+* the MarkTechPost article "Together AI 开源 OSCAR：一种用于长上下文 LLM 服务的注意力感知 2
+  位 KV 缓存量化系统" (Chinese translation), cited as MarkTechPost article "Together AI 开源 OSCAR…". Sections
   used: "OSCAR 有何不同做法" (logit-error identity, C_Q, C_S, R_K, R_V,
   Lemma 1, bit reversal), "服务系统：混合精度缓存布局" (S0, W, clipping,
   G_K = 64, per-token asymmetric INT2, R_V absorbed into the projections),

@@ -1,11 +1,11 @@
 """Exact decode attention over the mixed-precision cache, and the segmented merge (fp64).
 
 Sources:
-* Page A, "OSCAR 的设计思路": at decode time the cache is split into a BF16
+* The news article "超越 TurboQuant…", section "OSCAR 的设计思路": at decode time the cache is split into a BF16
   segment (sink and recent, handled by a BF16 kernel) and an INT2 segment
   (unpack, restore scale/zero, accumulate in floating point), and the two
   results are combined with an online-softmax merge.
-* Page B, "服务系统：混合精度缓存布局": the INT2 read path dequantises and
+* The MarkTechPost article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局": the INT2 read path dequantises and
   inverse-rotates before attention; the value rotation R_V may be absorbed
   offline into the projection weights so no online inverse rotation of V is
   needed.

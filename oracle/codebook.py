@@ -1,7 +1,7 @@
 """Lloyd-Max 4-level codebook variant of the INT2 history (test infrastructure: only the tests,
 the smoke check and the bench's CPU baseline use this package).
 
-Source: Page A, "总结与展望" (the project's latest code replaces the uniform 2-bit levels by a
+Source: the news article "超越 TurboQuant…", section "总结与展望" (the project's latest code replaces the uniform 2-bit levels by a
 stronger Lloyd-Max codebook inside the attention-aware rotation). The pages give no more than
 that sentence, so everything below is this library's reading, stated in full:
 

@@ -1,12 +1,12 @@
 """Byte-exact model of the paged mixed-precision token pool.
 
 Sources:
-* Page A, "OSCAR 的设计思路": one token pool per request laid out as
+* The news article "超越 TurboQuant…", section "OSCAR 的设计思路": one token pool per request laid out as
   BF16 sink (64 tokens) | INT2 history | BF16 recent (256 tokens); a new token
   is written into the recent window and, as decoding proceeds, the oldest
   recent token is rotated, clipped, quantised, packed and demoted into the INT2
   history; the pool stays compatible with paged KV and prefix caching.
-* Page B, "服务系统：混合精度缓存布局": sink = first S0 = 64 tokens, recent =
+* The MarkTechPost article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局": sink = first S0 = 64 tokens, recent =
   the last W = 256 tokens before the current position, history = everything
   in between, stored as INT2 after rotation and clipping.
 

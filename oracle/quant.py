@@ -1,10 +1,10 @@
 """Clip, per-token asymmetric INT2 quantiser, dequantiser and 2-bit packing.
 
 Sources:
-* Page B, "服务系统：混合精度缓存布局": on the write path every token is
+* The MarkTechPost article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局": on the write path every token is
   rotated, clipped to calibration-derived percentile thresholds, then quantised
   with per-token asymmetric INT2 over groups of G_K = 64 channels.
-* Page A, "OSCAR 的设计思路": four 2-bit values are packed into one byte; the
+* The news article "超越 TurboQuant…", section "OSCAR 的设计思路": four 2-bit values are packed into one byte; the
   INT2 read path restores values from scale and zero point.
 
 Readings taken where the pages are silent:

@@ -1,6 +1,6 @@
 """Offline rotation construction (fp64).
 
-Page B, section "OSCAR 有何不同做法":
+The MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法":
 
 * Key error is measured in the attention logits, and
   ||Q K^T - Q Khat^T||_F^2 = tr((K - Khat) Q^T Q (K - Khat)^T), so the key
@@ -12,7 +12,7 @@ Page B, section "OSCAR 有何不同做法":
   P_br is the bit-reversal permutation; R_K = U_Q H_Had P_br and
   R_V = U_S H_Had P_br.
 
-Page A, section "OSCAR 的设计思路", names the same three factors (U aligns the
+The news article "超越 TurboQuant…", section "OSCAR 的设计思路", names the same three factors (U aligns the
 attention-relevant directions, Hadamard spreads outliers, bit reversal
 balances the INT2 groups) and says thresholds and rotations are fixed per layer
 and head.
@@ -29,7 +29,7 @@ Conventions (readings where the pages are silent):
   with no causal mask.
 * Clip thresholds: tau[j] = quantile_c(|X_cal R|[:, j]) per rotated channel,
   numpy's default (linear) interpolation; c = 0.96 for K, 0.92 for V
-  (Page B, visual guide step 4 table and "服务系统" section).
+  (the MarkTechPost article "Together AI 开源 OSCAR…", visual guide step 4 table and "服务系统" section).
 """
 from __future__ import annotations
 

@@ -72,7 +72,7 @@ def test_no_history_is_textbook_attention():
 
 @pytest.mark.parametrize("v_absorbed", [False, True])
 def test_history_is_dequantise_inverse_rotate_attend(v_absorbed):
-    # Page B, "服务系统：混合精度缓存布局": the INT2 read path unpacks, dequantises and
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "服务系统：混合精度缓存布局": the INT2 read path unpacks, dequantises and
     # inverse-rotates before attention (V-absorbed mode skips V's inverse rotation).
     geo = P.PoolGeometry(hkv=2)
     prm = _params(22, 2)
@@ -146,7 +146,7 @@ def _logit_errors(model: str, seeds=range(3)):
 
 
 def test_attention_aware_rotation_wins_when_keys_share_query_directions():
-    # Page B, "OSCAR 有何不同做法": the key rotation should come from the query
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法": the key rotation should come from the query
     # covariance, because the logit error is weighted by Q^T Q. When the keys'
     # large components lie along the queries' principal directions, U_Q maps
     # them onto a few channels that H_Had then spreads evenly, while a
@@ -157,8 +157,8 @@ def test_attention_aware_rotation_wins_when_keys_share_query_directions():
 
 
 def test_any_rotation_beats_naive_on_massive_channels():
-    # Page B, "为什么 INT2 KV 缓存量化很难": a few channels with huge values dominate
-    # the per-group scale; rotations spread them (Page A, "OSCAR 的设计思路": Hadamard
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "为什么 INT2 KV 缓存量化很难": a few channels with huge values dominate
+    # the per-group scale; rotations spread them (the news article "超越 TurboQuant…", section "OSCAR 的设计思路": Hadamard
     # disperses outliers). On axis-aligned outlier channels both rotations beat naive INT2.
     e = _logit_errors("axis")
     assert e["hadamard"] < 0.5 * e["naive"]

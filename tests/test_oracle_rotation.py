@@ -33,7 +33,7 @@ def test_hadamard_orthonormal_symmetric():
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_lemma1_hadamard_equalises_diagonal(seed):
-    # Page B, "OSCAR 有何不同做法", Lemma 1: every diagonal entry of H^T Lambda H equals tr(Lambda)/d.
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法", Lemma 1: every diagonal entry of H^T Lambda H equals tr(Lambda)/d.
     rng = np.random.default_rng(seed)
     lam = np.diag(rng.exponential(size=D) * 10.0 ** rng.uniform(-3, 3, size=D))
     h = rotation.hadamard(D)
@@ -71,7 +71,7 @@ def test_bitrev_matrix_action():
 
 @pytest.mark.parametrize("gsize", [2, 4, 8, 16, 32, 64, 128])
 def test_bitrev_every_group_gets_every_tier(gsize):
-    # Page B, "OSCAR 有何不同做法": after P_br each power-of-two group holds one
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法": after P_br each power-of-two group holds one
     # representative of every level of the importance order. Source channel i
     # (sorted by importance) is in tier i // (d / gsize); output block b holds
     # positions [b*gsize, (b+1)*gsize).
@@ -154,7 +154,7 @@ def test_composite_rotation_orthogonal_and_preserves_logits():
 
 
 def test_logit_error_identity():
-    # Page B, "OSCAR 有何不同做法": ||Q K^T - Q Khat^T||_F^2 = tr((K - Khat) Q^T Q (K - Khat)^T)
+    # The MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法": ||Q K^T - Q Khat^T||_F^2 = tr((K - Khat) Q^T Q (K - Khat)^T)
     rng = np.random.default_rng(1)
     q = rng.standard_normal((40, D))
     k = rng.standard_normal((70, D))

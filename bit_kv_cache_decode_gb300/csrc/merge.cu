@@ -1,6 +1,6 @@
 // Log-sum-exp merge of a decode call's partial results (sm_103a), shared by
-// both decode algorithms (the online-softmax merge of split partials: the news article "超越 TurboQuant…" of
-// the OSCAR write-ups, "online softmax"; partial = (m, l, acc) with l and acc
+// both decode algorithms (the news article "超越 TurboQuant…", section "OSCAR 的设计思路":
+// the split partials are combined by an online softmax; partial = (m, l, acc) with l and acc
 // relative to 2^m, m in log2 units).
 //
 // grid = (Hq, B), block = 256: one CTA per (request, query head). The head's

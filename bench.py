@@ -384,7 +384,7 @@ def run_ours(args, rank: int, world: int, device):
                       else "k_int2_simt (INT2 history)") +
                      ", CUDA events around each launch in an eager copy of the timed steps",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
+                     "frac": achieved / peak, "frac_of_nominal_7900_gbs": achieved / 7900.0, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
                      "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
         "gpu_launches": launches_per_layer * nl * args.steps,
         "clocks": clk.summary(),

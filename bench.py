@@ -429,8 +429,8 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
 # 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
 # CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "7f988f4bae3b199bfb1aa14839dd68bac64a2e8a11aaddf796b727f0a36f2879",
-                      "bytes_per_launch": 66764800 + 107264}
+NCU_DECODE_TRAFFIC = {"sources_sha256": "2a070bc26a5f824753b45e21bb29e4940788332b18e49f70b95fdcaefc709fe0",
+                      "bytes_per_launch": 66766080 + 133376}
 
 
 # the sources the fused decode kernel is compiled from (its file and the headers it includes)

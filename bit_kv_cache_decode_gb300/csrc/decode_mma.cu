@@ -16,10 +16,12 @@
 //  * logits: A = codes [16 tokens x 16 channels of one group], B = query
 //    fragments [16 channels x 8 columns], column = (head, hi or lo fp16 part
 //    of the query) of a 4-head n-tile, one accumulator per channel group; the
-//    code c of channel ch is shifted into mantissa bits 6-7 or 8-9 and fed as
-//    the fp16 value 1024 + c*64 or 1024 + c*256 (one LOP3: mask | 0x6400),
-//    whose constant part and scale the query prologue folded into the
-//    fragments and the per-head offsets;
+//    code c at bit position 2p of a 16-bit half is masked in place (one AND)
+//    and fed as the fp16 subnormal c 4^(p mod 4) 2^-24; the query prologue
+//    folded 4^-(p mod 4) and a power of two 2^sigma into the fragments (which
+//    keeps the products clear of the subnormal range) and the logit scale
+//    takes back 2^24 (codebook pools feed 1024 + k_c and subtract per-head
+//    offsets instead);
 //  * P.Vhat: A = codes [16 channels x 16 tokens] (the V page layout pairs two
 //    tokens in one 32-bit word, so mask | 0x6400 and one HFMA2 give the exact
 //    fp16 codes of one channel for two tokens), B = p * scale [16 tokens x 8
@@ -476,9 +478,9 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             a2 = exact_codes(cb_lookup(vlut, vw[2] >> sh), 4);
             a3 = exact_codes(cb_lookup(vlut, vw[3] >> sh), 4);
           } else {
-            // the masked code bits as an fp16 subnormal, exactly c 4^k 2^-24: no bias (the accumulators stay
-            // the size of the result) and no conversion; the power of two 2^24 4^-k is applied to the
-            // accumulators once, after the loop
+            // exact fp16 codes c from the masked bits: (1024 + c 4^k) 4^-k - 1024 4^-k (a V operand fed as
+            // subnormals, as the logits' K operand is, loses accuracy: p * scale is too small to lift the
+            // products clear of the subnormal range)
             const uint32_t m = 0x00030003u << (2 * k);
             a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
             a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
@@ -534,11 +536,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     float v[16];                                  // channels 16g .. 16g + 15
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      // codes were fed as c 4^k 2^-24, k = mt & 3 (the codebook build feeds its levels / 256 and its
-      // P operand carries the 256)
-      const float un = 1.f;
-      v[mt] = fmaf(grp ? acc[nt][mt][1] : acc[nt][mt][0], un, zs);
-      v[8 + mt] = fmaf(grp ? acc[nt][mt][3] : acc[nt][mt][2], un, zs);
+      // the accumulators hold sum p s c exactly scaled (the codebook build feeds its levels / 256 and its
+      // P operand carries the 256): add the zero-point part
+      v[mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
+      v[8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
     }
     float4* dst = reinterpret_cast<float4*>(ca + (w * 8 + head) * kCaStride + 16 * g);
 #pragma unroll

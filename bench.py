@@ -560,6 +560,19 @@ def run_e2e_eager(wl, args, device, start_lens):
             "path": "pinned host -> device copy, direct C-ABI calls from Python, device -> host copy"}
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's numpy can use: its BLAS pool (matrix products) as the environment sets it,
+    else one per core this process may run on; the elementwise steps run on one of them."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return int(v)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
     """The CPU oracle's decode of one layer of the workload (unpack, dequantise, fp64 exact softmax),
     from the pool bytes of layer 0, on the host cores; KV heads are added until the time budget is used."""
@@ -578,7 +591,7 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
            for c in wl["cals"][:H]]
     q = np.random.default_rng(seed).standard_normal((hq, 128)).astype(np.float32)
     Lnow = int(L)
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     heads = 0
     while heads < H:
         A.decode_request(q, Lnow, pm, wl["hist_np"][0], wl["bf16_np"][0], prm, True, 1 / math.sqrt(128),
@@ -587,8 +600,9 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    busy = (time.process_time() - c0) / dt
     units = Lnow * heads / H            # KV tokens of one layer-step, scaled by the share of heads done
-    return {"value": units / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+    return {"value": units / dt, "unit": UNIT, "cores": oracle_threads(), "cpu_s_per_wall_s": busy, "kind": "oracle",
             "sample": f"layer 0, {heads} of {H} kv heads ({heads * hq // H} q heads), context {Lnow}, "
                       f"{dt:.1f} s; numpy fp64 unpack + dequantise + exact softmax"}
 
@@ -627,16 +641,18 @@ def run_reference(args, rank, world):
     q = synth.queries(seed, 0, 0, hq // H)
     for _ in range(args.warmup):
         A.decode_request(q, L, pm, np.arange(nh), np.arange(5), prm, True, synth.sm_scale())
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     for _ in range(args.steps):
         A.decode_request(q, L, pm, np.arange(nh), np.arange(5), prm, True, synth.sm_scale())
+    busy = (time.process_time() - c0) / (time.perf_counter() - t0)
     dt = (time.perf_counter() - t0) / args.steps
     value = L / H / dt        # one kv head of one layer per step: L/H of the layer's KV tokens
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": args.workload, **w},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "cpu_s_per_wall_s": busy,
+                             "kind": "oracle",
                              "sample": f"layer 0, 1 of {H} kv heads ({hq // H} q heads), the first {L} tokens of "
                                        f"the {ctx}-token context as one request, per step; numpy fp64 unpack + "
                                        f"dequantise + exact softmax"},

@@ -35,4 +35,6 @@ def test_reference_arm_line(monkeypatch):
     assert res["value"] > 0 and res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["cores"] >= 1
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
     assert "first 1024 tokens" in res["cpu_baseline"]["sample"]
+    # cores: the threads numpy may use; the measured CPU seconds per wall second cannot exceed them by much
+    assert res["cpu_baseline"]["cpu_s_per_wall_s"] <= res["cpu_baseline"]["cores"] * 1.1 + 0.1
     assert bench.run_reference(args, 1, 2) is None            # other ranks print nothing

@@ -573,9 +573,10 @@ def oracle_threads() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
-    """The CPU oracle's decode of one layer of the workload (unpack, dequantise, fp64 exact softmax),
-    from the pool bytes of layer 0, on the host cores; KV heads are added until the time budget is used."""
+def cpu_baseline(wl, seed, device, min_s: float = 10.0, budget_s: float = 20.0):
+    """The CPU oracle's decode of layer 0 of the workload (unpack, dequantise, fp64 exact softmax), from
+    the pool bytes the GPU wrote, on the host cores: its kv heads in turn until about min_s seconds of
+    work are done."""
     from oracle import attention as A
     from oracle import pool as P
     cache, H, hq, L = wl["cache"], wl["H"], wl["hq"], int(wl["lens"][0])
@@ -591,20 +592,30 @@ def cpu_baseline(wl, seed, device, budget_s: float = 20.0):
            for c in wl["cals"][:H]]
     q = np.random.default_rng(seed).standard_normal((hq, 128)).astype(np.float32)
     Lnow = int(L)
+    heads, dt, busy = time_head_decodes(
+        lambda hd: A.decode_request(q, Lnow, pm, wl["hist_np"][0], wl["bf16_np"][0], prm, True, 1 / math.sqrt(128),
+                                    kv_heads=[hd]), H, min_s, budget_s)
+    units = Lnow * heads / H            # KV tokens of one layer-step per H head decodes
+    return {"value": units / dt, "unit": UNIT, "cores": oracle_threads(), "cpu_s_per_wall_s": busy, "kind": "oracle",
+            "sample": f"layer 0, {heads} kv-head decodes (its {H} kv heads in turn, {hq // H} q heads each), "
+                      f"context {Lnow}, {dt:.1f} s; numpy fp64 unpack + dequantise + exact softmax"}
+
+
+def time_head_decodes(decode_head, H: int, min_s: float, budget_s: float):
+    """Run decode_head(0), decode_head(1), ..., cycling over the H kv heads, until at least min_s seconds
+    have passed (and at least one decode ran), stopping early once budget_s is used. Returns (decodes,
+    wall seconds, process CPU seconds per wall second: an upper bound on the busy cores, since BLAS
+    threads spinning between products count too)."""
     t0, c0 = time.perf_counter(), time.process_time()
-    heads = 0
-    while heads < H:
-        A.decode_request(q, Lnow, pm, wl["hist_np"][0], wl["bf16_np"][0], prm, True, 1 / math.sqrt(128),
-                         kv_heads=[heads])
-        heads += 1
-        if time.perf_counter() - t0 > budget_s:
+    n = 0
+    while True:
+        decode_head(n % H)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_s or el > budget_s:
             break
     dt = time.perf_counter() - t0
-    busy = (time.process_time() - c0) / dt
-    units = Lnow * heads / H            # KV tokens of one layer-step, scaled by the share of heads done
-    return {"value": units / dt, "unit": UNIT, "cores": oracle_threads(), "cpu_s_per_wall_s": busy, "kind": "oracle",
-            "sample": f"layer 0, {heads} of {H} kv heads ({heads * hq // H} q heads), context {Lnow}, "
-                      f"{dt:.1f} s; numpy fp64 unpack + dequantise + exact softmax"}
+    return n, dt, (time.process_time() - c0) / dt
 
 
 REFERENCE_SAMPLE_TOKENS = 32768

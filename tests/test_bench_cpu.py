@@ -38,3 +38,20 @@ def test_reference_arm_line(monkeypatch):
     # cores: the threads numpy may use; the measured CPU seconds per wall second cannot exceed them by much
     assert res["cpu_baseline"]["cpu_s_per_wall_s"] <= res["cpu_baseline"]["cores"] * 1.1 + 0.1
     assert bench.run_reference(args, 1, 2) is None            # other ranks print nothing
+
+
+def test_cpu_baseline_sampler_cycles_heads_until_min_time():
+    import time
+    seen = []
+
+    def fake(hd):
+        seen.append(hd)
+        time.sleep(0.01)
+
+    n, dt, busy = bench.time_head_decodes(fake, 3, 0.08, 5.0)
+    assert n == len(seen) and n >= 4 and dt >= 0.08
+    assert seen == [i % 3 for i in range(n)]            # the layer's kv heads in turn
+    assert busy >= 0.0                                   # (a BLAS pool left spinning by earlier work counts)
+    seen.clear()
+    n, dt, _ = bench.time_head_decodes(fake, 3, 10.0, 0.03)
+    assert 1 <= n <= 10 and dt < 1.0                     # the budget ends it long before the minimum time

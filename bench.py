@@ -134,7 +134,7 @@ class ClockSampler:
 
 
 def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_capacity: int = 64, algo: int = 1,
-                   meta: str = "f16"):
+                   meta: str = "f16", v_explicit: bool = False):
     import torch
     import bit_kv_cache_decode_gb300 as osc
     import synth
@@ -162,7 +162,8 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
         else:
             bf16_pt[r] = 5 * r + np.arange(5)
     cfg = osc.CacheConfig(num_layers=nl, num_kv_heads=H, num_q_heads=hq, num_int2_pages=n_int2,
-                          num_bf16_pages=n_bf16, max_batch=B, max_splits=512, v_mode=osc.V_ABSORBED,
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=512,
+                          v_mode=osc.V_EXPLICIT if v_explicit else osc.V_ABSORBED,
                           meta_format=META_FORMATS[meta])
     cache = osc.OscarCache(cfg, device=device)
     cache.set_decode_algo(algo)
@@ -288,8 +289,11 @@ def run_ours(args, rank: int, world: int, device):
     seed = replica_seed(rank)
     total_steps = args.warmup + args.steps
     mixed = isinstance(WORKLOADS[args.workload]["ctx"], tuple)
+    # every leg appends one token per step: the eager step before capture, the graph's warm-up and timed
+    # steps, the profiled eager steps, and the warm-up and timed steps of the two end-to-end legs
+    appends = 1 + (args.warmup - 1 + args.steps) + args.steps + 2 * (args.warmup + args.steps)
     wl = build_workload(args.workload, seed, device, with_bf16=not (args.no_bf16 or mixed),
-                        steps_capacity=3 * total_steps + 16, algo=args.algo, meta=args.meta_format)
+                        steps_capacity=appends + 16, algo=args.algo, meta=args.meta_format)
     cache, nl, B, H, hq = wl["cache"], wl["layers"], wl["B"], wl["H"], wl["hq"]
     stream = torch.cuda.current_stream()
     sm = synth.sm_scale()
@@ -367,7 +371,8 @@ def run_ours(args, rank: int, world: int, device):
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic",
+        "dtype": "f32 (bf16 I/O)" if args.algo == 0 else "fp16 MMA operands, f32 accumulate (bf16 I/O)",
+        "data": "synthetic",
         "config": {"workload": args.workload, **{k: v for k, v in WORKLOADS[args.workload].items()},
                    "head_dim": 128, "sink": 64, "recent": 256, "group": 64, "page": 64, "v_mode": "absorbed",
                    "storage": STORAGE[args.meta_format], "meta_format": args.meta_format,
@@ -401,7 +406,11 @@ def run_ours(args, rank: int, world: int, device):
                           "algorithmic_bytes": moved, "gbs": moved / (pf["ms"] / 1e3) / 1e9,
                           "frac_of_peak": moved / (pf["ms"] / 1e3) / 1e9 / peak}
     res["e2e"] = run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq)
+    if cache.get_status() != 0:
+        raise RuntimeError("device status error during the end-to-end steps")
     res["e2e_eager"] = run_e2e_eager(wl, args, device, start_lens=seq.cpu().numpy())
+    if cache.get_status() != 0:
+        raise RuntimeError("device status error during the eager end-to-end steps")
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(wl, seed, device, budget_s=args.cpu_budget)
     return res

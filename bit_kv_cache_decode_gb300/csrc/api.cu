@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -141,13 +142,21 @@ void composite_rotation_fragments(const float* U, uint32_t* frag) {
       }
 }
 
-int g_configured = 0;
+// Kernel attributes (dynamic shared memory limits, carveout) belong to one device's context: they are
+// set once per device, the first time a call needs the kernels on that device.
+constexpr int kMaxConfiguredDevices = 64;
+std::mutex g_configure_mu;
+bool g_configured[kMaxConfiguredDevices];
 
 int configure_once() {
-  if (g_configured) return OSCAR_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxConfiguredDevices) return OSCAR_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_configure_mu);
+  if (g_configured[dev]) return OSCAR_OK;
   int rc = configure_write_path_kernels();
   if (rc == OSCAR_OK) rc = configure_decode_kernels();
-  if (rc == OSCAR_OK) g_configured = 1;
+  if (rc == OSCAR_OK) g_configured[dev] = true;
   return rc;
 }
 

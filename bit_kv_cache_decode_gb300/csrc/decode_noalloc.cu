@@ -1,9 +1,8 @@
 // Decode attention that allocates no device memory (sm_103a).
 //
-// Some callers cannot call cudaMalloc: code that runs while a CUDA graph is
-// being captured (allocation is not a capturable stream operation), serving
-// engines whose allocator already owns all device memory and forbids side
-// allocations, and hosts that may not allocate on a latency-critical path.
+// Some callers cannot call cudaMalloc: serving engines whose allocator already
+// owns all device memory and forbids side allocations, and hosts that may not
+// allocate on a latency-critical path (cudaMalloc can synchronise the device).
 // oscar_decode_attention needs a caller-allocated workspace for its scratch
 // (rotated queries, query fragments and sums, split partials, status word);
 // this entry point runs the same kernels with that scratch taken from a fixed

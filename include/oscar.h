@@ -370,11 +370,10 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
 #define OSCAR_ERR_TOO_LARGE (-7)  /* the call needs more than the fixed device scratch */
 
 /* Decode attention that allocates nothing. The paper has no counterpart: this
- * entry point exists for callers that cannot call cudaMalloc, such as code
- * that runs while a CUDA graph is being captured (allocation is not a
- * capturable operation), serving engines whose allocator already owns all
- * device memory and forbids side allocations, and hosts that may not allocate
- * on a latency-critical path.
+ * entry point exists for callers that cannot call cudaMalloc, such as serving
+ * engines whose allocator already owns all device memory and forbids side
+ * allocations, and hosts that may not allocate on a latency-critical path
+ * (cudaMalloc can synchronise the device and take milliseconds).
  *
  * It computes exactly what oscar_decode_attention computes, with the same
  * arguments, except:

@@ -6,6 +6,8 @@ the oracle's fp64 attention over the pool bytes the GPU wrote.
 
 * Qwen3-8B full stack: 36 layers x (32 q / 8 kv heads), batch 1, 102,400-token
   context; layers 0, 17 and 35 checked after two steps.
+* the same stack in explicit-V mode (raw V in the cache, rotated back in the
+  merge); layers 0 and 35 checked after two steps.
 * Qwen3-4B batched: 36 layers, batch 32 x 102,400 tokens sharing a 92,160-token
   prefix (the shared-prefix kernel for the shared pages); layers 0 and 35,
   requests 0, 13 and 31 checked after two steps.
@@ -20,6 +22,7 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import bench
+    import bit_kv_cache_decode_gb300 as osc
     from gpu_cases import DEV, bf16_ulp, pool_from_device
 import synth
 from oracle import attention as A
@@ -55,8 +58,8 @@ def _check(wl, qn, on, lens, layers, requests):
         cs = wl["cals"][layer * H:(layer + 1) * H]
         prm = [P.HeadParams(c["U_K"], c["U_V"], c["tau_K"], c["tau_V"]) for c in cs]
         for r in requests:
-            ref, _ = A.decode_request(qn[layer, r], int(lens[r]), pm, wl["hist_np"][r], wl["bf16_np"][r], prm, True,
-                                      synth.sm_scale())
+            ref, _ = A.decode_request(qn[layer, r], int(lens[r]), pm, wl["hist_np"][r], wl["bf16_np"][r], prm,
+                                      wl["cfg"].v_mode == osc.V_ABSORBED, synth.sm_scale())
             got = on[layer, r]
             slack = TOL * np.abs(ref).max(axis=-1, keepdims=True)
             bad = np.abs(got - ref) > bf16_ulp(ref) + slack
@@ -67,6 +70,13 @@ def test_qwen3_8b_36_layers_100k_context():
     wl = bench.build_workload("qwen3_8b_36l", 1234, DEV, with_bf16=False, steps_capacity=8, algo=1)
     qn, on, lens = _run_steps(wl, 2, 77)
     _check(wl, qn, on, lens, layers=(0, 17, 35), requests=(0,))
+
+
+def test_qwen3_8b_36_layers_100k_context_explicit_v():
+    wl = bench.build_workload("qwen3_8b_36l", 1235, DEV, with_bf16=False, steps_capacity=8, algo=1, v_explicit=True)
+    assert wl["cfg"].v_mode == osc.V_EXPLICIT
+    qn, on, lens = _run_steps(wl, 2, 79)
+    _check(wl, qn, on, lens, layers=(0, 35), requests=(0,))
 
 
 def test_qwen3_4b_batch32_shared_prefix_100k_context():

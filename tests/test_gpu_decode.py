@@ -13,62 +13,14 @@ pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     import bit_kv_cache_decode_gb300 as osc
-    from gpu_cases import (DEV, bf16_ulp, head_params, pool_from_device, queries, row_rel_err, to_dev_bf16, tokens,
-                           upload_params, with_codebooks)
+    from gpu_cases import (DEV, bf16_ulp, build_decode_case as _build, pool_from_device, queries, row_rel_err,
+                           to_dev_bf16, tokens)
 import synth
 from oracle import attention as A
 from oracle import pool as P
 
 TOL = 2e-3
 ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma")]
-
-
-def _build(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64, meta="f16"):
-    """Prefill B requests on the GPU. With shared_prefix > 0 all requests share their first
-    `shared_prefix` tokens (sink page and the history pages covering them)."""
-    B = len(lens)
-    nh = [max(0, (L - 320 + 63) // 64) for L in lens]
-    mhp = max(1, max(nh))
-    shp = (shared_prefix - 64) // 64 if shared_prefix else 0           # shared history pages
-    n_int2 = shp + sum(n - shp for n in nh) + 1
-    n_bf16 = 1 + 4 * B if shared_prefix else 5 * B
-    rng = np.random.default_rng(seed)
-    perm_i, perm_b = rng.permutation(n_int2).astype(np.int32), rng.permutation(n_bf16).astype(np.int32)
-    hist_pt = np.full((B, mhp), -1, np.int32)
-    bf16_pt = np.zeros((B, 5), np.int32)
-    oi, ob = shp, (1 if shared_prefix else 0)
-    for r in range(B):
-        hist_pt[r, :shp] = perm_i[:shp]
-        hist_pt[r, shp:nh[r]] = perm_i[oi:oi + nh[r] - shp]
-        oi += nh[r] - shp
-        if shared_prefix:
-            bf16_pt[r, 0] = perm_b[0]
-            bf16_pt[r, 1:] = perm_b[ob:ob + 4]
-            ob += 4
-        else:
-            bf16_pt[r] = perm_b[ob:ob + 5]
-            ob += 5
-    cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=hkv * gq, num_int2_pages=n_int2,
-                          num_bf16_pages=n_bf16, max_batch=B, max_splits=max_splits, v_mode=v_mode,
-                          meta_format={"f16": 0, "u8": 1, "cb": 2}[meta])
-    cache = osc.OscarCache(cfg, device=DEV)
-    cache.set_decode_algo(algo)
-    prm = head_params(seed, 0, hkv)
-    if meta == "cb":
-        prm = with_codebooks(seed, 0, prm)
-    upload_params(cache, 0, prm)
-    ks, vs = [], []
-    for r, L in enumerate(lens):
-        k, v = tokens(seed, 0, hkv, L, extra=r + 1)
-        if shared_prefix:
-            k0, v0 = tokens(seed, 0, hkv, shared_prefix, extra=0)
-            k[:shared_prefix], v[:shared_prefix] = k0, v0
-        ks.append(k)
-        vs.append(v)
-    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-    cache.quantize_prefill(0, to_dev_bf16(np.concatenate(ks)), to_dev_bf16(np.concatenate(vs)), cu, hist_pt, bf16_pt)
-    assert cache.get_status() == 0
-    return cache, prm, hist_pt, bf16_pt
 
 
 def _check(cache, prm, hist_pt, bf16_pt, lens, gq, v_mode, seed, out_dtype=1, kv_heads=None, shared_pages=0):

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "liboscar.so")
 OK = 0
 ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_STATUS, ERR_TIMEOUT, ERR_NOT_ORTHOGONAL = -1, -2, -3, -4, -5, -6
 ERR_TOO_LARGE = -7
-STATUS_BAD_PAGE, STATUS_BAD_SEQLEN, STATUS_TIMEOUT = 1, 2, 4
+STATUS_BAD_PAGE, STATUS_BAD_SEQLEN, STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_SATURATED = 1, 2, 4, 8, 16
 V_ABSORBED, V_EXPLICIT = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 KIND_K, KIND_V = 0, 1

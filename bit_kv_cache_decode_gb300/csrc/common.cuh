@@ -71,6 +71,15 @@ struct LayerView {
 
 __device__ __forceinline__ void flag(int* status, int bits) { atomicOr(status, bits); }
 
+// NaN or infinity (false for every finite float)
+__device__ __forceinline__ bool nonfinite(float x) { return !(fabsf(x) <= 3.402823466e38f); }
+// one of the two bf16 values of a 32-bit word is a NaN or an infinity (exponent bits all set)
+__device__ __forceinline__ bool bf16x2_nonfinite(uint32_t w) {
+  return ((w & 0x7F80u) == 0x7F80u) || ((w & 0x7F800000u) == 0x7F800000u);
+}
+// fp16 metadata that would not fit: |x| beyond the largest finite fp16 (or NaN)
+__device__ __forceinline__ bool fp16_saturates(float x) { return !(fabsf(x) <= 65504.f); }
+
 __device__ __forceinline__ const uint8_t* int2_block(const LayerView& lv, int page, int head) {
   return lv.int2 + ((size_t)page * lv.hkv + head) * lv.blk_bytes;
 }

@@ -141,10 +141,11 @@ __device__ __forceinline__ uint32_t pack16(uint4 b) {
 
 // Rotate (or take) and quantise the staged 16-row tile xs, one 64-channel group (8 n-tiles) at a
 // time; codes and fp16 metadata of every row go to codes_s [16][128] (one code per byte) and
-// meta_s [16][2] (fp16 scale, zero per group).
+// meta_s [16][2] (fp16 scale, zero per group). Rows whose bit is set in `checked` (the history rows)
+// flag non-finite rotated values and saturated fp16 metadata in `status`.
 __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotate, const __nv_bfloat16* xs,
                                               const float* tau_s, const float* mc, const float* cb,
-                                              uint8_t* codes_s, uint32_t* meta_s) {
+                                              uint8_t* codes_s, uint32_t* meta_s, int* status, uint32_t checked) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   uint32_t a[8][4];
   if (rotate) {
@@ -189,14 +190,18 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
         acc[j][3] = __uint_as_float(w8 & 0xffff0000u);
       }
     }
-    // clip, then per row half rr min / max over the quad's 64 values of the group
+    // clip (flagging non-finite values first), then per row half rr min / max over the quad's 64 values of
+    // the group
+    bool bad = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float tau = tau_s[8 * (8 * G + j) + 2 * t + (e & 1)];
+        bad |= nonfinite(acc[j][e]) && ((checked >> (g + 8 * (e >> 1))) & 1u);
         acc[j][e] = fminf(fmaxf(acc[j][e], -tau), tau);
       }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) flag(status, OSCAR_STATUS_NONFINITE);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       float mn = acc[0][2 * rr], mx = mn;
@@ -217,6 +222,8 @@ __device__ __forceinline__ void quantize_tile(const uint32_t* frag_s, bool rotat
       if (mc == nullptr) {                          // fp16 (scale, zero), or (range, zero) with a codebook
         const float diff = __fsub_rn(mx, mn);
         const float scale = cb != nullptr ? diff : __fdiv_rn(diff, 3.0f);
+        if ((fp16_saturates(scale) || fp16_saturates(mn)) && t == 0 && ((checked >> (g + 8 * rr)) & 1u))
+          flag(status, OSCAR_STATUS_SATURATED);
         const __half2 sz = __halves2half2(__float2half_rn(sat_fp16(scale)), __float2half_rn(sat_fp16(mn)));
         sq = __low2float(sz);
         zq = __high2float(sz);
@@ -313,10 +320,13 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
       const int r = __ffs(m) - 1;
       const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
       __nv_bfloat16* out = bf16_row(lv, page, h, kind, row);
-      reinterpret_cast<uint2*>(out)[lane] = reinterpret_cast<const uint2*>(xs + r * kXStride)[lane];
+      const uint2 x = reinterpret_cast<const uint2*>(xs + r * kXStride)[lane];
+      if (__any_sync(0xffffffffu, bf16x2_nonfinite(x.x) || bf16x2_nonfinite(x.y)) && lane == 0)
+        flag(lv.status, OSCAR_STATUS_NONFINITE);
+      reinterpret_cast<uint2*>(out)[lane] = x;
     }
     if (hist_rows != 0) {
-      quantize_tile(frag_s, rotate, xs, tau_s, mc, cbc, codes_s, meta_s);
+      quantize_tile(frag_s, rotate, xs, tau_s, mc, cbc, codes_s, meta_s, lv.status, hist_rows);
       __syncwarp();
       // packed codes: 16 rows x 8 words of 16 codes; word idx = lane + 32 j
 #pragma unroll

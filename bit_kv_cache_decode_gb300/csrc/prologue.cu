@@ -112,7 +112,11 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
   // scheduled; it waits for this grid before it reads anything this kernel writes.
   pdl_wait();
   pdl_launch_dependents();
-  if (r >= 1 && r <= gq && do_q) u = *reinterpret_cast<const uint4*>(q + ((size_t)b * lv.hq + h * gq + r - 1) * kD + 8 * c8);
+  if (r >= 1 && r <= gq && do_q) {
+    u = *reinterpret_cast<const uint4*>(q + ((size_t)b * lv.hq + h * gq + r - 1) * kD + 8 * c8);
+    if (bf16x2_nonfinite(u.x) || bf16x2_nonfinite(u.y) || bf16x2_nonfinite(u.z) || bf16x2_nonfinite(u.w))
+      flag(lv.status, OSCAR_STATUS_NONFINITE);
+  }
   {
     const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
     float4* dst = reinterpret_cast<float4*>(rows + r * kTileStride + 8 * c8);
@@ -138,7 +142,8 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
 #pragma unroll
       for (int r = 0; r < 4; ++r) y[r] = rows[rot_channel(lane, r)];
       quantize_pack_row(y, tau_s, int2_block_w(lv, hpage, h), hh % kP, kind,
-                        lv.meta_u8 ? meta_consts(lv, h, kind) : nullptr, lv.meta_cb ? cb_consts(lv, h, kind) : nullptr);
+                        lv.meta_u8 ? meta_consts(lv, h, kind) : nullptr, lv.meta_cb ? cb_consts(lv, h, kind) : nullptr,
+                        lv.status);
     }
   } else if (do_q) {
     constexpr int kQWarps = kPrologueWarps - 1;
@@ -163,7 +168,10 @@ __global__ void __launch_bounds__(kPrologueWarps * 32, 1)
     return;
   }
   const __nv_bfloat16* src = (kind == OSCAR_KIND_K ? k : v) + ((size_t)b * lv.hkv + h) * kD;
-  reinterpret_cast<uint2*>(bf16_row(lv, page, h, kind, row))[lane] = reinterpret_cast<const uint2*>(src)[lane];
+  const uint2 x = reinterpret_cast<const uint2*>(src)[lane];
+  if (__any_sync(0xffffffffu, bf16x2_nonfinite(x.x) || bf16x2_nonfinite(x.y)) && lane == 0)
+    flag(lv.status, OSCAR_STATUS_NONFINITE);
+  reinterpret_cast<uint2*>(bf16_row(lv, page, h, kind, row))[lane] = x;
 }
 
 constexpr int kPrologueSmem = (kRFragWords + kTileFloats + kD) * 4 + 64;

@@ -83,10 +83,15 @@ __device__ __forceinline__ float sat_fp16(float x) { return fminf(fmaxf(x, -6550
 // thresholds indexed by rotated channel. mc: null for the fp16 (scale, zero) metadata, else the
 // kind's compact-format constants {T, D, E, 0} for groups 0 and 1 (8 floats). cb: null, or the kind's
 // codebook constants {k_0..k_3, theta_0..theta_2, 0} (codebook format: fp16 range and zero).
+// status: when not null, OSCAR_STATUS_NONFINITE is flagged for a non-finite input value and
+// OSCAR_STATUS_SATURATED for fp16 metadata stored saturated.
 __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const float* __restrict__ tau,
                                                   uint8_t* blk, int row, int kind, const float* __restrict__ mc,
-                                                  const float* __restrict__ cb = nullptr) {
+                                                  const float* __restrict__ cb = nullptr, int* status = nullptr) {
   const int lane = threadIdx.x & 31;
+  bool bad = false;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) bad |= nonfinite(y_in[r]);
   float y[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -106,6 +111,8 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
   if (mc == nullptr) {
     const float diff = __fsub_rn(mx, mn);
     const float scale = cb != nullptr ? diff : __fdiv_rn(diff, 3.0f);   // codebook format: the range
+    if (status != nullptr && (fp16_saturates(scale) || fp16_saturates(mn)) && (lane & 30) == 0)
+      flag(status, OSCAR_STATUS_SATURATED);
     s16 = __float2half_rn(sat_fp16(scale));
     z16 = __float2half_rn(sat_fp16(mn));
     sq = __half2float(s16);
@@ -124,6 +131,7 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
     }
     byte |= ((unsigned)c) << (2 * rev2(r));
   }
+  if (status != nullptr && __any_sync(0xffffffffu, bad) && lane == 0) flag(status, OSCAR_STATUS_NONFINITE);
   const int b = rev5(lane);
   if (kind == OSCAR_KIND_K) blk[kKCodesOff + row * (kD / 4) + b] = (uint8_t)byte;
   else blk[v_byte_off(row, b)] = (uint8_t)byte;

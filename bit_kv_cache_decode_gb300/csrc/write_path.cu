@@ -52,7 +52,7 @@ __global__ void k_pack_rotated(LayerView lv, int kind, const float* __restrict__
   for (int r = 0; r < 4; ++r) y[r] = x[rot_channel(lane, r)];
   const float* tau = lv.params + (size_t)h * kParamFloats + (kind == OSCAR_KIND_K ? kTauKOff : kTauVOff);
   quantize_pack_row(y, tau, int2_block_w(lv, page, h), row, kind, lv.meta_u8 ? meta_consts(lv, h, kind) : nullptr,
-                    lv.meta_cb ? cb_consts(lv, h, kind) : nullptr);
+                    lv.meta_cb ? cb_consts(lv, h, kind) : nullptr, lv.status);
 }
 
 // ---------------------------------------------------------------------------

@@ -90,6 +90,13 @@ extern "C" {
 #define OSCAR_STATUS_BAD_PAGE    1    /* a page id outside [0, pages)         */
 #define OSCAR_STATUS_BAD_SEQLEN  2    /* seq_len < 1 or beyond its page table */
 #define OSCAR_STATUS_TIMEOUT     4    /* a bounded wait expired               */
+#define OSCAR_STATUS_NONFINITE   8    /* a NaN or infinity in an input q, k or v row (or in a
+                                         rotated row the writers quantise); the row is still
+                                         written: NaN and infinities are clipped like any value */
+#define OSCAR_STATUS_SATURATED  16    /* an fp16 scale, range or zero of a history group fell
+                                         outside +-65504 and was stored saturated (fp16 and
+                                         codebook metadata formats; clip thresholds that keep
+                                         every group inside +-65504 rule it out) */
 
 /* V handling (MarkTechPost article, "服务系统：混合精度缓存布局": R_V may be
  * absorbed offline into the value/output projections). */

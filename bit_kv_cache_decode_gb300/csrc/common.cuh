@@ -124,10 +124,19 @@ __device__ __forceinline__ __nv_bfloat16* bf16_row(const LayerView& lv, int page
          (size_t)kind * kP * kD + (size_t)row * kD;
 }
 
-// Byte offset, inside a page block, of packed byte b (0..31) of row t in the V codes region:
-// rows (2p, 2p+1) share 64 bytes; channel octet o = b/2 is a 32-bit word whose low half is row 2p.
-__device__ __forceinline__ int v_byte_off(int t, int b) {
-  return kVCodesOff + (t >> 1) * 64 + (b >> 1) * 4 + (t & 1) * 2 + (b & 1);
+// V codes are channel-major: channel c's 64 codes occupy bytes [16 c, 16 c + 16) of the V region, the
+// code of row t at bits 2 (t % 16) of the 32-bit word t / 16 (the transposed codes packed like K rows).
+constexpr int kVChanBytes = kP / 4;            // 16
+__device__ __forceinline__ int v_word_off(int c, int t) { return kVCodesOff + c * kVChanBytes + (t >> 4) * 4; }
+
+// Set the 2-bit V field of (channel c, row t) of a page block to `code`, leaving the other rows' bits:
+// two atomics on the field's 32-bit word, so that writers of other rows of the same word may run at the
+// same time.
+__device__ __forceinline__ void v_set_code(uint8_t* blk, int c, int t, unsigned code) {
+  unsigned* w = reinterpret_cast<unsigned*>(blk + v_word_off(c, t));
+  const int sh = 2 * (t & 15);
+  atomicAnd(w, ~(3u << sh));
+  if (code != 0u) atomicOr(w, code << sh);
 }
 
 // 7-bit bit reversal (d = 128).

@@ -154,6 +154,9 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   int& any_timeout = *reinterpret_cast<int*>(smem + kWarps * kStages * kBlockBytes + kWarps * kStages * 8);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
+  // rows g and g + 8 of every 16-token tile are tokens tok_lo = (0, 8, 1, 9, 2, 10, 3, 11)[g] and tok_hi =
+  // tok_lo + 4 of the tile: the order in which the P.Vhat B fragments meet the channel-major V code words
+  const int tok_lo = (g >> 1) + 8 * (g & 1), tok_hi = tok_lo + 4;
   const int gq = lv.hq / lv.hkv;
   constexpr bool U8 = FMT == kFmtU8, CB = FMT == kFmtCB;
   if (tid == 0) any_timeout = 0;
@@ -313,7 +316,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       float lg[4][NT][2];
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {
-        const int r0 = 16 * mt + g, r1 = r0 + 8;
+        const int r0 = 16 * mt + tok_lo, r1 = 16 * mt + tok_hi;
         // words t (channels 16t .. 16t+15, group 0) and t + 4 (group 1) of rows r0, r1
         const uint32_t kx[2] = {*reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r0 * 32 + 4 * t),
                                 *reinterpret_cast<const uint32_t*>(blk + kKCodesOff + r0 * 32 + 16 + 4 * t)};
@@ -415,9 +418,14 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       }
 
       // ---- P.Vhat over the page's four 16-token tiles -----------------------------------
+      // weights p * scale of the page's 64 tokens: the B fragments of the four 16-token tiles, whose k order
+      // (k = 2u + e is token 16 kt + u + 8 e) is that of the channel-major code words; rows g and g + 8 of
+      // logits tile kt are the tokens tok_lo(g), tok_hi(g) that the transposes place at k = (2t', 2t'+1)
+      // and (2t'+8, 2t'+9)
+      uint32_t bf[4][NT][2];
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
-        const int r0 = 16 * kt + g, r1 = r0 + 8;
+        const int r0 = 16 * kt + tok_lo, r1 = 16 * kt + tok_hi;
         float2 sv00, sv01, sv10, sv11;
         if constexpr (U8) {
           u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kVMetaOffU8 + r0 * 4), vmc, sv00, sv01);
@@ -440,7 +448,6 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);
           if (r1 >= ntok) sv10 = sv11 = make_float2(0.f, 0.f);
         }
-        uint32_t bf[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float pa = fast_exp2(lg[kt][nt][0] - mrun[nt]);
@@ -448,47 +455,41 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           lsum[nt] += pa + pb;
           zacc[nt][0] = fmaf(pa, sv00.y, fmaf(pb, sv10.y, zacc[nt][0]));
           zacc[nt][1] = fmaf(pa, sv01.y, fmaf(pb, sv11.y, zacc[nt][1]));
-          bf[nt][0] = movmatrix_t(pack_f16x2(pa * sv00.x, pa * sv01.x));
-          bf[nt][1] = movmatrix_t(pack_f16x2(pb * sv10.x, pb * sv11.x));
+          // lane (g, t): the weights of token row g (rows 0-7) and g + 8 of the tile for head t, groups 0 and 1;
+          // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'
+          bf[kt][nt][0] = movmatrix_t(pack_f16x2(pa * sv00.x, pa * sv01.x));
+          bf[kt][nt][1] = movmatrix_t(pack_f16x2(pb * sv10.x, pb * sv11.x));
         }
-        const uint2 wab = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t) * 64 + 8 * g);
-        const uint2 wcd = *reinterpret_cast<const uint2*>(blk + kVCodesOff + (8 * kt + t + 4) * 64 + 8 * g);
-        // exact codes (the accumulators stay the size of the result: the tensor cores' fp32
-        // accumulation truncates, so a large constant part would grow the error with the split length)
-        const uint32_t wah = wab.x >> 8, wbh = wab.y >> 8, wch = wcd.x >> 8, wdh = wcd.y >> 8;
-        // codebook format: each word's bytes reordered to (row 2p, row 2p+1) pairs per channel quartet,
-        // so that one shift puts a channel's two codes 8 bits apart, as the lookup's selector wants them
-        uint32_t vw[4];
-        if constexpr (CB) {
-          vw[0] = __byte_perm(wab.x, 0u, 0x3120u);
-          vw[1] = __byte_perm(wab.y, 0u, 0x3120u);
-          vw[2] = __byte_perm(wcd.x, 0u, 0x3120u);
-          vw[3] = __byte_perm(wcd.y, 0u, 0x3120u);
-        }
+      }
+      // P.Vhat: tile mt takes channels 16 g + mt (rows g) and 16 g + 8 + mt (rows g + 8). A channel's 16-byte
+      // code row holds tokens 16 kt .. 16 kt + 15 in word kt: the k pair (2t, 2t+1) = tokens (t, t + 8) is
+      // code position t of the two halves, (2t+8, 2t+9) = tokens (t + 4, t + 12) position t + 4
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int k = mt & 3;
+      for (int mt = 0; mt < 8; ++mt) {
+        const uint4 ca = *reinterpret_cast<const uint4*>(blk + kVCodesOff + (16 * g + mt) * kVChanBytes);
+        const uint4 cb = *reinterpret_cast<const uint4*>(blk + kVCodesOff + (16 * g + 8 + mt) * kVChanBytes);
+        const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w}, wb[4] = {cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          const uint32_t xa = wa[kt] >> (2 * t), xb = wb[kt] >> (2 * t);
           uint32_t a0, a1, a2, a3;
           if constexpr (CB) {
-            // k_c / 256 exactly: (1024 + k_c) / 256 - 4 (the P operand carries range * 256 / 255, which keeps
-            // it clear of fp16 subnormals)
-            const int sh = 2 * k + (mt < 4 ? 0 : 16);
-            a0 = exact_codes(cb_lookup(vlut, vw[0] >> sh), 4);
-            a1 = exact_codes(cb_lookup(vlut, vw[1] >> sh), 4);
-            a2 = exact_codes(cb_lookup(vlut, vw[2] >> sh), 4);
-            a3 = exact_codes(cb_lookup(vlut, vw[3] >> sh), 4);
+            // level k_c / 256 exactly: the two codes (bits 0-1 and 16-17, or 8-9 and 24-25) gathered 8 bits
+            // apart as the lookup's selector wants them
+            a0 = exact_codes(cb_lookup(vlut, (xa & 3u) | ((xa >> 8) & 0x300u)), 4);
+            a1 = exact_codes(cb_lookup(vlut, (xb & 3u) | ((xb >> 8) & 0x300u)), 4);
+            a2 = exact_codes(cb_lookup(vlut, ((xa >> 8) & 3u) | ((xa >> 16) & 0x300u)), 4);
+            a3 = exact_codes(cb_lookup(vlut, ((xb >> 8) & 3u) | ((xb >> 16) & 0x300u)), 4);
           } else {
-            // exact fp16 codes c from the masked bits: (1024 + c 4^k) 4^-k - 1024 4^-k (a V operand fed as
-            // subnormals, as the logits' K operand is, loses accuracy: p * scale is too small to lift the
-            // products clear of the subnormal range)
-            const uint32_t m = 0x00030003u << (2 * k);
-            a0 = exact_codes(and_or(mt < 4 ? wab.x : wah, m, kMagic), k);   // channel 16g + mt, tokens 2t, 2t+1
-            a1 = exact_codes(and_or(mt < 4 ? wab.y : wbh, m, kMagic), k);   // channel 16g + 8 + mt
-            a2 = exact_codes(and_or(mt < 4 ? wcd.x : wch, m, kMagic), k);   // tokens 2t + 8, 2t + 9
-            a3 = exact_codes(and_or(mt < 4 ? wcd.y : wdh, m, kMagic), k);
+            // exact fp16 codes: position t at bits 0-1 becomes 1024 + c, then c; position t + 4 at bits 8-9
+            // becomes 1024 + 256 c, then c
+            a0 = exact_codes(and_or(xa, 0x00030003u, kMagic), 0);
+            a1 = exact_codes(and_or(xb, 0x00030003u, kMagic), 0);
+            a2 = exact_codes(and_or(xa, 0x03000300u, kMagic), 4);
+            a3 = exact_codes(and_or(xb, 0x03000300u, kMagic), 4);
           }
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[nt][0], bf[nt][1]);
+          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[kt][nt][0], bf[kt][nt][1]);
         }
       }
     } else if (i == 0) {

@@ -277,18 +277,17 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     mk[2 * kP] = b.x;
     mk[3 * kP] = b.y;
   }
-  for (int vi = et; vi < (kD / 8) * (kP / 8); vi += kExpThreads) {   // V: octet o (channels 8o ..), tokens 8 kb ..
-    const int o = vi & 15, kb = vi >> 4;          // a quarter warp: 8 consecutive octets (consecutive code words)
-    uint32_t x[4];
+  for (int c = et; c < kD; c += kExpThreads) {   // V: channel c, its 64 tokens (one 16-byte load, channel-major)
+    const uint4 x4 = *reinterpret_cast<const uint4*>(blk + kVCodesOff + c * kVChanBytes);
+    const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp)
-      x[pp] = *reinterpret_cast<const uint32_t*>(blk + kVCodesOff + (4 * kb + pp) * 64 + 4 * o);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {                // row i of core matrix (o, kb): channel 8o + i, tokens 8kb ..
-      uint32_t c[4];
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) c[pp] = vval(x[pp], i);
-      *reinterpret_cast<uint4*>(vt + o * kVtSbo + kb * 128 + i * 16) = make_uint4(c[0], c[1], c[2], c[3]);
+    for (int kb = 0; kb < kP / 8; ++kb) {        // row c % 8 of core matrix (c / 8, kb): tokens 8 kb .. 8 kb + 7
+      // the 8 codes of half kb % 2 of word kb / 2 (token 8 kb + u at bits 2u); the high half takes them shifted
+      // by one code, so that code position 2v gives the fp16 pair (token 2v, token 2v + 1)
+      const uint32_t hw = (xw[kb >> 1] >> (16 * (kb & 1))) & 0xffffu;
+      const uint32_t x2 = hw | ((hw >> 2) << 16);
+      *reinterpret_cast<uint4*>(vt + (c >> 3) * kVtSbo + kb * 128 + (c & 7) * 16) =
+          make_uint4(vval(x2, 0), vval(x2, 2), vval(x2, 4), vval(x2, 6));
     }
   }
 }

@@ -163,12 +163,12 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
     __syncthreads();
     {
       const int c = tid, g = c / kG;
-      const int woff = kVCodesOff + (c / 8) * 4, sh = 2 * (c % 8);
+      const int woff = kVCodesOff + c * kVChanBytes;      // channel-major V codes
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) acc[hh] *= alpha[hh];
       for (int tk = 0; tk < ntok; ++tk) {
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + (tk >> 1) * 64);
-        const unsigned ci = (word >> ((tk & 1) * 16 + sh)) & 3u;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + (tk >> 4) * 4);
+        const unsigned ci = (word >> (2 * (tk & 15))) & 3u;
         const float code = CB ? lvk[8 + ci] : (float)ci;
         const float vhat = fmaf(msz[1][tk][g].x, code, msz[1][tk][g].y);
 #pragma unroll

@@ -328,21 +328,49 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
     if (hist_rows != 0) {
       quantize_tile(frag_s, rotate, xs, tau_s, mc, cbc, codes_s, meta_s, lv.status, hist_rows);
       __syncwarp();
-      // packed codes: 16 rows x 8 words of 16 codes; word idx = lane + 32 j
+      if (kind == OSCAR_KIND_K) {
+        // packed codes: 16 rows x 8 words of 16 codes; word idx = lane + 32 j
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int idx = lane + 32 * j, r = idx >> 3, wd = idx & 7;
-        const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
-        if (!((hist_rows >> r) & 1u)) continue;
-        const uint32_t word = pack16(*reinterpret_cast<const uint4*>(codes_s + r * kD + 16 * wd));
-        uint8_t* blk = int2_block_w(lv, page, h);
-        if (kind == OSCAR_KIND_K) {
-          *reinterpret_cast<uint32_t*>(blk + kKCodesOff + row * (kD / 4) + 4 * wd) = word;
-        } else {
-          // bytes 4 wd .. 4 wd + 3 = octets 2 wd, 2 wd + 1; each octet is the row's 16-bit half of a pair word
-          *reinterpret_cast<uint16_t*>(blk + v_byte_off(row, 4 * wd)) = (uint16_t)(word & 0xffffu);
-          *reinterpret_cast<uint16_t*>(blk + v_byte_off(row, 4 * wd + 2)) = (uint16_t)(word >> 16);
+        for (int j = 0; j < 4; ++j) {
+          const int idx = lane + 32 * j, r = idx >> 3, wd = idx & 7;
+          const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
+          if (!((hist_rows >> r) & 1u)) continue;
+          const uint32_t word = pack16(*reinterpret_cast<const uint4*>(codes_s + r * kD + 16 * wd));
+          *reinterpret_cast<uint32_t*>(int2_block_w(lv, page, h) + kKCodesOff + row * (kD / 4) + 4 * wd) = word;
         }
+      } else {
+        // channel-major V: lane takes channels lane + 32 j; the tile's rows are gathered per 32-bit word
+        // (16 rows of one channel of one page) and each word is updated by two atomics on its own fields
+        // (a word may also hold rows of a neighbouring tile, written by another warp)
+        unsigned* wp[4] = {nullptr, nullptr, nullptr, nullptr};
+        unsigned msk[4] = {0u, 0u, 0u, 0u}, val[4] = {0u, 0u, 0u, 0u};
+        for (int r = 0; r < kTileRows; ++r) {
+          if (!((hist_rows >> r) & 1u)) continue;  // warp-uniform
+          const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
+          uint8_t* blk = int2_block_w(lv, page, h);
+          const int sh = 2 * (row & 15);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c = lane + 32 * j;
+            unsigned* w = reinterpret_cast<unsigned*>(blk + v_word_off(c, row));
+            if (w != wp[j]) {
+              if (wp[j] != nullptr) {
+                atomicAnd(wp[j], ~msk[j]);
+                atomicOr(wp[j], val[j]);
+              }
+              wp[j] = w;
+              msk[j] = val[j] = 0u;
+            }
+            msk[j] |= 3u << sh;
+            val[j] |= (unsigned)codes_s[r * kD + c] << sh;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (wp[j] != nullptr) {
+            atomicAnd(wp[j], ~msk[j]);
+            atomicOr(wp[j], val[j]);
+          }
       }
       {
         const int r = lane >> 1, G = lane & 1;

@@ -133,8 +133,12 @@ __device__ __forceinline__ void quantize_pack_row(const float (&y_in)[4], const 
   }
   if (status != nullptr && __any_sync(0xffffffffu, bad) && lane == 0) flag(status, OSCAR_STATUS_NONFINITE);
   const int b = rev5(lane);
-  if (kind == OSCAR_KIND_K) blk[kKCodesOff + row * (kD / 4) + b] = (uint8_t)byte;
-  else blk[v_byte_off(row, b)] = (uint8_t)byte;
+  if (kind == OSCAR_KIND_K) {
+    blk[kKCodesOff + row * (kD / 4) + b] = (uint8_t)byte;
+  } else {                                       // channel-major: one 2-bit field per channel
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v_set_code(blk, rot_channel(lane, r), row, (byte >> (2 * rev2(r))) & 3u);
+  }
   if (lane < 2) {                                // lane 0: group 0, lane 1: group 1
     if (mc == nullptr) {
       __half2 sz = __halves2half2(s16, z16);

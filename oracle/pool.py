@@ -28,11 +28,9 @@ bytes (5120 for P = 64, d = 128, G = 64), in this order:
 
 1. K codes, token-major: row t occupies bytes [t*d/4, (t+1)*d/4), the token's
    codes packed with channel j in byte j//4 at bits 2*(j%4).
-2. V codes, token-pair interleaved: rows (2p, 2p+1) share d/2 bytes starting at
-   p*d/2; inside them, for channel octet o (channels 8o..8o+7) four bytes
-   [row 2p bytes (2o, 2o+1) | row 2p+1 bytes (2o, 2o+1)] of the same packed
-   form, i.e. one little-endian 32-bit word whose low half is row 2p and high
-   half row 2p+1.
+2. V codes, channel-major: channel c occupies bytes [c*P/4, (c+1)*P/4) of the
+   region, the code of row t in byte t//4 at bits 2*(t%4); i.e. the transposed
+   codes V^T packed like K rows, four rows per byte.
 3. K metadata: row t at t*(d/G)*m, m = 4 (fp16 format, the default): for each
    group g, fp16 scale then fp16 zero; m = 2 (compact u8 format): for each group
    g, the byte mn8 then the byte mx8 (see ``quant``: indices on the group's grid
@@ -109,13 +107,22 @@ class PoolModel:
         g = self.geo
         return rows[:, None] * (g.d // 4) + np.arange(g.d // 4)[None, :]
 
-    def _v_byte_index(self, rows: np.ndarray) -> np.ndarray:
-        """[n, d/4] byte offsets (within the block) of rows' packed V bytes 0..d/4-1."""
+    def _v_field(self, rows: np.ndarray):
+        """([n, d] byte offsets within the block, [n, d] bit shifts) of rows' V codes, channel-major."""
         g = self.geo
-        p, e = np.divmod(rows, 2)
-        j = np.arange(g.d // 4)                  # packed byte index within the row
-        o, b = np.divmod(j, 2)                   # channel octet, byte within the row's half word
-        return g.codes_bytes + p[:, None] * (g.d // 2) + (4 * o + b)[None, :] + 2 * e[:, None]
+        c = np.arange(g.d)[None, :]
+        return g.codes_bytes + c * (g.page // 4) + (rows[:, None] // 4), 2 * (rows[:, None] % 4) + 0 * c
+
+    def _write_v_codes(self, blk: np.ndarray, rows: np.ndarray, codes: np.ndarray):
+        """Set the 2-bit V fields of rows (codes [n, d] in 0..3), leaving the other rows' bits."""
+        idx, sh = self._v_field(rows)
+        for i in range(len(rows)):               # rows in order: a later write of a row wins
+            keep = blk[idx[i]] & ~(np.uint8(3) << sh[i].astype(np.uint8))
+            blk[idx[i]] = keep | (codes[i].astype(np.uint8) << sh[i].astype(np.uint8))
+
+    def _read_v_codes(self, blk: np.ndarray, rows: np.ndarray) -> np.ndarray:
+        idx, sh = self._v_field(rows)
+        return ((blk[idx] >> sh.astype(np.uint8)) & 3).astype(np.uint8)
 
     def _meta_index(self, rows: np.ndarray, which: int) -> np.ndarray:
         """[n, (d/G)*m] byte offsets of rows' metadata; which = 0 for K, 1 for V."""
@@ -142,7 +149,7 @@ class PoolModel:
         rows = np.atleast_1d(np.asarray(rows, dtype=np.int64))
         blk = self.int2[page, head]
         blk[self._k_byte_index(rows)] = np.asarray(k_pack).reshape(len(rows), -1)
-        blk[self._v_byte_index(rows)] = np.asarray(v_pack).reshape(len(rows), -1)
+        self._write_v_codes(blk, rows, quant.unpack_codes(np.asarray(v_pack).reshape(len(rows), -1)))
         blk[self._meta_index(rows, 0)] = self._meta_bytes(np.reshape(k_s, (len(rows), -1)), np.reshape(k_z, (len(rows), -1)))
         blk[self._meta_index(rows, 1)] = self._meta_bytes(np.reshape(v_s, (len(rows), -1)), np.reshape(v_z, (len(rows), -1)))
 
@@ -152,7 +159,7 @@ class PoolModel:
         rows = np.atleast_1d(np.asarray(rows, dtype=np.int64))
         blk = self.int2[page, head]
         kc = quant.unpack_codes(blk[self._k_byte_index(rows)])
-        vc = quant.unpack_codes(blk[self._v_byte_index(rows)])
+        vc = self._read_v_codes(blk, rows)
         out = []
         for which in (0, 1):
             sz = np.ascontiguousarray(blk[self._meta_index(rows, which)]).view(self._meta_dtype())

@@ -106,22 +106,26 @@ def test_int2_block_layout_hand_built():
     v1 = quant.pack_codes(np.full((1, 128), 2, np.uint8))
     s = np.array([[0.5, 0.25]], np.float16)
     zz = np.array([[-1.0, 2.0]], np.float16)
+    v3 = quant.pack_codes(np.full((1, 128), 3, np.uint8))
+    pm.write_history(0, [5], 0, k0, z, z, v0, z, z)
     pm.write_history(0, [0], 0, k0, s, zz, v0, s, zz)
     pm.write_history(0, [1], 0, k0, z, z, v1, z, z)
+    pm.write_history(0, [5], 0, k0, z, z, v3, z, z)      # rewriting row 5 replaces only its own bits
     blk = pm.int2[0, 0]
     assert geo.block_bytes == 5120
     assert np.all(blk[0:32] == 0x55) and np.all(blk[32:64] == 0x55)   # K rows 0, 1 token-major
-    # V codes region: first pair of rows, octet 0: word = row0 half | row1 half << 16
-    w = blk[2048:2052].view("<u4")[0]
-    assert w == 0xAAAA5555
-    assert np.all(blk[2048:2048 + 64].view("<u4") == 0xAAAA5555)
+    # V codes region, channel-major: channel c's 16 bytes at 2048 + 16 c, rows 0-3 in byte 0 (row 0 at
+    # bits 0-1 = 1, row 1 at bits 2-3 = 2), rows 4-7 in byte 1 (row 5 at bits 2-3 = 3)
+    vreg = blk[2048:4096].reshape(128, 16)
+    assert np.all(vreg[:, 0] == 0b1001) and np.all(vreg[:, 1] == 0b1100) and np.all(vreg[:, 2:] == 0)
     # K metadata of row 0: fp16 scale, zero per group
     meta = blk[4096:4104].view(np.float16)
     assert list(meta) == [0.5, -1.0, 0.25, 2.0]
     assert list(blk[4608:4616].view(np.float16)) == [0.5, -1.0, 0.25, 2.0]
     # round trip through the reader
-    kc, ks, kz, vc, vs, vz = pm.read_history(0, [0, 1], 0)
-    assert np.all(kc == 1) and np.all(vc[0] == 1) and np.all(vc[1] == 2)
+    kc, ks, kz, vc, vs, vz = pm.read_history(0, [0, 1, 5, 2], 0)
+    assert np.all(kc[:3] == 1) and np.all(vc[0] == 1) and np.all(vc[1] == 2) and np.all(vc[2] == 3)
+    assert np.all(vc[3] == 0)
     assert list(ks[0]) == [0.5, 0.25] and list(vz[0]) == [-1.0, 2.0]
 
 

@@ -39,6 +39,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn KV tokens/s and achieved HBM GB/s vs GB300 peak, 100K ctx"
+ALGO_NAMES = {0: "simt", 1: "mma", 2: "tc"}
+DECODE_KERNEL_NAMES = {0: "k_int2_simt (INT2 history)", 1: "k_decode_mma (fused INT2 history + BF16 pages, mma.sync)",
+                       2: "k_decode_tc (INT2 history on tcgen05 + BF16 pages)"}
 UNIT = "KV tokens/s"
 HIST_BYTES = 80          # per history token per kv head: 32 B K codes + 32 B V codes + 16 B fp16 scale/zero
 HIST_BYTES_BY_META = {"f16": 80, "u8": 72, "cb": 80}   # the compact format stores 8 B of (mn8, mx8) per token
@@ -304,7 +307,7 @@ def run_ours(args, rank: int, world: int, device):
     seq = torch.from_numpy(wl["lens"].astype(np.int32)).to(device)
     # per layer, oscar_decode_step launches the step prologue (append with demotion, query rotation), then
     # the fused decode and the merge (mma), or the history kernel, the BF16 segment and the merge (simt)
-    launches_per_layer = (4 if wl["shp"] else 3) if args.algo == 1 else 4   # + the shared-prefix kernel
+    launches_per_layer = (4 if wl["shp"] else 3) if args.algo >= 1 else 4   # + the shared-prefix kernel
 
     def layers():
         for layer in range(nl):
@@ -377,16 +380,15 @@ def run_ours(args, rank: int, world: int, device):
                    "head_dim": 128, "sink": 64, "recent": 256, "group": 64, "page": 64, "v_mode": "absorbed",
                    "storage": STORAGE[args.meta_format], "meta_format": args.meta_format,
                    "l2": "inputs larger than L2 (%.2f GB of pool streamed per step)" % (step_bytes / 1e9),
-                   "parallelism": f"replicas x{world}", "decode_algo": "simt" if args.algo == 0 else "mma",
+                   "parallelism": f"replicas x{world}", "decode_algo": ALGO_NAMES[args.algo],
                    "launch": "one CUDA graph per step (oscar_decode_step%s per layer), new tokens copied in"
                              % ("_shared, %d shared history pages" % wl["shp"] if wl["shp"] else "")},
         "hbm": {"step_algorithmic_bytes": step_bytes, "step_gbs": step_bytes / (ms_step / 1e3) / 1e9,
                 "step_frac_of_peak": step_bytes / (ms_step / 1e3) / 1e9 / peak,
                 "step_unique_bytes": step_unique, "step_unique_gbs": step_unique / (ms_step / 1e3) / 1e9},
         "roofline": {"bound": "hbm", "kernel": ("k_decode_shared (shared-prefix pages, all requests) + "
-                                                if args.algo == 1 and wl["shp"] else "") +
-                     ("k_decode_mma (fused INT2 history + BF16 pages)" if args.algo == 1
-                      else "k_int2_simt (INT2 history)") +
+                                                if args.algo >= 1 and wl["shp"] else "") +
+                     DECODE_KERNEL_NAMES[args.algo] +
                      ", CUDA events around each launch in an eager copy of the timed steps",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_nominal_7900_gbs": achieved / 7900.0, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
@@ -435,22 +437,23 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
     return ms, n, lens0 + (args.steps - 1) // 2
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one fused decode launch of the
-# 102,400-token Qwen3-8B layer, from the ncu capture summarised under profiles/, and the digest of the
-# CUDA sources it was taken on: a changed kernel reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {"sources_sha256": "2a070bc26a5f824753b45e21bb29e4940788332b18e49f70b95fdcaefc709fe0",
-                      "bytes_per_launch": 66766080 + 133376}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch of the 102,400-token
+# Qwen3-8B layer, per decode kernel, from the ncu captures summarised under profiles/, with the digest of the
+# CUDA sources each was taken on: a kernel changed since reports null until it is captured again.
+NCU_DECODE_TRAFFIC = {}
+
+# the sources each decode kernel is compiled from (its file and the headers it includes)
+DECODE_KERNEL_SOURCES = {
+    1: ("decode_mma.cu", "bf16_page.cuh", "kernels.cuh", "common.cuh", "rotate.cuh", "tma.cuh", "timeline.cuh"),
+    2: ("decode_tc.cu", "bf16_page.cuh", "tcgen05.cuh", "kernels.cuh", "common.cuh", "tma.cuh", "timeline.cuh"),
+}
 
 
-# the sources the fused decode kernel is compiled from (its file and the headers it includes)
-DECODE_KERNEL_SOURCES = ("decode_mma.cu", "kernels.cuh", "common.cuh", "rotate.cuh", "tma.cuh", "timeline.cuh")
-
-
-def sources_digest() -> str:
+def sources_digest(algo: int) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_kv_cache_decode_gb300", "csrc")
-    for f in DECODE_KERNEL_SOURCES:
+    for f in DECODE_KERNEL_SOURCES[algo]:
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "oscar.h"), "rb").read())
@@ -458,11 +461,12 @@ def sources_digest() -> str:
 
 
 def decode_traffic(args):
-    if args.algo != 1 or args.workload not in ("qwen3_8b_36l", "qwen3_8b_100k_l1") or args.meta_format != "f16":
+    rec = NCU_DECODE_TRAFFIC.get(args.algo)
+    if rec is None or args.workload not in ("qwen3_8b_36l", "qwen3_8b_100k_l1") or args.meta_format != "f16":
         return None
-    if NCU_DECODE_TRAFFIC["sources_sha256"] != sources_digest():
+    if rec["sources_sha256"] != sources_digest(args.algo):
         return None
-    return NCU_DECODE_TRAFFIC["bytes_per_launch"]
+    return rec["bytes_per_launch"]
 
 
 def run_bf16(wl, args, q_all, device):
@@ -716,7 +720,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_36l")
-    ap.add_argument("--algo", type=int, default=None, help="INT2 decode kernel: 0 simt, 1 mma (default: library's)")
+    ap.add_argument("--algo", type=int, default=None, choices=(0, 1, 2),
+                    help="INT2 decode kernel: 0 simt, 1 mma.sync, 2 tcgen05 (default: tcgen05)")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -745,7 +750,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     if args.algo is None:
-        args.algo = 1
+        args.algo = 2
     res = run_ours(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res))

@@ -26,7 +26,7 @@ STATUS_BAD_PAGE, STATUS_BAD_SEQLEN, STATUS_TIMEOUT, STATUS_NONFINITE, STATUS_SAT
 V_ABSORBED, V_EXPLICIT = 0, 1
 OUT_BF16, OUT_FP32 = 0, 1
 KIND_K, KIND_V = 0, 1
-DECODE_SIMT, DECODE_MMA = 0, 1
+DECODE_SIMT, DECODE_MMA, DECODE_TC = 0, 1, 2
 META_F16, META_U8, META_CB = 0, 1, 2
 
 # every symbol include/oscar.h declares

@@ -181,6 +181,23 @@ void choose_splits_simt(int B, int hkv, int max_pages, int max_splits, int sms, 
   *nsplit = (max_pages + best_p - 1) / best_p;
 }
 
+// tcgen05 split policy. Two history CTAs fit an SM (TMEM and registers); one more CTA per (request, kv
+// head) takes the BF16 pages and the step prologue holds about half a CTA's registers per (request, kv
+// head, K / V) while the decode is scheduled. The history CTAs fill the remaining slots of one wave,
+// each taking at least one tile of two pages and at most 256 pages (the output accumulates in TMEM over
+// a split; longer contexts take more splits).
+void choose_splits_tc(int B, int hkv, int max_pages, int max_splits, int sms, int* nsplit, int* pps) {
+  if (max_pages <= 0) { *nsplit = 1; *pps = 1; return; }
+  const long units = (long)B * hkv;
+  const long budget = 2L * sms - units - std::min((long)sms, units);
+  int n = (int)std::max(1L, budget / std::max(1L, units));
+  n = std::max(n, (max_pages + 255) / 256);
+  n = std::min(n, std::max(1, max_pages / 2));
+  n = std::min(std::min(n, max_splits), kMaxMmaSplits);
+  *nsplit = std::max(1, n);
+  *pps = (max_pages + *nsplit - 1) / *nsplit;
+}
+
 // Tensor-core split policy. A request's history pages are spread evenly over n splits of 4 warps,
 // a warp taking every fourth page of its split; the grid has B * hkv * (n + nbf) CTAs (the BF16
 // pages are light ones), ctas_per_sm resident per SM. A CTA's time is about its warps' rounds
@@ -427,7 +444,8 @@ int oscar_append_kv(oscar_cache* c, int layer, int B, const void* k, const void*
 }
 
 int oscar_set_decode_algo(oscar_cache* c, int algo) {
-  if (!c || (algo != OSCAR_DECODE_SIMT && algo != OSCAR_DECODE_MMA)) return OSCAR_ERR_INVALID_ARG;
+  if (!c || (algo != OSCAR_DECODE_SIMT && algo != OSCAR_DECODE_MMA && algo != OSCAR_DECODE_TC))
+    return OSCAR_ERR_INVALID_ARG;
   c->algo = algo;
   return OSCAR_OK;
 }
@@ -443,7 +461,7 @@ void set_splits(const oscar_cache* c, int B, int max_hist_pages, int shared_page
   const int hkv = c->lay.num_kv_heads, gq = c->lay.num_q_heads / c->lay.num_kv_heads;
   a.shared_pages = 0;
   a.nsplit_shared = 0;
-  if (shared_pages > 0 && a.algo == OSCAR_DECODE_MMA && c->lay.max_splits >= 2) {
+  if (shared_pages > 0 && a.algo != OSCAR_DECODE_SIMT && c->lay.max_splits >= 2) {
     decode_split_policy(B, hkv, gq, a.nbf, max_hist_pages - shared_pages, c->lay.max_splits - 1, c->sms, a.algo,
                         &a.nsplit, &a.pages_per_split, &a.mma_occupancy);
     const int qtiles = (B * gq + kSharedRows - 1) / kSharedRows;
@@ -480,7 +498,7 @@ int decode_impl(oscar_cache* c, int layer, int B, const void* q, const int32_t* 
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.algo = c->algo;
+  a.algo = resolve_decode_algo(c->algo, c->lay.meta_format, c->lay.num_q_heads / c->lay.num_kv_heads);
   a.len_add = 0;
   a.skip_qprep = 0;
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
@@ -521,7 +539,7 @@ int step_impl(oscar_cache* c, int layer, int B, const void* q, const void* k, co
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.algo = c->algo;
+  a.algo = resolve_decode_algo(c->algo, c->lay.meta_format, c->lay.num_q_heads / c->lay.num_kv_heads);
   a.nbf = (c->lay.sink + c->lay.recent) / kP;
   set_splits(c, B, max_hist_pages, shared_pages, a);
   a.ev0 = a.ev1 = nullptr;
@@ -721,7 +739,8 @@ int pool_layer_view(const oscar_layout* L, void* pool, int layer, int* status, L
 void decode_split_policy(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int algo,
                          int* nsplit, int* pps, int* occupancy) {
   *occupancy = 3;
-  if (algo == OSCAR_DECODE_MMA) choose_splits_mma(B, hkv, gq, nbf, max_pages, max_splits, sms, nsplit, pps, occupancy);
+  if (algo == OSCAR_DECODE_TC) choose_splits_tc(B, hkv, max_pages, max_splits, sms, nsplit, pps);
+  else if (algo == OSCAR_DECODE_MMA) choose_splits_mma(B, hkv, gq, nbf, max_pages, max_splits, sms, nsplit, pps, occupancy);
   else choose_splits_simt(B, hkv, max_pages, max_splits, sms, nsplit, pps);
 }
 

@@ -124,17 +124,23 @@ __device__ __forceinline__ __nv_bfloat16* bf16_row(const LayerView& lv, int page
          (size_t)kind * kP * kD + (size_t)row * kD;
 }
 
-// V codes are channel-major: channel c's 64 codes occupy bytes [16 c, 16 c + 16) of the V region, the
-// code of row t at bits 2 (t % 16) of the 32-bit word t / 16 (the transposed codes packed like K rows).
+// V codes are channel-major: channel c's 64 codes occupy the 16-byte slot c ^ ((c >> 4) & 7) of the V
+// region (the swizzle puts channels 16 g + m, g = 0..7, in distinct banks). Row t's code sits in the
+// slot's 32-bit word (t >> 1) & 3 at bit 16 (t & 1) + 4 (t >> 4) + 2 ((t >> 3) & 1): word w holds the rows
+// t with t % 16 in {2w, 2w + 1, 2w + 8, 2w + 9}, even rows in its low half and each odd partner at the
+// same position of the high half, code position 2 (t >> 4) + ((t >> 3) & 1). One masked word is then the
+// fp16 pair of two consecutive rows, and word w gives a tensor-core lane t = w all its pairs of a page.
 constexpr int kVChanBytes = kP / 4;            // 16
-__device__ __forceinline__ int v_word_off(int c, int t) { return kVCodesOff + c * kVChanBytes + (t >> 4) * 4; }
+__device__ __forceinline__ int v_chan_off(int c) { return kVCodesOff + (c ^ ((c >> 4) & 7)) * kVChanBytes; }
+__device__ __forceinline__ int v_word(int t) { return (t >> 1) & 3; }
+__device__ __forceinline__ int v_bit(int t) { return 16 * (t & 1) + 4 * (t >> 4) + 2 * ((t >> 3) & 1); }
 
 // Set the 2-bit V field of (channel c, row t) of a page block to `code`, leaving the other rows' bits:
 // two atomics on the field's 32-bit word, so that writers of other rows of the same word may run at the
 // same time.
 __device__ __forceinline__ void v_set_code(uint8_t* blk, int c, int t, unsigned code) {
-  unsigned* w = reinterpret_cast<unsigned*>(blk + v_word_off(c, t));
-  const int sh = 2 * (t & 15);
+  unsigned* w = reinterpret_cast<unsigned*>(blk + v_chan_off(c) + 4 * v_word(t));
+  const int sh = v_bit(t);
   atomicAnd(w, ~(3u << sh));
   if (code != 0u) atomicOr(w, code << sh);
 }

@@ -106,7 +106,7 @@ extern "C" int oscar_decode_attention_noalloc(const oscar_layout* layout, void* 
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
-  a.algo = kDefaultDecodeAlgo;
+  a.algo = resolve_decode_algo(kDefaultDecodeAlgo, layout->meta_format, (int)(hq / hkv));
   a.len_add = 0;
   a.skip_qprep = 0;
   a.ev0 = a.ev1 = nullptr;

@@ -34,6 +34,7 @@
 // slot `slot0 + split`; the merge kernel combines it with the request's other
 // slots.
 #include "kernels.cuh"
+#include "tcgen05.cuh"
 #include "tma.cuh"
 #include "timeline.cuh"
 
@@ -86,129 +87,9 @@ constexpr int kBarRing = 0, kBarExp = 3, kBarSDone = 6, kBarSFree = 8, kBarPRead
 // the S MMAs' A operand) at 384 (high parts) and 448 (low parts)
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256, kColQh = 384, kColQl = 448;
 
-// UMMA shared-memory descriptor: no swizzle, K-major; lbo = byte step between the core matrices of a row
-// block along K, sbo = byte step between 8-row blocks.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
-}
 // instruction descriptor of kind::f16: D f32, A and B f16, both K-major, M = 128, N = 64
-constexpr uint32_t kIdesc = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_f16(128, 64);
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, bool accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(kIdesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-// The same with A in tensor memory (its M rows in the TMEM lanes, K along the columns, two fp16 per column).
-__device__ __forceinline__ void umma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, bool accumulate) {
-  asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.u32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(kIdesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void mbar_init_n(uint32_t bar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// 32 columns of this warp's 32 TMEM lanes (one row per thread)
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
-      "%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 32 columns at each of two TMEM addresses: both loads in flight, then one wait
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32], float (&vb)[32]) {
-  uint32_t r[32], q[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
-      "%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(ta));
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,"
-      "%28,%29,%30,%31}, [%32];"
-      : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]), "=r"(q[6]), "=r"(q[7]), "=r"(q[8]),
-        "=r"(q[9]), "=r"(q[10]), "=r"(q[11]), "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]),
-        "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]), "=r"(q[22]), "=r"(q[23]), "=r"(q[24]),
-        "=r"(q[25]), "=r"(q[26]), "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
-      : "r"(tb));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    va[i] = __uint_as_float(r[i]);
-    vb[i] = __uint_as_float(q[i]);
-  }
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,"
-      "%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
-      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
-      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
-  return d;
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
-  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b),
-                            *reinterpret_cast<const __half2*>(&c));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// fp16 rounding of a fragment value, subnormal results flushed to zero
-__device__ __forceinline__ float frag_round16(float x) {
-  const float r = __half2float(__float2half_rn(x));
-  return fabsf(r) < 6.103515625e-05f ? 0.f : r;
-}
 // The 2-bit code i (bits 2i, i may be a run-time value) of both 16-bit halves of x, moved to bits 8-9 and
 // fed as fp16 1024 + 256 c.
 __device__ __forceinline__ uint32_t code_at(uint32_t x, int i) {
@@ -236,7 +117,8 @@ __device__ __forceinline__ int canon_off(int row, int k, int kcols) {
 
 
 // Expand one packed page block into K (rows = tokens, K-major over the 128 channel positions) and V^T
-// (rows = channels, K-major over the 64 tokens); et = 0 .. kExpThreads - 1 is the expanding thread.
+// (rows = channels, K-major over the 64 tokens in the V words' order: k position 2 (8 w + p) + e is token
+// 16 (p >> 1) + 2 w + 8 (p & 1) + e); et = 0 .. kExpThreads - 1 is the expanding thread.
 // Both hold exact codes. K position 2q of 16-channel block u holds channel 16u + q, position 2q + 1 channel
 // 16u + 8 + q (the query fragments use the same order). mc: null for the fp16 metadata, else the compact
 // format's grid constants {T, D, E, 0} per (kind, group) (16 floats). cb: codebook format, whose K and V
@@ -278,16 +160,14 @@ __device__ __forceinline__ void expand_page(const uint8_t* blk, uint8_t* kh, uin
     mk[3 * kP] = b.y;
   }
   for (int c = et; c < kD; c += kExpThreads) {   // V: channel c, its 64 tokens (one 16-byte load, channel-major)
-    const uint4 x4 = *reinterpret_cast<const uint4*>(blk + kVCodesOff + c * kVChanBytes);
+    const uint4 x4 = *reinterpret_cast<const uint4*>(blk + v_chan_off(c));
     const uint32_t xw[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
-    for (int kb = 0; kb < kP / 8; ++kb) {        // row c % 8 of core matrix (c / 8, kb): tokens 8 kb .. 8 kb + 7
-      // the 8 codes of half kb % 2 of word kb / 2 (token 8 kb + u at bits 2u); the high half takes them shifted
-      // by one code, so that code position 2v gives the fp16 pair (token 2v, token 2v + 1)
-      const uint32_t hw = (xw[kb >> 1] >> (16 * (kb & 1))) & 0xffffu;
-      const uint32_t x2 = hw | ((hw >> 2) << 16);
+    for (int kb = 0; kb < kP / 8; ++kb) {        // row c % 8 of core matrix (c / 8, kb): k positions 8 kb .. 8 kb + 7
+      // k positions 2 (4 kb + i) and + 1 are code position 4 (kb % 2) + i of word kb / 2, its even and odd row
+      const uint32_t x = xw[kb >> 1] >> (8 * (kb & 1));
       *reinterpret_cast<uint4*>(vt + (c >> 3) * kVtSbo + kb * 128 + (c & 7) * 16) =
-          make_uint4(vval(x2, 0), vval(x2, 2), vval(x2, 4), vval(x2, 6));
+          make_uint4(vval(x, 0), vval(x, 1), vval(x, 2), vval(x, 3));
     }
   }
 }
@@ -445,8 +325,8 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
             const uint64_t bd = umma_desc(kh_a + kb3 * kKhBytes + koff, 128, (kD / 8) * 128);
             const uint32_t d = tmem + kColS + 128 * b + 64 * G;
             const uint32_t qcol = 8 * (4 * G + kk);                      // K = 16 channels: 8 TMEM columns
-            umma_ta(d, tmem + kColQh + qcol, bd, kk > 0);
-            umma_ta(d, tmem + kColQl + qcol, bd, true);
+            umma_ta(d, tmem + kColQh + qcol, bd, kIdesc, kk > 0);
+            umma_ta(d, tmem + kColQl + qcol, bd, kIdesc, true);
           }
         umma_commit(B_(kBarSDone + b));
       };
@@ -505,7 +385,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma(tmem + kColO + 64 * G, umma_desc(p_a + ((i & 1) * 2 + G) * kPBytes + 2 * kk * 128, 128, (kP / 8) * 128),
-                 umma_desc(vt_a + kb3 * kVtBytes + G * 8 * kVtSbo + 2 * kk * 128, 128, kVtSbo),
+                 umma_desc(vt_a + kb3 * kVtBytes + G * 8 * kVtSbo + 2 * kk * 128, 128, kVtSbo), kIdesc,
                  i > 0 || kk > 0);
         umma_commit(B_(kBarODone + (i & 1)));
         umma_commit(B_(kBarBufFree + kb3));      // S of page i completed before its weights were written
@@ -645,11 +525,11 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
       // weights p = 2^(l - m) <= 2^8; P_G = p s_G in fp16, rows in the canonical layout; two tokens per op
       const float2 negm = make_float2(-m, -m);
 #pragma unroll
-      for (int j = 0; j < kSliceTok / 8; ++j) {   // tokens kSliceTok sl + 8j .. + 7
+      for (int j = 0; j < kSliceTok / 8; ++j) {   // k positions 16 j + 8 sl .. + 7 (V word j of this slice's rows)
         uint32_t w0[4], w1[4];
 #pragma unroll
         for (int pr = 0; pr < 4; ++pr) {
-          const int c = 8 * j + 2 * pr;
+          const int c = 16 * (pr >> 1) + 2 * j + 8 * (pr & 1);   // slice tokens c, c + 1 at k positions 16 j + 8 sl + 2 pr, + 1
           const float2 d = __fadd2_rn(make_float2(l[c], l[c + 1]), negm);
           const float2 pv = make_float2(fast_exp2(d.x), fast_exp2(d.y));
           lsum2 = __fadd2_rn(lsum2, pv);
@@ -659,7 +539,7 @@ __global__ void __launch_bounds__(kShThreads, 1) k_decode_shared(LayerView lv, D
           w0[pr] = pack_f16x2(a0.x, a0.y);
           w1[pr] = pack_f16x2(a1.x, a1.y);
         }
-        const int off = canon_off(q, kSliceTok * sl + 8 * j, kP);
+        const int off = canon_off(q, 16 * j + 8 * sl, kP);
         uint8_t* const pbase = pbuf + (i & 1) * 2 * kPBytes;
         *reinterpret_cast<uint4*>(pbase + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
         *reinterpret_cast<uint4*>(pbase + kPBytes + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);

@@ -163,12 +163,12 @@ __global__ void __launch_bounds__(128) k_int2_simt(LayerView lv, DecodeWorkspace
     __syncthreads();
     {
       const int c = tid, g = c / kG;
-      const int woff = kVCodesOff + c * kVChanBytes;      // channel-major V codes
+      const int woff = v_chan_off(c);                     // channel-major V codes
 #pragma unroll
       for (int hh = 0; hh < GQ; ++hh) acc[hh] *= alpha[hh];
       for (int tk = 0; tk < ntok; ++tk) {
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + (tk >> 4) * 4);
-        const unsigned ci = (word >> (2 * (tk & 15))) & 3u;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(blk + woff + 4 * v_word(tk));
+        const unsigned ci = (word >> v_bit(tk)) & 3u;
         const float code = CB ? lvk[8 + ci] : (float)ci;
         const float vhat = fmaf(msz[1][tk][g].x, code, msz[1][tk][g].y);
 #pragma unroll
@@ -379,13 +379,15 @@ static int launch_decode_gq(const LayerView& lv, const DecodeWorkspace& ws, cons
                                    a.bf16_pt, a.sm_scale, st);
     if (rc != OSCAR_OK) return rc;
   }
-  if (a.algo == OSCAR_DECODE_MMA) {
+  if (a.algo == OSCAR_DECODE_MMA || a.algo == OSCAR_DECODE_TC) {
     // the shared-prefix pages for all requests at once (if any), one fused launch for each request's
     // own history pages and the BF16 pages, then the merge kernel; the profiled span is the decode
     // launches (the events make them wait for the query prologue)
     if (a.ev0) cudaEventRecord(a.ev0, st);
     int rc = launch_decode_shared(lv, ws, a, st);
-    if (rc == OSCAR_OK) rc = launch_decode_mma(lv, ws, a, scale_log2, st);
+    if (rc == OSCAR_OK)
+      rc = (a.algo == OSCAR_DECODE_TC && decode_tc_supported(lv)) ? launch_decode_tc(lv, ws, a, scale_log2, st)
+                                                                   : launch_decode_mma(lv, ws, a, scale_log2, st);
     if (a.ev1) cudaEventRecord(a.ev1, st);
     if (rc != OSCAR_OK) return rc;
     return launch_merge(lv, ws, a.B, a.nsplit + a.nsplit_shared, a.nbf, a.out, a.out_dtype, a.lse, st);
@@ -444,7 +446,9 @@ int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pag
 int configure_mma_kernels();   // decode_mma.cu
 
 int configure_decode_kernels() {
-  if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
+  if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK ||
+      configure_tc_kernel() != OSCAR_OK)
+    return OSCAR_ERR_CUDA;
   return configure_shared_kernel();
 }
 

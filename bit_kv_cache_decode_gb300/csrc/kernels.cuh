@@ -79,6 +79,18 @@ struct DecodeArgs {
 };
 
 int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, cudaStream_t st);
+// tcgen05 decode (decode_tc.cu): the history splits and, in one more CTA per (request, kv head), the
+// BF16 pages; the layouts it serves (fp16 metadata, gq <= 4)
+bool decode_tc_supported(const LayerView& lv);
+int launch_decode_tc(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
+                     cudaStream_t st);
+int configure_tc_kernel();
+// the decode kernel that runs for a requested algorithm: OSCAR_DECODE_TC only where the tcgen05 kernel
+// serves the layout (fp16 metadata, up to 4 query heads per kv head), else OSCAR_DECODE_MMA
+inline int resolve_decode_algo(int algo, int meta_format, int gq) {
+  if (algo == OSCAR_DECODE_TC && (meta_format != OSCAR_META_F16 || gq > 4)) return OSCAR_DECODE_MMA;
+  return algo;
+}
 // Merge of the partial slots of every (request, q head): history slots [0, nsplit),
 // BF16 slots [nsplit, nsplit + nbfs). Launched as a programmatic dependent of the
 // kernel that wrote the partials.

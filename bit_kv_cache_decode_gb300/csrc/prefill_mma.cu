@@ -339,38 +339,46 @@ __global__ void __launch_bounds__(kPrefillWarps * 32, 2)
           *reinterpret_cast<uint32_t*>(int2_block_w(lv, page, h) + kKCodesOff + row * (kD / 4) + 4 * wd) = word;
         }
       } else {
-        // channel-major V: lane takes channels lane + 32 j; the tile's rows are gathered per 32-bit word
-        // (16 rows of one channel of one page) and each word is updated by two atomics on its own fields
-        // (a word may also hold rows of a neighbouring tile, written by another warp)
-        unsigned* wp[4] = {nullptr, nullptr, nullptr, nullptr};
-        unsigned msk[4] = {0u, 0u, 0u, 0u}, val[4] = {0u, 0u, 0u, 0u};
+        // channel-major V: lane takes channels lane + 32 j; the tile's rows of one page are gathered per
+        // 32-bit word of each channel (4 words a channel) and each word is updated by two atomics on its own
+        // fields (a word may also hold rows of a neighbouring tile, written by another warp)
+        uint8_t* cur = nullptr;
+        unsigned msk[4][4], val[4][4];
+        auto flush = [&]() {
+          if (cur == nullptr) return;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (msk[j][q] != 0u) {
+                unsigned* wp = reinterpret_cast<unsigned*>(cur + v_chan_off(lane + 32 * j) + 4 * q);
+                atomicAnd(wp, ~msk[j][q]);
+                atomicOr(wp, val[j][q]);
+              }
+        };
         for (int r = 0; r < kTileRows; ++r) {
           if (!((hist_rows >> r) & 1u)) continue;  // warp-uniform
           const int page = __shfl_sync(0xffffffffu, dst.page, r), row = __shfl_sync(0xffffffffu, dst.row, r);
           uint8_t* blk = int2_block_w(lv, page, h);
-          const int sh = 2 * (row & 15);
+          if (blk != cur) {
+            flush();
+            cur = blk;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int c = lane + 32 * j;
-            unsigned* w = reinterpret_cast<unsigned*>(blk + v_word_off(c, row));
-            if (w != wp[j]) {
-              if (wp[j] != nullptr) {
-                atomicAnd(wp[j], ~msk[j]);
-                atomicOr(wp[j], val[j]);
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) msk[j][q] = val[j][q] = 0u;
+          }
+          const int sh = v_bit(row), q0 = v_word(row);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q == q0) {
+                msk[j][q] |= 3u << sh;
+                val[j][q] |= (unsigned)codes_s[r * kD + lane + 32 * j] << sh;
               }
-              wp[j] = w;
-              msk[j] = val[j] = 0u;
-            }
-            msk[j] |= 3u << sh;
-            val[j] |= (unsigned)codes_s[r * kD + c] << sh;
-          }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (wp[j] != nullptr) {
-            atomicAnd(wp[j], ~msk[j]);
-            atomicOr(wp[j], val[j]);
-          }
+        flush();
       }
       {
         const int r = lane >> 1, G = lane & 1;

@@ -112,7 +112,10 @@ extern "C" {
 
 /* decode kernel choice (oscar_set_decode_algo) */
 #define OSCAR_DECODE_SIMT 0  /* CUDA-core INT2 decode                          */
-#define OSCAR_DECODE_MMA  1  /* tensor-core (mma.sync) INT2 decode, default    */
+#define OSCAR_DECODE_MMA  1  /* tensor-core (mma.sync) INT2 decode             */
+#define OSCAR_DECODE_TC   2  /* 5th-generation tensor-core (tcgen05, TMEM) INT2
+                                decode: fp16 metadata and up to 4 query heads
+                                per kv head; other layouts run OSCAR_DECODE_MMA */
 
 /* INT2 group metadata format (oscar_layout.meta_format). The pages budget the
  * history at 2.25 bits per element (news article "超越 TurboQuant…", section

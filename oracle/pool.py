@@ -28,9 +28,12 @@ bytes (5120 for P = 64, d = 128, G = 64), in this order:
 
 1. K codes, token-major: row t occupies bytes [t*d/4, (t+1)*d/4), the token's
    codes packed with channel j in byte j//4 at bits 2*(j%4).
-2. V codes, channel-major: channel c occupies bytes [c*P/4, (c+1)*P/4) of the
-   region, the code of row t in byte t//4 at bits 2*(t%4); i.e. the transposed
-   codes V^T packed like K rows, four rows per byte.
+2. V codes, channel-major: channel c occupies the 16 bytes (P = 64) of slot
+   c ^ ((c >> 4) & 7) of the region. Its 4 little-endian 32-bit words hold the
+   64 rows: row t sits in word (t >> 1) & 3 at bit 16 (t & 1) + 4 (t >> 4) +
+   2 ((t >> 3) & 1). So word w holds the rows t with t % 16 in
+   {2w, 2w+1, 2w+8, 2w+9}, even rows in its low half and odd rows in its high
+   half, each row next to its odd (even) partner.
 3. K metadata: row t at t*(d/G)*m, m = 4 (fp16 format, the default): for each
    group g, fp16 scale then fp16 zero; m = 2 (compact u8 format): for each group
    g, the byte mn8 then the byte mx8 (see ``quant``: indices on the group's grid
@@ -108,10 +111,15 @@ class PoolModel:
         return rows[:, None] * (g.d // 4) + np.arange(g.d // 4)[None, :]
 
     def _v_field(self, rows: np.ndarray):
-        """([n, d] byte offsets within the block, [n, d] bit shifts) of rows' V codes, channel-major."""
+        """([n, d] byte offsets within the block, [n, d] bit shifts within the byte) of rows' V codes."""
         g = self.geo
+        assert g.page == 64, "the V word layout is defined for 64-row pages"
         c = np.arange(g.d)[None, :]
-        return g.codes_bytes + c * (g.page // 4) + (rows[:, None] // 4), 2 * (rows[:, None] % 4) + 0 * c
+        t = rows[:, None].astype(np.int64)
+        slot = c ^ ((c >> 4) & 7)
+        word = (t >> 1) & 3
+        bit = 16 * (t & 1) + 4 * (t >> 4) + 2 * ((t >> 3) & 1)
+        return g.codes_bytes + slot * (g.page // 4) + 4 * word + bit // 8 + 0 * c, bit % 8 + 0 * c
 
     def _write_v_codes(self, blk: np.ndarray, rows: np.ndarray, codes: np.ndarray):
         """Set the 2-bit V fields of rows (codes [n, d] in 0..3), leaving the other rows' bits."""

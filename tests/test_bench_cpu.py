@@ -1,6 +1,7 @@
 """Host-side checks of bench.py: the algorithmic byte counts behind the roofline, the whole-job rate,
 and the reference arm's JSON line (the oracle on the host cores, on a small sample)."""
 import argparse
+import os
 
 import numpy as np
 
@@ -35,8 +36,9 @@ def test_reference_arm_line(monkeypatch):
     assert res["value"] > 0 and res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["cores"] >= 1
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
     assert "first 1024 tokens" in res["cpu_baseline"]["sample"]
-    # cores: the threads numpy may use; the measured CPU seconds per wall second cannot exceed them by much
-    assert res["cpu_baseline"]["cpu_s_per_wall_s"] <= res["cpu_baseline"]["cores"] * 1.1 + 0.1
+    # the measured CPU seconds per wall second cover every thread of the process (numpy's BLAS pool and any
+    # other library's), so they are bounded by the machine's cores, not by the BLAS pool alone
+    assert 0 < res["cpu_baseline"]["cpu_s_per_wall_s"] <= (os.cpu_count() or 1) * 1.1 + 0.1
     assert bench.run_reference(args, 1, 2) is None            # other ranks print nothing
 
 

@@ -20,7 +20,7 @@ from oracle import attention as A
 from oracle import pool as P
 
 TOL = 2e-3
-ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma")]
+ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma"), pytest.param(2, id="tc")]
 
 
 def _check(cache, prm, hist_pt, bf16_pt, lens, gq, v_mode, seed, out_dtype=1, kv_heads=None, shared_pages=0):

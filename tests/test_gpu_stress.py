@@ -13,8 +13,9 @@ by more than 2^8). These cases move the logits far from the default scale:
   channels, so a single token takes almost all of the weight;
 * equal: the query is zero, every logit is 0 and the output is the plain mean.
 
-Every case runs on the CUDA-core decoder, the per-request tensor-core decoder
-and the shared-prefix tensor-core decoder, on fp32 output, against the oracle's
+Every case runs on the CUDA-core decoder, the per-request mma.sync and tcgen05
+decoders and the shared-prefix tensor-core decoder (followed by either
+per-request decoder), on fp32 output, against the oracle's
 fp64 attention over the pool bytes the GPU wrote, with the decode tolerance
 (per (request, q-head) row, max |o - ref| / max |ref| <= 2e-3).
 """
@@ -33,7 +34,8 @@ from oracle import attention as A
 TOL = 2e-3
 SHARED = 64 + 64 * 24                     # shared prefix: the sink page and 24 history pages
 LENS = [SHARED + 64 * 6 + 37 + 256, SHARED + 64 * 2 + 256, SHARED + 300]
-KERNELS = [pytest.param((0, 0), id="simt"), pytest.param((1, 0), id="mma"), pytest.param((1, 24), id="shared")]
+KERNELS = [pytest.param((0, 0), id="simt"), pytest.param((1, 0), id="mma"), pytest.param((1, 24), id="shared"),
+           pytest.param((2, 0), id="tc"), pytest.param((2, 24), id="shared_tc")]
 CASES = ["peaked", "diffuse", "aligned", "equal"]
 
 

@@ -114,10 +114,12 @@ def test_int2_block_layout_hand_built():
     blk = pm.int2[0, 0]
     assert geo.block_bytes == 5120
     assert np.all(blk[0:32] == 0x55) and np.all(blk[32:64] == 0x55)   # K rows 0, 1 token-major
-    # V codes region, channel-major: channel c's 16 bytes at 2048 + 16 c, rows 0-3 in byte 0 (row 0 at
-    # bits 0-1 = 1, row 1 at bits 2-3 = 2), rows 4-7 in byte 1 (row 5 at bits 2-3 = 3)
-    vreg = blk[2048:4096].reshape(128, 16)
-    assert np.all(vreg[:, 0] == 0b1001) and np.all(vreg[:, 1] == 0b1100) and np.all(vreg[:, 2:] == 0)
+    # V codes region, channel-major: channel c's 16 bytes in slot c ^ ((c >> 4) & 7). Row 0 (code 1) is word 0,
+    # bits 0-1; row 1 (code 2) word 0, bits 16-17; row 5 (code 3) word 2 ((5 >> 1) & 3), bits 16-17.
+    vreg = blk[2048:4096].reshape(128, 4, 4).view("<u4")[..., 0]       # [slot][word]
+    for c in (0, 5, 17, 63, 100, 127):
+        s = c ^ ((c >> 4) & 7)
+        assert vreg[s, 0] == 1 | (2 << 16) and vreg[s, 1] == 0 and vreg[s, 2] == 3 << 16 and vreg[s, 3] == 0
     # K metadata of row 0: fp16 scale, zero per group
     meta = blk[4096:4104].view(np.float16)
     assert list(meta) == [0.5, -1.0, 0.25, 2.0]

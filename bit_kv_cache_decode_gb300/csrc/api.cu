@@ -644,8 +644,12 @@ int oscar_bf16_decode(int B, int num_q_heads, int num_kv_heads, const void* kv_p
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return OSCAR_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return OSCAR_ERR_CUDA;
-  int nsplit, pps;
-  choose_splits_simt(B, num_kv_heads, max_pages, max_splits, sms, &nsplit, &pps);
+  // the streaming kernel holds two CTAs per SM: one wave of splits over the (request, kv head) pairs
+  const long units = (long)B * num_kv_heads;
+  int nsplit = (int)std::max(1L, 2L * sms / units);
+  nsplit = std::min(std::min(nsplit, max_splits), max_pages);
+  const int pps = (max_pages + nsplit - 1) / nsplit;
+  nsplit = (max_pages + pps - 1) / pps;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   return launch_bf16_decode(B, num_q_heads, num_kv_heads, kv_pages, num_pages, q, seq_lens, page_table, max_pages,
                             sm_scale, out, out_dtype, lse, reinterpret_cast<float*>(w + kAlign), max_splits, nsplit,

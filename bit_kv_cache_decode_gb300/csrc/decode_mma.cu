@@ -121,6 +121,11 @@ __device__ __forceinline__ void u8_row_meta(uint32_t m, const float (&c)[6], flo
 __device__ __forceinline__ uint32_t cb_lookup(uint32_t lut, uint32_t sel) {
   return __byte_perm(lut, 0x64646464u, (sel & 0x0303u) | 0x4040u);
 }
+// The same level as the fp16 subnormal k_c 2^-24 (high bytes zero): the key operand, which then needs no
+// constant part cancelled after the tensor cores' truncating accumulation.
+__device__ __forceinline__ uint32_t cb_lookup_sub(uint32_t lut, uint32_t sel) {
+  return __byte_perm(lut, 0u, (sel & 0x0303u) | 0x4040u);
+}
 
 // History split `split` of group (b, h): see the file comment. FMT: the pool's metadata format,
 // kFmtF16, kFmtU8 (compact (mn8, mx8) metadata, 4608-byte blocks staged in the same 5120-byte slots) or
@@ -241,7 +246,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     cF[nt] = cZ0[nt] = cZ1[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
-      cF[nt] = CB ? qc[kQF] : qc[kQF] * 16777216.f;   // 2^24: the codes were fed as subnormals
+      cF[nt] = qc[kQF] * 16777216.f;               // 2^24: the codes (or levels) were fed as subnormals
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
       o0h = qc[kQOff0H];
@@ -311,10 +316,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             if constexpr (CB) {
               // k rows (2t, 2t+1): channels (16t + j, 16t + 4 + j) of the word (bytes 0, 1 at bits 2j);
               // (2t+8, 2t+9): channels (16t + 8 + j, 16t + 12 + j) (bytes 2, 3)
-              a0 = cb_lookup(klut, kx[G] >> (2 * j));
-              a1 = cb_lookup(klut, ky[G] >> (2 * j));
-              a2 = cb_lookup(klut, kx[G] >> (2 * j + 16));
-              a3 = cb_lookup(klut, ky[G] >> (2 * j + 16));
+              a0 = cb_lookup_sub(klut, kx[G] >> (2 * j));
+              a1 = cb_lookup_sub(klut, ky[G] >> (2 * j));
+              a2 = cb_lookup_sub(klut, kx[G] >> (2 * j + 16));
+              a3 = cb_lookup_sub(klut, ky[G] >> (2 * j + 16));
             } else {
               // the masked bits as fp16 subnormals c 4^(p mod 4) 2^-24, p the code's position (no bias, no
               // conversion; the query fragments carry 4^-(p mod 4))

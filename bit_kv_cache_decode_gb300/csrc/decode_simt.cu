@@ -300,50 +300,6 @@ __global__ void __launch_bounds__(128) k_bf16_seg(LayerView lv, DecodeWorkspace 
 // in the rotated value basis, is multiplied by R_V^T = P_br H U_V^T before it
 // meets the BF16 partial.
 // ---------------------------------------------------------------------------
-// All-BF16 paged decode (the comparison kernel): split over pages, then a plain merge.
-template <int GQ>
-__global__ void __launch_bounds__(128) k_bf16_base(const uint8_t* __restrict__ pages, int hkv, int hq_total,
-                                                   int num_pages, const __nv_bfloat16* __restrict__ q,
-                                                   const int* __restrict__ seq_lens, const int* __restrict__ page_table,
-                                                   int max_pages, int pages_per_split, float scale_log2,
-                                                   float* __restrict__ partials, int nslots, int* status) {
-  __shared__ __align__(16) __nv_bfloat16 ks[kP][kD + 8];
-  __shared__ __align__(16) __nv_bfloat16 vs[kP][kD];
-  __shared__ float qs[GQ][kD];
-  __shared__ float pbuf[GQ][kP];
-  __shared__ float mrow[GQ], lrow[GQ], alpha[GQ];
-  __shared__ int valid[kP];
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int hq0 = h * GQ;
-  int L = seq_lens[b];
-  if (L > max_pages * kP || L < 1) {
-    if (tid == 0 && s == 0) flag(status, OSCAR_STATUS_BAD_SEQLEN);
-    L = max(0, min(L, max_pages * kP));
-  }
-  const int t0 = min(L, s * pages_per_split * kP), t1 = min(L, (s + 1) * pages_per_split * kP);
-  for (int i = tid; i < GQ * kD; i += 128) qs[i / kD][i % kD] = __bfloat162float(q[((size_t)b * hq_total + hq0) * kD + i]);
-  if (tid < GQ) { mrow[tid] = -INFINITY; lrow[tid] = 0.f; }
-  float acc[GQ];
-#pragma unroll
-  for (int i = 0; i < GQ; ++i) acc[i] = 0.f;
-  __syncthreads();
-  const int* pt = page_table + (size_t)b * max_pages;
-  auto locate = [&](int i, int& page, int& row) -> bool {
-    const int pos = t0 + i;
-    page = pt[pos / kP];
-    row = pos % kP;
-    if (page < 0 || page >= num_pages) { flag(status, OSCAR_STATUS_BAD_PAGE); return false; }
-    return true;
-  };
-  attend_bf16_list<GQ>(pages, hkv, h, t1 - t0, scale_log2, locate, ks, vs, qs, pbuf, mrow, lrow, alpha, valid, acc);
-#pragma unroll
-  for (int hh = 0; hh < GQ; ++hh) {
-    float* part = part_ptr(partials, b, hq_total, hq0 + hh, nslots, s);
-    if (tid == 0) { part[0] = mrow[hh]; part[1] = lrow[hh]; }
-    part[4 + tid] = acc[hh];
-  }
-}
-
 __global__ void __launch_bounds__(128) k_merge_plain(const float* __restrict__ partials, int hq_total, int nslots,
                                                      int nsplit, void* out, int out_dtype, float* lse) {
   const int hq = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
@@ -418,36 +374,22 @@ int launch_decode(const LayerView& lv, const DecodeWorkspace& ws, const DecodeAr
   }
 }
 
-template <int GQ>
-static int launch_bf16_gq(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,
-                          const int* seq_lens, const int* page_table, int max_pages, float sm_scale, void* out,
-                          int out_dtype, float* lse, float* partials, int max_splits, int nsplit, int pps, int* status,
-                          cudaStream_t st) {
-  k_bf16_base<GQ><<<dim3(nsplit, hkv, B), 128, 0, st>>>(static_cast<const uint8_t*>(kv_pages), hkv, hq, num_pages,
-                                                        static_cast<const __nv_bfloat16*>(q), seq_lens, page_table,
-                                                        max_pages, pps, sm_scale * kLog2e, partials, max_splits, status);
-  k_merge_plain<<<dim3(hq, B), 128, 0, st>>>(partials, hq, max_splits, nsplit, out, out_dtype, lse);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
-}
-
 int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q, const int* seq_lens,
                        const int* page_table, int max_pages, float sm_scale, void* out, int out_dtype, float* lse,
                        float* partials, int max_splits, int nsplit, int pps, int* status, cudaStream_t st) {
   if (B == 0) return OSCAR_OK;
-  switch (hq / hkv) {
-    case 1: return launch_bf16_gq<1>(B, hq, hkv, kv_pages, num_pages, q, seq_lens, page_table, max_pages, sm_scale, out, out_dtype, lse, partials, max_splits, nsplit, pps, status, st);
-    case 2: return launch_bf16_gq<2>(B, hq, hkv, kv_pages, num_pages, q, seq_lens, page_table, max_pages, sm_scale, out, out_dtype, lse, partials, max_splits, nsplit, pps, status, st);
-    case 4: return launch_bf16_gq<4>(B, hq, hkv, kv_pages, num_pages, q, seq_lens, page_table, max_pages, sm_scale, out, out_dtype, lse, partials, max_splits, nsplit, pps, status, st);
-    case 8: return launch_bf16_gq<8>(B, hq, hkv, kv_pages, num_pages, q, seq_lens, page_table, max_pages, sm_scale, out, out_dtype, lse, partials, max_splits, nsplit, pps, status, st);
-    default: return OSCAR_ERR_UNSUPPORTED;
-  }
+  const int rc = launch_bf16_stream(B, hkv, hq, kv_pages, num_pages, q, seq_lens, page_table, max_pages, pps, nsplit,
+                                    sm_scale * kLog2e, partials, max_splits, status, st);
+  if (rc != OSCAR_OK) return rc;
+  k_merge_plain<<<dim3(hq, B), 128, 0, st>>>(partials, hq, max_splits, nsplit, out, out_dtype, lse);
+  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_mma_kernels();   // decode_mma.cu
 
 int configure_decode_kernels() {
   if (configure_mma_kernels() != OSCAR_OK || configure_merge_kernel() != OSCAR_OK ||
-      configure_tc_kernel() != OSCAR_OK)
+      configure_tc_kernel() != OSCAR_OK || configure_bf16_stream() != OSCAR_OK)
     return OSCAR_ERR_CUDA;
   return configure_shared_kernel();
 }

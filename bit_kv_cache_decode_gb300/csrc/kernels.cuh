@@ -113,6 +113,11 @@ inline int set_max_shared_carveout(const void* fn) {
 int configure_decode_kernels();
 int launch_wait_probe(int* status, cudaStream_t st);   // checks.cu
 
+// the streaming BF16 comparison kernel (bf16_decode.cu): partials of `nsplit` splits of pages_per_split pages
+int launch_bf16_stream(int B, int hkv, int hq, const void* kv_pages, int num_pages, const void* q,
+                       const int* seq_lens, const int* page_table, int max_pages, int pages_per_split, int nsplit,
+                       float scale_log2, float* partials, int nslots, int* status, cudaStream_t st);
+int configure_bf16_stream();
 int launch_bf16_decode(int B, int hq, int hkv, const void* kv_pages, int num_pages, const void* q,
                        const int* seq_lens, const int* page_table, int max_pages, float sm_scale, void* out,
                        int out_dtype, float* lse, float* partials, int max_splits, int nsplit, int pages_per_split,

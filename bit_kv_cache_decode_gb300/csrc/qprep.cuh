@@ -17,13 +17,13 @@
 //               fragments carry hi and lo in separate columns; summing both,
 //               sum_{ch in g} c W(ch) 2^-24 (hi + lo)(ch) = 2^(sigma - 24) sum c q~
 //               to about 22 bits, with no constant part to cancel (the offsets
-//               below are 0). Codebook pools feed 1024 + k_c instead and use the
-//               offsets off_{g,part} = 1024 * sum_{ch in g} part(ch).
+//               below are 0). Codebook pools feed the level k_c the same way, as
+//               the fp16 subnormal k_c 2^-24.
 //               k-block kb = 4 G + j (G the channel group) at lane (g', t') holds
 //               k rows (2t', 2t'+1) -> channels (c0, c0 + 8) and (2t'+8, 2t'+9) ->
 //               channels (c0 + 1, c0 + 9), c0 = 16 (t' + 4 G) + 2 j; column g' is
 //               (head 4 nt + g'/2, part g'%2). sigma puts max|q~| near 2^12.
-//               Codebook pools (OSCAR_META_CB): the kernel feeds level k_c as 1024 + k_c
+//               Codebook pools (OSCAR_META_CB): the kernel feeds level k_c as k_c 2^-24
 //               (W = 1 for every channel), k rows (2t', 2t'+1) -> channels (c0, c0 + 4) and
 //               (2t'+8, 2t'+9) -> channels (c0 + 8, c0 + 12), c0 = 16 (t' + 4 G) + j.
 #pragma once
@@ -166,18 +166,10 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
   const int gq = lv.hq / lv.hkv;
   for (int qi = wib; qi < gq; qi += nwarps) {
     const float sc = pow2i(sig[qi]);
-    float offh = 0.f, offl = 0.f, sum = 0.f;
+    float offh = 0.f, offl = 0.f, sum = 0.f;       // the offsets stay 0: no operand carries a constant part
+    (void)sc;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {                   // channel 4 lane + e
-      const float v = xs[qi * stride + 4 * lane + e];
-      if (lv.meta_cb) {                             // offsets of the biased codebook levels 1024 + k_c
-        const float x = v * sc;
-        const float hi = frag_round(x);
-        offh += hi;
-        offl += frag_round(x - hi);
-      }
-      sum += v;
-    }
+    for (int e = 0; e < 4; ++e) sum += xs[qi * stride + 4 * lane + e];   // channel 4 lane + e
 #pragma unroll
     for (int m = 1; m < 16; m <<= 1) {              // lanes 0..15 hold group 0, 16..31 group 1
       offh += __shfl_xor_sync(0xffffffffu, offh, m);
@@ -207,7 +199,7 @@ __device__ __forceinline__ void qprep_finish(const LayerView& lv, const DecodeWo
       // r = 0: channels (c0, c0 + 8), code position p = 2 (kb & 3) in its 16-bit half; r = 1: (c0 + 1,
       // c0 + 9), p + 1. The code of position p is fed as c 4^(p mod 4) 2^-24, so the fragment carries
       // q~ 2^sigma / 4^(p mod 4) (the kernel's F takes the 2^24). Codebook pools: r = 0: (c0, c0 + 4),
-      // r = 1: (c0 + 8, c0 + 12), levels fed as 1024 + k_c (W = 1).
+      // r = 1: (c0 + 8, c0 + 12), levels fed as k_c 2^-24 (W = 1).
       const float sc = lv.meta_cb ? pow2i(sig[head]) : pow2i(sig[head] - 2 * ((2 * (kb & 3) + r) & 3));
       const int c0 = lv.meta_cb ? 16 * (tp + 4 * (kb >> 2)) + (kb & 3) + 8 * r
                                 : 16 * (tp + 4 * (kb >> 2)) + 2 * (kb & 3) + r;

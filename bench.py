@@ -50,6 +50,7 @@ STORAGE = {"f16": "int2 history (fp16 scale/zero per 64-group) + bf16 sink/recen
            "cb": "int2 history (Lloyd-Max 4-level codebook per kv head, fp16 range/zero per 64-group) + bf16 "
                  "sink/recent"}
 META_FORMATS = {"f16": 0, "u8": 1, "cb": 2}
+PREFILL_REPS = 3       # timed bulk prefill calls per layer (averaged)
 BF16_BYTES = 512         # per BF16 token per kv head: K and V, 128 x 2 B each
 
 WORKLOADS = {
@@ -217,13 +218,17 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
             tot = int(lens.sum())
             k, v = synth.torch_kv_tokens(tot, H, outl, gen, device)
             cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+            # one untimed call (module loading, first touch of the pool), then PREFILL_REPS timed calls
+            # that rewrite the same pool bytes; the inputs (bf16 K and V) are far larger than L2
+            cache.quantize_prefill(layer, k, v, cu, hp_d, bp_d, total_tokens=tot)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             e0.record()
-            cache.quantize_prefill(layer, k, v, cu, hp_d, bp_d, total_tokens=tot)
+            for _ in range(PREFILL_REPS):
+                cache.quantize_prefill(layer, k, v, cu, hp_d, bp_d, total_tokens=tot)
             e1.record()
             torch.cuda.synchronize()
-            prefill["ms"] += e0.elapsed_time(e1)
+            prefill["ms"] += e0.elapsed_time(e1) / PREFILL_REPS
             prefill["tokens"] += tot
             del k, v
             continue
@@ -721,7 +726,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen3_8b_36l")
     ap.add_argument("--algo", type=int, default=None, choices=(0, 1, 2),
-                    help="INT2 decode kernel: 0 simt, 1 mma.sync, 2 tcgen05 (default: tcgen05)")
+                    help="INT2 decode kernel: 0 simt, 1 mma.sync (default), 2 tcgen05")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -750,7 +755,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     if args.algo is None:
-        args.algo = 2
+        args.algo = 1
     res = run_ours(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res))

@@ -400,8 +400,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       }
 
       // ---- P.Vhat over the page's four 16-token tiles -----------------------------------
-      // weights p * scale of the page's 64 tokens: the B fragments of the four 16-token tiles
+      // weights p * scale of the page's 64 tokens: the B fragments of the four 16-token tiles; the codebook
+      // format also keeps their fp16 rounding remainders (a second MMA per tile: its levels span the whole
+      // range, so the weights' rounding would otherwise dominate its error)
       uint32_t bf[4][NT][2];
+      uint32_t bfl[CB ? 4 : 1][NT][2];
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const int r0 = 16 * kt + g, r1 = r0 + 8;
@@ -436,8 +439,16 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           zacc[nt][1] = fmaf(pa, sv01.y, fmaf(pb, sv11.y, zacc[nt][1]));
           // lane (g, t): the weights of token row g (rows 0-7) and g + 8 of the tile for head t, groups 0 and 1;
           // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'
-          bf[kt][nt][0] = movmatrix_t(pack_f16x2(pa * sv00.x, pa * sv01.x));
-          bf[kt][nt][1] = movmatrix_t(pack_f16x2(pb * sv10.x, pb * sv11.x));
+          const float x0 = pa * sv00.x, x1 = pa * sv01.x, x2 = pb * sv10.x, x3 = pb * sv11.x;
+          const uint32_t h01 = pack_f16x2(x0, x1), h23 = pack_f16x2(x2, x3);
+          bf[kt][nt][0] = movmatrix_t(h01);
+          bf[kt][nt][1] = movmatrix_t(h23);
+          if constexpr (CB) {
+            const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+            const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+            bfl[kt][nt][0] = movmatrix_t(pack_f16x2(x0 - f01.x, x1 - f01.y));
+            bfl[kt][nt][1] = movmatrix_t(pack_f16x2(x2 - f23.x, x3 - f23.y));
+          }
         }
       }
       // P.Vhat: tile mt takes channels 16 g + mt (rows g) and 16 g + 8 + mt (rows g + 8). Word t of a
@@ -468,7 +479,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             a3 = exact_codes(and_or(xb[hh], 0x00030003u << (2 * pp + 2), kMagic), pp + 1);
           }
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][mt], a0, a1, a2, a3, bf[kt][nt][0], bf[kt][nt][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(acc[nt][mt], a0, a1, a2, a3, bf[kt][nt][0], bf[kt][nt][1]);
+            if constexpr (CB) mma16816(acc[nt][mt], a0, a1, a2, a3, bfl[kt][nt][0], bfl[kt][nt][1]);
+          }
         }
       }
     } else if (i == 0) {

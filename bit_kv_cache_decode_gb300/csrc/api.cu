@@ -100,12 +100,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // R = U H P_br (MarkTechPost article "Together AI 开源 OSCAR…", section "OSCAR 有何不同做法"), composed in
 // double from the float32 U as loaded: (U H)[i][c] = sum_m U[i][m] (-1)^popcount(m & c) / sqrt(128), and
-// column j of R is column bitrev7(j) of U H. R is stored as fp16 hi = fp16(R), lo = fp16(R - hi)
-// (about 22 significant bits) in the B-fragment order of mma.m16n8k16 (k = input channel, n = rotated
-// channel): for k-block kb, n-tile nt and lane (g = lane / 4, t = lane % 4), b0 holds rows 16 kb + 2t,
-// +1 and b1 rows 16 kb + 2t + 8, +9, all of column 8 nt + g.
-void composite_rotation_fragments(const float* U, uint32_t* frag) {
-  std::vector<double> uh((size_t)kD * kD);
+// column j of R is column bitrev7(j) of U H. R[i][j]: i = input channel, j = rotated channel.
+std::vector<double> composite_rotation(const float* U) {
+  std::vector<double> uh((size_t)kD * kD), R((size_t)kD * kD);
   const double inv = 1.0 / std::sqrt((double)kD);
   for (int i = 0; i < kD; ++i)
     for (int c = 0; c < kD; ++c) {
@@ -113,11 +110,18 @@ void composite_rotation_fragments(const float* U, uint32_t* frag) {
       for (int m = 0; m < kD; ++m) s += (double)U[i * kD + m] * ((__builtin_popcount(m & c) & 1) ? -inv : inv);
       uh[(size_t)i * kD + c] = s;
     }
-  auto R = [&](int i, int j) {
+  for (int j = 0; j < kD; ++j) {
     int rj = 0;
     for (int bit = 0; bit < 7; ++bit) rj |= ((j >> bit) & 1) << (6 - bit);
-    return uh[(size_t)i * kD + rj];
-  };
+    for (int i = 0; i < kD; ++i) R[(size_t)i * kD + j] = uh[(size_t)i * kD + rj];
+  }
+  return R;
+}
+
+// R as fp16 hi = fp16(R), lo = fp16(R - hi) (about 22 significant bits) in the B-fragment order of
+// mma.m16n8k16 (k = input channel, n = rotated channel): for k-block kb, n-tile nt and lane (g = lane / 4,
+// t = lane % 4), b0 holds rows 16 kb + 2t, +1 and b1 rows 16 kb + 2t + 8, +9, all of column 8 nt + g.
+void rotation_fragments(const std::vector<double>& R, uint32_t* frag) {
   auto half_bits = [](double x) -> uint32_t {
     const __half hv = __double2half(x);
     return (uint32_t)__half_as_ushort(hv);
@@ -130,7 +134,7 @@ void composite_rotation_fragments(const float* U, uint32_t* frag) {
         const int rows[4] = {16 * kb + 2 * t, 16 * kb + 2 * t + 1, 16 * kb + 2 * t + 8, 16 * kb + 2 * t + 9};
         uint32_t hi[4], lo[4];
         for (int e = 0; e < 4; ++e) {
-          const double r = R(rows[e], col);
+          const double r = R[(size_t)rows[e] * kD + col];
           hi[e] = half_bits(r);
           lo[e] = half_bits(r - half_val(r));
         }
@@ -140,6 +144,33 @@ void composite_rotation_fragments(const float* U, uint32_t* frag) {
         w[2] = lo[0] | (lo[1] << 16);
         w[3] = lo[2] | (lo[3] << 16);
       }
+}
+
+// R as three bf16 parts b1 = bf16(R), b2 = bf16(R - b1), b3 = bf16(R - b1 - b2), each laid out as the
+// bulk prefill's tensor-core B operand (n = rotated channel, k = input channel, K-major, 128-byte swizzle):
+// element (n, k) of part p at byte p * 32768 + (k / 64) * 16384 + n * 128 + (((k % 64) / 8) ^ (n % 8)) * 16
+// + (k % 8) * 2.
+void rotation_image(const std::vector<double>& R, uint8_t* img) {
+  auto bf16_bits = [](double x) -> uint16_t {
+    const __nv_bfloat16 b = __float2bfloat16_rn((float)x);
+    return *reinterpret_cast<const uint16_t*>(&b);
+  };
+  auto bf16_val = [](uint16_t bits) -> double {
+    const uint32_t w = (uint32_t)bits << 16;
+    float f;
+    std::memcpy(&f, &w, 4);
+    return (double)f;
+  };
+  for (int n = 0; n < kD; ++n)
+    for (int k = 0; k < kD; ++k) {
+      double r = R[(size_t)k * kD + n];
+      const size_t off = (size_t)(k >> 6) * 16384 + (size_t)n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
+      for (int p = 0; p < 3; ++p) {
+        const uint16_t b = bf16_bits(r);
+        std::memcpy(img + (size_t)p * 32768 + off, &b, 2);
+        r -= bf16_val(b);
+      }
+    }
 }
 
 // Kernel attributes (dynamic shared memory limits, carveout) belong to one device's context: they are
@@ -385,13 +416,21 @@ int oscar_set_rotation(oscar_cache* c, int layer, const float* U_K, const float*
   for (int h = 0; h < hkv; ++h) {
     float* dst = host.data() + (size_t)h * kParamFloats;
     std::memcpy(dst + kUKOff, U_K + (size_t)h * kD * kD, kD * kD * sizeof(float));
-    composite_rotation_fragments(U_K + (size_t)h * kD * kD, reinterpret_cast<uint32_t*>(dst + kRKFragOff));
+    {
+      const std::vector<double> R = composite_rotation(U_K + (size_t)h * kD * kD);
+      rotation_fragments(R, reinterpret_cast<uint32_t*>(dst + kRKFragOff));
+      rotation_image(R, reinterpret_cast<uint8_t*>(dst + kRKImgOff));
+    }
     if (U_V) {
       const float* u = U_V + (size_t)h * kD * kD;
       std::memcpy(dst + kUVOff, u, kD * kD * sizeof(float));
       for (int i = 0; i < kD; ++i)
         for (int j = 0; j < kD; ++j) dst[kUVtOff + j * kD + i] = u[i * kD + j];
-      if (expl) composite_rotation_fragments(u, reinterpret_cast<uint32_t*>(dst + kRVFragOff));
+      if (expl) {
+        const std::vector<double> R = composite_rotation(u);
+        rotation_fragments(R, reinterpret_cast<uint32_t*>(dst + kRVFragOff));
+        rotation_image(R, reinterpret_cast<uint8_t*>(dst + kRVImgOff));
+      }
     }
     std::memcpy(dst + kTauKOff, tau_K + (size_t)h * kD, kD * sizeof(float));
     std::memcpy(dst + kTauVOff, tau_V + (size_t)h * kD, kD * sizeof(float));

@@ -48,7 +48,14 @@ constexpr int kUKOff = 0, kUVOff = kD * kD, kUVtOff = 2 * kD * kD, kTauKOff = 3 
 // 0}, and per kind the codebook {k_0, k_1, k_2, k_3, theta_0, theta_1, theta_2, 0} as floats
 // (kMetaCFloats words, padded so that a head's parameters stay 128-byte aligned)
 constexpr int kMetaCOff = kRVFragOff + kRFragWords, kCbOff = kMetaCOff + 16, kMetaCFloats = 32;
-constexpr int kParamFloats = kMetaCOff + kMetaCFloats;
+// then R_K and R_V (explicit-V mode) as three bf16 parts (R = b1 + b2 + b3, about 24 significant bits),
+// each part the tensor-core B operand of the bulk prefill as it sits in shared memory: [part 3][k half 2]
+// [n 128][128 bytes], K-major with the 128-byte swizzle (the 16-byte chunk j of row n at j ^ (n & 7)),
+// kRImgBytes each, 128-byte aligned
+constexpr int kRImgBytes = 3 * 2 * kD * 128;  // 98,304
+constexpr int kRKImgOff = kMetaCOff + kMetaCFloats, kRVImgOff = kRKImgOff + kRImgBytes / 4;
+constexpr int kParamFloats = kRVImgOff + kRImgBytes / 4;
+static_assert(kRKImgOff % 32 == 0 && kParamFloats % 32 == 0, "128-byte aligned parameter regions");
 // one split partial: m (log2 units), l, then acc[D]; padded to 132 floats (528 B, 16 B aligned)
 constexpr int kPartFloats = kD + 4;
 constexpr float kLog2e = 1.4426950408889634f;

@@ -37,8 +37,10 @@ def test_reference_arm_line(monkeypatch):
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
     assert "first 1024 tokens" in res["cpu_baseline"]["sample"]
     # the measured CPU seconds per wall second cover every thread of the process (numpy's BLAS pool and any
-    # other library's), so they are bounded by the machine's cores, not by the BLAS pool alone
-    assert 0 < res["cpu_baseline"]["cpu_s_per_wall_s"] <= (os.cpu_count() or 1) * 1.1 + 0.1
+    # other library's), so they are bounded by the machine's cores, not by the BLAS pool alone; over a
+    # sample this short the process clock's granularity (and a container whose quota exceeds the cores it
+    # reports) allow a generous margin
+    assert 0 < res["cpu_baseline"]["cpu_s_per_wall_s"] <= (os.cpu_count() or 1) * 2.0 + 1.0
     assert bench.run_reference(args, 1, 2) is None            # other ranks print nothing
 
 

@@ -61,9 +61,10 @@ def _bytes(osc, **kw):
 def test_layout_sizes(osc, meta, block):
     rc, pb, wb = _bytes(osc, meta_format=meta)
     assert rc == 0
-    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V, R_K and R_V fragments and
-    # the compact format's 32 grid constants per kv head
-    per_layer = (10 * 8 * block) + (5 * 8 * 32768) + 8 * (5 * 128 * 128 + 2 * 128 + 32) * 4
+    # per layer: INT2 blocks, BF16 blocks, and U_K, U_V, U_V^T, tau_K, tau_V, R_K and R_V fragments,
+    # the compact format's 32 grid constants and R_K and R_V as three bf16 parts (98,304 bytes each) per
+    # kv head
+    per_layer = (10 * 8 * block) + (5 * 8 * 32768) + 8 * ((5 * 128 * 128 + 2 * 128 + 32) * 4 + 2 * 98304)
     assert pb >= 2 * per_layer and pb < 2 * per_layer + 2 * 3 * 256
     parts = 2 * 32 * (16 + 5) * 132 * 4          # history splits + 5 BF16 chunks per (request, q head)
     assert wb >= parts

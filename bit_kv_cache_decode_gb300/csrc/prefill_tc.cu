@@ -233,6 +233,11 @@ __device__ __forceinline__ void quantise_group(uint32_t ty, const float* prm, in
     }
     const float rh4 = __fmul_rn(rh, 0.25f), rl4 = __fmul_rn(rl, 0.25f);
     const float* cbc = prm + kCbOff + kind * 8;
+    // the quotient is monotone in y: unless the group's largest one rounds past 3, no code needs the
+    // upper clamp (it takes fp16 rounding of a narrow group's scale and zero to get there)
+    const float dmax = __fsub_rn(mx, zq);
+    const bool hi_clamp = __fmaf_rn(dmax, rh, __fmul_rn(dmax, rl)) >= 3.5f;
+    const bool any_hi = __any_sync(0xffffffffu, hi_clamp);
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       float y[32];
@@ -241,21 +246,34 @@ __device__ __forceinline__ void quantise_group(uint32_t ty, const float* prm, in
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t acc = 0u;
+        if constexpr (FMT == kFmtCB) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float d = __fsub_rn(y[16 * q2 + m], zq);
-          if constexpr (FMT == kFmtCB) {
+          for (int m = 0; m < 16; ++m) {
+            const float d = __fsub_rn(y[16 * q2 + m], zq);
             const float c = sq != 0.f ? cb_code(__fmaf_rn(d, rh, __fmul_rn(d, rl)), cbc) : 0.f;
             acc |= ((uint32_t)c) << (2 * m);
-          } else {
-            // q/4 = sat(q / 4) (the scaling by 4 is exact), t = 4 (q/4) + kMagic rounds half to even,
-            // min(t, kMagic + 3) clamps the code
-            const float q4 = __saturatef(__fmaf_rn(d, rh4, __fmul_rn(d, rl4)));
-            const float t = __fmaf_rn(q4, 4.f, kMagic);
-            acc += __float_as_uint(fminf(t, kMagic + 3.f)) << (2 * m);
           }
+          w2[q2] = acc;
+        } else {
+          // q/4 = sat(q / 4) (the scaling by 4 is exact), t = 4 (q/4) + kMagic rounds half to even;
+          // min(t, kMagic + 3) clamps the code where a group needs it
+          if (any_hi) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const float q4 = __saturatef(__fmaf_rn(__fsub_rn(y[16 * q2 + m], zq), rh4,
+                                                     __fmul_rn(__fsub_rn(y[16 * q2 + m], zq), rl4)));
+              acc += __float_as_uint(fminf(__fmaf_rn(q4, 4.f, kMagic), kMagic + 3.f)) << (2 * m);
+            }
+          } else {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const float q4 = __saturatef(__fmaf_rn(__fsub_rn(y[16 * q2 + m], zq), rh4,
+                                                     __fmul_rn(__fsub_rn(y[16 * q2 + m], zq), rl4)));
+              acc += __float_as_uint(__fmaf_rn(q4, 4.f, kMagic)) << (2 * m);
+            }
+          }
+          w2[q2] = acc - kMagicPack;
         }
-        w2[q2] = FMT == kFmtCB ? acc : acc - kMagicPack;
       }
       if (hf == 0) {
         wd[0] = w2[0];
@@ -568,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(128) k_prefill_bf16(LayerView lv, const __nv_bfloat16* __restrict__ k,
                                                       const __nv_bfloat16* __restrict__ v,
                                                       const int* __restrict__ cu_seqlens, const int* __restrict__ bf16_pt) {
+  pdl_launch_dependents();                       // the history kernel touches other memory: let it start
   const int r = blockIdx.x, h = blockIdx.y, kind = blockIdx.z;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = cu_seqlens[r + 1] - cu_seqlens[r];
@@ -642,14 +661,26 @@ int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, con
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long items_max = 2LL * lv.hkv * ((long long)total / kTile + B);
   const int grid = (int)std::max(1LL, std::min((long long)sms, items_max));
+  // launched as a programmatic dependent of the sink / recent copy, which it runs beside (neither waits
+  // for the other; later work on the stream waits for both)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPrefSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (lv.meta_u8)
-    k_prefill_tc<kFmtU8><<<grid, kThreads, kPrefSmem, st>>>(lv, map_k, map_v, cu_seqlens, B, hist_pt, max_hist_pages);
+    e = cudaLaunchKernelEx(&cfg, k_prefill_tc<kFmtU8>, lv, map_k, map_v, cu_seqlens, B, hist_pt, max_hist_pages);
   else if (lv.meta_cb)
-    k_prefill_tc<kFmtCB><<<grid, kThreads, kPrefSmem, st>>>(lv, map_k, map_v, cu_seqlens, B, hist_pt, max_hist_pages);
+    e = cudaLaunchKernelEx(&cfg, k_prefill_tc<kFmtCB>, lv, map_k, map_v, cu_seqlens, B, hist_pt, max_hist_pages);
   else
-    k_prefill_tc<kFmtF16><<<grid, kThreads, kPrefSmem, st>>>(lv, map_k, map_v, cu_seqlens, B, hist_pt,
-                                                             max_hist_pages);
-  return cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+    e = cudaLaunchKernelEx(&cfg, k_prefill_tc<kFmtF16>, lv, map_k, map_v, cu_seqlens, B, hist_pt, max_hist_pages);
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 
 int configure_prefill_kernel() {

@@ -16,6 +16,7 @@ Workloads (synthetic, seeded; Qwen3-shaped random data, no model weights):
   qwen3_8b_100k_l1  1 layer of qwen3_8b_36l (the same decode launch), for profiler captures
   qwen3_32b_mixed   1 layer x (64 q / 8 kv heads), batch 8, lengths ~ U[98,304, 131,072]: one timed bulk
                     prefill of all requests, then decode steps (append + demotion + decode)
+  qwen3_32b_mixed_b2  the same shapes, batch 2, lengths ~ U[30,000, 34,000], for profiler captures
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling).
@@ -61,6 +62,8 @@ WORKLOADS = {
     "qwen3_8b_100k_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
     # ctx as (lo, hi): per-request lengths drawn uniformly, all requests prefilled by one bulk call
     "qwen3_32b_mixed": dict(layers=1, hq=64, hkv=8, batch=8, ctx=(98304, 131072), shared=0),
+    # the same shapes at a size an ncu capture of the prefill handles (about 0.3 GB of bf16 K and V)
+    "qwen3_32b_mixed_b2": dict(layers=1, hq=64, hkv=8, batch=2, ctx=(30000, 34000), shared=0),
 }
 
 

@@ -28,5 +28,6 @@ Modules:
   quant     -- clip, per-token asymmetric INT2 quantiser, dequantiser, packing
   pool      -- byte-exact model of the paged mixed-precision token pool
   attention -- exact softmax decode attention and the segmented LSE merge
+  projection -- K / V projection (x W^T, rounded to bf16) in front of the write path
 """
-from . import rotation, quant, pool, attention  # noqa: F401
+from . import rotation, quant, pool, attention, projection  # noqa: F401

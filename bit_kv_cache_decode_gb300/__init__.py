@@ -32,7 +32,7 @@ META_F16, META_U8, META_CB = 0, 1, 2
 # every symbol include/oscar.h declares
 EXPORTS = (
     "oscar_cache_bytes", "oscar_cache_create", "oscar_cache_destroy", "oscar_layer_offsets", "oscar_set_rotation",
-    "oscar_quantize_prefill", "oscar_append_kv", "oscar_decode_attention", "oscar_set_decode_algo",
+    "oscar_quantize_prefill", "oscar_project_quantize_prefill", "oscar_append_kv", "oscar_decode_attention", "oscar_set_decode_algo",
     "oscar_get_status", "oscar_pack_rotated", "oscar_rotate", "oscar_bf16_decode_workspace_bytes",
     "oscar_bf16_decode", "oscar_calibrate", "oscar_profile_begin", "oscar_profile_read", "oscar_error_string",
     "oscar_decode_attention_noalloc", "oscar_trace_ctas", "oscar_decode_step",
@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
         "oscar_set_codebook": [vp, c_int, vp, vp, vp],
         "oscar_calibrate_codebook": [vp, c_int, vp, vp],
         "oscar_quantize_prefill": [vp, c_int, c_int, vp, vp, i32p, c_int, i32p, c_int, i32p, vp],
+        "oscar_project_quantize_prefill": [vp, c_int, c_int, vp, c_int, vp, vp, i32p, c_int, i32p, c_int, i32p, vp],
         "oscar_append_kv": [vp, c_int, c_int, vp, vp, i32p, i32p, c_int, i32p, vp],
         "oscar_decode_attention": [vp, c_int, c_int, vp, i32p, i32p, c_int, i32p, c_float, vp, c_int, vp, vp],
         "oscar_set_decode_algo": [vp, c_int],
@@ -240,6 +241,19 @@ class OscarCache:
         mhp = hp.shape[1] if hp.dim() == 2 else 0
         _check(_lib.oscar_quantize_prefill(self._h, layer, B, _ptr(k), _ptr(v), _ptr(cu), total, _ptr(hp), mhp,
                                            _ptr(bp), _stream(stream)), "oscar_quantize_prefill")
+
+    def project_quantize_prefill(self, layer: int, x, w_k, w_v, cu_seqlens, hist_pt, bf16_pt,
+                                 total_tokens: int | None = None, stream=None):
+        """quantize_prefill of K = bf16(x W_k^T), V = bf16(x W_v^T): x bf16 [T, d_model], w bf16 [Hkv*128, d_model]."""
+        cu = _dev_i32(cu_seqlens, self.device)
+        hp = _dev_i32(hist_pt, self.device)
+        bp = _dev_i32(bf16_pt, self.device)
+        B = cu.numel() - 1
+        total = int(x.shape[0]) if total_tokens is None else total_tokens
+        mhp = hp.shape[1] if hp.dim() == 2 else 0
+        _check(_lib.oscar_project_quantize_prefill(self._h, layer, B, _ptr(x), int(x.shape[1]), _ptr(w_k), _ptr(w_v),
+                                                   _ptr(cu), total, _ptr(hp), mhp, _ptr(bp), _stream(stream)),
+               "oscar_project_quantize_prefill")
 
     def append_kv(self, layer: int, k, v, seq_lens_before, hist_pt, bf16_pt, stream=None):
         sl = _dev_i32(seq_lens_before, self.device)

@@ -472,6 +472,19 @@ int oscar_quantize_prefill(oscar_cache* c, int layer, int B, const void* k, cons
                         static_cast<cudaStream_t>(stream));
 }
 
+int oscar_project_quantize_prefill(oscar_cache* c, int layer, int B, const void* x, int d_model, const void* w_k,
+                                   const void* w_v, const int32_t* cu_seqlens, int total_tokens,
+                                   const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, void* stream) {
+  if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || total_tokens < 0 || max_hist_pages < 0 ||
+      d_model <= 0)
+    return OSCAR_ERR_INVALID_ARG;
+  if (B == 0 || total_tokens == 0) return OSCAR_OK;
+  if (!x || !w_k || !w_v || !cu_seqlens || !bf16_pt || (max_hist_pages > 0 && !hist_pt)) return OSCAR_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_k) || !aligned16(w_v)) return OSCAR_ERR_INVALID_ARG;
+  return launch_project_prefill(view(c, layer), B, x, d_model, w_k, w_v, cu_seqlens, total_tokens, hist_pt,
+                                max_hist_pages, bf16_pt, static_cast<cudaStream_t>(stream));
+}
+
 int oscar_append_kv(oscar_cache* c, int layer, int B, const void* k, const void* v, const int32_t* seq_lens_before,
                     const int32_t* hist_pt, int max_hist_pages, const int32_t* bf16_pt, void* stream) {
   if (!c || layer < 0 || layer >= c->lay.num_layers || B < 0 || max_hist_pages < 0) return OSCAR_ERR_INVALID_ARG;

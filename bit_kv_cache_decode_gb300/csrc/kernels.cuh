@@ -46,6 +46,11 @@ int launch_pack_rotated(const LayerView& lv, int kind, const float* xrot, const 
 int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N, cudaStream_t st);
 int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, const int* cu_seqlens, int total,
                    const int* hist_pt, int max_hist_pages, const int* bf16_pt, cudaStream_t st);
+// fused projection + write path: K = x W_k^T, V = x W_v^T (bf16), placed and quantised like launch_prefill
+int launch_project_prefill(const LayerView& lv, int B, const void* x, int d_model, const void* w_k, const void* w_v,
+                           const int* cu_seqlens, int total, const int* hist_pt, int max_hist_pages,
+                           const int* bf16_pt, cudaStream_t st);
+int configure_project_prefill_kernel();
 // Append (k, v non-null: new tokens, demotion) and / or the decode's query prologue (q non-null) in one
 // launch, a programmatic dependent of the kernel before it (prologue.cu).
 int launch_prologue(const LayerView& lv, const DecodeWorkspace& ws, int B, const void* q, const void* k,
@@ -53,7 +58,7 @@ int launch_prologue(const LayerView& lv, const DecodeWorkspace& ws, int B, const
                     const int* bf16_pt, float sm_scale, cudaStream_t st);
 int configure_prologue_kernel();
 int configure_write_path_kernels();
-int configure_prefill_kernel();   // prefill_mma.cu
+int configure_prefill_kernel();   // prefill_tc.cu
 
 struct DecodeArgs {
   int B;

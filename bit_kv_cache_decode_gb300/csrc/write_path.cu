@@ -93,6 +93,7 @@ int launch_rotate(const LayerView& lv, int kind, const void* x, float* y, int N,
 
 int configure_write_path_kernels() {
   if (configure_prefill_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
+  if (configure_project_prefill_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
   if (configure_prologue_kernel() != OSCAR_OK) return OSCAR_ERR_CUDA;
   return OSCAR_OK;
 }

@@ -230,6 +230,26 @@ int oscar_quantize_prefill(oscar_cache* cache, int layer, int B, const void* k, 
                            const int32_t* cu_seqlens, int total_tokens, const int32_t* hist_pt,
                            int max_hist_pages, const int32_t* bf16_pt, void* stream);
 
+/* The same bulk write from the prompt's hidden states, fused with the K and V
+ * projections (MarkTechPost article, "服务系统：混合精度缓存布局": the write path
+ * runs fused, so K and V are never written out and read back):
+ *   K = bf16(x W_k^T), V = bf16(x W_v^T), rounded to nearest even,
+ * then placed and quantised exactly as oscar_quantize_prefill does with those K
+ * and V.
+ *  x        : device bf16 [total_tokens][d_model], requests concatenated as in
+ *             cu_seqlens (row-major, 16-byte aligned)
+ *  w_k, w_v : device bf16 [Hkv * 128][d_model] (a linear layer's weight: output
+ *             row j is kv head j / 128, channel j % 128), 16-byte aligned
+ *  d_model  : a multiple of 64
+ * The products accumulate in float32 on the tensor cores, then round to bf16.
+ * Errors: INVALID_ARG (as oscar_quantize_prefill, d_model <= 0, a pointer not
+ * 16-byte aligned), UNSUPPORTED (d_model not a multiple of 64, an odd Hkv,
+ * B > 4096), CUDA. */
+int oscar_project_quantize_prefill(oscar_cache* cache, int layer, int B, const void* x, int d_model,
+                                   const void* w_k, const void* w_v, const int32_t* cu_seqlens,
+                                   int total_tokens, const int32_t* hist_pt, int max_hist_pages,
+                                   const int32_t* bf16_pt, void* stream);
+
 /* Append one token per request at position seq_lens_before[r] (news article,
  * "OSCAR 的设计思路": a new token enters the recent window; the oldest recent
  * token is rotated / clipped / quantised / packed into the INT2 history).

@@ -1,0 +1,138 @@
+"""GPU parity of the fused projection + write path (oscar_project_quantize_prefill) against the oracle's
+projection step followed by its prefill (oracle/projection.py).
+
+Two kinds of inputs:
+* exact: x and W with few significant bits, so that every partial sum of x W^T is exact in float32. The
+  tensor cores' accumulation order and rounding then cannot matter, and K and V are the oracle's to the
+  bit. The BF16 pages must match bit for bit; the INT2 history passes the write-path gate of the bulk
+  prefill (code flips <= 1e-4 from the float32 rotation, metadata fields <= 4e-3).
+* Gaussian: x ~ N(0, 1) and W ~ N(0, 1 / d_model), in bf16. Here the float32 accumulation differs from
+  the oracle's float64 sum by at most d_model 2^-23 sum_i |x_i w_i| (the bound used is 2^-12 sum_i |x_i
+  w_i| at d_model = 1024; near-cancelling sums may thus differ by many bf16 ulps), so every BF16 value
+  must be within one bf16 ulp of the oracle's plus that bound. The test reports how many values
+  differ at all. The history keeps the code gate (<= 1e-4 flips). Its metadata gate is 1e-2: with
+  about 4e-4 of the K / V values one or more bf16 ulps off, some 5 % of the rows hold one, and the
+  rotation spreads that change over all 128 channels, which moves a group's fp16 scale or zero
+  across a rounding boundary in roughly one such row in ten.
+Lengths cover a request shorter than the sink, one with no history, ragged history tiles, exact tile
+boundaries and several requests in one call.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import bit_kv_cache_decode_gb300 as osc
+    from gpu_cases import DEV, compare_int2_pools, head_params, pool_from_device, upload_params, with_codebooks
+from oracle import pool as P
+from oracle import projection as PR
+
+FMT = {"f16": 0, "u8": 1, "cb": 2}
+
+
+def _bf16(a):
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return ((a.view(np.uint32) + 0x7FFF + ((a.view(np.uint32) >> 16) & 1)) & 0xFFFF0000).view(np.float32)
+
+
+def _inputs(kind, seed, T, d, hkv):
+    rng = np.random.default_rng(seed)
+    if kind == "exact":
+        x = rng.integers(-3, 4, (T, d)).astype(np.float32) * 0.25
+        wk = rng.integers(-3, 4, (hkv * 128, d)).astype(np.float32) / 32.0
+        wv = rng.integers(-3, 4, (hkv * 128, d)).astype(np.float32) / 32.0
+    else:
+        x = _bf16(rng.standard_normal((T, d)))
+        wk = _bf16(rng.standard_normal((hkv * 128, d)) / np.sqrt(d))
+        wv = _bf16(rng.standard_normal((hkv * 128, d)) / np.sqrt(d))
+    return x, wk, wv
+
+
+def _bf16_up(a):
+    """the smallest bf16 value >= a, for a >= 0"""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32)
+    return ((u + 0xFFFF) & 0xFFFF0000).view(np.float32)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(DEV).to(torch.bfloat16)
+
+
+def _run(kind, lens, v_mode, meta, d=256, hkv=2, seed=71):
+    B = len(lens)
+    nh = [max(0, (L - 320 + 63) // 64) for L in lens]
+    mhp = max(1, max(nh))
+    n_int2, n_bf16 = sum(nh) + 1, 5 * B
+    perm_i = np.random.default_rng(seed).permutation(n_int2).astype(np.int32)
+    perm_b = np.random.default_rng(seed + 1).permutation(n_bf16).astype(np.int32)
+    hist_pt = np.full((B, mhp), -1, np.int32)
+    bf16_pt = perm_b.reshape(B, 5)
+    o = 0
+    for r in range(B):
+        hist_pt[r, :nh[r]] = perm_i[o:o + nh[r]]
+        o += nh[r]
+    cfg = osc.CacheConfig(num_layers=1, num_kv_heads=hkv, num_q_heads=4 * hkv, num_int2_pages=n_int2,
+                          num_bf16_pages=n_bf16, max_batch=B, max_splits=32, v_mode=v_mode, meta_format=FMT[meta])
+    cache = osc.OscarCache(cfg, device=DEV)
+    prm = head_params(seed, 0, hkv)
+    if meta == "cb":
+        prm = with_codebooks(seed, 0, prm)
+    upload_params(cache, 0, prm)
+    T = int(sum(lens))
+    x, wk, wv = _inputs(kind, seed, T, d, hkv)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    cache.project_quantize_prefill(0, _dev(x), _dev(wk), _dev(wv), cu, hist_pt, bf16_pt)
+    assert cache.get_status() == 0
+    geo = P.PoolGeometry(hkv=hkv, meta_format=meta)
+    ref = P.PoolModel(geo, n_int2, n_bf16)
+    for r in range(B):
+        PR.project_prefill(ref, x[cu[r]:cu[r + 1]], wk, wv, hist_pt[r], bf16_pt[r], prm, v_mode == osc.V_ABSORBED)
+    rows = [(int(hist_pt[r, h // 64]), h % 64) for r in range(B) for h in range(max(0, lens[r] - 320))]
+    # per element 2^-12 sum_i |x_i w_i|, placed in a pool like K and V (rounded up to bf16)
+    bnd = P.PoolModel(geo, n_int2, n_bf16)
+    for r in range(B):
+        xa = np.abs(x[cu[r]:cu[r + 1]]).astype(np.float64)
+        sk = (xa @ np.abs(wk).T.astype(np.float64)) * 2.0 ** -12 * 1.01
+        sv = (xa @ np.abs(wv).T.astype(np.float64)) * 2.0 ** -12 * 1.01
+        P.prefill(bnd, _bf16_up(sk).reshape(-1, hkv, 128), _bf16_up(sv).reshape(-1, hkv, 128), hist_pt[r], bf16_pt[r],
+                  prm, True)
+    return pool_from_device(cache, 0), ref, rows, prm, bnd
+
+
+LENS = [1, 63, 300, 64 + 128 * 3 + 40 + 256, 64 + 256 * 2 + 256, 1400]
+
+
+@pytest.mark.parametrize("meta", ["f16", "u8", "cb"])
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_fused_projection_exact_inputs(v_mode, meta):
+    got, ref, rows, prm, _ = _run("exact", LENS, v_mode, meta)
+    assert np.array_equal(got.bf16, ref.bf16)
+    compare_int2_pools(got, ref, rows, params=prm)
+
+
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_fused_projection_gaussian(v_mode):
+    got, ref, rows, prm, bnd = _run("gaussian", LENS, v_mode, "f16", d=1024)
+    g = P.bits_to_f64(got.bf16)
+    r = P.bits_to_f64(ref.bf16)
+    ulp = np.where(r != 0, 2.0 ** (np.floor(np.log2(np.abs(np.where(r != 0, r, 1.0)))) - 7), 2.0 ** -133)
+    assert np.all(np.abs(g - r) <= ulp + P.bits_to_f64(bnd.bf16))
+    diff = got.bf16 != ref.bf16
+    print(f"fused projection: {int(diff.sum())} of {diff.size} bf16 values differ from the float64 sums' "
+          f"({diff.mean():.2e})")
+    compare_int2_pools(got, ref, rows, params=prm, meta_tol=1e-2)
+
+
+def test_fused_projection_rejects_unsupported_shapes():
+    cfg = osc.CacheConfig(num_layers=1, num_kv_heads=2, num_q_heads=8, num_int2_pages=4, num_bf16_pages=5,
+                          max_batch=1, max_splits=32)
+    cache = osc.OscarCache(cfg, device=DEV)
+    upload_params(cache, 0, head_params(72, 0, 2))
+    x = torch.zeros(400, 96, dtype=torch.bfloat16, device=DEV)            # d_model not a multiple of 64
+    w = torch.zeros(256, 96, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(RuntimeError):
+        cache.project_quantize_prefill(0, x, w, w, np.array([0, 400], np.int32), np.arange(2, dtype=np.int32)[None],
+                                       np.arange(5, dtype=np.int32)[None])

@@ -61,7 +61,7 @@ WORKLOADS = {
     "qwen3_8b_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=32768, shared=0),
     "qwen3_8b_100k_l1": dict(layers=1, hq=32, hkv=8, batch=1, ctx=102400, shared=0),
     # ctx as (lo, hi): per-request lengths drawn uniformly, all requests prefilled by one bulk call
-    "qwen3_32b_mixed": dict(layers=1, hq=64, hkv=8, batch=8, ctx=(98304, 131072), shared=0),
+    "qwen3_32b_mixed": dict(layers=1, hq=64, hkv=8, batch=8, ctx=(98304, 131072), shared=0, d_model=5120),
     # the same shapes at a size an ncu capture of the prefill handles (about 0.3 GB of bf16 K and V)
     "qwen3_32b_mixed_b2": dict(layers=1, hq=64, hkv=8, batch=2, ctx=(30000, 34000), shared=0),
 }
@@ -73,6 +73,14 @@ def peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor throughput (TFLOP/s): the measured burst figure, else the recipe's fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -201,6 +209,7 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
     hp_d = torch.from_numpy(hist_pt).to(device)
     bp_d = torch.from_numpy(bf16_pt).to(device)
     prefill = {"ms": 0.0, "tokens": 0}
+    fused = {"ms": 0.0, "tokens": 0, "d_model": w.get("d_model", 0)}
     for layer in range(nl):
         cs = cals[layer * H:(layer + 1) * H]
         cache.set_rotation(layer, np.stack([c["U_K"] for c in cs]), np.stack([c["U_V"] for c in cs]),
@@ -216,6 +225,26 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
             cache.set_codebook(layer, np.stack([c["cb_k"] for c in cs]), np.stack([c["cb_v"] for c in cs]))
         outl = np.stack([synth.head_stats(seed, layer, h).outliers for h in range(H)])
         gen.manual_seed(seed * 1000003 + layer)
+        if mixed and fused["d_model"]:
+            # the fused projection + write path from synthetic hidden states (timed like the bulk prefill;
+            # the bulk prefill below then rewrites the pool with the workload's own K and V)
+            tot, dm = int(lens.sum()), fused["d_model"]
+            cu = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+            x = torch.randn(tot, dm, generator=gen, device=device).to(torch.bfloat16)
+            wk = (torch.randn(H * 128, dm, generator=gen, device=device) * dm ** -0.5).to(torch.bfloat16)
+            wv = (torch.randn(H * 128, dm, generator=gen, device=device) * dm ** -0.5).to(torch.bfloat16)
+            cache.project_quantize_prefill(layer, x, wk, wv, cu, hp_d, bp_d, total_tokens=tot)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record()
+            for _ in range(PREFILL_REPS):
+                cache.project_quantize_prefill(layer, x, wk, wv, cu, hp_d, bp_d, total_tokens=tot)
+            e1.record()
+            torch.cuda.synchronize()
+            fused["ms"] += e0.elapsed_time(e1) / PREFILL_REPS
+            fused["tokens"] += tot
+            del x, wk, wv
+            gen.manual_seed(seed * 1000003 + layer)
         if mixed:
             # all requests in one bulk prefill call, timed: its throughput is this workload's write-path figure
             tot = int(lens.sum())
@@ -255,7 +284,8 @@ def build_workload(name: str, seed: int, device, with_bf16: bool = True, steps_c
         torch.cuda.synchronize()
     if cache.get_status() != 0:
         raise RuntimeError("device status error while building the workload")
-    return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, lens=lens, prefill=prefill, B=B, H=H, hq=hq,
+    return dict(cache=cache, cfg=cfg, hist_pt=hp_d, bf16_pt=bp_d, L=L, lens=lens, prefill=prefill, fused=fused, B=B,
+                H=H, hq=hq,
                 layers=nl,
                 bf16_pages=bf16_pages, base_pt=(torch.from_numpy(bpt).to(device) if with_bf16 else None),
                 hist_np=hist_pt, bf16_np=bf16_pt, cals=cals, shared=shared, shp=shp)
@@ -415,6 +445,17 @@ def run_ours(args, rank: int, world: int, device):
                           "tokens_per_s": pf["tokens"] / (pf["ms"] / 1e3),
                           "algorithmic_bytes": moved, "gbs": moved / (pf["ms"] / 1e3) / 1e9,
                           "frac_of_peak": moved / (pf["ms"] / 1e3) / 1e9 / peak}
+    if wl["fused"]["tokens"]:
+        fz = wl["fused"]
+        flops = 2.0 * fz["tokens"] * fz["d_model"] * 2 * H * 128 * nl          # x W_k^T and x W_v^T
+        tpeak, tkind = bf16_peak()
+        moved = fz["tokens"] * fz["d_model"] * 2 + layer_bytes(wl["lens"], H, 0) * nl   # x read + pool written
+        res["fused_prefill"] = {"call": "oscar_project_quantize_prefill (x W^T, rotate, quantise, pack), one call per "
+                                        "layer", "d_model": fz["d_model"], "tokens": fz["tokens"], "ms": fz["ms"],
+                                "tokens_per_s": fz["tokens"] / (fz["ms"] / 1e3),
+                                "tflops": flops / (fz["ms"] / 1e3) / 1e12, "bound": "tensor",
+                                "frac_of_bf16_peak": flops / (fz["ms"] / 1e3) / 1e12 / tpeak, "peak_kind": tkind,
+                                "algorithmic_bytes": moved, "gbs": moved / (fz["ms"] / 1e3) / 1e9}
     res["e2e"] = run_e2e(wl, args, device, graph, kv_cur, q_cur, out, seq)
     if cache.get_status() != 0:
         raise RuntimeError("device status error during the end-to-end steps")

@@ -491,7 +491,13 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch of the 102,400-token
 # Qwen3-8B layer, per decode kernel, from the ncu captures summarised under profiles/, with the digest of the
 # CUDA sources each was taken on: a kernel changed since reports null until it is captured again.
-NCU_DECODE_TRAFFIC = {}
+NCU_DECODE_TRAFFIC = {
+    1: {"bytes_per_launch": 66765568 + 113920, "kernel": "k_decode_mma<1, 3, 0>",
+        "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+                   "--clock-control none -k regex:k_decode_mma -s 3 -c 1 python bench.py --workload "
+                   "qwen3_8b_100k_l1 --steps 3 --warmup 3 --no-bf16 --no-cpu",
+        "sources_sha256": "1bcb9a4d649c5f227a52a3c3691a6a29c1e5ed9f6e2f45cbf49f5da27e1fb903"},
+}
 
 # the sources each decode kernel is compiled from (its file and the headers it includes)
 DECODE_KERNEL_SOURCES = {

@@ -417,8 +417,7 @@ int oscar_profile_read(oscar_cache* cache, double* total_ms, int* launches);
  *    may be NULL) at the end of the call.
  * The call performs no cudaMalloc, cudaFree or other allocating call.
  * Set-up: the first call on a device resolves the array's address for that
- * device (cudaGetSymbolAddress) and configures the kernels; make that first
- * call before any stream capture. Every call shares the array and it keeps the
+ * device (cudaGetSymbolAddress) and configures the kernels. Every call shares the array and it keeps the
  * last call's contents (the status word is cleared at the start of each
  * call): calls that may overlap on the GPU (different streams, or threads
  * without ordering) race and give wrong results; calls ordered on one stream

@@ -496,7 +496,7 @@ NCU_DECODE_TRAFFIC = {
         "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                    "--clock-control none -k regex:k_decode_mma -s 3 -c 1 python bench.py --workload "
                    "qwen3_8b_100k_l1 --steps 3 --warmup 3 --no-bf16 --no-cpu",
-        "sources_sha256": "1bcb9a4d649c5f227a52a3c3691a6a29c1e5ed9f6e2f45cbf49f5da27e1fb903"},
+        "sources_sha256": "ab6b6f788ac72d81838233c2636c6ce565f55b0d5eed929173e4b3bead151d6d"},
 }
 
 # the sources each decode kernel is compiled from (its file and the headers it includes)

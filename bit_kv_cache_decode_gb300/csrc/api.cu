@@ -229,14 +229,16 @@ void choose_splits_tc(int B, int hkv, int max_pages, int max_splits, int sms, in
   *pps = (max_pages + *nsplit - 1) / *nsplit;
 }
 
-// Tensor-core split policy. A request's history pages are spread evenly over n splits of 4 warps,
-// a warp taking every fourth page of its split; the grid has B * hkv * (n + nbf) CTAs (the BF16
-// pages are light ones), ctas_per_sm resident per SM. A CTA's time is about its warps' rounds
-// (pages per warp), so n minimises waves x (rounds + 2 rounds of per-CTA cost: the first page's
-// latency, the warps' combine, one more merge slot), with at most
-// kMaxPagesPerMmaSplit pages per split when the split budget allows. The step prologue, which
-// runs as the decode is scheduled (2 CTAs per request and kv head), holds one decode CTA's
-// registers on each SM it occupies: the first wave has that many fewer slots.
+// Tensor-core split policy. A request's history pages are spread over n splits of 4 warps, a warp
+// taking every fourth page of its split. With n >= nbf the BF16 pages fold into the last nbf splits,
+// each kBf16FoldPages history pages lighter for it: the grid has B * hkv * n CTAs, all about equally
+// heavy, so the SMs finish together whichever CTAs they hold. With fewer splits each BF16 page takes a
+// light CTA of its own (B * hkv * (n + nbf) CTAs). ctas_per_sm are resident per SM. The kernel is
+// issue-bound, so an SM's time follows the pages it holds: n minimises waves x (pages per warp, as a
+// fraction, + 2 rounds of per-CTA cost: the first page's latency, the warps' combine, one more merge
+// slot), with at most kMaxPagesPerMmaSplit pages per split when the split budget allows. The step
+// prologue, which runs as the decode is scheduled (2 CTAs per request and kv head), holds one decode
+// CTA's registers on each SM it occupies: the first wave has that many fewer slots.
 void choose_splits_mma(int B, int hkv, int gq, int nbf, int max_pages, int max_splits, int sms, int* nsplit,
                        int* pps, int* occupancy) {
   *occupancy = gq <= 4 ? 3 : 2;                      // the kernel variants' resident CTAs per SM
@@ -249,11 +251,12 @@ void choose_splits_mma(int B, int hkv, int gq, int nbf, int max_pages, int max_s
     int best_n = nmax;
     long best_waves = 1;
     for (int n = 1; n <= nmax; ++n) {
-      const int per = (max_pages + n - 1) / n;
+      const bool fold = n >= nbf;
+      const int per = fold ? (max_pages + nbf * kBf16FoldPages + n - 1) / n : (max_pages + n - 1) / n;
       if (per > kMaxPagesPerMmaSplit && n < nmax) continue;
-      const long ctas = units * (n + nbf);
+      const long ctas = units * (fold ? n : n + nbf);
       const long waves = std::max(1L, (ctas + reserved + slots - 1) / slots);
-      const double cost = (double)waves * ((per + 3) / 4 + 2.0);
+      const double cost = (double)waves * (per / 4.0 + 2.0);   // issue-bound: an SM's pages, not its slowest warp
       if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_n = n; best_waves = waves; }
     }
     *waves_out = best_waves;

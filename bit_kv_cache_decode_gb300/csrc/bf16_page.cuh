@@ -18,8 +18,10 @@ struct FusedArgs {
   int len_add;                       // attend over seq_lens[b] + len_add tokens
   const int* hist_pt;
   int max_hist_pages;
-  int nsplit;                        // history CTAs per group; the next nbf CTAs take one BF16 page each
-  int nbf;
+  int nsplit;                        // history CTAs per group
+  int nbf;                           // BF16 pages per request
+  int bf_fold;                       // > 0: the last nbf history CTAs also take one BF16 page each and give up
+                                     // this many history pages for it; 0: the next nbf CTAs take one each
   int hist_start;                    // first history page of the splits (the pages before are shared ones)
   int bf_slot0;                      // partial slot of BF16 page 0
   const int* bf16_pt;

@@ -127,6 +127,24 @@ __device__ __forceinline__ uint32_t cb_lookup_sub(uint32_t lut, uint32_t sel) {
   return __byte_perm(lut, 0u, (sel & 0x0303u) | 0x4040u);
 }
 
+// First page (of n) of split s. Even: floor(s n / nsplit). Folded: the first nsplit - nbf splits take q
+// pages each and the last nbf take q - bf_fold (q chosen so the pages add up to n; if n is too short for
+// that, the light splits take none), the boundaries rounded down from the exact quotas.
+__device__ __forceinline__ int split_start(const FusedArgs& fa, int n, int s) {
+  if (fa.bf_fold <= 0) return (int)((long long)s * n / fa.nsplit);
+  if (s >= fa.nsplit) return n;
+  const int np = fa.nsplit - fa.nbf;                // splits without a BF16 page
+  const long long nb = fa.nbf, beta = fa.bf_fold;
+  // quotas as fractions over the common denominator: plain q = (n + nb beta) / nsplit, light q - beta;
+  // if n < np beta the light splits take nothing and the plain ones n / np
+  if ((long long)n >= (long long)np * beta || np == 0) {
+    const long long num = (long long)n + nb * beta;  // q = num / nsplit
+    if (s <= np) return (int)((long long)s * num / fa.nsplit);
+    return (int)(((long long)s * num - (long long)(s - np) * beta * fa.nsplit) / fa.nsplit);
+  }
+  return s <= np ? (int)((long long)s * n / np) : n;
+}
+
 // History split `split` of group (b, h): see the file comment. FMT: the pool's metadata format,
 // kFmtF16, kFmtU8 (compact (mn8, mx8) metadata, 4608-byte blocks staged in the same 5120-byte slots) or
 // kFmtCB (codebook levels k_c instead of the codes, fp16 range / 255 as the scale).
@@ -153,12 +171,13 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     npages = max_hist_pages;
     Lh = npages * kP;
   }
-  // The request's pages from hist_start on are spread evenly over the splits: split s starts at page
-  // hist_start + floor(s n / nsplit), n = npages - hist_start.
+  // The request's pages from hist_start on are spread over the splits: evenly (split s starts at page
+  // hist_start + floor(s n / nsplit), n = npages - hist_start), or, with the BF16 pages folded into the
+  // last nbf splits, with those splits bf_fold pages lighter (split_start).
   const int nown = npages - fa.hist_start;
   if (nown < 0 && tid == 0 && split == 0) flag(lv.status, OSCAR_STATUS_BAD_SEQLEN);   // shorter than the shared prefix
-  const int p0 = fa.hist_start + (int)((long long)split * max(nown, 0) / fa.nsplit) + w;
-  const int p1 = fa.hist_start + (int)((long long)(split + 1) * max(nown, 0) / fa.nsplit);
+  const int p0 = fa.hist_start + split_start(fa, max(nown, 0), split) + w;
+  const int p1 = fa.hist_start + split_start(fa, max(nown, 0), split + 1);
   const int my_pages = p0 < p1 ? (p1 - p0 + kWarps - 1) / kWarps : 0;
   const int* pt = hist_pt + (size_t)b * max_hist_pages;
 
@@ -591,8 +610,23 @@ __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWo
     __syncthreads();
   }
   pdl_launch_dependents();                         // the merge kernel may be scheduled now; it waits for this grid
-  if (blockIdx.x < fa.nsplit) int2_split<NT, FMT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
-  else bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
+  if (blockIdx.x < fa.nsplit) {
+    const int c = (int)blockIdx.x - (fa.nsplit - fa.nbf);
+    if (fa.bf_fold > 0 && c >= 0 && threadIdx.x == 0) {
+      // this split's BF16 page, read after its history pages: into L2 now (a hint; the append may still
+      // write one row of it, which L2 then holds)
+      const int page = fa.bf16_pt[(size_t)b * ((lv.sink + lv.recent) / kP) + c];
+      if (page >= 0 && page < lv.n_bf16)
+        l2_prefetch(lv.bf16 + ((size_t)page * lv.hkv + h) * kBf16BlockBytes, kBf16BlockBytes, l2_evict_last());
+    }
+    int2_split<NT, FMT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
+    if (fa.bf_fold > 0 && c >= 0) {              // this split's BF16 page, in the ring's memory
+      __syncthreads();
+      bf16_page(lv, ws, fa, smem, c, h, b);
+    }
+  } else {
+    bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);
+  }
   if (trace != nullptr && threadIdx.x == 0) trace[5] = global_ns();
 }
 
@@ -609,13 +643,14 @@ static cudaError_t launch_fmt(cudaLaunchConfig_t& cfg, const LayerView& lv, cons
 
 int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
                       cudaStream_t st) {
-  FusedArgs fa;
+  FusedArgs fa = {};
   fa.seq_lens = a.seq_lens;
   fa.len_add = a.len_add;
   fa.hist_pt = a.hist_pt;
   fa.max_hist_pages = a.max_hist_pages;
   fa.nsplit = a.nsplit;
   fa.nbf = a.nbf;
+  fa.bf_fold = a.nsplit >= a.nbf ? kBf16FoldPages : 0;
   fa.hist_start = a.shared_pages;
   fa.bf_slot0 = a.nsplit + a.nsplit_shared;
   fa.bf16_pt = a.bf16_pt;
@@ -629,7 +664,7 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(a.nsplit + a.nbf, lv.hkv, a.B);
+  cfg.gridDim = dim3(a.nsplit + (fa.bf_fold > 0 ? 0 : a.nbf), lv.hkv, a.B);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = kMmaSmem;
   cfg.stream = st;

@@ -551,7 +551,7 @@ bool decode_tc_supported(const LayerView& lv) {
 
 int launch_decode_tc(const LayerView& lv, const DecodeWorkspace& ws, const DecodeArgs& a, float scale_log2,
                      cudaStream_t st) {
-  FusedArgs fa;
+  FusedArgs fa = {};
   fa.seq_lens = a.seq_lens;
   fa.len_add = a.len_add;
   fa.hist_pt = a.hist_pt;

@@ -12,6 +12,10 @@ constexpr int kMaxMmaSplits = 2048;        // history splits of the fused decode
 // its error grows with the number of MMAs summed into one accumulator; longer
 // contexts take more splits, whose partials the merge adds with rounding.
 constexpr int kMaxPagesPerMmaSplit = 64;
+// a BF16 page folded into a history CTA of the fused decode costs about this many history pages of
+// that CTA's time (its bulk copies, waited on after the history loop, and its tensor-core products:
+// about 4 us on the 102,400-token Qwen3-8B layer, where a CTA's warps take some 2 us per page)
+constexpr int kBf16FoldPages = 8;
 // partial slots per (request, q head): history splits, then one per BF16 page
 inline int partial_slots(int max_splits, int nbf) { return max_splits + nbf; }
 constexpr int kPrefillTok = 1024;                                  // tokens per prefill CTA

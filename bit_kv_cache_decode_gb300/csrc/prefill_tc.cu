@@ -45,6 +45,11 @@ namespace {
 using namespace qtile;
 
 constexpr int kTile = kRows;                           // history rows per tile
+// relative cost of a K and a V item (a tile of one kind and head), from the CTAs' end times on the
+// 911,226-token Qwen3-32B-shaped batch: in V-absorbed mode a K item (24 MMAs) takes about 6 % longer
+// than a V item (8 MMAs and the channel transpose); in explicit-V mode a V item (rotation and transpose)
+// about 8 % longer than a K item
+constexpr long long kCostK = 106, kCostV = 100, kCostRot = 100, kCostVRot = 108;
 constexpr int kStages = 3;
 constexpr int kStageBytes = 2 * kBoxBytes;             // 32 KB
 constexpr int kYBufs = 4;                              // TMEM accumulators of 128 columns
@@ -161,8 +166,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   const int T = batch_tiles(lv, cu_seqlens, B);
-  const long long N = 2LL * lv.hkv * T;
-  const long long n0 = N * blockIdx.x / gridDim.x, n1 = N * (blockIdx.x + 1) / gridDim.x;
+  // CTA x takes the items of cost share [x W / grid, (x + 1) W / grid): the K items come first and cost
+  // kCostK each, the V items kCostV (V-absorbed: no rotation; explicit V: the rotation and the channel
+  // transpose), so that the CTAs of both kinds end together
+  const long long nk = (long long)lv.hkv * T;
+  const long long ck = lv.v_explicit ? kCostRot : kCostK, cv = lv.v_explicit ? kCostVRot : kCostV;
+  const long long W = nk * (ck + cv);
+  auto item_at = [&](long long cost) { return cost <= nk * ck ? cost / ck : nk + (cost - nk * ck) / cv; };
+  const long long n0 = item_at(W * blockIdx.x / gridDim.x);
+  const long long n1 = blockIdx.x + 1 == gridDim.x ? 2 * nk : item_at(W * (blockIdx.x + 1) / gridDim.x);
   const int cnt = (int)(n1 - n0);
   bool ok = true;
 
@@ -403,6 +415,10 @@ int launch_prefill(const LayerView& lv, int B, const void* k, const void* v, con
 }
 
 int configure_prefill_kernel() {
+  // the sink / recent copy runs beside the history kernel: with the largest shared-memory carveout an SM
+  // running one of its CTAs can also take a history CTA (206 KB) instead of waiting for it to finish
+  if (cudaFuncSetAttribute(k_prefill_bf16, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
   const bool ok =
       cudaFuncSetAttribute(k_prefill_tc<kFmtF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefSmem) ==
           cudaSuccess &&

@@ -66,14 +66,14 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// d = a * b + c with a separate accumulator input c
-__device__ __forceinline__ void mma16816_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                           uint32_t b0, uint32_t b1, const float (&c)[4]) {
+// d = a * b, the accumulator starting from zero
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%11,%12,%13};\n"
+      "{%10,%10,%10,%10};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -255,28 +255,19 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         qf[kb][nt][1] = v.y;
       }
   }
-  // cOff[G][nt]: the logits accumulators' start, minus the fragment offsets of
-  // group G in the accumulator layout (columns 2t, 2t+1 = high, low part)
-  float cF[NT], cZ0[NT], cZ1[NT], cOff[2][NT][4];
+  // the logits' scale and zero-point constants per head (the key operands carry no constant part, so
+  // each key tile's accumulator starts from zero)
+  float cF[NT], cZ0[NT], cZ1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = 4 * nt + t;
-    float o0h = 0.f, o0l = 0.f, o1h = 0.f, o1l = 0.f;
     cF[nt] = cZ0[nt] = cZ1[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
       cF[nt] = qc[kQF] * 16777216.f;               // 2^24: the codes (or levels) were fed as subnormals
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
-      o0h = qc[kQOff0H];
-      o0l = qc[kQOff0L];
-      o1h = qc[kQOff1H];
-      o1l = qc[kQOff1L];
     }
-    cOff[0][nt][0] = cOff[0][nt][2] = -o0h;
-    cOff[0][nt][1] = cOff[0][nt][3] = -o0l;
-    cOff[1][nt][0] = cOff[1][nt][2] = -o1h;
-    cOff[1][nt][1] = cOff[1][nt][3] = -o1l;
   }
 
   // ---- running state ----------------------------------------------------------------
@@ -350,8 +341,8 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              if (j == 0) mma16816_c(c[G][nt], a0, a1, a2, a3, qf[4 * G][nt][0], qf[4 * G][nt][1], cOff[G][nt]);
-              else mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+              if (j == 0) c[G][nt][0] = c[G][nt][1] = c[G][nt][2] = c[G][nt][3] = 0.f;
+              mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
             }
           }
         }
@@ -611,18 +602,20 @@ __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWo
   }
   pdl_launch_dependents();                         // the merge kernel may be scheduled now; it waits for this grid
   if (blockIdx.x < fa.nsplit) {
-    const int c = (int)blockIdx.x - (fa.nsplit - fa.nbf);
-    if (fa.bf_fold > 0 && c >= 0 && threadIdx.x == 0) {
+    if (fa.bf_fold > 0 && (int)blockIdx.x >= fa.nsplit - fa.nbf && threadIdx.x == 0) {
       // this split's BF16 page, read after its history pages: into L2 now (a hint; the append may still
       // write one row of it, which L2 then holds)
+      const int c = (int)blockIdx.x - (fa.nsplit - fa.nbf);
       const int page = fa.bf16_pt[(size_t)b * ((lv.sink + lv.recent) / kP) + c];
       if (page >= 0 && page < lv.n_bf16)
         l2_prefetch(lv.bf16 + ((size_t)page * lv.hkv + h) * kBf16BlockBytes, kBf16BlockBytes, l2_evict_last());
     }
     int2_split<NT, FMT>(lv, ws, fa, smem, blockIdx.x, h, b, trace);
-    if (fa.bf_fold > 0 && c >= 0) {              // this split's BF16 page, in the ring's memory
+    // this split's BF16 page, in the ring's memory (its index recomputed here: nothing stays live across
+    // the history loop)
+    if (fa.bf_fold > 0 && (int)blockIdx.x >= fa.nsplit - fa.nbf) {
       __syncthreads();
-      bf16_page(lv, ws, fa, smem, c, h, b);
+      bf16_page(lv, ws, fa, smem, (int)blockIdx.x - (fa.nsplit - fa.nbf), blockIdx.y, blockIdx.z);
     }
   } else {
     bf16_page(lv, ws, fa, smem, blockIdx.x - fa.nsplit, h, b);

@@ -492,11 +492,11 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # Qwen3-8B layer, per decode kernel, from the ncu captures summarised under profiles/, with the digest of the
 # CUDA sources each was taken on: a kernel changed since reports null until it is captured again.
 NCU_DECODE_TRAFFIC = {
-    1: {"bytes_per_launch": 66765568 + 113920, "kernel": "k_decode_mma<1, 3, 0>",
+    1: {"bytes_per_launch": 66782464 + 120064, "kernel": "k_decode_mma<1, 3, 0>",
         "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                    "--clock-control none -k regex:k_decode_mma -s 3 -c 1 python bench.py --workload "
                    "qwen3_8b_100k_l1 --steps 3 --warmup 3 --no-bf16 --no-cpu",
-        "sources_sha256": "ab6b6f788ac72d81838233c2636c6ce565f55b0d5eed929173e4b3bead151d6d"},
+        "sources_sha256": "5c0e2a999e305ae42a1b89e81aca6930d17188b16e4c17fd5a0aabd6ac278f57"},
 }
 
 # the sources each decode kernel is compiled from (its file and the headers it includes)

@@ -163,11 +163,16 @@ __device__ __forceinline__ void quantise_group(uint32_t ty, const float* prm, in
     }
     const float rh4 = __fmul_rn(rh, 0.25f), rl4 = __fmul_rn(rl, 0.25f);
     const float* cbc = prm + kCbOff + kind * 8;
-    // the quotient is monotone in y: unless the group's largest one rounds past 3, no code needs the
-    // upper clamp (it takes fp16 rounding of a narrow group's scale and zero to get there)
-    const float dmax = __fsub_rn(mx, zq);
+    // the quotient is monotone in y: unless the group's smallest one rounds below 0 or its largest past
+    // 3 (it takes fp16 rounding of a narrow group's scale and zero to get there), no code needs a clamp,
+    // and the codes come from packed pairs of adjacent values (no saturating form exists for those)
+    const float dmax = __fsub_rn(mx, zq), dmin = __fsub_rn(mn, zq);
     const bool hi_clamp = __fmaf_rn(dmax, rh, __fmul_rn(dmax, rl)) >= 3.5f;
+    const bool lo_clamp = __fmaf_rn(dmin, rh, __fmul_rn(dmin, rl)) < -0.5f;
     const bool any_hi = __any_sync(0xffffffffu, hi_clamp);
+    const bool all_in = !__any_sync(0xffffffffu, hi_clamp || lo_clamp);
+    const float2 nzq2 = make_float2(-zq, -zq), rh2 = make_float2(rh, rh), rl2 = make_float2(rl, rl),
+                 mg2 = make_float2(kMagic, kMagic);
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
       float y[32];
@@ -187,7 +192,16 @@ __device__ __forceinline__ void quantise_group(uint32_t ty, const float* prm, in
         } else {
           // q/4 = sat(q / 4) (the scaling by 4 is exact), t = 4 (q/4) + kMagic rounds half to even;
           // min(t, kMagic + 3) clamps the code where a group needs it
-          if (any_hi) {
+          if (FMT == kFmtF16 && all_in) {
+            // every quotient in [-0.5, 3.5): t = q + kMagic needs no clamp (-0.5 rounds to -0, code 0)
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+              const float2 dd = __fadd2_rn(make_float2(y[16 * q2 + m], y[16 * q2 + m + 1]), nzq2);
+              const float2 t = __fadd2_rn(__ffma2_rn(dd, rh2, __fmul2_rn(dd, rl2)), mg2);
+              acc += __float_as_uint(t.x) << (2 * m);
+              acc += __float_as_uint(t.y) << (2 * m + 2);
+            }
+          } else if (any_hi) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
               const float q4 = __saturatef(__fmaf_rn(__fsub_rn(y[16 * q2 + m], zq), rh4,

@@ -23,10 +23,12 @@
 //    takes back 2^24 (codebook pools feed 1024 + k_c and subtract per-head
 //    offsets instead);
 //  * P.Vhat: A = codes [16 channels x 16 tokens] (the V page layout pairs two
-//    tokens in one 32-bit word, so mask | 0x6400 and one HFMA2 give the exact
-//    fp16 codes of one channel for two tokens), B = p * scale [16 tokens x 8
-//    columns], built from the logits' accumulator layout with two movmatrix
-//    transposes; the zero-point part sum_t p_t z_t is accumulated in fp32.
+//    tokens in one 32-bit word, so one AND gives the codes of one channel for
+//    two tokens, as fp16 subnormals c 4^pos 2^-24 like the keys'), B = p *
+//    scale * 4^-pos * 2^sw [16 tokens x 8 columns], sw a per-head power of two
+//    from the largest V clip threshold, built from the logits' accumulator
+//    layout with two movmatrix transposes; the zero-point part sum_t p_t z_t is
+//    accumulated in fp32. Codebook pools feed their levels exactly instead.
 // A history CTA ends with a combine of its 4 warps' online-softmax partials
 // and writes one partial (m, l, acc[128]) per query head and split.
 //
@@ -46,7 +48,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kStages = 2;
-constexpr uint32_t kMagic = 0x64006400u;       // fp16 1024.0 in both halves
 // stage ring, mbarriers, a timeout flag, and slack to align the ring to 128 bytes
 constexpr int kMmaSmem = kWarps * kStages * kBlockBytes + kWarps * kStages * 8 + 16 + 128;
 
@@ -66,16 +67,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// d = a * b, the accumulator starting from zero
-__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                           uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%10,%10,%10};\n"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
-}
-
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t d;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(x));
@@ -85,13 +76,6 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// (x & mask) | magic as one three-input logic op (LUT 0xEA = (a & b) | c)
-__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t mask, uint32_t magic) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(mask), "r"(magic));
-  return d;
 }
 
 // exact fp16 codes: ((1024 + c*4^k) * 4^-k) - 1024*4^-k = c, for both halves
@@ -221,6 +205,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   };
 
   // ---- per-lane constants -------------------------------------------------------
+  // largest V clip threshold of the head (every warp reduces all 128): it bounds every V scale, hence
+  // the P.V weights' range (below)
+  float4 tv4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (!CB) tv4 = *reinterpret_cast<const float4*>(lv.params + (size_t)h * kParamFloats + kTauVOff + 4 * lane);
   float kmc[6], vmc[6];                // compact format: {T, D, E} of groups 0, 1 for K and for V
   uint32_t klut = 0, vlut = 0;         // codebook format: the bytes k_0 .. k_3 of K and of V
   if constexpr (CB) {
@@ -268,6 +256,25 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       cZ0[nt] = qc[kQZ0];
       cZ1[nt] = qc[kQZ1];
     }
+  }
+
+  // P.V weights (non-codebook formats): the V codes are fed like the keys', as fp16 subnormals
+  // c 4^pos 2^-24 masked in place, so the weights of the tokens at code position pos carry
+  // 4^-pos 2^sw. With s < 2^e (s <= fp16(2 tau_max / 3), tau_max < 2^e) and p <= 1, sw = 15 - e keeps
+  // every weight below 2^15; the accumulators then hold sum p s c 2^(sw - 24).
+  float wsc = 1.f, wback = 1.f;
+  if constexpr (!CB) {
+    float tv = fmaxf(fmaxf(fabsf(tv4.x), fabsf(tv4.y)), fmaxf(fabsf(tv4.z), fabsf(tv4.w)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tv = fmaxf(tv, __shfl_xor_sync(0xffffffffu, tv, o));
+    int sw = 0;
+    if (tv > 0.f && tv < INFINITY) {
+      int e;
+      frexpf(tv, &e);                              // tv = m 2^e, 0.5 <= m < 1
+      sw = min(max(15 - e, -60), 60);
+    }
+    wsc = exp2f((float)sw);
+    wback = exp2f((float)(24 - sw));
   }
 
   // ---- running state ----------------------------------------------------------------
@@ -448,8 +455,14 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           zacc[nt][0] = fmaf(pa, sv00.y, fmaf(pb, sv10.y, zacc[nt][0]));
           zacc[nt][1] = fmaf(pa, sv01.y, fmaf(pb, sv11.y, zacc[nt][1]));
           // lane (g, t): the weights of token row g (rows 0-7) and g + 8 of the tile for head t, groups 0 and 1;
-          // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'
-          const float x0 = pa * sv00.x, x1 = pa * sv01.x, x2 = pb * sv10.x, x3 = pb * sv11.x;
+          // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'.
+          // Rows g sit at code position 2 (kt & 1) of their V word, rows g + 8 one position higher.
+          float fa_ = pa, fb_ = pb;
+          if constexpr (!CB) {
+            fa_ = pa * (wsc * ((kt & 1) ? 1.f / 16.f : 1.f));
+            fb_ = pb * (wsc * ((kt & 1) ? 1.f / 64.f : 1.f / 4.f));
+          }
+          const float x0 = fa_ * sv00.x, x1 = fa_ * sv01.x, x2 = fb_ * sv10.x, x3 = fb_ * sv11.x;
           const uint32_t h01 = pack_f16x2(x0, x1), h23 = pack_f16x2(x2, x3);
           bf[kt][nt][0] = movmatrix_t(h01);
           bf[kt][nt][1] = movmatrix_t(h23);
@@ -482,11 +495,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             a2 = exact_codes(cb_lookup(vlut, sel(xa[hh], pp + 1)), 4);
             a3 = exact_codes(cb_lookup(vlut, sel(xb[hh], pp + 1)), 4);
           } else {
-            // exact fp16 codes c from the masked bits: (1024 + c 4^p) 4^-p - 1024 4^-p
-            a0 = exact_codes(and_or(xa[hh], 0x00030003u << (2 * pp), kMagic), pp);
-            a1 = exact_codes(and_or(xb[hh], 0x00030003u << (2 * pp), kMagic), pp);
-            a2 = exact_codes(and_or(xa[hh], 0x00030003u << (2 * pp + 2), kMagic), pp + 1);
-            a3 = exact_codes(and_or(xb[hh], 0x00030003u << (2 * pp + 2), kMagic), pp + 1);
+            // the masked bits as fp16 subnormals c 4^p 2^-24 (the weights carry 4^-p)
+            a0 = xa[hh] & (0x00030003u << (2 * pp));
+            a1 = xb[hh] & (0x00030003u << (2 * pp));
+            a2 = xa[hh] & (0x00030003u << (2 * pp + 2));
+            a3 = xb[hh] & (0x00030003u << (2 * pp + 2));
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -540,10 +553,10 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     float v[16];                                  // channels 16g .. 16g + 15
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      // the accumulators hold sum p s c exactly scaled (the codebook build feeds its levels / 256 and its
-      // P operand carries the 256): add the zero-point part
-      v[mt] = (grp ? acc[nt][mt][1] : acc[nt][mt][0]) + zs;
-      v[8 + mt] = (grp ? acc[nt][mt][3] : acc[nt][mt][2]) + zs;
+      // the accumulators hold sum p s c 2^(sw - 24) (the codebook build: exactly scaled, its levels fed / 256
+      // and its P operand carrying the 256): scale back, add the zero-point part
+      v[mt] = fmaf(grp ? acc[nt][mt][1] : acc[nt][mt][0], wback, zs);
+      v[8 + mt] = fmaf(grp ? acc[nt][mt][3] : acc[nt][mt][2], wback, zs);
     }
     float4* dst = reinterpret_cast<float4*>(ca + (w * 8 + head) * kCaStride + 16 * g);
 #pragma unroll

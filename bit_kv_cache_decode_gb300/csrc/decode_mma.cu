@@ -32,10 +32,11 @@
 // A history CTA ends with a combine of its 4 warps' online-softmax partials
 // and writes one partial (m, l, acc[128]) per query head and split.
 //
-// The same launch carries the BF16 sink + recent tokens as one extra CTA per
-// BF16 page (row-wise bulk copies, tensor-core products). The log-sum-exp merge of
-// all slots runs as the next kernel (merge.cu), a programmatic dependent that
-// is scheduled while this grid runs and waits for its completion.
+// The same launch carries the BF16 sink + recent tokens (row-wise bulk copies,
+// tensor-core products), folded into the last history splits or as one extra
+// CTA per BF16 page. The log-sum-exp merge of all slots runs as the next
+// kernel (merge.cu), a programmatic dependent that is scheduled while this
+// grid runs and waits for its completion.
 #include "kernels.cuh"
 #include "bf16_page.cuh"
 #include "rotate.cuh"
@@ -47,9 +48,13 @@ namespace oscar {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 2;
-// stage ring, mbarriers, a timeout flag, and slack to align the ring to 128 bytes
-constexpr int kMmaSmem = kWarps * kStages * kBlockBytes + kWarps * kStages * 8 + 16 + 128;
+constexpr int kStages = 2;                     // pages per warp: one in use, one in flight
+// stage ring, mbarriers, a timeout flag, per warp the float32 metadata rows of its current page
+// ([K, V][64 rows] x (scale, zero of group 0, scale, zero of group 1)), and slack to align to 128 bytes
+constexpr int kMeta32Off = kWarps * kStages * kBlockBytes + kWarps * kStages * 8 + 16;
+constexpr int kMeta32Bytes = 2 * kP * 16;
+static_assert(kMeta32Off % 16 == 0, "float4 metadata rows");
+constexpr int kMmaSmem = kMeta32Off + kWarps * kMeta32Bytes + 128;
 
 // 2^x with the SFU (inputs are logit differences <= 0 or -inf)
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -65,6 +70,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d = a * b: the accumulator input is the constant zero (no registers to clear first)
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -194,14 +209,17 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   // pages the preceding append cannot touch are fetched: it writes one row of
   // the last history page (the demoted token).
   // Page ids are read from the page table a stage ahead of their use.
-  const int pid0 = my_pages > 0 ? pt[p0] : 0;
-  const int pid1 = my_pages > 1 ? pt[p0 + kWarps] : 0;
-  if (my_pages > 0 && p0 < npages - 1 && issue(0, pid0)) issued |= 1u;
+  int pids[kStages];
+#pragma unroll
+  for (int k = 0; k < kStages; ++k) pids[k] = k < my_pages ? pt[p0 + kWarps * k] : 0;
+  if (my_pages > 0 && p0 < npages - 1 && issue(0, pids[0])) issued |= 1u;
   pdl_wait();
-  if (my_pages > 0 && p0 >= npages - 1 && issue(0, pid0)) issued |= 1u;
-  static_assert(kStages == 2, "the prologue requests pages 0 and 1");
-  auto issue_rest = [&]() {            // page 1, once page 0 is in (or was never requested)
-    if (1 < my_pages && issue(1, pid1)) issued |= 2u;
+  if (trace != nullptr && tid == 0) trace[7] = global_ns();                  // the programmatic wait returned
+  if (my_pages > 0 && p0 >= npages - 1 && issue(0, pids[0])) issued |= 1u;
+  auto issue_rest = [&]() {            // pages 1 .. kStages - 1, once page 0 is in (or was never requested)
+#pragma unroll
+    for (int k = 1; k < kStages; ++k)
+      if (k < my_pages && issue(k, pids[k])) issued |= 1u << k;
   };
 
   // ---- per-lane constants -------------------------------------------------------
@@ -245,16 +263,19 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   }
   // the logits' scale and zero-point constants per head (the key operands carry no constant part, so
   // each key tile's accumulator starts from zero)
+  // The logit is cF (s0 a0 + s1 a1 + z0 cZ0 / cF + z1 cZ1 / cF): the page keeps the bracket (X), the
+  // softmax applies cF (> 0) to its maximum and inside the exponential. Heads past the group: cF = 1, cZ = 0.
   float cF[NT], cZ0[NT], cZ1[NT];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int head = 4 * nt + t;
-    cF[nt] = cZ0[nt] = cZ1[nt] = 0.f;
+    cF[nt] = 1.f;
+    cZ0[nt] = cZ1[nt] = 0.f;
     if (head < gq) {
       const float* qc = ws.qconst + ((size_t)b * lv.hq + h * gq + head) * kQConst;
       cF[nt] = qc[kQF] * 16777216.f;               // 2^24: the codes (or levels) were fed as subnormals
-      cZ0[nt] = qc[kQZ0];
-      cZ1[nt] = qc[kQZ1];
+      cZ0[nt] = __fdiv_rn(qc[kQZ0], cF[nt]);
+      cZ1[nt] = __fdiv_rn(qc[kQZ1], cF[nt]);
     }
   }
 
@@ -276,6 +297,13 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     wsc = exp2f((float)sw);
     wback = exp2f((float)(24 - sw));
   }
+  // this lane converts metadata rows lane and lane + 32 of each page: their V scales carry the weight
+  // factor of their code position 2 ((row >> 4) & 1) + ((row >> 3) & 1) (the same for both rows;
+  // codebook: 256 / 255 instead), their K scales 1 / 255 in the codebook format
+  const int vpos = 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);
+  const float vfac = CB ? 256.f / 255.f : wsc * exp2f(-2.f * (float)vpos);
+  const float kfac = CB ? 1.f / 255.f : 1.f;
+  float4* meta_w = reinterpret_cast<float4*>(smem + kMeta32Off + w * kMeta32Bytes);   // [K, V][64 rows]
 
   // ---- running state ----------------------------------------------------------------
   float acc[NT][8][4];
@@ -295,8 +323,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
   uint32_t phase = 0;
   bool timed_out = false;
 
-  for (int i = 0; i < my_pages; ++i) {
-    const int s = i % kStages;
+  for (int i = 0, s = 0; i < my_pages; ++i, s = (s + 1 == kStages) ? 0 : s + 1) {   // s = i % kStages
     const int pid_ahead = (i + kStages < my_pages) ? pt[p0 + kWarps * (i + kStages)] : 0;   // used after this page
     if (issued & (1u << s)) {
       const bool landed = __all_sync(0xffffffffu, mbar_wait(bar_s + 8 * s, (phase >> s) & 1u));
@@ -310,6 +337,46 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
       if (i == 0) issue_rest();
       const uint8_t* blk = stage0 + s * kBlockBytes;
       const int ntok = min(kP, Lh - (p0 + kWarps * i) * kP);
+
+      // ---- the page's metadata as float32 rows, converted once for the warp (rows past the end zero) ----
+#pragma unroll
+      for (int kind = 0; kind < 2; ++kind) {
+        float4 m[2];                               // rows lane, lane + 32
+        if constexpr (U8) {
+          const uint8_t* mb = blk + (kind ? kVMetaOffU8 : kKMetaOff);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            float2 g0, g1;
+            u8_row_meta(*reinterpret_cast<const uint32_t*>(mb + 4 * (lane + 32 * r)), kind ? vmc : kmc, g0, g1);
+            m[r] = make_float4(g0.x, g0.y, g1.x, g1.y);
+          }
+        } else {
+          const uint8_t* mb = blk + (kind ? kVMetaOff : kKMetaOff);
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint2 u = *reinterpret_cast<const uint2*>(mb + 8 * (lane + 32 * r));
+            const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            m[r] = make_float4(a0.x, a0.y, a1.x, a1.y);
+          }
+        }
+        const float f = kind ? vfac : kfac;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          if (kind == 1 || CB) {
+            m[r].x = __fmul_rn(m[r].x, f);
+            m[r].z = __fmul_rn(m[r].z, f);
+          }
+        }
+        if (ntok < kP) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+            if (lane + 32 * r >= ntok) m[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        meta_w[kind * kP + lane] = m[0];
+        meta_w[kind * kP + lane + 32] = m[1];
+      }
+      __syncwarp();
 
       // ---- logits of the page's 64 tokens -----------------------------------------
       float lg[4][NT][2];
@@ -348,35 +415,20 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              if (j == 0) c[G][nt][0] = c[G][nt][1] = c[G][nt][2] = c[G][nt][3] = 0.f;
-              mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+              if (j == 0) mma16816_z(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
+              else mma16816(c[G][nt], a0, a1, a2, a3, qf[4 * G + j][nt][0], qf[4 * G + j][nt][1]);
             }
           }
         }
-        float2 sz00, sz01, sz10, sz11;             // (scale, zero) of groups 0, 1 of rows r0, r1
-        if constexpr (U8) {
-          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kKMetaOff + r0 * 4), kmc, sz00, sz01);
-          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kKMetaOff + r1 * 4), kmc, sz10, sz11);
-        } else {
-          const uint2 mk0 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r0 * 8);
-          const uint2 mk1 = *reinterpret_cast<const uint2*>(blk + kKMetaOff + r1 * 8);
-          sz00 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.x));
-          sz01 = __half22float2(*reinterpret_cast<const __half2*>(&mk0.y));
-          sz10 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.x));
-          sz11 = __half22float2(*reinterpret_cast<const __half2*>(&mk1.y));
-          if constexpr (CB) {                      // range / 255: the dequantised value is zero + that * k_c
-            sz00.x = __fmul_rn(sz00.x, 1.f / 255.f);
-            sz01.x = __fmul_rn(sz01.x, 1.f / 255.f);
-            sz10.x = __fmul_rn(sz10.x, 1.f / 255.f);
-            sz11.x = __fmul_rn(sz11.x, 1.f / 255.f);
-          }
-        }
+        // (scale, zero of group 0, scale, zero of group 1) of rows r0, r1 (codebook: scale = range / 255, the
+        // dequantised value being zero + scale k_c)
+        const float4 k0 = meta_w[r0], k1 = meta_w[r1];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const float a00 = c[0][nt][0] + c[0][nt][1], a01 = c[1][nt][0] + c[1][nt][1];   // row r0: hi + lo per group
           const float a10 = c[0][nt][2] + c[0][nt][3], a11 = c[1][nt][2] + c[1][nt][3];   // row r1
-          lg[mt][nt][0] = fmaf(cF[nt], fmaf(sz00.x, a00, sz01.x * a01), fmaf(sz00.y, cZ0[nt], sz01.y * cZ1[nt]));
-          lg[mt][nt][1] = fmaf(cF[nt], fmaf(sz10.x, a10, sz11.x * a11), fmaf(sz10.y, cZ0[nt], sz11.y * cZ1[nt]));
+          lg[mt][nt][0] = fmaf(k0.x, a00, fmaf(k0.z, a01, fmaf(k0.y, cZ0[nt], k0.w * cZ1[nt])));
+          lg[mt][nt][1] = fmaf(k1.x, a10, fmaf(k1.z, a11, fmaf(k1.y, cZ0[nt], k1.w * cZ1[nt])));
         }
         if (ntok < kP) {                           // ragged last page: rows past the end take no weight
 #pragma unroll
@@ -398,7 +450,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mnew[nt] = fmaxf(mrun[nt], mx);
+        mnew[nt] = fmaxf(mrun[nt], cF[nt] * mx);
         grow |= mnew[nt] > mrun[nt];
       }
       if (__any_sync(0xffffffffu, grow)) {
@@ -425,44 +477,19 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
 #pragma unroll
       for (int kt = 0; kt < 4; ++kt) {
         const int r0 = 16 * kt + g, r1 = r0 + 8;
-        float2 sv00, sv01, sv10, sv11;
-        if constexpr (U8) {
-          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kVMetaOffU8 + r0 * 4), vmc, sv00, sv01);
-          u8_row_meta(*reinterpret_cast<const uint32_t*>(blk + kVMetaOffU8 + r1 * 4), vmc, sv10, sv11);
-        } else {
-          const uint2 mv0 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r0 * 8);
-          const uint2 mv1 = *reinterpret_cast<const uint2*>(blk + kVMetaOff + r1 * 8);
-          sv00 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.x));
-          sv01 = __half22float2(*reinterpret_cast<const __half2*>(&mv0.y));
-          sv10 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.x));
-          sv11 = __half22float2(*reinterpret_cast<const __half2*>(&mv1.y));
-          if constexpr (CB) {                      // range * 256 / 255: the V operand holds k_c / 256
-            sv00.x = __fmul_rn(sv00.x, 256.f / 255.f);
-            sv01.x = __fmul_rn(sv01.x, 256.f / 255.f);
-            sv10.x = __fmul_rn(sv10.x, 256.f / 255.f);
-            sv11.x = __fmul_rn(sv11.x, 256.f / 255.f);
-          }
-        }
-        if (ntok < kP) {                           // rows past the end: no stale metadata
-          if (r0 >= ntok) sv00 = sv01 = make_float2(0.f, 0.f);
-          if (r1 >= ntok) sv10 = sv11 = make_float2(0.f, 0.f);
-        }
+        // (scale x weight factor, zero) of groups 0, 1 of rows r0, r1 (codebook: range x 256 / 255, the V
+        // operand holding k_c / 256); zero rows past the end
+        const float4 v0 = meta_w[kP + r0], v1 = meta_w[kP + r1];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float pa = fast_exp2(lg[kt][nt][0] - mrun[nt]);
-          const float pb = fast_exp2(lg[kt][nt][1] - mrun[nt]);
+          const float pa = fast_exp2(fmaf(cF[nt], lg[kt][nt][0], -mrun[nt]));
+          const float pb = fast_exp2(fmaf(cF[nt], lg[kt][nt][1], -mrun[nt]));
           lsum[nt] += pa + pb;
-          zacc[nt][0] = fmaf(pa, sv00.y, fmaf(pb, sv10.y, zacc[nt][0]));
-          zacc[nt][1] = fmaf(pa, sv01.y, fmaf(pb, sv11.y, zacc[nt][1]));
+          zacc[nt][0] = fmaf(pa, v0.y, fmaf(pb, v1.y, zacc[nt][0]));
+          zacc[nt][1] = fmaf(pa, v0.w, fmaf(pb, v1.w, zacc[nt][1]));
           // lane (g, t): the weights of token row g (rows 0-7) and g + 8 of the tile for head t, groups 0 and 1;
-          // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'.
-          // Rows g sit at code position 2 (kt & 1) of their V word, rows g + 8 one position higher.
-          float fa_ = pa, fb_ = pb;
-          if constexpr (!CB) {
-            fa_ = pa * (wsc * ((kt & 1) ? 1.f / 16.f : 1.f));
-            fb_ = pb * (wsc * ((kt & 1) ? 1.f / 64.f : 1.f / 4.f));
-          }
-          const float x0 = fa_ * sv00.x, x1 = fa_ * sv01.x, x2 = fb_ * sv10.x, x3 = fb_ * sv11.x;
+          // the transposes give lane (g', t') B rows k = (2t', 2t'+1) and (2t'+8, 2t'+9) of column g'
+          const float x0 = pa * v0.x, x1 = pa * v0.z, x2 = pb * v1.x, x3 = pb * v1.z;
           const uint32_t h01 = pack_f16x2(x0, x1), h23 = pack_f16x2(x2, x3);
           bf[kt][nt][0] = movmatrix_t(h01);
           bf[kt][nt][1] = movmatrix_t(h23);
@@ -563,17 +590,19 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
   __syncthreads();
-  for (int hh = 0; hh < gq; ++hh) {
+  // the query heads unrolled (gq <= 4 NT), so that their shared-memory loads and exponentials overlap
+  const bool ok = !any_timeout;
+#pragma unroll
+  for (int hh = 0; hh < 4 * NT; ++hh) {
+    if (hh >= gq) break;
     float M = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, cm[ww * 8 + hh]);
     float Ls = 0.f, A = 0.f;
-    if (M != -INFINITY && !any_timeout) {
+    if (M != -INFINITY && ok) {
 #pragma unroll
       for (int ww = 0; ww < kWarps; ++ww) {
-        const float mw = cm[ww * 8 + hh];
-        if (mw == -INFINITY) continue;
-        const float f = exp2f(mw - M);
+        const float f = fast_exp2(cm[ww * 8 + hh] - M);    // 0 for a warp without pages (m = -inf)
         Ls = fmaf(cl[ww * 8 + hh], f, Ls);
         A = fmaf(ca[(ww * 8 + hh) * kCaStride + tid], f, A);
       }
@@ -600,7 +629,8 @@ __global__ void __launch_bounds__(128, MINB) k_decode_mma(LayerView lv, DecodeWo
   const int h = blockIdx.y, b = blockIdx.z;
   // optional timeline record of this CTA (ns, %globaltimer):
   // [0] linear CTA id, [1] SM id, [2] start, [3] first history page landed (warp 0),
-  // [4] last warp's main loop done, [5] partials written, [6], [7] 0
+  // [4] last warp's main loop done, [5] partials written, [6] 0, [7] the programmatic wait returned
+  // (history CTAs)
   const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   unsigned long long* trace =
       (ws.cta_trace != nullptr && (int)cta < ws.trace_cap) ? ws.cta_trace + 8ull * cta : nullptr;
@@ -675,7 +705,9 @@ int launch_decode_mma(const LayerView& lv, const DecodeWorkspace& ws, const Deco
   cfg.dynamicSmemBytes = kMmaSmem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // right behind a profiling event the launch is ordered after the prologue anyway: without the attribute
+  // (which lets it start early only behind a kernel)
+  cfg.numAttrs = (a.ev0 != nullptr && a.nsplit_shared == 0) ? 0 : 1;
   cudaError_t e;
   if (lv.meta_u8) e = launch_fmt<kFmtU8>(cfg, lv, ws, fa, a.mma_occupancy);
   else if (lv.meta_cb) e = launch_fmt<kFmtCB>(cfg, lv, ws, fa, a.mma_occupancy);

@@ -626,7 +626,7 @@ int launch_decode_shared(const LayerView& lv, const DecodeWorkspace& ws, const D
   cfg.dynamicSmemBytes = kShSmem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.ev0 != nullptr ? 0 : 1;        // right behind a profiling event: as in launch_decode_mma
   return cudaLaunchKernelEx(&cfg, k_decode_shared, lv, ws, sa) == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }
 

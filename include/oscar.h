@@ -436,8 +436,8 @@ int oscar_decode_attention_noalloc(const oscar_layout* layout, void* pool, int l
  * (each launch overwrites it): for CTA i (linear block index) the eight
  * uint64 values at buf[8 i] are its id, SM id, start time, time its first
  * history page landed, time its last warp finished the main loop, time its
- * partials were written, time it finished the merge (last CTA of a request /
- * kv-head group only, else 0) and 0; times are %globaltimer nanoseconds.
+ * partials were written, 0, and the time its wait for the kernel before it
+ * returned (history CTAs); times are %globaltimer nanoseconds.
  * buf: device memory for `capacity` records (64 bytes each); NULL stops
  * recording. CTAs beyond `capacity` are not recorded. */
 int oscar_trace_ctas(oscar_cache* cache, void* buf, int capacity);

@@ -49,6 +49,7 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kStages = 2;                     // pages per warp: one in use, one in flight
+constexpr float kLag = 8.f;                     // the softmax reference may lag the maximum by 2^kLag
 // stage ring, mbarriers, a timeout flag, per warp the float32 metadata rows of its current page
 // ([K, V][64 rows] x (scale, zero of group 0, scale, zero of group 1)), and slack to align to 128 bytes
 constexpr int kMeta32Off = kWarps * kStages * kBlockBytes + kWarps * kStages * 8 + 16;
@@ -279,10 +280,13 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     }
   }
 
+  // the softmax reference's lag (the codebook format, whose weights' low parts matter, keeps p <= 1)
+  constexpr float lag = CB ? 0.f : kLag;
   // P.V weights (non-codebook formats): the V codes are fed like the keys', as fp16 subnormals
   // c 4^pos 2^-24 masked in place, so the weights of the tokens at code position pos carry
-  // 4^-pos 2^sw. With s < 2^e (s <= fp16(2 tau_max / 3), tau_max < 2^e) and p <= 1, sw = 15 - e keeps
-  // every weight below 2^15; the accumulators then hold sum p s c 2^(sw - 24).
+  // 4^-pos 2^sw. With s < 2^e (s <= fp16(2 tau_max / 3), tau_max < 2^e) and p < 2^kLag (the softmax
+  // below), sw = 15 - e - kLag keeps every weight below 2^15; the accumulators then hold
+  // sum p s c 2^(sw - 24).
   float wsc = 1.f, wback = 1.f;
   if constexpr (!CB) {
     float tv = fmaxf(fmaxf(fabsf(tv4.x), fabsf(tv4.y)), fmaxf(fabsf(tv4.z), fabsf(tv4.w)));
@@ -292,7 +296,7 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
     if (tv > 0.f && tv < INFINITY) {
       int e;
       frexpf(tv, &e);                              // tv = m 2^e, 0.5 <= m < 1
-      sw = min(max(15 - e, -60), 60);
+      sw = min(max(15 - e - (int)lag, -60), 60);
     }
     wsc = exp2f((float)sw);
     wback = exp2f((float)(24 - sw));
@@ -439,24 +443,33 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         }
       }
 
-      // ---- online softmax update ------------------------------------------------------
-      float mnew[NT];
-      bool grow = false;
+      // ---- online softmax with a lagging reference -------------------------------------
+      // The weights 2^(logit - mrun) use the running reference mrun of their head. Only if a logit of the
+      // page exceeds it by more than kLag (the first page always does) is the reference raised to the
+      // page's maximum, the state rescaled and the weights' exponents taken again: the common path
+      // needs one vote, not the maximum's shuffles, before its exponentials. Weights stay below 2^kLag.
+      float pw[4][NT][2];                          // log2 of the weights
+      bool raise = false;
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float mx = -INFINITY;
+      for (int mt = 0; mt < 4; ++mt)
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(lg[mt][nt][0], lg[mt][nt][1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        mnew[nt] = fmaxf(mrun[nt], cF[nt] * mx);
-        grow |= mnew[nt] > mrun[nt];
-      }
-      if (__any_sync(0xffffffffu, grow)) {
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            pw[mt][nt][r] = fmaf(cF[nt], lg[mt][nt][r], -mrun[nt]);
+            raise |= pw[mt][nt][r] > lag;          // +inf against a reference of -inf
+          }
+      if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float al = (mnew[nt] > mrun[nt]) ? exp2f(mrun[nt] - mnew[nt]) : 1.f;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(lg[mt][nt][0], lg[mt][nt][1]));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(mrun[nt], cF[nt] * mx);
+          const float al = (mnew > mrun[nt]) ? exp2f(mrun[nt] - mnew) : 1.f;
           lsum[nt] *= al;
           zacc[nt][0] *= al;
           zacc[nt][1] *= al;
@@ -464,7 +477,11 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][mt][e] *= al;
-          mrun[nt] = mnew[nt];
+          mrun[nt] = mnew;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) pw[mt][nt][r] = fmaf(cF[nt], lg[mt][nt][r], -mrun[nt]);
         }
       }
 
@@ -482,8 +499,8 @@ __device__ __forceinline__ void int2_split(const LayerView& lv, const DecodeWork
         const float4 v0 = meta_w[kP + r0], v1 = meta_w[kP + r1];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float pa = fast_exp2(fmaf(cF[nt], lg[kt][nt][0], -mrun[nt]));
-          const float pb = fast_exp2(fmaf(cF[nt], lg[kt][nt][1], -mrun[nt]));
+          const float pa = fast_exp2(pw[kt][nt][0]);
+          const float pb = fast_exp2(pw[kt][nt][1]);
           lsum[nt] += pa + pb;
           zacc[nt][0] = fmaf(pa, v0.y, fmaf(pb, v1.y, zacc[nt][0]));
           zacc[nt][1] = fmaf(pa, v0.w, fmaf(pb, v1.w, zacc[nt][1]));

@@ -162,9 +162,11 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
-def build_decode_case(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64, meta="f16"):
+def build_decode_case(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_splits=64, meta="f16",
+                      kv_hook=None):
     """Prefill B requests on the GPU. With shared_prefix > 0 all requests share their first
-    `shared_prefix` tokens (sink page and the history pages covering them)."""
+    `shared_prefix` tokens (sink page and the history pages covering them). kv_hook(r, k, v), if given,
+    may edit request r's K and V [L, hkv, 128] (bf16 values) in place before the prefill."""
     B = len(lens)
     nh = [max(0, (L - 320 + 63) // 64) for L in lens]
     mhp = max(1, max(nh))
@@ -202,6 +204,8 @@ def build_decode_case(lens, hkv, gq, v_mode, seed, shared_prefix=0, algo=0, max_
         if shared_prefix:
             k0, v0 = tokens(seed, 0, hkv, shared_prefix, extra=0)
             k[:shared_prefix], v[:shared_prefix] = k0, v0
+        if kv_hook is not None:
+            kv_hook(r, k, v)
         ks.append(k)
         vs.append(v)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)

@@ -18,6 +18,7 @@ if torch.cuda.is_available():
 import synth
 from oracle import attention as A
 from oracle import pool as P
+from oracle import rotation
 
 TOL = 2e-3
 ALGOS = [pytest.param(0, id="simt"), pytest.param(1, id="mma"), pytest.param(2, id="tc")]
@@ -59,6 +60,42 @@ def test_tiny_config_decode(algo, v_mode, out_dtype):
     lens, gq = [1024], 4
     cache, prm, hp, bp = _build(lens, 1, gq, v_mode, seed=11, algo=algo)
     _check(cache, prm, hp, bp, lens, gq, v_mode, seed=11, out_dtype=out_dtype)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("v_mode", [0, 1])
+def test_running_maximum_jumps(algo, v_mode):
+    # One split (4 warps, each taking every fourth history page): keys aligned with the first query head of
+    # each kv head on history pages 40 and 52 raise that head's logit maximum twice, each time by more than
+    # 8 (log2 units) over everything before it, after the warp's first page. The tensor-core decode keeps
+    # its softmax reference until a logit exceeds it by 2^8, then rescales and retakes the page's weights.
+    lens, hkv, gq, seed = [4096], 2, 4, 17
+    q = queries(seed, 0, hkv, gq, batch=1)[0]
+    pos = [64 + 40 * 64 + 10, 64 + 52 * 64 + 33]
+
+    def align(r, k, v):
+        for j, p_ in enumerate(pos):
+            for h in range(hkv):
+                d = q[h * gq] / np.linalg.norm(q[h * gq])
+                k[p_, h] = _bf16((1.0 + 3.0 * j) * np.linalg.norm(k[p_, h]) * d)
+
+    cache, prm, hp, bp = _build(lens, hkv, gq, v_mode, seed=seed, algo=algo, max_splits=1, kv_hook=align)
+    # the jumps, in the logits of the cache as stored (oracle decode of the pool the GPU wrote)
+    pm = pool_from_device(cache, 0)
+    seg, kk, _ = P.gather_request(pm, lens[0], hp[0], bp[0], heads=[0], params=prm)
+    rk = rotation.composite_rotation(np.asarray(prm[0].u_k, np.float64))
+    lg = synth.sm_scale() * 1.4426950408889634 * (kk[:, 0] @ (np.asarray(q[0], np.float64) @ rk))
+    hist = np.array([s_ == "history" for s_ in seg])
+    before = lg[hist & (np.arange(lens[0]) < pos[0])].max()
+    assert lg[pos[0]] > before + 8 and lg[pos[1]] > lg[pos[0]] + 8, (before, lg[pos[0]], lg[pos[1]])
+    _check(cache, prm, hp, bp, lens, gq, v_mode, seed=seed, out_dtype=osc.OUT_FP32)
+
+
+def _bf16(x):
+    """float32 -> nearest bf16 value (ties to even), as float32."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    b = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return b.astype(np.uint32).view(np.float32)
 
 
 @pytest.mark.parametrize("algo", ALGOS)

@@ -506,11 +506,11 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
 # Qwen3-8B layer, per decode kernel, from the ncu captures summarised under profiles/, with the digest of the
 # CUDA sources each was taken on: a kernel changed since reports null until it is captured again.
 NCU_DECODE_TRAFFIC = {
-    1: {"bytes_per_launch": 66786304 + 114944, "kernel": "k_decode_mma<1, 3, 0>",
+    1: {"bytes_per_launch": 66788864 + 142848, "kernel": "k_decode_mma<1, 3, 0>",
         "command": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
                    "--clock-control none -k regex:k_decode_mma -s 3 -c 1 python bench.py --workload "
                    "qwen3_8b_100k_l1 --steps 3 --warmup 3 --no-bf16 --no-cpu",
-        "sources_sha256": "6439c896d05fc32f276ccea6c5cdf8891fc2034c093cf54fa91f65718c279da5"},
+        "sources_sha256": "264da5c45f7e2ffbc9061a25edb1f11e6bcdb5dd2881ec6ff728db679f4dfb3d"},
 }
 
 # the sources each decode kernel is compiled from (its file and the headers it includes)

@@ -407,7 +407,7 @@ def run_ours(args, rank: int, world: int, device):
     peak, peak_src = peaks()
     # dominant kernel: the fused decode kernel, timed per launch with the library's CUDA events in a second
     # timed region that issues the same steps without the graph
-    dec_ms, dec_n, lens_prof = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
+    dec_ms, dec_n, lens_prof, span_us = profile_decode_calls(wl, args, kv_new, q_all, seq, out)
     # algorithmic bytes of one layer's decode: with a shared prefix read once for the batch, its pages count once
     hb = shared_unique_bytes(lens_prof, wl["shared"], H, hq) if wl["shp"] else layer_bytes(lens_prof, H, hq)
     dec_avg_ms = dec_ms / max(dec_n, 1)
@@ -433,7 +433,11 @@ def run_ours(args, rank: int, world: int, device):
                      ", CUDA events around each launch in an eager copy of the timed steps (enqueued ahead of the GPU)",
                      "achieved": achieved, "peak": peak, "peak_source": peak_src, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_nominal_7900_gbs": achieved / 7900.0, "traffic": decode_traffic(args), "algorithmic_bytes_per_launch": hb,
-                     "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n},
+                     "avg_launch_us": dec_avg_ms * 1e3, "launches": dec_n,
+                     # one profiled launch's CTAs, first start to last end (device timestamps): the
+                     # launch time above also holds the GPU's gap between an event and a kernel's first CTA
+                     "cta_span_us": span_us,
+                     "achieved_over_cta_span": hb / (span_us / 1e6) / 1e9 if span_us else None},
         "gpu_launches": launches_per_layer * nl * args.steps,
         "clocks": clk.summary(),
     }
@@ -472,16 +476,22 @@ def run_ours(args, rank: int, world: int, device):
 
 def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
     """Eager steps with the library's CUDA events around the history (fused decode) kernel of every
-    oscar_decode_step: returns (summed ms, launches, mean context)."""
+    oscar_decode_step: returns (summed ms, launches, mean context, CTA span in us or None). The CTA
+    span is the first profiled step's middle-layer decode kernel from its first CTA's start to its last
+    CTA's end (%globaltimer stamps of oscar_trace_ctas; fused decode without a shared prefix only)."""
     import torch
     import synth
     cache, nl = wl["cache"], wl["layers"]
     sm = synth.sm_scale()
 
-    def enqueue(i):
+    def enqueue(i, trace_layer=-1, tbuf=None):
         for layer in range(nl):
+            if layer == trace_layer:
+                cache.trace_ctas(tbuf)
             cache.decode_step(layer, q_all[i, layer], kv_new[i, layer, 0], kv_new[i, layer, 1], seq, wl["hist_pt"],
                               wl["bf16_pt"], sm, out=out[layer], shared_hist_pages=wl["shp"])
+            if layer == trace_layer:
+                cache.trace_ctas(None)           # the launch above keeps the buffer it was given
         seq.add_(1)
 
     # Each step starts behind a GPU-side delay longer than the host needs to enqueue it, so the GPU runs the
@@ -494,12 +504,21 @@ def profile_decode_calls(wl, args, kv_new, q_all, seq, out):
     torch.cuda.synchronize()
     delay_cycles = int(max(2.0 * host_s, 1e-3) * 2.2e9)
     lens0 = seq.cpu().numpy().astype(np.int64) + 1
+    tbuf = None
+    if args.algo == 1 and not wl["shp"]:
+        tbuf = torch.zeros(8 * 16384, dtype=torch.int64, device=out.device)
     cache.profile_begin(nl * args.steps)
     for i in range(args.steps):
         torch.cuda._sleep(delay_cycles)
-        enqueue(i)
+        enqueue(i, nl // 2 if i == 0 else -1, tbuf)
     ms, n = cache.profile_read()
-    return ms, n, lens0 + (args.steps - 1) // 2
+    span_us = None
+    if tbuf is not None:
+        tr = tbuf.view(-1, 8).cpu().numpy()
+        tr = tr[tr[:, 2] > 0]
+        if 0 < len(tr) < 16384 and (tr[:, 5] > 0).all():     # every CTA of the launch recorded
+            span_us = float(tr[:, 5].max() - tr[:, 2].min()) / 1e3
+    return ms, n, lens0 + (args.steps - 1) // 2, span_us
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one decode launch of the 102,400-token
